@@ -1,0 +1,20 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+    config.addinivalue_line("markers", "slow: large oracle case (still CPU)")
+
+
+@pytest.fixture(scope="session")
+def lib():
+    """The CUDA library through its C ABI (built in-tree by __graft_entry__.build())."""
+    import block_draft_model_proj_gb300 as dflash
+    return dflash.load()
