@@ -1,0 +1,608 @@
+// C ABI of libdflash: argument checks, workspace layout and the launch sequence of each call.
+// The operations and their sources are documented in include/dflash.h.
+#include <math.h>
+#include <stdarg.h>
+
+#include <atomic>
+#include <mutex>
+#include <vector>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/dflash.h"
+#include "../../include/dflash_testing.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace dflash {
+
+__device__ unsigned g_device_status;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(DFLASH_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+#define DF_CUDA(expr)                                   \
+  do {                                                  \
+    cudaError_t e_ = (expr);                            \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #expr); \
+  } while (0)
+
+constexpr int kMaxDevices = 64;
+unsigned* g_status_ptr[kMaxDevices] = {};
+
+// Address of this device's status word (looked up once per device).
+unsigned* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+// ---- launch counting and optional event timing ----------------------------------------
+std::atomic<long> g_launches{0};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+struct ProfRec {
+  int kind;
+  int count;
+  cudaEvent_t a, b;
+};
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Brackets the kernel launches of one step; `count` = kernels launched inside.
+class Prof {
+ public:
+  Prof(int kind, int count, cudaStream_t s) : kind_(kind), count_(count), s_(s) {
+    g_launches += count;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (g_prof_on) {
+      a_ = take_event();
+      b_ = take_event();
+      cudaEventRecord(a_, s_);
+    }
+  }
+  ~Prof() {
+    if (!a_) return;
+    cudaEventRecord(b_, s_);
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof.push_back({kind_, count_, a_, b_});
+  }
+
+ private:
+  int kind_, count_;
+  cudaStream_t s_;
+  cudaEvent_t a_ = nullptr, b_ = nullptr;
+};
+
+int num_sms() {
+  static int cached[kMaxDevices] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) dev = 0;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
+// ---- workspace carving -----------------------------------------------------------------
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<uint8_t*>(b)) {}
+  template <typename T>
+  T* take(size_t count) {
+    off = (off + 255) & ~(size_t)255;
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+size_t esize(int dtype) { return dtype == DFLASH_DTYPE_BF16 ? 2 : 4; }
+
+struct Act;
+
+// K-split used for a GEMM of this shape: enough tiles to cover the SMs, at least 4 K-steps
+// of 64 per split, at most 8 splits; never an empty split.
+int gemm_splits(long M, int N, int K) {
+  const long tiles = ((M + 127) / 128) * ((N + 255) / 256);
+  const int sms = num_sms();
+  const int kb = (K + 63) / 64;
+  int s = 1;
+  while (s < 8 && tiles * s < sms && kb / (2 * s) >= 4) s *= 2;
+  const int per = (kb + s - 1) / s;
+  return (kb + per - 1) / per;
+}
+
+int check_cfg(const dflash_config_t* c) {
+  if (!c) return fail(DFLASH_ERR_INVALID_ARG, "cfg is null");
+  if (c->dtype != DFLASH_DTYPE_BF16 && c->dtype != DFLASH_DTYPE_F32)
+    return fail(DFLASH_ERR_INVALID_ARG, "cfg->dtype must be DFLASH_DTYPE_BF16 or DFLASH_DTYPE_F32");
+  if (c->target_hidden < 1 || c->num_target_layers < 1 || c->hidden < 1 || c->num_layers < 1 ||
+      c->num_heads < 1 || c->num_kv_heads < 1 || c->head_dim < 2 || c->intermediate < 1 ||
+      c->block_size < 1)
+    return fail(DFLASH_ERR_INVALID_ARG, "cfg sizes must be positive");
+  if (c->num_heads % c->num_kv_heads != 0)
+    return fail(DFLASH_ERR_INVALID_ARG, "num_heads (%d) must be a multiple of num_kv_heads (%d)",
+                c->num_heads, c->num_kv_heads);
+  if (c->head_dim % 2 != 0) return fail(DFLASH_ERR_INVALID_ARG, "head_dim must be even");
+  if (!(c->rope_theta > 0.0) || !(c->rms_eps >= 0.0))
+    return fail(DFLASH_ERR_INVALID_ARG, "rope_theta must be > 0 and rms_eps >= 0");
+  if (c->dtype == DFLASH_DTYPE_BF16) {
+    const long widths[] = {(long)c->target_hidden * c->num_target_layers, c->hidden,
+                           (long)c->num_heads * c->head_dim, c->intermediate};
+    for (long w : widths)
+      if (w % 8 != 0)
+        return fail(DFLASH_ERR_UNSUPPORTED,
+                    "bf16 path needs every matrix row width to be a multiple of 8 elements "
+                    "(16-byte rows for TMA); got %ld", w);
+  }
+  const int grp = c->num_heads / c->num_kv_heads;
+  if ((long)c->block_size * grp > 128 || c->head_dim > 256)
+    return fail(DFLASH_ERR_UNSUPPORTED, "block_size * num_heads/num_kv_heads must be <= 128 and "
+                "head_dim <= 256");
+  return DFLASH_OK;
+}
+
+int check_ptr16(const void* p, const char* what, int dtype) {
+  if (!p) return fail(DFLASH_ERR_INVALID_ARG, "%s is null", what);
+  if (dtype == DFLASH_DTYPE_BF16 && ((uintptr_t)p % 16) != 0)
+    return fail(DFLASH_ERR_INVALID_ARG, "%s must be 16-byte aligned", what);
+  return DFLASH_OK;
+}
+
+int check_weights(const dflash_config_t* c, const dflash_weights_t* w, bool need_layers_body) {
+  if (!w) return fail(DFLASH_ERR_INVALID_ARG, "weights is null");
+  if (w->num_layers != c->num_layers || !w->layers)
+    return fail(DFLASH_ERR_INVALID_ARG, "weights->layers must hold cfg->num_layers entries");
+  int r;
+  if ((r = check_ptr16(w->w_proj, "w_proj", c->dtype))) return r;
+  if ((r = check_ptr16(w->g_ctx, "g_ctx", DFLASH_DTYPE_F32))) return r;
+  if ((r = check_ptr16(w->g_final, "g_final", DFLASH_DTYPE_F32))) return r;
+  for (int l = 0; l < c->num_layers; ++l) {
+    const dflash_layer_weights_t& lw = w->layers[l];
+    if ((r = check_ptr16(lw.w_qkv, "w_qkv", c->dtype))) return r;
+    if (need_layers_body) {
+      if ((r = check_ptr16(lw.w_o, "w_o", c->dtype))) return r;
+      if ((r = check_ptr16(lw.w_gate_up, "w_gate_up", c->dtype))) return r;
+      if ((r = check_ptr16(lw.w_down, "w_down", c->dtype))) return r;
+      if ((r = check_ptr16(lw.g_in, "g_in", DFLASH_DTYPE_F32))) return r;
+      if ((r = check_ptr16(lw.g_post, "g_post", DFLASH_DTYPE_F32))) return r;
+    }
+  }
+  return DFLASH_OK;
+}
+
+int check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (need > ws_bytes) return fail(DFLASH_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  if (need > 0 && !ws) return fail(DFLASH_ERR_INVALID_ARG, "workspace is null");
+  if ((uintptr_t)ws % 256 != 0) return fail(DFLASH_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  return DFLASH_OK;
+}
+
+// C[z] = A * B^T (fp32 out): tcgen05 for bf16 (two-term A when A_lo is given), CUDA cores
+// for fp32.
+cudaError_t gemm(int dtype, const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
+                 float* C, long ldc, long M, int N, int K, int splits, cudaStream_t s) {
+  if (dtype == DFLASH_DTYPE_BF16)
+    return launch_gemm_tc(A, A_lo, lda, Bm, ldb, C, ldc, M, N, K, splits, status_ptr(), s);
+  return launch_gemm_simt(dtype, A, lda, Bm, ldb, C, ldc, M, N, K, splits, s);
+}
+
+// A computed activation buffer: fp32, or the two-term bf16 pair.
+struct Act {
+  void* hi = nullptr;
+  __nv_bfloat16* lo = nullptr;
+  int dtype = DFLASH_DTYPE_F32;
+  ActOut out() const {
+    ActOut o;
+    o.hi = hi;
+    o.lo = lo;
+    o.dtype = dtype;
+    return o;
+  }
+};
+
+Act take_act(struct Carver& cv, size_t n, int dtype);
+
+// ---- layouts shared by the size queries and the calls -----------------------------------
+Act take_act(Carver& cv, size_t n, int dtype) {
+  Act a;
+  a.dtype = dtype;
+  if (dtype == DFLASH_DTYPE_BF16) {
+    a.hi = cv.take<__nv_bfloat16>(n);
+    a.lo = cv.take<__nv_bfloat16>(n);
+  } else {
+    a.hi = cv.take<float>(n);
+  }
+  return a;
+}
+
+struct ProjLayout {
+  float* y;
+  Act ctx;
+  float* cos_t;
+  float* sin_t;
+  int split_proj, split_kv;
+  size_t bytes;
+};
+
+ProjLayout proj_layout(const dflash_config_t* c, int B, int L, void* ws) {
+  ProjLayout p;
+  const long M = (long)B * L;
+  const int D = c->hidden, Kc = c->target_hidden * c->num_target_layers;
+  const int kvw = 2 * c->num_kv_heads * c->head_dim;
+  p.split_proj = gemm_splits(M, D, Kc);
+  p.split_kv = gemm_splits(M, kvw, D);
+  const long ycols = (long)p.split_proj * D > (long)p.split_kv * kvw ? (long)p.split_proj * D
+                                                                       : (long)p.split_kv * kvw;
+  Carver cv(ws);
+  p.y = cv.take<float>((size_t)M * ycols);
+  p.ctx = take_act(cv, (size_t)M * D, c->dtype);
+  p.cos_t = cv.take<float>((size_t)L * (c->head_dim / 2));
+  p.sin_t = cv.take<float>((size_t)L * (c->head_dim / 2));
+  p.bytes = cv.off;
+  return p;
+}
+
+struct BodyLayout {
+  float* x;
+  Act h, attn, act;
+  float *q, *kb, *vb;
+  float* y;
+  float* cos_t;
+  float* sin_t;
+  int sp_qkv, sp_o, sp_gu, sp_down;
+  int P;
+  size_t bytes;
+};
+
+BodyLayout body_layout(const dflash_config_t* c, int B, int L, int N, void* ws) {
+  BodyLayout b;
+  const long T = (long)B * N * c->block_size;
+  const int D = c->hidden, qw = c->num_heads * c->head_dim, kw = c->num_kv_heads * c->head_dim;
+  const int qkvw = qw + 2 * kw, I = c->intermediate;
+  b.sp_qkv = gemm_splits(T, qkvw, D);
+  b.sp_o = gemm_splits(T, D, qw);
+  b.sp_gu = gemm_splits(T, 2 * I, D);
+  b.sp_down = gemm_splits(T, D, I);
+  long ycols = (long)b.sp_qkv * qkvw;
+  if ((long)b.sp_o * D > ycols) ycols = (long)b.sp_o * D;
+  if ((long)b.sp_gu * 2 * I > ycols) ycols = (long)b.sp_gu * 2 * I;
+  if ((long)b.sp_down * D > ycols) ycols = (long)b.sp_down * D;
+  Carver cv(ws);
+  b.x = cv.take<float>((size_t)T * D);
+  b.h = take_act(cv, (size_t)T * D, c->dtype);
+  b.q = cv.take<float>((size_t)T * qw);
+  b.kb = cv.take<float>((size_t)T * kw);
+  b.vb = cv.take<float>((size_t)T * kw);
+  b.attn = take_act(cv, (size_t)T * qw, c->dtype);
+  b.act = take_act(cv, (size_t)T * I, c->dtype);
+  b.y = cv.take<float>((size_t)T * ycols);
+  b.P = L + c->block_size;
+  b.cos_t = cv.take<float>((size_t)b.P * (c->head_dim / 2));
+  b.sin_t = cv.take<float>((size_t)b.P * (c->head_dim / 2));
+  b.bytes = cv.off;
+  return b;
+}
+
+}  // namespace
+}  // namespace dflash
+
+using namespace dflash;
+
+extern "C" {
+
+const char* dflash_last_error(void) { return g_msg; }
+
+int dflash_version(void) { return 100; }
+
+int dflash_device_status(int reset) {
+  unsigned* p = status_ptr();
+  if (!p) return fail(DFLASH_ERR_CUDA, "no CUDA device");
+  DF_CUDA(cudaDeviceSynchronize());
+  unsigned v = 0;
+  DF_CUDA(cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost));
+  if (reset) DF_CUDA(cudaMemset(p, 0, sizeof(unsigned)));
+  if (v & kStatusTimeout) return fail(DFLASH_ERR_TIMEOUT, "device wait timed out (kernel id %u)", (v >> 8) & 0xFF);
+  if (v & kStatusCheck) return fail(DFLASH_ERR_DEVICE_CHECK, "device index check failed (kernel id %u)", (v >> 8) & 0xFF);
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------------------------------
+size_t dflash_plan_workspace_size(int, int, int, int) { return 0; }
+
+int dflash_plan(const uint8_t* mask, const int64_t* sample_ids, int B, int L, int64_t step,
+                uint64_t seed, int num_anchors, int block_size, int32_t* anchors,
+                uint8_t* block_valid, uint8_t* loss_mask, int32_t* position_ids, void* ws,
+                size_t ws_bytes, void* stream) {
+  if (B < 1 || L < 1 || num_anchors < 1 || block_size < 1)
+    return fail(DFLASH_ERR_INVALID_ARG, "B, L, num_anchors and block_size must be >= 1");
+  if (num_anchors > 1024) return fail(DFLASH_ERR_UNSUPPORTED, "num_anchors must be <= 1024");
+  if (!mask || !sample_ids || !anchors || !block_valid || !loss_mask || !position_ids)
+    return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
+  (void)ws;
+  (void)ws_bytes;
+  {
+    Prof pr(DFLASH_PROF_PLAN, 1, (cudaStream_t)stream);
+    DF_CUDA(launch_plan(mask, sample_ids, B, L, (uint64_t)step, seed, num_anchors, block_size,
+                        anchors, block_valid, loss_mask, position_ids, (cudaStream_t)stream));
+  }
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------------------------------
+size_t dflash_project_context_workspace_size(const dflash_config_t* cfg, int B, int L) {
+  if (check_cfg(cfg) != DFLASH_OK || B < 1 || L < 1) return 0;
+  return proj_layout(cfg, B, L, nullptr).bytes;
+}
+
+int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w,
+                           const void* target_hidden, int B, int L, int pos_offset, int L_cache,
+                           const int32_t* ctx_len, void* kv_cache, void* ws, size_t ws_bytes,
+                           void* stream) {
+  int r;
+  if ((r = check_cfg(cfg))) return r;
+  if ((r = check_weights(cfg, w, false))) return r;
+  if (B < 1 || L < 1 || pos_offset < 0 || (long)pos_offset + L > L_cache)
+    return fail(DFLASH_ERR_INVALID_ARG, "need B, L >= 1 and 0 <= pos_offset, pos_offset + L <= L_cache");
+  if ((r = check_ptr16(target_hidden, "target_hidden", cfg->dtype))) return r;
+  if ((r = check_ptr16(kv_cache, "kv_cache", cfg->dtype))) return r;
+  (void)ctx_len;  // every position is projected (allowed by the contract)
+  const ProjLayout lay = proj_layout(cfg, B, L, ws);
+  if ((r = check_ws(ws, ws_bytes, lay.bytes))) return r;
+  cudaStream_t s = (cudaStream_t)stream;
+  const long M = (long)B * L;
+  const int D = cfg->hidden, Kc = cfg->target_hidden * cfg->num_target_layers;
+  const int dh = cfg->head_dim, Hkv = cfg->num_kv_heads, qw = cfg->num_heads * dh;
+  const int kvw = 2 * Hkv * dh;
+  const size_t es = esize(cfg->dtype);
+  {
+    Prof pr(DFLASH_PROF_ROWS, 1, s);
+    DF_CUDA(launch_rope_table(lay.cos_t, lay.sin_t, pos_offset, L, dh, cfg->rope_theta, s));
+  }
+  {
+    Prof pr(DFLASH_PROF_GEMM, 1, s);
+    DF_CUDA(gemm(cfg->dtype, target_hidden, nullptr, Kc, w->w_proj, Kc, lay.y, D, M, D, Kc,
+                 lay.split_proj, s));
+  }
+  {
+    Prof pr(DFLASH_PROF_ROWS, 1, s);
+    DF_CUDA(launch_rows_norm(cfg->dtype, lay.y, lay.split_proj, w->g_ctx, cfg->rms_eps,
+                             (cfg->flags & DFLASH_FLAG_CTX_NORM) != 0, lay.ctx.out(), M, D, s));
+  }
+  const size_t layer_elems = (size_t)B * 2 * Hkv * L_cache * dh;
+  for (int l = 0; l < cfg->num_layers; ++l) {
+    const uint8_t* wkv = static_cast<const uint8_t*>(w->layers[l].w_qkv) + (size_t)qw * D * es;
+    {
+      Prof pr(DFLASH_PROF_GEMM, 1, s);
+      DF_CUDA(gemm(cfg->dtype, lay.ctx.hi, lay.ctx.lo, D, wkv, D, lay.y, kvw, M, kvw, D,
+                   lay.split_kv, s));
+    }
+    void* kv_layer = static_cast<uint8_t*>(kv_cache) + (size_t)l * layer_elems * es;
+    Prof pr(DFLASH_PROF_ROWS, 1, s);
+    DF_CUDA(launch_ctx_kv_scatter(cfg->dtype, lay.y, lay.split_kv, lay.cos_t, lay.sin_t, kv_layer,
+                                  B, L, pos_offset, L_cache, Hkv, dh, s));
+  }
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------------------------------
+size_t dflash_body_workspace_size(const dflash_config_t* cfg, int B, int L, int N) {
+  if (check_cfg(cfg) != DFLASH_OK || B < 1 || L < 1 || N < 1) return 0;
+  return body_layout(cfg, B, L, N, nullptr).bytes;
+}
+
+int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
+                        const void* block_emb, const int32_t* anchors,
+                        const uint8_t* block_valid, const int32_t* position_ids,
+                        const uint8_t* mask, const void* kv_cache, int B, int L, int N,
+                        float* out, void* ws, size_t ws_bytes, void* stream) {
+  int r;
+  if ((r = check_cfg(cfg))) return r;
+  if ((r = check_weights(cfg, w, true))) return r;
+  if (B < 1 || L < 1 || N < 1) return fail(DFLASH_ERR_INVALID_ARG, "B, L and N must be >= 1");
+  if (!anchors || !block_valid || !position_ids || !mask || !out)
+    return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
+  if ((r = check_ptr16(block_emb, "block_emb", cfg->dtype))) return r;
+  if ((r = check_ptr16(kv_cache, "kv_cache", cfg->dtype))) return r;
+  const BodyLayout lay = body_layout(cfg, B, L, N, ws);
+  if ((r = check_ws(ws, ws_bytes, lay.bytes))) return r;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int S = cfg->block_size;
+  const long T = (long)B * N * S;
+  const int D = cfg->hidden, dh = cfg->head_dim, Hq = cfg->num_heads, Hkv = cfg->num_kv_heads;
+  const int qw = Hq * dh, kw = Hkv * dh, qkvw = qw + 2 * kw, I = cfg->intermediate;
+  const int dt = cfg->dtype;
+  const size_t es = esize(dt);
+  unsigned* st = status_ptr();
+  const size_t layer_elems = (size_t)B * 2 * Hkv * L * dh;
+
+  {
+    Prof pr(DFLASH_PROF_ROWS, 2, s);
+    DF_CUDA(launch_rope_table(lay.cos_t, lay.sin_t, 0, lay.P, dh, cfg->rope_theta, s));
+    DF_CUDA(launch_residual_norm(kNormInit, dt, lay.x, block_emb, nullptr, 0, w->layers[0].g_in,
+                                 cfg->rms_eps, lay.h.out(), nullptr, nullptr, false, T, D, s));
+  }
+  for (int l = 0; l < cfg->num_layers; ++l) {
+    const dflash_layer_weights_t& lw = w->layers[l];
+    {
+      Prof pr(DFLASH_PROF_GEMM, 1, s);
+      DF_CUDA(gemm(dt, lay.h.hi, lay.h.lo, D, lw.w_qkv, D, lay.y, qkvw, T, qkvw, D, lay.sp_qkv, s));
+    }
+    {
+      Prof pr(DFLASH_PROF_ROWS, 1, s);
+      DF_CUDA(launch_qkv_rope(lay.y, lay.sp_qkv, position_ids, block_valid, lay.cos_t, lay.sin_t,
+                              lay.P, lay.q, lay.kb, lay.vb, T, Hq, Hkv, dh, st, s));
+    }
+    AttnArgs aa;
+    aa.q = lay.q;
+    aa.kb = lay.kb;
+    aa.vb = lay.vb;
+    aa.kv_layer = static_cast<const uint8_t*>(kv_cache) + (size_t)l * layer_elems * es;
+    aa.anchors = anchors;
+    aa.valid = block_valid;
+    aa.mask = mask;
+    aa.out = lay.attn.out();
+    aa.B = B;
+    aa.N = N;
+    aa.S = S;
+    aa.L = L;
+    aa.Hq = Hq;
+    aa.Hkv = Hkv;
+    aa.dh = dh;
+    aa.status = st;
+    {
+      Prof pr(DFLASH_PROF_ATTENTION, 1, s);
+      DF_CUDA(launch_attention_simt(dt, aa, s));
+    }
+    {
+      Prof pr(DFLASH_PROF_GEMM, 1, s);
+      DF_CUDA(gemm(dt, lay.attn.hi, lay.attn.lo, qw, lw.w_o, qw, lay.y, D, T, D, qw, lay.sp_o, s));
+    }
+    {
+      Prof pr(DFLASH_PROF_ROWS, 1, s);
+      DF_CUDA(launch_residual_norm(kNormAdd, dt, lay.x, nullptr, lay.y, lay.sp_o, lw.g_post,
+                                   cfg->rms_eps, lay.h.out(), nullptr, nullptr, false, T, D, s));
+    }
+    {
+      Prof pr(DFLASH_PROF_GEMM, 1, s);
+      DF_CUDA(gemm(dt, lay.h.hi, lay.h.lo, D, lw.w_gate_up, D, lay.y, 2 * I, T, 2 * I, D,
+                   lay.sp_gu, s));
+    }
+    {
+      Prof pr(DFLASH_PROF_ROWS, 1, s);
+      DF_CUDA(launch_swiglu(lay.y, lay.sp_gu, lay.act.out(), T, I, s));
+    }
+    {
+      Prof pr(DFLASH_PROF_GEMM, 1, s);
+      DF_CUDA(gemm(dt, lay.act.hi, lay.act.lo, I, lw.w_down, I, lay.y, D, T, D, I, lay.sp_down, s));
+    }
+    Prof pr(DFLASH_PROF_ROWS, 1, s);
+    if (l + 1 < cfg->num_layers) {
+      DF_CUDA(launch_residual_norm(kNormAdd, dt, lay.x, nullptr, lay.y, lay.sp_down,
+                                   w->layers[l + 1].g_in, cfg->rms_eps, lay.h.out(), nullptr,
+                                   nullptr, false, T, D, s));
+    } else {
+      DF_CUDA(launch_residual_norm(kNormFinal, dt, lay.x, nullptr, lay.y, lay.sp_down, w->g_final,
+                                   cfg->rms_eps, ActOut(), out, block_valid,
+                                   (cfg->flags & DFLASH_FLAG_FINAL_NORM) != 0, T, D, s));
+    }
+  }
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------------------------------
+size_t dflash_verify_workspace_size(int B, int gamma, int V) {
+  if (B < 1 || gamma < 0 || V < 1) return 0;
+  return plan_verify(B, gamma, V, num_sms()).ws_bytes + 256;
+}
+
+int dflash_verify_greedy(const void* logits, int logits_dtype, const int32_t* draft, int B,
+                         int gamma, int V, int32_t eos, int32_t* emitted, int32_t* num_emitted,
+                         int32_t* accepted, int32_t* target_choices, void* ws, size_t ws_bytes,
+                         void* stream) {
+  if (B < 1 || gamma < 0 || V < 1)
+    return fail(DFLASH_ERR_INVALID_ARG,
+                "need B >= 1, gamma >= 0, V >= 1 (one target choice per draft token plus a bonus)");
+  if (logits_dtype != DFLASH_DTYPE_BF16 && logits_dtype != DFLASH_DTYPE_F32)
+    return fail(DFLASH_ERR_INVALID_ARG, "logits_dtype must be DFLASH_DTYPE_BF16 or _F32");
+  if (!logits || (!draft && gamma > 0) || !emitted || !num_emitted || !accepted)
+    return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
+  const VerifyPlan vp = plan_verify(B, gamma, V, num_sms());
+  Carver cv(ws);
+  const size_t rows = (size_t)B * (gamma + 1);
+  float* pv = cv.take<float>(rows * vp.chunks);
+  int* pi = cv.take<int>(rows * vp.chunks);
+  int r;
+  if ((r = check_ws(ws, ws_bytes, cv.off))) return r;
+  Prof pr(DFLASH_PROF_VERIFY, 2, (cudaStream_t)stream);
+  DF_CUDA(launch_verify(logits, logits_dtype, draft, B, gamma, V, eos, emitted, num_emitted,
+                        accepted, target_choices, pv, pi, vp, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+// ---- testing hooks -----------------------------------------------------------------------
+int dflash_testing_gemm(int engine, int dtype, const void* A, const void* A_lo, long lda,
+                        const void* Bm, long ldb, float* C, long ldc, long M, int N, int K,
+                        int splits, void* stream) {
+  if (M < 1 || N < 1 || K < 1 || !A || !Bm || !C) return fail(DFLASH_ERR_INVALID_ARG, "bad gemm args");
+  cudaStream_t s = (cudaStream_t)stream;
+  if (engine == DFLASH_TESTING_ENGINE_TC) {
+    if (dtype != DFLASH_DTYPE_BF16 || !gemm_tc_supported(M, N, K, lda, ldb))
+      return fail(DFLASH_ERR_UNSUPPORTED, "tensor-core GEMM needs bf16 and 16-byte rows");
+    DF_CUDA(launch_gemm_tc(A, A_lo, lda, Bm, ldb, C, ldc, M, N, K, splits, status_ptr(), s));
+  } else {
+    if (A_lo) return fail(DFLASH_ERR_UNSUPPORTED, "the CUDA-core GEMM takes a single-term A");
+    DF_CUDA(launch_gemm_simt(dtype, A, lda, Bm, ldb, C, ldc, M, N, K, splits, s));
+  }
+  return DFLASH_OK;
+}
+
+int dflash_testing_gemm_splits(long M, int N, int K) { return gemm_splits(M, N, K); }
+
+int dflash_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (auto& r : g_prof) {
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  g_prof.clear();
+  g_prof_on = on != 0;
+  return DFLASH_OK;
+}
+
+int dflash_profile_read(int kind, double* total_ms, long* launches) {
+  if (!total_ms || !launches || kind < 0 || kind >= DFLASH_PROF_KINDS)
+    return fail(DFLASH_ERR_INVALID_ARG, "bad profile query");
+  DF_CUDA(cudaDeviceSynchronize());
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  double ms = 0.0;
+  long n = 0;
+  for (const auto& r : g_prof) {
+    if (r.kind != kind) continue;
+    float t = 0.f;
+    DF_CUDA(cudaEventElapsedTime(&t, r.a, r.b));
+    ms += t;
+    n += r.count;
+  }
+  *total_ms = ms;
+  *launches = n;
+  return DFLASH_OK;
+}
+
+long dflash_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,98 @@
+// Shared device/host helpers of libdflash (no method arithmetic here).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dflash.h"
+
+namespace dflash {
+
+// ---- device status word ------------------------------------------------------------
+// One sticky word per device (defined in api.cu).  Kernels receive its address as a
+// parameter.  Bit layout: bit 0 = a bounded wait ran out, bit 1 = an index check failed;
+// bits 8..15 = id of the first kernel that reported (kernel ids below).
+enum : unsigned {
+  kStatusTimeout = 1u,
+  kStatusCheck = 2u,
+};
+enum : unsigned {
+  kKernPlan = 1, kKernVerify = 2, kKernGemmTc = 3, kKernAttn = 4, kKernEpilogue = 5,
+  kKernNorm = 6, kKernAttnTc = 7,
+};
+
+__device__ __forceinline__ void report(unsigned* status, unsigned bit, unsigned kernel_id) {
+  if (status) {
+    unsigned prev = atomicOr(status, bit);
+    if ((prev & 0xFF00u) == 0) atomicOr(status, kernel_id << 8);
+  }
+}
+
+// ---- element types -------------------------------------------------------------------
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static __device__ __forceinline__ float to_f(float v) { return v; }
+  static __device__ __forceinline__ float from_f(float v) { return v; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+template <typename T> __device__ __forceinline__ float to_f(T v) { return Elem<T>::to_f(v); }
+template <typename T> __device__ __forceinline__ T from_f(float v) { return Elem<T>::from_f(v); }
+
+// Destination of a computed activation that feeds a projection GEMM.  fp32 configuration:
+// one fp32 array.  bf16 configuration: the two-term pair hi = bf16(v), lo = bf16(v - hi),
+// which keeps v to about 2^-17 relative for the tensor-core GEMM's two-term path.
+struct ActOut {
+  void* hi = nullptr;
+  __nv_bfloat16* lo = nullptr;
+  int dtype = DFLASH_DTYPE_F32;
+  __device__ __forceinline__ void store(long i, float v) const {
+    if (dtype == DFLASH_DTYPE_BF16) {
+      const __nv_bfloat16 h = __float2bfloat16_rn(v);
+      static_cast<__nv_bfloat16*>(hi)[i] = h;
+      lo[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+    } else {
+      static_cast<float*>(hi)[i] = v;
+    }
+  }
+};
+
+// ---- reductions --------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Sum over the block; every thread gets the result.  `red` holds >= 33 floats.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    float t = lane < nwarps ? red[lane] : 0.f;
+    t = warp_sum(t);
+    if (lane == 0) red[32] = t;
+  }
+  __syncthreads();
+  return red[32];
+}
+
+// ---- time-bounded waits ----------------------------------------------------------------
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Any device-side wait gives up after this long and reports kStatusTimeout.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+}  // namespace dflash

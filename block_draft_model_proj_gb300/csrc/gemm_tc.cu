@@ -1,0 +1,450 @@
+// bf16 GEMM on the 5th-generation tensor cores: C[z] (fp32) = A[:, Kz] * B[:, Kz]^T.
+//
+// A [M, K] and B [N, K] are row-major bf16 (both K-major), C is fp32 row-major.  This is
+// the contraction behind every projection of the draft body: W_proj ("DFlash", How it
+// works: target hidden states projected into the K/V space), the context K/V projections,
+// and the per-layer QKV / O / gate-up / down projections.
+//
+// Two-term activations: a computed activation (a norm output, the attention output, the
+// SwiGLU product) is carried as a pair of bf16 arrays A = A_hi + A_lo (A_hi = bf16(a),
+// A_lo = bf16(a - A_hi)), which holds a to about 2^-17 relative.  The kernel then issues
+// two MMAs per K step against the same weight tile, C += A_hi W^T + A_lo W^T, so the
+// product is as accurate as an fp32 GEMM of bf16 weights.  Exact bf16 inputs (the target
+// hidden states) take the single-term path.
+//
+// Design (sm_103a):
+//  * persistent CTAs (one per SM), 128 x 256 output tile, K stepped 64 at a time;
+//  * warp 0 = TMA producer: cp.async.bulk.tensor loads of 128x64 A (and A_lo) and
+//    2x(128x64) B boxes, 128-byte swizzle, into a shared-memory ring (4 stages, 3 with
+//    the two-term A) guarded by mbarriers;
+//  * warp 1 = MMA issuer: one thread issues tcgen05.mma.cta_group::1.kind::f16 (M=128,
+//    N=256, K=16) with fp32 accumulation in tensor memory; tcgen05.commit frees a stage;
+//  * warps 2-5 = epilogue: tcgen05.ld of the accumulator (each warp owns its 32-lane
+//    quarter of TMEM), transposed through shared memory into coalesced fp32 row stores;
+//  * two 256-column accumulators (all 512 TMEM columns) so the epilogue of tile i overlaps
+//    the main loop of tile i+1;
+//  * optional K-split: split z writes its own C slice (deterministic; the consumer adds the
+//    slices in a fixed order).
+// Every mbarrier wait is bounded in time: on expiry the CTA raises a shared abort flag,
+// reports DFLASH_ERR_TIMEOUT through the device status word, waits (bounded) for its own
+// outstanding TMA copies and MMAs, frees its tensor memory and exits.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dflash {
+
+namespace {
+
+constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTileABytes = kBM * kBK * 2;    // 16 KB
+constexpr uint32_t kStageBBytes = kBN * kBK * 2;   // 32 KB
+constexpr uint32_t kStagingFloats = 32 * 33;       // per epilogue warp
+
+template <bool kSplit>
+struct Cfg {
+  static constexpr int kStages = kSplit ? 3 : 4;
+  static constexpr uint32_t kStageABytes = (kSplit ? 2 : 1) * kTileABytes;
+  static constexpr uint32_t kTxBytes = kStageABytes + kStageBBytes;
+  static constexpr size_t kSmemBytes = 1024 + kStages * (size_t)(kStageABytes + kStageBBytes) +
+                                       4 * kStagingFloats * sizeof(float) + 256;
+};
+
+// Instruction descriptor, kind::f16: D = fp32 (bits 4-5 = 1), A = bf16 (bits 7-9 = 1),
+// B = bf16 (bits 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
+// M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `bar` with parity `parity`.  Returns false if the CTA is
+// aborting (another role timed out) or this wait itself ran out of time.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups of
+// 1024 bytes (stride byte offset), version bits 46-48 = 0b001, swizzle mode 2 (128B).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+        "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+        "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+        "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+struct TcParams {
+  long M;
+  int N, K;
+  int m_tiles, n_tiles, splits, kb_per_split, num_kb;
+  float* C;
+  long ldc;
+  unsigned* status;
+};
+
+template <bool kSplit>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_alo,
+               const __grid_constant__ CUtensorMap map_b, const TcParams p) {
+  constexpr int kStages = Cfg<kSplit>::kStages;
+  constexpr uint32_t kStageABytes = Cfg<kSplit>::kStageABytes;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kStageABytes;
+  float* staging = reinterpret_cast<float*>(sB + kStages * kStageBBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + 4 * kStagingFloats);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
+    if (kSplit)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_alo)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total = p.m_tiles * p.n_tiles * p.splits;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t ph = 0;
+      int issued[kStages];
+      uint32_t issued_ph[kStages];
+      for (int s = 0; s < kStages; ++s) issued[s] = 0, issued_ph[s] = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const int n_t = t % p.n_tiles;
+        const int rest = t / p.n_tiles;
+        const int m_t = rest % p.m_tiles;
+        const int z = rest / p.m_tiles;
+        const int kb0 = z * p.kb_per_split;
+        const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[stage], Cfg<kSplit>::kTxBytes);
+          uint8_t* a_dst = sA + stage * kStageABytes;
+          uint8_t* b_dst = sB + stage * kStageBBytes;
+          tma_load_2d(&map_a, &full[stage], a_dst, kb * kBK, m_t * kBM);
+          if (kSplit) tma_load_2d(&map_alo, &full[stage], a_dst + kTileABytes, kb * kBK, m_t * kBM);
+          tma_load_2d(&map_b, &full[stage], b_dst, kb * kBK, n_t * kBN);
+          tma_load_2d(&map_b, &full[stage], b_dst + kStageBBytes / 2, kb * kBK, n_t * kBN + 128);
+          issued[stage] = 1;
+          issued_ph[stage] = ph;
+          if (++stage == kStages) { stage = 0; ph ^= 1u; }
+        }
+      }
+      // wait for this thread's own copies still in flight
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s]) mbar_wait(&full[s], issued_ph[s], abort_flag, kWaitLimitNs / 4);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int stage = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const int rest = t / p.n_tiles;
+        const int z = rest / p.m_tiles;
+        const int kb0 = z * p.kb_per_split;
+        const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+        if (!mbar_wait(&tempty[acc], acc_ph ^ 1u, abort_flag, kWaitLimitNs)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], ph, abort_flag, kWaitLimitNs)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * kStageABytes);
+          const uint32_t b_addr = smem_u32(sB + stage * kStageBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            // advancing K by 16 bf16 = 32 bytes inside the 128-byte swizzle atom
+            const uint64_t bdesc = sw128_desc(b_addr + k * 32);
+            umma_bf16(d_tmem, sw128_desc(a_addr + k * 32), bdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            if (kSplit) umma_bf16(d_tmem, sw128_desc(a_addr + kTileABytes + k * 32), bdesc, 1u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == kStages) { stage = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        if (++acc == 2) { acc = 0; acc_ph ^= 1u; }
+      }
+      // all MMAs issued by this thread complete before tensor memory is released
+      umma_commit(drain);
+      mbar_wait(drain, 0, abort_flag, kWaitLimitNs / 4);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    float* stg = staging + (warp - 2) * kStagingFloats;
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const int n_t = t % p.n_tiles;
+      const int rest = t / p.n_tiles;
+      const int m_t = rest % p.m_tiles;
+      const int z = rest / p.m_tiles;
+      if (!mbar_wait(&tfull[acc], acc_ph, abort_flag, kWaitLimitNs)) break;
+      tc_fence_after();
+      float* Cz = p.C + (long)z * p.M * p.ldc;
+      const long row0 = (long)m_t * kBM + quarter * 32;
+      const int col0 = n_t * kBN;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t v[32];
+        const uint32_t taddr =
+            tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN + c * 32);
+        tmem_ld_32x32b_x32(taddr, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) stg[lane * 33 + i] = __uint_as_float(v[i]);
+        __syncwarp();
+        const int col = col0 + c * 32 + lane;
+#pragma unroll 4
+        for (int r = 0; r < 32; ++r) {
+          const long row = row0 + r;
+          if (row < p.M && col < p.N) Cz[row * p.ldc + col] = stg[r * 33 + lane];
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == 2) { acc = 0; acc_ph ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+  if (threadIdx.x == 0 && *abort_flag) report(p.status, kStatusTimeout, kKernGemmTc);
+}
+
+// ---- host side ------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D bf16 map over a [rows, cols] row-major matrix with row stride ld (elements),
+// box = box_rows x 64 columns, 128-byte swizzle, zero fill out of bounds.
+bool encode_kmajor(CUtensorMap* map, const void* base, long rows, int cols, long ld,
+                   int box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+bool gemm_tc_supported(long M, int N, int K, long lda, long ldb) {
+  return M >= 1 && N >= 1 && K >= 1 && lda % 8 == 0 && ldb % 8 == 0 && lda >= K && ldb >= K &&
+         get_encode_fn() != nullptr;
+}
+
+cudaError_t launch_gemm_tc(const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
+                           float* C, long ldc, long M, int N, int K, int splits, unsigned* status,
+                           cudaStream_t stream) {
+  if (((uintptr_t)A | (uintptr_t)A_lo | (uintptr_t)Bm) % 16 != 0) return cudaErrorInvalidValue;
+  CUtensorMap ma, malo, mb;
+  if (!encode_kmajor(&ma, A, M, K, lda, kBM)) return cudaErrorInvalidValue;
+  if (A_lo && !encode_kmajor(&malo, A_lo, M, K, lda, kBM)) return cudaErrorInvalidValue;
+  if (!A_lo) malo = ma;
+  if (!encode_kmajor(&mb, Bm, N, K, ldb, 128)) return cudaErrorInvalidValue;
+  TcParams p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.m_tiles = (int)((M + kBM - 1) / kBM);
+  p.n_tiles = (N + kBN - 1) / kBN;
+  p.num_kb = (K + kBK - 1) / kBK;
+  if (splits < 1) splits = 1;
+  if (splits > p.num_kb) splits = p.num_kb;
+  p.kb_per_split = (p.num_kb + splits - 1) / splits;
+  p.splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;  // no empty split
+  p.C = C;
+  p.ldc = ldc;
+  p.status = status;
+  static bool attr_set[2] = {false, false};
+  const int which = A_lo ? 1 : 0;
+  if (!attr_set[which]) {
+    cudaError_t e = A_lo ? cudaFuncSetAttribute(gemm_tc_kernel<true>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)Cfg<true>::kSmemBytes)
+                         : cudaFuncSetAttribute(gemm_tc_kernel<false>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)Cfg<false>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[which] = true;
+  }
+  const long tiles = (long)p.m_tiles * p.n_tiles * p.splits;
+  const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
+  if (A_lo)
+    gemm_tc_kernel<true><<<grid, kThreads, Cfg<true>::kSmemBytes, stream>>>(ma, malo, mb, p);
+  else
+    gemm_tc_kernel<false><<<grid, kThreads, Cfg<false>::kSmemBytes, stream>>>(ma, malo, mb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace dflash

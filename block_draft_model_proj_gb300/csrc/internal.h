@@ -1,0 +1,96 @@
+// Internal launch interfaces between the C ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace dflash {
+
+// ---- plan.cu ----
+cudaError_t launch_plan(const uint8_t* mask, const int64_t* sids, int B, int L, uint64_t step,
+                        uint64_t seed, int N, int S, int32_t* anchors, uint8_t* block_valid,
+                        uint8_t* loss_mask, int32_t* position_ids, cudaStream_t stream);
+
+// ---- verify.cu ----
+struct VerifyPlan {
+  int chunks = 1;
+  int chunk_len = 0;
+  size_t ws_bytes = 0;
+};
+VerifyPlan plan_verify(int B, int gamma, int V, int num_sms);
+cudaError_t launch_verify(const void* logits, int dtype, const int32_t* draft, int B, int gamma,
+                          int V, int32_t eos, int32_t* emitted, int32_t* num_emitted,
+                          int32_t* accepted, int32_t* choices, float* part_v, int* part_i,
+                          const VerifyPlan& vp, cudaStream_t stream);
+
+// ---- rows.cu: row-wise kernels (norms, RoPE table, GEMM epilogues) ----
+// RoPE table: cos/sin [P, dh/2] fp32 for positions p0 .. p0+P-1, angles formed and
+// range-reduced in fp64.
+cudaError_t launch_rope_table(float* cos_t, float* sin_t, int p0, int P, int head_dim,
+                              double theta, cudaStream_t stream);
+
+enum NormMode { kNormInit = 0, kNormAdd = 1, kNormFinal = 2 };
+// Residual-stream step on rows of width D:
+//  kNormInit : x = emb; h = RMSNorm(x) * g
+//  kNormAdd  : x += sum_s y[s]; h = RMSNorm(x) * g
+//  kNormFinal: x += sum_s y[s]; out = valid ? (final_norm ? RMSNorm(x) * g : x) : 0
+// y: nsplit partial results [nsplit][rows][D] (fp32); emb and g have type `dtype`.
+cudaError_t launch_residual_norm(int mode, int dtype, float* x, const void* emb, const float* y,
+                                 int nsplit, const void* g, double eps, ActOut h, float* out,
+                                 const uint8_t* valid, bool final_norm, long rows, int D,
+                                 cudaStream_t stream);
+
+// Plain RMSNorm of fp32 rows (the context norm); with_norm=false copies.
+cudaError_t launch_rows_norm(int dtype, const float* y, int nsplit, const void* g, double eps,
+                             bool with_norm, ActOut out, long rows, int D, cudaStream_t stream);
+
+// QKV epilogue: y [nsplit][T][(Hq+2Hkv)*dh] fp32 -> q [T][Hq*dh], k/v [T][Hkv*dh] (fp32),
+// RoPE on q and k at position pos[t] (table of P positions; out-of-range valid slots report
+// a device check and use position 0).
+cudaError_t launch_qkv_rope(const float* y, int nsplit, const int32_t* pos, const uint8_t* valid,
+                            const float* cos_t, const float* sin_t, int P, float* q, float* k,
+                            float* v, long T, int Hq, int Hkv, int dh, unsigned* status,
+                            cudaStream_t stream);
+
+// Context K/V epilogue: y [nsplit][B*L][2*Hkv*dh] fp32 -> kv_layer [B][2][Hkv][L_cache][dh]
+// at positions pos_offset + c, RoPE on K (table row c = position pos_offset + c).
+cudaError_t launch_ctx_kv_scatter(int dtype, const float* y, int nsplit,
+                                  const float* cos_t, const float* sin_t, void* kv_layer, int B,
+                                  int L, int pos_offset, int L_cache, int Hkv, int dh,
+                                  cudaStream_t stream);
+
+// SwiGLU epilogue: y [nsplit][T][2I] fp32 (gate | up) -> act [T][I] = SiLU(gate) * up.
+cudaError_t launch_swiglu(const float* y, int nsplit, ActOut act, long T, int I,
+                          cudaStream_t stream);
+
+// ---- gemm_simt.cu: C[z][M][N] (fp32) = A[M][K] * B[N][K]^T over K-split z ----
+cudaError_t launch_gemm_simt(int dtype, const void* A, long lda, const void* Bm, long ldb,
+                             float* C, long ldc, long M, int N, int K, int splits,
+                             cudaStream_t stream);
+
+// ---- gemm_tc.cu: tcgen05 bf16 GEMM, fp32 output, optional K-split ----
+// A_lo != nullptr selects the two-term activation path C = (A + A_lo) B^T.
+bool gemm_tc_supported(long M, int N, int K, long lda, long ldb);
+cudaError_t launch_gemm_tc(const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
+                           float* C, long ldc, long M, int N, int K, int splits, unsigned* status,
+                           cudaStream_t stream);
+
+// ---- attention.cu ----
+struct AttnArgs {
+  const float* q;           // [T][Hq*dh] fp32, T = B*N*S
+  const float* kb;          // [T][Hkv*dh] fp32
+  const float* vb;          // [T][Hkv*dh] fp32
+  const void* kv_layer;     // [B][2][Hkv][L][dh], configuration dtype
+  const int32_t* anchors;   // [B][N]
+  const uint8_t* valid;     // [B][N][S]
+  const uint8_t* mask;      // [B][L]
+  ActOut out;               // [T][Hq*dh]
+  int B, N, S, L, Hq, Hkv, dh;
+  unsigned* status;
+};
+cudaError_t launch_attention_simt(int dtype, const AttnArgs& a, cudaStream_t stream);
+
+}  // namespace dflash

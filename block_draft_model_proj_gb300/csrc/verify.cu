@@ -1,0 +1,208 @@
+// Greedy block verification: vocab-wide argmax per position, then the accepted prefix.
+//
+// "DFlash: drafting, verification, and speed", One DFlash generation cycle: the target
+// chooses its highest-probability token at every position of the drafted block; the
+// longest prefix of proposals that agrees with those choices is accepted; the target's
+// choice at the first disagreement is emitted, or the last choice (the bonus) when every
+// proposal agrees; a matched EOS proposal ends the block.
+//
+// Kernel 1 (HBM-bound, the whole cost): the [B*(gamma+1), V] logits are cut into
+// `chunks` equal column ranges per row; one CTA reduces one range with 16-byte vector loads
+// to (max value, lowest index of that value) and writes it to the workspace.  Values are
+// compared exactly in fp32 (bf16 and fp32 inputs convert to fp32 without rounding), ties
+// keep the lower index, so the result does not depend on the split.
+// Kernel 2: one warp per request combines its rows' partials in chunk order and runs the
+// accepted-prefix scan.
+#include "common.cuh"
+#include "internal.h"
+
+namespace dflash {
+
+namespace {
+
+constexpr int kVerifyThreads = 256;
+
+struct ArgMax {
+  float v;
+  int i;
+};
+
+// (v, i) beats (w, j): larger value, or equal value and lower index.  NaN never wins.
+__device__ __forceinline__ bool better(float v, int i, float w, int j) {
+  return v > w || (v == w && i < j);
+}
+
+__device__ __forceinline__ void consider(ArgMax& a, float v, int i) {
+  if (better(v, i, a.v, a.i)) { a.v = v; a.i = i; }
+}
+
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    f[2 * q] = __uint_as_float(w[q] << 16);
+    f[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kVerifyThreads)
+argmax_partial_kernel(const T* __restrict__ logits, int V, int chunks, int chunk_len,
+                      bool vec_ok, float* __restrict__ part_v, int* __restrict__ part_i) {
+  const int row = blockIdx.y, chunk = blockIdx.x;
+  const int c0 = chunk * chunk_len;
+  const int c1 = min(V, c0 + chunk_len);
+  const T* p = logits + (size_t)row * V;
+  ArgMax best{-INFINITY, 0x7fffffff};
+  constexpr int kVec = 16 / sizeof(T);  // elements per 16-byte load
+  int c = c0;
+  if (vec_ok) {
+    const int nvec = (c1 - c0) / kVec;
+    const uint4* pv = reinterpret_cast<const uint4*>(p + c0);
+    int t = threadIdx.x;
+    // 4 independent 16-byte loads in flight per thread
+    for (; t + 3 * kVerifyThreads < nvec; t += 4 * kVerifyThreads) {
+      uint4 u[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) u[q] = __ldcs(pv + t + q * kVerifyThreads);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int base = c0 + (t + q * kVerifyThreads) * kVec;
+        if constexpr (sizeof(T) == 2) {
+          float f[8];
+          unpack8(u[q], f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) consider(best, f[e], base + e);
+        } else {
+          consider(best, __uint_as_float(u[q].x), base);
+          consider(best, __uint_as_float(u[q].y), base + 1);
+          consider(best, __uint_as_float(u[q].z), base + 2);
+          consider(best, __uint_as_float(u[q].w), base + 3);
+        }
+      }
+    }
+    for (; t < nvec; t += kVerifyThreads) {
+      const uint4 u = __ldcs(pv + t);
+      const int base = c0 + t * kVec;
+      if constexpr (sizeof(T) == 2) {
+        float f[8];
+        unpack8(u, f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) consider(best, f[e], base + e);
+      } else {
+        consider(best, __uint_as_float(u.x), base);
+        consider(best, __uint_as_float(u.y), base + 1);
+        consider(best, __uint_as_float(u.z), base + 2);
+        consider(best, __uint_as_float(u.w), base + 3);
+      }
+    }
+    c = c0 + nvec * kVec;
+  }
+  for (int e = c + threadIdx.x; e < c1; e += kVerifyThreads) consider(best, to_f(p[e]), e);
+
+  // block reduction of (v, i)
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best.v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, best.i, o);
+    consider(best, ov, oi);
+  }
+  __shared__ float sv[kVerifyThreads / 32];
+  __shared__ int si[kVerifyThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) { sv[warp] = best.v; si[warp] = best.i; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    ArgMax r = {sv[0], si[0]};
+    for (int w = 1; w < kVerifyThreads / 32; ++w) consider(r, sv[w], si[w]);
+    part_v[(size_t)row * chunks + chunk] = r.v;
+    part_i[(size_t)row * chunks + chunk] = r.i;
+  }
+}
+
+// One warp per request b: lanes compute the target choices of its S = gamma + 1 rows,
+// lane 0 scans the proposals.
+__global__ void verify_scan_kernel(const float* __restrict__ part_v, const int* __restrict__ part_i,
+                                   int chunks, const int32_t* __restrict__ draft, int B, int gamma,
+                                   int32_t eos, int32_t* __restrict__ emitted,
+                                   int32_t* __restrict__ num_emitted, int32_t* __restrict__ accepted,
+                                   int32_t* __restrict__ choices_out) {
+  const int warps_per_block = blockDim.x >> 5;
+  const int b = blockIdx.x * warps_per_block + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (b >= B) return;
+  const int S = gamma + 1;
+  extern __shared__ int sh_choice[];
+  int* choice = sh_choice + (threadIdx.x >> 5) * S;
+  for (int i = lane; i < S; i += 32) {
+    const size_t row = (size_t)b * S + i;
+    ArgMax r = {part_v[row * chunks], part_i[row * chunks]};
+    for (int c = 1; c < chunks; ++c) consider(r, part_v[row * chunks + c], part_i[row * chunks + c]);
+    // an all-NaN row keeps index 0x7fffffff: report index 0 like a first-element argmax
+    const int ch = r.i == 0x7fffffff ? 0 : r.i;
+    choice[i] = ch;
+    if (choices_out) choices_out[row] = ch;
+  }
+  __syncwarp();
+  if (lane == 0) {
+    const int32_t* d = draft + (size_t)b * gamma;
+    int32_t* em = emitted + (size_t)b * S;
+    int n = 0;
+    bool stopped = false;
+    while (n < gamma && d[n] == choice[n]) {
+      em[n] = d[n];
+      ++n;
+      if (eos >= 0 && d[n - 1] == eos) { stopped = true; break; }
+    }
+    int count = n;
+    if (!stopped) em[count++] = choice[n];  // correction at the mismatch, or the bonus
+    for (int e = count; e < S; ++e) em[e] = -1;
+    num_emitted[b] = count;
+    accepted[b] = n;
+  }
+}
+
+}  // namespace
+
+VerifyPlan plan_verify(int B, int gamma, int V, int num_sms) {
+  VerifyPlan vp;
+  const long rows = (long)B * (gamma + 1);
+  // aim for ~8 CTAs per SM in total, chunks of at least 4096 elements, multiple of 8
+  long want = (8L * num_sms + rows - 1) / rows;
+  long max_chunks = (V + 4095) / 4096;
+  if (want > max_chunks) want = max_chunks;
+  if (want < 1) want = 1;
+  long len = (V + want - 1) / want;
+  len = (len + 7) / 8 * 8;
+  vp.chunk_len = (int)len;
+  vp.chunks = (int)((V + len - 1) / len);
+  vp.ws_bytes = (size_t)rows * vp.chunks * (sizeof(float) + sizeof(int));
+  return vp;
+}
+
+cudaError_t launch_verify(const void* logits, int dtype, const int32_t* draft, int B, int gamma,
+                          int V, int32_t eos, int32_t* emitted, int32_t* num_emitted,
+                          int32_t* accepted, int32_t* choices, float* part_v, int* part_i,
+                          const VerifyPlan& vp, cudaStream_t stream) {
+  const int rows = B * (gamma + 1);
+  dim3 grid(vp.chunks, rows);
+  const size_t elem = dtype == DFLASH_DTYPE_BF16 ? 2 : 4;
+  const bool vec_ok = ((uintptr_t)logits % 16 == 0) && ((size_t)V * elem % 16 == 0) &&
+                      ((size_t)vp.chunk_len * elem % 16 == 0);
+  if (dtype == DFLASH_DTYPE_BF16) {
+    argmax_partial_kernel<__nv_bfloat16><<<grid, kVerifyThreads, 0, stream>>>(
+        (const __nv_bfloat16*)logits, V, vp.chunks, vp.chunk_len, vec_ok, part_v, part_i);
+  } else {
+    argmax_partial_kernel<float><<<grid, kVerifyThreads, 0, stream>>>(
+        (const float*)logits, V, vp.chunks, vp.chunk_len, vec_ok, part_v, part_i);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int warps = 4;
+  const size_t smem = (size_t)warps * (gamma + 1) * sizeof(int);
+  verify_scan_kernel<<<(B + warps - 1) / warps, warps * 32, smem, stream>>>(
+      part_v, part_i, vp.chunks, draft, B, gamma, eos, emitted, num_emitted, accepted, choices);
+  return cudaGetLastError();
+}
+
+}  // namespace dflash

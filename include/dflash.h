@@ -1,0 +1,202 @@
+/*
+ * dflash.h -- C ABI of libdflash.so: the DFlash draft-body forward pass and greedy block
+ * verification on one NVIDIA GB300 (sm_103a).
+ *
+ * The operations come from three public pages about DFlash:
+ *   [P1] "DFlash" (angelspec docs): "How it works" (block-parallel prediction with a
+ *        block-causal mask, dual-source KV context through W_proj, anchor sampling) and
+ *        "Configuration" (the JSON fields mirrored by dflash_config_t).
+ *   [P2] "DFlash Draft Body" (NeMo RL design doc): "How It Works" steps 1-4 (anchor plan,
+ *        draft blocks, block update, loss mask) and "Scope".
+ *   [P3] "DFlash: drafting, verification, and speed": "One DFlash generation cycle"
+ *        (greedy verification of a drafted block, the bonus token, EOS).
+ *
+ * Conventions shared by every call
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller, unless a parameter
+ *    says "host".  The library allocates no device memory: scratch space comes from a
+ *    caller-provided workspace `ws` of at least the size the matching *_workspace_size
+ *    query returns, aligned to 256 bytes (cudaMalloc alignment).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and returns a status code.  Host-side argument checks return
+ *    DFLASH_ERR_INVALID_ARG before anything is launched.  Device-side checks (an index
+ *    outside its documented range, a bounded wait that ran out) do not stop the stream:
+ *    they set a sticky per-device status word read by dflash_device_status().
+ *  - Dense matrices are row-major; weight matrices are stored [out_features, in_features]
+ *    (y = x W^T).  Row strides are exactly the row widths given below.
+ *  - Floating-point storage type is cfg->dtype for weights, activations and the context
+ *    K/V cache: DFLASH_DTYPE_BF16 (arithmetic: bf16 operands, fp32 accumulation, fp32
+ *    residual stream) or DFLASH_DTYPE_F32 (fp32 throughout, no TF32).
+ *  - The thread-local message of the last failing call: dflash_last_error().
+ */
+#ifndef DFLASH_H_
+#define DFLASH_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DFLASH_API __attribute__((visibility("default")))
+#else
+#define DFLASH_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------------------ */
+#define DFLASH_OK 0
+#define DFLASH_ERR_INVALID_ARG 1   /* bad shape, null pointer, misalignment, too small ws */
+#define DFLASH_ERR_UNSUPPORTED 2   /* valid request this build does not handle */
+#define DFLASH_ERR_CUDA 3          /* a CUDA runtime call failed */
+#define DFLASH_ERR_TIMEOUT 4       /* device status: a bounded device-side wait ran out */
+#define DFLASH_ERR_DEVICE_CHECK 5  /* device status: a device-side index check failed */
+
+#define DFLASH_DTYPE_F32 0
+#define DFLASH_DTYPE_BF16 1
+
+#define DFLASH_FLAG_FINAL_NORM 1u  /* output = RMSNorm(x; g_final) (else the raw residual) */
+#define DFLASH_FLAG_CTX_NORM 2u    /* context = RMSNorm(H_cat W_proj^T; g_ctx) (else raw) */
+
+/* Draft model shape ([P1] "Configuration"; the attention/MLP sizes of the draft layers).
+ * num_heads % num_kv_heads == 0; head_dim even. */
+typedef struct dflash_config {
+  int32_t target_hidden;      /* D_t: width of one selected target layer */
+  int32_t num_target_layers;  /* n_tl: number of selected target layers (concat width n_tl*D_t) */
+  int32_t hidden;             /* D: draft hidden size */
+  int32_t num_layers;         /* NL: draft decoder layers */
+  int32_t num_heads;          /* Hq */
+  int32_t num_kv_heads;       /* Hkv */
+  int32_t head_dim;           /* dh */
+  int32_t intermediate;       /* I: SwiGLU width */
+  int32_t block_size;         /* S = gamma + 1: anchor plus gamma draft positions */
+  int32_t dtype;              /* DFLASH_DTYPE_* */
+  uint32_t flags;             /* DFLASH_FLAG_* */
+  int32_t reserved;
+  double rope_theta;          /* RoPE base ([P1] "Configuration": rope_theta) */
+  double rms_eps;             /* RMSNorm epsilon */
+} dflash_config_t;
+
+/* One draft decoder layer (pre-norm attention + SwiGLU MLP), device pointers, dtype cfg->dtype. */
+typedef struct dflash_layer_weights {
+  const void* g_in;       /* [D] input RMSNorm gain */
+  const void* w_qkv;      /* [(Hq + 2*Hkv)*dh, D]: rows = Q heads, then K heads, then V heads */
+  const void* w_o;        /* [D, Hq*dh] */
+  const void* g_post;     /* [D] post-attention RMSNorm gain */
+  const void* w_gate_up;  /* [2*I, D]: rows 0..I-1 gate, rows I..2I-1 up */
+  const void* w_down;     /* [D, I] */
+} dflash_layer_weights_t;
+
+typedef struct dflash_weights {
+  const void* w_proj;                    /* [D, n_tl*D_t] context projection W_proj */
+  const void* g_ctx;                     /* [D] context RMSNorm gain */
+  const void* g_final;                   /* [D] output RMSNorm gain */
+  const dflash_layer_weights_t* layers;  /* HOST array of num_layers entries */
+  int32_t num_layers;                    /* must equal cfg->num_layers */
+} dflash_weights_t;
+
+/* ---- housekeeping ------------------------------------------------------------------ */
+
+/* Message of the last non-OK status returned on this host thread ("" if none). */
+DFLASH_API const char* dflash_last_error(void);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+DFLASH_API int dflash_version(void);
+
+/* Synchronizes the current device, then returns its sticky device-side status:
+ * DFLASH_OK, DFLASH_ERR_TIMEOUT or DFLASH_ERR_DEVICE_CHECK (DFLASH_ERR_CUDA if the
+ * synchronization itself fails).  reset != 0 clears the word afterwards. */
+DFLASH_API int dflash_device_status(int reset);
+
+/* ---- 1. anchor plan ([P2] How It Works, steps 1, 2 and 4) ---------------------------- */
+
+DFLASH_API size_t dflash_plan_workspace_size(int B, int L, int num_anchors, int block_size);
+
+/* Deterministic anchor plan for B rows of L target positions.
+ *   mask        [B, L] uint8, nonzero = valid target position
+ *   sample_ids  [B] int64; rows sharing an id get the anchors of the lowest such row
+ *   step, seed  optimizer step and seed (taken as uint64)
+ * Candidate anchor a: mask[a] and mask[a+1] valid (a+1 < L).  The num_anchors candidates
+ * with the smallest (key, a), key = SplitMix64 chain of (seed, step, sample id, a), sorted
+ * by position; missing anchors are -1 and come last.
+ * Outputs (device, caller-owned, fully written):
+ *   anchors      [B, N] int32
+ *   block_valid  [B, N, S] uint8: anchor != -1, position a valid, position a+j valid
+ *   loss_mask    [B, N, S] uint8: block_valid and j >= 1 (the anchor never counts)
+ *   position_ids [B, N, S] int32: a + j, or -1 in an empty slot
+ * Errors: INVALID_ARG for B, L, N or S < 1, null pointers, ws too small. */
+DFLASH_API int dflash_plan(const uint8_t* mask, const int64_t* sample_ids, int B, int L, int64_t step,
+                uint64_t seed, int num_anchors, int block_size, int32_t* anchors,
+                uint8_t* block_valid, uint8_t* loss_mask, int32_t* position_ids, void* ws,
+                size_t ws_bytes, void* stream);
+
+/* ---- 2. context projection ([P1] How it works: dual-source KV context) ---------------- */
+
+DFLASH_API size_t dflash_project_context_workspace_size(const dflash_config_t* cfg, int B, int L);
+
+/* Projects the target's selected hidden states into every draft layer's K/V space.
+ *   target_hidden [B, L, n_tl*D_t]: the selected target layers concatenated in
+ *                 target_layer_ids order, for context positions pos_offset .. pos_offset+L-1
+ *   kv_cache      [NL, B, 2, Hkv, L_cache, dh] (dtype cfg->dtype): for every layer l,
+ *                 kv_cache[l, b, 0] = RoPE(ctx W_k^T) and kv_cache[l, b, 1] = ctx W_v^T,
+ *                 ctx = RMSNorm(target_hidden W_proj^T; g_ctx), W_k / W_v = the K / V rows
+ *                 of layer l's w_qkv; written at positions pos_offset .. pos_offset+L-1 only.
+ *   ctx_len       optional [B] int32 (NULL = L): positions c >= ctx_len[b] of row b may be
+ *                 left unwritten (no block of that row reads them); values are clamped to [0, L].
+ * Requires 0 <= pos_offset, pos_offset + L <= L_cache.  RoPE positions are the absolute
+ * positions pos_offset + c. */
+DFLASH_API int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w,
+                           const void* target_hidden, int B, int L, int pos_offset, int L_cache,
+                           const int32_t* ctx_len, void* kv_cache, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/* ---- 3. draft body ([P2] How It Works, step 3; [P1] block-parallel prediction) -------- */
+
+DFLASH_API size_t dflash_body_workspace_size(const dflash_config_t* cfg, int B, int L, int N);
+
+/* Runs the draft decoder layers over B*N blocks of S slots.
+ *   block_emb    [B, N, S, D] (dtype cfg->dtype): caller-supplied slot embeddings
+ *   anchors      [B, N] int32 in [-1, L] (-1 = empty block)
+ *   block_valid  [B, N, S] uint8
+ *   position_ids [B, N, S] int32: RoPE position of each slot, in [0, L + S) for valid slots
+ *   mask         [B, L] uint8: context validity
+ *   kv_cache     [NL, B, 2, Hkv, L, dh] from dflash_project_context (L = its L_cache)
+ *   out          [B, N, S, D] float32: one hidden state per slot; exactly 0 where
+ *                block_valid == 0.
+ * Attention of a valid slot of block (b, k) reads exactly: context positions c < anchors[b,k]
+ * (c < L) with mask[b,c] != 0, and the valid slots of the same block (all of them, in both
+ * directions).  It never reads another block and never writes kv_cache.
+ * Layer: x += W_o Attn(RMSNorm(x; g_in)); x += W_down(SiLU(h W_gate^T) * h W_up^T),
+ * h = RMSNorm(x; g_post); out = RMSNorm(x; g_final) when DFLASH_FLAG_FINAL_NORM.
+ * A valid slot whose position id is out of range sets DFLASH_ERR_DEVICE_CHECK. */
+DFLASH_API int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
+                        const void* block_emb, const int32_t* anchors,
+                        const uint8_t* block_valid, const int32_t* position_ids,
+                        const uint8_t* mask, const void* kv_cache, int B, int L, int N,
+                        float* out, void* ws, size_t ws_bytes, void* stream);
+
+/* ---- 4. greedy verification ([P3] One DFlash generation cycle) ----------------------- */
+
+DFLASH_API size_t dflash_verify_workspace_size(int B, int gamma, int V);
+
+/* Greedy block verification of B drafted blocks.
+ *   logits  [B, gamma+1, V] of type logits_dtype (DFLASH_DTYPE_BF16 or _F32): row i is the
+ *           target's distribution after the anchor and draft[0..i-1]; row gamma gives the bonus
+ *   draft   [B, gamma] int32 proposed tokens
+ *   eos     EOS token id, or -1 for none: a matching EOS proposal ends the block (no bonus)
+ * target choice i = argmax over V of logits row i (exact comparison, lowest index on ties).
+ * Outputs: emitted [B, gamma+1] int32 (the accepted proposals, then the target's choice at
+ * the first mismatch or the bonus, padded with -1); num_emitted [B]; accepted [B];
+ * target_choices [B, gamma+1] (optional, may be NULL).
+ * Errors: INVALID_ARG for gamma < 0, V < 1, B < 1 (the length rule of the page's
+ * verification: one target choice per draft token plus the bonus). */
+DFLASH_API int dflash_verify_greedy(const void* logits, int logits_dtype, const int32_t* draft, int B,
+                         int gamma, int V, int32_t eos, int32_t* emitted, int32_t* num_emitted,
+                         int32_t* accepted, int32_t* target_choices, void* ws, size_t ws_bytes,
+                         void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_H_ */

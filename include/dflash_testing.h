@@ -1,0 +1,56 @@
+/*
+ * dflash_testing.h -- test hooks of libdflash.so (not part of the DFlash operations).
+ *
+ * They expose single kernels of the library so tests can check them in isolation.  The
+ * four operations of dflash.h never depend on these hooks.
+ */
+#ifndef DFLASH_TESTING_H_
+#define DFLASH_TESTING_H_
+
+#include <stdint.h>
+
+#include "dflash.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DFLASH_TESTING_ENGINE_TC 0   /* tcgen05 / TMEM / TMA kernel (bf16 only) */
+#define DFLASH_TESTING_ENGINE_SIMT 1 /* CUDA-core kernel (fp32 accumulation, no TF32) */
+
+/* C[z] (float32, [splits][M][ldc]) = (A + A_lo)[:, Kz] * B[:, Kz]^T, A and the optional
+ * second term A_lo [M, K] (row stride lda; A_lo only with the tensor-core engine),
+ * B [N, K] (row stride ldb), all of type dtype (DFLASH_DTYPE_*), device pointers.
+ * The K range is cut into `splits` contiguous slices of 64-element steps; slice z goes to
+ * C + z*M*ldc.  Asynchronous on `stream`.  Returns a DFLASH_* status. */
+DFLASH_API int dflash_testing_gemm(int engine, int dtype, const void* A, const void* A_lo, long lda,
+                                   const void* B, long ldb, float* C, long ldc, long M, int N,
+                                   int K, int splits, void* stream);
+
+/* The K-split the library picks for an M x N x K projection on the current device. */
+DFLASH_API int dflash_testing_gemm_splits(long M, int N, int K);
+
+/* ---- live kernel timing ----------------------------------------------------------------
+ * While enabled, every kernel launch of the four operations is bracketed by two CUDA events
+ * recorded on the launch stream, grouped by kind.  Enabling clears earlier records. */
+#define DFLASH_PROF_GEMM 0       /* tensor-core / CUDA-core projection GEMMs */
+#define DFLASH_PROF_ATTENTION 1  /* block-sparse attention */
+#define DFLASH_PROF_ROWS 2       /* norms, RoPE table, GEMM epilogues */
+#define DFLASH_PROF_PLAN 3       /* anchor plan */
+#define DFLASH_PROF_VERIFY 4     /* argmax + accepted-prefix scan */
+#define DFLASH_PROF_KINDS 5
+
+DFLASH_API int dflash_profile_enable(int on);
+
+/* Synchronizes the current device, then returns the summed event time (ms) and the number
+ * of launches of one kind recorded since profiling was enabled. */
+DFLASH_API int dflash_profile_read(int kind, double* total_ms, long* launches);
+
+/* Kernel launches issued by the library in this process (always counted). */
+DFLASH_API long dflash_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_TESTING_H_ */

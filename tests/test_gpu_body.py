@@ -1,0 +1,193 @@
+"""GPU context projection + draft body vs the fp64 oracle, plus the body's structural
+guarantees on the GPU (block isolation, strict prefix, no writes to the context K/V, exact
+zeros at invalid slots, identical rows for shared sample ids)."""
+import numpy as np
+import pytest
+
+import dflash_inputs as di
+from dflash_testlib import SynthModel, compare_hidden, np_to_device, to_device, tol_for
+from oracle import dflash_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+
+class Case:
+    """One workload's inputs, the GPU outputs, and oracle access to selected blocks."""
+
+    def __init__(self, w: di.Workload, gain_std=0.0, plan=None, mask=None):
+        self.w = w
+        s = w.shape
+        self.model = SynthModel(w, gain_std)
+        self.mask = di.gen_mask(w) if mask is None else mask
+        self.sids = di.gen_sample_ids(w)
+        if plan is None:
+            if w.inference:
+                a, v, p = di.inference_block_layout(w)
+                plan = {"anchors": a, "block_valid": v, "position_ids": p}
+            else:
+                plan = orc.build_plan(self.mask, self.sids, w.plan_step, w.plan_seed,
+                                      w.num_anchors, s.block_size)
+        self.plan = plan
+        self.emb = di.gen_block_emb(w)
+        self.N = plan["anchors"].shape[1]
+
+    def run_gpu(self, emb=None, hidden=None, mask=None, check_cache=False):
+        import torch
+        import block_draft_model_proj_gb300 as dflash
+        w, s = self.w, self.w.shape
+        B, L, N, S = w.batch, w.seq_len, self.N, s.block_size
+        cfg = dflash.make_config(s)
+        wts = self.model.lib_weights()
+        H = to_device(di.gen_target_hidden(w) if hidden is None else hidden)
+        tdt = torch.bfloat16 if s.dtype == "bf16" else torch.float32
+        kv = torch.empty((s.num_layers, B, 2, s.num_kv_heads, L, s.head_dim), dtype=tdt,
+                         device="cuda")
+        dflash.dflash_project_context(cfg, wts, H, B, L, 0, L, kv)
+        del H
+        out = torch.full((B, N, S, s.hidden), float("nan"), dtype=torch.float32, device="cuda")
+        m = np_to_device(self.mask if mask is None else mask)
+        before = kv.clone() if check_cache else None
+        dflash.dflash_body_forward(cfg, wts, to_device(self.emb if emb is None else emb),
+                                   np_to_device(self.plan["anchors"]),
+                                   np_to_device(self.plan["block_valid"]),
+                                   np_to_device(self.plan["position_ids"]), m, kv, B, L, N, out)
+        dflash.dflash_device_status()
+        if check_cache:
+            assert torch.equal(before, kv), "the body must not write the context K/V"
+        return out.cpu().numpy()
+
+    def oracle_blocks(self, blocks, emb=None, hidden_fn=None, mask=None):
+        """blocks: list of (b, k).  Returns {(b, k): [S, D] fp64}."""
+        w, s = self.w, self.w.shape
+        mask = self.mask if mask is None else mask
+        emb = (self.emb if emb is None else emb).f64()
+        out = {}
+        by_row = {}
+        for b, k in blocks:
+            by_row.setdefault(b, []).append(k)
+        for b, ks in by_row.items():
+            need = max(min(int(self.plan["anchors"][b, k]), w.seq_len) for k in ks)
+            need = max(need, 1)
+            rows = (di.gen_target_hidden_rows(w, b, 0, need) if hidden_fn is None
+                    else hidden_fn(b, need))
+            kv = orc.project_context_row(s, self.model.top64(), self.model.layer64, rows.f64())
+            for k in ks:
+                out[(b, k)] = orc.block_forward(
+                    s, self.model.top64(), self.model.layer64, emb[b, k],
+                    int(self.plan["anchors"][b, k]), self.plan["block_valid"][b, k], mask[b], kv,
+                    self.plan["position_ids"][b, k])
+        return out
+
+    def compare(self, got, blocks, ref=None):
+        ref = self.oracle_blocks(blocks) if ref is None else ref
+        g = np.stack([got[b, k] for b, k in blocks])
+        r = np.stack([ref[(b, k)] for b, k in blocks])
+        v = np.stack([self.plan["block_valid"][b, k] for b, k in blocks])
+        return compare_hidden(g, r, v, tol_for(self.w.shape))
+
+
+def small_bf16_workload():
+    """Several tiles in every GEMM dimension plus ragged tails; masks with holes."""
+    shape = di.DraftShape(target_hidden=192, num_target_layers=2, hidden=256, num_layers=2,
+                          num_heads=4, num_kv_heads=2, head_dim=64, intermediate=392,
+                          block_size=4, dtype="bf16")
+    return di.Workload("small_bf16", 7, shape, batch=3, seq_len=300, num_anchors=5,
+                       padded_rows=((1, 170),), verify_batch=0, vocab=0)
+
+
+def test_small_bf16_full_parity_with_gains(lib):
+    w = small_bf16_workload()
+    mask = di.gen_mask(w)
+    mask[2, 50:60] = 0              # a hole inside the context
+    c = Case(w, gain_std=0.1, mask=mask)
+    got = c.run_gpu(check_cache=True)
+    blocks = [(b, k) for b in range(w.batch) for k in range(c.N)]
+    c.compare(got, blocks)
+
+
+def test_tiny_f32_config_full_parity(lib):
+    w = di.WORKLOADS["tiny_f32"]
+    c = Case(w)
+    got = c.run_gpu()
+    stats = c.compare(got, [(0, k) for k in range(c.N)])
+    assert stats["n"] > 0
+
+
+def test_train_8b_b4_parity(lib):
+    w = di.WORKLOADS["train_8b_b4_l2048"]
+    c = Case(w)
+    got = c.run_gpu(check_cache=True)
+    # row 3 is padded to one valid token: no window, every slot exactly zero
+    assert np.all(got[3] == 0.0)
+    c.compare(got, [(0, k) for k in range(c.N)] + [(2, 0), (2, 1)])
+
+
+@pytest.mark.parametrize("batch", [1, 8])
+def test_decode_8b_parity(lib, batch):
+    w = di.WORKLOADS[f"decode_8b_b{batch}_ctx4096"]
+    c = Case(w)
+    got = c.run_gpu()
+    c.compare(got, [(0, 0)] + ([(batch - 1, 0)] if batch > 1 else []))
+
+
+def test_longctx_8b_sampled_parity(lib):
+    w = di.WORKLOADS["longctx_8b_l32768"]
+    c = Case(w)
+    got = c.run_gpu()
+    anchors = c.plan["anchors"][0]
+    ks = [int(k) for k in np.argsort(anchors)[:3]]        # shortest prefixes
+    c.compare(got, [(0, k) for k in ks])
+    assert np.all(np.isfinite(got))
+
+
+def test_train_8b_b16_sampled_parity_and_shared_rows(lib):
+    w = di.WORKLOADS["train_8b_b16_l4096"]
+    c = Case(w)
+    got = c.run_gpu()
+    for grp in w.shared_sid_groups:
+        for b in grp[1:]:
+            assert np.array_equal(got[b], got[grp[0]]), "rows sharing a sample id must match"
+    ks = [int(k) for k in np.argsort(c.plan["anchors"][8])[:2]]
+    c.compare(got, [(8, k) for k in ks] + [(0, 0)])
+
+
+def test_block_isolation_and_strict_prefix_on_gpu(lib):
+    """Perturbing other blocks' embeddings, or the target context at/after a block's anchor,
+    leaves that block's output bit-identical; perturbing its strict prefix changes it."""
+    w = small_bf16_workload()
+    c = Case(w)
+    base = c.run_gpu()
+    b = 0
+    k = int(np.argmax(c.plan["anchors"][b]))
+    a = int(c.plan["anchors"][b, k])
+    assert a > 10
+    emb2 = di.Tensor(c.emb.data.copy(), c.emb.dtype)
+    rng = np.random.default_rng(0)
+    for kk in range(c.N):
+        if kk != k:
+            emb2.data[b, kk] = di.f32_to_bf16_bits(rng.standard_normal(emb2.data[b, kk].shape)
+                                                   .astype(np.float32))
+    H = di.gen_target_hidden(w)
+    H2 = di.Tensor(H.data.copy(), H.dtype)
+    H2.data[b, a:] = di.f32_to_bf16_bits(
+        5 * rng.standard_normal(H2.data[b, a:].shape).astype(np.float32))
+    got = c.run_gpu(emb=emb2, hidden=H2)
+    assert np.array_equal(got[b, k], base[b, k])
+    H3 = di.Tensor(H.data.copy(), H.dtype)
+    H3.data[b, a - 1] = di.f32_to_bf16_bits(
+        5 * rng.standard_normal(H3.data[b, a - 1].shape).astype(np.float32))
+    got3 = c.run_gpu(hidden=H3)
+    assert not np.array_equal(got3[b, k], base[b, k])
+
+
+def test_out_of_range_position_reports_device_check(lib):
+    import block_draft_model_proj_gb300 as dflash
+    w = small_bf16_workload()
+    c = Case(w)
+    c.plan = {k: v.copy() for k, v in c.plan.items()}
+    b, k = 0, 0
+    assert c.plan["block_valid"][b, k, 0]
+    c.plan["position_ids"][b, k, 0] = w.seq_len + 10_000   # beyond L + S
+    with pytest.raises(RuntimeError, match="index check"):
+        c.run_gpu()
+    dflash.dflash_device_status(reset=True)
