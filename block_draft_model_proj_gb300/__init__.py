@@ -75,6 +75,8 @@ _SIGS = {
     "dflash_verify_workspace_size": (_Z, [_I, _I, _I]),
     "dflash_verify_greedy": (_I, [_P, _I, _P, _I, _I, _I, ctypes.c_int32, _P, _P, _P, _P, _P, _Z,
                                   _P]),
+    "dflash_verify_greedy_static": (_I, [_P, _I, _P, _I, _I, _I, ctypes.c_int32, _P, _P, _P, _P,
+                                         _P]),
     "dflash_testing_gemm": (_I, [_I, _I, _P, _P, _L, _P, _L, _P, _L, _L, _I, _I, _I, _P]),
     "dflash_testing_gemm_splits": (_I, [_L, _I, _I]),
     "dflash_profile_enable": (_I, [_I]),
@@ -222,6 +224,15 @@ def dflash_verify_greedy(logits, logits_dtype, draft, B, gamma, V, eos, emitted,
     _check(lib.dflash_verify_greedy(_ptr(logits), logits_dtype, _ptr(draft), B, gamma, V,
                                     int(eos), _ptr(emitted), _ptr(num_emitted), _ptr(accepted),
                                     _ptr(target_choices), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def dflash_verify_greedy_static(logits, logits_dtype, draft, B, gamma, V, eos, emitted,
+                                num_emitted, accepted, target_choices=None, stream=None):
+    """Greedy verification that allocates nothing (fixed scratch inside the library)."""
+    _check(load().dflash_verify_greedy_static(_ptr(logits), logits_dtype, _ptr(draft), B, gamma,
+                                              V, int(eos), _ptr(emitted), _ptr(num_emitted),
+                                              _ptr(accepted), _ptr(target_choices),
+                                              _stream(stream)))
 
 
 def dflash_device_status(reset: bool = True) -> None:

@@ -319,6 +319,15 @@ BodyLayout body_layout(const dflash_config_t* c, int B, int L, int N, void* ws) 
 }
 
 }  // namespace
+
+int set_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
 }  // namespace dflash
 
 using namespace dflash;

@@ -9,6 +9,10 @@
 
 namespace dflash {
 
+// ---- api.cu ----
+// Records the thread-local message returned by dflash_last_error(); returns `code`.
+int set_error(int code, const char* fmt, ...);
+
 // ---- plan.cu ----
 cudaError_t launch_plan(const uint8_t* mask, const int64_t* sids, int B, int L, uint64_t step,
                         uint64_t seed, int N, int S, int32_t* anchors, uint8_t* block_valid,

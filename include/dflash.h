@@ -195,6 +195,28 @@ DFLASH_API int dflash_verify_greedy(const void* logits, int logits_dtype, const 
                          int32_t* accepted, int32_t* target_choices, void* ws, size_t ws_bytes,
                          void* stream);
 
+/* ---- greedy verification without a workspace ----------------------------------------
+ * The pages have no counterpart for this call: it is a deployment variant of
+ * dflash_verify_greedy for callers that cannot allocate device memory -- code embedded in
+ * a host framework that owns the whole device memory pool and forbids side allocations,
+ * or a latency-critical loop that must never call cudaMalloc/cudaFree (both may
+ * synchronize the device).  Same arguments, outputs and errors as dflash_verify_greedy,
+ * minus the workspace: the scratch lives in a fixed 128 KiB array inside this library's
+ * device memory, held by every GPU that loads the library until the process exits.
+ *  - Limit: B * (gamma + 1) <= 16384; larger requests return DFLASH_ERR_INVALID_ARG with a
+ *    message (use dflash_verify_greedy with a workspace instead).
+ *  - The first call on each device (with that device current) looks up the array's device
+ *    address; make that first call before any stream capture on that device.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *  - Every call on a device shares the one array and no call needs it zeroed (each call
+ *    writes every entry it reads).  Calls whose kernels overlap on the GPU (different
+ *    streams, or host threads racing on one device) race on the array: serialize them. */
+DFLASH_API int dflash_verify_greedy_static(const void* logits, int logits_dtype,
+                                           const int32_t* draft, int B, int gamma, int V,
+                                           int32_t eos, int32_t* emitted, int32_t* num_emitted,
+                                           int32_t* accepted, int32_t* target_choices,
+                                           void* stream);
+
 #ifdef __cplusplus
 }
 #endif
