@@ -191,9 +191,8 @@ class GpuStep:
         self.d_emb = self.h_emb.to(device)
         self.d_logits = self.h_logits.to(device)
         self.d_draft = self.h_draft.to(device)
-        tdt = torch.bfloat16 if s.dtype == "bf16" else torch.float32
-        self.kv = torch.empty((s.num_layers, B, 2, s.num_kv_heads, L, s.head_dim), dtype=tdt,
-                              device=device)
+        self.kv = torch.empty((s.num_layers, B, 2, s.num_kv_heads, L, s.head_dim),
+                              dtype=torch.float32, device=device)
         self.anchors = torch.empty((B, N), dtype=torch.int32, device=device)
         self.bv = torch.empty((B, N, S), dtype=torch.uint8, device=device)
         self.lm = torch.empty_like(self.bv)

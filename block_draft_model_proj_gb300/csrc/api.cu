@@ -173,6 +173,10 @@ int check_cfg(const dflash_config_t* c) {
   if ((long)c->block_size * grp > 128 || c->head_dim > 256)
     return fail(DFLASH_ERR_UNSUPPORTED, "block_size * num_heads/num_kv_heads must be <= 128 and "
                 "head_dim <= 256");
+  if (c->dtype == DFLASH_DTYPE_BF16 &&
+      !attention_tc_supported(c->block_size, c->num_heads, c->num_kv_heads, c->head_dim))
+    return fail(DFLASH_ERR_UNSUPPORTED, "bf16 attention needs head_dim == 128 and "
+                "block_size * num_heads/num_kv_heads dividing 128");
   return DFLASH_OK;
 }
 
@@ -280,7 +284,9 @@ ProjLayout proj_layout(const dflash_config_t* c, int B, int L, void* ws) {
 struct BodyLayout {
   float* x;
   Act h, attn, act;
-  float *q, *kb, *vb;
+  float *q, *kb, *vbt;  // attention-ready operands
+  int ns_pad;
+  float* partials;      // tensor-core attention partials (bf16 configuration)
   float* y;
   float* cos_t;
   float* sin_t;
@@ -307,7 +313,12 @@ BodyLayout body_layout(const dflash_config_t* c, int B, int L, int N, void* ws) 
   b.h = take_act(cv, (size_t)T * D, c->dtype);
   b.q = cv.take<float>((size_t)T * qw);
   b.kb = cv.take<float>((size_t)T * kw);
-  b.vb = cv.take<float>((size_t)T * kw);
+  b.ns_pad = (N * c->block_size + 3) / 4 * 4;
+  b.vbt = cv.take<float>((size_t)B * c->num_kv_heads * c->head_dim * b.ns_pad);
+  b.partials = nullptr;
+  if (c->dtype == DFLASH_DTYPE_BF16)
+    b.partials = cv.take<float>((size_t)attention_tc_layout(B, N, c->block_size, L, c->num_heads,
+                                                            c->num_kv_heads).part_floats);
   b.attn = take_act(cv, (size_t)T * qw, c->dtype);
   b.act = take_act(cv, (size_t)T * I, c->dtype);
   b.y = cv.take<float>((size_t)T * ycols);
@@ -388,7 +399,9 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
   if (B < 1 || L < 1 || pos_offset < 0 || (long)pos_offset + L > L_cache)
     return fail(DFLASH_ERR_INVALID_ARG, "need B, L >= 1 and 0 <= pos_offset, pos_offset + L <= L_cache");
   if ((r = check_ptr16(target_hidden, "target_hidden", cfg->dtype))) return r;
-  if ((r = check_ptr16(kv_cache, "kv_cache", cfg->dtype))) return r;
+  if ((r = check_ptr16(kv_cache, "kv_cache", DFLASH_DTYPE_BF16))) return r;
+  if (cfg->dtype == DFLASH_DTYPE_BF16 && L_cache % 4 != 0)
+    return fail(DFLASH_ERR_INVALID_ARG, "L_cache must be a multiple of 4 (16-byte cache rows)");
   (void)ctx_len;  // every position is projected (allowed by the contract)
   const ProjLayout lay = proj_layout(cfg, B, L, ws);
   if ((r = check_ws(ws, ws_bytes, lay.bytes))) return r;
@@ -413,6 +426,7 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
                              (cfg->flags & DFLASH_FLAG_CTX_NORM) != 0, lay.ctx.out(), M, D, s));
   }
   const size_t layer_elems = (size_t)B * 2 * Hkv * L_cache * dh;
+  const bool to_tf32 = cfg->dtype == DFLASH_DTYPE_BF16;
   for (int l = 0; l < cfg->num_layers; ++l) {
     const uint8_t* wkv = static_cast<const uint8_t*>(w->layers[l].w_qkv) + (size_t)qw * D * es;
     {
@@ -420,10 +434,10 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
       DF_CUDA(gemm(cfg->dtype, lay.ctx.hi, lay.ctx.lo, D, wkv, D, lay.y, kvw, M, kvw, D,
                    lay.split_kv, s));
     }
-    void* kv_layer = static_cast<uint8_t*>(kv_cache) + (size_t)l * layer_elems * es;
-    Prof pr(DFLASH_PROF_ROWS, 1, s);
-    DF_CUDA(launch_ctx_kv_scatter(cfg->dtype, lay.y, lay.split_kv, lay.cos_t, lay.sin_t, kv_layer,
-                                  B, L, pos_offset, L_cache, Hkv, dh, s));
+    float* kv_layer = static_cast<float*>(kv_cache) + (size_t)l * layer_elems;
+    Prof pr(DFLASH_PROF_ROWS, 2, s);
+    DF_CUDA(launch_ctx_kv_scatter(lay.y, lay.split_kv, lay.cos_t, lay.sin_t, kv_layer, B, L,
+                                  pos_offset, L_cache, Hkv, dh, to_tf32, s));
   }
   return DFLASH_OK;
 }
@@ -446,7 +460,9 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
   if (!anchors || !block_valid || !position_ids || !mask || !out)
     return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
   if ((r = check_ptr16(block_emb, "block_emb", cfg->dtype))) return r;
-  if ((r = check_ptr16(kv_cache, "kv_cache", cfg->dtype))) return r;
+  if ((r = check_ptr16(kv_cache, "kv_cache", DFLASH_DTYPE_BF16))) return r;
+  if (cfg->dtype == DFLASH_DTYPE_BF16 && L % 4 != 0)
+    return fail(DFLASH_ERR_INVALID_ARG, "L must be a multiple of 4 (16-byte cache rows)");
   const BodyLayout lay = body_layout(cfg, B, L, N, ws);
   if ((r = check_ws(ws, ws_bytes, lay.bytes))) return r;
   cudaStream_t s = (cudaStream_t)stream;
@@ -474,26 +490,50 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
     {
       Prof pr(DFLASH_PROF_ROWS, 1, s);
       DF_CUDA(launch_qkv_rope(lay.y, lay.sp_qkv, position_ids, block_valid, lay.cos_t, lay.sin_t,
-                              lay.P, lay.q, lay.kb, lay.vb, T, Hq, Hkv, dh, st, s));
+                              lay.P, lay.q, lay.kb, lay.vbt, lay.ns_pad, T, N, S, Hq, Hkv, dh,
+                              dt == DFLASH_DTYPE_BF16, st, s));
     }
-    AttnArgs aa;
-    aa.q = lay.q;
-    aa.kb = lay.kb;
-    aa.vb = lay.vb;
-    aa.kv_layer = static_cast<const uint8_t*>(kv_cache) + (size_t)l * layer_elems * es;
-    aa.anchors = anchors;
-    aa.valid = block_valid;
-    aa.mask = mask;
-    aa.out = lay.attn.out();
-    aa.B = B;
-    aa.N = N;
-    aa.S = S;
-    aa.L = L;
-    aa.Hq = Hq;
-    aa.Hkv = Hkv;
-    aa.dh = dh;
-    aa.status = st;
-    {
+    const float* kv_layer = static_cast<const float*>(kv_cache) + (size_t)l * layer_elems;
+    if (dt == DFLASH_DTYPE_BF16) {
+      AttnTcArgs aa;
+      aa.q = lay.q;
+      aa.kb = lay.kb;
+      aa.vbt = lay.vbt;
+      aa.ns_pad = lay.ns_pad;
+      aa.kv_layer = kv_layer;
+      aa.anchors = anchors;
+      aa.valid = block_valid;
+      aa.mask = mask;
+      aa.partials = lay.partials;
+      aa.out = lay.attn.out();
+      aa.B = B;
+      aa.N = N;
+      aa.S = S;
+      aa.L = L;
+      aa.Hq = Hq;
+      aa.Hkv = Hkv;
+      aa.status = st;
+      Prof pr(DFLASH_PROF_ATTENTION, 2, s);
+      DF_CUDA(launch_attention_tc(aa, s));
+    } else {
+      AttnArgs aa;
+      aa.q = lay.q;
+      aa.kb = lay.kb;
+      aa.vbt = lay.vbt;
+      aa.ns_pad = lay.ns_pad;
+      aa.kv_layer = kv_layer;
+      aa.anchors = anchors;
+      aa.valid = block_valid;
+      aa.mask = mask;
+      aa.out = lay.attn.out();
+      aa.B = B;
+      aa.N = N;
+      aa.S = S;
+      aa.L = L;
+      aa.Hq = Hq;
+      aa.Hkv = Hkv;
+      aa.dh = dh;
+      aa.status = st;
       Prof pr(DFLASH_PROF_ATTENTION, 1, s);
       DF_CUDA(launch_attention_simt(dt, aa, s));
     }

@@ -13,8 +13,9 @@
 // so whatever lies beyond the anchor cannot leak in even if it is not finite.
 //
 // One CTA per (block, KV head): its rows are the S slots x (Hq/Hkv) query heads.  Keys are
-// streamed in tiles of kKT through shared memory with an fp32 online softmax.  This kernel
-// serves the fp32 configuration and is the reference-style path for small shapes.
+// streamed in tiles of kKT through shared memory with an fp32 online softmax.  This is the
+// fp32 configuration's attention (every product and sum an fp32 FMA, no TF32); the bf16
+// configuration uses the tensor-core kernel in attention_tc.cu on the same layouts.
 #include "common.cuh"
 #include "internal.h"
 
@@ -25,10 +26,9 @@ namespace {
 constexpr int kKT = 32;
 constexpr int kThreads = 256;
 
-template <typename T>
 __global__ void __launch_bounds__(kThreads)
 attention_simt_kernel(const float* __restrict__ q, const float* __restrict__ kb,
-                      const float* __restrict__ vb, const T* __restrict__ kv_layer,
+                      const float* __restrict__ vbt, int ns_pad, const float* __restrict__ kv_layer,
                       const int32_t* __restrict__ anchors, const uint8_t* __restrict__ valid,
                       const uint8_t* __restrict__ mask, ActOut out, int N, int S, int L, int Hq,
                       int Hkv, int dh) {
@@ -51,15 +51,20 @@ attention_simt_kernel(const float* __restrict__ q, const float* __restrict__ kb,
   const int a = anchors[blk];
   const uint8_t* vrow = valid + (long)blk * S;
   const long t0 = (long)blk * S;   // first slot row of this block
-  const int Dq = Hq * dh, Dkv = Hkv * dh;
+  const int Dq = Hq * dh;
+  const int k = blk - b * N;
+  const long bg = (long)b * Hkv + g;
+  const float* qblk = q + ((bg * N + k) * R) * (long)dh;     // rows r = j * grp + hh
+  const float* kblk = kb + ((bg * N + k) * S) * (long)dh;    // [S][dh]
+  const float* vblk = vbt + bg * dh * (long)ns_pad + (long)k * S;  // [dh][ns_pad] from key 0
 
   // queries (pre-scaled by 1/sqrt(dh)); invalid slots are zero rows and get zero output
   const float scale = rsqrtf((float)dh);
   for (int e = threadIdx.x; e < R * dh; e += kThreads) {
-    const int r = e / dh, d = e - r * dh;
-    const int j = r / grp, hh = g * grp + (r - j * grp);
+    const int r = e / dh;
+    const int j = r / grp;
     const bool ok = a >= 0 && vrow[j];
-    Qs[e] = ok ? q[(t0 + j) * Dq + (long)hh * dh + d] * scale : 0.f;
+    Qs[e] = ok ? qblk[e] * scale : 0.f;
     Os[e] = 0.f;
   }
   for (int r = threadIdx.x; r < R; r += kThreads) { mrow[r] = -INFINITY; lrow[r] = 0.f; }
@@ -68,8 +73,8 @@ attention_simt_kernel(const float* __restrict__ q, const float* __restrict__ kb,
   const int n_ctx = a < 0 ? 0 : min(a, L);
   const int n_tiles_ctx = (n_ctx + kKT - 1) / kKT;
   const int n_tiles_blk = a < 0 ? 0 : (S + kKT - 1) / kKT;
-  const T* Kc = kv_layer + (((long)b * 2 + 0) * Hkv + g) * (long)L * dh;
-  const T* Vc = kv_layer + (((long)b * 2 + 1) * Hkv + g) * (long)L * dh;
+  const float* Kc = kv_layer + (((long)b * 2 + 0) * Hkv + g) * (long)L * dh;   // [L][dh]
+  const float* Vc = kv_layer + (((long)b * 2 + 1) * Hkv + g) * (long)L * dh;   // [dh][L]
   const uint8_t* mrow_b = mask + (long)b * L;
 
   for (int tile = 0; tile < n_tiles_ctx + n_tiles_blk; ++tile) {
@@ -87,10 +92,10 @@ attention_simt_kernel(const float* __restrict__ q, const float* __restrict__ kb,
       const int key = base + kk;
       float kvk = 0.f, kvv = 0.f;
       if (is_ctx) {
-        if (key < n_ctx) { kvk = to_f(Kc[(long)key * dh + d]); kvv = to_f(Vc[(long)key * dh + d]); }
+        if (key < n_ctx) { kvk = Kc[(long)key * dh + d]; kvv = Vc[(long)d * L + key]; }
       } else if (key < S) {
-        kvk = kb[(t0 + key) * Dkv + (long)g * dh + d];
-        kvv = vb[(t0 + key) * Dkv + (long)g * dh + d];
+        kvk = kblk[(long)key * dh + d];
+        kvv = vblk[(long)d * ns_pad + key];
       }
       Ks[kk * (dh + 1) + d] = kvk;
       Vs[kk * dh + d] = kvv;
@@ -153,24 +158,15 @@ size_t attention_simt_smem(int S, int grp, int dh) {
 }
 
 cudaError_t launch_attention_simt(int dtype, const AttnArgs& a, cudaStream_t stream) {
+  (void)dtype;
   const size_t smem = attention_simt_smem(a.S, a.Hq / a.Hkv, a.dh);
   dim3 grid(a.B * a.N, a.Hkv);
-  cudaError_t e;
-  if (dtype == DFLASH_DTYPE_BF16) {
-    auto kern = attention_simt_kernel<__nv_bfloat16>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, stream>>>(a.q, a.kb, a.vb, (const __nv_bfloat16*)a.kv_layer,
-                                           a.anchors, a.valid, a.mask, a.out, a.N, a.S, a.L, a.Hq,
-                                           a.Hkv, a.dh);
-  } else {
-    auto kern = attention_simt_kernel<float>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, stream>>>(a.q, a.kb, a.vb, (const float*)a.kv_layer, a.anchors,
-                                           a.valid, a.mask, a.out, a.N, a.S, a.L, a.Hq, a.Hkv,
-                                           a.dh);
-  }
+  cudaError_t e = cudaFuncSetAttribute(attention_simt_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  attention_simt_kernel<<<grid, kThreads, smem, stream>>>(a.q, a.kb, a.vbt, a.ns_pad, a.kv_layer,
+                                                          a.anchors, a.valid, a.mask, a.out, a.N,
+                                                          a.S, a.L, a.Hq, a.Hkv, a.dh);
   return cudaGetLastError();
 }
 

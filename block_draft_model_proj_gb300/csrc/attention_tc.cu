@@ -1,0 +1,560 @@
+// Anchored block-sparse dual-source attention on the 5th-generation tensor cores.
+//
+// "DFlash Draft Body", How It Works step 3: within a layer each block reads the target
+// prefix before its anchor and all positions of the same block, never another block, and
+// the target sequence is not updated.  "DFlash" (How it works): the target's projected K/V
+// are attended alongside the draft tokens' own K/V.  "DFlash: drafting, verification, and
+// speed" (One DFlash generation cycle): a block must not read target features containing
+// its future answers, hence the strict prefix c < anchor.
+//
+// Key set of a valid slot of block (b, k), anchor a: context positions c < min(a, L) with
+// mask[b, c] != 0, plus every valid slot of block (b, k).  GQA: query head h reads KV head
+// h / (Hq / Hkv).  Excluded keys are removed by selection (never by an additive -inf), and
+// value columns past the last readable key are zeroed in shared memory, so nothing beyond
+// a block's prefix -- not even a non-finite value -- can reach its output.
+//
+// Work unit = (row b, KV head g, query tile t, key chunk c).  A query tile packs the
+// S x (Hq/Hkv) query rows of 128 / (S * Hq/Hkv) consecutive blocks of (b, g) into the 128
+// lanes of an M = 128 MMA; consecutive blocks have nearby anchors (the plan sorts them), so
+// one key range serves the whole tile and per-row anchors only mask the tail.  The prefix is
+// cut into chunks of `chunk` keys so long prefixes spread over many SMs; chunk 0 also takes
+// the tile's own-block keys.  Each unit writes an unnormalised partial (m, l, O) per row;
+// attn_combine_kernel merges the chunks of a tile in chunk order (deterministic) and writes
+// the two-term bf16 attention output for the O projection.
+//
+// Arithmetic: kind::tf32 MMAs with fp32 accumulation.  Q, the block K/V and the context K/V
+// cache are fp32 values rounded to tf32, P is rounded to tf32; the softmax runs in fp32 in
+// registers (one TMEM lane = one query row per thread), base-2 exponent, with a lazily
+// updated running maximum (the accumulator is rescaled only when the maximum grows by more
+// than 2^8, so P stays <= 256).
+//
+// Warp roles: warp 0 TMA producer (Q once; K and V^T tiles of 64 keys, 2-stage ring),
+// warp 1 MMA issuer (S = Q K^T into a double-buffered TMEM S/P area; O += P V with P read
+// from TMEM), warps 2-5 softmax / correction / partial output.  Every mbarrier wait is
+// bounded in time; on expiry the CTA reports DFLASH_ERR_TIMEOUT, drains its own copies and
+// MMAs, frees tensor memory and exits.
+#include "common.cuh"
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace dflash {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kDH = 128;   // head dim handled by this kernel
+constexpr int kM = 128;    // query rows per tile (TMEM lanes)
+constexpr int kKT = 64;    // keys per tile
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 256;      // O [0,128) + S/P buffers [128,192), [192,256)
+constexpr uint32_t kQSub = kM * 32 * 4;  // [128 rows][32 dh] fp32, 16 KB
+constexpr uint32_t kQBytes = 4 * kQSub;  // 64 KB
+constexpr uint32_t kKSub = kKT * 32 * 4; // [64 keys][32 dh], 8 KB
+constexpr uint32_t kKBytes = 4 * kKSub;  // 32 KB
+constexpr uint32_t kVSub = kDH * 32 * 4; // V^T [128 dh][32 keys], 16 KB
+constexpr uint32_t kVBytes = 2 * kVSub;  // 32 KB
+constexpr uint32_t kStageBytes = kKBytes + kVBytes;
+constexpr size_t kSmemBytes = 1024 + kQBytes + kStages * (size_t)kStageBytes + 256;
+constexpr uint32_t kIdescS = idesc_tf32(kM, kKT);
+constexpr uint32_t kIdescPV = idesc_tf32(kM, kDH);
+constexpr float kRescaleLog2 = 8.0f;
+
+struct AttnTcParams {
+  int B, N, S, L, Hkv, grp, R, bpt, tiles, chunk, max_chunks;
+  const int32_t* anchors;
+  const uint8_t* valid;
+  const uint8_t* mask;
+  float* part_o;  // [units][128][128]
+  float* part_m;  // [units][128]
+  float* part_l;  // [units][128]
+  unsigned* status;
+  float scale_log2;
+};
+
+struct UnitInfo {
+  int b, g, t, c, k0, k1, a_max, cs, ce, nblk, n;
+};
+
+__device__ __forceinline__ UnitInfo decode_unit(const AttnTcParams& p, int unit) {
+  UnitInfo u;
+  u.c = unit % p.max_chunks;
+  int rest = unit / p.max_chunks;
+  u.t = rest % p.tiles;
+  rest /= p.tiles;
+  u.g = rest % p.Hkv;
+  u.b = rest / p.Hkv;
+  u.k0 = u.t * p.bpt;
+  u.k1 = min(p.N, u.k0 + p.bpt);
+  int amax = 0;
+  for (int k = u.k0; k < u.k1; ++k) {
+    const int a = p.anchors[u.b * p.N + k];
+    if (a > amax) amax = a;
+  }
+  u.a_max = min(amax, p.L);
+  u.cs = u.c * p.chunk;
+  u.ce = min(u.cs + p.chunk, u.a_max);
+  // chunk 0 also takes the tile's own-block keys: bpt * S of them, in tiles of kKT
+  u.nblk = u.c == 0 ? (p.bpt * p.S + kKT - 1) / kKT : 0;
+  const int nctx = u.ce > u.cs ? (u.ce - u.cs + kKT - 1) / kKT : 0;
+  u.n = u.nblk + nctx;
+  return u;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kc,
+               const __grid_constant__ CUtensorMap map_vc, const __grid_constant__ CUtensorMap map_kb,
+               const __grid_constant__ CUtensorMap map_vb, const AttnTcParams p) {
+  const UnitInfo u = decode_unit(p, blockIdx.x);
+  if (u.n == 0) return;  // a chunk past this tile's longest prefix: no work
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + kQBytes;  // stage s: K at s*kStageBytes, V^T after it
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + kStages * kStageBytes);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + kStages;
+  uint64_t* s_full = kv_empty + kStages;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* drain = pv_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&pv_done[i], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem_o = tmem;
+  const uint32_t tmem_s0 = tmem + 128;
+
+  const int planes_per_b = 2 * p.Hkv;
+  const int plane_k = u.b * planes_per_b + u.g;
+  const int plane_v = u.b * planes_per_b + p.Hkv + u.g;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      const int qrow0 = ((u.b * p.Hkv + u.g) * p.N + u.k0) * p.R;
+      mbar_arrive_expect_tx(q_full, kQBytes);
+      for (int q = 0; q < 4; ++q) tma_load_2d(&map_q, q_full, sQ + q * kQSub, q * 32, qrow0);
+      int issued[kStages] = {0, 0};
+      uint32_t issued_ph[kStages] = {0, 0};
+      for (int i = 0; i < u.n; ++i) {
+        const int st = i % kStages;
+        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+        if (!mbar_wait(&kv_empty[st], ph ^ 1u, abort_flag, kWaitLimitNs)) break;
+        mbar_arrive_expect_tx(&kv_full[st], kStageBytes);
+        uint8_t* sK = sKV + st * kStageBytes;
+        uint8_t* sV = sK + kKBytes;
+        if (i < u.nblk) {
+          const int kbrow0 = ((u.b * p.Hkv + u.g) * p.N + u.k0) * p.S + i * kKT;
+          for (int q = 0; q < 4; ++q) tma_load_2d(&map_kb, &kv_full[st], sK + q * kKSub, q * 32, kbrow0);
+          for (int v = 0; v < 2; ++v)
+            tma_load_2d(&map_vb, &kv_full[st], sV + v * kVSub, u.k0 * p.S + i * kKT + v * 32,
+                        (u.b * p.Hkv + u.g) * kDH);
+        } else {
+          const int c0 = u.cs + (i - u.nblk) * kKT;
+          for (int q = 0; q < 4; ++q) tma_load_3d(&map_kc, &kv_full[st], sK + q * kKSub, q * 32, c0, plane_k);
+          for (int v = 0; v < 2; ++v)
+            tma_load_3d(&map_vc, &kv_full[st], sV + v * kVSub, c0 + v * 32, 0, plane_v);
+        }
+        issued[st] = 1;
+        issued_ph[st] = ph;
+      }
+      mbar_wait(q_full, 0, abort_flag, kWaitLimitNs / 4);
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s]) mbar_wait(&kv_full[s], issued_ph[s], abort_flag, kWaitLimitNs / 4);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      bool ok = mbar_wait(q_full, 0, abort_flag, kWaitLimitNs);
+      const uint32_t q_addr = smem_u32(sQ);
+      auto issue_pv = [&](int j) -> bool {
+        if (!mbar_wait(&p_full[j & 1], (uint32_t)(j >> 1) & 1u, abort_flag, kWaitLimitNs)) return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sKV + (j % kStages) * kStageBytes + kKBytes);
+        const uint32_t a_base = tmem_s0 + (uint32_t)((j & 1) * kKT);
+        for (int v = 0; v < 2; ++v)
+          for (int k = 0; k < 4; ++k)
+            umma_tf32_ts(tmem_o, a_base + v * 32 + k * 8, sw128_desc(v_addr + v * kVSub + k * 32),
+                         kIdescPV, (j == 0 && v == 0 && k == 0) ? 0u : 1u);
+        umma_commit(&pv_done[j & 1]);
+        umma_commit(&kv_empty[j % kStages]);
+        return true;
+      };
+      for (int i = 0; i < u.n && ok; ++i) {
+        const int st = i % kStages;
+        if (!mbar_wait(&kv_full[st], (uint32_t)(i / kStages) & 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
+        // the S/P buffer of tile i last held P of tile i-2: its PV must be complete
+        if (i >= 2 && !mbar_wait(&pv_done[i & 1], (uint32_t)((i - 2) >> 1) & 1u, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sKV + st * kStageBytes);
+        const uint32_t s_tmem = tmem_s0 + (uint32_t)((i & 1) * kKT);
+        for (int q = 0; q < 4; ++q)
+          for (int k = 0; k < 4; ++k)
+            umma_tf32_ss(s_tmem, sw128_desc(q_addr + q * kQSub + k * 32),
+                         sw128_desc(k_addr + q * kKSub + k * 32), kIdescS, (q | k) ? 1u : 0u);
+        umma_commit(&s_full[i & 1]);
+        if (i >= 1 && !issue_pv(i - 1)) { ok = false; break; }
+      }
+      if (ok) issue_pv(u.n - 1);
+      umma_commit(drain);
+      mbar_wait(drain, 0, abort_flag, kWaitLimitNs / 4);
+    }
+  } else {
+    // ---------------- softmax / correction / partial output (warps 2..5) ----------------
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // query row = TMEM lane
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int kbo = r / p.R;
+    const int within = r - kbo * p.R;
+    const int j = within / p.grp;
+    const int kb = u.k0 + kbo;
+    bool row_valid = false;
+    int a_row = 0;
+    if (kb < u.k1) {
+      const int a = p.anchors[u.b * p.N + kb];
+      row_valid = a >= 0 && p.valid[(u.b * p.N + kb) * p.S + j] != 0;
+      a_row = min(max(a, 0), p.L);
+    }
+    const uint8_t* mrow = p.mask + (size_t)u.b * p.L;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    // every wait result is made warp-uniform: the tcgen05.ld / st below are .sync.aligned
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, kWaitLimitNs) ? 1 : 0) != 0;
+    };
+    for (int i = 0; i < u.n && ok; ++i) {
+      if (!wait_all(&s_full[i & 1], (uint32_t)(i >> 1) & 1u)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t s_tmem = tmem_s0 + (uint32_t)((i & 1) * kKT) + lane_off;
+      uint32_t sv[kKT];
+      tmem_ld_32x32b_x32(s_tmem, sv);
+      tmem_ld_32x32b_x32(s_tmem + 32, sv + 32);
+      const bool blk_tile = i < u.nblk;
+      const int c0 = blk_tile ? 0 : u.cs + (i - u.nblk) * kKT;
+      float x[kKT];
+      float mt = -INFINITY;
+      if (blk_tile) {
+#pragma unroll
+        for (int kk = 0; kk < kKT; ++kk) {
+          const int q = u.k0 * p.S + i * kKT + kk;
+          const int kbk = q / p.S, jj = q - kbk * p.S;
+          const bool okk = row_valid && kbk == kb && p.valid[(u.b * p.N + kbk) * p.S + jj] != 0;
+          x[kk] = okk ? __uint_as_float(sv[kk]) * p.scale_log2 : -INFINITY;
+          mt = fmaxf(mt, x[kk]);
+        }
+      } else {
+#pragma unroll
+        for (int w4 = 0; w4 < kKT / 4; ++w4) {
+          const int c = c0 + 4 * w4;
+          uint32_t mw = 0;
+          if (row_valid && c < a_row && c < u.ce) mw = *reinterpret_cast<const uint32_t*>(mrow + c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int kk = 4 * w4 + e;
+            const bool okk = ((mw >> (8 * e)) & 0xFFu) != 0 && c + e < a_row && c + e < u.ce;
+            x[kk] = okk ? __uint_as_float(sv[kk]) * p.scale_log2 : -INFINITY;
+            mt = fmaxf(mt, x[kk]);
+          }
+        }
+      }
+      // running maximum: taken as is the first time a row sees a key, otherwise kept
+      // unless the tile's maximum exceeds it by more than 2^8 (then the accumulator and
+      // the row sum are rescaled)
+      float factor = 1.f;
+      if (mt > m_run) {
+        if (m_run == -INFINITY) {
+          m_run = mt;
+        } else if (mt > m_run + kRescaleLog2) {
+          factor = exp2f(m_run - mt);
+          m_run = mt;
+        }
+      }
+      if (__any_sync(0xffffffffu, factor != 1.f)) {
+        // the PV of the previous tile must have landed before the accumulator is touched
+        if (!wait_all(&pv_done[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1u)) { ok = false; break; }
+        tc_fence_after();
+        for (int part = 0; part < 4; ++part) {
+          uint32_t ov[32];
+          tmem_ld_32x32b_x32(tmem_o + lane_off + part * 32, ov);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
+          tmem_st_32x32b_x32(tmem_o + lane_off + part * 32, ov);
+        }
+        tmem_wait_st();
+        l_run *= factor;
+      }
+      float lsum = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < kKT; ++kk) {
+        const float pv = x[kk] == -INFINITY ? 0.f : round_tf32(exp2f(x[kk] - m_run));
+        lsum += pv;
+        sv[kk] = __float_as_uint(pv);
+      }
+      l_run += lsum;
+      tmem_st_32x32b_x32(s_tmem, sv);
+      tmem_st_32x32b_x32(s_tmem + 32, sv + 32);
+      tmem_wait_st();
+      // value columns past the last readable key of this tile: zero them (thread r owns
+      // V^T row r) so that whatever the cache holds there cannot meet a zero P as NaN
+      if (!blk_tile && c0 + kKT > u.a_max) {
+        const int st = i % kStages;
+        if (!wait_all(&kv_full[st], (uint32_t)(i / kStages) & 1u)) { ok = false; break; }
+        const int nvalid = u.a_max - c0;
+        uint8_t* sV = sKV + st * kStageBytes + kKBytes;
+        for (int v = 0; v < 2; ++v) {
+          uint8_t* rowp = sV + v * kVSub + (r >> 3) * 1024 + (r & 7) * 128;
+          for (int ch = 0; ch < 8; ++ch) {
+            const int key0 = v * 32 + ch * 4;
+            if (key0 + 4 <= nvalid) continue;
+            float4* dst = reinterpret_cast<float4*>(rowp + ((ch ^ (r & 7)) * 16));
+            float4 val = *dst;
+            if (key0 + 0 >= nvalid) val.x = 0.f;
+            if (key0 + 1 >= nvalid) val.y = 0.f;
+            if (key0 + 2 >= nvalid) val.z = 0.f;
+            if (key0 + 3 >= nvalid) val.w = 0.f;
+            *dst = val;
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[i & 1]);
+    }
+    // final accumulator -> partial (m, l, O) of this unit
+    if (ok && wait_all(&pv_done[(u.n - 1) & 1], (uint32_t)((u.n - 1) >> 1) & 1u)) {
+      tc_fence_after();
+      const size_t rowi = (size_t)blockIdx.x * kM + r;
+      float4* po = reinterpret_cast<float4*>(p.part_o + rowi * kDH);
+      for (int part = 0; part < 4; ++part) {
+        uint32_t ov[32];
+        tmem_ld_32x32b_x32(tmem_o + lane_off + part * 32, ov);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          po[part * 8 + e] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                                         __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]));
+      }
+      p.part_m[rowi] = m_run;
+      p.part_l[rowi] = l_run;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 0 && *abort_flag) report(p.status, kStatusTimeout, kKernAttnTc);
+}
+
+// One warp per query row of a tile: merge the chunk partials in chunk order, normalise,
+// write the two-term attention output row [t][(g*grp + h)*dh ...].
+__global__ void attn_combine_kernel(const AttnTcParams p, ActOut out, int Hq) {
+  const int warps = blockDim.x >> 5;
+  const long gw = (long)blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const long total = (long)p.B * p.Hkv * p.tiles * kM;
+  if (gw >= total) return;
+  const int r = (int)(gw % kM);
+  long rest = gw / kM;
+  const int t = (int)(rest % p.tiles);
+  rest /= p.tiles;
+  const int g = (int)(rest % p.Hkv);
+  const int b = (int)(rest / p.Hkv);
+  const int k0 = t * p.bpt, k1 = min(p.N, k0 + p.bpt);
+  const int kbo = r / p.R;
+  if (kbo >= p.bpt) return;
+  const int kb = k0 + kbo;
+  if (kb >= k1) return;
+  const int within = r - kbo * p.R;
+  const int j = within / p.grp, h = within - j * p.grp;
+  const long trow = ((long)b * p.N + kb) * p.S + j;
+  const long col0 = (long)(g * p.grp + h) * kDH;
+  const long orow = trow * (long)Hq * kDH + col0;
+  const int a = p.anchors[b * p.N + kb];
+  const bool row_valid = a >= 0 && p.valid[((long)b * p.N + kb) * p.S + j] != 0;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float lsum = 0.f;
+  if (row_valid) {
+    int amax = 0;
+    for (int k = k0; k < k1; ++k) amax = max(amax, p.anchors[b * p.N + k]);
+    amax = min(amax, p.L);
+    const int nch = amax > p.chunk ? (amax + p.chunk - 1) / p.chunk : 1;
+    const long unit0 = (((long)b * p.Hkv + g) * p.tiles + t) * p.max_chunks;
+    float M = -INFINITY;
+    for (int c = 0; c < nch; ++c) {
+      const long ri = (unit0 + c) * kM + r;
+      if (p.part_l[ri] > 0.f) M = fmaxf(M, p.part_m[ri]);
+    }
+    for (int c = 0; c < nch; ++c) {
+      const long ri = (unit0 + c) * kM + r;
+      const float l = p.part_l[ri];
+      if (!(l > 0.f)) continue;
+      const float f = exp2f(p.part_m[ri] - M);
+      lsum += l * f;
+      const float4 o = reinterpret_cast<const float4*>(p.part_o + ri * kDH)[lane];
+      acc[0] += o.x * f;
+      acc[1] += o.y * f;
+      acc[2] += o.z * f;
+      acc[3] += o.w * f;
+    }
+  }
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  for (int e = 0; e < 4; ++e) out.store(orow + lane * 4 + e, acc[e] * inv);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// fp32 map with a 128-byte swizzle; dims/box innermost first; strides in bytes for dims 1..
+bool encode_f32(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                const cuuint64_t* strides, const cuuint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+AttnTcLayout attention_tc_layout(int B, int N, int S, int L, int Hq, int Hkv) {
+  AttnTcLayout lay;
+  lay.grp = Hq / Hkv;
+  lay.R = S * lay.grp;
+  lay.bpt = kM / lay.R;
+  lay.tiles = (N + lay.bpt - 1) / lay.bpt;
+  lay.chunk = L > 16384 ? 4096 : 2048;
+  lay.max_chunks = (L + lay.chunk - 1) / lay.chunk;
+  if (lay.max_chunks < 1) lay.max_chunks = 1;
+  lay.units = (long)B * Hkv * lay.tiles * lay.max_chunks;
+  lay.part_floats = lay.units * kM * (kDH + 2);
+  return lay;
+}
+
+bool attention_tc_supported(int S, int Hq, int Hkv, int dh) {
+  if (dh != kDH || Hq % Hkv != 0) return false;
+  const int R = S * (Hq / Hkv);
+  return R >= 1 && R <= kM && (kM % R) == 0;
+}
+
+cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream) {
+  const AttnTcLayout lay = attention_tc_layout(a.B, a.N, a.S, a.L, a.Hq, a.Hkv);
+  AttnTcParams p;
+  p.B = a.B;
+  p.N = a.N;
+  p.S = a.S;
+  p.L = a.L;
+  p.Hkv = a.Hkv;
+  p.grp = lay.grp;
+  p.R = lay.R;
+  p.bpt = lay.bpt;
+  p.tiles = lay.tiles;
+  p.chunk = lay.chunk;
+  p.max_chunks = lay.max_chunks;
+  p.anchors = a.anchors;
+  p.valid = a.valid;
+  p.mask = a.mask;
+  p.part_o = a.partials;
+  p.part_m = a.partials + lay.units * kM * kDH;
+  p.part_l = p.part_m + lay.units * kM;
+  p.status = a.status;
+  p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)kDH));
+
+  CUtensorMap mq, mkc, mvc, mkb, mvb;
+  const long q_rows = (long)a.B * a.Hkv * a.N * lay.R;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)kDH, (cuuint64_t)q_rows};
+    cuuint64_t str[1] = {(cuuint64_t)kDH * 4};
+    cuuint32_t box[2] = {32, (cuuint32_t)kM};
+    if (!encode_f32(&mq, a.q, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  const long planes = (long)a.B * 2 * a.Hkv;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)kDH, (cuuint64_t)a.L, (cuuint64_t)planes};
+    cuuint64_t str[2] = {(cuuint64_t)kDH * 4, (cuuint64_t)a.L * kDH * 4};
+    cuuint32_t box[3] = {32, (cuuint32_t)kKT, 1};
+    if (!encode_f32(&mkc, a.kv_layer, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)a.L, (cuuint64_t)kDH, (cuuint64_t)planes};
+    cuuint64_t str[2] = {(cuuint64_t)a.L * 4, (cuuint64_t)a.L * kDH * 4};
+    cuuint32_t box[3] = {32, (cuuint32_t)kDH, 1};
+    if (!encode_f32(&mvc, a.kv_layer, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const long kb_rows = (long)a.B * a.Hkv * a.N * a.S;
+    cuuint64_t dims[2] = {(cuuint64_t)kDH, (cuuint64_t)kb_rows};
+    cuuint64_t str[1] = {(cuuint64_t)kDH * 4};
+    cuuint32_t box[2] = {32, (cuuint32_t)kKT};
+    if (!encode_f32(&mkb, a.kb, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)a.N * a.S, (cuuint64_t)a.B * a.Hkv * kDH};
+    cuuint64_t str[1] = {(cuuint64_t)a.ns_pad * 4};
+    cuuint32_t box[2] = {32, (cuuint32_t)kDH};
+    if (!encode_f32(&mvb, a.vbt, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  attn_tc_kernel<<<(unsigned)lay.units, kThreads, kSmemBytes, stream>>>(mq, mkc, mvc, mkb, mvb, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long rows = (long)a.B * a.Hkv * lay.tiles * kM;
+  const int threads = 256;
+  const long blocks = (rows * 32 + threads - 1) / threads;
+  attn_combine_kernel<<<(unsigned)blocks, threads, 0, stream>>>(p, a.out, a.Hq);
+  return cudaGetLastError();
+}
+
+}  // namespace dflash

@@ -51,19 +51,21 @@ cudaError_t launch_residual_norm(int mode, int dtype, float* x, const void* emb,
 cudaError_t launch_rows_norm(int dtype, const float* y, int nsplit, const void* g, double eps,
                              bool with_norm, ActOut out, long rows, int D, cudaStream_t stream);
 
-// QKV epilogue: y [nsplit][T][(Hq+2Hkv)*dh] fp32 -> q [T][Hq*dh], k/v [T][Hkv*dh] (fp32),
-// RoPE on q and k at position pos[t] (table of P positions; out-of-range valid slots report
-// a device check and use position 0).
+// QKV epilogue: y [nsplit][T][(Hq+2Hkv)*dh] fp32 -> attention-ready fp32 operands
+// q [B][Hkv][N][S][grp][dh], kb [B][Hkv][N*S][dh], vbt [B][Hkv][dh][ns_pad]; RoPE on q and
+// k at position pos[t] (table of P positions; out-of-range valid slots report a device
+// check and use position 0); values rounded to tf32 when to_tf32.
 cudaError_t launch_qkv_rope(const float* y, int nsplit, const int32_t* pos, const uint8_t* valid,
-                            const float* cos_t, const float* sin_t, int P, float* q, float* k,
-                            float* v, long T, int Hq, int Hkv, int dh, unsigned* status,
-                            cudaStream_t stream);
+                            const float* cos_t, const float* sin_t, int P, float* q, float* kb,
+                            float* vbt, int ns_pad, long T, int N, int S, int Hq, int Hkv, int dh,
+                            bool to_tf32, unsigned* status, cudaStream_t stream);
 
-// Context K/V epilogue: y [nsplit][B*L][2*Hkv*dh] fp32 -> kv_layer [B][2][Hkv][L_cache][dh]
-// at positions pos_offset + c, RoPE on K (table row c = position pos_offset + c).
-cudaError_t launch_ctx_kv_scatter(int dtype, const float* y, int nsplit,
-                                  const float* cos_t, const float* sin_t, void* kv_layer, int B,
-                                  int L, int pos_offset, int L_cache, int Hkv, int dh,
+// Context K/V epilogue: y [nsplit][B*L][2*Hkv*dh] fp32 -> the fp32 cache planes of one layer
+// [B][2][Hkv]: K as [L_cache][dh] (RoPE'd; table row c = position pos_offset + c) and V^T as
+// [dh][L_cache], at positions pos_offset + c; rounded to tf32 when to_tf32.
+cudaError_t launch_ctx_kv_scatter(const float* y, int nsplit, const float* cos_t,
+                                  const float* sin_t, float* kv_layer, int B, int L,
+                                  int pos_offset, int L_cache, int Hkv, int dh, bool to_tf32,
                                   cudaStream_t stream);
 
 // SwiGLU epilogue: y [nsplit][T][2I] fp32 (gate | up) -> act [T][I] = SiLU(gate) * up.
@@ -84,10 +86,11 @@ cudaError_t launch_gemm_tc(const void* A, const void* A_lo, long lda, const void
 
 // ---- attention.cu ----
 struct AttnArgs {
-  const float* q;           // [T][Hq*dh] fp32, T = B*N*S
-  const float* kb;          // [T][Hkv*dh] fp32
-  const float* vb;          // [T][Hkv*dh] fp32
-  const void* kv_layer;     // [B][2][Hkv][L][dh], configuration dtype
+  const float* q;           // [B][Hkv][N][S][grp][dh]
+  const float* kb;          // [B][Hkv][N*S][dh]
+  const float* vbt;         // [B][Hkv][dh][ns_pad]
+  int ns_pad;
+  const float* kv_layer;    // [B][2][Hkv] planes: K [L][dh], V^T [dh][L]
   const int32_t* anchors;   // [B][N]
   const uint8_t* valid;     // [B][N][S]
   const uint8_t* mask;      // [B][L]
@@ -96,5 +99,29 @@ struct AttnArgs {
   unsigned* status;
 };
 cudaError_t launch_attention_simt(int dtype, const AttnArgs& a, cudaStream_t stream);
+
+// ---- attention_tc.cu: tcgen05 (kind::tf32) attention over attention-ready layouts ----
+struct AttnTcArgs {
+  const float* q;           // [B][Hkv][N][S][grp][dh], tf32-rounded
+  const float* kb;          // [B][Hkv][N*S][dh] block keys, tf32-rounded
+  const float* vbt;         // [B][Hkv][dh][ns_pad] block values transposed, tf32-rounded
+  int ns_pad;               // row stride of vbt (>= N*S, multiple of 4)
+  const float* kv_layer;    // [B][2][Hkv] planes: K [L][dh], V^T [dh][L] (fp32)
+  const int32_t* anchors;
+  const uint8_t* valid;
+  const uint8_t* mask;
+  float* partials;          // attention_tc_layout(...).part_floats floats
+  ActOut out;               // [T][Hq*dh]
+  int B, N, S, L, Hq, Hkv;
+  unsigned* status;
+};
+struct AttnTcLayout {
+  int grp, R, bpt, tiles, chunk, max_chunks;
+  long units;
+  long part_floats;
+};
+AttnTcLayout attention_tc_layout(int B, int N, int S, int L, int Hq, int Hkv);
+bool attention_tc_supported(int S, int Hq, int Hkv, int dh);
+cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream);
 
 }  // namespace dflash

@@ -24,11 +24,6 @@ __device__ __forceinline__ float ld(const void* p, int dt, long i) {
                                  : static_cast<const float*>(p)[i];
 }
 
-__device__ __forceinline__ void st(void* p, int dt, long i, float v) {
-  if (dt == DFLASH_DTYPE_BF16) static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
-  else static_cast<float*>(p)[i] = v;
-}
-
 __global__ void rope_table_kernel(float* __restrict__ cos_t, float* __restrict__ sin_t, int p0,
                                   int P, int half, int head_dim, double theta) {
   const long n = (long)P * half;
@@ -106,15 +101,27 @@ __device__ __forceinline__ float sum_splits(const float* y, int nsplit, long str
   return v;
 }
 
-// one thread per (row t, head, channel pair i); q / k / v are written in fp32
+__device__ __forceinline__ float maybe_tf32(float v, bool to_tf32) {
+  if (!to_tf32) return v;
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+  return __uint_as_float(r);
+}
+
+// One thread per (row t, head, channel pair i).  Writes the attention operands in the
+// attention-ready layouts (fp32; rounded to tf32 when `to_tf32`):
+//   q   [B][Hkv][N][S][grp][dh]   (the query rows of one KV head are contiguous per block)
+//   kb  [B][Hkv][N*S][dh]         (block keys)
+//   vbt [B][Hkv][dh][ns_pad]      (block values, transposed)
 __global__ void qkv_rope_kernel(const float* __restrict__ y, int nsplit, long split_stride,
                                 const int32_t* __restrict__ pos, const uint8_t* __restrict__ valid,
                                 const float* __restrict__ cos_t, const float* __restrict__ sin_t,
-                                int P, float* __restrict__ q, float* __restrict__ k,
-                                float* __restrict__ v, long T, int Hq, int Hkv, int dh,
-                                unsigned* status) {
+                                int P, float* __restrict__ q, float* __restrict__ kb,
+                                float* __restrict__ vbt, int ns_pad, long T, int N, int S, int Hq,
+                                int Hkv, int dh, bool to_tf32, unsigned* status) {
   const int half = dh / 2;
   const int heads = Hq + 2 * Hkv;
+  const int grp = Hq / Hkv;
   const long width = (long)heads * dh;
   const long n = T * heads * half;
   for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n;
@@ -125,59 +132,79 @@ __global__ void qkv_rope_kernel(const float* __restrict__ y, int nsplit, long sp
     const long base = t * width + (long)hd * dh;
     const float a = sum_splits(y, nsplit, split_stride, base + i);
     const float bb = sum_splits(y, nsplit, split_stride, base + i + half);
-    if (hd >= Hq + Hkv) {  // V: no rotation
-      const long o = t * Hkv * dh + (long)(hd - Hq - Hkv) * dh;
-      v[o + i] = a;
-      v[o + i + half] = bb;
+    const int b = (int)(t / ((long)N * S));
+    const int ks = (int)(t - (long)b * N * S);  // k * S + j
+    const int k = ks / S, j = ks - k * S;
+    if (hd >= Hq + Hkv) {  // V: no rotation, transposed
+      const int g = hd - Hq - Hkv;
+      float* dst = vbt + ((long)(b * Hkv + g) * dh) * ns_pad + ks;
+      dst[(long)i * ns_pad] = maybe_tf32(a, to_tf32);
+      dst[(long)(i + half) * ns_pad] = maybe_tf32(bb, to_tf32);
       continue;
     }
-    int p = pos[t];
-    if (p < 0 || p >= P) {
+    int pp = pos[t];
+    if (pp < 0 || pp >= P) {
       if (valid[t] && i == 0) report(status, kStatusCheck, kKernEpilogue);
-      p = 0;
+      pp = 0;
     }
-    const float c = cos_t[(long)p * half + i], s = sin_t[(long)p * half + i];
-    const float lo = a * c - bb * s, hi = bb * c + a * s;
+    const float c = cos_t[(long)pp * half + i], sn = sin_t[(long)pp * half + i];
+    const float lo = a * c - bb * sn, hi = bb * c + a * sn;
+    float* dst;
     if (hd < Hq) {
-      const long o = t * Hq * dh + (long)hd * dh;
-      q[o + i] = lo;
-      q[o + i + half] = hi;
+      const int g = hd / grp, h = hd - g * grp;
+      dst = q + (((((long)b * Hkv + g) * N + k) * S + j) * grp + h) * dh;
     } else {
-      const long o = t * Hkv * dh + (long)(hd - Hq) * dh;
-      k[o + i] = lo;
-      k[o + i + half] = hi;
+      const int g = hd - Hq;
+      dst = kb + ((((long)b * Hkv + g) * N + k) * S + j) * dh;
     }
+    dst[i] = maybe_tf32(lo, to_tf32);
+    dst[i + half] = maybe_tf32(hi, to_tf32);
   }
 }
 
-// one thread per (b, c, kv, head, pair i); the cache is stored in the configuration dtype
-__global__ void ctx_kv_scatter_kernel(int dt, const float* __restrict__ y, int nsplit,
-                                      long split_stride, const float* __restrict__ cos_t,
-                                      const float* __restrict__ sin_t, void* __restrict__ kv,
-                                      int B, int L, int pos_offset, int L_cache, int Hkv, int dh) {
+// Context K: one thread per (b, c, head, pair i); plane (b, 0, g) holds K as [L_cache][dh].
+__global__ void ctx_k_scatter_kernel(const float* __restrict__ y, int nsplit, long split_stride,
+                                     const float* __restrict__ cos_t,
+                                     const float* __restrict__ sin_t, float* __restrict__ kv,
+                                     int B, int L, int pos_offset, int L_cache, int Hkv, int dh,
+                                     bool to_tf32) {
   const int half = dh / 2;
-  const long per_row = 2L * Hkv * half;
+  const long per_row = (long)Hkv * half;
   const long n = (long)B * L * per_row;
   for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n;
        e += (long)gridDim.x * blockDim.x) {
     const long bc = e / per_row;
     const int rem = (int)(e - bc * per_row);
-    const int hd = rem / half, i = rem - hd * half;  // hd in [0, 2*Hkv): K heads then V heads
+    const int g = rem / half, i = rem - g * half;
     const int b = (int)(bc / L), c = (int)(bc - (long)b * L);
-    const long src = bc * 2L * Hkv * dh + (long)hd * dh;
-    float a = sum_splits(y, nsplit, split_stride, src + i);
-    float bb = sum_splits(y, nsplit, split_stride, src + i + half);
-    const int kvsel = hd / Hkv, g = hd - kvsel * Hkv;
-    const int p = pos_offset + c;
-    if (kvsel == 0) {  // table row c holds position pos_offset + c
-      const float cs = cos_t[(long)c * half + i], sn = sin_t[(long)c * half + i];
-      const float lo = a * cs - bb * sn, hi = bb * cs + a * sn;
-      a = lo;
-      bb = hi;
-    }
-    const long dst = ((((long)b * 2 + kvsel) * Hkv + g) * L_cache + p) * dh;
-    st(kv, dt, dst + i, a);
-    st(kv, dt, dst + i + half, bb);
+    const long src = bc * 2L * Hkv * dh + (long)g * dh;
+    const float a = sum_splits(y, nsplit, split_stride, src + i);
+    const float bb = sum_splits(y, nsplit, split_stride, src + i + half);
+    // table row c holds position pos_offset + c
+    const float cs = cos_t[(long)c * half + i], sn = sin_t[(long)c * half + i];
+    float* dst = kv + ((((long)b * 2) * Hkv + g) * L_cache + pos_offset + c) * dh;
+    dst[i] = maybe_tf32(a * cs - bb * sn, to_tf32);
+    dst[i + half] = maybe_tf32(bb * cs + a * sn, to_tf32);
+  }
+}
+
+// Context V: one thread per (b, head, channel d, c), c fastest so the transposed writes
+// are coalesced; plane (b, 1, g) holds V^T as [dh][L_cache].
+__global__ void ctx_vt_scatter_kernel(const float* __restrict__ y, int nsplit, long split_stride,
+                                      float* __restrict__ kv, int B, int L, int pos_offset,
+                                      int L_cache, int Hkv, int dh, bool to_tf32) {
+  const long n = (long)B * Hkv * dh * L;
+  for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n;
+       e += (long)gridDim.x * blockDim.x) {
+    const int c = (int)(e % L);
+    long rest = e / L;
+    const int d = (int)(rest % dh);
+    rest /= dh;
+    const int g = (int)(rest % Hkv);
+    const int b = (int)(rest / Hkv);
+    const long src = ((long)b * L + c) * 2L * Hkv * dh + (long)(Hkv + g) * dh + d;
+    const float v = sum_splits(y, nsplit, split_stride, src);
+    kv[((((long)b * 2 + 1) * Hkv + g) * dh + d) * L_cache + pos_offset + c] = maybe_tf32(v, to_tf32);
   }
 }
 
@@ -230,24 +257,30 @@ cudaError_t launch_rows_norm(int dtype, const float* y, int nsplit, const void* 
 }
 
 cudaError_t launch_qkv_rope(const float* y, int nsplit, const int32_t* pos, const uint8_t* valid,
-                            const float* cos_t, const float* sin_t, int P, float* q, float* k,
-                            float* v, long T, int Hq, int Hkv, int dh, unsigned* status,
-                            cudaStream_t stream) {
+                            const float* cos_t, const float* sin_t, int P, float* q, float* kb,
+                            float* vbt, int ns_pad, long T, int N, int S, int Hq, int Hkv, int dh,
+                            bool to_tf32, unsigned* status, cudaStream_t stream) {
   const long n = T * (Hq + 2 * Hkv) * (dh / 2);
   const long stride = T * (long)(Hq + 2 * Hkv) * dh;
   qkv_rope_kernel<<<grid_for(n, 256), 256, 0, stream>>>(y, nsplit, stride, pos, valid, cos_t,
-                                                        sin_t, P, q, k, v, T, Hq, Hkv, dh, status);
+                                                        sin_t, P, q, kb, vbt, ns_pad, T, N, S, Hq,
+                                                        Hkv, dh, to_tf32, status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_ctx_kv_scatter(int dtype, const float* y, int nsplit, const float* cos_t,
-                                  const float* sin_t, void* kv_layer, int B, int L,
-                                  int pos_offset, int L_cache, int Hkv, int dh,
+cudaError_t launch_ctx_kv_scatter(const float* y, int nsplit, const float* cos_t,
+                                  const float* sin_t, float* kv_layer, int B, int L,
+                                  int pos_offset, int L_cache, int Hkv, int dh, bool to_tf32,
                                   cudaStream_t stream) {
-  const long n = (long)B * L * 2 * Hkv * (dh / 2);
   const long stride = (long)B * L * 2 * Hkv * dh;
-  ctx_kv_scatter_kernel<<<grid_for(n, 256), 256, 0, stream>>>(
-      dtype, y, nsplit, stride, cos_t, sin_t, kv_layer, B, L, pos_offset, L_cache, Hkv, dh);
+  const long nk = (long)B * L * Hkv * (dh / 2);
+  ctx_k_scatter_kernel<<<grid_for(nk, 256), 256, 0, stream>>>(
+      y, nsplit, stride, cos_t, sin_t, kv_layer, B, L, pos_offset, L_cache, Hkv, dh, to_tf32);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long nv = (long)B * Hkv * dh * L;
+  ctx_vt_scatter_kernel<<<grid_for(nv, 256), 256, 0, stream>>>(y, nsplit, stride, kv_layer, B, L,
+                                                               pos_offset, L_cache, Hkv, dh, to_tf32);
   return cudaGetLastError();
 }
 

@@ -23,9 +23,11 @@
  *    they set a sticky per-device status word read by dflash_device_status().
  *  - Dense matrices are row-major; weight matrices are stored [out_features, in_features]
  *    (y = x W^T).  Row strides are exactly the row widths given below.
- *  - Floating-point storage type is cfg->dtype for weights, activations and the context
- *    K/V cache: DFLASH_DTYPE_BF16 (arithmetic: bf16 operands, fp32 accumulation, fp32
- *    residual stream) or DFLASH_DTYPE_F32 (fp32 throughout, no TF32).
+ *  - Floating-point storage type is cfg->dtype for weights, inputs and embeddings:
+ *    DFLASH_DTYPE_BF16 (bf16 tensor-core projections with fp32 accumulation, computed
+ *    activations carried as two-term bf16 pairs, fp32 residual stream, attention on tf32
+ *    tensor cores) or DFLASH_DTYPE_F32 (fp32 throughout, no TF32).  The context K/V cache
+ *    is fp32 in both (tf32-rounded values in the bf16 configuration).
  *  - The thread-local message of the last failing call: dflash_last_error().
  */
 #ifndef DFLASH_H_
@@ -59,7 +61,9 @@ extern "C" {
 #define DFLASH_FLAG_CTX_NORM 2u    /* context = RMSNorm(H_cat W_proj^T; g_ctx) (else raw) */
 
 /* Draft model shape ([P1] "Configuration"; the attention/MLP sizes of the draft layers).
- * num_heads % num_kv_heads == 0; head_dim even. */
+ * num_heads % num_kv_heads == 0; head_dim even.  The bf16 configuration also needs
+ * head_dim == 128, block_size * num_heads / num_kv_heads dividing 128, and every matrix row
+ * width a multiple of 8 (DFLASH_ERR_UNSUPPORTED otherwise). */
 typedef struct dflash_config {
   int32_t target_hidden;      /* D_t: width of one selected target layer */
   int32_t num_target_layers;  /* n_tl: number of selected target layers (concat width n_tl*D_t) */
@@ -137,10 +141,13 @@ DFLASH_API size_t dflash_project_context_workspace_size(const dflash_config_t* c
 /* Projects the target's selected hidden states into every draft layer's K/V space.
  *   target_hidden [B, L, n_tl*D_t]: the selected target layers concatenated in
  *                 target_layer_ids order, for context positions pos_offset .. pos_offset+L-1
- *   kv_cache      [NL, B, 2, Hkv, L_cache, dh] (dtype cfg->dtype): for every layer l,
- *                 kv_cache[l, b, 0] = RoPE(ctx W_k^T) and kv_cache[l, b, 1] = ctx W_v^T,
- *                 ctx = RMSNorm(target_hidden W_proj^T; g_ctx), W_k / W_v = the K / V rows
- *                 of layer l's w_qkv; written at positions pos_offset .. pos_offset+L-1 only.
+ *   kv_cache      float32, NL x B x 2 x Hkv planes of L_cache*dh elements: for layer l,
+ *                 row b, head g, plane (l, b, 0, g) = K as [L_cache][dh] with
+ *                 K = RoPE(ctx W_k^T), and plane (l, b, 1, g) = V transposed, [dh][L_cache],
+ *                 V = ctx W_v^T; ctx = RMSNorm(target_hidden W_proj^T; g_ctx), W_k / W_v =
+ *                 the K / V rows of layer l's w_qkv.  Written at positions
+ *                 pos_offset .. pos_offset+L-1 only; 16-byte aligned; in the bf16
+ *                 configuration L_cache must be a multiple of 4.
  *   ctx_len       optional [B] int32 (NULL = L): positions c >= ctx_len[b] of row b may be
  *                 left unwritten (no block of that row reads them); values are clamped to [0, L].
  * Requires 0 <= pos_offset, pos_offset + L <= L_cache.  RoPE positions are the absolute
@@ -160,7 +167,9 @@ DFLASH_API size_t dflash_body_workspace_size(const dflash_config_t* cfg, int B, 
  *   block_valid  [B, N, S] uint8
  *   position_ids [B, N, S] int32: RoPE position of each slot, in [0, L + S) for valid slots
  *   mask         [B, L] uint8: context validity
- *   kv_cache     [NL, B, 2, Hkv, L, dh] from dflash_project_context (L = its L_cache)
+ *   kv_cache     float32 planes from dflash_project_context (L = its L_cache); the
+ *                positions a block reads (c < its anchor) must have been written; what the
+ *                other positions hold never reaches an output
  *   out          [B, N, S, D] float32: one hidden state per slot; exactly 0 where
  *                block_valid == 0.
  * Attention of a valid slot of block (b, k) reads exactly: context positions c < anchors[b,k]

@@ -39,8 +39,7 @@ class Case:
         cfg = dflash.make_config(s)
         wts = self.model.lib_weights()
         H = to_device(di.gen_target_hidden(w) if hidden is None else hidden)
-        tdt = torch.bfloat16 if s.dtype == "bf16" else torch.float32
-        kv = torch.empty((s.num_layers, B, 2, s.num_kv_heads, L, s.head_dim), dtype=tdt,
+        kv = torch.empty((s.num_layers, B, 2, s.num_kv_heads, L, s.head_dim), dtype=torch.float32,
                          device="cuda")
         dflash.dflash_project_context(cfg, wts, H, B, L, 0, L, kv)
         del H
@@ -89,7 +88,7 @@ class Case:
 def small_bf16_workload():
     """Several tiles in every GEMM dimension plus ragged tails; masks with holes."""
     shape = di.DraftShape(target_hidden=192, num_target_layers=2, hidden=256, num_layers=2,
-                          num_heads=4, num_kv_heads=2, head_dim=64, intermediate=392,
+                          num_heads=4, num_kv_heads=2, head_dim=128, intermediate=392,
                           block_size=4, dtype="bf16")
     return di.Workload("small_bf16", 7, shape, batch=3, seq_len=300, num_anchors=5,
                        padded_rows=((1, 170),), verify_batch=0, vocab=0)
