@@ -197,6 +197,7 @@ class GpuStep:
         self.bv = torch.empty((B, N, S), dtype=torch.uint8, device=device)
         self.lm = torch.empty_like(self.bv)
         self.pid = torch.empty((B, N, S), dtype=torch.int32, device=device)
+        self.ctx_len = torch.empty((B,), dtype=torch.int32, device=device)
         self.out = torch.empty((B, N, S, s.hidden), dtype=torch.float32, device=device)
         self.em = torch.empty((self.Bv, S), dtype=torch.int32, device=device)
         self.ne = torch.empty((self.Bv,), dtype=torch.int32, device=device)
@@ -218,9 +219,9 @@ class GpuStep:
         d, w = self.dflash, self.w
         st = self.stream.cuda_stream
         d.dflash_plan(self.d_mask, self.d_sids, w.plan_step, w.plan_seed, self.N, self.S,
-                      self.anchors, self.bv, self.lm, self.pid, stream=st)
+                      self.anchors, self.bv, self.lm, self.pid, ctx_len=self.ctx_len, stream=st)
         d.dflash_project_context(self.cfg, self.wts, self.d_hidden, self.B, self.L, 0, self.L,
-                                 self.kv, ws=self.ws, stream=st)
+                                 self.kv, ctx_len=self.ctx_len, ws=self.ws, stream=st)
         d.dflash_body_forward(self.cfg, self.wts, self.d_emb, self.anchors, self.bv, self.pid,
                               self.d_mask, self.kv, self.B, self.L, self.N, self.out, ws=self.ws,
                               stream=st)

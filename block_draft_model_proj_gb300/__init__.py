@@ -64,7 +64,7 @@ _SIGS = {
     "dflash_device_status": (_I, [_I]),
     "dflash_plan_workspace_size": (_Z, [_I, _I, _I, _I]),
     "dflash_plan": (_I, [_P, _P, _I, _I, ctypes.c_int64, ctypes.c_uint64, _I, _I, _P, _P, _P, _P,
-                         _P, _Z, _P]),
+                         _P, _P, _Z, _P]),
     "dflash_project_context_workspace_size": (_Z, [ctypes.POINTER(dflash_config_t), _I, _I]),
     "dflash_project_context": (_I, [ctypes.POINTER(dflash_config_t),
                                     ctypes.POINTER(dflash_weights_t), _P, _I, _I, _I, _I, _P, _P,
@@ -171,15 +171,16 @@ def workspace(nbytes: int, device="cuda"):
 # ---- the four operations ---------------------------------------------------------------------
 
 def dflash_plan(mask, sample_ids, step, seed, num_anchors, block_size, anchors, block_valid,
-                loss_mask, position_ids, ws=None, stream=None):
+                loss_mask, position_ids, ctx_len=None, ws=None, stream=None):
     lib = load()
     B, L = mask.shape
     need = lib.dflash_plan_workspace_size(B, L, num_anchors, block_size)
     ws = ws if ws is not None else (workspace(need, mask.device) if need else None)
     _check(lib.dflash_plan(_ptr(mask), _ptr(sample_ids), B, L, int(step),
                            int(seed) & ((1 << 64) - 1), num_anchors, block_size, _ptr(anchors),
-                           _ptr(block_valid), _ptr(loss_mask), _ptr(position_ids), _ptr(ws),
-                           0 if ws is None else ws.numel(), _stream(stream)))
+                           _ptr(block_valid), _ptr(loss_mask), _ptr(position_ids),
+                           _ptr(ctx_len), _ptr(ws), 0 if ws is None else ws.numel(),
+                           _stream(stream)))
 
 
 def dflash_project_context_workspace_size(cfg, B, L) -> int:

@@ -219,9 +219,11 @@ int check_ws(void* ws, size_t ws_bytes, size_t need) {
 // C[z] = A * B^T (fp32 out): tcgen05 for bf16 (two-term A when A_lo is given), CUDA cores
 // for fp32.
 cudaError_t gemm(int dtype, const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
-                 float* C, long ldc, long M, int N, int K, int splits, cudaStream_t s) {
+                 float* C, long ldc, long M, int N, int K, int splits, cudaStream_t s,
+                 const uint8_t* tile_active = nullptr) {
   if (dtype == DFLASH_DTYPE_BF16)
-    return launch_gemm_tc(A, A_lo, lda, Bm, ldb, C, ldc, M, N, K, splits, status_ptr(), s);
+    return launch_gemm_tc(A, A_lo, lda, Bm, ldb, C, ldc, M, N, K, splits, tile_active,
+                          status_ptr(), s);
   return launch_gemm_simt(dtype, A, lda, Bm, ldb, C, ldc, M, N, K, splits, s);
 }
 
@@ -259,6 +261,7 @@ struct ProjLayout {
   Act ctx;
   float* cos_t;
   float* sin_t;
+  uint8_t* tile_flags;
   int split_proj, split_kv;
   size_t bytes;
 };
@@ -277,6 +280,7 @@ ProjLayout proj_layout(const dflash_config_t* c, int B, int L, void* ws) {
   p.ctx = take_act(cv, (size_t)M * D, c->dtype);
   p.cos_t = cv.take<float>((size_t)L * (c->head_dim / 2));
   p.sin_t = cv.take<float>((size_t)L * (c->head_dim / 2));
+  p.tile_flags = cv.take<uint8_t>((size_t)(M + kGemmTileM - 1) / kGemmTileM);
   p.bytes = cv.off;
   return p;
 }
@@ -287,6 +291,7 @@ struct BodyLayout {
   float *q, *kb, *vbt;  // attention-ready operands
   int ns_pad;
   float* partials;      // tensor-core attention partials (bf16 configuration)
+  uint8_t* tile_flags;  // 128-row tiles of slots holding at least one valid slot
   float* y;
   float* cos_t;
   float* sin_t;
@@ -318,10 +323,12 @@ BodyLayout body_layout(const dflash_config_t* c, int B, int L, int N, void* ws) 
   b.partials = nullptr;
   if (c->dtype == DFLASH_DTYPE_BF16)
     b.partials = cv.take<float>((size_t)attention_tc_layout(B, N, c->block_size, L, c->num_heads,
-                                                            c->num_kv_heads).part_floats);
+                                                            c->num_kv_heads, num_sms())
+                                    .part_floats);
   b.attn = take_act(cv, (size_t)T * qw, c->dtype);
   b.act = take_act(cv, (size_t)T * I, c->dtype);
   b.y = cv.take<float>((size_t)T * ycols);
+  b.tile_flags = cv.take<uint8_t>((size_t)(T + kGemmTileM - 1) / kGemmTileM);
   b.P = L + c->block_size;
   b.cos_t = cv.take<float>((size_t)b.P * (c->head_dim / 2));
   b.sin_t = cv.take<float>((size_t)b.P * (c->head_dim / 2));
@@ -366,8 +373,8 @@ size_t dflash_plan_workspace_size(int, int, int, int) { return 0; }
 
 int dflash_plan(const uint8_t* mask, const int64_t* sample_ids, int B, int L, int64_t step,
                 uint64_t seed, int num_anchors, int block_size, int32_t* anchors,
-                uint8_t* block_valid, uint8_t* loss_mask, int32_t* position_ids, void* ws,
-                size_t ws_bytes, void* stream) {
+                uint8_t* block_valid, uint8_t* loss_mask, int32_t* position_ids,
+                int32_t* ctx_len, void* ws, size_t ws_bytes, void* stream) {
   if (B < 1 || L < 1 || num_anchors < 1 || block_size < 1)
     return fail(DFLASH_ERR_INVALID_ARG, "B, L, num_anchors and block_size must be >= 1");
   if (num_anchors > 1024) return fail(DFLASH_ERR_UNSUPPORTED, "num_anchors must be <= 1024");
@@ -378,7 +385,8 @@ int dflash_plan(const uint8_t* mask, const int64_t* sample_ids, int B, int L, in
   {
     Prof pr(DFLASH_PROF_PLAN, 1, (cudaStream_t)stream);
     DF_CUDA(launch_plan(mask, sample_ids, B, L, (uint64_t)step, seed, num_anchors, block_size,
-                        anchors, block_valid, loss_mask, position_ids, (cudaStream_t)stream));
+                        anchors, block_valid, loss_mask, position_ids, ctx_len,
+                        (cudaStream_t)stream));
   }
   return DFLASH_OK;
 }
@@ -402,7 +410,6 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
   if ((r = check_ptr16(kv_cache, "kv_cache", DFLASH_DTYPE_BF16))) return r;
   if (cfg->dtype == DFLASH_DTYPE_BF16 && L_cache % 4 != 0)
     return fail(DFLASH_ERR_INVALID_ARG, "L_cache must be a multiple of 4 (16-byte cache rows)");
-  (void)ctx_len;  // every position is projected (allowed by the contract)
   const ProjLayout lay = proj_layout(cfg, B, L, ws);
   if ((r = check_ws(ws, ws_bytes, lay.bytes))) return r;
   cudaStream_t s = (cudaStream_t)stream;
@@ -415,10 +422,17 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
     Prof pr(DFLASH_PROF_ROWS, 1, s);
     DF_CUDA(launch_rope_table(lay.cos_t, lay.sin_t, pos_offset, L, dh, cfg->rope_theta, s));
   }
+  // 128-row tiles no block reads (all c >= ctx_len[b]) are skipped by every projection
+  const uint8_t* flags = nullptr;
+  if (ctx_len && cfg->dtype == DFLASH_DTYPE_BF16) {
+    Prof pr(DFLASH_PROF_ROWS, 1, s);
+    DF_CUDA(launch_ctx_tile_flags(ctx_len, B, L, lay.tile_flags, s));
+    flags = lay.tile_flags;
+  }
   {
     Prof pr(DFLASH_PROF_GEMM, 1, s);
     DF_CUDA(gemm(cfg->dtype, target_hidden, nullptr, Kc, w->w_proj, Kc, lay.y, D, M, D, Kc,
-                 lay.split_proj, s));
+                 lay.split_proj, s, flags));
   }
   {
     Prof pr(DFLASH_PROF_ROWS, 1, s);
@@ -432,12 +446,12 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
     {
       Prof pr(DFLASH_PROF_GEMM, 1, s);
       DF_CUDA(gemm(cfg->dtype, lay.ctx.hi, lay.ctx.lo, D, wkv, D, lay.y, kvw, M, kvw, D,
-                   lay.split_kv, s));
+                   lay.split_kv, s, flags));
     }
     float* kv_layer = static_cast<float*>(kv_cache) + (size_t)l * layer_elems;
     Prof pr(DFLASH_PROF_ROWS, 2, s);
     DF_CUDA(launch_ctx_kv_scatter(lay.y, lay.split_kv, lay.cos_t, lay.sin_t, kv_layer, B, L,
-                                  pos_offset, L_cache, Hkv, dh, to_tf32, s));
+                                  pos_offset, L_cache, Hkv, dh, to_tf32, ctx_len, s));
   }
   return DFLASH_OK;
 }
@@ -475,6 +489,13 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
   unsigned* st = status_ptr();
   const size_t layer_elems = (size_t)B * 2 * Hkv * L * dh;
 
+  // 128-slot tiles without a valid slot are skipped by every projection
+  const uint8_t* flags = nullptr;
+  if (dt == DFLASH_DTYPE_BF16) {
+    Prof pr(DFLASH_PROF_ROWS, 1, s);
+    DF_CUDA(launch_slot_tile_flags(block_valid, T, lay.tile_flags, s));
+    flags = lay.tile_flags;
+  }
   {
     Prof pr(DFLASH_PROF_ROWS, 2, s);
     DF_CUDA(launch_rope_table(lay.cos_t, lay.sin_t, 0, lay.P, dh, cfg->rope_theta, s));
@@ -485,7 +506,8 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
     const dflash_layer_weights_t& lw = w->layers[l];
     {
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(gemm(dt, lay.h.hi, lay.h.lo, D, lw.w_qkv, D, lay.y, qkvw, T, qkvw, D, lay.sp_qkv, s));
+      DF_CUDA(gemm(dt, lay.h.hi, lay.h.lo, D, lw.w_qkv, D, lay.y, qkvw, T, qkvw, D, lay.sp_qkv, s,
+                   flags));
     }
     {
       Prof pr(DFLASH_PROF_ROWS, 1, s);
@@ -512,6 +534,7 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
       aa.L = L;
       aa.Hq = Hq;
       aa.Hkv = Hkv;
+      aa.num_sms = num_sms();
       aa.status = st;
       Prof pr(DFLASH_PROF_ATTENTION, 2, s);
       DF_CUDA(launch_attention_tc(aa, s));
@@ -539,7 +562,8 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
     }
     {
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(gemm(dt, lay.attn.hi, lay.attn.lo, qw, lw.w_o, qw, lay.y, D, T, D, qw, lay.sp_o, s));
+      DF_CUDA(gemm(dt, lay.attn.hi, lay.attn.lo, qw, lw.w_o, qw, lay.y, D, T, D, qw, lay.sp_o, s,
+                   flags));
     }
     {
       Prof pr(DFLASH_PROF_ROWS, 1, s);
@@ -549,7 +573,7 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
     {
       Prof pr(DFLASH_PROF_GEMM, 1, s);
       DF_CUDA(gemm(dt, lay.h.hi, lay.h.lo, D, lw.w_gate_up, D, lay.y, 2 * I, T, 2 * I, D,
-                   lay.sp_gu, s));
+                   lay.sp_gu, s, flags));
     }
     {
       Prof pr(DFLASH_PROF_ROWS, 1, s);
@@ -557,7 +581,8 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
     }
     {
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(gemm(dt, lay.act.hi, lay.act.lo, I, lw.w_down, I, lay.y, D, T, D, I, lay.sp_down, s));
+      DF_CUDA(gemm(dt, lay.act.hi, lay.act.lo, I, lw.w_down, I, lay.y, D, T, D, I, lay.sp_down, s,
+                   flags));
     }
     Prof pr(DFLASH_PROF_ROWS, 1, s);
     if (l + 1 < cfg->num_layers) {
@@ -612,7 +637,8 @@ int dflash_testing_gemm(int engine, int dtype, const void* A, const void* A_lo, 
   if (engine == DFLASH_TESTING_ENGINE_TC) {
     if (dtype != DFLASH_DTYPE_BF16 || !gemm_tc_supported(M, N, K, lda, ldb))
       return fail(DFLASH_ERR_UNSUPPORTED, "tensor-core GEMM needs bf16 and 16-byte rows");
-    DF_CUDA(launch_gemm_tc(A, A_lo, lda, Bm, ldb, C, ldc, M, N, K, splits, status_ptr(), s));
+    DF_CUDA(launch_gemm_tc(A, A_lo, lda, Bm, ldb, C, ldc, M, N, K, splits, nullptr, status_ptr(),
+                           s));
   } else {
     if (A_lo) return fail(DFLASH_ERR_UNSUPPORTED, "the CUDA-core GEMM takes a single-term A");
     DF_CUDA(launch_gemm_simt(dtype, A, lda, Bm, ldb, C, ldc, M, N, K, splits, s));

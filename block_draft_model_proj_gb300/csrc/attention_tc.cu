@@ -250,7 +250,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, kWaitLimitNs) ? 1 : 0) != 0;
     };
+    // context mask words of a tile, loaded one tile ahead so the global-memory latency is
+    // off the softmax's critical path
+    auto load_mask = [&](int i, uint32_t* mw) {
+      const int c0 = u.cs + (i - u.nblk) * kKT;
+#pragma unroll
+      for (int w4 = 0; w4 < kKT / 4; ++w4) {
+        const int c = c0 + 4 * w4;
+        mw[w4] = (i >= u.nblk && i < u.n && row_valid && c < a_row && c < u.ce)
+                     ? __ldg(reinterpret_cast<const uint32_t*>(mrow + c)) : 0u;
+      }
+    };
+    uint32_t mask_next[kKT / 4];
+    load_mask(0, mask_next);
     for (int i = 0; i < u.n && ok; ++i) {
+      uint32_t mask_cur[kKT / 4];
+#pragma unroll
+      for (int w4 = 0; w4 < kKT / 4; ++w4) mask_cur[w4] = mask_next[w4];
+      load_mask(i + 1, mask_next);
       if (!wait_all(&s_full[i & 1], (uint32_t)(i >> 1) & 1u)) { ok = false; break; }
       tc_fence_after();
       const uint32_t s_tmem = tmem_s0 + (uint32_t)((i & 1) * kKT) + lane_off;
@@ -274,8 +291,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 #pragma unroll
         for (int w4 = 0; w4 < kKT / 4; ++w4) {
           const int c = c0 + 4 * w4;
-          uint32_t mw = 0;
-          if (row_valid && c < a_row && c < u.ce) mw = *reinterpret_cast<const uint32_t*>(mrow + c);
+          const uint32_t mw = mask_cur[w4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int kk = 4 * w4 + e;
@@ -463,13 +479,17 @@ bool encode_f32(CUtensorMap* m, const void* base, int rank, const cuuint64_t* di
 
 }  // namespace
 
-AttnTcLayout attention_tc_layout(int B, int N, int S, int L, int Hq, int Hkv) {
+AttnTcLayout attention_tc_layout(int B, int N, int S, int L, int Hq, int Hkv, int num_sms) {
   AttnTcLayout lay;
   lay.grp = Hq / Hkv;
   lay.R = S * lay.grp;
   lay.bpt = kM / lay.R;
   lay.tiles = (N + lay.bpt - 1) / lay.bpt;
-  lay.chunk = L > 16384 ? 4096 : 2048;
+  // key chunk: enough units for about four waves over the SMs when every tile reads the
+  // whole context, between 256 and 4096 keys (a power of two)
+  const double per_unit = (double)L * B * Hkv * lay.tiles / (4.0 * (num_sms > 0 ? num_sms : 1));
+  lay.chunk = 256;
+  while (lay.chunk < 4096 && lay.chunk < per_unit) lay.chunk *= 2;
   lay.max_chunks = (L + lay.chunk - 1) / lay.chunk;
   if (lay.max_chunks < 1) lay.max_chunks = 1;
   lay.units = (long)B * Hkv * lay.tiles * lay.max_chunks;
@@ -484,7 +504,7 @@ bool attention_tc_supported(int S, int Hq, int Hkv, int dh) {
 }
 
 cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream) {
-  const AttnTcLayout lay = attention_tc_layout(a.B, a.N, a.S, a.L, a.Hq, a.Hkv);
+  const AttnTcLayout lay = attention_tc_layout(a.B, a.N, a.S, a.L, a.Hq, a.Hkv, a.num_sms);
   AttnTcParams p;
   p.B = a.B;
   p.N = a.N;

@@ -78,8 +78,13 @@ struct TcParams {
   int m_tiles, n_tiles, splits, kb_per_split, num_kb;
   float* C;
   long ldc;
+  const uint8_t* tile_active;  // per M tile, optional
   unsigned* status;
 };
+
+__device__ __forceinline__ bool tile_on(const TcParams& p, int m_t) {
+  return p.tile_active == nullptr || p.tile_active[m_t] != 0;
+}
 
 template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -148,6 +153,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         const int rest = t / p.n_tiles;
         const int m_t = rest % p.m_tiles;
         const int z = rest / p.m_tiles;
+        if (!tile_on(p, m_t)) continue;
         const int kb0 = z * p.kb_per_split;
         const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -179,6 +185,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const int rest = t / p.n_tiles;
         const int z = rest / p.m_tiles;
+        if (!tile_on(p, rest % p.m_tiles)) continue;
         const int kb0 = z * p.kb_per_split;
         const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         if (!mbar_wait(&tempty[acc], acc_ph ^ 1u, abort_flag, kWaitLimitNs)) break;
@@ -218,6 +225,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       const int rest = t / p.n_tiles;
       const int m_t = rest % p.m_tiles;
       const int z = rest / p.m_tiles;
+      if (!tile_on(p, m_t)) continue;
       // warp-uniform result: the tcgen05.ld below is .sync.aligned
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_ph, abort_flag, kWaitLimitNs) ? 1 : 0))
         break;
@@ -312,8 +320,8 @@ bool gemm_tc_supported(long M, int N, int K, long lda, long ldb) {
 }
 
 cudaError_t launch_gemm_tc(const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
-                           float* C, long ldc, long M, int N, int K, int splits, unsigned* status,
-                           cudaStream_t stream) {
+                           float* C, long ldc, long M, int N, int K, int splits,
+                           const uint8_t* tile_active, unsigned* status, cudaStream_t stream) {
   if (((uintptr_t)A | (uintptr_t)A_lo | (uintptr_t)Bm) % 16 != 0) return cudaErrorInvalidValue;
   CUtensorMap ma, malo, mb;
   if (!encode_kmajor(&ma, A, M, K, lda, kBM)) return cudaErrorInvalidValue;
@@ -333,6 +341,7 @@ cudaError_t launch_gemm_tc(const void* A, const void* A_lo, long lda, const void
   p.splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;  // no empty split
   p.C = C;
   p.ldc = ldc;
+  p.tile_active = tile_active;
   p.status = status;
   static bool attr_set[2] = {false, false};
   const int which = A_lo ? 1 : 0;

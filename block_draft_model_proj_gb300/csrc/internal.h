@@ -16,7 +16,8 @@ int set_error(int code, const char* fmt, ...);
 // ---- plan.cu ----
 cudaError_t launch_plan(const uint8_t* mask, const int64_t* sids, int B, int L, uint64_t step,
                         uint64_t seed, int N, int S, int32_t* anchors, uint8_t* block_valid,
-                        uint8_t* loss_mask, int32_t* position_ids, cudaStream_t stream);
+                        uint8_t* loss_mask, int32_t* position_ids, int32_t* ctx_len,
+                        cudaStream_t stream);
 
 // ---- verify.cu ----
 struct VerifyPlan {
@@ -32,7 +33,7 @@ cudaError_t launch_verify(const void* logits, int dtype, const int32_t* draft, i
 
 // ---- rows.cu: row-wise kernels (norms, RoPE table, GEMM epilogues) ----
 // RoPE table: cos/sin [P, dh/2] fp32 for positions p0 .. p0+P-1, angles formed and
-// range-reduced in fp64.
+// range-reduced in fp64 (inverse frequencies computed on the host in fp64; dh <= 256).
 cudaError_t launch_rope_table(float* cos_t, float* sin_t, int p0, int P, int head_dim,
                               double theta, cudaStream_t stream);
 
@@ -63,10 +64,11 @@ cudaError_t launch_qkv_rope(const float* y, int nsplit, const int32_t* pos, cons
 // Context K/V epilogue: y [nsplit][B*L][2*Hkv*dh] fp32 -> the fp32 cache planes of one layer
 // [B][2][Hkv]: K as [L_cache][dh] (RoPE'd; table row c = position pos_offset + c) and V^T as
 // [dh][L_cache], at positions pos_offset + c; rounded to tf32 when to_tf32.
+// Rows c >= ctx_len[b] (when ctx_len is given) are not written.
 cudaError_t launch_ctx_kv_scatter(const float* y, int nsplit, const float* cos_t,
                                   const float* sin_t, float* kv_layer, int B, int L,
                                   int pos_offset, int L_cache, int Hkv, int dh, bool to_tf32,
-                                  cudaStream_t stream);
+                                  const int32_t* ctx_len, cudaStream_t stream);
 
 // SwiGLU epilogue: y [nsplit][T][2I] fp32 (gate | up) -> act [T][I] = SiLU(gate) * up.
 cudaError_t launch_swiglu(const float* y, int nsplit, ActOut act, long T, int I,
@@ -79,10 +81,21 @@ cudaError_t launch_gemm_simt(int dtype, const void* A, long lda, const void* Bm,
 
 // ---- gemm_tc.cu: tcgen05 bf16 GEMM, fp32 output, optional K-split ----
 // A_lo != nullptr selects the two-term activation path C = (A + A_lo) B^T.
+// tile_active (optional, one byte per 128-row M tile): tiles flagged 0 are skipped entirely
+// (their C rows are left unwritten).
+constexpr int kGemmTileM = 128;
 bool gemm_tc_supported(long M, int N, int K, long lda, long ldb);
 cudaError_t launch_gemm_tc(const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
-                           float* C, long ldc, long M, int N, int K, int splits, unsigned* status,
-                           cudaStream_t stream);
+                           float* C, long ldc, long M, int N, int K, int splits,
+                           const uint8_t* tile_active, unsigned* status, cudaStream_t stream);
+
+// ---- rows.cu: M-tile activity flags for the GEMMs ----
+// Context rows m = b*L + c: tile active iff some row has c < ctx_len[b].
+cudaError_t launch_ctx_tile_flags(const int32_t* ctx_len, int B, int L, uint8_t* flags,
+                                  cudaStream_t stream);
+// Body rows t: tile active iff some row is a valid slot.
+cudaError_t launch_slot_tile_flags(const uint8_t* valid, long T, uint8_t* flags,
+                                   cudaStream_t stream);
 
 // ---- attention.cu ----
 struct AttnArgs {
@@ -113,6 +126,7 @@ struct AttnTcArgs {
   float* partials;          // attention_tc_layout(...).part_floats floats
   ActOut out;               // [T][Hq*dh]
   int B, N, S, L, Hq, Hkv;
+  int num_sms;
   unsigned* status;
 };
 struct AttnTcLayout {
@@ -120,7 +134,7 @@ struct AttnTcLayout {
   long units;
   long part_floats;
 };
-AttnTcLayout attention_tc_layout(int B, int N, int S, int L, int Hq, int Hkv);
+AttnTcLayout attention_tc_layout(int B, int N, int S, int L, int Hq, int Hkv, int num_sms);
 bool attention_tc_supported(int S, int Hq, int Hkv, int dh);
 cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream);
 

@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const uint8_t* __restrict__ mask, const int64_t* __restrict__ sids, int B, int L,
             uint64_t step, uint64_t seed, int N, int S, int32_t* __restrict__ anchors,
             uint8_t* __restrict__ block_valid, uint8_t* __restrict__ loss_mask,
-            int32_t* __restrict__ position_ids) {
+            int32_t* __restrict__ position_ids, int32_t* __restrict__ ctx_len) {
   __shared__ unsigned hist[256];
   __shared__ int warp_counts[kPlanThreads / 32];
   __shared__ int sh_sel_digit, sh_remaining, sh_cut, sh_equal;
@@ -156,6 +156,9 @@ plan_kernel(const uint8_t* __restrict__ mask, const int64_t* __restrict__ sids, 
 
   // outputs, validity from this row's own mask
   const uint8_t* own = mask + (size_t)b * L;
+  __shared__ int sh_ctx_len;
+  if (tid == 0) sh_ctx_len = 0;
+  __syncthreads();
   for (int k = tid; k < N; k += kPlanThreads) {
     anchors[(size_t)b * N + k] = k < n_sel ? sh_anchor[k] : -1;
   }
@@ -174,6 +177,11 @@ plan_kernel(const uint8_t* __restrict__ mask, const int64_t* __restrict__ sids, 
     block_valid[o] = v ? 1 : 0;
     loss_mask[o] = (v && j >= 1) ? 1 : 0;
     position_ids[o] = p;
+    if (v) atomicMax(&sh_ctx_len, a);
+  }
+  if (ctx_len) {
+    __syncthreads();
+    if (tid == 0) ctx_len[b] = sh_ctx_len;
   }
 }
 
@@ -181,9 +189,10 @@ plan_kernel(const uint8_t* __restrict__ mask, const int64_t* __restrict__ sids, 
 
 cudaError_t launch_plan(const uint8_t* mask, const int64_t* sids, int B, int L, uint64_t step,
                         uint64_t seed, int N, int S, int32_t* anchors, uint8_t* block_valid,
-                        uint8_t* loss_mask, int32_t* position_ids, cudaStream_t stream) {
+                        uint8_t* loss_mask, int32_t* position_ids, int32_t* ctx_len,
+                        cudaStream_t stream) {
   plan_kernel<<<B, kPlanThreads, 0, stream>>>(mask, sids, B, L, step, seed, N, S, anchors,
-                                              block_valid, loss_mask, position_ids);
+                                              block_valid, loss_mask, position_ids, ctx_len);
   return cudaGetLastError();
 }
 

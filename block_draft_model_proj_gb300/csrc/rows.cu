@@ -10,6 +10,8 @@
 // Computed activations that feed a projection GEMM are written through ActOut: fp32 for
 // the fp32 configuration, else the two-term bf16 pair (hi, lo) the tensor-core GEMM
 // consumes.  Attention operands (q, block k / v) are kept in fp32.
+#include <math.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -24,14 +26,17 @@ __device__ __forceinline__ float ld(const void* p, int dt, long i) {
                                  : static_cast<const float*>(p)[i];
 }
 
+struct InvFreq {
+  double v[128];
+};
+
 __global__ void rope_table_kernel(float* __restrict__ cos_t, float* __restrict__ sin_t, int p0,
-                                  int P, int half, int head_dim, double theta) {
+                                  int P, int half, const InvFreq inv) {
   const long n = (long)P * half;
   for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n;
        e += (long)gridDim.x * blockDim.x) {
     const int p = (int)(e / half), i = (int)(e - (long)p * half);
-    const double inv_freq = pow(theta, -2.0 * (double)i / (double)head_dim);
-    const double ang = (double)(p0 + p) * inv_freq;
+    const double ang = (double)(p0 + p) * inv.v[i];
     // reduce to [-pi, pi] in fp64, then evaluate in fp32
     const double r = fma(-rint(ang / kTwoPi), kTwoPi, ang);
     float s, c;
@@ -130,8 +135,11 @@ __global__ void qkv_rope_kernel(const float* __restrict__ y, int nsplit, long sp
     const int rem = (int)(e - t * heads * half);
     const int hd = rem / half, i = rem - hd * half;
     const long base = t * width + (long)hd * dh;
-    const float a = sum_splits(y, nsplit, split_stride, base + i);
-    const float bb = sum_splits(y, nsplit, split_stride, base + i + half);
+    // invalid slots get zero operands: they are never keys, and their GEMM rows may have
+    // been skipped (unwritten) when a whole 128-row tile held no valid slot
+    const bool vt = valid[t] != 0;
+    const float a = vt ? sum_splits(y, nsplit, split_stride, base + i) : 0.f;
+    const float bb = vt ? sum_splits(y, nsplit, split_stride, base + i + half) : 0.f;
     const int b = (int)(t / ((long)N * S));
     const int ks = (int)(t - (long)b * N * S);  // k * S + j
     const int k = ks / S, j = ks - k * S;
@@ -144,7 +152,7 @@ __global__ void qkv_rope_kernel(const float* __restrict__ y, int nsplit, long sp
     }
     int pp = pos[t];
     if (pp < 0 || pp >= P) {
-      if (valid[t] && i == 0) report(status, kStatusCheck, kKernEpilogue);
+      if (vt && i == 0) report(status, kStatusCheck, kKernEpilogue);
       pp = 0;
     }
     const float c = cos_t[(long)pp * half + i], sn = sin_t[(long)pp * half + i];
@@ -167,7 +175,7 @@ __global__ void ctx_k_scatter_kernel(const float* __restrict__ y, int nsplit, lo
                                      const float* __restrict__ cos_t,
                                      const float* __restrict__ sin_t, float* __restrict__ kv,
                                      int B, int L, int pos_offset, int L_cache, int Hkv, int dh,
-                                     bool to_tf32) {
+                                     bool to_tf32, const int32_t* __restrict__ ctx_len) {
   const int half = dh / 2;
   const long per_row = (long)Hkv * half;
   const long n = (long)B * L * per_row;
@@ -177,6 +185,7 @@ __global__ void ctx_k_scatter_kernel(const float* __restrict__ y, int nsplit, lo
     const int rem = (int)(e - bc * per_row);
     const int g = rem / half, i = rem - g * half;
     const int b = (int)(bc / L), c = (int)(bc - (long)b * L);
+    if (ctx_len && c >= ctx_len[b]) continue;
     const long src = bc * 2L * Hkv * dh + (long)g * dh;
     const float a = sum_splits(y, nsplit, split_stride, src + i);
     const float bb = sum_splits(y, nsplit, split_stride, src + i + half);
@@ -192,7 +201,8 @@ __global__ void ctx_k_scatter_kernel(const float* __restrict__ y, int nsplit, lo
 // are coalesced; plane (b, 1, g) holds V^T as [dh][L_cache].
 __global__ void ctx_vt_scatter_kernel(const float* __restrict__ y, int nsplit, long split_stride,
                                       float* __restrict__ kv, int B, int L, int pos_offset,
-                                      int L_cache, int Hkv, int dh, bool to_tf32) {
+                                      int L_cache, int Hkv, int dh, bool to_tf32,
+                                      const int32_t* __restrict__ ctx_len) {
   const long n = (long)B * Hkv * dh * L;
   for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n;
        e += (long)gridDim.x * blockDim.x) {
@@ -202,6 +212,7 @@ __global__ void ctx_vt_scatter_kernel(const float* __restrict__ y, int nsplit, l
     rest /= dh;
     const int g = (int)(rest % Hkv);
     const int b = (int)(rest / Hkv);
+    if (ctx_len && c >= ctx_len[b]) continue;
     const long src = ((long)b * L + c) * 2L * Hkv * dh + (long)(Hkv + g) * dh + d;
     const float v = sum_splits(y, nsplit, split_stride, src);
     kv[((((long)b * 2 + 1) * Hkv + g) * dh + d) * L_cache + pos_offset + c] = maybe_tf32(v, to_tf32);
@@ -232,9 +243,12 @@ inline int grid_for(long n, int threads) {
 
 cudaError_t launch_rope_table(float* cos_t, float* sin_t, int p0, int P, int head_dim,
                               double theta, cudaStream_t stream) {
-  const long n = (long)P * (head_dim / 2);
-  rope_table_kernel<<<grid_for(n, 256), 256, 0, stream>>>(cos_t, sin_t, p0, P, head_dim / 2,
-                                                          head_dim, theta);
+  const int half = head_dim / 2;
+  if (half > 128) return cudaErrorInvalidValue;
+  InvFreq inv;
+  for (int i = 0; i < half; ++i) inv.v[i] = pow(theta, -2.0 * (double)i / (double)head_dim);
+  const long n = (long)P * half;
+  rope_table_kernel<<<grid_for(n, 256), 256, 0, stream>>>(cos_t, sin_t, p0, P, half, inv);
   return cudaGetLastError();
 }
 
@@ -271,16 +285,65 @@ cudaError_t launch_qkv_rope(const float* y, int nsplit, const int32_t* pos, cons
 cudaError_t launch_ctx_kv_scatter(const float* y, int nsplit, const float* cos_t,
                                   const float* sin_t, float* kv_layer, int B, int L,
                                   int pos_offset, int L_cache, int Hkv, int dh, bool to_tf32,
-                                  cudaStream_t stream) {
+                                  const int32_t* ctx_len, cudaStream_t stream) {
   const long stride = (long)B * L * 2 * Hkv * dh;
   const long nk = (long)B * L * Hkv * (dh / 2);
   ctx_k_scatter_kernel<<<grid_for(nk, 256), 256, 0, stream>>>(
-      y, nsplit, stride, cos_t, sin_t, kv_layer, B, L, pos_offset, L_cache, Hkv, dh, to_tf32);
+      y, nsplit, stride, cos_t, sin_t, kv_layer, B, L, pos_offset, L_cache, Hkv, dh, to_tf32,
+      ctx_len);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long nv = (long)B * Hkv * dh * L;
-  ctx_vt_scatter_kernel<<<grid_for(nv, 256), 256, 0, stream>>>(y, nsplit, stride, kv_layer, B, L,
-                                                               pos_offset, L_cache, Hkv, dh, to_tf32);
+  ctx_vt_scatter_kernel<<<grid_for(nv, 256), 256, 0, stream>>>(
+      y, nsplit, stride, kv_layer, B, L, pos_offset, L_cache, Hkv, dh, to_tf32, ctx_len);
+  return cudaGetLastError();
+}
+
+namespace {
+
+// one thread per 128-row tile
+__global__ void ctx_tile_flags_kernel(const int32_t* __restrict__ ctx_len, int B, int L,
+                                      uint8_t* __restrict__ flags, long tiles) {
+  const long t = blockIdx.x * (long)blockDim.x + threadIdx.x;
+  if (t >= tiles) return;
+  const long m0 = t * kGemmTileM, m1 = min(m0 + kGemmTileM, (long)B * L);
+  uint8_t on = 0;
+  for (long m = m0; m < m1 && !on; ) {
+    const int b = (int)(m / L);
+    const long row_end = min(m1, (long)(b + 1) * L);
+    const int c = (int)(m - (long)b * L);
+    int cl = ctx_len[b];
+    cl = cl < 0 ? 0 : (cl > L ? L : cl);
+    if (c < cl) on = 1;
+    m = row_end;
+  }
+  flags[t] = on;
+}
+
+__global__ void slot_tile_flags_kernel(const uint8_t* __restrict__ valid, long T,
+                                       uint8_t* __restrict__ flags, long tiles) {
+  const long t = blockIdx.x * (long)blockDim.x + threadIdx.x;
+  if (t >= tiles) return;
+  uint8_t on = 0;
+  for (long r = t * kGemmTileM; r < min((t + 1) * kGemmTileM, T); ++r)
+    if (valid[r]) { on = 1; break; }
+  flags[t] = on;
+}
+
+}  // namespace
+
+cudaError_t launch_ctx_tile_flags(const int32_t* ctx_len, int B, int L, uint8_t* flags,
+                                  cudaStream_t stream) {
+  const long tiles = ((long)B * L + kGemmTileM - 1) / kGemmTileM;
+  ctx_tile_flags_kernel<<<(unsigned)((tiles + 127) / 128), 128, 0, stream>>>(ctx_len, B, L, flags,
+                                                                           tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_slot_tile_flags(const uint8_t* valid, long T, uint8_t* flags,
+                                   cudaStream_t stream) {
+  const long tiles = (T + kGemmTileM - 1) / kGemmTileM;
+  slot_tile_flags_kernel<<<(unsigned)((tiles + 127) / 128), 128, 0, stream>>>(valid, T, flags, tiles);
   return cudaGetLastError();
 }
 

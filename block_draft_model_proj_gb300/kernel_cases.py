@@ -1,0 +1,147 @@
+"""Single-kernel cases on synthetic inputs, for profiling one kernel at a time (ncu).
+
+    python -m block_draft_model_proj_gb300.kernel_cases gemm --m 8192 --n 4096 --k 20480
+    python -m block_draft_model_proj_gb300.kernel_cases gemm --m 512 --n 24576 --k 4096 --two-term
+    python -m block_draft_model_proj_gb300.kernel_cases body --workload train_8b_b4_l2048
+    python -m block_draft_model_proj_gb300.kernel_cases verify --workload decode_8b_b64_ctx4096
+
+Each case builds its inputs once, runs the kernel `--iters` times and prints the mean
+CUDA-event time per launch (a number printed under a profiler is not a benchmark).
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def _timed(fn, iters):
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record()
+    for _ in range(iters):
+        fn()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / iters
+
+
+def case_gemm(args):
+    import torch
+    import block_draft_model_proj_gb300 as dflash
+    g = torch.Generator(device="cuda").manual_seed(0)
+    A = torch.randn((args.m, args.k), generator=g, device="cuda").to(torch.bfloat16)
+    Alo = (torch.randn((args.m, args.k), generator=g, device="cuda") * 1e-3).to(torch.bfloat16) \
+        if args.two_term else None
+    B = (torch.randn((args.n, args.k), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    C = torch.empty((args.splits, args.m, args.n), dtype=torch.float32, device="cuda")
+
+    def run():
+        dflash.dflash_testing_gemm(dflash.DFLASH_TESTING_ENGINE_TC, dflash.DFLASH_DTYPE_BF16, A, B,
+                                   C, args.splits, A_lo=Alo)
+    run()
+    dflash.dflash_device_status()
+    ms = _timed(run, args.iters)
+    flops = 2.0 * args.m * args.n * args.k * (2 if args.two_term else 1)
+    print(f"gemm M={args.m} N={args.n} K={args.k} two_term={args.two_term} splits={args.splits}: "
+          f"{ms:.4f} ms/launch, {flops / ms / 1e9:.1f} TFLOP/s issued")
+
+
+def case_body(args):
+    import torch
+    import block_draft_model_proj_gb300 as dflash
+    import dflash_inputs as di
+    w = di.WORKLOADS[args.workload]
+    s = w.shape
+    B, L, N, S = w.batch, w.seq_len, w.num_anchors, s.block_size
+
+    def dev(t):
+        if t.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(t.data).view(np.int16)).cuda().view(
+                torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(t.data)).cuda()
+    top = {k: dev(v) for k, v in di.gen_top_weights(w).items()}
+    layers = [{k: dev(v) for k, v in di.gen_layer_weights(w, l).items()} for l in range(s.num_layers)]
+    wts = dflash.Weights(top, layers)
+    cfg = dflash.make_config(s)
+    mask = torch.from_numpy(di.gen_mask(w)).cuda()
+    sids = torch.from_numpy(di.gen_sample_ids(w)).cuda()
+    H = dev(di.gen_target_hidden(w))
+    emb = dev(di.gen_block_emb(w))
+    kv = torch.empty((s.num_layers, B, 2, s.num_kv_heads, L, s.head_dim), dtype=torch.float32,
+                     device="cuda")
+    if w.inference:
+        a_np, v_np, p_np = di.inference_block_layout(w)
+        anchors = torch.from_numpy(a_np).cuda()
+        bv = torch.from_numpy(v_np).cuda()
+        pid = torch.from_numpy(p_np).cuda()
+    else:
+        anchors = torch.empty((B, N), dtype=torch.int32, device="cuda")
+        bv = torch.empty((B, N, S), dtype=torch.uint8, device="cuda")
+        lm = torch.empty_like(bv)
+        pid = torch.empty((B, N, S), dtype=torch.int32, device="cuda")
+        dflash.dflash_plan(mask, sids, w.plan_step, w.plan_seed, N, S, anchors, bv, lm, pid)
+    out = torch.empty((B, anchors.shape[1], S, s.hidden), dtype=torch.float32, device="cuda")
+    ws = dflash.workspace(max(dflash.dflash_project_context_workspace_size(cfg, B, L),
+                              dflash.dflash_body_workspace_size(cfg, B, L, anchors.shape[1])))
+    dflash.dflash_project_context(cfg, wts, H, B, L, 0, L, kv, ws=ws)
+
+    def run():
+        dflash.dflash_body_forward(cfg, wts, emb, anchors, bv, pid, mask, kv, B, L,
+                                   anchors.shape[1], out, ws=ws)
+    run()
+    dflash.dflash_device_status()
+    ms = _timed(run, args.iters)
+    print(f"body {w.name}: {ms:.4f} ms/call")
+
+
+def case_verify(args):
+    import torch
+    import block_draft_model_proj_gb300 as dflash
+    import dflash_inputs as di
+    w = di.WORKLOADS[args.workload]
+    vi = di.gen_verify(w)
+    Bv, S, V = vi.logits.shape
+    logits = torch.from_numpy(vi.logits.data.view(np.int16)).cuda().view(torch.bfloat16)
+    draft = torch.from_numpy(vi.draft).cuda()
+    em = torch.empty((Bv, S), dtype=torch.int32, device="cuda")
+    ne = torch.empty((Bv,), dtype=torch.int32, device="cuda")
+    ac = torch.empty_like(ne)
+    ws = dflash.workspace(dflash.dflash_verify_workspace_size(Bv, S - 1, V))
+
+    def run():
+        dflash.dflash_verify_greedy(logits, dflash.DFLASH_DTYPE_BF16, draft, Bv, S - 1, V, -1, em,
+                                    ne, ac, ws=ws)
+    run()
+    dflash.dflash_device_status()
+    ms = _timed(run, args.iters)
+    nbytes = Bv * S * V * 2
+    print(f"verify [{Bv},{S},{V}] bf16: {ms * 1e3:.2f} us/call, {nbytes / ms / 1e6:.1f} GB/s")
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=["gemm", "body", "verify"])
+    ap.add_argument("--m", type=int, default=8192)
+    ap.add_argument("--n", type=int, default=4096)
+    ap.add_argument("--k", type=int, default=20480)
+    ap.add_argument("--splits", type=int, default=1)
+    ap.add_argument("--two-term", action="store_true")
+    ap.add_argument("--workload", default="train_8b_b4_l2048")
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args(argv)
+    from block_draft_model_proj_gb300 import build as b
+    b.build()
+    {"gemm": case_gemm, "body": case_body, "verify": case_verify}[args.case](args)
+
+
+if __name__ == "__main__":
+    main()

@@ -128,11 +128,15 @@ DFLASH_API size_t dflash_plan_workspace_size(int B, int L, int num_anchors, int 
  *   block_valid  [B, N, S] uint8: anchor != -1, position a valid, position a+j valid
  *   loss_mask    [B, N, S] uint8: block_valid and j >= 1 (the anchor never counts)
  *   position_ids [B, N, S] int32: a + j, or -1 in an empty slot
+ *   ctx_len      [B] int32, optional (NULL = not written): the largest anchor of a block of
+ *                row b with at least one valid slot (0 if none) -- the number of context
+ *                positions any block of the row reads; dflash_project_context takes it to
+ *                skip the rest
  * Errors: INVALID_ARG for B, L, N or S < 1, null pointers, ws too small. */
 DFLASH_API int dflash_plan(const uint8_t* mask, const int64_t* sample_ids, int B, int L, int64_t step,
                 uint64_t seed, int num_anchors, int block_size, int32_t* anchors,
-                uint8_t* block_valid, uint8_t* loss_mask, int32_t* position_ids, void* ws,
-                size_t ws_bytes, void* stream);
+                uint8_t* block_valid, uint8_t* loss_mask, int32_t* position_ids,
+                int32_t* ctx_len, void* ws, size_t ws_bytes, void* stream);
 
 /* ---- 2. context projection ([P1] How it works: dual-source KV context) ---------------- */
 

@@ -38,10 +38,12 @@ def test_internal_symbols_are_hidden(cpu_lib):
 
 
 def test_plan_rejects_bad_sizes_on_host(cpu_lib):
-    st = cpu_lib.dflash_plan(None, None, 0, 10, 0, 0, 4, 16, None, None, None, None, None, 0, None)
+    st = cpu_lib.dflash_plan(None, None, 0, 10, 0, 0, 4, 16, None, None, None, None, None, None,
+                             0, None)
     assert st == dflash.DFLASH_ERR_INVALID_ARG
     assert b"must be >= 1" in cpu_lib.dflash_last_error()
-    st = cpu_lib.dflash_plan(None, None, 2, 10, 0, 0, 4, 16, None, None, None, None, None, 0, None)
+    st = cpu_lib.dflash_plan(None, None, 2, 10, 0, 0, 4, 16, None, None, None, None, None, None,
+                             0, None)
     assert st == dflash.DFLASH_ERR_INVALID_ARG
     assert b"null" in cpu_lib.dflash_last_error()
 

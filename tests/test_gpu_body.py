@@ -31,7 +31,7 @@ class Case:
         self.emb = di.gen_block_emb(w)
         self.N = plan["anchors"].shape[1]
 
-    def run_gpu(self, emb=None, hidden=None, mask=None, check_cache=False):
+    def run_gpu(self, emb=None, hidden=None, mask=None, check_cache=False, ctx_len=None):
         import torch
         import block_draft_model_proj_gb300 as dflash
         w, s = self.w, self.w.shape
@@ -41,7 +41,8 @@ class Case:
         H = to_device(di.gen_target_hidden(w) if hidden is None else hidden)
         kv = torch.empty((s.num_layers, B, 2, s.num_kv_heads, L, s.head_dim), dtype=torch.float32,
                          device="cuda")
-        dflash.dflash_project_context(cfg, wts, H, B, L, 0, L, kv)
+        cl = None if ctx_len is None else np_to_device(np.asarray(ctx_len, np.int32))
+        dflash.dflash_project_context(cfg, wts, H, B, L, 0, L, kv, ctx_len=cl)
         del H
         out = torch.full((B, N, S, s.hidden), float("nan"), dtype=torch.float32, device="cuda")
         m = np_to_device(self.mask if mask is None else mask)
@@ -177,6 +178,24 @@ def test_block_isolation_and_strict_prefix_on_gpu(lib):
         5 * rng.standard_normal(H3.data[b, a - 1].shape).astype(np.float32))
     got3 = c.run_gpu(hidden=H3)
     assert not np.array_equal(got3[b, k], base[b, k])
+
+
+def _ctx_len_of(plan):
+    a, v = plan["anchors"], plan["block_valid"].astype(bool).any(axis=-1)
+    return [max([int(x) for x, ok in zip(a[b], v[b]) if ok] + [0]) for b in range(a.shape[0])]
+
+
+@pytest.mark.parametrize("wname", ["small", "train_8b_b4_l2048"])
+def test_skipping_unread_context_and_empty_slot_tiles_changes_nothing(lib, wname):
+    """Context rows no block reads (c >= ctx_len) and 128-slot tiles without a valid slot are
+    skipped by the projections; the body's outputs must be bit-identical to the full run."""
+    w = small_bf16_workload() if wname == "small" else di.WORKLOADS[wname]
+    c = Case(w)
+    full = c.run_gpu()
+    cl = _ctx_len_of(c.plan)
+    assert min(cl) < w.seq_len
+    skipped = c.run_gpu(ctx_len=cl)
+    assert np.array_equal(full, skipped)
 
 
 def test_out_of_range_position_reports_device_check(lib):

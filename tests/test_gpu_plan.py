@@ -22,15 +22,25 @@ def gpu_plan(mask, sids, step, seed, N, S):
     bv = torch.full((B, N, S), 9, dtype=torch.uint8, device="cuda")
     lm = torch.full((B, N, S), 9, dtype=torch.uint8, device="cuda")
     pid = torch.full((B, N, S), -7, dtype=torch.int32, device="cuda")
-    dflash.dflash_plan(dm, ds, step, seed, N, S, anchors, bv, lm, pid)
+    cl = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    dflash.dflash_plan(dm, ds, step, seed, N, S, anchors, bv, lm, pid, ctx_len=cl)
     dflash.dflash_device_status()
     return {"anchors": anchors.cpu().numpy(), "block_valid": bv.cpu().numpy(),
-            "loss_mask": lm.cpu().numpy(), "position_ids": pid.cpu().numpy()}
+            "loss_mask": lm.cpu().numpy(), "position_ids": pid.cpu().numpy(),
+            "ctx_len": cl.cpu().numpy()}
+
+
+def expected_ctx_len(ref):
+    """Largest anchor of a block with a valid slot, per row (0 if none), from the oracle plan."""
+    a, v = ref["anchors"], ref["block_valid"].astype(bool).any(axis=-1)
+    return np.array([max([int(x) for x, ok in zip(a[b], v[b]) if ok] + [0])
+                     for b in range(a.shape[0])], np.int32)
 
 
 def assert_same_plan(got, ref):
     for k in ("anchors", "block_valid", "loss_mask", "position_ids"):
         assert np.array_equal(got[k], ref[k]), k
+    assert np.array_equal(got["ctx_len"], expected_ctx_len(ref))
 
 
 @pytest.mark.parametrize("name", ["plan_small.txt", "plan_shared_sid.txt"])
