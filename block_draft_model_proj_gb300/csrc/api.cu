@@ -180,9 +180,11 @@ int check_cfg(const dflash_config_t* c) {
   return DFLASH_OK;
 }
 
+// Tensor arguments are read and written with 16-byte vector accesses (and TMA).
 int check_ptr16(const void* p, const char* what, int dtype) {
+  (void)dtype;
   if (!p) return fail(DFLASH_ERR_INVALID_ARG, "%s is null", what);
-  if (dtype == DFLASH_DTYPE_BF16 && ((uintptr_t)p % 16) != 0)
+  if (((uintptr_t)p % 16) != 0)
     return fail(DFLASH_ERR_INVALID_ARG, "%s must be 16-byte aligned", what);
   return DFLASH_OK;
 }
@@ -443,12 +445,29 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
   const bool to_tf32 = cfg->dtype == DFLASH_DTYPE_BF16;
   for (int l = 0; l < cfg->num_layers; ++l) {
     const uint8_t* wkv = static_cast<const uint8_t*>(w->layers[l].w_qkv) + (size_t)qw * D * es;
+    float* kv_layer = static_cast<float*>(kv_cache) + (size_t)l * layer_elems;
+    if (cfg->dtype == DFLASH_DTYPE_BF16) {
+      // RoPE and the cache layout are applied in the GEMM epilogue
+      KvCacheEpilogue kv;
+      kv.kv = kv_layer;
+      kv.cos_t = lay.cos_t;
+      kv.sin_t = lay.sin_t;
+      kv.ctx_len = ctx_len;
+      kv.L = L;
+      kv.pos_offset = pos_offset;
+      kv.L_cache = L_cache;
+      kv.Hkv = Hkv;
+      kv.to_tf32 = 1;
+      Prof pr(DFLASH_PROF_GEMM, 1, s);
+      DF_CUDA(launch_gemm_tc_kv_cache(lay.ctx.hi, lay.ctx.lo, D, wkv, D, M, kvw, D, flags, kv,
+                                      status_ptr(), s));
+      continue;
+    }
     {
       Prof pr(DFLASH_PROF_GEMM, 1, s);
       DF_CUDA(gemm(cfg->dtype, lay.ctx.hi, lay.ctx.lo, D, wkv, D, lay.y, kvw, M, kvw, D,
                    lay.split_kv, s, flags));
     }
-    float* kv_layer = static_cast<float*>(kv_cache) + (size_t)l * layer_elems;
     Prof pr(DFLASH_PROF_ROWS, 2, s);
     DF_CUDA(launch_ctx_kv_scatter(lay.y, lay.split_kv, lay.cos_t, lay.sin_t, kv_layer, B, L,
                                   pos_offset, L_cache, Hkv, dh, to_tf32, ctx_len, s));
@@ -473,6 +492,8 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
   if (B < 1 || L < 1 || N < 1) return fail(DFLASH_ERR_INVALID_ARG, "B, L and N must be >= 1");
   if (!anchors || !block_valid || !position_ids || !mask || !out)
     return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
+  if ((r = check_ptr16(out, "out", cfg->dtype))) return r;
+  if ((r = check_ptr16(mask, "mask", cfg->dtype))) return r;
   if ((r = check_ptr16(block_emb, "block_emb", cfg->dtype))) return r;
   if ((r = check_ptr16(kv_cache, "kv_cache", DFLASH_DTYPE_BF16))) return r;
   if (cfg->dtype == DFLASH_DTYPE_BF16 && L % 4 != 0)

@@ -30,9 +30,12 @@
 //
 // Warp roles: warp 0 TMA producer (Q once; K and V^T tiles of 64 keys, 2-stage ring),
 // warp 1 MMA issuer (S = Q K^T into a double-buffered TMEM S/P area; O += P V with P read
-// from TMEM), warps 2-5 softmax / correction / partial output.  Every mbarrier wait is
-// bounded in time; on expiry the CTA reports DFLASH_ERR_TIMEOUT, drains its own copies and
-// MMAs, frees tensor memory and exits.
+// from TMEM), warps 2-9 softmax / correction / partial output: two warps per TMEM lane
+// quarter, one per half of the key columns (and of the O columns), so each SM sub-partition
+// runs two softmax warps; the halves agree on the running row maximum through shared
+// memory behind an mbarrier.  Every mbarrier wait is bounded in time; on expiry the CTA
+// reports DFLASH_ERR_TIMEOUT, drains its own copies and MMAs, frees tensor memory and
+// exits.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
@@ -47,7 +50,9 @@ constexpr int kDH = 128;   // head dim handled by this kernel
 constexpr int kM = 128;    // query rows per tile (TMEM lanes)
 constexpr int kKT = 64;    // keys per tile
 constexpr int kStages = 2;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;          // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
+constexpr int kSoftmaxWarps = 8;       // two per TMEM lane quarter, each owns half the keys
+constexpr int kHalfKT = 32;            // key columns per softmax thread
 constexpr uint32_t kTmemCols = 256;      // O [0,128) + S/P buffers [128,192), [192,256)
 constexpr uint32_t kQSub = kM * 32 * 4;  // [128 rows][32 dh] fp32, 16 KB
 constexpr uint32_t kQBytes = 4 * kQSub;  // 64 KB
@@ -56,7 +61,9 @@ constexpr uint32_t kKBytes = 4 * kKSub;  // 32 KB
 constexpr uint32_t kVSub = kDH * 32 * 4; // V^T [128 dh][32 keys], 16 KB
 constexpr uint32_t kVBytes = 2 * kVSub;  // 32 KB
 constexpr uint32_t kStageBytes = kKBytes + kVBytes;
-constexpr size_t kSmemBytes = 1024 + kQBytes + kStages * (size_t)kStageBytes + 256;
+// + barriers, the row-max exchange [2 tiles][2 halves][128 rows] and the row-sum exchange
+constexpr size_t kSmemBytes = 1024 + kQBytes + kStages * (size_t)kStageBytes + 256 +
+                              (4 * 128 + 2 * 128) * sizeof(float);
 constexpr uint32_t kIdescS = idesc_tf32(kM, kKT);
 constexpr uint32_t kIdescPV = idesc_tf32(kM, kDH);
 constexpr float kRescaleLog2 = 8.0f;
@@ -122,8 +129,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 2;
   uint64_t* drain = pv_done + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* max_bar = drain + 1;   // [2]: row-max exchange of tiles with parity 0 / 1
+  uint64_t* sum_bar = max_bar + 2; // row-sum exchange at the end
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sum_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* red_max = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);  // [2][2][128]
+  float* red_sum = red_max + 4 * 128;                                                 // [2][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -134,10 +145,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&p_full[i], kSoftmaxWarps);
       mbar_init(&pv_done[i], 1);
+      mbar_init(&max_bar[i], kSoftmaxWarps);
     }
     mbar_init(drain, 1);
+    mbar_init(sum_bar, kSoftmaxWarps);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -228,8 +241,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       mbar_wait(drain, 0, abort_flag, kWaitLimitNs / 4);
     }
   } else {
-    // ---------------- softmax / correction / partial output (warps 2..5) ----------------
+    // ---------------- softmax / correction / partial output (warps 2..9) ----------------
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;   // key columns [32*half, 32*half + 32) of each tile
     const int r = quarter * 32 + lane;  // query row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int kbo = r / p.R;
@@ -244,52 +258,51 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       a_row = min(max(a, 0), p.L);
     }
     const uint8_t* mrow = p.mask + (size_t)u.b * p.L;
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;  // l_run: this half's share of the row sum
     bool ok = true;
     // every wait result is made warp-uniform: the tcgen05.ld / st below are .sync.aligned
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, kWaitLimitNs) ? 1 : 0) != 0;
     };
-    // context mask words of a tile, loaded one tile ahead so the global-memory latency is
-    // off the softmax's critical path
+    // context mask words of this half of a tile, loaded one tile ahead so the global-memory
+    // latency is off the softmax's critical path
     auto load_mask = [&](int i, uint32_t* mw) {
-      const int c0 = u.cs + (i - u.nblk) * kKT;
+      const int c0 = u.cs + (i - u.nblk) * kKT + half * kHalfKT;
 #pragma unroll
-      for (int w4 = 0; w4 < kKT / 4; ++w4) {
+      for (int w4 = 0; w4 < kHalfKT / 4; ++w4) {
         const int c = c0 + 4 * w4;
         mw[w4] = (i >= u.nblk && i < u.n && row_valid && c < a_row && c < u.ce)
                      ? __ldg(reinterpret_cast<const uint32_t*>(mrow + c)) : 0u;
       }
     };
-    uint32_t mask_next[kKT / 4];
+    uint32_t mask_next[kHalfKT / 4];
     load_mask(0, mask_next);
     for (int i = 0; i < u.n && ok; ++i) {
-      uint32_t mask_cur[kKT / 4];
+      uint32_t mask_cur[kHalfKT / 4];
 #pragma unroll
-      for (int w4 = 0; w4 < kKT / 4; ++w4) mask_cur[w4] = mask_next[w4];
+      for (int w4 = 0; w4 < kHalfKT / 4; ++w4) mask_cur[w4] = mask_next[w4];
       load_mask(i + 1, mask_next);
       if (!wait_all(&s_full[i & 1], (uint32_t)(i >> 1) & 1u)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t s_tmem = tmem_s0 + (uint32_t)((i & 1) * kKT) + lane_off;
-      uint32_t sv[kKT];
+      const uint32_t s_tmem = tmem_s0 + (uint32_t)((i & 1) * kKT + half * kHalfKT) + lane_off;
+      uint32_t sv[kHalfKT];
       tmem_ld_32x32b_x32(s_tmem, sv);
-      tmem_ld_32x32b_x32(s_tmem + 32, sv + 32);
       const bool blk_tile = i < u.nblk;
-      const int c0 = blk_tile ? 0 : u.cs + (i - u.nblk) * kKT;
-      float x[kKT];
-      float mt = -INFINITY;
+      const int c0 = blk_tile ? 0 : u.cs + (i - u.nblk) * kKT + half * kHalfKT;
+      float x[kHalfKT];
+      float mh = -INFINITY;
       if (blk_tile) {
 #pragma unroll
-        for (int kk = 0; kk < kKT; ++kk) {
-          const int q = u.k0 * p.S + i * kKT + kk;
+        for (int kk = 0; kk < kHalfKT; ++kk) {
+          const int q = u.k0 * p.S + i * kKT + half * kHalfKT + kk;
           const int kbk = q / p.S, jj = q - kbk * p.S;
           const bool okk = row_valid && kbk == kb && p.valid[(u.b * p.N + kbk) * p.S + jj] != 0;
           x[kk] = okk ? __uint_as_float(sv[kk]) * p.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x[kk]);
+          mh = fmaxf(mh, x[kk]);
         }
       } else {
 #pragma unroll
-        for (int w4 = 0; w4 < kKT / 4; ++w4) {
+        for (int w4 = 0; w4 < kHalfKT / 4; ++w4) {
           const int c = c0 + 4 * w4;
           const uint32_t mw = mask_cur[w4];
 #pragma unroll
@@ -297,10 +310,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
             const int kk = 4 * w4 + e;
             const bool okk = ((mw >> (8 * e)) & 0xFFu) != 0 && c + e < a_row && c + e < u.ce;
             x[kk] = okk ? __uint_as_float(sv[kk]) * p.scale_log2 : -INFINITY;
-            mt = fmaxf(mt, x[kk]);
+            mh = fmaxf(mh, x[kk]);
           }
         }
       }
+      // the two halves of a row agree on the tile maximum
+      float* xm = red_max + (i & 1) * 256;
+      xm[half * 128 + r] = mh;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&max_bar[i & 1]);
+      if (!wait_all(&max_bar[i & 1], (uint32_t)(i >> 1) & 1u)) { ok = false; break; }
+      const float mt = fmaxf(mh, xm[(1 - half) * 128 + r]);
       // running maximum: taken as is the first time a row sees a key, otherwise kept
       // unless the tile's maximum exceeds it by more than 2^8 (then the accumulator and
       // the row sum are rescaled)
@@ -314,50 +334,50 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         }
       }
       if (__any_sync(0xffffffffu, factor != 1.f)) {
-        // the PV of the previous tile must have landed before the accumulator is touched
+        // the PV of the previous tile must have landed before the accumulator is touched;
+        // this half rescales O columns [64*half, 64*half + 64)
         if (!wait_all(&pv_done[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1u)) { ok = false; break; }
         tc_fence_after();
-        for (int part = 0; part < 4; ++part) {
+        for (int part = 0; part < 2; ++part) {
           uint32_t ov[32];
-          tmem_ld_32x32b_x32(tmem_o + lane_off + part * 32, ov);
+          const uint32_t oa = tmem_o + lane_off + half * 64 + part * 32;
+          tmem_ld_32x32b_x32(oa, ov);
 #pragma unroll
           for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
-          tmem_st_32x32b_x32(tmem_o + lane_off + part * 32, ov);
+          tmem_st_32x32b_x32(oa, ov);
         }
         tmem_wait_st();
         l_run *= factor;
       }
       float lsum = 0.f;
 #pragma unroll
-      for (int kk = 0; kk < kKT; ++kk) {
+      for (int kk = 0; kk < kHalfKT; ++kk) {
         const float pv = x[kk] == -INFINITY ? 0.f : round_tf32(exp2f(x[kk] - m_run));
         lsum += pv;
         sv[kk] = __float_as_uint(pv);
       }
       l_run += lsum;
       tmem_st_32x32b_x32(s_tmem, sv);
-      tmem_st_32x32b_x32(s_tmem + 32, sv + 32);
       tmem_wait_st();
-      // value columns past the last readable key of this tile: zero them (thread r owns
-      // V^T row r) so that whatever the cache holds there cannot meet a zero P as NaN
-      if (!blk_tile && c0 + kKT > u.a_max) {
+      // value columns past the last readable key of this tile: zero them (this thread owns
+      // V^T row r of key sub-tile `half`) so that whatever the cache holds there cannot
+      // meet a zero P as NaN
+      if (!blk_tile && u.cs + (i - u.nblk) * kKT + kKT > u.a_max) {
         const int st = i % kStages;
         if (!wait_all(&kv_full[st], (uint32_t)(i / kStages) & 1u)) { ok = false; break; }
-        const int nvalid = u.a_max - c0;
-        uint8_t* sV = sKV + st * kStageBytes + kKBytes;
-        for (int v = 0; v < 2; ++v) {
-          uint8_t* rowp = sV + v * kVSub + (r >> 3) * 1024 + (r & 7) * 128;
-          for (int ch = 0; ch < 8; ++ch) {
-            const int key0 = v * 32 + ch * 4;
-            if (key0 + 4 <= nvalid) continue;
-            float4* dst = reinterpret_cast<float4*>(rowp + ((ch ^ (r & 7)) * 16));
-            float4 val = *dst;
-            if (key0 + 0 >= nvalid) val.x = 0.f;
-            if (key0 + 1 >= nvalid) val.y = 0.f;
-            if (key0 + 2 >= nvalid) val.z = 0.f;
-            if (key0 + 3 >= nvalid) val.w = 0.f;
-            *dst = val;
-          }
+        const int nvalid = u.a_max - (u.cs + (i - u.nblk) * kKT);
+        uint8_t* rowp = sKV + st * kStageBytes + kKBytes + half * kVSub + (r >> 3) * 1024 +
+                        (r & 7) * 128;
+        for (int ch = 0; ch < 8; ++ch) {
+          const int key0 = half * 32 + ch * 4;
+          if (key0 + 4 <= nvalid) continue;
+          float4* dst = reinterpret_cast<float4*>(rowp + ((ch ^ (r & 7)) * 16));
+          float4 val = *dst;
+          if (key0 + 0 >= nvalid) val.x = 0.f;
+          if (key0 + 1 >= nvalid) val.y = 0.f;
+          if (key0 + 2 >= nvalid) val.z = 0.f;
+          if (key0 + 3 >= nvalid) val.w = 0.f;
+          *dst = val;
         }
         fence_proxy_async_smem();
       }
@@ -365,21 +385,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[i & 1]);
     }
-    // final accumulator -> partial (m, l, O) of this unit
+    // final accumulator -> partial (m, l, O) of this unit; each half writes its 64 columns
     if (ok && wait_all(&pv_done[(u.n - 1) & 1], (uint32_t)((u.n - 1) >> 1) & 1u)) {
       tc_fence_after();
       const size_t rowi = (size_t)blockIdx.x * kM + r;
-      float4* po = reinterpret_cast<float4*>(p.part_o + rowi * kDH);
-      for (int part = 0; part < 4; ++part) {
+      float4* po = reinterpret_cast<float4*>(p.part_o + rowi * kDH + half * 64);
+      for (int part = 0; part < 2; ++part) {
         uint32_t ov[32];
-        tmem_ld_32x32b_x32(tmem_o + lane_off + part * 32, ov);
+        tmem_ld_32x32b_x32(tmem_o + lane_off + half * 64 + part * 32, ov);
 #pragma unroll
         for (int e = 0; e < 8; ++e)
           po[part * 8 + e] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
                                          __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]));
       }
-      p.part_m[rowi] = m_run;
-      p.part_l[rowi] = l_run;
+      red_sum[half * 128 + r] = l_run;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sum_bar);
+      if (wait_all(sum_bar, 0) && half == 0) {
+        p.part_m[rowi] = m_run;
+        p.part_l[rowi] = l_run + red_sum[128 + r];
+      }
     }
   }
 

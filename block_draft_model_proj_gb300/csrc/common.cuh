@@ -59,7 +59,36 @@ struct ActOut {
       static_cast<float*>(hi)[i] = v;
     }
   }
+  // four consecutive elements starting at i (i a multiple of 4)
+  __device__ __forceinline__ void store4(long i, float4 v) const {
+    if (dtype == DFLASH_DTYPE_BF16) {
+      const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
+      const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
+      const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+      const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
+      const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
+      uint2 hw, lw;
+      hw.x = *reinterpret_cast<const uint32_t*>(&h01);
+      hw.y = *reinterpret_cast<const uint32_t*>(&h23);
+      lw.x = *reinterpret_cast<const uint32_t*>(&l01);
+      lw.y = *reinterpret_cast<const uint32_t*>(&l23);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(hi) + i) = hw;
+      *reinterpret_cast<uint2*>(lo + i) = lw;
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(hi) + i) = v;
+    }
+  }
 };
+
+// Four consecutive elements of a bf16 or fp32 array as fp32 (i a multiple of 4).
+__device__ __forceinline__ float4 load4(const void* p, int dtype, long i) {
+  if (dtype == DFLASH_DTYPE_BF16) {
+    const uint2 w = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p) + i);
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                       __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+  }
+  return *reinterpret_cast<const float4*>(static_cast<const float*>(p) + i);
+}
 
 // ---- reductions --------------------------------------------------------------------
 __device__ __forceinline__ float warp_sum(float v) {

@@ -72,6 +72,8 @@ __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint6
       : "memory");
 }
 
+enum : int { kEpiStoreF32 = 0, kEpiKvCache = 1 };
+
 struct TcParams {
   long M;
   int N, K;
@@ -80,13 +82,83 @@ struct TcParams {
   long ldc;
   const uint8_t* tile_active;  // per M tile, optional
   unsigned* status;
+  KvCacheEpilogue kv;          // used by the kEpiKvCache epilogue only
 };
 
 __device__ __forceinline__ bool tile_on(const TcParams& p, int m_t) {
   return p.tile_active == nullptr || p.tile_active[m_t] != 0;
 }
 
-template <bool kSplit>
+
+// Context K/V epilogue of the per-layer K/V projection (N = 2*Hkv*dh, dh = 128: every
+// 256-column tile holds two whole heads; K heads first).  Row m of the tile is context
+// position c = m mod L of row b = m / L, cache position pos_offset + c.  K heads get RoPE
+// (rotate-half: channel i pairs with i + 64; table row c) and are written as cache rows
+// [pos][dh]; V heads are written transposed, [dh][pos] -- consecutive lanes hold consecutive
+// positions, so those stores are coalesced.  Rows at or past ctx_len[b] are not written.
+__device__ __forceinline__ void kv_cache_epilogue(const TcParams& p, uint32_t tbase, int m_t,
+                                                  int n_t, int quarter, int lane) {
+  const KvCacheEpilogue& e = p.kv;
+  const long m = (long)m_t * kBM + quarter * 32 + lane;
+  const int b = (int)(m / e.L);
+  const int c = (int)(m - (long)b * e.L);
+  bool row_ok = m < p.M;
+  if (row_ok && e.ctx_len) row_ok = c < e.ctx_len[b];
+  const long pos = (long)e.pos_offset + c;
+  const long plane = (long)e.L_cache * 128;
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    const int head = n_t * 2 + hh;  // 0 .. 2*Hkv-1: K heads, then V heads
+    if (head >= 2 * e.Hkv) break;   // warp-uniform
+    const uint32_t hbase = tbase + hh * 128;
+    if (head < e.Hkv) {
+      float* dst = e.kv + ((long)b * 2 * e.Hkv + head) * plane + pos * 128;
+#pragma unroll 1
+      for (int ch = 0; ch < 2; ++ch) {  // channel chunks (32ch .. 32ch+31) and their pairs +64
+        uint32_t lo[32], hi[32];
+        tmem_ld_32x32b_x32(hbase + ch * 32, lo);
+        tmem_ld_32x32b_x32(hbase + 64 + ch * 32, hi);
+        if (row_ok) {
+          const float* cs = e.cos_t + (long)c * 64 + ch * 32;
+          const float* sn = e.sin_t + (long)c * 64 + ch * 32;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 c4 = reinterpret_cast<const float4*>(cs)[q];
+            const float4 s4 = reinterpret_cast<const float4*>(sn)[q];
+            const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, ss[4] = {s4.x, s4.y, s4.z, s4.w};
+            float a[4], bb[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const float x0 = __uint_as_float(lo[4 * q + t]), x1 = __uint_as_float(hi[4 * q + t]);
+              a[t] = x0 * cc[t] - x1 * ss[t];
+              bb[t] = x1 * cc[t] + x0 * ss[t];
+              if (e.to_tf32) { a[t] = round_tf32(a[t]); bb[t] = round_tf32(bb[t]); }
+            }
+            reinterpret_cast<float4*>(dst + ch * 32)[q] = make_float4(a[0], a[1], a[2], a[3]);
+            reinterpret_cast<float4*>(dst + 64 + ch * 32)[q] = make_float4(bb[0], bb[1], bb[2], bb[3]);
+          }
+        }
+      }
+    } else {
+      float* dst = e.kv + ((long)b * 2 * e.Hkv + e.Hkv + (head - e.Hkv)) * plane + pos;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(hbase + ch * 32, v);
+        if (row_ok) {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) {
+            float x = __uint_as_float(v[t]);
+            if (e.to_tf32) x = round_tf32(x);
+            dst[(long)(ch * 32 + t) * e.L_cache] = x;
+          }
+        }
+      }
+    }
+  }
+}
+
+template <bool kSplit, int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_alo,
                const __grid_constant__ CUtensorMap map_b, const TcParams p) {
@@ -230,25 +302,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_ph, abort_flag, kWaitLimitNs) ? 1 : 0))
         break;
       tc_fence_after();
-      float* Cz = p.C + (long)z * p.M * p.ldc;
-      const long row0 = (long)m_t * kBM + quarter * 32;
-      const int col0 = n_t * kBN;
+      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
+      if constexpr (kEpi == kEpiStoreF32) {
+        float* Cz = p.C + (long)z * p.M * p.ldc;
+        const long row0 = (long)m_t * kBM + quarter * 32;
+        const int col0 = n_t * kBN;
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t v[32];
-        const uint32_t taddr =
-            tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN + c * 32);
-        tmem_ld_32x32b_x32(taddr, v);
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) stg[lane * 33 + i] = __uint_as_float(v[i]);
-        __syncwarp();
-        const int col = col0 + c * 32 + lane;
+          for (int i = 0; i < 32; ++i) stg[lane * 33 + i] = __uint_as_float(v[i]);
+          __syncwarp();
+          const int col = col0 + c * 32 + lane;
 #pragma unroll 4
-        for (int r = 0; r < 32; ++r) {
-          const long row = row0 + r;
-          if (row < p.M && col < p.N) Cz[row * p.ldc + col] = stg[r * 33 + lane];
+          for (int r = 0; r < 32; ++r) {
+            const long row = row0 + r;
+            if (row < p.M && col < p.N) Cz[row * p.ldc + col] = stg[r * 33 + lane];
+          }
+          __syncwarp();
         }
-        __syncwarp();
+      } else {
+        kv_cache_epilogue(p, tbase, m_t, n_t, quarter, lane);
       }
       tc_fence_before();
       __syncwarp();
@@ -319,9 +394,27 @@ bool gemm_tc_supported(long M, int N, int K, long lda, long ldb) {
          get_encode_fn() != nullptr;
 }
 
-cudaError_t launch_gemm_tc(const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
-                           float* C, long ldc, long M, int N, int K, int splits,
-                           const uint8_t* tile_active, unsigned* status, cudaStream_t stream) {
+namespace {
+
+template <bool kSplit, int kEpi>
+cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& malo, const CUtensorMap& mb,
+                           const TcParams& p, int grid, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<kSplit, kEpi>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Cfg<kSplit>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  gemm_tc_kernel<kSplit, kEpi><<<grid, kThreads, Cfg<kSplit>::kSmemBytes, stream>>>(ma, malo, mb, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_common(const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
+                          float* C, long ldc, long M, int N, int K, int splits,
+                          const uint8_t* tile_active, unsigned* status, int epi,
+                          const KvCacheEpilogue* kv, cudaStream_t stream) {
   if (((uintptr_t)A | (uintptr_t)A_lo | (uintptr_t)Bm) % 16 != 0) return cudaErrorInvalidValue;
   CUtensorMap ma, malo, mb;
   if (!encode_kmajor(&ma, A, M, K, lda, kBM)) return cudaErrorInvalidValue;
@@ -343,25 +436,34 @@ cudaError_t launch_gemm_tc(const void* A, const void* A_lo, long lda, const void
   p.ldc = ldc;
   p.tile_active = tile_active;
   p.status = status;
-  static bool attr_set[2] = {false, false};
-  const int which = A_lo ? 1 : 0;
-  if (!attr_set[which]) {
-    cudaError_t e = A_lo ? cudaFuncSetAttribute(gemm_tc_kernel<true>,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)Cfg<true>::kSmemBytes)
-                         : cudaFuncSetAttribute(gemm_tc_kernel<false>,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)Cfg<false>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set[which] = true;
-  }
+  if (kv) p.kv = *kv;
   const long tiles = (long)p.m_tiles * p.n_tiles * p.splits;
   const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-  if (A_lo)
-    gemm_tc_kernel<true><<<grid, kThreads, Cfg<true>::kSmemBytes, stream>>>(ma, malo, mb, p);
-  else
-    gemm_tc_kernel<false><<<grid, kThreads, Cfg<false>::kSmemBytes, stream>>>(ma, malo, mb, p);
-  return cudaGetLastError();
+  if (epi == kEpiKvCache)
+    return A_lo ? launch_variant<true, kEpiKvCache>(ma, malo, mb, p, grid, stream)
+                : launch_variant<false, kEpiKvCache>(ma, malo, mb, p, grid, stream);
+  return A_lo ? launch_variant<true, kEpiStoreF32>(ma, malo, mb, p, grid, stream)
+              : launch_variant<false, kEpiStoreF32>(ma, malo, mb, p, grid, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
+                           float* C, long ldc, long M, int N, int K, int splits,
+                           const uint8_t* tile_active, unsigned* status, cudaStream_t stream) {
+  return launch_common(A, A_lo, lda, Bm, ldb, C, ldc, M, N, K, splits, tile_active, status,
+                       kEpiStoreF32, nullptr, stream);
+}
+
+cudaError_t launch_gemm_tc_kv_cache(const void* A, const void* A_lo, long lda, const void* Bm,
+                                    long ldb, long M, int N, int K, const uint8_t* tile_active,
+                                    const KvCacheEpilogue& kv, unsigned* status,
+                                    cudaStream_t stream) {
+  if (N != 2 * kv.Hkv * 128 || kv.L < 1) return cudaErrorInvalidValue;
+  if (((uintptr_t)kv.kv | (uintptr_t)kv.cos_t | (uintptr_t)kv.sin_t) % 16 != 0)
+    return cudaErrorInvalidValue;
+  return launch_common(A, A_lo, lda, Bm, ldb, nullptr, 0, M, N, K, 1, tile_active, status,
+                       kEpiKvCache, &kv, stream);
 }
 
 }  // namespace dflash

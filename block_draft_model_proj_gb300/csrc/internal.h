@@ -85,6 +85,22 @@ cudaError_t launch_gemm_simt(int dtype, const void* A, long lda, const void* Bm,
 // (their C rows are left unwritten).
 constexpr int kGemmTileM = 128;
 bool gemm_tc_supported(long M, int N, int K, long lda, long ldb);
+
+// Destination of the context K/V projection written straight from the GEMM epilogue
+// (head_dim 128): rows m = b*L + c of the GEMM are cache positions pos_offset + c.
+struct KvCacheEpilogue {
+  float* kv = nullptr;           // one layer: [B][2][Hkv] planes, K [L_cache][128], V^T [128][L_cache]
+  const float* cos_t = nullptr;  // [L][64], row c = position pos_offset + c
+  const float* sin_t = nullptr;
+  const int32_t* ctx_len = nullptr;  // optional [B]: rows c >= ctx_len[b] are not written
+  int L = 0, pos_offset = 0, L_cache = 0, Hkv = 0;
+  int to_tf32 = 0;
+};
+// C = (A + A_lo) B^T with N = 2*Hkv*128, written to the cache by the epilogue (no K-split).
+cudaError_t launch_gemm_tc_kv_cache(const void* A, const void* A_lo, long lda, const void* Bm,
+                                    long ldb, long M, int N, int K, const uint8_t* tile_active,
+                                    const KvCacheEpilogue& kv, unsigned* status,
+                                    cudaStream_t stream);
 cudaError_t launch_gemm_tc(const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
                            float* C, long ldc, long M, int N, int K, int splits,
                            const uint8_t* tile_active, unsigned* status, cudaStream_t stream);

@@ -106,6 +106,123 @@ __device__ __forceinline__ float sum_splits(const float* y, int nsplit, long str
   return v;
 }
 
+__device__ __forceinline__ float4 sum_splits4(const float* y, int nsplit, long stride, long idx) {
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < nsplit; ++s) {
+    const float4 t = *reinterpret_cast<const float4*>(y + s * stride + idx);
+    v.x += t.x;
+    v.y += t.y;
+    v.z += t.z;
+    v.w += t.w;
+  }
+  return v;
+}
+
+// Vectorised residual step: one CTA per row, each thread owns kV float4 groups of the row
+// (D % 4 == 0, D <= 4 * kV * blockDim.x), a single pass over global memory.
+template <int kV>
+__global__ void residual_norm_vec_kernel(int mode, int dt, float* __restrict__ x,
+                                         const void* __restrict__ emb, const float* __restrict__ y,
+                                         int nsplit, long split_stride, const void* __restrict__ g,
+                                         float eps, ActOut h, float* __restrict__ out,
+                                         const uint8_t* __restrict__ valid, bool final_norm, int D) {
+  __shared__ float red[33];
+  const long r = blockIdx.x;
+  const int D4 = D / 4;
+  float4 v[kV];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < kV; ++k) {
+    const int q = threadIdx.x + k * blockDim.x;
+    if (q >= D4) { v[k] = make_float4(0.f, 0.f, 0.f, 0.f); continue; }
+    const long idx = r * D + 4L * q;
+    float4 t;
+    if (mode == kNormInit) {
+      t = load4(emb, dt, idx);
+    } else {
+      t = *reinterpret_cast<const float4*>(x + idx);
+      const float4 a = sum_splits4(y, nsplit, split_stride, idx);
+      t.x += a.x;
+      t.y += a.y;
+      t.z += a.z;
+      t.w += a.w;
+    }
+    *reinterpret_cast<float4*>(x + idx) = t;
+    v[k] = t;
+    ss += t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w;
+  }
+  ss = block_sum(ss, red);
+  const float rstd = rsqrtf(ss / (float)D + eps);
+  const bool ok = mode != kNormFinal || valid[r] != 0;
+#pragma unroll
+  for (int k = 0; k < kV; ++k) {
+    const int q = threadIdx.x + k * blockDim.x;
+    if (q >= D4) continue;
+    const long idx = r * D + 4L * q;
+    const float4 gg = load4(g, dt, 4L * q);
+    if (mode == kNormFinal) {
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ok)
+        o = final_norm ? make_float4(v[k].x * rstd * gg.x, v[k].y * rstd * gg.y,
+                                     v[k].z * rstd * gg.z, v[k].w * rstd * gg.w)
+                       : v[k];
+      *reinterpret_cast<float4*>(out + idx) = o;
+    } else {
+      h.store4(idx, make_float4(v[k].x * rstd * gg.x, v[k].y * rstd * gg.y, v[k].z * rstd * gg.z,
+                                v[k].w * rstd * gg.w));
+    }
+  }
+}
+
+template <int kV>
+__global__ void rows_norm_vec_kernel(int dt, const float* __restrict__ y, int nsplit,
+                                     long split_stride, const void* __restrict__ g, float eps,
+                                     bool with_norm, ActOut out, int D) {
+  __shared__ float red[33];
+  const long r = blockIdx.x;
+  const int D4 = D / 4;
+  float4 v[kV];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < kV; ++k) {
+    const int q = threadIdx.x + k * blockDim.x;
+    v[k] = q < D4 ? sum_splits4(y, nsplit, split_stride, r * D + 4L * q)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+  }
+  ss = with_norm ? block_sum(ss, red) : 0.f;
+  const float rstd = with_norm ? rsqrtf(ss / (float)D + eps) : 1.f;
+#pragma unroll
+  for (int k = 0; k < kV; ++k) {
+    const int q = threadIdx.x + k * blockDim.x;
+    if (q >= D4) continue;
+    float4 o = v[k];
+    if (with_norm) {
+      const float4 gg = load4(g, dt, 4L * q);
+      o = make_float4(o.x * rstd * gg.x, o.y * rstd * gg.y, o.z * rstd * gg.z, o.w * rstd * gg.w);
+    }
+    out.store4(r * D + 4L * q, o);
+  }
+}
+
+__device__ __forceinline__ float silu_mul(float gt, float up) { return gt / (1.f + expf(-gt)) * up; }
+
+// SwiGLU, four consecutive channels per thread (I % 4 == 0)
+__global__ void swiglu_vec_kernel(const float* __restrict__ y, int nsplit, long split_stride,
+                                  ActOut act, long T, int I) {
+  const int I4 = I / 4;
+  const long n = T * I4;
+  for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n;
+       e += (long)gridDim.x * blockDim.x) {
+    const long t = e / I4;
+    const int i = (int)(e - t * I4) * 4;
+    const float4 gt = sum_splits4(y, nsplit, split_stride, t * 2 * I + i);
+    const float4 up = sum_splits4(y, nsplit, split_stride, t * 2 * I + I + i);
+    act.store4(t * I + i, make_float4(silu_mul(gt.x, up.x), silu_mul(gt.y, up.y),
+                                      silu_mul(gt.z, up.z), silu_mul(gt.w, up.w)));
+  }
+}
+
 __device__ __forceinline__ float maybe_tf32(float v, bool to_tf32) {
   if (!to_tf32) return v;
   uint32_t r;
@@ -256,6 +373,20 @@ cudaError_t launch_residual_norm(int mode, int dtype, float* x, const void* emb,
                                  int nsplit, const void* g, double eps, ActOut h, float* out,
                                  const uint8_t* valid, bool final_norm, long rows, int D,
                                  cudaStream_t stream) {
+  if (D % 4 == 0 && D <= 4 * 4 * 1024) {
+    const int D4 = D / 4;
+    const int threads = D4 >= 1024 ? 1024 : ((D4 + 31) / 32) * 32;
+    const int per = (D4 + threads - 1) / threads;
+    if (per <= 1)
+      residual_norm_vec_kernel<1><<<rows, threads, 0, stream>>>(mode, dtype, x, emb, y, nsplit,
+                                                                rows * D, g, (float)eps, h, out,
+                                                                valid, final_norm, D);
+    else
+      residual_norm_vec_kernel<4><<<rows, threads, 0, stream>>>(mode, dtype, x, emb, y, nsplit,
+                                                                rows * D, g, (float)eps, h, out,
+                                                                valid, final_norm, D);
+    return cudaGetLastError();
+  }
   const int threads = D >= 2048 ? 512 : 256;
   residual_norm_kernel<<<rows, threads, 0, stream>>>(mode, dtype, x, emb, y, nsplit, rows * D, g,
                                                      (float)eps, h, out, valid, final_norm, D);
@@ -264,6 +395,18 @@ cudaError_t launch_residual_norm(int mode, int dtype, float* x, const void* emb,
 
 cudaError_t launch_rows_norm(int dtype, const float* y, int nsplit, const void* g, double eps,
                              bool with_norm, ActOut out, long rows, int D, cudaStream_t stream) {
+  if (D % 4 == 0 && D <= 4 * 4 * 1024) {
+    const int D4 = D / 4;
+    const int threads = D4 >= 1024 ? 1024 : ((D4 + 31) / 32) * 32;
+    const int per = (D4 + threads - 1) / threads;
+    if (per <= 1)
+      rows_norm_vec_kernel<1><<<rows, threads, 0, stream>>>(dtype, y, nsplit, rows * D, g,
+                                                            (float)eps, with_norm, out, D);
+    else
+      rows_norm_vec_kernel<4><<<rows, threads, 0, stream>>>(dtype, y, nsplit, rows * D, g,
+                                                            (float)eps, with_norm, out, D);
+    return cudaGetLastError();
+  }
   const int threads = D >= 2048 ? 512 : 256;
   rows_norm_kernel<<<rows, threads, 0, stream>>>(dtype, y, nsplit, rows * D, g, (float)eps,
                                                  with_norm, out, D);
@@ -349,6 +492,11 @@ cudaError_t launch_slot_tile_flags(const uint8_t* valid, long T, uint8_t* flags,
 
 cudaError_t launch_swiglu(const float* y, int nsplit, ActOut act, long T, int I,
                           cudaStream_t stream) {
+  if (I % 4 == 0) {
+    const long n4 = T * (I / 4);
+    swiglu_vec_kernel<<<grid_for(n4, 256), 256, 0, stream>>>(y, nsplit, T * 2L * I, act, T, I);
+    return cudaGetLastError();
+  }
   const long n = T * I;
   swiglu_kernel<<<grid_for(n, 256), 256, 0, stream>>>(y, nsplit, T * 2L * I, act, T, I);
   return cudaGetLastError();

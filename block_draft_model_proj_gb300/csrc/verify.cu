@@ -60,13 +60,14 @@ argmax_partial_kernel(const T* __restrict__ logits, int V, int chunks, int chunk
     const int nvec = (c1 - c0) / kVec;
     const uint4* pv = reinterpret_cast<const uint4*>(p + c0);
     int t = threadIdx.x;
-    // 4 independent 16-byte loads in flight per thread
-    for (; t + 3 * kVerifyThreads < nvec; t += 4 * kVerifyThreads) {
-      uint4 u[4];
+    // 8 independent 16-byte loads in flight per thread
+    constexpr int kUnroll = 8;
+    for (; t + (kUnroll - 1) * kVerifyThreads < nvec; t += kUnroll * kVerifyThreads) {
+      uint4 u[kUnroll];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) u[q] = __ldcs(pv + t + q * kVerifyThreads);
+      for (int q = 0; q < kUnroll; ++q) u[q] = __ldcs(pv + t + q * kVerifyThreads);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < kUnroll; ++q) {
         const int base = c0 + (t + q * kVerifyThreads) * kVec;
         if constexpr (sizeof(T) == 2) {
           float f[8];

@@ -13,7 +13,8 @@
  *
  * Conventions shared by every call
  *  - Every tensor pointer is a DEVICE pointer owned by the caller, unless a parameter
- *    says "host".  The library allocates no device memory: scratch space comes from a
+ *    says "host".  Weight, embedding, hidden-state, cache, mask and output pointers of the
+ *    body and projection calls must be 16-byte aligned (cudaMalloc gives 256).  The library allocates no device memory: scratch space comes from a
  *    caller-provided workspace `ws` of at least the size the matching *_workspace_size
  *    query returns, aligned to 256 bytes (cudaMalloc alignment).
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
