@@ -591,12 +591,17 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
       DF_CUDA(launch_residual_norm(kNormAdd, dt, lay.x, nullptr, lay.y, lay.sp_o, lw.g_post,
                                    cfg->rms_eps, lay.h.out(), nullptr, nullptr, false, T, D, s));
     }
-    {
+    if (dt == DFLASH_DTYPE_BF16 && lay.sp_gu == 1) {
+      // SiLU(gate) * up is formed in the GEMM epilogue
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(gemm(dt, lay.h.hi, lay.h.lo, D, lw.w_gate_up, D, lay.y, 2 * I, T, 2 * I, D,
-                   lay.sp_gu, s, flags));
-    }
-    {
+      DF_CUDA(launch_gemm_tc_swiglu(lay.h.hi, lay.h.lo, D, lw.w_gate_up, D, T, I, D, flags,
+                                    lay.act.out(), st, s));
+    } else {
+      {
+        Prof pr(DFLASH_PROF_GEMM, 1, s);
+        DF_CUDA(gemm(dt, lay.h.hi, lay.h.lo, D, lw.w_gate_up, D, lay.y, 2 * I, T, 2 * I, D,
+                     lay.sp_gu, s, flags));
+      }
       Prof pr(DFLASH_PROF_ROWS, 1, s);
       DF_CUDA(launch_swiglu(lay.y, lay.sp_gu, lay.act.out(), T, I, s));
     }

@@ -72,7 +72,7 @@ __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint6
       : "memory");
 }
 
-enum : int { kEpiStoreF32 = 0, kEpiKvCache = 1 };
+enum : int { kEpiStoreF32 = 0, kEpiKvCache = 1, kEpiSwiGLU = 2 };
 
 struct TcParams {
   long M;
@@ -83,6 +83,8 @@ struct TcParams {
   const uint8_t* tile_active;  // per M tile, optional
   unsigned* status;
   KvCacheEpilogue kv;          // used by the kEpiKvCache epilogue only
+  ActOut act;                  // kEpiSwiGLU: two-term SiLU(gate) * up, [M][swiglu_I]
+  int swiglu_I;                // kEpiSwiGLU: B rows [0, I) gate, [I, 2I) up
 };
 
 __device__ __forceinline__ bool tile_on(const TcParams& p, int m_t) {
@@ -153,6 +155,39 @@ __device__ __forceinline__ void kv_cache_epilogue(const TcParams& p, uint32_t tb
             dst[(long)(ch * 32 + t) * e.L_cache] = x;
           }
         }
+      }
+    }
+  }
+}
+
+// SwiGLU epilogue: accumulator columns [0, 128) are the gate and [128, 256) the up
+// projections of channels n_t*128 .. +127; writes act = SiLU(gate) * up as a two-term pair.
+__device__ __forceinline__ void swiglu_epilogue(const TcParams& p, uint32_t tbase, int m_t, int n_t,
+                                                int quarter, int lane) {
+  const long m = (long)m_t * kBM + quarter * 32 + lane;
+  const bool row_ok = m < p.M;
+  const int I = p.swiglu_I;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t g[32], up[32];
+    tmem_ld_32x32b_x32(tbase + c * 32, g);
+    tmem_ld_32x32b_x32(tbase + 128 + c * 32, up);
+    const int ch0 = n_t * 128 + c * 32;
+    if (!row_ok) continue;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float a[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float gt = __uint_as_float(g[4 * q + t]);
+        a[t] = gt / (1.f + expf(-gt)) * __uint_as_float(up[4 * q + t]);
+      }
+      const int ch = ch0 + 4 * q;
+      if (ch + 3 < I) {
+        p.act.store4(m * I + ch, make_float4(a[0], a[1], a[2], a[3]));
+      } else {
+        for (int t = 0; t < 4; ++t)
+          if (ch + t < I) p.act.store(m * I + ch + t, a[t]);
       }
     }
   }
@@ -235,8 +270,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           uint8_t* b_dst = sB + stage * kStageBBytes;
           tma_load_2d(&map_a, &full[stage], a_dst, kb * kBK, m_t * kBM);
           if (kSplit) tma_load_2d(&map_alo, &full[stage], a_dst + kTileABytes, kb * kBK, m_t * kBM);
-          tma_load_2d(&map_b, &full[stage], b_dst, kb * kBK, n_t * kBN);
-          tma_load_2d(&map_b, &full[stage], b_dst + kStageBBytes / 2, kb * kBK, n_t * kBN + 128);
+          // the two 128-row halves of the B tile: consecutive rows, or (SwiGLU) the gate
+          // rows of 128 channels and the up rows of the same channels
+          const int brow0 = kEpi == kEpiSwiGLU ? n_t * 128 : n_t * kBN;
+          const int brow1 = kEpi == kEpiSwiGLU ? p.swiglu_I + n_t * 128 : n_t * kBN + 128;
+          tma_load_2d(&map_b, &full[stage], b_dst, kb * kBK, brow0);
+          tma_load_2d(&map_b, &full[stage], b_dst + kStageBBytes / 2, kb * kBK, brow1);
           issued[stage] = 1;
           issued_ph[stage] = ph;
           if (++stage == kStages) { stage = 0; ph ^= 1u; }
@@ -322,8 +361,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           }
           __syncwarp();
         }
-      } else {
+      } else if constexpr (kEpi == kEpiKvCache) {
         kv_cache_epilogue(p, tbase, m_t, n_t, quarter, lane);
+      } else {
+        swiglu_epilogue(p, tbase, m_t, n_t, quarter, lane);
       }
       tc_fence_before();
       __syncwarp();
@@ -414,7 +455,7 @@ cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& malo, const
 cudaError_t launch_common(const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
                           float* C, long ldc, long M, int N, int K, int splits,
                           const uint8_t* tile_active, unsigned* status, int epi,
-                          const KvCacheEpilogue* kv, cudaStream_t stream) {
+                          const KvCacheEpilogue* kv, const ActOut* act, cudaStream_t stream) {
   if (((uintptr_t)A | (uintptr_t)A_lo | (uintptr_t)Bm) % 16 != 0) return cudaErrorInvalidValue;
   CUtensorMap ma, malo, mb;
   if (!encode_kmajor(&ma, A, M, K, lda, kBM)) return cudaErrorInvalidValue;
@@ -427,6 +468,12 @@ cudaError_t launch_common(const void* A, const void* A_lo, long lda, const void*
   p.K = K;
   p.m_tiles = (int)((M + kBM - 1) / kBM);
   p.n_tiles = (N + kBN - 1) / kBN;
+  p.swiglu_I = 0;
+  if (epi == kEpiSwiGLU) {  // N = 2I: one tile per 128 channels
+    p.swiglu_I = N / 2;
+    p.n_tiles = (p.swiglu_I + 127) / 128;
+    p.act = *act;
+  }
   p.num_kb = (K + kBK - 1) / kBK;
   if (splits < 1) splits = 1;
   if (splits > p.num_kb) splits = p.num_kb;
@@ -442,6 +489,9 @@ cudaError_t launch_common(const void* A, const void* A_lo, long lda, const void*
   if (epi == kEpiKvCache)
     return A_lo ? launch_variant<true, kEpiKvCache>(ma, malo, mb, p, grid, stream)
                 : launch_variant<false, kEpiKvCache>(ma, malo, mb, p, grid, stream);
+  if (epi == kEpiSwiGLU)
+    return A_lo ? launch_variant<true, kEpiSwiGLU>(ma, malo, mb, p, grid, stream)
+                : launch_variant<false, kEpiSwiGLU>(ma, malo, mb, p, grid, stream);
   return A_lo ? launch_variant<true, kEpiStoreF32>(ma, malo, mb, p, grid, stream)
               : launch_variant<false, kEpiStoreF32>(ma, malo, mb, p, grid, stream);
 }
@@ -452,7 +502,15 @@ cudaError_t launch_gemm_tc(const void* A, const void* A_lo, long lda, const void
                            float* C, long ldc, long M, int N, int K, int splits,
                            const uint8_t* tile_active, unsigned* status, cudaStream_t stream) {
   return launch_common(A, A_lo, lda, Bm, ldb, C, ldc, M, N, K, splits, tile_active, status,
-                       kEpiStoreF32, nullptr, stream);
+                       kEpiStoreF32, nullptr, nullptr, stream);
+}
+
+cudaError_t launch_gemm_tc_swiglu(const void* A, const void* A_lo, long lda, const void* Bm,
+                                  long ldb, long M, int I, int K, const uint8_t* tile_active,
+                                  const ActOut& act, unsigned* status, cudaStream_t stream) {
+  if (I < 1) return cudaErrorInvalidValue;
+  return launch_common(A, A_lo, lda, Bm, ldb, nullptr, 0, M, 2 * I, K, 1, tile_active, status,
+                       kEpiSwiGLU, nullptr, &act, stream);
 }
 
 cudaError_t launch_gemm_tc_kv_cache(const void* A, const void* A_lo, long lda, const void* Bm,
@@ -463,7 +521,7 @@ cudaError_t launch_gemm_tc_kv_cache(const void* A, const void* A_lo, long lda, c
   if (((uintptr_t)kv.kv | (uintptr_t)kv.cos_t | (uintptr_t)kv.sin_t) % 16 != 0)
     return cudaErrorInvalidValue;
   return launch_common(A, A_lo, lda, Bm, ldb, nullptr, 0, M, N, K, 1, tile_active, status,
-                       kEpiKvCache, &kv, stream);
+                       kEpiKvCache, &kv, nullptr, stream);
 }
 
 }  // namespace dflash

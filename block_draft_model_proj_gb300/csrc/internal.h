@@ -96,6 +96,11 @@ struct KvCacheEpilogue {
   int L = 0, pos_offset = 0, L_cache = 0, Hkv = 0;
   int to_tf32 = 0;
 };
+// act = SiLU(gate) * up with [gate | up] = (A + A_lo) W_gate_up^T (W_gate_up [2I][K]: gate
+// rows then up rows), written as a two-term activation by the epilogue (no K-split).
+cudaError_t launch_gemm_tc_swiglu(const void* A, const void* A_lo, long lda, const void* Bm,
+                                  long ldb, long M, int I, int K, const uint8_t* tile_active,
+                                  const ActOut& act, unsigned* status, cudaStream_t stream);
 // C = (A + A_lo) B^T with N = 2*Hkv*128, written to the cache by the epilogue (no K-split).
 cudaError_t launch_gemm_tc_kv_cache(const void* A, const void* A_lo, long lda, const void* Bm,
                                     long ldb, long M, int N, int K, const uint8_t* tile_active,
