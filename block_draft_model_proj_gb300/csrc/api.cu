@@ -439,7 +439,8 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
   {
     Prof pr(DFLASH_PROF_ROWS, 1, s);
     DF_CUDA(launch_rows_norm(cfg->dtype, lay.y, lay.split_proj, w->g_ctx, cfg->rms_eps,
-                             (cfg->flags & DFLASH_FLAG_CTX_NORM) != 0, lay.ctx.out(), M, D, s));
+                             (cfg->flags & DFLASH_FLAG_CTX_NORM) != 0, lay.ctx.out(), M, D,
+                             ctx_len, L, s));
   }
   const size_t layer_elems = (size_t)B * 2 * Hkv * L_cache * dh;
   const bool to_tf32 = cfg->dtype == DFLASH_DTYPE_BF16;

@@ -28,14 +28,20 @@
 // updated running maximum (the accumulator is rescaled only when the maximum grows by more
 // than 2^8, so P stays <= 256).
 //
-// Warp roles: warp 0 TMA producer (Q once; K and V^T tiles of 64 keys, 2-stage ring),
-// warp 1 MMA issuer (S = Q K^T into a double-buffered TMEM S/P area; O += P V with P read
-// from TMEM), warps 2-9 softmax / correction / partial output: two warps per TMEM lane
-// quarter, one per half of the key columns (and of the O columns), so each SM sub-partition
-// runs two softmax warps; the halves agree on the running row maximum through shared
-// memory behind an mbarrier.  Every mbarrier wait is bounded in time; on expiry the CTA
-// reports DFLASH_ERR_TIMEOUT, drains its own copies and MMAs, frees tensor memory and
-// exits.
+// Tensor memory holds the whole working set of a tile: Q (loaded once per unit from global
+// by the softmax warps), the O accumulator, and four S/P buffers (S = Q K^T lands there, the
+// softmax overwrites it with P, and O += P V reads P from there).  Shared memory holds only
+// K and V^T tiles of 64 keys in two separate 3-stage TMA rings.
+// Warp roles: warp 0 TMA producers (lane 0 the K ring, lane 1 the V^T ring); warp 1 MMA
+// issuer, which polls its barriers without blocking and issues S of the next tiles as soon as
+// a K tile and an S/P buffer are free, independently of the PV of earlier tiles; warps 2-9
+// softmax / correction / partial output: two warps per TMEM lane quarter, one per half of
+// the key columns (and of the O columns), so each SM sub-partition runs two softmax warps;
+// the halves agree on the running row maximum through shared memory behind an mbarrier.
+// Fully readable half-tiles take a short path (one zero-byte test per mask word), and
+// P = 2^(x - m) uses the special-function unit directly (an excluded key gives exactly 0).
+// Every mbarrier wait is bounded in time; on expiry the CTA reports DFLASH_ERR_TIMEOUT,
+// drains its own copies and MMAs, frees tensor memory and exits.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
@@ -49,20 +55,20 @@ using namespace tc;
 constexpr int kDH = 128;   // head dim handled by this kernel
 constexpr int kM = 128;    // query rows per tile (TMEM lanes)
 constexpr int kKT = 64;    // keys per tile
-constexpr int kStages = 2;
+constexpr int kRing = 3;   // stages of each of the K and V^T rings
+constexpr int kSP = 4;     // S/P buffers in tensor memory
 constexpr int kThreads = 320;          // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
 constexpr int kSoftmaxWarps = 8;       // two per TMEM lane quarter, each owns half the keys
 constexpr int kHalfKT = 32;            // key columns per softmax thread
-constexpr uint32_t kTmemCols = 256;      // O [0,128) + S/P buffers [128,192), [192,256)
-constexpr uint32_t kQSub = kM * 32 * 4;  // [128 rows][32 dh] fp32, 16 KB
-constexpr uint32_t kQBytes = 4 * kQSub;  // 64 KB
-constexpr uint32_t kKSub = kKT * 32 * 4; // [64 keys][32 dh], 8 KB
+constexpr uint32_t kTmemCols = 512;    // Q [0,128), O [128,256), S/P 4 x 64 [256,512)
+constexpr uint32_t kTmemQ = 0, kTmemO = 128, kTmemS = 256;
+constexpr uint32_t kKSub = kKT * 32 * 4; // K [64 keys][32 dh] fp32, 8 KB
 constexpr uint32_t kKBytes = 4 * kKSub;  // 32 KB
 constexpr uint32_t kVSub = kDH * 32 * 4; // V^T [128 dh][32 keys], 16 KB
 constexpr uint32_t kVBytes = 2 * kVSub;  // 32 KB
-constexpr uint32_t kStageBytes = kKBytes + kVBytes;
-// + barriers, the row-max exchange [2 tiles][2 halves][128 rows] and the row-sum exchange
-constexpr size_t kSmemBytes = 1024 + kQBytes + kStages * (size_t)kStageBytes + 256 +
+constexpr uint32_t kBarBytes = 512;
+// K ring + V ring + barriers + row-max exchange [2][2][128] + row-sum exchange [2][128]
+constexpr size_t kSmemBytes = 1024 + kRing * (size_t)(kKBytes + kVBytes) + kBarBytes +
                               (4 * 128 + 2 * 128) * sizeof(float);
 constexpr uint32_t kIdescS = idesc_tf32(kM, kKT);
 constexpr uint32_t kIdescPV = idesc_tf32(kM, kDH);
@@ -70,6 +76,8 @@ constexpr float kRescaleLog2 = 8.0f;
 
 struct AttnTcParams {
   int B, N, S, L, Hkv, grp, R, bpt, tiles, chunk, max_chunks;
+  const float* q;  // [B][Hkv][N][S][grp][dh], tf32-rounded
+  long q_rows;
   const int32_t* anchors;
   const uint8_t* valid;
   const uint8_t* mask;
@@ -110,46 +118,51 @@ __device__ __forceinline__ UnitInfo decode_unit(const AttnTcParams& p, int unit)
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kc,
-               const __grid_constant__ CUtensorMap map_vc, const __grid_constant__ CUtensorMap map_kb,
-               const __grid_constant__ CUtensorMap map_vb, const AttnTcParams p) {
+attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant__ CUtensorMap map_vc,
+               const __grid_constant__ CUtensorMap map_kb, const __grid_constant__ CUtensorMap map_vb,
+               const AttnTcParams p) {
   const UnitInfo u = decode_unit(p, blockIdx.x);
   if (u.n == 0) return;  // a chunk past this tile's longest prefix: no work
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint8_t* sQ = smem;
-  uint8_t* sKV = smem + kQBytes;  // stage s: K at s*kStageBytes, V^T after it
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + kStages * kStageBytes);
-  uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + kStages;
-  uint64_t* s_full = kv_empty + kStages;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* pv_done = p_full + 2;
-  uint64_t* drain = pv_done + 2;
-  uint64_t* max_bar = drain + 1;   // [2]: row-max exchange of tiles with parity 0 / 1
-  uint64_t* sum_bar = max_bar + 2; // row-sum exchange at the end
+  uint8_t* sK = smem;                        // K ring: stage s at s * kKBytes
+  uint8_t* sV = sK + kRing * kKBytes;        // V^T ring: stage s at s * kVBytes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kRing * kVBytes);
+  uint64_t* k_full = bars;
+  uint64_t* k_empty = k_full + kRing;
+  uint64_t* v_full = k_empty + kRing;
+  uint64_t* v_empty = v_full + kRing;
+  uint64_t* s_full = v_empty + kRing;
+  uint64_t* p_full = s_full + kSP;
+  uint64_t* pv_done = p_full + kSP;
+  uint64_t* q_ready = pv_done + kSP;
+  uint64_t* drain = q_ready + 1;
+  uint64_t* max_bar = drain + 1;    // [2]: row-max exchange of tiles with parity 0 / 1
+  uint64_t* sum_bar = max_bar + 2;  // row-sum exchange at the end
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sum_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* red_max = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);  // [2][2][128]
-  float* red_sum = red_max + 4 * 128;                                                 // [2][128]
+  float* red_max = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + kBarBytes);  // [2][2][128]
+  float* red_sum = red_max + 4 * 128;                                                       // [2][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s2 = 0; s2 < kRing; ++s2) {
+      mbar_init(&k_full[s2], 1);
+      mbar_init(&k_empty[s2], 1);
+      mbar_init(&v_full[s2], 1);
+      mbar_init(&v_empty[s2], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSP; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], kSoftmaxWarps);
       mbar_init(&pv_done[i], 1);
-      mbar_init(&max_bar[i], kSoftmaxWarps);
     }
+    mbar_init(q_ready, kSoftmaxWarps);
     mbar_init(drain, 1);
+    mbar_init(&max_bar[0], kSoftmaxWarps);
+    mbar_init(&max_bar[1], kSoftmaxWarps);
     mbar_init(sum_bar, kSoftmaxWarps);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -159,84 +172,105 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_o = tmem;
-  const uint32_t tmem_s0 = tmem + 128;
+  const uint32_t tmem_q = tmem + kTmemQ, tmem_o = tmem + kTmemO, tmem_s0 = tmem + kTmemS;
 
   const int planes_per_b = 2 * p.Hkv;
   const int plane_k = u.b * planes_per_b + u.g;
   const int plane_v = u.b * planes_per_b + p.Hkv + u.g;
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      const int qrow0 = ((u.b * p.Hkv + u.g) * p.N + u.k0) * p.R;
-      mbar_arrive_expect_tx(q_full, kQBytes);
-      for (int q = 0; q < 4; ++q) tma_load_2d(&map_q, q_full, sQ + q * kQSub, q * 32, qrow0);
-      int issued[kStages] = {0, 0};
-      uint32_t issued_ph[kStages] = {0, 0};
+    // ---------------- TMA producers: lane 0 = the K ring, lane 1 = the V^T ring ----------------
+    if (lane < 2) {
+      const bool is_k = lane == 0;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      int issued[kRing] = {0, 0, 0};
+      uint32_t issued_ph[kRing] = {0, 0, 0};
       for (int i = 0; i < u.n; ++i) {
-        const int st = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        if (!mbar_wait(&kv_empty[st], ph ^ 1u, abort_flag, kWaitLimitNs)) break;
-        mbar_arrive_expect_tx(&kv_full[st], kStageBytes);
-        uint8_t* sK = sKV + st * kStageBytes;
-        uint8_t* sV = sK + kKBytes;
-        if (i < u.nblk) {
-          const int kbrow0 = ((u.b * p.Hkv + u.g) * p.N + u.k0) * p.S + i * kKT;
-          for (int q = 0; q < 4; ++q) tma_load_2d(&map_kb, &kv_full[st], sK + q * kKSub, q * 32, kbrow0);
-          for (int v = 0; v < 2; ++v)
-            tma_load_2d(&map_vb, &kv_full[st], sV + v * kVSub, u.k0 * p.S + i * kKT + v * 32,
-                        (u.b * p.Hkv + u.g) * kDH);
+        const int st = i % kRing;
+        const uint32_t ph = (uint32_t)(i / kRing) & 1u;
+        if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, kWaitLimitNs)) break;
+        if (is_k) {
+          mbar_arrive_expect_tx(&full[st], kKBytes);
+          uint8_t* dst = sK + st * kKBytes;
+          if (i < u.nblk) {
+            const int kbrow0 = ((u.b * p.Hkv + u.g) * p.N + u.k0) * p.S + i * kKT;
+            for (int q = 0; q < 4; ++q) tma_load_2d(&map_kb, &full[st], dst + q * kKSub, q * 32, kbrow0);
+          } else {
+            const int c0 = u.cs + (i - u.nblk) * kKT;
+            for (int q = 0; q < 4; ++q) tma_load_3d(&map_kc, &full[st], dst + q * kKSub, q * 32, c0, plane_k);
+          }
         } else {
-          const int c0 = u.cs + (i - u.nblk) * kKT;
-          for (int q = 0; q < 4; ++q) tma_load_3d(&map_kc, &kv_full[st], sK + q * kKSub, q * 32, c0, plane_k);
-          for (int v = 0; v < 2; ++v)
-            tma_load_3d(&map_vc, &kv_full[st], sV + v * kVSub, c0 + v * 32, 0, plane_v);
+          mbar_arrive_expect_tx(&full[st], kVBytes);
+          uint8_t* dst = sV + st * kVBytes;
+          if (i < u.nblk) {
+            for (int v = 0; v < 2; ++v)
+              tma_load_2d(&map_vb, &full[st], dst + v * kVSub, u.k0 * p.S + i * kKT + v * 32,
+                          (u.b * p.Hkv + u.g) * kDH);
+          } else {
+            const int c0 = u.cs + (i - u.nblk) * kKT;
+            for (int v = 0; v < 2; ++v)
+              tma_load_3d(&map_vc, &full[st], dst + v * kVSub, c0 + v * 32, 0, plane_v);
+          }
         }
         issued[st] = 1;
         issued_ph[st] = ph;
       }
-      mbar_wait(q_full, 0, abort_flag, kWaitLimitNs / 4);
-      for (int s = 0; s < kStages; ++s)
-        if (issued[s]) mbar_wait(&kv_full[s], issued_ph[s], abort_flag, kWaitLimitNs / 4);
+      for (int s2 = 0; s2 < kRing; ++s2)
+        if (issued[s2]) mbar_wait(&full[s2], issued_ph[s2], abort_flag, kWaitLimitNs / 4);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      bool ok = mbar_wait(q_full, 0, abort_flag, kWaitLimitNs);
-      const uint32_t q_addr = smem_u32(sQ);
-      auto issue_pv = [&](int j) -> bool {
-        if (!mbar_wait(&p_full[j & 1], (uint32_t)(j >> 1) & 1u, abort_flag, kWaitLimitNs)) return false;
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(sKV + (j % kStages) * kStageBytes + kKBytes);
-        const uint32_t a_base = tmem_s0 + (uint32_t)((j & 1) * kKT);
-        for (int v = 0; v < 2; ++v)
-          for (int k = 0; k < 4; ++k)
-            umma_tf32_ts(tmem_o, a_base + v * 32 + k * 8, sw128_desc(v_addr + v * kVSub + k * 32),
-                         kIdescPV, (j == 0 && v == 0 && k == 0) ? 0u : 1u);
-        umma_commit(&pv_done[j & 1]);
-        umma_commit(&kv_empty[j % kStages]);
-        return true;
-      };
-      for (int i = 0; i < u.n && ok; ++i) {
-        const int st = i % kStages;
-        if (!mbar_wait(&kv_full[st], (uint32_t)(i / kStages) & 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
-        // the S/P buffer of tile i last held P of tile i-2: its PV must be complete
-        if (i >= 2 && !mbar_wait(&pv_done[i & 1], (uint32_t)((i - 2) >> 1) & 1u, abort_flag, kWaitLimitNs)) {
-          ok = false;
-          break;
+      // S(i) = Q K_i^T into S/P buffer i % kSP once K_i has landed and the PV that last read
+      // that buffer (tile i - kSP) is complete; O += P_j V_j once the softmax has written P_j
+      // and V_j has landed.  Both are polled without blocking, S first, so the S of the next
+      // tiles is computed while the softmax works on the current one.
+      bool ok = mbar_wait(q_ready, 0, abort_flag, kWaitLimitNs);
+      tc_fence_after();
+      int ns = 0, npv = 0;
+      uint64_t t_idle = 0;
+      while (ok && npv < u.n) {
+        bool progressed = false;
+        if (ns < u.n && ns - npv < kSP &&
+            mbar_test(&k_full[ns % kRing], (uint32_t)(ns / kRing) & 1u) &&
+            (ns < kSP || mbar_test(&pv_done[ns % kSP], (uint32_t)((ns - kSP) / kSP) & 1u))) {
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(sK + (ns % kRing) * kKBytes);
+          const uint32_t s_tmem = tmem_s0 + (uint32_t)((ns % kSP) * kKT);
+#pragma unroll 1
+          for (int k = 0; k < kDH / 8; ++k)
+            umma_tf32_ts(s_tmem, tmem_q + k * 8, sw128_desc(k_addr + (k >> 2) * kKSub + (k & 3) * 32),
+                         kIdescS, k ? 1u : 0u);
+          umma_commit(&s_full[ns % kSP]);
+          umma_commit(&k_empty[ns % kRing]);
+          ++ns;
+          progressed = true;
+        } else if (npv < ns && mbar_test(&p_full[npv % kSP], (uint32_t)(npv / kSP) & 1u) &&
+                   mbar_test(&v_full[npv % kRing], (uint32_t)(npv / kRing) & 1u)) {
+          tc_fence_after();
+          const uint32_t v_addr = smem_u32(sV + (npv % kRing) * kVBytes);
+          const uint32_t a_base = tmem_s0 + (uint32_t)((npv % kSP) * kKT);
+#pragma unroll 1
+          for (int v = 0; v < 2; ++v)
+            for (int k = 0; k < 4; ++k)
+              umma_tf32_ts(tmem_o, a_base + v * 32 + k * 8, sw128_desc(v_addr + v * kVSub + k * 32),
+                           kIdescPV, (npv == 0 && v == 0 && k == 0) ? 0u : 1u);
+          umma_commit(&pv_done[npv % kSP]);
+          umma_commit(&v_empty[npv % kRing]);
+          ++npv;
+          progressed = true;
         }
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(sKV + st * kStageBytes);
-        const uint32_t s_tmem = tmem_s0 + (uint32_t)((i & 1) * kKT);
-        for (int q = 0; q < 4; ++q)
-          for (int k = 0; k < 4; ++k)
-            umma_tf32_ss(s_tmem, sw128_desc(q_addr + q * kQSub + k * 32),
-                         sw128_desc(k_addr + q * kKSub + k * 32), kIdescS, (q | k) ? 1u : 0u);
-        umma_commit(&s_full[i & 1]);
-        if (i >= 1 && !issue_pv(i - 1)) { ok = false; break; }
+        if (progressed) {
+          t_idle = 0;
+        } else {
+          __nanosleep(32);  // leave the issue slots to the softmax warps of this sub-partition
+          const uint64_t now = globaltimer_ns();
+          if (t_idle == 0) t_idle = now;
+          if (*abort_flag) ok = false;
+          else if (now - t_idle > kWaitLimitNs) { *abort_flag = 1; ok = false; }
+        }
       }
-      if (ok) issue_pv(u.n - 1);
       umma_commit(drain);
       mbar_wait(drain, 0, abort_flag, kWaitLimitNs / 4);
     }
@@ -256,6 +290,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       const int a = p.anchors[u.b * p.N + kb];
       row_valid = a >= 0 && p.valid[(u.b * p.N + kb) * p.S + j] != 0;
       a_row = min(max(a, 0), p.L);
+    }
+    // this thread's half of the query row -> tensor memory (columns [64*half, +64) of Q)
+    {
+      const long qrow = (long)((u.b * p.Hkv + u.g) * p.N + u.k0) * p.R + r;
+      const float4* qsrc = reinterpret_cast<const float4*>(p.q + qrow * kDH + half * 64);
+      for (int part = 0; part < 2; ++part) {
+        uint32_t qv[32];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float4 f = qrow < p.q_rows ? __ldg(qsrc + part * 8 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+          qv[4 * e] = __float_as_uint(f.x);
+          qv[4 * e + 1] = __float_as_uint(f.y);
+          qv[4 * e + 2] = __float_as_uint(f.z);
+          qv[4 * e + 3] = __float_as_uint(f.w);
+        }
+        tmem_st_32x32b_x32(tmem_q + lane_off + half * 64 + part * 32, qv);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_ready);
     }
     const uint8_t* mrow = p.mask + (size_t)u.b * p.L;
     float m_run = -INFINITY, l_run = 0.f;  // l_run: this half's share of the row sum
@@ -282,21 +337,38 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 #pragma unroll
       for (int w4 = 0; w4 < kHalfKT / 4; ++w4) mask_cur[w4] = mask_next[w4];
       load_mask(i + 1, mask_next);
-      if (!wait_all(&s_full[i & 1], (uint32_t)(i >> 1) & 1u)) { ok = false; break; }
+      if (!wait_all(&s_full[i % kSP], (uint32_t)(i / kSP) & 1u)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t s_tmem = tmem_s0 + (uint32_t)((i & 1) * kKT + half * kHalfKT) + lane_off;
+      const uint32_t s_tmem = tmem_s0 + (uint32_t)((i % kSP) * kKT + half * kHalfKT) + lane_off;
       uint32_t sv[kHalfKT];
       tmem_ld_32x32b_x32(s_tmem, sv);
       const bool blk_tile = i < u.nblk;
       const int c0 = blk_tile ? 0 : u.cs + (i - u.nblk) * kKT + half * kHalfKT;
       float x[kHalfKT];
       float mh = -INFINITY;
-      if (blk_tile) {
+      // short path: every key of this half-tile is readable (inside the row's prefix and the
+      // chunk, and no mask word has a zero byte)
+      bool all_ok = !blk_tile && row_valid && c0 + kHalfKT <= a_row && c0 + kHalfKT <= u.ce;
+#pragma unroll
+      for (int w4 = 0; w4 < kHalfKT / 4; ++w4) {
+        const uint32_t mw = mask_cur[w4];
+        all_ok = all_ok && (((mw - 0x01010101u) & ~mw & 0x80808080u) == 0u);
+      }
+      if (all_ok) {
+#pragma unroll
+        for (int kk = 0; kk < kHalfKT; ++kk) {
+          x[kk] = __uint_as_float(sv[kk]) * p.scale_log2;
+          mh = fmaxf(mh, x[kk]);
+        }
+      } else if (!row_valid) {
+#pragma unroll
+        for (int kk = 0; kk < kHalfKT; ++kk) x[kk] = -INFINITY;
+      } else if (blk_tile) {
 #pragma unroll
         for (int kk = 0; kk < kHalfKT; ++kk) {
           const int q = u.k0 * p.S + i * kKT + half * kHalfKT + kk;
           const int kbk = q / p.S, jj = q - kbk * p.S;
-          const bool okk = row_valid && kbk == kb && p.valid[(u.b * p.N + kbk) * p.S + jj] != 0;
+          const bool okk = kbk == kb && p.valid[(u.b * p.N + kbk) * p.S + jj] != 0;
           x[kk] = okk ? __uint_as_float(sv[kk]) * p.scale_log2 : -INFINITY;
           mh = fmaxf(mh, x[kk]);
         }
@@ -336,7 +408,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       if (__any_sync(0xffffffffu, factor != 1.f)) {
         // the PV of the previous tile must have landed before the accumulator is touched;
         // this half rescales O columns [64*half, 64*half + 64)
-        if (!wait_all(&pv_done[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1u)) { ok = false; break; }
+        if (!wait_all(&pv_done[(i - 1) % kSP], (uint32_t)((i - 1) / kSP) & 1u)) { ok = false; break; }
         tc_fence_after();
         for (int part = 0; part < 2; ++part) {
           uint32_t ov[32];
@@ -349,12 +421,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         tmem_wait_st();
         l_run *= factor;
       }
+      // P = 2^(x - m): an excluded key (x = -inf) gives exactly +0; a row that has not seen
+      // a readable key yet (m_run = -inf) has only excluded keys here
       float lsum = 0.f;
+      if (m_run == -INFINITY) {
 #pragma unroll
-      for (int kk = 0; kk < kHalfKT; ++kk) {
-        const float pv = x[kk] == -INFINITY ? 0.f : round_tf32(exp2f(x[kk] - m_run));
-        lsum += pv;
-        sv[kk] = __float_as_uint(pv);
+        for (int kk = 0; kk < kHalfKT; ++kk) sv[kk] = 0u;
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < kHalfKT; ++kk) {
+          const float pv = round_tf32(ex2_approx(x[kk] - m_run));
+          lsum += pv;
+          sv[kk] = __float_as_uint(pv);
+        }
       }
       l_run += lsum;
       tmem_st_32x32b_x32(s_tmem, sv);
@@ -363,11 +442,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       // V^T row r of key sub-tile `half`) so that whatever the cache holds there cannot
       // meet a zero P as NaN
       if (!blk_tile && u.cs + (i - u.nblk) * kKT + kKT > u.a_max) {
-        const int st = i % kStages;
-        if (!wait_all(&kv_full[st], (uint32_t)(i / kStages) & 1u)) { ok = false; break; }
+        const int st = i % kRing;
+        if (!wait_all(&v_full[st], (uint32_t)(i / kRing) & 1u)) { ok = false; break; }
         const int nvalid = u.a_max - (u.cs + (i - u.nblk) * kKT);
-        uint8_t* rowp = sKV + st * kStageBytes + kKBytes + half * kVSub + (r >> 3) * 1024 +
-                        (r & 7) * 128;
+        uint8_t* rowp = sV + st * kVBytes + half * kVSub + (r >> 3) * 1024 + (r & 7) * 128;
         for (int ch = 0; ch < 8; ++ch) {
           const int key0 = half * 32 + ch * 4;
           if (key0 + 4 <= nvalid) continue;
@@ -383,10 +461,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[i & 1]);
+      if (lane == 0) mbar_arrive(&p_full[i % kSP]);
     }
     // final accumulator -> partial (m, l, O) of this unit; each half writes its 64 columns
-    if (ok && wait_all(&pv_done[(u.n - 1) & 1], (uint32_t)((u.n - 1) >> 1) & 1u)) {
+    if (ok && wait_all(&pv_done[(u.n - 1) % kSP], (uint32_t)((u.n - 1) / kSP) & 1u)) {
       tc_fence_after();
       const size_t rowi = (size_t)blockIdx.x * kM + r;
       float4* po = reinterpret_cast<float4*>(p.part_o + rowi * kDH + half * 64);
@@ -542,6 +620,8 @@ cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream) {
   p.tiles = lay.tiles;
   p.chunk = lay.chunk;
   p.max_chunks = lay.max_chunks;
+  p.q = a.q;
+  p.q_rows = (long)a.B * a.Hkv * a.N * lay.R;
   p.anchors = a.anchors;
   p.valid = a.valid;
   p.mask = a.mask;
@@ -551,14 +631,7 @@ cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream) {
   p.status = a.status;
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)kDH));
 
-  CUtensorMap mq, mkc, mvc, mkb, mvb;
-  const long q_rows = (long)a.B * a.Hkv * a.N * lay.R;
-  {
-    cuuint64_t dims[2] = {(cuuint64_t)kDH, (cuuint64_t)q_rows};
-    cuuint64_t str[1] = {(cuuint64_t)kDH * 4};
-    cuuint32_t box[2] = {32, (cuuint32_t)kM};
-    if (!encode_f32(&mq, a.q, 2, dims, str, box)) return cudaErrorInvalidValue;
-  }
+  CUtensorMap mkc, mvc, mkb, mvb;
   const long planes = (long)a.B * 2 * a.Hkv;
   {
     cuuint64_t dims[3] = {(cuuint64_t)kDH, (cuuint64_t)a.L, (cuuint64_t)planes};
@@ -592,7 +665,7 @@ cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  attn_tc_kernel<<<(unsigned)lay.units, kThreads, kSmemBytes, stream>>>(mq, mkc, mvc, mkb, mvb, p);
+  attn_tc_kernel<<<(unsigned)lay.units, kThreads, kSmemBytes, stream>>>(mkc, mvc, mkb, mvb, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long rows = (long)a.B * a.Hkv * lay.tiles * kM;

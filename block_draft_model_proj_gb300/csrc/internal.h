@@ -48,9 +48,11 @@ cudaError_t launch_residual_norm(int mode, int dtype, float* x, const void* emb,
                                  const uint8_t* valid, bool final_norm, long rows, int D,
                                  cudaStream_t stream);
 
-// Plain RMSNorm of fp32 rows (the context norm); with_norm=false copies.
+// Plain RMSNorm of fp32 rows (the context norm); with_norm=false copies.  Rows r = b*L + c
+// with c >= ctx_len[b] are skipped when ctx_len is given (vectorised path).
 cudaError_t launch_rows_norm(int dtype, const float* y, int nsplit, const void* g, double eps,
-                             bool with_norm, ActOut out, long rows, int D, cudaStream_t stream);
+                             bool with_norm, ActOut out, long rows, int D,
+                             const int32_t* ctx_len, int L, cudaStream_t stream);
 
 // QKV epilogue: y [nsplit][T][(Hq+2Hkv)*dh] fp32 -> attention-ready fp32 operands
 // q [B][Hkv][N][S][grp][dh], kb [B][Hkv][N*S][dh], vbt [B][Hkv][dh][ns_pad]; RoPE on q and

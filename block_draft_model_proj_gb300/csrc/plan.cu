@@ -98,15 +98,32 @@ plan_kernel(const uint8_t* __restrict__ mask, const int64_t* __restrict__ sids, 
         if ((key & prefix_mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
       }
       __syncthreads();
-      if (tid == 0) {
-        int cum = 0, d = 0;
-        for (; d < 256; ++d) {
-          if (cum + (int)hist[d] >= remaining) break;
-          cum += (int)hist[d];
+      if (tid < 32) {
+        // warp 0 finds the digit d where the running count of smaller digits first reaches
+        // `remaining`: lane l owns bins 8l .. 8l+7
+        const int lane = tid;
+        int mine = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mine += (int)hist[lane * 8 + q];
+        int incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int up = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += up;
         }
-        sh_sel_digit = d;
-        sh_remaining = remaining - cum;
-        sh_equal = d < 256 ? (int)hist[d] : 0;
+        const int excl = incl - mine;
+        const unsigned hit = __ballot_sync(0xffffffffu, incl >= remaining);
+        const int owner = __ffs(hit) - 1;  // more candidates than anchors: always a hit
+        if (lane == owner) {
+          int cum = excl, d = lane * 8;
+          for (; d < lane * 8 + 7; ++d) {
+            if (cum + (int)hist[d] >= remaining) break;
+            cum += (int)hist[d];
+          }
+          sh_sel_digit = d;
+          sh_remaining = remaining - cum;
+          sh_equal = (int)hist[d];
+        }
       }
       __syncthreads();
       prefix |= (uint64_t)sh_sel_digit << shift;

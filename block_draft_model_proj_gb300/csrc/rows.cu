@@ -177,9 +177,12 @@ __global__ void residual_norm_vec_kernel(int mode, int dt, float* __restrict__ x
 template <int kV>
 __global__ void rows_norm_vec_kernel(int dt, const float* __restrict__ y, int nsplit,
                                      long split_stride, const void* __restrict__ g, float eps,
-                                     bool with_norm, ActOut out, int D) {
+                                     bool with_norm, ActOut out, int D,
+                                     const int32_t* __restrict__ ctx_len, int L) {
   __shared__ float red[33];
   const long r = blockIdx.x;
+  // context rows no block reads (c >= ctx_len[b]) are left unwritten
+  if (ctx_len && (int)(r % L) >= ctx_len[r / L]) return;
   const int D4 = D / 4;
   float4 v[kV];
   float ss = 0.f;
@@ -394,17 +397,20 @@ cudaError_t launch_residual_norm(int mode, int dtype, float* x, const void* emb,
 }
 
 cudaError_t launch_rows_norm(int dtype, const float* y, int nsplit, const void* g, double eps,
-                             bool with_norm, ActOut out, long rows, int D, cudaStream_t stream) {
+                             bool with_norm, ActOut out, long rows, int D,
+                             const int32_t* ctx_len, int L, cudaStream_t stream) {
   if (D % 4 == 0 && D <= 4 * 4 * 1024) {
     const int D4 = D / 4;
     const int threads = D4 >= 1024 ? 1024 : ((D4 + 31) / 32) * 32;
     const int per = (D4 + threads - 1) / threads;
     if (per <= 1)
       rows_norm_vec_kernel<1><<<rows, threads, 0, stream>>>(dtype, y, nsplit, rows * D, g,
-                                                            (float)eps, with_norm, out, D);
+                                                            (float)eps, with_norm, out, D,
+                                                            ctx_len, L);
     else
       rows_norm_vec_kernel<4><<<rows, threads, 0, stream>>>(dtype, y, nsplit, rows * D, g,
-                                                            (float)eps, with_norm, out, D);
+                                                            (float)eps, with_norm, out, D,
+                                                            ctx_len, L);
     return cudaGetLastError();
   }
   const int threads = D >= 2048 ? 512 : 256;
