@@ -134,6 +134,22 @@ class ClockSampler:
 # the GPU arm
 # --------------------------------------------------------------------------------------
 
+def profiled_traffic(workload: str):
+    """DRAM bytes per GEMM launch from the committed ncu capture of this workload, or None
+    when there is none or the GEMM kernel's sources changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"gemm_tc_traffic_{workload}.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    h = hashlib.sha256()
+    for src in rec["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return rec["dram_bytes_per_launch"] if h.hexdigest() == rec["source_sha256"] else None
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -364,7 +380,9 @@ def run_ours(args, rank, world, local_rank):
                          "logits 0.16 GB read per step)",
                    "parallelism": f"replicas: {world} rank(s), each its own rows, no collective"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": (achieved / peak) if achieved else None, "traffic": None,
+                     "frac": (achieved / peak) if achieved else None,
+                     "traffic": profiled_traffic(base.name),
+                     "traffic_unit": "bytes per launch (ncu dram read + write)",
                      "kernel": "gemm_tc (tcgen05 projection GEMMs)",
                      "peak_source": f"{peaks['source']} bf16_tflops_sustained",
                      "launches_per_step": gemm_n / args.steps},
