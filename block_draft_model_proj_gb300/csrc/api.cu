@@ -222,9 +222,9 @@ int check_ws(void* ws, size_t ws_bytes, size_t need) {
 // for fp32.
 cudaError_t gemm(int dtype, const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
                  float* C, long ldc, long M, int N, int K, int splits, cudaStream_t s,
-                 const uint8_t* tile_active = nullptr) {
+                 const int32_t* tile_list = nullptr) {
   if (dtype == DFLASH_DTYPE_BF16)
-    return launch_gemm_tc(A, A_lo, lda, Bm, ldb, C, ldc, M, N, K, splits, tile_active,
+    return launch_gemm_tc(A, A_lo, lda, Bm, ldb, C, ldc, M, N, K, splits, tile_list,
                           status_ptr(), s);
   return launch_gemm_simt(dtype, A, lda, Bm, ldb, C, ldc, M, N, K, splits, s);
 }
@@ -263,7 +263,7 @@ struct ProjLayout {
   Act ctx;
   float* cos_t;
   float* sin_t;
-  uint8_t* tile_flags;
+  int32_t* tile_list;
   int split_proj, split_kv;
   size_t bytes;
 };
@@ -282,7 +282,7 @@ ProjLayout proj_layout(const dflash_config_t* c, int B, int L, void* ws) {
   p.ctx = take_act(cv, (size_t)M * D, c->dtype);
   p.cos_t = cv.take<float>((size_t)L * (c->head_dim / 2));
   p.sin_t = cv.take<float>((size_t)L * (c->head_dim / 2));
-  p.tile_flags = cv.take<uint8_t>((size_t)(M + kGemmTileM - 1) / kGemmTileM);
+  p.tile_list = cv.take<int32_t>(1 + (size_t)(M + kGemmTileM - 1) / kGemmTileM);
   p.bytes = cv.off;
   return p;
 }
@@ -293,7 +293,7 @@ struct BodyLayout {
   float *q, *kb, *vbt;  // attention-ready operands
   int ns_pad;
   float* partials;      // tensor-core attention partials (bf16 configuration)
-  uint8_t* tile_flags;  // 128-row tiles of slots holding at least one valid slot
+  int32_t* tile_list;   // 128-slot tiles holding at least one valid slot (count first)
   float* y;
   float* cos_t;
   float* sin_t;
@@ -330,7 +330,7 @@ BodyLayout body_layout(const dflash_config_t* c, int B, int L, int N, void* ws) 
   b.attn = take_act(cv, (size_t)T * qw, c->dtype);
   b.act = take_act(cv, (size_t)T * I, c->dtype);
   b.y = cv.take<float>((size_t)T * ycols);
-  b.tile_flags = cv.take<uint8_t>((size_t)(T + kGemmTileM - 1) / kGemmTileM);
+  b.tile_list = cv.take<int32_t>(1 + (size_t)(T + kGemmTileM - 1) / kGemmTileM);
   b.P = L + c->block_size;
   b.cos_t = cv.take<float>((size_t)b.P * (c->head_dim / 2));
   b.sin_t = cv.take<float>((size_t)b.P * (c->head_dim / 2));
@@ -425,11 +425,11 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
     DF_CUDA(launch_rope_table(lay.cos_t, lay.sin_t, pos_offset, L, dh, cfg->rope_theta, s));
   }
   // 128-row tiles no block reads (all c >= ctx_len[b]) are skipped by every projection
-  const uint8_t* flags = nullptr;
+  const int32_t* flags = nullptr;
   if (ctx_len && cfg->dtype == DFLASH_DTYPE_BF16) {
     Prof pr(DFLASH_PROF_ROWS, 1, s);
-    DF_CUDA(launch_ctx_tile_flags(ctx_len, B, L, lay.tile_flags, s));
-    flags = lay.tile_flags;
+    DF_CUDA(launch_ctx_tile_list(ctx_len, B, L, lay.tile_list, s));
+    flags = lay.tile_list;
   }
   {
     Prof pr(DFLASH_PROF_GEMM, 1, s);
@@ -512,11 +512,11 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
   const size_t layer_elems = (size_t)B * 2 * Hkv * L * dh;
 
   // 128-slot tiles without a valid slot are skipped by every projection
-  const uint8_t* flags = nullptr;
+  const int32_t* flags = nullptr;
   if (dt == DFLASH_DTYPE_BF16) {
     Prof pr(DFLASH_PROF_ROWS, 1, s);
-    DF_CUDA(launch_slot_tile_flags(block_valid, T, lay.tile_flags, s));
-    flags = lay.tile_flags;
+    DF_CUDA(launch_slot_tile_list(block_valid, T, lay.tile_list, s));
+    flags = lay.tile_list;
   }
   {
     Prof pr(DFLASH_PROF_ROWS, 2, s);

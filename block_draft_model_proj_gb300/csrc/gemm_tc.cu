@@ -80,15 +80,35 @@ struct TcParams {
   int m_tiles, n_tiles, splits, kb_per_split, num_kb;
   float* C;
   long ldc;
-  const uint8_t* tile_active;  // per M tile, optional
+  const int32_t* tile_list;    // optional: [0] = count, [1..] = active M tiles in order
+  int m_fastest;               // tile order: M tiles fastest (shares each B tile) or N fastest
   unsigned* status;
   KvCacheEpilogue kv;          // used by the kEpiKvCache epilogue only
   ActOut act;                  // kEpiSwiGLU: two-term SiLU(gate) * up, [M][swiglu_I]
   int swiglu_I;                // kEpiSwiGLU: B rows [0, I) gate, [I, 2I) up
 };
 
-__device__ __forceinline__ bool tile_on(const TcParams& p, int m_t) {
-  return p.tile_active == nullptr || p.tile_active[m_t] != 0;
+// Number of M tiles the work list runs over: all, or the compacted active ones.
+__device__ __forceinline__ int active_m_tiles(const TcParams& p) {
+  return p.tile_list ? p.tile_list[0] : p.m_tiles;
+}
+
+// Work item t -> (M tile, N tile, K split).  Every role walks the same sequence.
+__device__ __forceinline__ void decode_tile(const TcParams& p, int m_cnt, int t, int& m_t, int& n_t,
+                                            int& z) {
+  int mi;
+  if (p.m_fastest) {
+    mi = t % m_cnt;
+    const int rest = t / m_cnt;
+    n_t = rest % p.n_tiles;
+    z = rest / p.n_tiles;
+  } else {
+    n_t = t % p.n_tiles;
+    const int rest = t / p.n_tiles;
+    mi = rest % m_cnt;
+    z = rest / m_cnt;
+  }
+  m_t = p.tile_list ? p.tile_list[1 + mi] : mi;
 }
 
 
@@ -244,7 +264,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int total = p.m_tiles * p.n_tiles * p.splits;
+  const int m_cnt = active_m_tiles(p);
+  const int total = m_cnt * p.n_tiles * p.splits;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -256,11 +277,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       for (int s = 0; s < kStages; ++s) issued[s] = 0, issued_ph[s] = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const int n_t = t % p.n_tiles;
-        const int rest = t / p.n_tiles;
-        const int m_t = rest % p.m_tiles;
-        const int z = rest / p.m_tiles;
-        if (!tile_on(p, m_t)) continue;
+        int m_t, n_t, z;
+        decode_tile(p, m_cnt, t, m_t, n_t, z);
         const int kb0 = z * p.kb_per_split;
         const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -294,9 +312,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       uint32_t acc_ph = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const int rest = t / p.n_tiles;
-        const int z = rest / p.m_tiles;
-        if (!tile_on(p, rest % p.m_tiles)) continue;
+        int m_t, n_t, z;
+        decode_tile(p, m_cnt, t, m_t, n_t, z);
         const int kb0 = z * p.kb_per_split;
         const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         if (!mbar_wait(&tempty[acc], acc_ph ^ 1u, abort_flag, kWaitLimitNs)) break;
@@ -332,11 +349,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const int n_t = t % p.n_tiles;
-      const int rest = t / p.n_tiles;
-      const int m_t = rest % p.m_tiles;
-      const int z = rest / p.m_tiles;
-      if (!tile_on(p, m_t)) continue;
+      int m_t, n_t, z;
+      decode_tile(p, m_cnt, t, m_t, n_t, z);
       // warp-uniform result: the tcgen05.ld below is .sync.aligned
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_ph, abort_flag, kWaitLimitNs) ? 1 : 0))
         break;
@@ -454,7 +468,7 @@ cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& malo, const
 
 cudaError_t launch_common(const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
                           float* C, long ldc, long M, int N, int K, int splits,
-                          const uint8_t* tile_active, unsigned* status, int epi,
+                          const int32_t* tile_list, unsigned* status, int epi,
                           const KvCacheEpilogue* kv, const ActOut* act, cudaStream_t stream) {
   if (((uintptr_t)A | (uintptr_t)A_lo | (uintptr_t)Bm) % 16 != 0) return cudaErrorInvalidValue;
   CUtensorMap ma, malo, mb;
@@ -481,7 +495,11 @@ cudaError_t launch_common(const void* A, const void* A_lo, long lda, const void*
   p.splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;  // no empty split
   p.C = C;
   p.ldc = ldc;
-  p.tile_active = tile_active;
+  p.tile_list = tile_list;
+  // M tiles fastest when A is the smaller operand: the CTAs that share a B tile then run
+  // in the same wave and read it once
+  const double a_bytes = (double)M * K * 2 * (A_lo ? 2 : 1), b_bytes = (double)N * K * 2;
+  p.m_fastest = a_bytes <= b_bytes ? 1 : 0;
   p.status = status;
   if (kv) p.kv = *kv;
   const long tiles = (long)p.m_tiles * p.n_tiles * p.splits;
@@ -500,27 +518,27 @@ cudaError_t launch_common(const void* A, const void* A_lo, long lda, const void*
 
 cudaError_t launch_gemm_tc(const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
                            float* C, long ldc, long M, int N, int K, int splits,
-                           const uint8_t* tile_active, unsigned* status, cudaStream_t stream) {
-  return launch_common(A, A_lo, lda, Bm, ldb, C, ldc, M, N, K, splits, tile_active, status,
+                           const int32_t* tile_list, unsigned* status, cudaStream_t stream) {
+  return launch_common(A, A_lo, lda, Bm, ldb, C, ldc, M, N, K, splits, tile_list, status,
                        kEpiStoreF32, nullptr, nullptr, stream);
 }
 
 cudaError_t launch_gemm_tc_swiglu(const void* A, const void* A_lo, long lda, const void* Bm,
-                                  long ldb, long M, int I, int K, const uint8_t* tile_active,
+                                  long ldb, long M, int I, int K, const int32_t* tile_list,
                                   const ActOut& act, unsigned* status, cudaStream_t stream) {
   if (I < 1) return cudaErrorInvalidValue;
-  return launch_common(A, A_lo, lda, Bm, ldb, nullptr, 0, M, 2 * I, K, 1, tile_active, status,
+  return launch_common(A, A_lo, lda, Bm, ldb, nullptr, 0, M, 2 * I, K, 1, tile_list, status,
                        kEpiSwiGLU, nullptr, &act, stream);
 }
 
 cudaError_t launch_gemm_tc_kv_cache(const void* A, const void* A_lo, long lda, const void* Bm,
-                                    long ldb, long M, int N, int K, const uint8_t* tile_active,
+                                    long ldb, long M, int N, int K, const int32_t* tile_list,
                                     const KvCacheEpilogue& kv, unsigned* status,
                                     cudaStream_t stream) {
   if (N != 2 * kv.Hkv * 128 || kv.L < 1) return cudaErrorInvalidValue;
   if (((uintptr_t)kv.kv | (uintptr_t)kv.cos_t | (uintptr_t)kv.sin_t) % 16 != 0)
     return cudaErrorInvalidValue;
-  return launch_common(A, A_lo, lda, Bm, ldb, nullptr, 0, M, N, K, 1, tile_active, status,
+  return launch_common(A, A_lo, lda, Bm, ldb, nullptr, 0, M, N, K, 1, tile_list, status,
                        kEpiKvCache, &kv, nullptr, stream);
 }
 

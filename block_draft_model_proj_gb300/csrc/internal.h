@@ -83,8 +83,8 @@ cudaError_t launch_gemm_simt(int dtype, const void* A, long lda, const void* Bm,
 
 // ---- gemm_tc.cu: tcgen05 bf16 GEMM, fp32 output, optional K-split ----
 // A_lo != nullptr selects the two-term activation path C = (A + A_lo) B^T.
-// tile_active (optional, one byte per 128-row M tile): tiles flagged 0 are skipped entirely
-// (their C rows are left unwritten).
+// tile_list (optional, device): [0] = count, [1..] = the 128-row M tiles to compute, in
+// order; tiles not listed are skipped entirely (their C rows are left unwritten).
 constexpr int kGemmTileM = 128;
 bool gemm_tc_supported(long M, int N, int K, long lda, long ldb);
 
@@ -101,24 +101,25 @@ struct KvCacheEpilogue {
 // act = SiLU(gate) * up with [gate | up] = (A + A_lo) W_gate_up^T (W_gate_up [2I][K]: gate
 // rows then up rows), written as a two-term activation by the epilogue (no K-split).
 cudaError_t launch_gemm_tc_swiglu(const void* A, const void* A_lo, long lda, const void* Bm,
-                                  long ldb, long M, int I, int K, const uint8_t* tile_active,
+                                  long ldb, long M, int I, int K, const int32_t* tile_list,
                                   const ActOut& act, unsigned* status, cudaStream_t stream);
 // C = (A + A_lo) B^T with N = 2*Hkv*128, written to the cache by the epilogue (no K-split).
 cudaError_t launch_gemm_tc_kv_cache(const void* A, const void* A_lo, long lda, const void* Bm,
-                                    long ldb, long M, int N, int K, const uint8_t* tile_active,
+                                    long ldb, long M, int N, int K, const int32_t* tile_list,
                                     const KvCacheEpilogue& kv, unsigned* status,
                                     cudaStream_t stream);
 cudaError_t launch_gemm_tc(const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
                            float* C, long ldc, long M, int N, int K, int splits,
-                           const uint8_t* tile_active, unsigned* status, cudaStream_t stream);
+                           const int32_t* tile_list, unsigned* status, cudaStream_t stream);
 
-// ---- rows.cu: M-tile activity flags for the GEMMs ----
+// ---- rows.cu: compacted lists of active 128-row M tiles for the GEMMs ----
+// list[0] = count, list[1..] = tile indices in increasing order; list holds 1 + tiles ints.
 // Context rows m = b*L + c: tile active iff some row has c < ctx_len[b].
-cudaError_t launch_ctx_tile_flags(const int32_t* ctx_len, int B, int L, uint8_t* flags,
-                                  cudaStream_t stream);
+cudaError_t launch_ctx_tile_list(const int32_t* ctx_len, int B, int L, int32_t* list,
+                                 cudaStream_t stream);
 // Body rows t: tile active iff some row is a valid slot.
-cudaError_t launch_slot_tile_flags(const uint8_t* valid, long T, uint8_t* flags,
-                                   cudaStream_t stream);
+cudaError_t launch_slot_tile_list(const uint8_t* valid, long T, int32_t* list,
+                                  cudaStream_t stream);
 
 // ---- attention.cu ----
 struct AttnArgs {

@@ -13,6 +13,8 @@
 #include <math.h>
 
 #include "common.cuh"
+#include <algorithm>
+
 #include "internal.h"
 
 namespace dflash {
@@ -377,8 +379,10 @@ cudaError_t launch_residual_norm(int mode, int dtype, float* x, const void* emb,
                                  const uint8_t* valid, bool final_norm, long rows, int D,
                                  cudaStream_t stream) {
   if (D % 4 == 0 && D <= 4 * 4 * 1024) {
+    // a quarter of the row's float4 groups per thread: 4 independent 16-byte loads in
+    // flight per thread and several rows per SM
     const int D4 = D / 4;
-    const int threads = D4 >= 1024 ? 1024 : ((D4 + 31) / 32) * 32;
+    const int threads = std::min(1024, std::max(32, ((D4 + 3) / 4 + 31) / 32 * 32));
     const int per = (D4 + threads - 1) / threads;
     if (per <= 1)
       residual_norm_vec_kernel<1><<<rows, threads, 0, stream>>>(mode, dtype, x, emb, y, nsplit,
@@ -400,8 +404,10 @@ cudaError_t launch_rows_norm(int dtype, const float* y, int nsplit, const void* 
                              bool with_norm, ActOut out, long rows, int D,
                              const int32_t* ctx_len, int L, cudaStream_t stream) {
   if (D % 4 == 0 && D <= 4 * 4 * 1024) {
+    // a quarter of the row's float4 groups per thread: 4 independent 16-byte loads in
+    // flight per thread and several rows per SM
     const int D4 = D / 4;
-    const int threads = D4 >= 1024 ? 1024 : ((D4 + 31) / 32) * 32;
+    const int threads = std::min(1024, std::max(32, ((D4 + 3) / 4 + 31) / 32 * 32));
     const int per = (D4 + threads - 1) / threads;
     if (per <= 1)
       rows_norm_vec_kernel<1><<<rows, threads, 0, stream>>>(dtype, y, nsplit, rows * D, g,
@@ -450,49 +456,68 @@ cudaError_t launch_ctx_kv_scatter(const float* y, int nsplit, const float* cos_t
 
 namespace {
 
-// one thread per 128-row tile
-__global__ void ctx_tile_flags_kernel(const int32_t* __restrict__ ctx_len, int B, int L,
-                                      uint8_t* __restrict__ flags, long tiles) {
-  const long t = blockIdx.x * (long)blockDim.x + threadIdx.x;
-  if (t >= tiles) return;
-  const long m0 = t * kGemmTileM, m1 = min(m0 + kGemmTileM, (long)B * L);
-  uint8_t on = 0;
-  for (long m = m0; m < m1 && !on; ) {
-    const int b = (int)(m / L);
-    const long row_end = min(m1, (long)(b + 1) * L);
-    const int c = (int)(m - (long)b * L);
-    int cl = ctx_len[b];
-    cl = cl < 0 ? 0 : (cl > L ? L : cl);
-    if (c < cl) on = 1;
-    m = row_end;
+// Ordered compaction of the active tiles by one CTA of 1024 threads.
+template <typename Pred>
+__device__ __forceinline__ void compact_tiles(long tiles, int32_t* list, Pred active) {
+  __shared__ int warp_counts[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int base = 0;
+  for (long t0 = 0; t0 < tiles; t0 += blockDim.x) {
+    const long t = t0 + threadIdx.x;
+    const bool on = t < tiles && active(t);
+    const unsigned bal = __ballot_sync(0xffffffffu, on);
+    __syncthreads();
+    if (lane == 0) warp_counts[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0, sum = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+      if (w < warp) before += warp_counts[w];
+      sum += warp_counts[w];
+    }
+    if (on) list[1 + base + before + __popc(bal & ((1u << lane) - 1u))] = (int32_t)t;
+    base += sum;
   }
-  flags[t] = on;
+  if (threadIdx.x == 0) list[0] = base;
 }
 
-__global__ void slot_tile_flags_kernel(const uint8_t* __restrict__ valid, long T,
-                                       uint8_t* __restrict__ flags, long tiles) {
-  const long t = blockIdx.x * (long)blockDim.x + threadIdx.x;
-  if (t >= tiles) return;
-  uint8_t on = 0;
-  for (long r = t * kGemmTileM; r < min((t + 1) * kGemmTileM, T); ++r)
-    if (valid[r]) { on = 1; break; }
-  flags[t] = on;
+__global__ void __launch_bounds__(1024) ctx_tile_list_kernel(const int32_t* __restrict__ ctx_len,
+                                                             int B, int L, int32_t* list,
+                                                             long tiles) {
+  compact_tiles(tiles, list, [&](long t) {
+    const long m0 = t * kGemmTileM, m1 = min(m0 + kGemmTileM, (long)B * L);
+    for (long m = m0; m < m1;) {
+      const int b = (int)(m / L);
+      int cl = ctx_len[b];
+      cl = cl < 0 ? 0 : (cl > L ? L : cl);
+      if ((int)(m - (long)b * L) < cl) return true;
+      m = (long)(b + 1) * L;
+    }
+    return false;
+  });
+}
+
+__global__ void __launch_bounds__(1024) slot_tile_list_kernel(const uint8_t* __restrict__ valid,
+                                                              long T, int32_t* list, long tiles) {
+  compact_tiles(tiles, list, [&](long t) {
+    for (long r = t * kGemmTileM; r < min((t + 1) * kGemmTileM, T); ++r)
+      if (valid[r]) return true;
+    return false;
+  });
 }
 
 }  // namespace
 
-cudaError_t launch_ctx_tile_flags(const int32_t* ctx_len, int B, int L, uint8_t* flags,
-                                  cudaStream_t stream) {
+cudaError_t launch_ctx_tile_list(const int32_t* ctx_len, int B, int L, int32_t* list,
+                                 cudaStream_t stream) {
   const long tiles = ((long)B * L + kGemmTileM - 1) / kGemmTileM;
-  ctx_tile_flags_kernel<<<(unsigned)((tiles + 127) / 128), 128, 0, stream>>>(ctx_len, B, L, flags,
-                                                                           tiles);
+  ctx_tile_list_kernel<<<1, 1024, 0, stream>>>(ctx_len, B, L, list, tiles);
   return cudaGetLastError();
 }
 
-cudaError_t launch_slot_tile_flags(const uint8_t* valid, long T, uint8_t* flags,
-                                   cudaStream_t stream) {
+cudaError_t launch_slot_tile_list(const uint8_t* valid, long T, int32_t* list,
+                                  cudaStream_t stream) {
   const long tiles = (T + kGemmTileM - 1) / kGemmTileM;
-  slot_tile_flags_kernel<<<(unsigned)((tiles + 127) / 128), 128, 0, stream>>>(valid, T, flags, tiles);
+  slot_tile_list_kernel<<<1, 1024, 0, stream>>>(valid, T, list, tiles);
   return cudaGetLastError();
 }
 
