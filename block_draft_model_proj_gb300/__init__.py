@@ -22,13 +22,17 @@ DFLASH_ERR_UNSUPPORTED = 2
 DFLASH_ERR_CUDA = 3
 DFLASH_ERR_TIMEOUT = 4
 DFLASH_ERR_DEVICE_CHECK = 5
+DFLASH_ERR_RANGE = 6
 DFLASH_DTYPE_F32 = 0
 DFLASH_DTYPE_BF16 = 1
+DFLASH_DTYPE_F16 = 2
 DFLASH_FLAG_FINAL_NORM = 1
 DFLASH_FLAG_CTX_NORM = 2
+DFLASH_FLAG_F16_LAYERS = 4
 DFLASH_TESTING_ENGINE_TC = 0
 DFLASH_TESTING_ENGINE_SIMT = 1
-PROF_KINDS = {"gemm": 0, "attention": 1, "rows": 2, "plan": 3, "verify": 4}
+PROF_KINDS = {"gemm": 0, "attention": 1, "rows": 2, "plan": 3, "verify": 4, "convert": 5}
+LAYER_MATRICES = ("w_qkv", "w_o", "w_gate_up", "w_down")
 
 
 class dflash_config_t(ctypes.Structure):
@@ -62,6 +66,7 @@ _SIGS = {
     "dflash_last_error": (ctypes.c_char_p, []),
     "dflash_version": (_I, []),
     "dflash_device_status": (_I, [_I]),
+    "dflash_convert_bf16_to_f16": (_I, [_P, _P, _Z, _P]),
     "dflash_plan_workspace_size": (_Z, [_I, _I, _I, _I]),
     "dflash_plan": (_I, [_P, _P, _I, _I, ctypes.c_int64, ctypes.c_uint64, _I, _I, _P, _P, _P, _P,
                          _P, _P, _Z, _P]),
@@ -77,7 +82,7 @@ _SIGS = {
                                   _P]),
     "dflash_verify_greedy_static": (_I, [_P, _I, _P, _I, _I, _I, ctypes.c_int32, _P, _P, _P, _P,
                                          _P]),
-    "dflash_testing_gemm": (_I, [_I, _I, _P, _P, _L, _P, _L, _P, _L, _L, _I, _I, _I, _P]),
+    "dflash_testing_gemm": (_I, [_I, _I, _P, _L, _P, _L, _P, _L, _L, _I, _I, _I, _P]),
     "dflash_testing_gemm_splits": (_I, [_L, _I, _I]),
     "dflash_profile_enable": (_I, [_I]),
     "dflash_profile_read": (_I, [_I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_L)]),
@@ -135,8 +140,9 @@ def _stream(stream) -> int | None:
     return stream if isinstance(stream, int) else stream.cuda_stream
 
 
-def make_config(shape) -> dflash_config_t:
-    """dflash_config_t from any object with the DFlash shape fields (see dflash_inputs)."""
+def make_config(shape, f16_layers: bool = False) -> dflash_config_t:
+    """dflash_config_t from any object with the DFlash shape fields (see dflash_inputs);
+    f16_layers sets DFLASH_FLAG_F16_LAYERS (weights from prepare_f16_layers)."""
     return dflash_config_t(
         target_hidden=shape.target_hidden, num_target_layers=shape.num_target_layers,
         hidden=shape.hidden, num_layers=shape.num_layers, num_heads=shape.num_heads,
@@ -144,7 +150,8 @@ def make_config(shape) -> dflash_config_t:
         intermediate=shape.intermediate, block_size=shape.block_size,
         dtype=DFLASH_DTYPE_BF16 if shape.dtype == "bf16" else DFLASH_DTYPE_F32,
         flags=(DFLASH_FLAG_FINAL_NORM if shape.final_norm else 0) |
-              (DFLASH_FLAG_CTX_NORM if shape.ctx_norm else 0),
+              (DFLASH_FLAG_CTX_NORM if shape.ctx_norm else 0) |
+              (DFLASH_FLAG_F16_LAYERS if f16_layers else 0),
         reserved=0, rope_theta=float(shape.rope_theta), rms_eps=float(shape.rms_eps))
 
 
@@ -161,6 +168,30 @@ class Weights:
         self._layers = arr
         self.struct = dflash_weights_t(top["w_proj"].data_ptr(), top["g_ctx"].data_ptr(),
                                        top["g_final"].data_ptr(), arr, len(layers))
+
+
+def dflash_convert_bf16_to_f16(src, dst, stream=None) -> None:
+    if dst.numel() != src.numel():
+        raise ValueError("dst must have as many elements as src")
+    _check(load().dflash_convert_bf16_to_f16(_ptr(src), _ptr(dst), src.numel(), _stream(stream)))
+
+
+def prepare_f16_layers(weights: Weights, out: list | None = None, stream=None) -> Weights:
+    """Weights whose layer matrices are fp16 copies (dflash_convert_bf16_to_f16) of the bf16
+    ones, for a config made with f16_layers=True.  `out` (optional) is a list of per-layer
+    dicts of preallocated fp16 tensors to fill, reused across weight updates."""
+    import torch
+    top, layers = weights.tensors
+    new_layers = []
+    for i, lw in enumerate(layers):
+        nl = dict(lw)
+        for k in LAYER_MATRICES:
+            dst = out[i][k] if out is not None else torch.empty(lw[k].shape, dtype=torch.float16,
+                                                                 device=lw[k].device)
+            dflash_convert_bf16_to_f16(lw[k], dst, stream)
+            nl[k] = dst
+        new_layers.append(nl)
+    return Weights(top, new_layers)
 
 
 def workspace(nbytes: int, device="cuda"):
@@ -240,12 +271,11 @@ def dflash_device_status(reset: bool = True) -> None:
     _check(load().dflash_device_status(1 if reset else 0))
 
 
-def dflash_testing_gemm(engine, dtype, A, B, C, splits=1, A_lo=None, stream=None):
+def dflash_testing_gemm(engine, dtype, A, B, C, splits=1, stream=None):
     M, K = A.shape
     N = B.shape[0]
-    _check(load().dflash_testing_gemm(engine, dtype, _ptr(A), _ptr(A_lo), A.stride(0), _ptr(B),
-                                      B.stride(0), _ptr(C), C.stride(-2), M, N, K, splits,
-                                      _stream(stream)))
+    _check(load().dflash_testing_gemm(engine, dtype, _ptr(A), A.stride(0), _ptr(B), B.stride(0),
+                                      _ptr(C), C.stride(-2), M, N, K, splits, _stream(stream)))
 
 
 def dflash_profile_enable(on: bool = True) -> None:

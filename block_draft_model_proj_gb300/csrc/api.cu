@@ -160,6 +160,10 @@ int check_cfg(const dflash_config_t* c) {
   if (c->head_dim % 2 != 0) return fail(DFLASH_ERR_INVALID_ARG, "head_dim must be even");
   if (!(c->rope_theta > 0.0) || !(c->rms_eps >= 0.0))
     return fail(DFLASH_ERR_INVALID_ARG, "rope_theta must be > 0 and rms_eps >= 0");
+  if ((c->flags & ~(DFLASH_FLAG_FINAL_NORM | DFLASH_FLAG_CTX_NORM | DFLASH_FLAG_F16_LAYERS)) != 0)
+    return fail(DFLASH_ERR_INVALID_ARG, "unknown bits in cfg->flags");
+  if ((c->flags & DFLASH_FLAG_F16_LAYERS) && c->dtype != DFLASH_DTYPE_BF16)
+    return fail(DFLASH_ERR_INVALID_ARG, "DFLASH_FLAG_F16_LAYERS needs the bf16 configuration");
   if (c->dtype == DFLASH_DTYPE_BF16) {
     const long widths[] = {(long)c->target_hidden * c->num_target_layers, c->hidden,
                            (long)c->num_heads * c->head_dim, c->intermediate};
@@ -218,49 +222,51 @@ int check_ws(void* ws, size_t ws_bytes, size_t need) {
   return DFLASH_OK;
 }
 
-// C[z] = A * B^T (fp32 out): tcgen05 for bf16 (two-term A when A_lo is given), CUDA cores
-// for fp32.
-cudaError_t gemm(int dtype, const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
-                 float* C, long ldc, long M, int N, int K, int splits, cudaStream_t s,
+// C[z] = A * B^T (fp32 out): tcgen05 for 16-bit operands (elem bf16 or fp16), CUDA cores
+// for the fp32 configuration.
+cudaError_t gemm(int dtype, int elem, const void* A, long lda, const void* Bm, long ldb, float* C,
+                 long ldc, long M, int N, int K, int splits, cudaStream_t s,
                  const int32_t* tile_list = nullptr) {
   if (dtype == DFLASH_DTYPE_BF16)
-    return launch_gemm_tc(A, A_lo, lda, Bm, ldb, C, ldc, M, N, K, splits, tile_list,
+    return launch_gemm_tc(elem, A, lda, Bm, ldb, C, ldc, M, N, K, splits, tile_list,
                           status_ptr(), s);
   return launch_gemm_simt(dtype, A, lda, Bm, ldb, C, ldc, M, N, K, splits, s);
 }
 
-// A computed activation buffer: fp32, or the two-term bf16 pair.
+// A computed activation buffer: fp32 (fp32 configuration) or fp16 (bf16 configuration).
 struct Act {
-  void* hi = nullptr;
-  __nv_bfloat16* lo = nullptr;
+  void* p = nullptr;
   int dtype = DFLASH_DTYPE_F32;
   ActOut out() const {
     ActOut o;
-    o.hi = hi;
-    o.lo = lo;
+    o.p = p;
     o.dtype = dtype;
+    o.status = status_ptr();
     return o;
   }
 };
 
-Act take_act(struct Carver& cv, size_t n, int dtype);
-
-// ---- layouts shared by the size queries and the calls -----------------------------------
 Act take_act(Carver& cv, size_t n, int dtype) {
   Act a;
   a.dtype = dtype;
-  if (dtype == DFLASH_DTYPE_BF16) {
-    a.hi = cv.take<__nv_bfloat16>(n);
-    a.lo = cv.take<__nv_bfloat16>(n);
-  } else {
-    a.hi = cv.take<float>(n);
-  }
+  if (dtype == DFLASH_DTYPE_BF16)
+    a.p = cv.take<__half>(n);
+  else
+    a.p = cv.take<float>(n);
   return a;
+}
+
+// The draft layers' projection matrices as the layer GEMMs read them: the caller's (fp32
+// configuration, or fp16 given with DFLASH_FLAG_F16_LAYERS), or fp16 copies in the
+// workspace, converted at the start of the call that uses them.
+bool layers_need_copy(const dflash_config_t* c) {
+  return c->dtype == DFLASH_DTYPE_BF16 && (c->flags & DFLASH_FLAG_F16_LAYERS) == 0;
 }
 
 struct ProjLayout {
   float* y;
   Act ctx;
+  __half* wkv16;  // one layer's K/V rows of w_qkv as fp16 (when converted here)
   float* cos_t;
   float* sin_t;
   int32_t* tile_list;
@@ -283,6 +289,7 @@ ProjLayout proj_layout(const dflash_config_t* c, int B, int L, void* ws) {
   p.cos_t = cv.take<float>((size_t)L * (c->head_dim / 2));
   p.sin_t = cv.take<float>((size_t)L * (c->head_dim / 2));
   p.tile_list = cv.take<int32_t>(1 + (size_t)(M + kGemmTileM - 1) / kGemmTileM);
+  p.wkv16 = layers_need_copy(c) ? cv.take<__half>((size_t)kvw * D) : nullptr;
   p.bytes = cv.off;
   return p;
 }
@@ -297,6 +304,7 @@ struct BodyLayout {
   float* y;
   float* cos_t;
   float* sin_t;
+  __half* wl16;         // one layer's four matrices as fp16 (when converted here)
   int sp_qkv, sp_o, sp_gu, sp_down;
   int P;
   size_t bytes;
@@ -334,6 +342,9 @@ BodyLayout body_layout(const dflash_config_t* c, int B, int L, int N, void* ws) 
   b.P = L + c->block_size;
   b.cos_t = cv.take<float>((size_t)b.P * (c->head_dim / 2));
   b.sin_t = cv.take<float>((size_t)b.P * (c->head_dim / 2));
+  b.wl16 = layers_need_copy(c)
+               ? cv.take<__half>((size_t)qkvw * D + (size_t)D * qw + (size_t)2 * I * D + (size_t)D * I)
+               : nullptr;
   b.bytes = cv.off;
   return b;
 }
@@ -356,7 +367,17 @@ extern "C" {
 
 const char* dflash_last_error(void) { return g_msg; }
 
-int dflash_version(void) { return 100; }
+int dflash_version(void) { return 200; }
+
+int dflash_convert_bf16_to_f16(const void* src, void* dst, size_t n, void* stream) {
+  if (n == 0) return DFLASH_OK;
+  int r;
+  if ((r = check_ptr16(src, "src", DFLASH_DTYPE_BF16))) return r;
+  if ((r = check_ptr16(dst, "dst", DFLASH_DTYPE_F16))) return r;
+  Prof pr(DFLASH_PROF_CONVERT, 1, (cudaStream_t)stream);
+  DF_CUDA(launch_convert_bf16_f16(src, dst, n, status_ptr(), (cudaStream_t)stream));
+  return DFLASH_OK;
+}
 
 int dflash_device_status(int reset) {
   unsigned* p = status_ptr();
@@ -367,6 +388,9 @@ int dflash_device_status(int reset) {
   if (reset) DF_CUDA(cudaMemset(p, 0, sizeof(unsigned)));
   if (v & kStatusTimeout) return fail(DFLASH_ERR_TIMEOUT, "device wait timed out (kernel id %u)", (v >> 8) & 0xFF);
   if (v & kStatusCheck) return fail(DFLASH_ERR_DEVICE_CHECK, "device index check failed (kernel id %u)", (v >> 8) & 0xFF);
+  if (v & kStatusRange)
+    return fail(DFLASH_ERR_RANGE, "a value outside the fp16 range was stored as fp16 (kernel id %u)",
+                (v >> 8) & 0xFF);
   return DFLASH_OK;
 }
 
@@ -433,8 +457,8 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
   }
   {
     Prof pr(DFLASH_PROF_GEMM, 1, s);
-    DF_CUDA(gemm(cfg->dtype, target_hidden, nullptr, Kc, w->w_proj, Kc, lay.y, D, M, D, Kc,
-                 lay.split_proj, s, flags));
+    DF_CUDA(gemm(cfg->dtype, DFLASH_DTYPE_BF16, target_hidden, Kc, w->w_proj, Kc, lay.y, D, M, D,
+                 Kc, lay.split_proj, s, flags));
   }
   {
     Prof pr(DFLASH_PROF_ROWS, 1, s);
@@ -445,7 +469,12 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
   const size_t layer_elems = (size_t)B * 2 * Hkv * L_cache * dh;
   const bool to_tf32 = cfg->dtype == DFLASH_DTYPE_BF16;
   for (int l = 0; l < cfg->num_layers; ++l) {
-    const uint8_t* wkv = static_cast<const uint8_t*>(w->layers[l].w_qkv) + (size_t)qw * D * es;
+    const void* wkv = static_cast<const uint8_t*>(w->layers[l].w_qkv) + (size_t)qw * D * es;
+    if (lay.wkv16) {
+      Prof pr(DFLASH_PROF_CONVERT, 1, s);
+      DF_CUDA(launch_convert_bf16_f16(wkv, lay.wkv16, (size_t)kvw * D, status_ptr(), s));
+      wkv = lay.wkv16;
+    }
     float* kv_layer = static_cast<float*>(kv_cache) + (size_t)l * layer_elems;
     if (cfg->dtype == DFLASH_DTYPE_BF16) {
       // RoPE and the cache layout are applied in the GEMM epilogue
@@ -460,13 +489,13 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
       kv.Hkv = Hkv;
       kv.to_tf32 = 1;
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(launch_gemm_tc_kv_cache(lay.ctx.hi, lay.ctx.lo, D, wkv, D, M, kvw, D, flags, kv,
-                                      status_ptr(), s));
+      DF_CUDA(launch_gemm_tc_kv_cache(DFLASH_DTYPE_F16, lay.ctx.p, D, wkv, D, M, kvw, D, flags,
+                                      kv, status_ptr(), s));
       continue;
     }
     {
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(gemm(cfg->dtype, lay.ctx.hi, lay.ctx.lo, D, wkv, D, lay.y, kvw, M, kvw, D,
+      DF_CUDA(gemm(cfg->dtype, DFLASH_DTYPE_F16, lay.ctx.p, D, wkv, D, lay.y, kvw, M, kvw, D,
                    lay.split_kv, s, flags));
     }
     Prof pr(DFLASH_PROF_ROWS, 2, s);
@@ -524,12 +553,24 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
     DF_CUDA(launch_residual_norm(kNormInit, dt, lay.x, block_emb, nullptr, 0, w->layers[0].g_in,
                                  cfg->rms_eps, lay.h.out(), nullptr, nullptr, false, T, D, s));
   }
+  const int el = DFLASH_DTYPE_F16;  // layer GEMM operands in the bf16 configuration
   for (int l = 0; l < cfg->num_layers; ++l) {
-    const dflash_layer_weights_t& lw = w->layers[l];
+    dflash_layer_weights_t lw = w->layers[l];
+    if (lay.wl16) {
+      // fp16 copies of this layer's matrices (exact for bf16 values in the fp16 range)
+      __half* dst = lay.wl16;
+      const void** mats[4] = {&lw.w_qkv, &lw.w_o, &lw.w_gate_up, &lw.w_down};
+      const size_t sizes[4] = {(size_t)qkvw * D, (size_t)D * qw, (size_t)2 * I * D, (size_t)D * I};
+      Prof pr(DFLASH_PROF_CONVERT, 4, s);
+      for (int m = 0; m < 4; ++m) {
+        DF_CUDA(launch_convert_bf16_f16(*mats[m], dst, sizes[m], st, s));
+        *mats[m] = dst;
+        dst += sizes[m];
+      }
+    }
     {
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(gemm(dt, lay.h.hi, lay.h.lo, D, lw.w_qkv, D, lay.y, qkvw, T, qkvw, D, lay.sp_qkv, s,
-                   flags));
+      DF_CUDA(gemm(dt, el, lay.h.p, D, lw.w_qkv, D, lay.y, qkvw, T, qkvw, D, lay.sp_qkv, s, flags));
     }
     {
       Prof pr(DFLASH_PROF_ROWS, 1, s);
@@ -584,8 +625,7 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
     }
     {
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(gemm(dt, lay.attn.hi, lay.attn.lo, qw, lw.w_o, qw, lay.y, D, T, D, qw, lay.sp_o, s,
-                   flags));
+      DF_CUDA(gemm(dt, el, lay.attn.p, qw, lw.w_o, qw, lay.y, D, T, D, qw, lay.sp_o, s, flags));
     }
     {
       Prof pr(DFLASH_PROF_ROWS, 1, s);
@@ -595,21 +635,20 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
     if (dt == DFLASH_DTYPE_BF16 && lay.sp_gu == 1) {
       // SiLU(gate) * up is formed in the GEMM epilogue
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(launch_gemm_tc_swiglu(lay.h.hi, lay.h.lo, D, lw.w_gate_up, D, T, I, D, flags,
+      DF_CUDA(launch_gemm_tc_swiglu(el, lay.h.p, D, lw.w_gate_up, D, T, I, D, flags,
                                     lay.act.out(), st, s));
     } else {
       {
         Prof pr(DFLASH_PROF_GEMM, 1, s);
-        DF_CUDA(gemm(dt, lay.h.hi, lay.h.lo, D, lw.w_gate_up, D, lay.y, 2 * I, T, 2 * I, D,
-                     lay.sp_gu, s, flags));
+        DF_CUDA(gemm(dt, el, lay.h.p, D, lw.w_gate_up, D, lay.y, 2 * I, T, 2 * I, D, lay.sp_gu, s,
+                     flags));
       }
       Prof pr(DFLASH_PROF_ROWS, 1, s);
       DF_CUDA(launch_swiglu(lay.y, lay.sp_gu, lay.act.out(), T, I, s));
     }
     {
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(gemm(dt, lay.act.hi, lay.act.lo, I, lw.w_down, I, lay.y, D, T, D, I, lay.sp_down, s,
-                   flags));
+      DF_CUDA(gemm(dt, el, lay.act.p, I, lw.w_down, I, lay.y, D, T, D, I, lay.sp_down, s, flags));
     }
     Prof pr(DFLASH_PROF_ROWS, 1, s);
     if (l + 1 < cfg->num_layers) {
@@ -656,18 +695,18 @@ int dflash_verify_greedy(const void* logits, int logits_dtype, const int32_t* dr
 }
 
 // ---- testing hooks -----------------------------------------------------------------------
-int dflash_testing_gemm(int engine, int dtype, const void* A, const void* A_lo, long lda,
-                        const void* Bm, long ldb, float* C, long ldc, long M, int N, int K,
-                        int splits, void* stream) {
+int dflash_testing_gemm(int engine, int dtype, const void* A, long lda, const void* Bm, long ldb,
+                        float* C, long ldc, long M, int N, int K, int splits, void* stream) {
   if (M < 1 || N < 1 || K < 1 || !A || !Bm || !C) return fail(DFLASH_ERR_INVALID_ARG, "bad gemm args");
   cudaStream_t s = (cudaStream_t)stream;
   if (engine == DFLASH_TESTING_ENGINE_TC) {
-    if (dtype != DFLASH_DTYPE_BF16 || !gemm_tc_supported(M, N, K, lda, ldb))
-      return fail(DFLASH_ERR_UNSUPPORTED, "tensor-core GEMM needs bf16 and 16-byte rows");
-    DF_CUDA(launch_gemm_tc(A, A_lo, lda, Bm, ldb, C, ldc, M, N, K, splits, nullptr, status_ptr(),
-                           s));
+    if ((dtype != DFLASH_DTYPE_BF16 && dtype != DFLASH_DTYPE_F16) ||
+        !gemm_tc_supported(M, N, K, lda, ldb))
+      return fail(DFLASH_ERR_UNSUPPORTED, "tensor-core GEMM needs bf16 or fp16 and 16-byte rows");
+    DF_CUDA(launch_gemm_tc(dtype, A, lda, Bm, ldb, C, ldc, M, N, K, splits, nullptr,
+                           status_ptr(), s));
   } else {
-    if (A_lo) return fail(DFLASH_ERR_UNSUPPORTED, "the CUDA-core GEMM takes a single-term A");
+    if (dtype == DFLASH_DTYPE_F16) return fail(DFLASH_ERR_UNSUPPORTED, "CUDA-core GEMM: bf16 or fp32");
     DF_CUDA(launch_gemm_simt(dtype, A, lda, Bm, ldb, C, ldc, M, N, K, splits, s));
   }
   return DFLASH_OK;

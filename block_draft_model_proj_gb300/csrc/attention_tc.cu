@@ -20,7 +20,7 @@
 // cut into chunks of `chunk` keys so long prefixes spread over many SMs; chunk 0 also takes
 // the tile's own-block keys.  Each unit writes an unnormalised partial (m, l, O) per row;
 // attn_combine_kernel merges the chunks of a tile in chunk order (deterministic) and writes
-// the two-term bf16 attention output for the O projection.
+// the attention output (fp16) for the O projection.
 //
 // Arithmetic: kind::tf32 MMAs with fp32 accumulation.  Q, the block K/V and the context K/V
 // cache are fp32 values rounded to tf32, P is rounded to tf32; the softmax runs in fp32 in
@@ -494,7 +494,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
 }
 
 // One warp per query row of a tile: merge the chunk partials in chunk order, normalise,
-// write the two-term attention output row [t][(g*grp + h)*dh ...].
+// write the attention output row [t][(g*grp + h)*dh ...].
 __global__ void attn_combine_kernel(const AttnTcParams p, ActOut out, int Hq) {
   const int warps = blockDim.x >> 5;
   const long gw = (long)blockIdx.x * warps + (threadIdx.x >> 5);

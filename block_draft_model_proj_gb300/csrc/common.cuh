@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -16,10 +17,11 @@ namespace dflash {
 enum : unsigned {
   kStatusTimeout = 1u,
   kStatusCheck = 2u,
+  kStatusRange = 4u,  // a value outside the fp16 range met an fp16 store
 };
 enum : unsigned {
   kKernPlan = 1, kKernVerify = 2, kKernGemmTc = 3, kKernAttn = 4, kKernEpilogue = 5,
-  kKernNorm = 6, kKernAttnTc = 7,
+  kKernNorm = 6, kKernAttnTc = 7, kKernActivation = 8, kKernConvert = 9,
 };
 
 __device__ __forceinline__ void report(unsigned* status, unsigned bit, unsigned kernel_id) {
@@ -43,39 +45,40 @@ template <> struct Elem<__nv_bfloat16> {
 template <typename T> __device__ __forceinline__ float to_f(T v) { return Elem<T>::to_f(v); }
 template <typename T> __device__ __forceinline__ T from_f(float v) { return Elem<T>::from_f(v); }
 
-// Destination of a computed activation that feeds a projection GEMM.  fp32 configuration:
-// one fp32 array.  bf16 configuration: the two-term pair hi = bf16(v), lo = bf16(v - hi),
-// which keeps v to about 2^-17 relative for the tensor-core GEMM's two-term path.
+// Destination of a computed activation that feeds a projection GEMM: one fp32 array in the
+// fp32 configuration; one IEEE fp16 array in the bf16 configuration, where the draft layers'
+// projections run fp16 x fp16 on the tensor cores.  fp16 keeps 11 significant bits (8 times
+// finer than bf16); a value outside its finite range is stored as +-inf / NaN and reported
+// through the status word (kStatusRange).
 struct ActOut {
-  void* hi = nullptr;
-  __nv_bfloat16* lo = nullptr;
+  void* p = nullptr;
   int dtype = DFLASH_DTYPE_F32;
+  unsigned* status = nullptr;
+  __device__ __forceinline__ void range_check(float v) const {
+    if (!(fabsf(v) < 65520.f)) report(status, kStatusRange, kKernActivation);
+  }
   __device__ __forceinline__ void store(long i, float v) const {
     if (dtype == DFLASH_DTYPE_BF16) {
-      const __nv_bfloat16 h = __float2bfloat16_rn(v);
-      static_cast<__nv_bfloat16*>(hi)[i] = h;
-      lo[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+      range_check(v);
+      static_cast<__half*>(p)[i] = __float2half_rn(v);
     } else {
-      static_cast<float*>(hi)[i] = v;
+      static_cast<float*>(p)[i] = v;
     }
   }
   // four consecutive elements starting at i (i a multiple of 4)
   __device__ __forceinline__ void store4(long i, float4 v) const {
     if (dtype == DFLASH_DTYPE_BF16) {
-      const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
-      const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
-      const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-      const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
-      const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
-      uint2 hw, lw;
-      hw.x = *reinterpret_cast<const uint32_t*>(&h01);
-      hw.y = *reinterpret_cast<const uint32_t*>(&h23);
-      lw.x = *reinterpret_cast<const uint32_t*>(&l01);
-      lw.y = *reinterpret_cast<const uint32_t*>(&l23);
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(hi) + i) = hw;
-      *reinterpret_cast<uint2*>(lo + i) = lw;
+      // fmaxf drops NaN operands; the product term is NaN when an element is NaN or inf
+      range_check(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))) +
+                  0.f * (v.x + v.y + v.z + v.w));
+      const __half2 h01 = __floats2half2_rn(v.x, v.y);
+      const __half2 h23 = __floats2half2_rn(v.z, v.w);
+      uint2 w;
+      w.x = *reinterpret_cast<const uint32_t*>(&h01);
+      w.y = *reinterpret_cast<const uint32_t*>(&h23);
+      *reinterpret_cast<uint2*>(static_cast<__half*>(p) + i) = w;
     } else {
-      *reinterpret_cast<float4*>(static_cast<float*>(hi) + i) = v;
+      *reinterpret_cast<float4*>(static_cast<float*>(p) + i) = v;
     }
   }
 };

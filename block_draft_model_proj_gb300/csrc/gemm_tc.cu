@@ -1,22 +1,18 @@
-// bf16 GEMM on the 5th-generation tensor cores: C[z] (fp32) = A[:, Kz] * B[:, Kz]^T.
+// 16-bit GEMM on the 5th-generation tensor cores: C[z] (fp32) = A[:, Kz] * B[:, Kz]^T.
 //
-// A [M, K] and B [N, K] are row-major bf16 (both K-major), C is fp32 row-major.  This is
-// the contraction behind every projection of the draft body: W_proj ("DFlash", How it
-// works: target hidden states projected into the K/V space), the context K/V projections,
-// and the per-layer QKV / O / gate-up / down projections.
-//
-// Two-term activations: a computed activation (a norm output, the attention output, the
-// SwiGLU product) is carried as a pair of bf16 arrays A = A_hi + A_lo (A_hi = bf16(a),
-// A_lo = bf16(a - A_hi)), which holds a to about 2^-17 relative.  The kernel then issues
-// two MMAs per K step against the same weight tile, C += A_hi W^T + A_lo W^T, so the
-// product is as accurate as an fp32 GEMM of bf16 weights.  Exact bf16 inputs (the target
-// hidden states) take the single-term path.
+// A [M, K] and B [N, K] are row-major (both K-major), both bf16 or both fp16; C is fp32
+// row-major.  This is the contraction behind every projection of the draft body: W_proj
+// ("DFlash", How it works: target hidden states projected into the K/V space) runs bf16 x
+// bf16 on the target's exact bf16 hidden states; the context K/V projections and the
+// per-layer QKV / O / gate-up / down projections run fp16 x fp16, on fp16 copies of the
+// layer weights and on activations (norm outputs, the attention output, the SwiGLU
+// product) rounded to fp16, whose 11 significant bits keep the body within its stated
+// error bound where bf16 activations (8 bits) do not.
 //
 // Design (sm_103a):
 //  * persistent CTAs (one per SM), 128 x 256 output tile, K stepped 64 at a time;
-//  * warp 0 = TMA producer: cp.async.bulk.tensor loads of 128x64 A (and A_lo) and
-//    2x(128x64) B boxes, 128-byte swizzle, into a shared-memory ring (4 stages, 3 with
-//    the two-term A) guarded by mbarriers;
+//  * warp 0 = TMA producer: cp.async.bulk.tensor loads of a 128x64 A box and two 128x64
+//    B boxes, 128-byte swizzle, into a 4-stage shared-memory ring guarded by mbarriers;
 //  * warp 1 = MMA issuer: one thread issues tcgen05.mma.cta_group::1.kind::f16 (M=128,
 //    N=256, K=16) with fp32 accumulation in tensor memory; tcgen05.commit frees a stage;
 //  * warps 2-5 = epilogue: tcgen05.ld of the accumulator (each warp owns its 32-lane
@@ -47,28 +43,27 @@ constexpr uint32_t kTileABytes = kBM * kBK * 2;    // 16 KB
 constexpr uint32_t kStageBBytes = kBN * kBK * 2;   // 32 KB
 constexpr uint32_t kStagingFloats = 32 * 33;       // per epilogue warp
 
-template <bool kSplit>
-struct Cfg {
-  static constexpr int kStages = kSplit ? 3 : 4;
-  static constexpr uint32_t kStageABytes = (kSplit ? 2 : 1) * kTileABytes;
-  static constexpr uint32_t kTxBytes = kStageABytes + kStageBBytes;
-  static constexpr size_t kSmemBytes = 1024 + kStages * (size_t)(kStageABytes + kStageBBytes) +
-                                       4 * kStagingFloats * sizeof(float) + 256;
-};
+constexpr int kStages = 4;
+constexpr uint32_t kStageABytes = kTileABytes;
+constexpr uint32_t kTxBytes = kStageABytes + kStageBBytes;
+constexpr size_t kSmemBytes = 1024 + kStages * (size_t)(kStageABytes + kStageBBytes) +
+                              4 * kStagingFloats * sizeof(float) + 256;
 
-// Instruction descriptor, kind::f16: D = fp32 (bits 4-5 = 1), A = bf16 (bits 7-9 = 1),
-// B = bf16 (bits 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
+// Instruction descriptor, kind::f16: D = fp32 (bits 4-5 = 1), A and B format at bits 7-9
+// and 10-12 (0 = fp16, 1 = bf16), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
 // M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                            ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+constexpr uint32_t idesc_16bit(bool bf16) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
 
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t accumulate) {
+__device__ __forceinline__ void umma_16bit(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -82,9 +77,10 @@ struct TcParams {
   long ldc;
   const int32_t* tile_list;    // optional: [0] = count, [1..] = active M tiles in order
   int m_fastest;               // tile order: M tiles fastest (shares each B tile) or N fastest
+  uint32_t idesc;              // instruction descriptor: bf16 or fp16 operands
   unsigned* status;
   KvCacheEpilogue kv;          // used by the kEpiKvCache epilogue only
-  ActOut act;                  // kEpiSwiGLU: two-term SiLU(gate) * up, [M][swiglu_I]
+  ActOut act;                  // kEpiSwiGLU: SiLU(gate) * up, [M][swiglu_I]
   int swiglu_I;                // kEpiSwiGLU: B rows [0, I) gate, [I, 2I) up
 };
 
@@ -181,7 +177,7 @@ __device__ __forceinline__ void kv_cache_epilogue(const TcParams& p, uint32_t tb
 }
 
 // SwiGLU epilogue: accumulator columns [0, 128) are the gate and [128, 256) the up
-// projections of channels n_t*128 .. +127; writes act = SiLU(gate) * up as a two-term pair.
+// projections of channels n_t*128 .. +127; writes act = SiLU(gate) * up.
 __device__ __forceinline__ void swiglu_epilogue(const TcParams& p, uint32_t tbase, int m_t, int n_t,
                                                 int quarter, int lane) {
   const long m = (long)m_t * kBM + quarter * 32 + lane;
@@ -213,12 +209,10 @@ __device__ __forceinline__ void swiglu_epilogue(const TcParams& p, uint32_t tbas
   }
 }
 
-template <bool kSplit, int kEpi>
+template <int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_alo,
-               const __grid_constant__ CUtensorMap map_b, const TcParams p) {
-  constexpr int kStages = Cfg<kSplit>::kStages;
-  constexpr uint32_t kStageABytes = Cfg<kSplit>::kStageABytes;
+gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+               const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -248,8 +242,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
-    if (kSplit)
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_alo)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
   }
   if (warp == 1) {
@@ -283,11 +275,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[stage], Cfg<kSplit>::kTxBytes);
+          mbar_arrive_expect_tx(&full[stage], kTxBytes);
           uint8_t* a_dst = sA + stage * kStageABytes;
           uint8_t* b_dst = sB + stage * kStageBBytes;
           tma_load_2d(&map_a, &full[stage], a_dst, kb * kBK, m_t * kBM);
-          if (kSplit) tma_load_2d(&map_alo, &full[stage], a_dst + kTileABytes, kb * kBK, m_t * kBM);
           // the two 128-row halves of the B tile: consecutive rows, or (SwiGLU) the gate
           // rows of 128 channels and the up rows of the same channels
           const int brow0 = kEpi == kEpiSwiGLU ? n_t * 128 : n_t * kBN;
@@ -327,9 +318,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             // advancing K by 16 bf16 = 32 bytes inside the 128-byte swizzle atom
-            const uint64_t bdesc = sw128_desc(b_addr + k * 32);
-            umma_bf16(d_tmem, sw128_desc(a_addr + k * 32), bdesc, (kb > kb0 || k > 0) ? 1u : 0u);
-            if (kSplit) umma_bf16(d_tmem, sw128_desc(a_addr + kTileABytes + k * 32), bdesc, 1u);
+            umma_16bit(d_tmem, sw128_desc(a_addr + k * 32), sw128_desc(b_addr + k * 32), p.idesc,
+                       (kb > kb0 || k > 0) ? 1u : 0u);
           }
           umma_commit(&empty[stage]);
           if (++stage == kStages) { stage = 0; ph ^= 1u; }
@@ -420,17 +410,19 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2-D bf16 map over a [rows, cols] row-major matrix with row stride ld (elements),
-// box = box_rows x 64 columns, 128-byte swizzle, zero fill out of bounds.
+// 2-D map of 16-bit elements (bf16 or fp16) over a [rows, cols] row-major matrix with row
+// stride ld (elements), box = box_rows x 64 columns, 128-byte swizzle, zero fill out of
+// bounds.
 bool encode_kmajor(CUtensorMap* map, const void* base, long rows, int cols, long ld,
-                   int box_rows) {
+                   int box_rows, bool bf16) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
   cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -451,31 +443,31 @@ bool gemm_tc_supported(long M, int N, int K, long lda, long ldb) {
 
 namespace {
 
-template <bool kSplit, int kEpi>
-cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& malo, const CUtensorMap& mb,
-                           const TcParams& p, int grid, cudaStream_t stream) {
+template <int kEpi>
+cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p,
+                           int grid, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<kSplit, kEpi>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<kEpi>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Cfg<kSplit>::kSmemBytes);
+                                         (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_tc_kernel<kSplit, kEpi><<<grid, kThreads, Cfg<kSplit>::kSmemBytes, stream>>>(ma, malo, mb, p);
+  gemm_tc_kernel<kEpi><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_common(const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
-                          float* C, long ldc, long M, int N, int K, int splits,
-                          const int32_t* tile_list, unsigned* status, int epi,
-                          const KvCacheEpilogue* kv, const ActOut* act, cudaStream_t stream) {
-  if (((uintptr_t)A | (uintptr_t)A_lo | (uintptr_t)Bm) % 16 != 0) return cudaErrorInvalidValue;
-  CUtensorMap ma, malo, mb;
-  if (!encode_kmajor(&ma, A, M, K, lda, kBM)) return cudaErrorInvalidValue;
-  if (A_lo && !encode_kmajor(&malo, A_lo, M, K, lda, kBM)) return cudaErrorInvalidValue;
-  if (!A_lo) malo = ma;
-  if (!encode_kmajor(&mb, Bm, N, K, ldb, 128)) return cudaErrorInvalidValue;
+cudaError_t launch_common(int elem, const void* A, long lda, const void* Bm, long ldb, float* C,
+                          long ldc, long M, int N, int K, int splits, const int32_t* tile_list,
+                          unsigned* status, int epi, const KvCacheEpilogue* kv, const ActOut* act,
+                          cudaStream_t stream) {
+  if (elem != DFLASH_DTYPE_BF16 && elem != DFLASH_DTYPE_F16) return cudaErrorInvalidValue;
+  if (((uintptr_t)A | (uintptr_t)Bm) % 16 != 0) return cudaErrorInvalidValue;
+  const bool bf16 = elem == DFLASH_DTYPE_BF16;
+  CUtensorMap ma, mb;
+  if (!encode_kmajor(&ma, A, M, K, lda, kBM, bf16)) return cudaErrorInvalidValue;
+  if (!encode_kmajor(&mb, Bm, N, K, ldb, 128, bf16)) return cudaErrorInvalidValue;
   TcParams p;
   p.M = M;
   p.N = N;
@@ -498,47 +490,42 @@ cudaError_t launch_common(const void* A, const void* A_lo, long lda, const void*
   p.tile_list = tile_list;
   // M tiles fastest when A is the smaller operand: the CTAs that share a B tile then run
   // in the same wave and read it once
-  const double a_bytes = (double)M * K * 2 * (A_lo ? 2 : 1), b_bytes = (double)N * K * 2;
-  p.m_fastest = a_bytes <= b_bytes ? 1 : 0;
+  p.m_fastest = (double)M <= (double)N ? 1 : 0;
+  p.idesc = idesc_16bit(bf16);
   p.status = status;
   if (kv) p.kv = *kv;
   const long tiles = (long)p.m_tiles * p.n_tiles * p.splits;
   const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-  if (epi == kEpiKvCache)
-    return A_lo ? launch_variant<true, kEpiKvCache>(ma, malo, mb, p, grid, stream)
-                : launch_variant<false, kEpiKvCache>(ma, malo, mb, p, grid, stream);
-  if (epi == kEpiSwiGLU)
-    return A_lo ? launch_variant<true, kEpiSwiGLU>(ma, malo, mb, p, grid, stream)
-                : launch_variant<false, kEpiSwiGLU>(ma, malo, mb, p, grid, stream);
-  return A_lo ? launch_variant<true, kEpiStoreF32>(ma, malo, mb, p, grid, stream)
-              : launch_variant<false, kEpiStoreF32>(ma, malo, mb, p, grid, stream);
+  if (epi == kEpiKvCache) return launch_variant<kEpiKvCache>(ma, mb, p, grid, stream);
+  if (epi == kEpiSwiGLU) return launch_variant<kEpiSwiGLU>(ma, mb, p, grid, stream);
+  return launch_variant<kEpiStoreF32>(ma, mb, p, grid, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_tc(const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
-                           float* C, long ldc, long M, int N, int K, int splits,
-                           const int32_t* tile_list, unsigned* status, cudaStream_t stream) {
-  return launch_common(A, A_lo, lda, Bm, ldb, C, ldc, M, N, K, splits, tile_list, status,
+cudaError_t launch_gemm_tc(int elem, const void* A, long lda, const void* Bm, long ldb, float* C,
+                           long ldc, long M, int N, int K, int splits, const int32_t* tile_list,
+                           unsigned* status, cudaStream_t stream) {
+  return launch_common(elem, A, lda, Bm, ldb, C, ldc, M, N, K, splits, tile_list, status,
                        kEpiStoreF32, nullptr, nullptr, stream);
 }
 
-cudaError_t launch_gemm_tc_swiglu(const void* A, const void* A_lo, long lda, const void* Bm,
-                                  long ldb, long M, int I, int K, const int32_t* tile_list,
+cudaError_t launch_gemm_tc_swiglu(int elem, const void* A, long lda, const void* Bm, long ldb,
+                                  long M, int I, int K, const int32_t* tile_list,
                                   const ActOut& act, unsigned* status, cudaStream_t stream) {
   if (I < 1) return cudaErrorInvalidValue;
-  return launch_common(A, A_lo, lda, Bm, ldb, nullptr, 0, M, 2 * I, K, 1, tile_list, status,
+  return launch_common(elem, A, lda, Bm, ldb, nullptr, 0, M, 2 * I, K, 1, tile_list, status,
                        kEpiSwiGLU, nullptr, &act, stream);
 }
 
-cudaError_t launch_gemm_tc_kv_cache(const void* A, const void* A_lo, long lda, const void* Bm,
-                                    long ldb, long M, int N, int K, const int32_t* tile_list,
+cudaError_t launch_gemm_tc_kv_cache(int elem, const void* A, long lda, const void* Bm, long ldb,
+                                    long M, int N, int K, const int32_t* tile_list,
                                     const KvCacheEpilogue& kv, unsigned* status,
                                     cudaStream_t stream) {
   if (N != 2 * kv.Hkv * 128 || kv.L < 1) return cudaErrorInvalidValue;
   if (((uintptr_t)kv.kv | (uintptr_t)kv.cos_t | (uintptr_t)kv.sin_t) % 16 != 0)
     return cudaErrorInvalidValue;
-  return launch_common(A, A_lo, lda, Bm, ldb, nullptr, 0, M, N, K, 1, tile_list, status,
+  return launch_common(elem, A, lda, Bm, ldb, nullptr, 0, M, N, K, 1, tile_list, status,
                        kEpiKvCache, &kv, nullptr, stream);
 }
 

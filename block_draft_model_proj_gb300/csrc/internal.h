@@ -81,8 +81,8 @@ cudaError_t launch_gemm_simt(int dtype, const void* A, long lda, const void* Bm,
                              float* C, long ldc, long M, int N, int K, int splits,
                              cudaStream_t stream);
 
-// ---- gemm_tc.cu: tcgen05 bf16 GEMM, fp32 output, optional K-split ----
-// A_lo != nullptr selects the two-term activation path C = (A + A_lo) B^T.
+// ---- gemm_tc.cu: tcgen05 16-bit GEMM, fp32 output, optional K-split ----
+// elem = DFLASH_DTYPE_BF16 (A and B bf16) or DFLASH_DTYPE_F16 (A and B fp16).
 // tile_list (optional, device): [0] = count, [1..] = the 128-row M tiles to compute, in
 // order; tiles not listed are skipped entirely (their C rows are left unwritten).
 constexpr int kGemmTileM = 128;
@@ -98,19 +98,25 @@ struct KvCacheEpilogue {
   int L = 0, pos_offset = 0, L_cache = 0, Hkv = 0;
   int to_tf32 = 0;
 };
-// act = SiLU(gate) * up with [gate | up] = (A + A_lo) W_gate_up^T (W_gate_up [2I][K]: gate
-// rows then up rows), written as a two-term activation by the epilogue (no K-split).
-cudaError_t launch_gemm_tc_swiglu(const void* A, const void* A_lo, long lda, const void* Bm,
-                                  long ldb, long M, int I, int K, const int32_t* tile_list,
+// act = SiLU(gate) * up with [gate | up] = A W_gate_up^T (W_gate_up [2I][K]: gate rows then
+// up rows), written by the epilogue (no K-split).
+cudaError_t launch_gemm_tc_swiglu(int elem, const void* A, long lda, const void* Bm, long ldb,
+                                  long M, int I, int K, const int32_t* tile_list,
                                   const ActOut& act, unsigned* status, cudaStream_t stream);
-// C = (A + A_lo) B^T with N = 2*Hkv*128, written to the cache by the epilogue (no K-split).
-cudaError_t launch_gemm_tc_kv_cache(const void* A, const void* A_lo, long lda, const void* Bm,
-                                    long ldb, long M, int N, int K, const int32_t* tile_list,
+// C = A B^T with N = 2*Hkv*128, written to the cache by the epilogue (no K-split).
+cudaError_t launch_gemm_tc_kv_cache(int elem, const void* A, long lda, const void* Bm, long ldb,
+                                    long M, int N, int K, const int32_t* tile_list,
                                     const KvCacheEpilogue& kv, unsigned* status,
                                     cudaStream_t stream);
-cudaError_t launch_gemm_tc(const void* A, const void* A_lo, long lda, const void* Bm, long ldb,
-                           float* C, long ldc, long M, int N, int K, int splits,
-                           const int32_t* tile_list, unsigned* status, cudaStream_t stream);
+cudaError_t launch_gemm_tc(int elem, const void* A, long lda, const void* Bm, long ldb, float* C,
+                           long ldc, long M, int N, int K, int splits, const int32_t* tile_list,
+                           unsigned* status, cudaStream_t stream);
+
+// ---- rows.cu: bf16 -> fp16 conversion (weights) ----
+// dst[i] = fp16(src[i]), round to nearest even; exact for bf16 values of magnitude in
+// [2^-14, 65504] and zero.  Non-finite results report kStatusRange.  16-byte aligned.
+cudaError_t launch_convert_bf16_f16(const void* src, void* dst, size_t n, unsigned* status,
+                                    cudaStream_t stream);
 
 // ---- rows.cu: compacted lists of active 128-row M tiles for the GEMMs ----
 // list[0] = count, list[1..] = tile indices in increasing order; list holds 1 + tiles ints.

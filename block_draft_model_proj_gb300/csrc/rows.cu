@@ -8,13 +8,13 @@
 // channel i + dh/2.
 //
 // Computed activations that feed a projection GEMM are written through ActOut: fp32 for
-// the fp32 configuration, else the two-term bf16 pair (hi, lo) the tensor-core GEMM
-// consumes.  Attention operands (q, block k / v) are kept in fp32.
+// the fp32 configuration, else fp16 for the tensor-core GEMM.  Attention operands (q, block
+// k / v) are kept in fp32.
 #include <math.h>
 
-#include "common.cuh"
 #include <algorithm>
 
+#include "common.cuh"
 #include "internal.h"
 
 namespace dflash {
@@ -456,6 +456,40 @@ cudaError_t launch_ctx_kv_scatter(const float* y, int nsplit, const float* cos_t
 
 namespace {
 
+// bf16 -> fp16, eight elements (16 bytes) per thread and iteration.  A bf16 value is the
+// upper half of an fp32 value; cvt.rn.f16x2.f32 rounds two of them to nearest even.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& bad) {
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
+  const float m = fmaxf(fabsf(lo), fabsf(hi)) + 0.f * (lo + hi);  // NaN if either is
+  bad = bad || !(m < 65520.f);
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__global__ void convert_bf16_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                        long n8, const uint16_t* __restrict__ src_tail,
+                                        uint16_t* __restrict__ dst_tail, int tail,
+                                        unsigned* status) {
+  bool bad = false;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n8;
+       i += (long)gridDim.x * blockDim.x) {
+    const uint4 w = __ldcs(src + i);
+    uint4 o;
+    o.x = bf16x2_to_f16x2(w.x, bad);
+    o.y = bf16x2_to_f16x2(w.y, bad);
+    o.z = bf16x2_to_f16x2(w.z, bad);
+    o.w = bf16x2_to_f16x2(w.w, bad);
+    dst[i] = o;
+  }
+  if (blockIdx.x == 0 && threadIdx.x < tail) {
+    const float v = __uint_as_float((uint32_t)src_tail[threadIdx.x] << 16);
+    bad = bad || !(fabsf(v) < 65520.f);
+    const __half h = __float2half_rn(v);
+    dst_tail[threadIdx.x] = *reinterpret_cast<const uint16_t*>(&h);
+  }
+  if (bad) report(status, kStatusRange, kKernConvert);
+}
+
 // Ordered compaction of the active tiles by one CTA of 1024 threads.
 template <typename Pred>
 __device__ __forceinline__ void compact_tiles(long tiles, int32_t* list, Pred active) {
@@ -518,6 +552,26 @@ cudaError_t launch_slot_tile_list(const uint8_t* valid, long T, int32_t* list,
                                   cudaStream_t stream) {
   const long tiles = (T + kGemmTileM - 1) / kGemmTileM;
   slot_tile_list_kernel<<<1, 1024, 0, stream>>>(valid, T, list, tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert_bf16_f16(const void* src, void* dst, size_t n, unsigned* status,
+                                    cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  if (((uintptr_t)src | (uintptr_t)dst) % 16 != 0) return cudaErrorInvalidValue;
+  const long n8 = (long)(n / 8);
+  const int tail = (int)(n % 8);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long blocks = (n8 + 255) / 256;
+  const long cap = (long)(sms > 0 ? sms : 1) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  convert_bf16_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+      static_cast<const uint4*>(src), static_cast<uint4*>(dst), n8,
+      static_cast<const uint16_t*>(src) + n8 * 8, static_cast<uint16_t*>(dst) + n8 * 8, tail,
+      status);
   return cudaGetLastError();
 }
 

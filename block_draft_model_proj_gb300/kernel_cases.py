@@ -1,7 +1,7 @@
 """Single-kernel cases on synthetic inputs, for profiling one kernel at a time (ncu).
 
     python -m block_draft_model_proj_gb300.kernel_cases gemm --m 8192 --n 4096 --k 20480
-    python -m block_draft_model_proj_gb300.kernel_cases gemm --m 512 --n 24576 --k 4096 --two-term
+    python -m block_draft_model_proj_gb300.kernel_cases gemm --m 512 --n 24576 --k 4096 --f16
     python -m block_draft_model_proj_gb300.kernel_cases body --workload train_8b_b4_l2048
     python -m block_draft_model_proj_gb300.kernel_cases verify --workload decode_8b_b64_ctx4096
 
@@ -38,21 +38,20 @@ def case_gemm(args):
     import torch
     import block_draft_model_proj_gb300 as dflash
     g = torch.Generator(device="cuda").manual_seed(0)
-    A = torch.randn((args.m, args.k), generator=g, device="cuda").to(torch.bfloat16)
-    Alo = (torch.randn((args.m, args.k), generator=g, device="cuda") * 1e-3).to(torch.bfloat16) \
-        if args.two_term else None
-    B = (torch.randn((args.n, args.k), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    tdt = torch.float16 if args.f16 else torch.bfloat16
+    A = torch.randn((args.m, args.k), generator=g, device="cuda").to(tdt)
+    B = (torch.randn((args.n, args.k), generator=g, device="cuda") * 0.02).to(tdt)
     C = torch.empty((args.splits, args.m, args.n), dtype=torch.float32, device="cuda")
+    dt = dflash.DFLASH_DTYPE_F16 if args.f16 else dflash.DFLASH_DTYPE_BF16
 
     def run():
-        dflash.dflash_testing_gemm(dflash.DFLASH_TESTING_ENGINE_TC, dflash.DFLASH_DTYPE_BF16, A, B,
-                                   C, args.splits, A_lo=Alo)
+        dflash.dflash_testing_gemm(dflash.DFLASH_TESTING_ENGINE_TC, dt, A, B, C, args.splits)
     run()
     dflash.dflash_device_status()
     ms = _timed(run, args.iters)
-    flops = 2.0 * args.m * args.n * args.k * (2 if args.two_term else 1)
-    print(f"gemm M={args.m} N={args.n} K={args.k} two_term={args.two_term} splits={args.splits}: "
-          f"{ms:.4f} ms/launch, {flops / ms / 1e9:.1f} TFLOP/s issued")
+    flops = 2.0 * args.m * args.n * args.k
+    print(f"gemm M={args.m} N={args.n} K={args.k} {'f16' if args.f16 else 'bf16'} "
+          f"splits={args.splits}: {ms:.4f} ms/launch, {flops / ms / 1e9:.1f} TFLOP/s")
 
 
 def case_body(args):
@@ -70,8 +69,8 @@ def case_body(args):
         return torch.from_numpy(np.ascontiguousarray(t.data)).cuda()
     top = {k: dev(v) for k, v in di.gen_top_weights(w).items()}
     layers = [{k: dev(v) for k, v in di.gen_layer_weights(w, l).items()} for l in range(s.num_layers)]
-    wts = dflash.Weights(top, layers)
-    cfg = dflash.make_config(s)
+    wts = dflash.prepare_f16_layers(dflash.Weights(top, layers))
+    cfg = dflash.make_config(s, f16_layers=True)
     mask = torch.from_numpy(di.gen_mask(w)).cuda()
     sids = torch.from_numpy(di.gen_sample_ids(w)).cuda()
     H = dev(di.gen_target_hidden(w))
@@ -134,7 +133,7 @@ def main(argv=None):
     ap.add_argument("--n", type=int, default=4096)
     ap.add_argument("--k", type=int, default=20480)
     ap.add_argument("--splits", type=int, default=1)
-    ap.add_argument("--two-term", action="store_true")
+    ap.add_argument("--f16", action="store_true", help="fp16 operands (else bf16)")
     ap.add_argument("--workload", default="train_8b_b4_l2048")
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args(argv)

@@ -25,10 +25,16 @@
  *  - Dense matrices are row-major; weight matrices are stored [out_features, in_features]
  *    (y = x W^T).  Row strides are exactly the row widths given below.
  *  - Floating-point storage type is cfg->dtype for weights, inputs and embeddings:
- *    DFLASH_DTYPE_BF16 (bf16 tensor-core projections with fp32 accumulation, computed
- *    activations carried as two-term bf16 pairs, fp32 residual stream, attention on tf32
- *    tensor cores) or DFLASH_DTYPE_F32 (fp32 throughout, no TF32).  The context K/V cache
- *    is fp32 in both (tf32-rounded values in the bf16 configuration).
+ *    DFLASH_DTYPE_BF16 or DFLASH_DTYPE_F32 (fp32 throughout, no TF32).  In the bf16
+ *    configuration W_proj runs bf16 x bf16 on the tensor cores (the target hidden states
+ *    are exact bf16); the draft layers' projections run fp16 x fp16 on the tensor cores:
+ *    their weights are fp16 copies of the bf16 matrices (see DFLASH_FLAG_F16_LAYERS and
+ *    dflash_convert_bf16_to_f16) and the activations feeding them (norm outputs, attention
+ *    output, SwiGLU product) are rounded to fp16, whose 11 significant bits keep the body
+ *    within its error bound; accumulation is fp32, the residual stream fp32, attention on
+ *    tf32 tensor cores.  An activation outside the fp16 range sets DFLASH_ERR_RANGE.
+ *    The context K/V cache is fp32 in both configurations (tf32-rounded values in the
+ *    bf16 one).
  *  - The thread-local message of the last failing call: dflash_last_error().
  */
 #ifndef DFLASH_H_
@@ -54,12 +60,20 @@ extern "C" {
 #define DFLASH_ERR_CUDA 3          /* a CUDA runtime call failed */
 #define DFLASH_ERR_TIMEOUT 4       /* device status: a bounded device-side wait ran out */
 #define DFLASH_ERR_DEVICE_CHECK 5  /* device status: a device-side index check failed */
+#define DFLASH_ERR_RANGE 6         /* device status: a value outside the fp16 range (or a
+                                      NaN) was stored as fp16 */
 
 #define DFLASH_DTYPE_F32 0
 #define DFLASH_DTYPE_BF16 1
+#define DFLASH_DTYPE_F16 2         /* IEEE binary16: prepared layer weights only */
 
 #define DFLASH_FLAG_FINAL_NORM 1u  /* output = RMSNorm(x; g_final) (else the raw residual) */
 #define DFLASH_FLAG_CTX_NORM 2u    /* context = RMSNorm(H_cat W_proj^T; g_ctx) (else raw) */
+/* bf16 configuration only: the layer matrices w_qkv, w_o, w_gate_up and w_down are given
+ * as fp16 (made once per weight update with dflash_convert_bf16_to_f16).  Without it they
+ * are bf16 and every projection or body call first converts the matrices it uses into its
+ * workspace (one extra read and write of them per call). */
+#define DFLASH_FLAG_F16_LAYERS 4u
 
 /* Draft model shape ([P1] "Configuration"; the attention/MLP sizes of the draft layers).
  * num_heads % num_kv_heads == 0; head_dim even.  The bf16 configuration also needs
@@ -82,7 +96,8 @@ typedef struct dflash_config {
   double rms_eps;             /* RMSNorm epsilon */
 } dflash_config_t;
 
-/* One draft decoder layer (pre-norm attention + SwiGLU MLP), device pointers, dtype cfg->dtype. */
+/* One draft decoder layer (pre-norm attention + SwiGLU MLP), device pointers, dtype cfg->dtype
+ * (the four matrices fp16 under DFLASH_FLAG_F16_LAYERS; the gains stay cfg->dtype). */
 typedef struct dflash_layer_weights {
   const void* g_in;       /* [D] input RMSNorm gain */
   const void* w_qkv;      /* [(Hq + 2*Hkv)*dh, D]: rows = Q heads, then K heads, then V heads */
@@ -109,9 +124,16 @@ DFLASH_API const char* dflash_last_error(void);
 DFLASH_API int dflash_version(void);
 
 /* Synchronizes the current device, then returns its sticky device-side status:
- * DFLASH_OK, DFLASH_ERR_TIMEOUT or DFLASH_ERR_DEVICE_CHECK (DFLASH_ERR_CUDA if the
- * synchronization itself fails).  reset != 0 clears the word afterwards. */
+ * DFLASH_OK, DFLASH_ERR_TIMEOUT, DFLASH_ERR_DEVICE_CHECK or DFLASH_ERR_RANGE
+ * (DFLASH_ERR_CUDA if the synchronization itself fails).  reset != 0 clears the word
+ * afterwards. */
 DFLASH_API int dflash_device_status(int reset);
+
+/* dst[i] = fp16(src[i]) for n bf16 values, round to nearest even (device pointers, 16-byte
+ * aligned, asynchronous on stream).  Exact for zero and for magnitudes in [2^-14, 65504];
+ * smaller magnitudes land on the fp16 subnormal grid (error <= 2^-25); a result that is not
+ * finite sets DFLASH_ERR_RANGE.  Prepares the layer matrices for DFLASH_FLAG_F16_LAYERS. */
+DFLASH_API int dflash_convert_bf16_to_f16(const void* src, void* dst, size_t n, void* stream);
 
 /* ---- 1. anchor plan ([P2] How It Works, steps 1, 2 and 4) ---------------------------- */
 

@@ -15,17 +15,17 @@
 extern "C" {
 #endif
 
-#define DFLASH_TESTING_ENGINE_TC 0   /* tcgen05 / TMEM / TMA kernel (bf16 only) */
+#define DFLASH_TESTING_ENGINE_TC 0   /* tcgen05 / TMEM / TMA kernel (bf16 or fp16) */
 #define DFLASH_TESTING_ENGINE_SIMT 1 /* CUDA-core kernel (fp32 accumulation, no TF32) */
 
-/* C[z] (float32, [splits][M][ldc]) = (A + A_lo)[:, Kz] * B[:, Kz]^T, A and the optional
- * second term A_lo [M, K] (row stride lda; A_lo only with the tensor-core engine),
- * B [N, K] (row stride ldb), all of type dtype (DFLASH_DTYPE_*), device pointers.
- * The K range is cut into `splits` contiguous slices of 64-element steps; slice z goes to
- * C + z*M*ldc.  Asynchronous on `stream`.  Returns a DFLASH_* status. */
-DFLASH_API int dflash_testing_gemm(int engine, int dtype, const void* A, const void* A_lo, long lda,
-                                   const void* B, long ldb, float* C, long ldc, long M, int N,
-                                   int K, int splits, void* stream);
+/* C[z] (float32, [splits][M][ldc]) = A[:, Kz] * B[:, Kz]^T, A [M, K] (row stride lda) and
+ * B [N, K] (row stride ldb) both of type dtype (tensor cores: DFLASH_DTYPE_BF16 or _F16;
+ * CUDA cores: _BF16 or _F32), device pointers.  The K range is cut into `splits`
+ * contiguous slices of 64-element steps; slice z goes to C + z*M*ldc.  Asynchronous on
+ * `stream`.  Returns a DFLASH_* status. */
+DFLASH_API int dflash_testing_gemm(int engine, int dtype, const void* A, long lda, const void* B,
+                                   long ldb, float* C, long ldc, long M, int N, int K, int splits,
+                                   void* stream);
 
 /* The K-split the library picks for an M x N x K projection on the current device. */
 DFLASH_API int dflash_testing_gemm_splits(long M, int N, int K);
@@ -38,7 +38,8 @@ DFLASH_API int dflash_testing_gemm_splits(long M, int N, int K);
 #define DFLASH_PROF_ROWS 2       /* norms, RoPE table, GEMM epilogues */
 #define DFLASH_PROF_PLAN 3       /* anchor plan */
 #define DFLASH_PROF_VERIFY 4     /* argmax + accepted-prefix scan */
-#define DFLASH_PROF_KINDS 5
+#define DFLASH_PROF_CONVERT 5    /* bf16 -> fp16 weight conversion */
+#define DFLASH_PROF_KINDS 6
 
 DFLASH_API int dflash_profile_enable(int on);
 

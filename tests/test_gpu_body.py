@@ -31,13 +31,18 @@ class Case:
         self.emb = di.gen_block_emb(w)
         self.N = plan["anchors"].shape[1]
 
-    def run_gpu(self, emb=None, hidden=None, mask=None, check_cache=False, ctx_len=None):
+    def run_gpu(self, emb=None, hidden=None, mask=None, check_cache=False, ctx_len=None,
+                f16_layers=False):
+        """f16_layers: hand the library fp16 copies of the layer matrices (prepared once,
+        DFLASH_FLAG_F16_LAYERS) instead of the bf16 ones it converts inside each call."""
         import torch
         import block_draft_model_proj_gb300 as dflash
         w, s = self.w, self.w.shape
         B, L, N, S = w.batch, w.seq_len, self.N, s.block_size
-        cfg = dflash.make_config(s)
+        cfg = dflash.make_config(s, f16_layers=f16_layers)
         wts = self.model.lib_weights()
+        if f16_layers:
+            wts = dflash.prepare_f16_layers(wts)
         H = to_device(di.gen_target_hidden(w) if hidden is None else hidden)
         kv = torch.empty((s.num_layers, B, 2, s.num_kv_heads, L, s.head_dim), dtype=torch.float32,
                          device="cuda")
@@ -209,3 +214,26 @@ def test_out_of_range_position_reports_device_check(lib):
     with pytest.raises(RuntimeError, match="index check"):
         c.run_gpu()
     dflash.dflash_device_status(reset=True)
+
+
+def test_prepared_f16_layer_weights_match_in_call_conversion(lib):
+    """Layer matrices converted once (DFLASH_FLAG_F16_LAYERS) and converted inside each call
+    feed the same GEMMs: the outputs are bit-identical."""
+    c = Case(small_bf16_workload())
+    assert np.array_equal(c.run_gpu(), c.run_gpu(f16_layers=True))
+
+
+def test_activation_outside_fp16_range_is_reported(lib):
+    """A gain of 1e5 on the first input norm pushes the normalised activations past the fp16
+    range: the device status reports DFLASH_ERR_RANGE."""
+    import torch
+    import block_draft_model_proj_gb300 as dflash
+    c = Case(small_bf16_workload())
+    g = c.model.dev_layers[0]["g_in"]
+    c.model.dev_layers[0]["g_in"] = torch.full_like(g, 1e5)
+    try:
+        with pytest.raises(RuntimeError, match="fp16 range"):
+            c.run_gpu()
+    finally:
+        c.model.dev_layers[0]["g_in"] = g
+        dflash.dflash_device_status(reset=True)

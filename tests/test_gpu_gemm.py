@@ -1,5 +1,5 @@
 """The projection GEMM kernels in isolation (test hook of the library) vs an fp64 product of
-the same bf16/fp32 operands.  Tensor-core (tcgen05) and CUDA-core engines, ragged shapes,
+the same bf16/fp16/fp32 operands.  Tensor-core (tcgen05) and CUDA-core engines, ragged shapes,
 K-splits."""
 import numpy as np
 import pytest
@@ -9,7 +9,7 @@ import dflash_inputs as di
 pytestmark = pytest.mark.gpu
 
 
-def run(engine, dtype, M, N, K, splits, seed=0, lda_pad=0, two_term=False):
+def run(engine, dtype, M, N, K, splits, seed=0, lda_pad=0):
     import torch
     import block_draft_model_proj_gb300 as dflash
     rng = np.random.default_rng(seed)
@@ -19,26 +19,27 @@ def run(engine, dtype, M, N, K, splits, seed=0, lda_pad=0, two_term=False):
         A = di.Tensor(di.f32_to_bf16_bits(a32), "bf16")
         B = di.Tensor(di.f32_to_bf16_bits(b32), "bf16")
         dt = dflash.DFLASH_DTYPE_BF16
+        ref_a, ref_b = A.f64(), B.f64()
+    elif dtype == "f16":
+        a16, b16 = a32.astype(np.float16), b32.astype(np.float16)
+        dt = dflash.DFLASH_DTYPE_F16
+        ref_a, ref_b = a16.astype(np.float64), b16.astype(np.float64)
     else:
         A, B = di.Tensor(a32, "f32"), di.Tensor(b32, "f32")
         dt = dflash.DFLASH_DTYPE_F32
-    from dflash_testlib import to_device
-    dA, dB = to_device(A), to_device(B)
+        ref_a, ref_b = A.f64(), B.f64()
+    from dflash_testlib import np_to_device, to_device
+    if dtype == "f16":
+        dA, dB = np_to_device(a16), np_to_device(b16)
+    else:
+        dA, dB = to_device(A), to_device(B)
     dA = dA[:, :K] if lda_pad else dA
-    dAlo = None
-    ref_a = A.f64()[:, :K]
-    if two_term:
-        # second term: the rounding residual of a fp32 activation, as the library stores it
-        lo = di.f32_to_bf16_bits((a32 - A.f32()).astype(np.float32))
-        Alo = di.Tensor(lo, "bf16")
-        dAlo = to_device(Alo)
-        dAlo = dAlo[:, :K] if lda_pad else dAlo
-        ref_a = ref_a + Alo.f64()[:, :K]
+    ref_a = ref_a[:, :K]
     C = torch.full((splits, M, N), float("nan"), dtype=torch.float32, device="cuda")
-    dflash.dflash_testing_gemm(engine, dt, dA, dB, C, splits, A_lo=dAlo)
+    dflash.dflash_testing_gemm(engine, dt, dA, dB, C, splits)
     dflash.dflash_device_status()
     got = C.cpu().numpy().astype(np.float64).sum(axis=0)
-    ref = ref_a @ B.f64().T
+    ref = ref_a @ ref_b.T
     return got, ref, K
 
 
@@ -70,17 +71,15 @@ def test_tcgen05_gemm(lib, M, N, K, splits):
 
 @pytest.mark.parametrize("M,N,K,splits", [(128, 256, 64, 1), (300, 520, 200, 1),
                                           (16, 6144, 4096, 4), (1000, 300, 4104, 2)])
-def test_tcgen05_gemm_two_term(lib, M, N, K, splits):
+def test_tcgen05_gemm_f16(lib, M, N, K, splits):
     import block_draft_model_proj_gb300 as dflash
-    got, ref, K = run(dflash.DFLASH_TESTING_ENGINE_TC, "bf16", M, N, K, splits, seed=5,
-                      two_term=True)
+    got, ref, K = run(dflash.DFLASH_TESTING_ENGINE_TC, "f16", M, N, K, splits, seed=5)
     assert_close(got, ref, K)
 
 
-def test_tcgen05_gemm_two_term_strided(lib):
+def test_tcgen05_gemm_f16_strided(lib):
     import block_draft_model_proj_gb300 as dflash
-    got, ref, K = run(dflash.DFLASH_TESTING_ENGINE_TC, "bf16", 200, 256, 320, 1, lda_pad=64,
-                      two_term=True)
+    got, ref, K = run(dflash.DFLASH_TESTING_ENGINE_TC, "f16", 200, 256, 320, 1, lda_pad=64)
     assert_close(got, ref, K)
 
 
