@@ -222,7 +222,7 @@ class GpuStep:
         self.d_logits = self.h_logits.to(device)
         self.d_draft = self.h_draft.to(device)
         self.kv = torch.empty((s.num_layers, B, 2, s.num_kv_heads, L, s.head_dim),
-                              dtype=torch.float32, device=device)
+                              dtype=dflash.kv_cache_dtype(self.cfg), device=device)
         self.anchors = torch.empty((B, N), dtype=torch.int32, device=device)
         self.bv = torch.empty((B, N, S), dtype=torch.uint8, device=device)
         self.lm = torch.empty_like(self.bv)
@@ -383,7 +383,8 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f16",
         "precision": "bf16 inputs and weights; W_proj bf16 x bf16, draft-layer projections "
                      "f16 x f16 (fp16 copies of the bf16 layer weights, fp16 activations), "
-                     "fp32 accumulation and residual stream, attention tf32 x tf32",
+                     "fp32 accumulation and residual stream, attention f16 x f16 over an "
+                     "fp16 context K/V cache",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, bf16)",
         "config": {"workload": f"{w.name}: B={w.batch} L={w.seq_len} N={w.num_anchors} "
                                f"S={w.shape.block_size} D={w.shape.hidden} "

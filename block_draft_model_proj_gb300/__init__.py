@@ -194,6 +194,13 @@ def prepare_f16_layers(weights: Weights, out: list | None = None, stream=None) -
     return Weights(top, new_layers)
 
 
+def kv_cache_dtype(cfg):
+    """torch dtype of the context K/V cache planes for a config: fp16 in the bf16
+    configuration, fp32 in the fp32 one."""
+    import torch
+    return torch.float16 if cfg.dtype == DFLASH_DTYPE_BF16 else torch.float32
+
+
 def workspace(nbytes: int, device="cuda"):
     import torch
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)

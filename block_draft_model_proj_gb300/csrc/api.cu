@@ -179,8 +179,9 @@ int check_cfg(const dflash_config_t* c) {
                 "head_dim <= 256");
   if (c->dtype == DFLASH_DTYPE_BF16 &&
       !attention_tc_supported(c->block_size, c->num_heads, c->num_kv_heads, c->head_dim))
-    return fail(DFLASH_ERR_UNSUPPORTED, "bf16 attention needs head_dim == 128 and "
-                "block_size * num_heads/num_kv_heads dividing 128");
+    return fail(DFLASH_ERR_UNSUPPORTED, "bf16 attention needs head_dim == 128, "
+                "block_size * num_heads/num_kv_heads dividing 128 and num_heads/num_kv_heads "
+                "dividing 16");
   return DFLASH_OK;
 }
 
@@ -297,7 +298,7 @@ ProjLayout proj_layout(const dflash_config_t* c, int B, int L, void* ws) {
 struct BodyLayout {
   float* x;
   Act h, attn, act;
-  float *q, *kb, *vbt;  // attention-ready operands
+  void *q, *kb, *vbt;   // attention-ready operands (fp16 in the bf16 configuration, else fp32)
   int ns_pad;
   float* partials;      // tensor-core attention partials (bf16 configuration)
   int32_t* tile_list;   // 128-slot tiles holding at least one valid slot (count first)
@@ -326,10 +327,17 @@ BodyLayout body_layout(const dflash_config_t* c, int B, int L, int N, void* ws) 
   Carver cv(ws);
   b.x = cv.take<float>((size_t)T * D);
   b.h = take_act(cv, (size_t)T * D, c->dtype);
-  b.q = cv.take<float>((size_t)T * qw);
-  b.kb = cv.take<float>((size_t)T * kw);
-  b.ns_pad = (N * c->block_size + 3) / 4 * 4;
-  b.vbt = cv.take<float>((size_t)B * c->num_kv_heads * c->head_dim * b.ns_pad);
+  b.ns_pad = (N * c->block_size + 7) / 8 * 8;
+  const size_t nvbt = (size_t)B * c->num_kv_heads * c->head_dim * b.ns_pad;
+  if (c->dtype == DFLASH_DTYPE_BF16) {
+    b.q = cv.take<__half>((size_t)T * qw);
+    b.kb = cv.take<__half>((size_t)T * kw);
+    b.vbt = cv.take<__half>(nvbt);
+  } else {
+    b.q = cv.take<float>((size_t)T * qw);
+    b.kb = cv.take<float>((size_t)T * kw);
+    b.vbt = cv.take<float>(nvbt);
+  }
   b.partials = nullptr;
   if (c->dtype == DFLASH_DTYPE_BF16)
     b.partials = cv.take<float>((size_t)attention_tc_layout(B, N, c->block_size, L, c->num_heads,
@@ -434,8 +442,8 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
     return fail(DFLASH_ERR_INVALID_ARG, "need B, L >= 1 and 0 <= pos_offset, pos_offset + L <= L_cache");
   if ((r = check_ptr16(target_hidden, "target_hidden", cfg->dtype))) return r;
   if ((r = check_ptr16(kv_cache, "kv_cache", DFLASH_DTYPE_BF16))) return r;
-  if (cfg->dtype == DFLASH_DTYPE_BF16 && L_cache % 4 != 0)
-    return fail(DFLASH_ERR_INVALID_ARG, "L_cache must be a multiple of 4 (16-byte cache rows)");
+  if (cfg->dtype == DFLASH_DTYPE_BF16 && L_cache % 8 != 0)
+    return fail(DFLASH_ERR_INVALID_ARG, "L_cache must be a multiple of 8 (16-byte fp16 cache rows)");
   const ProjLayout lay = proj_layout(cfg, B, L, ws);
   if ((r = check_ws(ws, ws_bytes, lay.bytes))) return r;
   cudaStream_t s = (cudaStream_t)stream;
@@ -467,7 +475,6 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
                              ctx_len, L, s));
   }
   const size_t layer_elems = (size_t)B * 2 * Hkv * L_cache * dh;
-  const bool to_tf32 = cfg->dtype == DFLASH_DTYPE_BF16;
   for (int l = 0; l < cfg->num_layers; ++l) {
     const void* wkv = static_cast<const uint8_t*>(w->layers[l].w_qkv) + (size_t)qw * D * es;
     if (lay.wkv16) {
@@ -475,11 +482,10 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
       DF_CUDA(launch_convert_bf16_f16(wkv, lay.wkv16, (size_t)kvw * D, status_ptr(), s));
       wkv = lay.wkv16;
     }
-    float* kv_layer = static_cast<float*>(kv_cache) + (size_t)l * layer_elems;
     if (cfg->dtype == DFLASH_DTYPE_BF16) {
-      // RoPE and the cache layout are applied in the GEMM epilogue
+      // RoPE and the fp16 cache layout are applied in the GEMM epilogue
       KvCacheEpilogue kv;
-      kv.kv = kv_layer;
+      kv.kv = static_cast<__half*>(kv_cache) + (size_t)l * layer_elems;
       kv.cos_t = lay.cos_t;
       kv.sin_t = lay.sin_t;
       kv.ctx_len = ctx_len;
@@ -487,7 +493,6 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
       kv.pos_offset = pos_offset;
       kv.L_cache = L_cache;
       kv.Hkv = Hkv;
-      kv.to_tf32 = 1;
       Prof pr(DFLASH_PROF_GEMM, 1, s);
       DF_CUDA(launch_gemm_tc_kv_cache(DFLASH_DTYPE_F16, lay.ctx.p, D, wkv, D, M, kvw, D, flags,
                                       kv, status_ptr(), s));
@@ -499,8 +504,9 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
                    lay.split_kv, s, flags));
     }
     Prof pr(DFLASH_PROF_ROWS, 2, s);
-    DF_CUDA(launch_ctx_kv_scatter(lay.y, lay.split_kv, lay.cos_t, lay.sin_t, kv_layer, B, L,
-                                  pos_offset, L_cache, Hkv, dh, to_tf32, ctx_len, s));
+    DF_CUDA(launch_ctx_kv_scatter(lay.y, lay.split_kv, lay.cos_t, lay.sin_t,
+                                  static_cast<float*>(kv_cache) + (size_t)l * layer_elems, B, L,
+                                  pos_offset, L_cache, Hkv, dh, ctx_len, s));
   }
   return DFLASH_OK;
 }
@@ -526,8 +532,8 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
   if ((r = check_ptr16(mask, "mask", cfg->dtype))) return r;
   if ((r = check_ptr16(block_emb, "block_emb", cfg->dtype))) return r;
   if ((r = check_ptr16(kv_cache, "kv_cache", DFLASH_DTYPE_BF16))) return r;
-  if (cfg->dtype == DFLASH_DTYPE_BF16 && L % 4 != 0)
-    return fail(DFLASH_ERR_INVALID_ARG, "L must be a multiple of 4 (16-byte cache rows)");
+  if (cfg->dtype == DFLASH_DTYPE_BF16 && L % 8 != 0)
+    return fail(DFLASH_ERR_INVALID_ARG, "L must be a multiple of 8 (16-byte fp16 cache rows)");
   const BodyLayout lay = body_layout(cfg, B, L, N, ws);
   if ((r = check_ws(ws, ws_bytes, lay.bytes))) return r;
   cudaStream_t s = (cudaStream_t)stream;
@@ -578,14 +584,13 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
                               lay.P, lay.q, lay.kb, lay.vbt, lay.ns_pad, T, N, S, Hq, Hkv, dh,
                               dt == DFLASH_DTYPE_BF16, st, s));
     }
-    const float* kv_layer = static_cast<const float*>(kv_cache) + (size_t)l * layer_elems;
     if (dt == DFLASH_DTYPE_BF16) {
       AttnTcArgs aa;
-      aa.q = lay.q;
-      aa.kb = lay.kb;
-      aa.vbt = lay.vbt;
+      aa.q = static_cast<const __half*>(lay.q);
+      aa.kb = static_cast<const __half*>(lay.kb);
+      aa.vbt = static_cast<const __half*>(lay.vbt);
       aa.ns_pad = lay.ns_pad;
-      aa.kv_layer = kv_layer;
+      aa.kv_layer = static_cast<const __half*>(kv_cache) + (size_t)l * layer_elems;
       aa.anchors = anchors;
       aa.valid = block_valid;
       aa.mask = mask;
@@ -603,11 +608,11 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
       DF_CUDA(launch_attention_tc(aa, s));
     } else {
       AttnArgs aa;
-      aa.q = lay.q;
-      aa.kb = lay.kb;
-      aa.vbt = lay.vbt;
+      aa.q = static_cast<const float*>(lay.q);
+      aa.kb = static_cast<const float*>(lay.kb);
+      aa.vbt = static_cast<const float*>(lay.vbt);
       aa.ns_pad = lay.ns_pad;
-      aa.kv_layer = kv_layer;
+      aa.kv_layer = static_cast<const float*>(kv_cache) + (size_t)l * layer_elems;
       aa.anchors = anchors;
       aa.valid = block_valid;
       aa.mask = mask;

@@ -22,16 +22,17 @@
 // attn_combine_kernel merges the chunks of a tile in chunk order (deterministic) and writes
 // the attention output (fp16) for the O projection.
 //
-// Arithmetic: kind::tf32 MMAs with fp32 accumulation.  Q, the block K/V and the context K/V
-// cache are fp32 values rounded to tf32, P is rounded to tf32; the softmax runs in fp32 in
-// registers (one TMEM lane = one query row per thread), base-2 exponent, with a lazily
-// updated running maximum (the accumulator is rescaled only when the maximum grows by more
-// than 2^8, so P stays <= 256).
+// Arithmetic: kind::f16 MMAs with fp32 accumulation.  Q, the block K/V and the context K/V
+// cache are fp16 (11 significant bits, as many as tf32), P is rounded to fp16; the softmax
+// runs in fp32 in registers (one TMEM lane = one query row per thread), base-2 exponent,
+// with a lazily updated running maximum (the accumulator is rescaled only when the maximum
+// grows by more than 2^8, so P stays <= 256).
 //
 // Tensor memory holds the whole working set of a tile: Q (loaded once per unit from global
-// by the softmax warps), the O accumulator, and four S/P buffers (S = Q K^T lands there, the
-// softmax overwrites it with P, and O += P V reads P from there).  Shared memory holds only
-// K and V^T tiles of 64 keys in two separate 3-stage TMA rings.
+// by the softmax warps, packed fp16 pairs), the O accumulator, and four S/P buffers (S = Q K^T
+// lands there; each softmax warp overwrites the first half of its own S columns with its
+// packed fp16 P, and O += P V reads P from there).  Shared memory holds only K and V^T tiles
+// of 64 keys in two separate 4-stage TMA rings.
 // Warp roles: warp 0 TMA producers (lane 0 the K ring, lane 1 the V^T ring); warp 1 MMA
 // issuer, which polls its barriers without blocking and issues S of the next tiles as soon as
 // a K tile and an S/P buffer are free, independently of the PV of earlier tiles; warps 2-9
@@ -55,28 +56,27 @@ using namespace tc;
 constexpr int kDH = 128;   // head dim handled by this kernel
 constexpr int kM = 128;    // query rows per tile (TMEM lanes)
 constexpr int kKT = 64;    // keys per tile
-constexpr int kRing = 3;   // stages of each of the K and V^T rings
+constexpr int kRing = 4;   // stages of each of the K and V^T rings
 constexpr int kSP = 4;     // S/P buffers in tensor memory
 constexpr int kThreads = 320;          // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
 constexpr int kSoftmaxWarps = 8;       // two per TMEM lane quarter, each owns half the keys
 constexpr int kHalfKT = 32;            // key columns per softmax thread
-constexpr uint32_t kTmemCols = 512;    // Q [0,128), O [128,256), S/P 4 x 64 [256,512)
+constexpr uint32_t kTmemCols = 512;    // Q [0,64), O [128,256), S/P 4 x 64 [256,512)
 constexpr uint32_t kTmemQ = 0, kTmemO = 128, kTmemS = 256;
-constexpr uint32_t kKSub = kKT * 32 * 4; // K [64 keys][32 dh] fp32, 8 KB
-constexpr uint32_t kKBytes = 4 * kKSub;  // 32 KB
-constexpr uint32_t kVSub = kDH * 32 * 4; // V^T [128 dh][32 keys], 16 KB
-constexpr uint32_t kVBytes = 2 * kVSub;  // 32 KB
+constexpr uint32_t kKSub = kKT * 64 * 2;   // K [64 keys][64 dh] fp16, 8 KB
+constexpr uint32_t kKBytes = 2 * kKSub;    // 16 KB
+constexpr uint32_t kVBytes = kDH * kKT * 2;  // V^T [128 dh][64 keys] fp16, 16 KB
 constexpr uint32_t kBarBytes = 512;
 // K ring + V ring + barriers + row-max exchange [2][2][128] + row-sum exchange [2][128]
 constexpr size_t kSmemBytes = 1024 + kRing * (size_t)(kKBytes + kVBytes) + kBarBytes +
                               (4 * 128 + 2 * 128) * sizeof(float);
-constexpr uint32_t kIdescS = idesc_tf32(kM, kKT);
-constexpr uint32_t kIdescPV = idesc_tf32(kM, kDH);
+constexpr uint32_t kIdescS = idesc_f16(kM, kKT);
+constexpr uint32_t kIdescPV = idesc_f16(kM, kDH);
 constexpr float kRescaleLog2 = 8.0f;
 
 struct AttnTcParams {
   int B, N, S, L, Hkv, grp, R, bpt, tiles, chunk, max_chunks;
-  const float* q;  // [B][Hkv][N][S][grp][dh], tf32-rounded
+  const __half* q;  // [B][Hkv][N][S][grp][dh]
   long q_rows;
   const int32_t* anchors;
   const uint8_t* valid;
@@ -184,8 +184,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       const bool is_k = lane == 0;
       uint64_t* full = is_k ? k_full : v_full;
       uint64_t* empty = is_k ? k_empty : v_empty;
-      int issued[kRing] = {0, 0, 0};
-      uint32_t issued_ph[kRing] = {0, 0, 0};
+      int issued[kRing] = {0, 0, 0, 0};
+      uint32_t issued_ph[kRing] = {0, 0, 0, 0};
       for (int i = 0; i < u.n; ++i) {
         const int st = i % kRing;
         const uint32_t ph = (uint32_t)(i / kRing) & 1u;
@@ -195,22 +195,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
           uint8_t* dst = sK + st * kKBytes;
           if (i < u.nblk) {
             const int kbrow0 = ((u.b * p.Hkv + u.g) * p.N + u.k0) * p.S + i * kKT;
-            for (int q = 0; q < 4; ++q) tma_load_2d(&map_kb, &full[st], dst + q * kKSub, q * 32, kbrow0);
+            for (int q = 0; q < 2; ++q) tma_load_2d(&map_kb, &full[st], dst + q * kKSub, q * 64, kbrow0);
           } else {
             const int c0 = u.cs + (i - u.nblk) * kKT;
-            for (int q = 0; q < 4; ++q) tma_load_3d(&map_kc, &full[st], dst + q * kKSub, q * 32, c0, plane_k);
+            for (int q = 0; q < 2; ++q) tma_load_3d(&map_kc, &full[st], dst + q * kKSub, q * 64, c0, plane_k);
           }
         } else {
           mbar_arrive_expect_tx(&full[st], kVBytes);
           uint8_t* dst = sV + st * kVBytes;
           if (i < u.nblk) {
-            for (int v = 0; v < 2; ++v)
-              tma_load_2d(&map_vb, &full[st], dst + v * kVSub, u.k0 * p.S + i * kKT + v * 32,
-                          (u.b * p.Hkv + u.g) * kDH);
+            tma_load_2d(&map_vb, &full[st], dst, u.k0 * p.S + i * kKT, (u.b * p.Hkv + u.g) * kDH);
           } else {
-            const int c0 = u.cs + (i - u.nblk) * kKT;
-            for (int v = 0; v < 2; ++v)
-              tma_load_3d(&map_vc, &full[st], dst + v * kVSub, c0 + v * 32, 0, plane_v);
+            tma_load_3d(&map_vc, &full[st], dst, u.cs + (i - u.nblk) * kKT, 0, plane_v);
           }
         }
         issued[st] = 1;
@@ -238,10 +234,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
           tc_fence_after();
           const uint32_t k_addr = smem_u32(sK + (ns % kRing) * kKBytes);
           const uint32_t s_tmem = tmem_s0 + (uint32_t)((ns % kSP) * kKT);
+          // K = 16 dh per MMA: Q columns 8k .. 8k+7 (packed pairs); K sub-tile k / 4, +32 bytes
 #pragma unroll 1
-          for (int k = 0; k < kDH / 8; ++k)
-            umma_tf32_ts(s_tmem, tmem_q + k * 8, sw128_desc(k_addr + (k >> 2) * kKSub + (k & 3) * 32),
-                         kIdescS, k ? 1u : 0u);
+          for (int k = 0; k < kDH / 16; ++k)
+            umma_f16_ts(s_tmem, tmem_q + k * 8, sw128_desc(k_addr + (k >> 2) * kKSub + (k & 3) * 32),
+                        kIdescS, k ? 1u : 0u);
           umma_commit(&s_full[ns % kSP]);
           umma_commit(&k_empty[ns % kRing]);
           ++ns;
@@ -251,11 +248,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
           tc_fence_after();
           const uint32_t v_addr = smem_u32(sV + (npv % kRing) * kVBytes);
           const uint32_t a_base = tmem_s0 + (uint32_t)((npv % kSP) * kKT);
+          // K = 16 keys per MMA: P of keys 16k .. 16k+15 sits at columns 32 * (k / 2) +
+          // 8 * (k % 2) of the buffer (each softmax half packs its 32 keys into the first 16
+          // of its own 32 S columns); V^T +32 bytes per 16 keys
 #pragma unroll 1
-          for (int v = 0; v < 2; ++v)
-            for (int k = 0; k < 4; ++k)
-              umma_tf32_ts(tmem_o, a_base + v * 32 + k * 8, sw128_desc(v_addr + v * kVSub + k * 32),
-                           kIdescPV, (npv == 0 && v == 0 && k == 0) ? 0u : 1u);
+          for (int k = 0; k < kKT / 16; ++k)
+            umma_f16_ts(tmem_o, a_base + (k >> 1) * 32 + (k & 1) * 8, sw128_desc(v_addr + k * 32),
+                        kIdescPV, (npv == 0 && k == 0) ? 0u : 1u);
           umma_commit(&pv_done[npv % kSP]);
           umma_commit(&v_empty[npv % kRing]);
           ++npv;
@@ -291,22 +290,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       row_valid = a >= 0 && p.valid[(u.b * p.N + kb) * p.S + j] != 0;
       a_row = min(max(a, 0), p.L);
     }
-    // this thread's half of the query row -> tensor memory (columns [64*half, +64) of Q)
+    // this thread's half of the query row (dh [64*half, +64), 32 packed fp16 pairs) ->
+    // tensor memory columns [32*half, +32) of Q
     {
       const long qrow = (long)((u.b * p.Hkv + u.g) * p.N + u.k0) * p.R + r;
-      const float4* qsrc = reinterpret_cast<const float4*>(p.q + qrow * kDH + half * 64);
-      for (int part = 0; part < 2; ++part) {
-        uint32_t qv[32];
+      const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + qrow * kDH + half * 64);
+      uint32_t qv[32];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float4 f = qrow < p.q_rows ? __ldg(qsrc + part * 8 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-          qv[4 * e] = __float_as_uint(f.x);
-          qv[4 * e + 1] = __float_as_uint(f.y);
-          qv[4 * e + 2] = __float_as_uint(f.z);
-          qv[4 * e + 3] = __float_as_uint(f.w);
-        }
-        tmem_st_32x32b_x32(tmem_q + lane_off + half * 64 + part * 32, qv);
+      for (int e = 0; e < 8; ++e) {
+        const uint4 f = qrow < p.q_rows ? __ldg(qsrc + e) : make_uint4(0u, 0u, 0u, 0u);
+        qv[4 * e] = f.x;
+        qv[4 * e + 1] = f.y;
+        qv[4 * e + 2] = f.z;
+        qv[4 * e + 3] = f.w;
       }
+      tmem_st_32x32b_x32(tmem_q + lane_off + half * 32, qv);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -422,21 +420,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
         l_run *= factor;
       }
       // P = 2^(x - m): an excluded key (x = -inf) gives exactly +0; a row that has not seen
-      // a readable key yet (m_run = -inf) has only excluded keys here
+      // a readable key yet (m_run = -inf) has only excluded keys here.  Packed as fp16 pairs
+      // into the first 16 of this half's S columns.
       float lsum = 0.f;
+      uint32_t pw[kHalfKT / 2];
       if (m_run == -INFINITY) {
 #pragma unroll
-        for (int kk = 0; kk < kHalfKT; ++kk) sv[kk] = 0u;
+        for (int kk = 0; kk < kHalfKT / 2; ++kk) pw[kk] = 0u;
       } else {
 #pragma unroll
-        for (int kk = 0; kk < kHalfKT; ++kk) {
-          const float pv = round_tf32(ex2_approx(x[kk] - m_run));
-          lsum += pv;
-          sv[kk] = __float_as_uint(pv);
+        for (int kk = 0; kk < kHalfKT / 2; ++kk) {
+          const float p0 = ex2_approx(x[2 * kk] - m_run), p1 = ex2_approx(x[2 * kk + 1] - m_run);
+          lsum += p0 + p1;
+          const __half2 h2 = __floats2half2_rn(p0, p1);
+          pw[kk] = *reinterpret_cast<const uint32_t*>(&h2);
         }
       }
       l_run += lsum;
-      tmem_st_32x32b_x32(s_tmem, sv);
+      tmem_st_32x32b_x16(s_tmem, pw);
       tmem_wait_st();
       // value columns past the last readable key of this tile: zero them (this thread owns
       // V^T row r of key sub-tile `half`) so that whatever the cache holds there cannot
@@ -445,17 +446,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
         const int st = i % kRing;
         if (!wait_all(&v_full[st], (uint32_t)(i / kRing) & 1u)) { ok = false; break; }
         const int nvalid = u.a_max - (u.cs + (i - u.nblk) * kKT);
-        uint8_t* rowp = sV + st * kVBytes + half * kVSub + (r >> 3) * 1024 + (r & 7) * 128;
-        for (int ch = 0; ch < 8; ++ch) {
-          const int key0 = half * 32 + ch * 4;
-          if (key0 + 4 <= nvalid) continue;
-          float4* dst = reinterpret_cast<float4*>(rowp + ((ch ^ (r & 7)) * 16));
-          float4 val = *dst;
-          if (key0 + 0 >= nvalid) val.x = 0.f;
-          if (key0 + 1 >= nvalid) val.y = 0.f;
-          if (key0 + 2 >= nvalid) val.z = 0.f;
-          if (key0 + 3 >= nvalid) val.w = 0.f;
-          *dst = val;
+        // row r of the swizzled [128][64] fp16 tile: 16-byte chunk c (keys 8c .. 8c+7) sits
+        // at chunk position c ^ (r % 8); this half owns chunks 4*half .. 4*half+3
+        uint8_t* rowp = sV + st * kVBytes + (r >> 3) * 1024 + (r & 7) * 128;
+        for (int cc = 0; cc < 4; ++cc) {
+          const int c = half * 4 + cc;
+          const int key0 = c * 8;
+          if (key0 + 8 <= nvalid) continue;
+          uint4* dst = reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) * 16));
+          uint4 val = *dst;
+          uint32_t wv[4] = {val.x, val.y, val.z, val.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int k0 = key0 + 2 * e;  // keys k0 (low half) and k0 + 1 (high half)
+            if (k0 >= nvalid) wv[e] = 0u;
+            else if (k0 + 1 >= nvalid) wv[e] &= 0xFFFFu;
+          }
+          *dst = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
         fence_proxy_async_smem();
       }
@@ -569,13 +576,13 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// fp32 map with a 128-byte swizzle; dims/box innermost first; strides in bytes for dims 1..
-bool encode_f32(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+// fp16 map with a 128-byte swizzle; dims/box innermost first; strides in bytes for dims 1..
+bool encode_f16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
                 const cuuint64_t* strides, const cuuint32_t* box) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<void*>(base), dims, strides, box,
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -602,8 +609,11 @@ AttnTcLayout attention_tc_layout(int B, int N, int S, int L, int Hq, int Hkv, in
 
 bool attention_tc_supported(int S, int Hq, int Hkv, int dh) {
   if (dh != kDH || Hq % Hkv != 0) return false;
-  const int R = S * (Hq / Hkv);
-  return R >= 1 && R <= kM && (kM % R) == 0;
+  const int grp = Hq / Hkv;
+  const int R = S * grp;
+  // a query tile covers 128 / grp block slots: the block V^T tiles then start at a key index
+  // that is a multiple of 8 (16 bytes of fp16), as a tiled TMA load requires
+  return R >= 1 && R <= kM && (kM % R) == 0 && (kM / grp) % 8 == 0;
 }
 
 cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream) {
@@ -635,28 +645,28 @@ cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream) {
   const long planes = (long)a.B * 2 * a.Hkv;
   {
     cuuint64_t dims[3] = {(cuuint64_t)kDH, (cuuint64_t)a.L, (cuuint64_t)planes};
-    cuuint64_t str[2] = {(cuuint64_t)kDH * 4, (cuuint64_t)a.L * kDH * 4};
-    cuuint32_t box[3] = {32, (cuuint32_t)kKT, 1};
-    if (!encode_f32(&mkc, a.kv_layer, 3, dims, str, box)) return cudaErrorInvalidValue;
+    cuuint64_t str[2] = {(cuuint64_t)kDH * 2, (cuuint64_t)a.L * kDH * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kKT, 1};
+    if (!encode_f16(&mkc, a.kv_layer, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     cuuint64_t dims[3] = {(cuuint64_t)a.L, (cuuint64_t)kDH, (cuuint64_t)planes};
-    cuuint64_t str[2] = {(cuuint64_t)a.L * 4, (cuuint64_t)a.L * kDH * 4};
-    cuuint32_t box[3] = {32, (cuuint32_t)kDH, 1};
-    if (!encode_f32(&mvc, a.kv_layer, 3, dims, str, box)) return cudaErrorInvalidValue;
+    cuuint64_t str[2] = {(cuuint64_t)a.L * 2, (cuuint64_t)a.L * kDH * 2};
+    cuuint32_t box[3] = {(cuuint32_t)kKT, (cuuint32_t)kDH, 1};
+    if (!encode_f16(&mvc, a.kv_layer, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     const long kb_rows = (long)a.B * a.Hkv * a.N * a.S;
     cuuint64_t dims[2] = {(cuuint64_t)kDH, (cuuint64_t)kb_rows};
-    cuuint64_t str[1] = {(cuuint64_t)kDH * 4};
-    cuuint32_t box[2] = {32, (cuuint32_t)kKT};
-    if (!encode_f32(&mkb, a.kb, 2, dims, str, box)) return cudaErrorInvalidValue;
+    cuuint64_t str[1] = {(cuuint64_t)kDH * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kKT};
+    if (!encode_f16(&mkb, a.kb, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     cuuint64_t dims[2] = {(cuuint64_t)a.N * a.S, (cuuint64_t)a.B * a.Hkv * kDH};
-    cuuint64_t str[1] = {(cuuint64_t)a.ns_pad * 4};
-    cuuint32_t box[2] = {32, (cuuint32_t)kDH};
-    if (!encode_f32(&mvb, a.vbt, 2, dims, str, box)) return cudaErrorInvalidValue;
+    cuuint64_t str[1] = {(cuuint64_t)a.ns_pad * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kKT, (cuuint32_t)kDH};
+    if (!encode_f16(&mvb, a.vbt, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   static bool attr = false;
   if (!attr) {

@@ -42,6 +42,11 @@ template <> struct Elem<__nv_bfloat16> {
   static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
 };
 
+template <> struct Elem<__half> {
+  static __device__ __forceinline__ float to_f(__half v) { return __half2float(v); }
+  static __device__ __forceinline__ __half from_f(float v) { return __float2half_rn(v); }
+};
+
 template <typename T> __device__ __forceinline__ float to_f(T v) { return Elem<T>::to_f(v); }
 template <typename T> __device__ __forceinline__ T from_f(float v) { return Elem<T>::from_f(v); }
 

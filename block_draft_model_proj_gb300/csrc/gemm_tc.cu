@@ -114,6 +114,7 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int m_cnt, int t,
 // (rotate-half: channel i pairs with i + 64; table row c) and are written as cache rows
 // [pos][dh]; V heads are written transposed, [dh][pos] -- consecutive lanes hold consecutive
 // positions, so those stores are coalesced.  Rows at or past ctx_len[b] are not written.
+// The cache holds fp16 (round to nearest even).
 __device__ __forceinline__ void kv_cache_epilogue(const TcParams& p, uint32_t tbase, int m_t,
                                                   int n_t, int quarter, int lane) {
   const KvCacheEpilogue& e = p.kv;
@@ -124,13 +125,14 @@ __device__ __forceinline__ void kv_cache_epilogue(const TcParams& p, uint32_t tb
   if (row_ok && e.ctx_len) row_ok = c < e.ctx_len[b];
   const long pos = (long)e.pos_offset + c;
   const long plane = (long)e.L_cache * 128;
+  bool bad = false;  // a value outside the fp16 range (or NaN) met the cache
 #pragma unroll 1
   for (int hh = 0; hh < 2; ++hh) {
     const int head = n_t * 2 + hh;  // 0 .. 2*Hkv-1: K heads, then V heads
     if (head >= 2 * e.Hkv) break;   // warp-uniform
     const uint32_t hbase = tbase + hh * 128;
     if (head < e.Hkv) {
-      float* dst = e.kv + ((long)b * 2 * e.Hkv + head) * plane + pos * 128;
+      __half* dst = e.kv + ((long)b * 2 * e.Hkv + head) * plane + pos * 128;
 #pragma unroll 1
       for (int ch = 0; ch < 2; ++ch) {  // channel chunks (32ch .. 32ch+31) and their pairs +64
         uint32_t lo[32], hi[32];
@@ -140,25 +142,31 @@ __device__ __forceinline__ void kv_cache_epilogue(const TcParams& p, uint32_t tb
           const float* cs = e.cos_t + (long)c * 64 + ch * 32;
           const float* sn = e.sin_t + (long)c * 64 + ch * 32;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 c4 = reinterpret_cast<const float4*>(cs)[q];
-            const float4 s4 = reinterpret_cast<const float4*>(sn)[q];
-            const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, ss[4] = {s4.x, s4.y, s4.z, s4.w};
-            float a[4], bb[4];
+          for (int q = 0; q < 4; ++q) {  // 8 channels (16 bytes of fp16) per step
+            uint32_t wa[4], wb[4];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const float x0 = __uint_as_float(lo[4 * q + t]), x1 = __uint_as_float(hi[4 * q + t]);
-              a[t] = x0 * cc[t] - x1 * ss[t];
-              bb[t] = x1 * cc[t] + x0 * ss[t];
-              if (e.to_tf32) { a[t] = round_tf32(a[t]); bb[t] = round_tf32(bb[t]); }
+            for (int t2 = 0; t2 < 4; ++t2) {
+              const int t = 8 * q + 2 * t2;
+              const float2 c2 = *reinterpret_cast<const float2*>(cs + t);
+              const float2 s2 = *reinterpret_cast<const float2*>(sn + t);
+              const float x00 = __uint_as_float(lo[t]), x10 = __uint_as_float(hi[t]);
+              const float x01 = __uint_as_float(lo[t + 1]), x11 = __uint_as_float(hi[t + 1]);
+              const float a0 = x00 * c2.x - x10 * s2.x, a1 = x01 * c2.y - x11 * s2.y;
+              const float b0 = x10 * c2.x + x00 * s2.x, b1 = x11 * c2.y + x01 * s2.y;
+              bad = bad || !(fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))) +
+                             0.f * (a0 + a1 + b0 + b1) < 65520.f);
+              const __half2 ha = __floats2half2_rn(a0, a1);
+              const __half2 hb = __floats2half2_rn(b0, b1);
+              wa[t2] = *reinterpret_cast<const uint32_t*>(&ha);
+              wb[t2] = *reinterpret_cast<const uint32_t*>(&hb);
             }
-            reinterpret_cast<float4*>(dst + ch * 32)[q] = make_float4(a[0], a[1], a[2], a[3]);
-            reinterpret_cast<float4*>(dst + 64 + ch * 32)[q] = make_float4(bb[0], bb[1], bb[2], bb[3]);
+            reinterpret_cast<uint4*>(dst + ch * 32)[q] = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+            reinterpret_cast<uint4*>(dst + 64 + ch * 32)[q] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
           }
         }
       }
     } else {
-      float* dst = e.kv + ((long)b * 2 * e.Hkv + e.Hkv + (head - e.Hkv)) * plane + pos;
+      __half* dst = e.kv + ((long)b * 2 * e.Hkv + e.Hkv + (head - e.Hkv)) * plane + pos;
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t v[32];
@@ -166,14 +174,15 @@ __device__ __forceinline__ void kv_cache_epilogue(const TcParams& p, uint32_t tb
         if (row_ok) {
 #pragma unroll
           for (int t = 0; t < 32; ++t) {
-            float x = __uint_as_float(v[t]);
-            if (e.to_tf32) x = round_tf32(x);
-            dst[(long)(ch * 32 + t) * e.L_cache] = x;
+            const float x = __uint_as_float(v[t]);
+            bad = bad || !(fabsf(x) < 65520.f);
+            dst[(long)(ch * 32 + t) * e.L_cache] = __float2half_rn(x);
           }
         }
       }
     }
   }
+  if (bad) report(p.status, kStatusRange, kKernEpilogue);
 }
 
 // SwiGLU epilogue: accumulator columns [0, 128) are the gate and [128, 256) the up

@@ -54,22 +54,22 @@ cudaError_t launch_rows_norm(int dtype, const float* y, int nsplit, const void* 
                              bool with_norm, ActOut out, long rows, int D,
                              const int32_t* ctx_len, int L, cudaStream_t stream);
 
-// QKV epilogue: y [nsplit][T][(Hq+2Hkv)*dh] fp32 -> attention-ready fp32 operands
-// q [B][Hkv][N][S][grp][dh], kb [B][Hkv][N*S][dh], vbt [B][Hkv][dh][ns_pad]; RoPE on q and
-// k at position pos[t] (table of P positions; out-of-range valid slots report a device
-// check and use position 0); values rounded to tf32 when to_tf32.
+// QKV epilogue: y [nsplit][T][(Hq+2Hkv)*dh] fp32 -> attention-ready operands (fp16 when
+// f16, else fp32) q [B][Hkv][N][S][grp][dh], kb [B][Hkv][N*S][dh], vbt [B][Hkv][dh][ns_pad];
+// RoPE on q and k at position pos[t] (table of P positions; out-of-range valid slots report
+// a device check and use position 0).
 cudaError_t launch_qkv_rope(const float* y, int nsplit, const int32_t* pos, const uint8_t* valid,
-                            const float* cos_t, const float* sin_t, int P, float* q, float* kb,
-                            float* vbt, int ns_pad, long T, int N, int S, int Hq, int Hkv, int dh,
-                            bool to_tf32, unsigned* status, cudaStream_t stream);
+                            const float* cos_t, const float* sin_t, int P, void* q, void* kb,
+                            void* vbt, int ns_pad, long T, int N, int S, int Hq, int Hkv, int dh,
+                            bool f16, unsigned* status, cudaStream_t stream);
 
-// Context K/V epilogue: y [nsplit][B*L][2*Hkv*dh] fp32 -> the fp32 cache planes of one layer
-// [B][2][Hkv]: K as [L_cache][dh] (RoPE'd; table row c = position pos_offset + c) and V^T as
-// [dh][L_cache], at positions pos_offset + c; rounded to tf32 when to_tf32.
+// Context K/V epilogue (fp32 configuration): y [nsplit][B*L][2*Hkv*dh] fp32 -> the fp32
+// cache planes of one layer [B][2][Hkv]: K as [L_cache][dh] (RoPE'd; table row c = position
+// pos_offset + c) and V^T as [dh][L_cache], at positions pos_offset + c.
 // Rows c >= ctx_len[b] (when ctx_len is given) are not written.
 cudaError_t launch_ctx_kv_scatter(const float* y, int nsplit, const float* cos_t,
                                   const float* sin_t, float* kv_layer, int B, int L,
-                                  int pos_offset, int L_cache, int Hkv, int dh, bool to_tf32,
+                                  int pos_offset, int L_cache, int Hkv, int dh,
                                   const int32_t* ctx_len, cudaStream_t stream);
 
 // SwiGLU epilogue: y [nsplit][T][2I] fp32 (gate | up) -> act [T][I] = SiLU(gate) * up.
@@ -91,12 +91,11 @@ bool gemm_tc_supported(long M, int N, int K, long lda, long ldb);
 // Destination of the context K/V projection written straight from the GEMM epilogue
 // (head_dim 128): rows m = b*L + c of the GEMM are cache positions pos_offset + c.
 struct KvCacheEpilogue {
-  float* kv = nullptr;           // one layer: [B][2][Hkv] planes, K [L_cache][128], V^T [128][L_cache]
+  __half* kv = nullptr;          // one layer: [B][2][Hkv] fp16 planes, K [L_cache][128], V^T [128][L_cache]
   const float* cos_t = nullptr;  // [L][64], row c = position pos_offset + c
   const float* sin_t = nullptr;
   const int32_t* ctx_len = nullptr;  // optional [B]: rows c >= ctx_len[b] are not written
   int L = 0, pos_offset = 0, L_cache = 0, Hkv = 0;
-  int to_tf32 = 0;
 };
 // act = SiLU(gate) * up with [gate | up] = A W_gate_up^T (W_gate_up [2I][K]: gate rows then
 // up rows), written by the epilogue (no K-split).
@@ -143,13 +142,13 @@ struct AttnArgs {
 };
 cudaError_t launch_attention_simt(int dtype, const AttnArgs& a, cudaStream_t stream);
 
-// ---- attention_tc.cu: tcgen05 (kind::tf32) attention over attention-ready layouts ----
+// ---- attention_tc.cu: tcgen05 (kind::f16) attention over attention-ready fp16 layouts ----
 struct AttnTcArgs {
-  const float* q;           // [B][Hkv][N][S][grp][dh], tf32-rounded
-  const float* kb;          // [B][Hkv][N*S][dh] block keys, tf32-rounded
-  const float* vbt;         // [B][Hkv][dh][ns_pad] block values transposed, tf32-rounded
-  int ns_pad;               // row stride of vbt (>= N*S, multiple of 4)
-  const float* kv_layer;    // [B][2][Hkv] planes: K [L][dh], V^T [dh][L] (fp32)
+  const __half* q;          // [B][Hkv][N][S][grp][dh]
+  const __half* kb;         // [B][Hkv][N*S][dh] block keys
+  const __half* vbt;        // [B][Hkv][dh][ns_pad] block values transposed
+  int ns_pad;               // row stride of vbt (>= N*S, multiple of 8)
+  const __half* kv_layer;   // [B][2][Hkv] planes: K [L][dh], V^T [dh][L] (fp16)
   const int32_t* anchors;
   const uint8_t* valid;
   const uint8_t* mask;

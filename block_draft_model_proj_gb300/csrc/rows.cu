@@ -228,24 +228,20 @@ __global__ void swiglu_vec_kernel(const float* __restrict__ y, int nsplit, long 
   }
 }
 
-__device__ __forceinline__ float maybe_tf32(float v, bool to_tf32) {
-  if (!to_tf32) return v;
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
-  return __uint_as_float(r);
-}
 
 // One thread per (row t, head, channel pair i).  Writes the attention operands in the
-// attention-ready layouts (fp32; rounded to tf32 when `to_tf32`):
+// attention-ready layouts (OutT: fp32 for the CUDA-core attention, fp16 for the tensor-core
+// attention):
 //   q   [B][Hkv][N][S][grp][dh]   (the query rows of one KV head are contiguous per block)
 //   kb  [B][Hkv][N*S][dh]         (block keys)
 //   vbt [B][Hkv][dh][ns_pad]      (block values, transposed)
+template <typename OutT>
 __global__ void qkv_rope_kernel(const float* __restrict__ y, int nsplit, long split_stride,
                                 const int32_t* __restrict__ pos, const uint8_t* __restrict__ valid,
                                 const float* __restrict__ cos_t, const float* __restrict__ sin_t,
-                                int P, float* __restrict__ q, float* __restrict__ kb,
-                                float* __restrict__ vbt, int ns_pad, long T, int N, int S, int Hq,
-                                int Hkv, int dh, bool to_tf32, unsigned* status) {
+                                int P, OutT* __restrict__ q, OutT* __restrict__ kb,
+                                OutT* __restrict__ vbt, int ns_pad, long T, int N, int S, int Hq,
+                                int Hkv, int dh, unsigned* status) {
   const int half = dh / 2;
   const int heads = Hq + 2 * Hkv;
   const int grp = Hq / Hkv;
@@ -267,9 +263,9 @@ __global__ void qkv_rope_kernel(const float* __restrict__ y, int nsplit, long sp
     const int k = ks / S, j = ks - k * S;
     if (hd >= Hq + Hkv) {  // V: no rotation, transposed
       const int g = hd - Hq - Hkv;
-      float* dst = vbt + ((long)(b * Hkv + g) * dh) * ns_pad + ks;
-      dst[(long)i * ns_pad] = maybe_tf32(a, to_tf32);
-      dst[(long)(i + half) * ns_pad] = maybe_tf32(bb, to_tf32);
+      OutT* dst = vbt + ((long)(b * Hkv + g) * dh) * ns_pad + ks;
+      dst[(long)i * ns_pad] = from_f<OutT>(a);
+      dst[(long)(i + half) * ns_pad] = from_f<OutT>(bb);
       continue;
     }
     int pp = pos[t];
@@ -279,7 +275,7 @@ __global__ void qkv_rope_kernel(const float* __restrict__ y, int nsplit, long sp
     }
     const float c = cos_t[(long)pp * half + i], sn = sin_t[(long)pp * half + i];
     const float lo = a * c - bb * sn, hi = bb * c + a * sn;
-    float* dst;
+    OutT* dst;
     if (hd < Hq) {
       const int g = hd / grp, h = hd - g * grp;
       dst = q + (((((long)b * Hkv + g) * N + k) * S + j) * grp + h) * dh;
@@ -287,8 +283,8 @@ __global__ void qkv_rope_kernel(const float* __restrict__ y, int nsplit, long sp
       const int g = hd - Hq;
       dst = kb + ((((long)b * Hkv + g) * N + k) * S + j) * dh;
     }
-    dst[i] = maybe_tf32(lo, to_tf32);
-    dst[i + half] = maybe_tf32(hi, to_tf32);
+    dst[i] = from_f<OutT>(lo);
+    dst[i + half] = from_f<OutT>(hi);
   }
 }
 
@@ -297,7 +293,7 @@ __global__ void ctx_k_scatter_kernel(const float* __restrict__ y, int nsplit, lo
                                      const float* __restrict__ cos_t,
                                      const float* __restrict__ sin_t, float* __restrict__ kv,
                                      int B, int L, int pos_offset, int L_cache, int Hkv, int dh,
-                                     bool to_tf32, const int32_t* __restrict__ ctx_len) {
+                                     const int32_t* __restrict__ ctx_len) {
   const int half = dh / 2;
   const long per_row = (long)Hkv * half;
   const long n = (long)B * L * per_row;
@@ -314,8 +310,8 @@ __global__ void ctx_k_scatter_kernel(const float* __restrict__ y, int nsplit, lo
     // table row c holds position pos_offset + c
     const float cs = cos_t[(long)c * half + i], sn = sin_t[(long)c * half + i];
     float* dst = kv + ((((long)b * 2) * Hkv + g) * L_cache + pos_offset + c) * dh;
-    dst[i] = maybe_tf32(a * cs - bb * sn, to_tf32);
-    dst[i + half] = maybe_tf32(bb * cs + a * sn, to_tf32);
+    dst[i] = a * cs - bb * sn;
+    dst[i + half] = bb * cs + a * sn;
   }
 }
 
@@ -323,7 +319,7 @@ __global__ void ctx_k_scatter_kernel(const float* __restrict__ y, int nsplit, lo
 // are coalesced; plane (b, 1, g) holds V^T as [dh][L_cache].
 __global__ void ctx_vt_scatter_kernel(const float* __restrict__ y, int nsplit, long split_stride,
                                       float* __restrict__ kv, int B, int L, int pos_offset,
-                                      int L_cache, int Hkv, int dh, bool to_tf32,
+                                      int L_cache, int Hkv, int dh,
                                       const int32_t* __restrict__ ctx_len) {
   const long n = (long)B * Hkv * dh * L;
   for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n;
@@ -337,7 +333,7 @@ __global__ void ctx_vt_scatter_kernel(const float* __restrict__ y, int nsplit, l
     if (ctx_len && c >= ctx_len[b]) continue;
     const long src = ((long)b * L + c) * 2L * Hkv * dh + (long)(Hkv + g) * dh + d;
     const float v = sum_splits(y, nsplit, split_stride, src);
-    kv[((((long)b * 2 + 1) * Hkv + g) * dh + d) * L_cache + pos_offset + c] = maybe_tf32(v, to_tf32);
+    kv[((((long)b * 2 + 1) * Hkv + g) * dh + d) * L_cache + pos_offset + c] = v;
   }
 }
 
@@ -426,31 +422,35 @@ cudaError_t launch_rows_norm(int dtype, const float* y, int nsplit, const void* 
 }
 
 cudaError_t launch_qkv_rope(const float* y, int nsplit, const int32_t* pos, const uint8_t* valid,
-                            const float* cos_t, const float* sin_t, int P, float* q, float* kb,
-                            float* vbt, int ns_pad, long T, int N, int S, int Hq, int Hkv, int dh,
-                            bool to_tf32, unsigned* status, cudaStream_t stream) {
+                            const float* cos_t, const float* sin_t, int P, void* q, void* kb,
+                            void* vbt, int ns_pad, long T, int N, int S, int Hq, int Hkv, int dh,
+                            bool f16, unsigned* status, cudaStream_t stream) {
   const long n = T * (Hq + 2 * Hkv) * (dh / 2);
   const long stride = T * (long)(Hq + 2 * Hkv) * dh;
-  qkv_rope_kernel<<<grid_for(n, 256), 256, 0, stream>>>(y, nsplit, stride, pos, valid, cos_t,
-                                                        sin_t, P, q, kb, vbt, ns_pad, T, N, S, Hq,
-                                                        Hkv, dh, to_tf32, status);
+  if (f16)
+    qkv_rope_kernel<__half><<<grid_for(n, 256), 256, 0, stream>>>(
+        y, nsplit, stride, pos, valid, cos_t, sin_t, P, static_cast<__half*>(q),
+        static_cast<__half*>(kb), static_cast<__half*>(vbt), ns_pad, T, N, S, Hq, Hkv, dh, status);
+  else
+    qkv_rope_kernel<float><<<grid_for(n, 256), 256, 0, stream>>>(
+        y, nsplit, stride, pos, valid, cos_t, sin_t, P, static_cast<float*>(q),
+        static_cast<float*>(kb), static_cast<float*>(vbt), ns_pad, T, N, S, Hq, Hkv, dh, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_ctx_kv_scatter(const float* y, int nsplit, const float* cos_t,
                                   const float* sin_t, float* kv_layer, int B, int L,
-                                  int pos_offset, int L_cache, int Hkv, int dh, bool to_tf32,
+                                  int pos_offset, int L_cache, int Hkv, int dh,
                                   const int32_t* ctx_len, cudaStream_t stream) {
   const long stride = (long)B * L * 2 * Hkv * dh;
   const long nk = (long)B * L * Hkv * (dh / 2);
   ctx_k_scatter_kernel<<<grid_for(nk, 256), 256, 0, stream>>>(
-      y, nsplit, stride, cos_t, sin_t, kv_layer, B, L, pos_offset, L_cache, Hkv, dh, to_tf32,
-      ctx_len);
+      y, nsplit, stride, cos_t, sin_t, kv_layer, B, L, pos_offset, L_cache, Hkv, dh, ctx_len);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long nv = (long)B * Hkv * dh * L;
   ctx_vt_scatter_kernel<<<grid_for(nv, 256), 256, 0, stream>>>(
-      y, nsplit, stride, kv_layer, B, L, pos_offset, L_cache, Hkv, dh, to_tf32, ctx_len);
+      y, nsplit, stride, kv_layer, B, L, pos_offset, L_cache, Hkv, dh, ctx_len);
   return cudaGetLastError();
 }
 

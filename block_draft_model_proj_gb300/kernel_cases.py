@@ -75,7 +75,7 @@ def case_body(args):
     sids = torch.from_numpy(di.gen_sample_ids(w)).cuda()
     H = dev(di.gen_target_hidden(w))
     emb = dev(di.gen_block_emb(w))
-    kv = torch.empty((s.num_layers, B, 2, s.num_kv_heads, L, s.head_dim), dtype=torch.float32,
+    kv = torch.empty((s.num_layers, B, 2, s.num_kv_heads, L, s.head_dim), dtype=dflash.kv_cache_dtype(cfg),
                      device="cuda")
     if w.inference:
         a_np, v_np, p_np = di.inference_block_layout(w)

@@ -31,10 +31,11 @@
  *    their weights are fp16 copies of the bf16 matrices (see DFLASH_FLAG_F16_LAYERS and
  *    dflash_convert_bf16_to_f16) and the activations feeding them (norm outputs, attention
  *    output, SwiGLU product) are rounded to fp16, whose 11 significant bits keep the body
- *    within its error bound; accumulation is fp32, the residual stream fp32, attention on
- *    tf32 tensor cores.  An activation outside the fp16 range sets DFLASH_ERR_RANGE.
- *    The context K/V cache is fp32 in both configurations (tf32-rounded values in the
- *    bf16 one).
+ *    within its error bound; accumulation is fp32, the residual stream fp32.  Attention
+ *    runs fp16 x fp16 on the tensor cores (fp16 Q, K, V and probabilities; fp32 softmax
+ *    and accumulation) over an fp16 context K/V cache.  A value outside the fp16 range
+ *    (an activation or a cache entry) sets DFLASH_ERR_RANGE.  The fp32 configuration keeps
+ *    an fp32 cache.
  *  - The thread-local message of the last failing call: dflash_last_error().
  */
 #ifndef DFLASH_H_
@@ -77,8 +78,9 @@ extern "C" {
 
 /* Draft model shape ([P1] "Configuration"; the attention/MLP sizes of the draft layers).
  * num_heads % num_kv_heads == 0; head_dim even.  The bf16 configuration also needs
- * head_dim == 128, block_size * num_heads / num_kv_heads dividing 128, and every matrix row
- * width a multiple of 8 (DFLASH_ERR_UNSUPPORTED otherwise). */
+ * head_dim == 128, block_size * num_heads / num_kv_heads dividing 128, num_heads /
+ * num_kv_heads dividing 16, and every matrix row width a multiple of 8
+ * (DFLASH_ERR_UNSUPPORTED otherwise). */
 typedef struct dflash_config {
   int32_t target_hidden;      /* D_t: width of one selected target layer */
   int32_t num_target_layers;  /* n_tl: number of selected target layers (concat width n_tl*D_t) */
@@ -168,13 +170,14 @@ DFLASH_API size_t dflash_project_context_workspace_size(const dflash_config_t* c
 /* Projects the target's selected hidden states into every draft layer's K/V space.
  *   target_hidden [B, L, n_tl*D_t]: the selected target layers concatenated in
  *                 target_layer_ids order, for context positions pos_offset .. pos_offset+L-1
- *   kv_cache      float32, NL x B x 2 x Hkv planes of L_cache*dh elements: for layer l,
+ *   kv_cache      fp16 (bf16 configuration) or float32 (fp32 configuration), NL x B x 2 x Hkv
+ *                 planes of L_cache*dh elements: for layer l,
  *                 row b, head g, plane (l, b, 0, g) = K as [L_cache][dh] with
  *                 K = RoPE(ctx W_k^T), and plane (l, b, 1, g) = V transposed, [dh][L_cache],
  *                 V = ctx W_v^T; ctx = RMSNorm(target_hidden W_proj^T; g_ctx), W_k / W_v =
  *                 the K / V rows of layer l's w_qkv.  Written at positions
  *                 pos_offset .. pos_offset+L-1 only; 16-byte aligned; in the bf16
- *                 configuration L_cache must be a multiple of 4.
+ *                 configuration L_cache must be a multiple of 8.
  *   ctx_len       optional [B] int32 (NULL = L): positions c >= ctx_len[b] of row b may be
  *                 left unwritten (no block of that row reads them); values are clamped to [0, L].
  * Requires 0 <= pos_offset, pos_offset + L <= L_cache.  RoPE positions are the absolute
@@ -194,7 +197,8 @@ DFLASH_API size_t dflash_body_workspace_size(const dflash_config_t* cfg, int B, 
  *   block_valid  [B, N, S] uint8
  *   position_ids [B, N, S] int32: RoPE position of each slot, in [0, L + S) for valid slots
  *   mask         [B, L] uint8: context validity
- *   kv_cache     float32 planes from dflash_project_context (L = its L_cache); the
+ *   kv_cache     the planes from dflash_project_context (L = its L_cache, a multiple of 8
+ *                in the bf16 configuration); the
  *                positions a block reads (c < its anchor) must have been written; what the
  *                other positions hold never reaches an output
  *   out          [B, N, S, D] float32: one hidden state per slot; exactly 0 where

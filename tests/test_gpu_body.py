@@ -44,7 +44,8 @@ class Case:
         if f16_layers:
             wts = dflash.prepare_f16_layers(wts)
         H = to_device(di.gen_target_hidden(w) if hidden is None else hidden)
-        kv = torch.empty((s.num_layers, B, 2, s.num_kv_heads, L, s.head_dim), dtype=torch.float32,
+        kv = torch.empty((s.num_layers, B, 2, s.num_kv_heads, L, s.head_dim),
+                         dtype=dflash.kv_cache_dtype(cfg),
                          device="cuda")
         cl = None if ctx_len is None else np_to_device(np.asarray(ctx_len, np.int32))
         dflash.dflash_project_context(cfg, wts, H, B, L, 0, L, kv, ctx_len=cl)
@@ -96,7 +97,7 @@ def small_bf16_workload():
     shape = di.DraftShape(target_hidden=192, num_target_layers=2, hidden=256, num_layers=2,
                           num_heads=4, num_kv_heads=2, head_dim=128, intermediate=392,
                           block_size=4, dtype="bf16")
-    return di.Workload("small_bf16", 7, shape, batch=3, seq_len=300, num_anchors=5,
+    return di.Workload("small_bf16", 7, shape, batch=3, seq_len=304, num_anchors=5,
                        padded_rows=((1, 170),), verify_batch=0, vocab=0)
 
 
