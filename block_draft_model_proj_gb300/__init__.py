@@ -84,6 +84,7 @@ _SIGS = {
                                          _P]),
     "dflash_testing_gemm": (_I, [_I, _I, _P, _L, _P, _L, _P, _L, _L, _I, _I, _I, _P]),
     "dflash_testing_gemm_splits": (_I, [_L, _I, _I]),
+    "dflash_testing_gemm_ws": (_I, [_P, _L, _P, _I, _L, _P, _L, _L, _I, _I, _I, _P, _P, _P]),
     "dflash_profile_enable": (_I, [_I]),
     "dflash_profile_read": (_I, [_I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_L)]),
     "dflash_launch_count": (_L, []),
@@ -283,6 +284,15 @@ def dflash_testing_gemm(engine, dtype, A, B, C, splits=1, stream=None):
     N = B.shape[0]
     _check(load().dflash_testing_gemm(engine, dtype, _ptr(A), A.stride(0), _ptr(B), B.stride(0),
                                       _ptr(C), C.stride(-2), M, N, K, splits, _stream(stream)))
+
+
+def dflash_testing_gemm_ws(X, W, w_dtype, C, max_splits, splits_out, tile_list=None,
+                           stream=None):
+    M, K = X.shape
+    N = W.shape[0]
+    _check(load().dflash_testing_gemm_ws(_ptr(X), X.stride(0), _ptr(W), w_dtype, W.stride(0),
+                                         _ptr(C), C.stride(-2), M, N, K, max_splits,
+                                         _ptr(tile_list), _ptr(splits_out), _stream(stream)))
 
 
 def dflash_profile_enable(on: bool = True) -> None:

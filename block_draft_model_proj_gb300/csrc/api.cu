@@ -257,17 +257,35 @@ Act take_act(Carver& cv, size_t n, int dtype) {
   return a;
 }
 
-// The draft layers' projection matrices as the layer GEMMs read them: the caller's (fp32
-// configuration, or fp16 given with DFLASH_FLAG_F16_LAYERS), or fp16 copies in the
-// workspace, converted at the start of the call that uses them.
-bool layers_need_copy(const dflash_config_t* c) {
-  return c->dtype == DFLASH_DTYPE_BF16 && (c->flags & DFLASH_FLAG_F16_LAYERS) == 0;
+// Element type of the draft layers' projection matrices in the bf16 configuration, as the
+// caller gives them: bf16, or fp16 under DFLASH_FLAG_F16_LAYERS.
+int layer_wdtype(const dflash_config_t* c) {
+  return (c->flags & DFLASH_FLAG_F16_LAYERS) ? DFLASH_DTYPE_F16 : DFLASH_DTYPE_BF16;
+}
+
+// Layer projections of at most this many tokens (a decode step) run on the weight-streaming
+// GEMM, which reads bf16 weights as given; larger ones on the 128 x 256-tile GEMM, which
+// takes fp16 weights (the caller's, or copies converted at the start of the call).
+constexpr long kWsMaxTokens = 128;
+
+// fp16 copies of the layer matrices are made inside the call (bf16 weights, large calls)
+bool convert_layers(const dflash_config_t* c, long tokens) {
+  return c->dtype == DFLASH_DTYPE_BF16 && layer_wdtype(c) == DFLASH_DTYPE_BF16 &&
+         tokens > kWsMaxTokens;
+}
+
+// Upper bound for the device-chosen K-split of a weight-streaming GEMM: about three waves
+// of units when every token tile is active, at most 8.
+int ws_max_splits(int Nw, long T) {
+  const long units = (long)((Nw + 127) / 128) * ((T + 127) / 128);
+  long s = (3L * num_sms() + units - 1) / units;
+  return (int)(s < 1 ? 1 : (s > 8 ? 8 : s));
 }
 
 struct ProjLayout {
   float* y;
   Act ctx;
-  __half* wkv16;  // one layer's K/V rows of w_qkv as fp16 (when converted here)
+  __half* wkv16;  // one layer's K/V rows of w_qkv as fp16 (converted in the call), or null
   float* cos_t;
   float* sin_t;
   int32_t* tile_list;
@@ -281,7 +299,7 @@ ProjLayout proj_layout(const dflash_config_t* c, int B, int L, void* ws) {
   const int D = c->hidden, Kc = c->target_hidden * c->num_target_layers;
   const int kvw = 2 * c->num_kv_heads * c->head_dim;
   p.split_proj = gemm_splits(M, D, Kc);
-  p.split_kv = gemm_splits(M, kvw, D);
+  p.split_kv = c->dtype == DFLASH_DTYPE_BF16 ? 1 : gemm_splits(M, kvw, D);
   const long ycols = (long)p.split_proj * D > (long)p.split_kv * kvw ? (long)p.split_proj * D
                                                                        : (long)p.split_kv * kvw;
   Carver cv(ws);
@@ -290,7 +308,7 @@ ProjLayout proj_layout(const dflash_config_t* c, int B, int L, void* ws) {
   p.cos_t = cv.take<float>((size_t)L * (c->head_dim / 2));
   p.sin_t = cv.take<float>((size_t)L * (c->head_dim / 2));
   p.tile_list = cv.take<int32_t>(1 + (size_t)(M + kGemmTileM - 1) / kGemmTileM);
-  p.wkv16 = layers_need_copy(c) ? cv.take<__half>((size_t)kvw * D) : nullptr;
+  p.wkv16 = convert_layers(c, M) ? cv.take<__half>((size_t)kvw * D) : nullptr;
   p.bytes = cv.off;
   return p;
 }
@@ -305,8 +323,10 @@ struct BodyLayout {
   float* y;
   float* cos_t;
   float* sin_t;
-  __half* wl16;         // one layer's four matrices as fp16 (when converted here)
-  int sp_qkv, sp_o, sp_gu, sp_down;
+  bool ws;              // layer projections on the weight-streaming GEMM (few tokens)
+  int* nsplit;          // weight-streaming GEMM: K-splits chosen on the device (QKV, O, down)
+  __half* wl16;         // one layer's four matrices as fp16 (converted in the call), or null
+  int sp_qkv, sp_o, sp_gu, sp_down;  // host K-splits, or the device upper bounds
   int P;
   size_t bytes;
 };
@@ -316,10 +336,23 @@ BodyLayout body_layout(const dflash_config_t* c, int B, int L, int N, void* ws) 
   const long T = (long)B * N * c->block_size;
   const int D = c->hidden, qw = c->num_heads * c->head_dim, kw = c->num_kv_heads * c->head_dim;
   const int qkvw = qw + 2 * kw, I = c->intermediate;
-  b.sp_qkv = gemm_splits(T, qkvw, D);
-  b.sp_o = gemm_splits(T, D, qw);
-  b.sp_gu = gemm_splits(T, 2 * I, D);
-  b.sp_down = gemm_splits(T, D, I);
+  b.ws = c->dtype == DFLASH_DTYPE_BF16 && T <= kWsMaxTokens;
+  if (b.ws) {
+    b.sp_qkv = ws_max_splits(qkvw, T);
+    b.sp_o = ws_max_splits(D, T);
+    b.sp_gu = 0;  // SiLU(gate) * up is formed in the GEMM epilogue
+    b.sp_down = ws_max_splits(D, T);
+  } else if (c->dtype == DFLASH_DTYPE_BF16) {
+    b.sp_qkv = gemm_splits(T, qkvw, D);
+    b.sp_o = gemm_splits(T, D, qw);
+    b.sp_gu = 0;
+    b.sp_down = gemm_splits(T, D, I);
+  } else {
+    b.sp_qkv = gemm_splits(T, qkvw, D);
+    b.sp_o = gemm_splits(T, D, qw);
+    b.sp_gu = gemm_splits(T, 2 * I, D);
+    b.sp_down = gemm_splits(T, D, I);
+  }
   long ycols = (long)b.sp_qkv * qkvw;
   if ((long)b.sp_o * D > ycols) ycols = (long)b.sp_o * D;
   if ((long)b.sp_gu * 2 * I > ycols) ycols = (long)b.sp_gu * 2 * I;
@@ -350,9 +383,10 @@ BodyLayout body_layout(const dflash_config_t* c, int B, int L, int N, void* ws) 
   b.P = L + c->block_size;
   b.cos_t = cv.take<float>((size_t)b.P * (c->head_dim / 2));
   b.sin_t = cv.take<float>((size_t)b.P * (c->head_dim / 2));
-  b.wl16 = layers_need_copy(c)
-               ? cv.take<__half>((size_t)qkvw * D + (size_t)D * qw + (size_t)2 * I * D + (size_t)D * I)
-               : nullptr;
+  b.nsplit = cv.take<int>(4);
+  b.wl16 = convert_layers(c, T) ? cv.take<__half>((size_t)qkvw * D + (size_t)D * qw +
+                                                  (size_t)2 * I * D + (size_t)D * I)
+                                : nullptr;
   b.bytes = cv.off;
   return b;
 }
@@ -477,11 +511,6 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
   const size_t layer_elems = (size_t)B * 2 * Hkv * L_cache * dh;
   for (int l = 0; l < cfg->num_layers; ++l) {
     const void* wkv = static_cast<const uint8_t*>(w->layers[l].w_qkv) + (size_t)qw * D * es;
-    if (lay.wkv16) {
-      Prof pr(DFLASH_PROF_CONVERT, 1, s);
-      DF_CUDA(launch_convert_bf16_f16(wkv, lay.wkv16, (size_t)kvw * D, status_ptr(), s));
-      wkv = lay.wkv16;
-    }
     if (cfg->dtype == DFLASH_DTYPE_BF16) {
       // RoPE and the fp16 cache layout are applied in the GEMM epilogue
       KvCacheEpilogue kv;
@@ -493,8 +522,14 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
       kv.pos_offset = pos_offset;
       kv.L_cache = L_cache;
       kv.Hkv = Hkv;
+      const void* wkv16 = wkv;
+      if (lay.wkv16) {
+        Prof pc(DFLASH_PROF_CONVERT, 1, s);
+        DF_CUDA(launch_convert_bf16_f16(wkv, lay.wkv16, (size_t)kvw * D, status_ptr(), s));
+        wkv16 = lay.wkv16;
+      }
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(launch_gemm_tc_kv_cache(DFLASH_DTYPE_F16, lay.ctx.p, D, wkv, D, M, kvw, D, flags,
+      DF_CUDA(launch_gemm_tc_kv_cache(DFLASH_DTYPE_F16, lay.ctx.p, D, wkv16, D, M, kvw, D, flags,
                                       kv, status_ptr(), s));
       continue;
     }
@@ -556,10 +591,31 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
   {
     Prof pr(DFLASH_PROF_ROWS, 2, s);
     DF_CUDA(launch_rope_table(lay.cos_t, lay.sin_t, 0, lay.P, dh, cfg->rope_theta, s));
-    DF_CUDA(launch_residual_norm(kNormInit, dt, lay.x, block_emb, nullptr, 0, w->layers[0].g_in,
-                                 cfg->rms_eps, lay.h.out(), nullptr, nullptr, false, T, D, s));
+    DF_CUDA(launch_residual_norm(kNormInit, dt, lay.x, block_emb, nullptr, 0, nullptr,
+                                 w->layers[0].g_in, cfg->rms_eps, lay.h.out(), nullptr,
+                                 block_valid, false, T, D, s));
   }
-  const int el = DFLASH_DTYPE_F16;  // layer GEMM operands in the bf16 configuration
+  const bool tc = dt == DFLASH_DTYPE_BF16;
+  // weight-streaming GEMM of one layer projection: X (fp16) [T][K] x W [Nw][K]^T
+  auto ws_args = [&](const void* X, int K, const void* W, int Nw, int max_splits, int* nsplit) {
+    WsArgs a;
+    a.X = X;
+    a.ldx = K;
+    a.M = T;
+    a.W = W;
+    a.w_dtype = layer_wdtype(cfg);
+    a.ldw = K;
+    a.Nw = Nw;
+    a.K = K;
+    a.tile_list = flags;
+    a.C = lay.y;
+    a.ldc = Nw;
+    a.max_splits = max_splits;
+    a.splits_out = nsplit;
+    a.status = st;
+    return a;
+  };
+  const bool use_ws = lay.ws;
   for (int l = 0; l < cfg->num_layers; ++l) {
     dflash_layer_weights_t lw = w->layers[l];
     if (lay.wl16) {
@@ -567,7 +623,7 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
       __half* dst = lay.wl16;
       const void** mats[4] = {&lw.w_qkv, &lw.w_o, &lw.w_gate_up, &lw.w_down};
       const size_t sizes[4] = {(size_t)qkvw * D, (size_t)D * qw, (size_t)2 * I * D, (size_t)D * I};
-      Prof pr(DFLASH_PROF_CONVERT, 4, s);
+      Prof pc(DFLASH_PROF_CONVERT, 4, s);
       for (int m = 0; m < 4; ++m) {
         DF_CUDA(launch_convert_bf16_f16(*mats[m], dst, sizes[m], st, s));
         *mats[m] = dst;
@@ -576,11 +632,16 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
     }
     {
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(gemm(dt, el, lay.h.p, D, lw.w_qkv, D, lay.y, qkvw, T, qkvw, D, lay.sp_qkv, s, flags));
+      if (use_ws)
+        DF_CUDA(launch_gemm_ws(ws_args(lay.h.p, D, lw.w_qkv, qkvw, lay.sp_qkv, lay.nsplit), s));
+      else
+        DF_CUDA(gemm(dt, DFLASH_DTYPE_F16, lay.h.p, D, lw.w_qkv, D, lay.y, qkvw, T, qkvw, D,
+                     lay.sp_qkv, s, flags));
     }
     {
       Prof pr(DFLASH_PROF_ROWS, 1, s);
-      DF_CUDA(launch_qkv_rope(lay.y, lay.sp_qkv, position_ids, block_valid, lay.cos_t, lay.sin_t,
+      DF_CUDA(launch_qkv_rope(lay.y, lay.sp_qkv, use_ws ? lay.nsplit : nullptr, position_ids,
+                              block_valid, lay.cos_t, lay.sin_t,
                               lay.P, lay.q, lay.kb, lay.vbt, lay.ns_pad, T, N, S, Hq, Hkv, dh,
                               dt == DFLASH_DTYPE_BF16, st, s));
     }
@@ -630,38 +691,52 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
     }
     {
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(gemm(dt, el, lay.attn.p, qw, lw.w_o, qw, lay.y, D, T, D, qw, lay.sp_o, s, flags));
+      if (use_ws)
+        DF_CUDA(launch_gemm_ws(ws_args(lay.attn.p, qw, lw.w_o, D, lay.sp_o, lay.nsplit + 1), s));
+      else
+        DF_CUDA(gemm(dt, DFLASH_DTYPE_F16, lay.attn.p, qw, lw.w_o, qw, lay.y, D, T, D, qw, lay.sp_o,
+                     s, flags));
     }
     {
       Prof pr(DFLASH_PROF_ROWS, 1, s);
-      DF_CUDA(launch_residual_norm(kNormAdd, dt, lay.x, nullptr, lay.y, lay.sp_o, lw.g_post,
-                                   cfg->rms_eps, lay.h.out(), nullptr, nullptr, false, T, D, s));
+      DF_CUDA(launch_residual_norm(kNormAdd, dt, lay.x, nullptr, lay.y, lay.sp_o,
+                                   use_ws ? lay.nsplit + 1 : nullptr, lw.g_post, cfg->rms_eps,
+                                   lay.h.out(), nullptr, block_valid, false, T, D, s));
     }
-    if (dt == DFLASH_DTYPE_BF16 && lay.sp_gu == 1) {
+    if (use_ws) {
       // SiLU(gate) * up is formed in the GEMM epilogue
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(launch_gemm_tc_swiglu(el, lay.h.p, D, lw.w_gate_up, D, T, I, D, flags,
+      DF_CUDA(launch_gemm_ws_swiglu(ws_args(lay.h.p, D, lw.w_gate_up, 2 * I, 1, nullptr),
+                                    lay.act.out(), s));
+    } else if (tc) {
+      Prof pr(DFLASH_PROF_GEMM, 1, s);
+      DF_CUDA(launch_gemm_tc_swiglu(DFLASH_DTYPE_F16, lay.h.p, D, lw.w_gate_up, D, T, I, D, flags,
                                     lay.act.out(), st, s));
     } else {
       {
         Prof pr(DFLASH_PROF_GEMM, 1, s);
-        DF_CUDA(gemm(dt, el, lay.h.p, D, lw.w_gate_up, D, lay.y, 2 * I, T, 2 * I, D, lay.sp_gu, s,
-                     flags));
+        DF_CUDA(gemm(dt, dt, lay.h.p, D, lw.w_gate_up, D, lay.y, 2 * I, T, 2 * I, D, lay.sp_gu, s));
       }
       Prof pr(DFLASH_PROF_ROWS, 1, s);
       DF_CUDA(launch_swiglu(lay.y, lay.sp_gu, lay.act.out(), T, I, s));
     }
     {
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(gemm(dt, el, lay.act.p, I, lw.w_down, I, lay.y, D, T, D, I, lay.sp_down, s, flags));
+      if (use_ws)
+        DF_CUDA(launch_gemm_ws(ws_args(lay.act.p, I, lw.w_down, D, lay.sp_down, lay.nsplit + 2), s));
+      else
+        DF_CUDA(gemm(dt, DFLASH_DTYPE_F16, lay.act.p, I, lw.w_down, I, lay.y, D, T, D, I,
+                     lay.sp_down, s, flags));
     }
     Prof pr(DFLASH_PROF_ROWS, 1, s);
     if (l + 1 < cfg->num_layers) {
       DF_CUDA(launch_residual_norm(kNormAdd, dt, lay.x, nullptr, lay.y, lay.sp_down,
+                                   use_ws ? lay.nsplit + 2 : nullptr,
                                    w->layers[l + 1].g_in, cfg->rms_eps, lay.h.out(), nullptr,
-                                   nullptr, false, T, D, s));
+                                   block_valid, false, T, D, s));
     } else {
-      DF_CUDA(launch_residual_norm(kNormFinal, dt, lay.x, nullptr, lay.y, lay.sp_down, w->g_final,
+      DF_CUDA(launch_residual_norm(kNormFinal, dt, lay.x, nullptr, lay.y, lay.sp_down,
+                                   use_ws ? lay.nsplit + 2 : nullptr, w->g_final,
                                    cfg->rms_eps, ActOut(), out, block_valid,
                                    (cfg->flags & DFLASH_FLAG_FINAL_NORM) != 0, T, D, s));
     }
@@ -718,6 +793,33 @@ int dflash_testing_gemm(int engine, int dtype, const void* A, long lda, const vo
 }
 
 int dflash_testing_gemm_splits(long M, int N, int K) { return gemm_splits(M, N, K); }
+
+int dflash_testing_gemm_ws(const void* X, long ldx, const void* W, int w_dtype, long ldw,
+                           float* C, long ldc, long M, int N, int K, int max_splits,
+                           const int32_t* tile_list, int32_t* splits_out, void* stream) {
+  if (M < 1 || N < 1 || K < 1 || !X || !W || !C || max_splits < 1 || max_splits > 8)
+    return fail(DFLASH_ERR_INVALID_ARG, "bad gemm_ws args");
+  if ((w_dtype != DFLASH_DTYPE_BF16 && w_dtype != DFLASH_DTYPE_F16) || ldx % 8 || ldw % 8 ||
+      ldx < K || ldw < K)
+    return fail(DFLASH_ERR_UNSUPPORTED, "gemm_ws needs bf16/fp16 weights and 16-byte rows");
+  WsArgs a;
+  a.X = X;
+  a.ldx = ldx;
+  a.M = M;
+  a.W = W;
+  a.w_dtype = w_dtype;
+  a.ldw = ldw;
+  a.Nw = N;
+  a.K = K;
+  a.tile_list = tile_list;
+  a.C = C;
+  a.ldc = ldc;
+  a.max_splits = max_splits;
+  a.splits_out = splits_out;
+  a.status = status_ptr();
+  DF_CUDA(launch_gemm_ws(a, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
 
 int dflash_profile_enable(int on) {
   std::lock_guard<std::mutex> lk(g_prof_mu);

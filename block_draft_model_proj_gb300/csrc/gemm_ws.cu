@@ -1,0 +1,633 @@
+// Weight-streaming projection GEMM of the draft layers on the 5th-generation tensor cores.
+//
+// C[z][t][n] (fp32) = sum over the K slice z of X[t][k] * W[n][k] for the token rows t of the
+// active 128-row tiles, computed transposed: D[n][t] = W[n, :] X[t, :]^T with the weight rows
+// as the MMA's M = 128 operand and up to 256 tokens (two 128-row token tiles) as N.  This
+// is the form of the draft
+// layers' projections ("DFlash Draft Body", How It Works step 3: QKV, O, gate/up, down; and
+// the per-layer context K/V projection of the "DFlash" page, How it works): a few hundred
+// to a few thousand tokens against 4096 x 4096 .. 24576 x 4096 weights.
+//
+//  * The weights arrive as bf16 (the model's own) or fp16 and are read from global memory
+//    exactly as given: TMA brings a 128 x 64 tile into shared memory, four converter warps
+//    turn it into fp16 (round to nearest even; exact for bf16 values of magnitude in
+//    [2^-14, 65504]) and store it into tensor memory, where the MMA reads its A operand
+//    (tcgen05.mma ... kind::f16 with A in tensor memory).  No converted copy of the
+//    weights ever exists in global memory.
+//  * The activations X are fp16 (their 11 significant bits keep the body within its error
+//    bound); TMA loads 128 x 64 tiles of the active token tiles only, two per unit, and the
+//    MMA's N covers only the rows present (16 for a 16-token decode step).
+//  * K is cut into `splits` slices when the (weight tile, token tile) units alone would
+//    leave SMs idle.  The count is chosen on the device from the number of active token
+//    tiles, written to *splits_out, and read by the kernel that sums the slices.
+//  * Epilogues: fp32 slices; SiLU(gate) * up (weight rows of a tile interleaved gate / up,
+//    so each pair of TMEM lanes holds one channel); the context K/V cache (a tile is one
+//    K or V head; K rows interleaved (i, i + 64) so RoPE pairs meet in neighbouring lanes).
+//
+// Warp roles (448 threads, one CTA per SM, persistent): warp 0 TMA producers (lane 0 the
+// weight ring, lane 1 the token ring); warp 1 MMA issuer; warps 2-9 converters in two
+// groups of four that take alternate K-steps; warps 10-13 epilogue.  Shared memory holds
+// two rings: weight tiles, freed as soon as the converters have read them, and token tiles,
+// freed by the MMA.  Tensor memory holds one 256-column accumulator and an 8-slot ring of
+// converted A tiles (32 columns each), so the conversion runs ahead of the MMA and the
+// weight tiles' load-and-convert latency stays off the token ring.  The converters and the
+// producers run ahead into the next unit while the epilogue drains.
+// Every mbarrier wait is bounded
+// in time; on expiry the CTA reports DFLASH_ERR_TIMEOUT, drains its own copies and MMAs,
+// frees its tensor memory and exits.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace dflash {
+namespace {
+
+using namespace tc;
+
+constexpr int kWM = 128;   // weight rows per unit (MMA M)
+constexpr int kTT = 128;   // rows of a token tile; a unit takes two (MMA N <= 256)
+constexpr int kBK = 64;    // K per stage
+constexpr int kMaxStages = 8;   // per ring
+constexpr int kASlots = 8;  // converted A tiles in tensor memory
+constexpr int kThreads = 448;
+constexpr uint32_t kWBytes = 128 * kBK * 2;             // 16 KB weight tile
+constexpr uint32_t kRingBytes = 196 * 1024;             // shared-memory ring budget
+constexpr uint32_t kTmemCols = 512;                     // acc 256, A ring 8 x 32
+constexpr uint32_t kTmemAcc = 0, kTmemA = 256;
+constexpr size_t kSmemBytes = 1024 + kRingBytes + 512;
+
+struct WsParams {
+  long M;            // token rows of X (and C)
+  int Nw;            // weight rows (output features)
+  int K;
+  int w_tiles;       // units along the weight rows
+  int m_tiles;       // 128-row token tiles (all)
+  int num_kb;
+  int max_splits;
+  int sms;
+  const int32_t* tile_list;  // optional: [0] = count, [1..] = active token tiles
+  int xrows;                 // rows of a token-tile load (128, or M rounded up to 16)
+  int two_tiles;             // units take two token tiles (M > 128)
+  int w_stages;              // weight ring stages (16 KB each)
+  int x_stages;              // token ring stages
+  uint32_t x_stage_bytes;    // token tile(s) of one K-step
+  int* splits_out;           // optional: the split count chosen on the device
+  int w_bf16;                // weights bf16 (converted here) or fp16
+  int interleave;            // TMEM lane 2i <- weight row i, lane 2i+1 <- row 64 + i:
+                             // 0 never, 1 always, 2 for the K heads of the K/V cache only
+  int epi;
+  float* C;
+  long ldc;
+  ActOut act;        // kEpiSwiGLU
+  int swiglu_I;
+  KvCacheEpilogue kv;  // kEpiKvCache
+  unsigned* status;
+};
+
+enum : int { kEpiF32 = 0, kEpiSwiGLU = 1, kEpiKvCache = 2 };
+
+// Split count for `units1` (weight tile, token tile) units of `kb` K-steps each: the fewest
+// waves over the SMs, weighing each unit's fixed cost as 6 K-steps; at least 8 K-steps per
+// slice.  Identical on every thread (and in the kernels that sum the slices).
+__host__ __device__ inline int ws_choose_splits(long units1, int kb, int max_splits, int sms) {
+  int best = 1;
+  long best_cost = -1;
+  for (int s = 1; s <= max_splits; ++s) {
+    const int per = (kb + s - 1) / s;
+    if ((kb + per - 1) / per != s) continue;  // that split count has an empty slice
+    if (s > 1 && per < 8) break;
+    const long waves = (units1 * s + sms - 1) / sms;
+    const long cost = waves * (per + 6);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+struct Sched {
+  int tiles;   // active token tiles
+  int pairs;   // units along the tokens: pairs of active token tiles
+  int splits;
+  int per;     // K-steps per slice
+  long units;
+};
+
+__device__ __forceinline__ Sched schedule(const WsParams& p) {
+  Sched s;
+  s.tiles = p.tile_list ? p.tile_list[0] : p.m_tiles;
+  s.pairs = p.two_tiles ? (s.tiles + 1) / 2 : s.tiles;
+  const long units1 = (long)p.w_tiles * s.pairs;
+  s.splits = ws_choose_splits(units1, p.num_kb, p.max_splits, p.sms);
+  s.per = (p.num_kb + s.splits - 1) / s.splits;
+  s.units = units1 * s.splits;
+  return s;
+}
+
+// A unit: weight tile wt, token tiles t0 and t1 (t1 < 0: none), K slice z.  The token
+// pairs of one weight tile are consecutive so the CTAs that share a weight tile run
+// together.  rows0 / rows1: token rows present in each tile.
+struct Unit {
+  int wt, t0, t1, z, rows0, rows1;
+};
+
+__device__ __forceinline__ Unit decode(const WsParams& p, const Sched& s, long u) {
+  Unit x;
+  const int pi = (int)(u % s.pairs);
+  const long rest = u / s.pairs;
+  x.wt = (int)(rest % p.w_tiles);
+  x.z = (int)(rest / p.w_tiles);
+  const int i0 = p.two_tiles ? 2 * pi : pi, i1 = 2 * pi + 1;
+  x.t0 = p.tile_list ? p.tile_list[1 + i0] : i0;
+  x.t1 = p.two_tiles && i1 < s.tiles ? (p.tile_list ? p.tile_list[1 + i1] : i1) : -1;
+  x.rows0 = (int)min((long)kTT, p.M - (long)x.t0 * kTT);
+  x.rows1 = x.t1 >= 0 ? (int)min((long)kTT, p.M - (long)x.t1 * kTT) : 0;
+  return x;
+}
+
+// MMA N of a unit: the rows present, rounded up to 16 (the second tile starts at column 128)
+__device__ __forceinline__ uint32_t unit_idesc(const Unit& x) {
+  const int n = x.t1 >= 0 ? kTT + ((x.rows1 + 15) & ~15) : ((x.rows0 + 15) & ~15);
+  return idesc_f16(kWM, n);
+}
+
+// bf16 pair -> fp16 pair (round to nearest even); `mag` collects the largest bf16 magnitude
+// bits of each half (a magnitude of 0x4780 or more, 65536 and up, leaves the fp16 range)
+__device__ __forceinline__ uint32_t cvt_pair(uint32_t w, bool bf16, uint32_t& mag) {
+  if (!bf16) return w;
+  mag = __vmaxu2(mag, w & 0x7FFF7FFFu);
+  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// ---- epilogues ---------------------------------------------------------------------------
+// The thread owns TMEM lane r (weight row of the unit) and reads the 128 token columns in
+// chunks of 32.
+
+__device__ __forceinline__ void epi_f32(const WsParams& p, uint32_t tacc, int wt, int tt, int rows,
+                                        int z, int r) {
+  float* Cz = p.C + (long)z * p.M * p.ldc;
+  const int n = wt * kWM + r;
+  const bool n_ok = n < p.Nw;
+#pragma unroll 1
+  for (int c = 0; c * 32 < rows; ++c) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(tacc + c * 32, v);
+    const long t0 = (long)tt * kTT + c * 32;
+    if (!n_ok) continue;
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j)
+      if (c * 32 + j < rows) Cz[(t0 + j) * p.ldc + n] = __uint_as_float(v[j]);
+  }
+}
+
+// Lanes 2i / 2i+1 hold gate / up of channel wt*64 + i.  The pair trades halves so that the
+// even lane forms tokens 0..15 and the odd lane tokens 16..31 of each chunk.
+__device__ __forceinline__ void epi_swiglu(const WsParams& p, uint32_t tacc, int wt, int tt,
+                                           int rows, int r, int lane) {
+  const int I = p.swiglu_I;
+  const int ch = wt * 64 + (r >> 1);
+  const bool odd = lane & 1;
+#pragma unroll 1
+  for (int c = 0; c * 32 < rows; ++c) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(tacc + c * 32, v);
+    const int j0 = c * 32 + (odd ? 16 : 0);
+    const long t0 = (long)tt * kTT + j0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float mine = __uint_as_float(odd ? v[j] : v[16 + j]);
+      const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+      const float g = odd ? other : __uint_as_float(v[j]);
+      const float u = odd ? __uint_as_float(v[16 + j]) : other;
+      if (ch < I && j0 + j < rows) p.act.store((t0 + j) * I + ch, g / (1.f + expf(-g)) * u);
+    }
+  }
+}
+
+// Context K/V cache.  Unit wt is head wt of the 2*Hkv K-then-V heads.  K: lanes 2i / 2i+1 hold
+// channels i / i+64 (interleaved), rotated by RoPE at the token's position and written to
+// rows [pos][dh]; V: lane d holds channel d, written to the transposed plane [dh][pos].
+__device__ __forceinline__ void epi_kv(const WsParams& p, uint32_t tacc, int wt, int tt, int rows,
+                                       int r, int lane, bool& bad) {
+  const KvCacheEpilogue& e = p.kv;
+  const long plane = (long)e.L_cache * 128;
+  const bool is_k = wt < e.Hkv;
+  const bool odd = lane & 1;
+  const long tend = (long)tt * kTT + rows;  // rows of this tile end here
+#pragma unroll 1
+  for (int c = 0; c * 32 < rows; ++c) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(tacc + c * 32, v);
+    const long tbase = (long)tt * kTT + c * 32;
+    if (is_k) {
+      const int i = r >> 1;  // frequency index; this pair holds channels i and i + 64
+#pragma unroll 4
+      for (int j = 0; j < 16; ++j) {
+        const float mine = __uint_as_float(odd ? v[j] : v[16 + j]);
+        const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+        const float x0 = odd ? other : __uint_as_float(v[j]);        // channel i
+        const float x1 = odd ? __uint_as_float(v[16 + j]) : other;   // channel i + 64
+        const long m = tbase + j + (odd ? 16 : 0);
+        if (m >= tend) continue;
+        const int b = (int)(m / e.L);
+        const int cpos = (int)(m - (long)b * e.L);
+        if (e.ctx_len && cpos >= e.ctx_len[b]) continue;
+        const float cs = e.cos_t[(long)cpos * 64 + i], sn = e.sin_t[(long)cpos * 64 + i];
+        const float a0 = x0 * cs - x1 * sn, a1 = x1 * cs + x0 * sn;
+        bad = bad || !(fmaxf(fabsf(a0), fabsf(a1)) + 0.f * (a0 + a1) < 65520.f);
+        __half* dst = e.kv + ((long)b * 2 * e.Hkv + wt) * plane + ((long)e.pos_offset + cpos) * 128;
+        dst[i] = __float2half_rn(a0);
+        dst[i + 64] = __float2half_rn(a1);
+      }
+    } else {
+      const int g = wt - e.Hkv;
+      // 8 consecutive tokens stay in one batch row (L % 8 == 0) and are 8 consecutive
+      // positions: one 16-byte store when the destination is aligned and all are kept
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        const long m0 = tbase + q * 8;
+        if (m0 >= tend) break;
+        const int b = (int)(m0 / e.L);
+        const int c0 = (int)(m0 - (long)b * e.L);
+        const int lim = e.ctx_len ? min(e.ctx_len[b], e.L) : e.L;
+        __half* dst = e.kv + ((long)b * 2 * e.Hkv + e.Hkv + g) * plane + (long)r * e.L_cache +
+                      e.pos_offset + c0;
+        float f[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          f[k] = __uint_as_float(v[q * 8 + k]);
+          bad = bad || !(fabsf(f[k]) < 65520.f);
+        }
+        if (c0 + 8 <= lim && m0 + 8 <= tend && ((e.pos_offset + c0) & 7) == 0) {
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const __half2 h = __floats2half2_rn(f[2 * k], f[2 * k + 1]);
+            w[k] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+          *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+          for (int k = 0; k < 8; ++k)
+            if (c0 + k < lim && m0 + k < tend) dst[k] = __float2half_rn(f[k]);
+        }
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
+               const WsParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int SW = p.w_stages, SX = p.x_stages;
+  uint8_t* wring = smem;                                  // SW x 16 KB
+  uint8_t* xring = smem + (size_t)SW * kWBytes;           // SX x x_stage_bytes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes);
+  uint64_t* wfull = bars;                   // weight tile landed
+  uint64_t* wempty = wfull + kMaxStages;    // converters done reading it
+  uint64_t* xfull = wempty + kMaxStages;    // token tiles landed
+  uint64_t* xempty = xfull + kMaxStages;    // MMA done with them
+  uint64_t* afull = xempty + kMaxStages;    // [8] converted A in tensor memory
+  uint64_t* aempty = afull + kASlots;       // [8] MMA done with the A slot
+  uint64_t* tfull = aempty + kASlots;       // accumulator ready
+  uint64_t* tempty = tfull + 1;             // accumulator drained
+  uint64_t* drain = tempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SW; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wempty[s], 4);
+    }
+    for (int s = 0; s < SX; ++s) {
+      mbar_init(&xfull[s], 1);
+      mbar_init(&xempty[s], 1);
+    }
+    for (int a = 0; a < kASlots; ++a) {
+      mbar_init(&afull[a], 4);
+      mbar_init(&aempty[a], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const Sched sc = schedule(p);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.splits_out) *p.splits_out = sc.splits;
+  const uint32_t xtile_bytes = (uint32_t)p.xrows * kBK * 2;
+
+  if (warp == 0) {
+    if (lane < 2) {
+      // ---------------- TMA producers: lane 0 weight tiles, lane 1 token tiles ----------------
+      const bool is_w = lane == 0;
+      const int S = is_w ? SW : SX;
+      uint64_t* full = is_w ? wfull : xfull;
+      uint64_t* empty = is_w ? wempty : xempty;
+      int stage = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      long n_issued = 0;
+      for (long u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
+        const Unit x = decode(p, sc, u);
+        const int kb0 = x.z * sc.per, kb1 = min(p.num_kb, kb0 + sc.per);
+        // a missing second tile is read past the last row: zeros, never stored
+        const int t1row = (x.t1 >= 0 ? x.t1 : p.m_tiles) * kTT;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
+          if (is_w) {
+            mbar_arrive_expect_tx(&full[stage], kWBytes);
+            uint8_t* dst = wring + (size_t)stage * kWBytes;
+            if (p.epi == kEpiSwiGLU) {  // 64 gate rows, then the 64 up rows of the same channels
+              tma_load_2d(&map_w, &full[stage], dst, kb * kBK, x.wt * 64);
+              tma_load_2d(&map_w, &full[stage], dst + kWBytes / 2, kb * kBK,
+                          p.swiglu_I + x.wt * 64);
+            } else {
+              tma_load_2d(&map_w, &full[stage], dst, kb * kBK, x.wt * kWM);
+            }
+          } else {
+            mbar_arrive_expect_tx(&full[stage], p.x_stage_bytes);
+            uint8_t* dst = xring + (size_t)stage * p.x_stage_bytes;
+            tma_load_2d(&map_x, &full[stage], dst, kb * kBK, x.t0 * kTT);
+            if (p.two_tiles) tma_load_2d(&map_x, &full[stage], dst + xtile_bytes, kb * kBK, t1row);
+          }
+          ++n_issued;
+          if (++stage == S) { stage = 0; ph ^= 1u; }
+        }
+      }
+      // wait for this thread's own copies still in flight (the last S issued)
+      for (long j = n_issued - S > 0 ? n_issued - S : 0; j < n_issued; ++j)
+        mbar_wait(&full[j % S], (uint32_t)((j / S) & 1), abort_flag, kWaitLimitNs / 4);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int stage = 0;  // token ring
+      uint32_t ph = 0;
+      long i = 0;  // K-step counter: A slot i % 8
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      for (long u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
+        const Unit x = decode(p, sc, u);
+        const int kb0 = x.z * sc.per, kb1 = min(p.num_kb, kb0 + sc.per);
+        const uint32_t idesc = unit_idesc(x);
+        if (!mbar_wait(tempty, acc_ph ^ 1u, abort_flag, kWaitLimitNs)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + kTmemAcc;
+        for (int kb = kb0; kb < kb1; ++kb, ++i) {
+          const int slot = (int)(i % kASlots);
+          if (!mbar_wait(&afull[slot], (uint32_t)((i / kASlots) & 1), abort_flag, kWaitLimitNs) ||
+              !mbar_wait(&xfull[stage], ph, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_tmem = tmem + kTmemA + (uint32_t)(slot * 32);
+          // the token tiles of a stage are consecutive: one K-major operand of 256 rows
+          const uint32_t x_addr = smem_u32(xring + (size_t)stage * p.x_stage_bytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            umma_f16_ts(d_tmem, a_tmem + k * 8, sw128_desc(x_addr + k * 32), idesc,
+                        (kb > kb0 || k > 0) ? 1u : 0u);
+          umma_commit(&xempty[stage]);
+          umma_commit(&aempty[slot]);
+          if (++stage == SX) { stage = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(tfull);
+        acc_ph ^= 1u;
+      }
+      umma_commit(drain);
+      mbar_wait(drain, 0, abort_flag, kWaitLimitNs / 4);
+    }
+  } else if (warp < 10) {
+    // ---------------- converters (warps 2..9): W tile -> fp16 A in tensor memory ----------------
+    // group g = 0 / 1 takes the K-steps with i % 2 == g; within a group, warp w covers TMEM
+    // lane quarter w % 4
+    const int group = (warp - 2) >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // TMEM lane = A row
+    const int srow_inter = (r & 1) ? 64 + (r >> 1) : (r >> 1);
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const bool wbf16 = p.w_bf16 != 0;
+    uint32_t mag = 0;
+    long i = 0;
+    bool ok = true;
+    for (long u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
+      const Unit x = decode(p, sc, u);
+      const bool inter = p.interleave == 1 || (p.interleave == 2 && x.wt < p.kv.Hkv);
+      const int srow = inter ? srow_inter : r;
+      const int kb0 = x.z * sc.per, kb1 = min(p.num_kb, kb0 + sc.per);
+      for (int kb = kb0; kb < kb1; ++kb, ++i) {
+        if ((int)(i & 1) != group) continue;
+        const int stage = (int)(i % SW);
+        const int slot = (int)(i % kASlots);
+        const bool got = mbar_wait(&wfull[stage], (uint32_t)((i / SW) & 1), abort_flag, kWaitLimitNs) &&
+                         mbar_wait(&aempty[slot], (uint32_t)(((i / kASlots) & 1) ^ 1), abort_flag,
+                                   kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, got ? 1 : 0)) { ok = false; break; }
+        tc_fence_after();
+        // row srow of the 128-byte-swizzled tile: 16-byte chunk c at chunk position c ^ (row % 8)
+        const uint8_t* row = wring + (size_t)stage * kWBytes + (srow >> 3) * 1024 + (srow & 7) * 128;
+        uint32_t a[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 w = *reinterpret_cast<const uint4*>(row + ((c ^ (srow & 7)) * 16));
+          a[4 * c] = cvt_pair(w.x, wbf16, mag);
+          a[4 * c + 1] = cvt_pair(w.y, wbf16, mag);
+          a[4 * c + 2] = cvt_pair(w.z, wbf16, mag);
+          a[4 * c + 3] = cvt_pair(w.w, wbf16, mag);
+        }
+        // the weight tile is in registers: hand the stage back before the tensor-memory store
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&wempty[stage]);
+        tmem_st_32x32b_x32(tmem + kTmemA + (uint32_t)(slot * 32) + lane_off, a);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&afull[slot]);
+      }
+    }
+    if ((mag & 0xFFFFu) >= 0x4780u || (mag >> 16) >= 0x4780u)
+      report(p.status, kStatusRange, kKernConvert);
+  } else {
+    // ---------------- epilogue (warps 10..13) ----------------
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    bool bad = false;
+    uint32_t acc_ph = 0;
+    for (long u = blockIdx.x; u < sc.units; u += gridDim.x) {
+      const Unit x = decode(p, sc, u);
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull, acc_ph, abort_flag, kWaitLimitNs) ? 1 : 0))
+        break;
+      tc_fence_after();
+      for (int h = 0; h < 2; ++h) {
+        const int tt = h ? x.t1 : x.t0;
+        const int rows = h ? x.rows1 : x.rows0;
+        if (tt < 0) break;
+        const uint32_t tacc = tmem + kTmemAcc + (uint32_t)(h * kTT) + lane_off;
+        if (p.epi == kEpiF32) epi_f32(p, tacc, x.wt, tt, rows, x.z, r);
+        else if (p.epi == kEpiSwiGLU) epi_swiglu(p, tacc, x.wt, tt, rows, r, lane);
+        else epi_kv(p, tacc, x.wt, tt, rows, r, lane, bad);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+      acc_ph ^= 1u;
+    }
+    if (bad) report(p.status, kStatusRange, kKernEpilogue);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 0 && *abort_flag) report(p.status, kStatusTimeout, kKernGemmTc);
+}
+
+// ---- host side ------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// [rows, cols] row-major 16-bit matrix, row stride ld elements; box = box_rows x 64 columns,
+// 128-byte swizzle, zero fill out of bounds
+bool encode_rows(CUtensorMap* map, const void* base, long rows, int cols, long ld, int box_rows,
+                 bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+cudaError_t launch(const WsArgs& a, int epi, int w_tiles, int interleave, const ActOut* act,
+                   const KvCacheEpilogue* kv, cudaStream_t stream) {
+  if (a.w_dtype != DFLASH_DTYPE_BF16 && a.w_dtype != DFLASH_DTYPE_F16) return cudaErrorInvalidValue;
+  if (((uintptr_t)a.X | (uintptr_t)a.W) % 16 != 0 || a.ldx % 8 != 0 || a.ldw % 8 != 0 ||
+      a.K < 1 || a.M < 1 || a.Nw < 1)
+    return cudaErrorInvalidValue;
+  CUtensorMap mw, mx;
+  const int wbox = epi == kEpiSwiGLU ? 64 : kWM;
+  if (!encode_rows(&mw, a.W, a.Nw, a.K, a.ldw, wbox, a.w_dtype == DFLASH_DTYPE_BF16))
+    return cudaErrorInvalidValue;
+  // token-tile loads: 128 rows, or all M rows (rounded up to 16) when M <= 128
+  const int xrows = a.M > kTT ? kTT : (int)((a.M + 15) / 16 * 16);
+  if (!encode_rows(&mx, a.X, a.M, a.K, a.ldx, xrows, false)) return cudaErrorInvalidValue;
+  WsParams p;
+  p.M = a.M;
+  p.Nw = a.Nw;
+  p.K = a.K;
+  p.w_tiles = w_tiles;
+  p.m_tiles = (int)((a.M + kTT - 1) / kTT);
+  p.num_kb = (a.K + kBK - 1) / kBK;
+  p.max_splits = epi == kEpiF32 ? (a.max_splits < 1 ? 1 : a.max_splits) : 1;
+  p.sms = sm_count();
+  p.tile_list = a.tile_list;
+  p.xrows = xrows;
+  p.two_tiles = a.M > kTT ? 1 : 0;
+  p.x_stage_bytes = (uint32_t)(p.two_tiles ? 2 : 1) * xrows * kBK * 2;
+  p.x_stages = p.x_stage_bytes <= 4096 ? kMaxStages : 4;
+  p.w_stages = (int)((kRingBytes - (uint32_t)p.x_stages * p.x_stage_bytes) / kWBytes);
+  if (p.w_stages > kMaxStages) p.w_stages = kMaxStages;
+  p.splits_out = a.splits_out;
+  p.w_bf16 = a.w_dtype == DFLASH_DTYPE_BF16;
+  p.interleave = interleave;
+  p.epi = epi;
+  p.C = a.C;
+  p.ldc = a.ldc;
+  if (act) p.act = *act;
+  p.swiglu_I = epi == kEpiSwiGLU ? a.Nw / 2 : 0;
+  if (kv) p.kv = *kv;
+  p.status = a.status;
+  // enough CTAs for the largest schedule the device can pick (all token tiles active)
+  long max_units = 0;
+  for (int s = 1; s <= p.max_splits; ++s) {
+    const long u = (long)w_tiles * (p.two_tiles ? (p.m_tiles + 1) / 2 : p.m_tiles) * s;
+    if (u > max_units) max_units = u;
+  }
+  const int grid = (int)(max_units < p.sms ? max_units : p.sms);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  gemm_ws_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mw, mx, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_ws_splits(long units1, int K, int max_splits) {
+  return ws_choose_splits(units1, (K + kBK - 1) / kBK, max_splits, sm_count());
+}
+
+cudaError_t launch_gemm_ws(const WsArgs& a, cudaStream_t stream) {
+  return launch(a, kEpiF32, (a.Nw + kWM - 1) / kWM, 0, nullptr, nullptr, stream);
+}
+
+cudaError_t launch_gemm_ws_swiglu(const WsArgs& a, const ActOut& act, cudaStream_t stream) {
+  if (a.Nw % 2 != 0) return cudaErrorInvalidValue;
+  // a unit covers 64 channels: its 64 gate rows and the 64 up rows of the same channels
+  // (rows past 2I read as zeros; channels past I are not stored)
+  return launch(a, kEpiSwiGLU, (a.Nw / 2 + 63) / 64, 1, &act, nullptr, stream);
+}
+
+cudaError_t launch_gemm_ws_kv_cache(const WsArgs& a, const KvCacheEpilogue& kv,
+                                    cudaStream_t stream) {
+  if (a.Nw != 2 * kv.Hkv * 128 || kv.L < 1 || kv.L % 8 != 0) return cudaErrorInvalidValue;
+  if (((uintptr_t)kv.kv | (uintptr_t)kv.cos_t | (uintptr_t)kv.sin_t) % 16 != 0)
+    return cudaErrorInvalidValue;
+  // K heads interleave their RoPE pairs; V heads keep the natural order
+  return launch(a, kEpiKvCache, 2 * kv.Hkv, 2, nullptr, &kv, stream);
+}
+
+}  // namespace dflash

@@ -42,11 +42,13 @@ enum NormMode { kNormInit = 0, kNormAdd = 1, kNormFinal = 2 };
 //  kNormInit : x = emb; h = RMSNorm(x) * g
 //  kNormAdd  : x += sum_s y[s]; h = RMSNorm(x) * g
 //  kNormFinal: x += sum_s y[s]; out = valid ? (final_norm ? RMSNorm(x) * g : x) : 0
-// y: nsplit partial results [nsplit][rows][D] (fp32); emb and g have type `dtype`.
+// y: nsplit partial results [nsplit][rows][D] (fp32; the count read from *nsplit_dev when
+// that is given); emb and g have type `dtype`.  With `valid`, a row of an invalid slot
+// writes zeros (h, or out) and reads nothing.
 cudaError_t launch_residual_norm(int mode, int dtype, float* x, const void* emb, const float* y,
-                                 int nsplit, const void* g, double eps, ActOut h, float* out,
-                                 const uint8_t* valid, bool final_norm, long rows, int D,
-                                 cudaStream_t stream);
+                                 int nsplit, const int* nsplit_dev, const void* g, double eps,
+                                 ActOut h, float* out, const uint8_t* valid, bool final_norm,
+                                 long rows, int D, cudaStream_t stream);
 
 // Plain RMSNorm of fp32 rows (the context norm); with_norm=false copies.  Rows r = b*L + c
 // with c >= ctx_len[b] are skipped when ctx_len is given (vectorised path).
@@ -57,8 +59,9 @@ cudaError_t launch_rows_norm(int dtype, const float* y, int nsplit, const void* 
 // QKV epilogue: y [nsplit][T][(Hq+2Hkv)*dh] fp32 -> attention-ready operands (fp16 when
 // f16, else fp32) q [B][Hkv][N][S][grp][dh], kb [B][Hkv][N*S][dh], vbt [B][Hkv][dh][ns_pad];
 // RoPE on q and k at position pos[t] (table of P positions; out-of-range valid slots report
-// a device check and use position 0).
-cudaError_t launch_qkv_rope(const float* y, int nsplit, const int32_t* pos, const uint8_t* valid,
+// a device check and use position 0).  nsplit_dev (optional) overrides nsplit.
+cudaError_t launch_qkv_rope(const float* y, int nsplit, const int* nsplit_dev, const int32_t* pos,
+                            const uint8_t* valid,
                             const float* cos_t, const float* sin_t, int P, void* q, void* kb,
                             void* vbt, int ns_pad, long T, int N, int S, int Hq, int Hkv, int dh,
                             bool f16, unsigned* status, cudaStream_t stream);
@@ -110,6 +113,36 @@ cudaError_t launch_gemm_tc_kv_cache(int elem, const void* A, long lda, const voi
 cudaError_t launch_gemm_tc(int elem, const void* A, long lda, const void* Bm, long ldb, float* C,
                            long ldc, long M, int N, int K, int splits, const int32_t* tile_list,
                            unsigned* status, cudaStream_t stream);
+
+// ---- gemm_ws.cu: weight-streaming tcgen05 GEMM of the draft layers ----
+// C[z][t][n] = X[t, Kz] W[n, Kz]^T over the active 128-row token tiles: X fp16 [M][K] (row
+// stride ldx), W bf16 or fp16 [Nw][K] (row stride ldw; converted to fp16 on the fly).  The
+// fp32 variant cuts K into up to max_splits slices (count chosen on the device, written to
+// *splits_out); the SwiGLU and K/V-cache variants never split.
+struct WsArgs {
+  const void* X = nullptr;
+  long ldx = 0;
+  long M = 0;
+  const void* W = nullptr;
+  int w_dtype = DFLASH_DTYPE_BF16;
+  long ldw = 0;
+  int Nw = 0;
+  int K = 0;
+  const int32_t* tile_list = nullptr;
+  float* C = nullptr;
+  long ldc = 0;
+  int max_splits = 1;
+  int* splits_out = nullptr;
+  unsigned* status = nullptr;
+};
+// Split count the device picks for units1 (weight tile, token tile) units and K.
+int gemm_ws_splits(long units1, int K, int max_splits);
+cudaError_t launch_gemm_ws(const WsArgs& a, cudaStream_t stream);
+// act[t][i] = SiLU(gate) * up, W = W_gate_up [2I][K] (gate rows, then up rows); Nw = 2I.
+cudaError_t launch_gemm_ws_swiglu(const WsArgs& a, const ActOut& act, cudaStream_t stream);
+// The context K/V cache of one layer from W = the K then V rows of w_qkv (Nw = 2*Hkv*128).
+cudaError_t launch_gemm_ws_kv_cache(const WsArgs& a, const KvCacheEpilogue& kv,
+                                    cudaStream_t stream);
 
 // ---- rows.cu: bf16 -> fp16 conversion (weights) ----
 // dst[i] = fp16(src[i]), round to nearest even; exact for bf16 values of magnitude in

@@ -50,11 +50,20 @@ __global__ void rope_table_kernel(float* __restrict__ cos_t, float* __restrict__
 
 __global__ void residual_norm_kernel(int mode, int dt, float* __restrict__ x,
                                      const void* __restrict__ emb, const float* __restrict__ y,
-                                     int nsplit, long split_stride, const void* __restrict__ g,
+                                     int nsplit, const int* __restrict__ nsplit_dev,
+                                     long split_stride, const void* __restrict__ g,
                                      float eps, ActOut h, float* __restrict__ out,
                                      const uint8_t* __restrict__ valid, bool final_norm, int D) {
   __shared__ float red[33];
   const long r = blockIdx.x;
+  if (nsplit_dev) nsplit = *nsplit_dev;
+  if (valid && valid[r] == 0) {  // an invalid slot: zero output / zero GEMM input, y unread
+    for (int c = threadIdx.x; c < D; c += blockDim.x) {
+      if (mode == kNormFinal) out[r * D + c] = 0.f;
+      else h.store(r * D + c, 0.f);
+    }
+    return;
+  }
   float* xr = x + r * D;
   float ss = 0.f;
   for (int c = threadIdx.x; c < D; c += blockDim.x) {
@@ -125,12 +134,23 @@ __device__ __forceinline__ float4 sum_splits4(const float* y, int nsplit, long s
 template <int kV>
 __global__ void residual_norm_vec_kernel(int mode, int dt, float* __restrict__ x,
                                          const void* __restrict__ emb, const float* __restrict__ y,
-                                         int nsplit, long split_stride, const void* __restrict__ g,
+                                         int nsplit, const int* __restrict__ nsplit_dev,
+                                         long split_stride, const void* __restrict__ g,
                                          float eps, ActOut h, float* __restrict__ out,
                                          const uint8_t* __restrict__ valid, bool final_norm, int D) {
   __shared__ float red[33];
   const long r = blockIdx.x;
   const int D4 = D / 4;
+  if (nsplit_dev) nsplit = *nsplit_dev;
+  if (valid && valid[r] == 0) {  // an invalid slot: zero output / zero GEMM input, y unread
+    for (int q = threadIdx.x; q < D4; q += blockDim.x) {
+      if (mode == kNormFinal)
+        *reinterpret_cast<float4*>(out + r * D + 4L * q) = make_float4(0.f, 0.f, 0.f, 0.f);
+      else
+        h.store4(r * D + 4L * q, make_float4(0.f, 0.f, 0.f, 0.f));
+    }
+    return;
+  }
   float4 v[kV];
   float ss = 0.f;
 #pragma unroll
@@ -236,12 +256,14 @@ __global__ void swiglu_vec_kernel(const float* __restrict__ y, int nsplit, long 
 //   kb  [B][Hkv][N*S][dh]         (block keys)
 //   vbt [B][Hkv][dh][ns_pad]      (block values, transposed)
 template <typename OutT>
-__global__ void qkv_rope_kernel(const float* __restrict__ y, int nsplit, long split_stride,
+__global__ void qkv_rope_kernel(const float* __restrict__ y, int nsplit,
+                                const int* __restrict__ nsplit_dev, long split_stride,
                                 const int32_t* __restrict__ pos, const uint8_t* __restrict__ valid,
                                 const float* __restrict__ cos_t, const float* __restrict__ sin_t,
                                 int P, OutT* __restrict__ q, OutT* __restrict__ kb,
                                 OutT* __restrict__ vbt, int ns_pad, long T, int N, int S, int Hq,
                                 int Hkv, int dh, unsigned* status) {
+  if (nsplit_dev) nsplit = *nsplit_dev;
   const int half = dh / 2;
   const int heads = Hq + 2 * Hkv;
   const int grp = Hq / Hkv;
@@ -371,9 +393,9 @@ cudaError_t launch_rope_table(float* cos_t, float* sin_t, int p0, int P, int hea
 }
 
 cudaError_t launch_residual_norm(int mode, int dtype, float* x, const void* emb, const float* y,
-                                 int nsplit, const void* g, double eps, ActOut h, float* out,
-                                 const uint8_t* valid, bool final_norm, long rows, int D,
-                                 cudaStream_t stream) {
+                                 int nsplit, const int* nsplit_dev, const void* g, double eps,
+                                 ActOut h, float* out, const uint8_t* valid, bool final_norm,
+                                 long rows, int D, cudaStream_t stream) {
   if (D % 4 == 0 && D <= 4 * 4 * 1024) {
     // a quarter of the row's float4 groups per thread: 4 independent 16-byte loads in
     // flight per thread and several rows per SM
@@ -381,18 +403,19 @@ cudaError_t launch_residual_norm(int mode, int dtype, float* x, const void* emb,
     const int threads = std::min(1024, std::max(32, ((D4 + 3) / 4 + 31) / 32 * 32));
     const int per = (D4 + threads - 1) / threads;
     if (per <= 1)
-      residual_norm_vec_kernel<1><<<rows, threads, 0, stream>>>(mode, dtype, x, emb, y, nsplit,
-                                                                rows * D, g, (float)eps, h, out,
-                                                                valid, final_norm, D);
+      residual_norm_vec_kernel<1><<<rows, threads, 0, stream>>>(
+          mode, dtype, x, emb, y, nsplit, nsplit_dev, rows * D, g, (float)eps, h, out, valid,
+          final_norm, D);
     else
-      residual_norm_vec_kernel<4><<<rows, threads, 0, stream>>>(mode, dtype, x, emb, y, nsplit,
-                                                                rows * D, g, (float)eps, h, out,
-                                                                valid, final_norm, D);
+      residual_norm_vec_kernel<4><<<rows, threads, 0, stream>>>(
+          mode, dtype, x, emb, y, nsplit, nsplit_dev, rows * D, g, (float)eps, h, out, valid,
+          final_norm, D);
     return cudaGetLastError();
   }
   const int threads = D >= 2048 ? 512 : 256;
-  residual_norm_kernel<<<rows, threads, 0, stream>>>(mode, dtype, x, emb, y, nsplit, rows * D, g,
-                                                     (float)eps, h, out, valid, final_norm, D);
+  residual_norm_kernel<<<rows, threads, 0, stream>>>(mode, dtype, x, emb, y, nsplit, nsplit_dev,
+                                                     rows * D, g, (float)eps, h, out, valid,
+                                                     final_norm, D);
   return cudaGetLastError();
 }
 
@@ -421,7 +444,8 @@ cudaError_t launch_rows_norm(int dtype, const float* y, int nsplit, const void* 
   return cudaGetLastError();
 }
 
-cudaError_t launch_qkv_rope(const float* y, int nsplit, const int32_t* pos, const uint8_t* valid,
+cudaError_t launch_qkv_rope(const float* y, int nsplit, const int* nsplit_dev, const int32_t* pos,
+                            const uint8_t* valid,
                             const float* cos_t, const float* sin_t, int P, void* q, void* kb,
                             void* vbt, int ns_pad, long T, int N, int S, int Hq, int Hkv, int dh,
                             bool f16, unsigned* status, cudaStream_t stream) {
@@ -429,11 +453,11 @@ cudaError_t launch_qkv_rope(const float* y, int nsplit, const int32_t* pos, cons
   const long stride = T * (long)(Hq + 2 * Hkv) * dh;
   if (f16)
     qkv_rope_kernel<__half><<<grid_for(n, 256), 256, 0, stream>>>(
-        y, nsplit, stride, pos, valid, cos_t, sin_t, P, static_cast<__half*>(q),
+        y, nsplit, nsplit_dev, stride, pos, valid, cos_t, sin_t, P, static_cast<__half*>(q),
         static_cast<__half*>(kb), static_cast<__half*>(vbt), ns_pad, T, N, S, Hq, Hkv, dh, status);
   else
     qkv_rope_kernel<float><<<grid_for(n, 256), 256, 0, stream>>>(
-        y, nsplit, stride, pos, valid, cos_t, sin_t, P, static_cast<float*>(q),
+        y, nsplit, nsplit_dev, stride, pos, valid, cos_t, sin_t, P, static_cast<float*>(q),
         static_cast<float*>(kb), static_cast<float*>(vbt), ns_pad, T, N, S, Hq, Hkv, dh, status);
   return cudaGetLastError();
 }
@@ -466,13 +490,29 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& bad) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-__global__ void convert_bf16_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                        long n8, const uint16_t* __restrict__ src_tail,
-                                        uint16_t* __restrict__ dst_tail, int tail,
-                                        unsigned* status) {
+__global__ void __launch_bounds__(256) convert_bf16_f16_kernel(
+    const uint4* __restrict__ src, uint4* __restrict__ dst, long n8,
+    const uint16_t* __restrict__ src_tail, uint16_t* __restrict__ dst_tail, int tail,
+    unsigned* status) {
   bool bad = false;
-  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n8;
-       i += (long)gridDim.x * blockDim.x) {
+  const long stride = (long)gridDim.x * blockDim.x;
+  long i = blockIdx.x * (long)blockDim.x + threadIdx.x;
+  // four independent 16-byte loads in flight per thread
+  for (; i + 3 * stride < n8; i += 4 * stride) {
+    uint4 w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) w[u] = __ldcs(src + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      uint4 o;
+      o.x = bf16x2_to_f16x2(w[u].x, bad);
+      o.y = bf16x2_to_f16x2(w[u].y, bad);
+      o.z = bf16x2_to_f16x2(w[u].z, bad);
+      o.w = bf16x2_to_f16x2(w[u].w, bad);
+      dst[i + u * stride] = o;
+    }
+  }
+  for (; i < n8; i += stride) {
     const uint4 w = __ldcs(src + i);
     uint4 o;
     o.x = bf16x2_to_f16x2(w.x, bad);
@@ -564,8 +604,8 @@ cudaError_t launch_convert_bf16_f16(const void* src, void* dst, size_t n, unsign
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  long blocks = (n8 + 255) / 256;
-  const long cap = (long)(sms > 0 ? sms : 1) * 8;
+  long blocks = (n8 + 1023) / 1024;
+  const long cap = (long)(sms > 0 ? sms : 1) * 4;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   convert_bf16_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(

@@ -54,6 +54,25 @@ def case_gemm(args):
           f"splits={args.splits}: {ms:.4f} ms/launch, {flops / ms / 1e9:.1f} TFLOP/s")
 
 
+def case_gemm_ws(args):
+    import torch
+    import block_draft_model_proj_gb300 as dflash
+    g = torch.Generator(device="cuda").manual_seed(0)
+    X = torch.randn((args.m, args.k), generator=g, device="cuda").to(torch.float16)
+    W = (torch.randn((args.n, args.k), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    C = torch.empty((args.splits, args.m, args.n), dtype=torch.float32, device="cuda")
+    so = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def run():
+        dflash.dflash_testing_gemm_ws(X, W, dflash.DFLASH_DTYPE_BF16, C, args.splits, so)
+    run()
+    dflash.dflash_device_status()
+    ms = _timed(run, args.iters)
+    flops = 2.0 * args.m * args.n * args.k
+    print(f"gemm_ws M={args.m} N={args.n} K={args.k} max_splits={args.splits} "
+          f"(chose {int(so.cpu()[0])}): {ms:.4f} ms/launch, {flops / ms / 1e9:.1f} TFLOP/s")
+
+
 def case_body(args):
     import torch
     import block_draft_model_proj_gb300 as dflash
@@ -69,8 +88,8 @@ def case_body(args):
         return torch.from_numpy(np.ascontiguousarray(t.data)).cuda()
     top = {k: dev(v) for k, v in di.gen_top_weights(w).items()}
     layers = [{k: dev(v) for k, v in di.gen_layer_weights(w, l).items()} for l in range(s.num_layers)]
-    wts = dflash.prepare_f16_layers(dflash.Weights(top, layers))
-    cfg = dflash.make_config(s, f16_layers=True)
+    wts = dflash.Weights(top, layers)
+    cfg = dflash.make_config(s)
     mask = torch.from_numpy(di.gen_mask(w)).cuda()
     sids = torch.from_numpy(di.gen_sample_ids(w)).cuda()
     H = dev(di.gen_target_hidden(w))
@@ -128,7 +147,7 @@ def case_verify(args):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["gemm", "body", "verify"])
+    ap.add_argument("case", choices=["gemm", "gemm_ws", "body", "verify"])
     ap.add_argument("--m", type=int, default=8192)
     ap.add_argument("--n", type=int, default=4096)
     ap.add_argument("--k", type=int, default=20480)
@@ -139,7 +158,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     from block_draft_model_proj_gb300 import build as b
     b.build()
-    {"gemm": case_gemm, "body": case_body, "verify": case_verify}[args.case](args)
+    {"gemm": case_gemm, "gemm_ws": case_gemm_ws, "body": case_body,
+     "verify": case_verify}[args.case](args)
 
 
 if __name__ == "__main__":

@@ -27,6 +27,18 @@ DFLASH_API int dflash_testing_gemm(int engine, int dtype, const void* A, long ld
                                    long ldb, float* C, long ldc, long M, int N, int K, int splits,
                                    void* stream);
 
+/* Weight-streaming projection GEMM of the draft layers (tcgen05 with the weight rows as the
+ * MMA's M operand, converted to fp16 in tensor memory): C[z] (float32, [splits][M][ldc]) =
+ * X[:, Kz] * W[:, Kz]^T for the token rows of the 128-row tiles in tile_list (device int32
+ * array: [0] = count, then tile indices; NULL = every tile).  X fp16 [M, K] (row stride ldx),
+ * W [N, K] of type w_dtype (DFLASH_DTYPE_BF16 or _F16; row stride ldw), strides multiples
+ * of 8 elements.  The device picks the split count (<= max_splits) and writes it to
+ * *splits_out (device int32).  Rows of unlisted tiles are left unwritten. */
+DFLASH_API int dflash_testing_gemm_ws(const void* X, long ldx, const void* W, int w_dtype,
+                                      long ldw, float* C, long ldc, long M, int N, int K,
+                                      int max_splits, const int32_t* tile_list,
+                                      int32_t* splits_out, void* stream);
+
 /* The K-split the library picks for an M x N x K projection on the current device. */
 DFLASH_API int dflash_testing_gemm_splits(long M, int N, int K);
 

@@ -102,3 +102,68 @@ def test_simt_gemm(lib, dtype, M, N, K, splits):
     import block_draft_model_proj_gb300 as dflash
     got, ref, K = run(dflash.DFLASH_TESTING_ENGINE_SIMT, dtype, M, N, K, splits)
     assert_close(got, ref, K)
+
+
+# ---- weight-streaming GEMM (weights as the M operand, bf16 -> fp16 in tensor memory) ----
+
+def run_ws(M, N, K, max_splits, w_dtype="bf16", tiles=None, seed=0, ldx_pad=0):
+    import torch
+    import block_draft_model_proj_gb300 as dflash
+    from dflash_testlib import np_to_device
+    rng = np.random.default_rng(seed)
+    x16 = rng.standard_normal((M, K + ldx_pad)).astype(np.float16)
+    w32 = rng.standard_normal((N, K), dtype=np.float32)
+    if w_dtype == "bf16":
+        wbits = di.f32_to_bf16_bits(w32)
+        dW = np_to_device(wbits.view(np.int16)).view(torch.bfloat16)
+        w64 = di.bf16_bits_to_f64(wbits)
+        dt = dflash.DFLASH_DTYPE_BF16
+    else:
+        w16 = w32.astype(np.float16)
+        dW = np_to_device(w16)
+        w64 = w16.astype(np.float64)
+        dt = dflash.DFLASH_DTYPE_F16
+    dX = np_to_device(x16)
+    dX = dX[:, :K] if ldx_pad else dX
+    C = torch.full((max_splits, M, N), float("nan"), dtype=torch.float32, device="cuda")
+    so = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tl = None
+    if tiles is not None:
+        tl = np_to_device(np.array([len(tiles)] + list(tiles), np.int32))
+    dflash.dflash_testing_gemm_ws(dX, dW, dt, C, max_splits, so, tl)
+    dflash.dflash_device_status()
+    s = int(so.cpu()[0])
+    assert 1 <= s <= max_splits
+    got = C[:s].cpu().numpy().astype(np.float64).sum(axis=0)
+    ref = x16[:, :K].astype(np.float64) @ w64.T
+    rows = np.arange(M) if tiles is None else np.concatenate(
+        [np.arange(t * 128, min((t + 1) * 128, M)) for t in tiles])
+    return got[rows], ref[rows], K, s
+
+
+WS_SHAPES = [
+    (128, 128, 64, 1),        # one unit, one K step
+    (300, 520, 200, 1),       # ragged tokens, weight rows and K
+    (16, 6144, 4096, 8),      # decode-shaped: splits chosen on the device
+    (384, 4096, 4096, 4),     # three token tiles, O-projection shape
+    (1000, 300, 4104, 3),     # K a multiple of 8 but not of 64
+    (2048, 2048, 512, 1),     # many units per CTA: both accumulators reused
+]
+
+
+@pytest.mark.parametrize("M,N,K,splits", WS_SHAPES)
+def test_weight_streaming_gemm_bf16_weights(lib, M, N, K, splits):
+    got, ref, K, _ = run_ws(M, N, K, splits)
+    assert_close(got, ref, K)
+
+
+@pytest.mark.parametrize("M,N,K,splits", [(300, 520, 200, 2), (16, 6144, 4096, 8)])
+def test_weight_streaming_gemm_f16_weights(lib, M, N, K, splits):
+    got, ref, K, _ = run_ws(M, N, K, splits, w_dtype="f16", seed=2)
+    assert_close(got, ref, K)
+
+
+def test_weight_streaming_gemm_tile_list_and_stride(lib):
+    # tiles 0 and 2 of four: the device schedule covers only those rows
+    got, ref, K, _ = run_ws(512, 768, 320, 4, tiles=[0, 2], seed=4, ldx_pad=64)
+    assert_close(got, ref, K)
