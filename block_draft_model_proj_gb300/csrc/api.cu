@@ -158,6 +158,8 @@ int check_cfg(const dflash_config_t* c) {
     return fail(DFLASH_ERR_INVALID_ARG, "num_heads (%d) must be a multiple of num_kv_heads (%d)",
                 c->num_heads, c->num_kv_heads);
   if (c->head_dim % 2 != 0) return fail(DFLASH_ERR_INVALID_ARG, "head_dim must be even");
+  if (c->head_dim % 8 != 0)
+    return fail(DFLASH_ERR_UNSUPPORTED, "head_dim must be a multiple of 8 (vectorised RoPE)");
   if (!(c->rope_theta > 0.0) || !(c->rms_eps >= 0.0))
     return fail(DFLASH_ERR_INVALID_ARG, "rope_theta must be > 0 and rms_eps >= 0");
   if ((c->flags & ~(DFLASH_FLAG_FINAL_NORM | DFLASH_FLAG_CTX_NORM | DFLASH_FLAG_F16_LAYERS)) != 0)
@@ -227,10 +229,10 @@ int check_ws(void* ws, size_t ws_bytes, size_t need) {
 // for the fp32 configuration.
 cudaError_t gemm(int dtype, int elem, const void* A, long lda, const void* Bm, long ldb, float* C,
                  long ldc, long M, int N, int K, int splits, cudaStream_t s,
-                 const int32_t* tile_list = nullptr) {
+                 const int32_t* tile_list = nullptr, int* splits_out = nullptr) {
   if (dtype == DFLASH_DTYPE_BF16)
     return launch_gemm_tc(elem, A, lda, Bm, ldb, C, ldc, M, N, K, splits, tile_list,
-                          status_ptr(), s);
+                          status_ptr(), s, splits_out);
   return launch_gemm_simt(dtype, A, lda, Bm, ldb, C, ldc, M, N, K, splits, s);
 }
 
@@ -274,10 +276,10 @@ bool convert_layers(const dflash_config_t* c, long tokens) {
          tokens > kWsMaxTokens;
 }
 
-// Upper bound for the device-chosen K-split of a weight-streaming GEMM: about three waves
-// of units when every token tile is active, at most 8.
-int ws_max_splits(int Nw, long T) {
-  const long units = (long)((Nw + 127) / 128) * ((T + 127) / 128);
+// Upper bound for a device-chosen K-split: about three waves of output tiles (tile_n
+// columns x 128 rows) when every row tile is active, at most 8.
+int ws_max_splits(int Nw, long T, int tile_n = 128) {
+  const long units = (long)((Nw + tile_n - 1) / tile_n) * ((T + 127) / 128);
   long s = (3L * num_sms() + units - 1) / units;
   return (int)(s < 1 ? 1 : (s > 8 ? 8 : s));
 }
@@ -342,11 +344,11 @@ BodyLayout body_layout(const dflash_config_t* c, int B, int L, int N, void* ws) 
     b.sp_o = ws_max_splits(D, T);
     b.sp_gu = 0;  // SiLU(gate) * up is formed in the GEMM epilogue
     b.sp_down = ws_max_splits(D, T);
-  } else if (c->dtype == DFLASH_DTYPE_BF16) {
-    b.sp_qkv = gemm_splits(T, qkvw, D);
-    b.sp_o = gemm_splits(T, D, qw);
+  } else if (c->dtype == DFLASH_DTYPE_BF16) {  // splits chosen on the device, these bound them
+    b.sp_qkv = ws_max_splits(qkvw, T, 256);
+    b.sp_o = ws_max_splits(D, T, 256);
     b.sp_gu = 0;
-    b.sp_down = gemm_splits(T, D, I);
+    b.sp_down = ws_max_splits(D, T, 256);
   } else {
     b.sp_qkv = gemm_splits(T, qkvw, D);
     b.sp_o = gemm_splits(T, D, qw);
@@ -636,11 +638,11 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
         DF_CUDA(launch_gemm_ws(ws_args(lay.h.p, D, lw.w_qkv, qkvw, lay.sp_qkv, lay.nsplit), s));
       else
         DF_CUDA(gemm(dt, DFLASH_DTYPE_F16, lay.h.p, D, lw.w_qkv, D, lay.y, qkvw, T, qkvw, D,
-                     lay.sp_qkv, s, flags));
+                     lay.sp_qkv, s, flags, tc ? lay.nsplit : nullptr));
     }
     {
       Prof pr(DFLASH_PROF_ROWS, 1, s);
-      DF_CUDA(launch_qkv_rope(lay.y, lay.sp_qkv, use_ws ? lay.nsplit : nullptr, position_ids,
+      DF_CUDA(launch_qkv_rope(lay.y, lay.sp_qkv, tc ? lay.nsplit : nullptr, position_ids,
                               block_valid, lay.cos_t, lay.sin_t,
                               lay.P, lay.q, lay.kb, lay.vbt, lay.ns_pad, T, N, S, Hq, Hkv, dh,
                               dt == DFLASH_DTYPE_BF16, st, s));
@@ -695,12 +697,12 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
         DF_CUDA(launch_gemm_ws(ws_args(lay.attn.p, qw, lw.w_o, D, lay.sp_o, lay.nsplit + 1), s));
       else
         DF_CUDA(gemm(dt, DFLASH_DTYPE_F16, lay.attn.p, qw, lw.w_o, qw, lay.y, D, T, D, qw, lay.sp_o,
-                     s, flags));
+                     s, flags, tc ? lay.nsplit + 1 : nullptr));
     }
     {
       Prof pr(DFLASH_PROF_ROWS, 1, s);
       DF_CUDA(launch_residual_norm(kNormAdd, dt, lay.x, nullptr, lay.y, lay.sp_o,
-                                   use_ws ? lay.nsplit + 1 : nullptr, lw.g_post, cfg->rms_eps,
+                                   tc ? lay.nsplit + 1 : nullptr, lw.g_post, cfg->rms_eps,
                                    lay.h.out(), nullptr, block_valid, false, T, D, s));
     }
     if (use_ws) {
@@ -726,17 +728,17 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
         DF_CUDA(launch_gemm_ws(ws_args(lay.act.p, I, lw.w_down, D, lay.sp_down, lay.nsplit + 2), s));
       else
         DF_CUDA(gemm(dt, DFLASH_DTYPE_F16, lay.act.p, I, lw.w_down, I, lay.y, D, T, D, I,
-                     lay.sp_down, s, flags));
+                     lay.sp_down, s, flags, tc ? lay.nsplit + 2 : nullptr));
     }
     Prof pr(DFLASH_PROF_ROWS, 1, s);
     if (l + 1 < cfg->num_layers) {
       DF_CUDA(launch_residual_norm(kNormAdd, dt, lay.x, nullptr, lay.y, lay.sp_down,
-                                   use_ws ? lay.nsplit + 2 : nullptr,
+                                   tc ? lay.nsplit + 2 : nullptr,
                                    w->layers[l + 1].g_in, cfg->rms_eps, lay.h.out(), nullptr,
                                    block_valid, false, T, D, s));
     } else {
       DF_CUDA(launch_residual_norm(kNormFinal, dt, lay.x, nullptr, lay.y, lay.sp_down,
-                                   use_ws ? lay.nsplit + 2 : nullptr, w->g_final,
+                                   tc ? lay.nsplit + 2 : nullptr, w->g_final,
                                    cfg->rms_eps, ActOut(), out, block_valid,
                                    (cfg->flags & DFLASH_FLAG_FINAL_NORM) != 0, T, D, s));
     }

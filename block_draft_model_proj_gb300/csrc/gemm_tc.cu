@@ -73,6 +73,8 @@ struct TcParams {
   long M;
   int N, K;
   int m_tiles, n_tiles, splits, kb_per_split, num_kb;
+  int* splits_out;  // non-null: splits is an upper bound, the count is chosen on the device
+  int sms;
   float* C;
   long ldc;
   const int32_t* tile_list;    // optional: [0] = count, [1..] = active M tiles in order
@@ -266,7 +268,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   const uint32_t tmem_base = *tmem_slot;
 
   const int m_cnt = active_m_tiles(p);
-  const int total = m_cnt * p.n_tiles * p.splits;
+  int n_splits = p.splits, kb_per = p.kb_per_split;
+  if (p.splits_out) {
+    n_splits = choose_splits((long)m_cnt * p.n_tiles, p.num_kb, p.splits, p.sms);
+    kb_per = (p.num_kb + n_splits - 1) / n_splits;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.splits_out = n_splits;
+  }
+  const int total = m_cnt * p.n_tiles * n_splits;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -280,8 +288,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         int m_t, n_t, z;
         decode_tile(p, m_cnt, t, m_t, n_t, z);
-        const int kb0 = z * p.kb_per_split;
-        const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+        const int kb0 = z * kb_per;
+        const int kb1 = min(p.num_kb, kb0 + kb_per);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], kTxBytes);
@@ -314,8 +322,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         int m_t, n_t, z;
         decode_tile(p, m_cnt, t, m_t, n_t, z);
-        const int kb0 = z * p.kb_per_split;
-        const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+        const int kb0 = z * kb_per;
+        const int kb1 = min(p.num_kb, kb0 + kb_per);
         if (!mbar_wait(&tempty[acc], acc_ph ^ 1u, abort_flag, kWaitLimitNs)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
@@ -469,7 +477,7 @@ cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const T
 
 cudaError_t launch_common(int elem, const void* A, long lda, const void* Bm, long ldb, float* C,
                           long ldc, long M, int N, int K, int splits, const int32_t* tile_list,
-                          unsigned* status, int epi, const KvCacheEpilogue* kv, const ActOut* act,
+                          unsigned* status, int* splits_out, int epi, const KvCacheEpilogue* kv, const ActOut* act,
                           cudaStream_t stream) {
   if (elem != DFLASH_DTYPE_BF16 && elem != DFLASH_DTYPE_F16) return cudaErrorInvalidValue;
   if (((uintptr_t)A | (uintptr_t)Bm) % 16 != 0) return cudaErrorInvalidValue;
@@ -494,6 +502,8 @@ cudaError_t launch_common(int elem, const void* A, long lda, const void* Bm, lon
   if (splits > p.num_kb) splits = p.num_kb;
   p.kb_per_split = (p.num_kb + splits - 1) / splits;
   p.splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;  // no empty split
+  p.splits_out = splits_out;
+  p.sms = sm_count();
   p.C = C;
   p.ldc = ldc;
   p.tile_list = tile_list;
@@ -514,9 +524,9 @@ cudaError_t launch_common(int elem, const void* A, long lda, const void* Bm, lon
 
 cudaError_t launch_gemm_tc(int elem, const void* A, long lda, const void* Bm, long ldb, float* C,
                            long ldc, long M, int N, int K, int splits, const int32_t* tile_list,
-                           unsigned* status, cudaStream_t stream) {
+                           unsigned* status, cudaStream_t stream, int* splits_out) {
   return launch_common(elem, A, lda, Bm, ldb, C, ldc, M, N, K, splits, tile_list, status,
-                       kEpiStoreF32, nullptr, nullptr, stream);
+                       splits_out, kEpiStoreF32, nullptr, nullptr, stream);
 }
 
 cudaError_t launch_gemm_tc_swiglu(int elem, const void* A, long lda, const void* Bm, long ldb,
@@ -524,6 +534,7 @@ cudaError_t launch_gemm_tc_swiglu(int elem, const void* A, long lda, const void*
                                   const ActOut& act, unsigned* status, cudaStream_t stream) {
   if (I < 1) return cudaErrorInvalidValue;
   return launch_common(elem, A, lda, Bm, ldb, nullptr, 0, M, 2 * I, K, 1, tile_list, status,
+                       nullptr,
                        kEpiSwiGLU, nullptr, &act, stream);
 }
 
@@ -534,7 +545,7 @@ cudaError_t launch_gemm_tc_kv_cache(int elem, const void* A, long lda, const voi
   if (N != 2 * kv.Hkv * 128 || kv.L < 1) return cudaErrorInvalidValue;
   if (((uintptr_t)kv.kv | (uintptr_t)kv.cos_t | (uintptr_t)kv.sin_t) % 16 != 0)
     return cudaErrorInvalidValue;
-  return launch_common(elem, A, lda, Bm, ldb, nullptr, 0, M, N, K, 1, tile_list, status,
+  return launch_common(elem, A, lda, Bm, ldb, nullptr, 0, M, N, K, 1, tile_list, status, nullptr,
                        kEpiKvCache, &kv, nullptr, stream);
 }
 

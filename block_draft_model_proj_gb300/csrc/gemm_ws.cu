@@ -88,26 +88,6 @@ struct WsParams {
 
 enum : int { kEpiF32 = 0, kEpiSwiGLU = 1, kEpiKvCache = 2 };
 
-// Split count for `units1` (weight tile, token tile) units of `kb` K-steps each: the fewest
-// waves over the SMs, weighing each unit's fixed cost as 6 K-steps; at least 8 K-steps per
-// slice.  Identical on every thread (and in the kernels that sum the slices).
-__host__ __device__ inline int ws_choose_splits(long units1, int kb, int max_splits, int sms) {
-  int best = 1;
-  long best_cost = -1;
-  for (int s = 1; s <= max_splits; ++s) {
-    const int per = (kb + s - 1) / s;
-    if ((kb + per - 1) / per != s) continue;  // that split count has an empty slice
-    if (s > 1 && per < 8) break;
-    const long waves = (units1 * s + sms - 1) / sms;
-    const long cost = waves * (per + 6);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best = s;
-    }
-  }
-  return best;
-}
-
 struct Sched {
   int tiles;   // active token tiles
   int pairs;   // units along the tokens: pairs of active token tiles
@@ -121,7 +101,7 @@ __device__ __forceinline__ Sched schedule(const WsParams& p) {
   s.tiles = p.tile_list ? p.tile_list[0] : p.m_tiles;
   s.pairs = p.two_tiles ? (s.tiles + 1) / 2 : s.tiles;
   const long units1 = (long)p.w_tiles * s.pairs;
-  s.splits = ws_choose_splits(units1, p.num_kb, p.max_splits, p.sms);
+  s.splits = choose_splits(units1, p.num_kb, p.max_splits, p.sms);
   s.per = (p.num_kb + s.splits - 1) / s.splits;
   s.units = units1 * s.splits;
   return s;
@@ -607,7 +587,7 @@ cudaError_t launch(const WsArgs& a, int epi, int w_tiles, int interleave, const 
 }  // namespace
 
 int gemm_ws_splits(long units1, int K, int max_splits) {
-  return ws_choose_splits(units1, (K + kBK - 1) / kBK, max_splits, sm_count());
+  return choose_splits(units1, (K + kBK - 1) / kBK, max_splits, sm_count());
 }
 
 cudaError_t launch_gemm_ws(const WsArgs& a, cudaStream_t stream) {

@@ -84,6 +84,27 @@ cudaError_t launch_gemm_simt(int dtype, const void* A, long lda, const void* Bm,
                              float* C, long ldc, long M, int N, int K, int splits,
                              cudaStream_t stream);
 
+// K-split for `units1` output tiles of `kb` K-steps each, at most max_splits: the fewest
+// waves over `sms` SMs, weighing each tile's fixed cost as 6 K-steps; at least 8 K-steps
+// per slice; never an empty slice.  The GEMMs that choose on the device and the kernels
+// that sum their slices call it with the same arguments.
+__host__ __device__ inline int choose_splits(long units1, int kb, int max_splits, int sms) {
+  int best = 1;
+  long best_cost = -1;
+  for (int s = 1; s <= max_splits; ++s) {
+    const int per = (kb + s - 1) / s;
+    if ((kb + per - 1) / per != s) continue;
+    if (s > 1 && per < 8) break;
+    const long waves = (units1 * s + sms - 1) / sms;
+    const long cost = waves * (per + 6);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
 // ---- gemm_tc.cu: tcgen05 16-bit GEMM, fp32 output, optional K-split ----
 // elem = DFLASH_DTYPE_BF16 (A and B bf16) or DFLASH_DTYPE_F16 (A and B fp16).
 // tile_list (optional, device): [0] = count, [1..] = the 128-row M tiles to compute, in
@@ -110,9 +131,11 @@ cudaError_t launch_gemm_tc_kv_cache(int elem, const void* A, long lda, const voi
                                     long M, int N, int K, const int32_t* tile_list,
                                     const KvCacheEpilogue& kv, unsigned* status,
                                     cudaStream_t stream);
+// splits_out == nullptr: exactly `splits` K-slices.  Otherwise at most `splits`, the count
+// chosen on the device from the active M tiles (choose_splits) and written to *splits_out.
 cudaError_t launch_gemm_tc(int elem, const void* A, long lda, const void* Bm, long ldb, float* C,
                            long ldc, long M, int N, int K, int splits, const int32_t* tile_list,
-                           unsigned* status, cudaStream_t stream);
+                           unsigned* status, cudaStream_t stream, int* splits_out = nullptr);
 
 // ---- gemm_ws.cu: weight-streaming tcgen05 GEMM of the draft layers ----
 // C[z][t][n] = X[t, Kz] W[n, Kz]^T over the active 128-row token tiles: X fp16 [M][K] (row

@@ -249,54 +249,62 @@ __global__ void swiglu_vec_kernel(const float* __restrict__ y, int nsplit, long 
 }
 
 
-// One thread per (row t, head, channel pair i).  Writes the attention operands in the
-// attention-ready layouts (OutT: fp32 for the CUDA-core attention, fp16 for the tensor-core
-// attention):
+// Attention operands in their attention-ready layouts (OutT: fp32 for the CUDA-core
+// attention, fp16 for the tensor-core attention):
 //   q   [B][Hkv][N][S][grp][dh]   (the query rows of one KV head are contiguous per block)
 //   kb  [B][Hkv][N*S][dh]         (block keys)
 //   vbt [B][Hkv][dh][ns_pad]      (block values, transposed)
+// Invalid slots get zero operands: they are never keys, and their GEMM rows may have been
+// skipped (unwritten) when a whole 128-row tile held no valid slot.
+
+__device__ __forceinline__ void store4(float* dst, float4 v) { *reinterpret_cast<float4*>(dst) = v; }
+__device__ __forceinline__ void store4(__half* dst, float4 v) {
+  const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+  uint2 w;
+  w.x = *reinterpret_cast<const uint32_t*>(&a);
+  w.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(dst) = w;
+}
+
+// Q and K heads with RoPE: one thread per (row t, head, 4 consecutive pairs i .. i+3), the
+// pairs (i, i + dh/2) rotated by the angle of position pos[t].  dh % 8 == 0.
 template <typename OutT>
-__global__ void qkv_rope_kernel(const float* __restrict__ y, int nsplit,
-                                const int* __restrict__ nsplit_dev, long split_stride,
-                                const int32_t* __restrict__ pos, const uint8_t* __restrict__ valid,
-                                const float* __restrict__ cos_t, const float* __restrict__ sin_t,
-                                int P, OutT* __restrict__ q, OutT* __restrict__ kb,
-                                OutT* __restrict__ vbt, int ns_pad, long T, int N, int S, int Hq,
-                                int Hkv, int dh, unsigned* status) {
+__global__ void qk_rope_kernel(const float* __restrict__ y, int nsplit,
+                               const int* __restrict__ nsplit_dev, long split_stride,
+                               const int32_t* __restrict__ pos, const uint8_t* __restrict__ valid,
+                               const float* __restrict__ cos_t, const float* __restrict__ sin_t,
+                               int P, OutT* __restrict__ q, OutT* __restrict__ kb, long T, int N,
+                               int S, int Hq, int Hkv, int dh, unsigned* status) {
   if (nsplit_dev) nsplit = *nsplit_dev;
-  const int half = dh / 2;
-  const int heads = Hq + 2 * Hkv;
+  const int half = dh / 2, q4 = half / 4;
+  const int heads = Hq + Hkv;  // Q then K heads (V is transposed by v_transpose_kernel)
   const int grp = Hq / Hkv;
-  const long width = (long)heads * dh;
-  const long n = T * heads * half;
+  const long width = (long)(Hq + 2 * Hkv) * dh;
+  const long n = T * heads * q4;
   for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n;
        e += (long)gridDim.x * blockDim.x) {
-    const long t = e / ((long)heads * half);
-    const int rem = (int)(e - t * heads * half);
-    const int hd = rem / half, i = rem - hd * half;
+    const long t = e / ((long)heads * q4);
+    const int rem = (int)(e - t * heads * q4);
+    const int hd = rem / q4, i = (rem - hd * q4) * 4;
     const long base = t * width + (long)hd * dh;
-    // invalid slots get zero operands: they are never keys, and their GEMM rows may have
-    // been skipped (unwritten) when a whole 128-row tile held no valid slot
     const bool vt = valid[t] != 0;
-    const float a = vt ? sum_splits(y, nsplit, split_stride, base + i) : 0.f;
-    const float bb = vt ? sum_splits(y, nsplit, split_stride, base + i + half) : 0.f;
+    const float4 a = vt ? sum_splits4(y, nsplit, split_stride, base + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 bb = vt ? sum_splits4(y, nsplit, split_stride, base + i + half)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
     const int b = (int)(t / ((long)N * S));
     const int ks = (int)(t - (long)b * N * S);  // k * S + j
     const int k = ks / S, j = ks - k * S;
-    if (hd >= Hq + Hkv) {  // V: no rotation, transposed
-      const int g = hd - Hq - Hkv;
-      OutT* dst = vbt + ((long)(b * Hkv + g) * dh) * ns_pad + ks;
-      dst[(long)i * ns_pad] = from_f<OutT>(a);
-      dst[(long)(i + half) * ns_pad] = from_f<OutT>(bb);
-      continue;
-    }
     int pp = pos[t];
     if (pp < 0 || pp >= P) {
       if (vt && i == 0) report(status, kStatusCheck, kKernEpilogue);
       pp = 0;
     }
-    const float c = cos_t[(long)pp * half + i], sn = sin_t[(long)pp * half + i];
-    const float lo = a * c - bb * sn, hi = bb * c + a * sn;
+    const float4 c = *reinterpret_cast<const float4*>(cos_t + (long)pp * half + i);
+    const float4 sn = *reinterpret_cast<const float4*>(sin_t + (long)pp * half + i);
+    const float4 lo = make_float4(a.x * c.x - bb.x * sn.x, a.y * c.y - bb.y * sn.y,
+                                  a.z * c.z - bb.z * sn.z, a.w * c.w - bb.w * sn.w);
+    const float4 hi = make_float4(bb.x * c.x + a.x * sn.x, bb.y * c.y + a.y * sn.y,
+                                  bb.z * c.z + a.z * sn.z, bb.w * c.w + a.w * sn.w);
     OutT* dst;
     if (hd < Hq) {
       const int g = hd / grp, h = hd - g * grp;
@@ -305,8 +313,45 @@ __global__ void qkv_rope_kernel(const float* __restrict__ y, int nsplit,
       const int g = hd - Hq;
       dst = kb + ((((long)b * Hkv + g) * N + k) * S + j) * dh;
     }
-    dst[i] = from_f<OutT>(lo);
-    dst[i + half] = from_f<OutT>(hi);
+    store4(dst + i, lo);
+    store4(dst + i + half, hi);
+  }
+}
+
+// V heads, transposed through shared memory: one block per (row b, KV head g, 32 slots);
+// reads 32 rows x dh channels (coalesced along the channels) and writes dh rows of 32
+// slots of vbt (coalesced along the slots).  dh <= 256.
+constexpr int kVtSlots = 32;
+template <typename OutT>
+__global__ void __launch_bounds__(256) v_transpose_kernel(
+    const float* __restrict__ y, int nsplit, const int* __restrict__ nsplit_dev, long split_stride,
+    const uint8_t* __restrict__ valid, OutT* __restrict__ vbt, int ns_pad, int N, int S, int Hq,
+    int Hkv, int dh) {
+  __shared__ float tile[kVtSlots][257];
+  if (nsplit_dev) nsplit = *nsplit_dev;
+  const int NS = N * S;
+  const int tiles = (NS + kVtSlots - 1) / kVtSlots;
+  const int bt = blockIdx.x % tiles;
+  const int bg = blockIdx.x / tiles;  // b * Hkv + g
+  const int b = bg / Hkv, g = bg - b * Hkv;
+  const int ks0 = bt * kVtSlots;
+  const long width = (long)(Hq + 2 * Hkv) * dh;
+  const int vcol = (Hq + Hkv + g) * dh;
+  for (int idx = threadIdx.x; idx < kVtSlots * dh; idx += blockDim.x) {
+    const int jj = idx / dh, d = idx - jj * dh;
+    const int ks = ks0 + jj;
+    float v = 0.f;
+    if (ks < NS) {
+      const long t = (long)b * NS + ks;
+      if (valid[t]) v = sum_splits(y, nsplit, split_stride, t * width + vcol + d);
+    }
+    tile[jj][d] = v;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < dh * kVtSlots; idx += blockDim.x) {
+    const int d = idx / kVtSlots, jj = idx - d * kVtSlots;
+    const int ks = ks0 + jj;
+    if (ks < ns_pad) vbt[((long)bg * dh + d) * ns_pad + ks] = from_f<OutT>(tile[jj][d]);
   }
 }
 
@@ -445,20 +490,27 @@ cudaError_t launch_rows_norm(int dtype, const float* y, int nsplit, const void* 
 }
 
 cudaError_t launch_qkv_rope(const float* y, int nsplit, const int* nsplit_dev, const int32_t* pos,
-                            const uint8_t* valid,
-                            const float* cos_t, const float* sin_t, int P, void* q, void* kb,
-                            void* vbt, int ns_pad, long T, int N, int S, int Hq, int Hkv, int dh,
-                            bool f16, unsigned* status, cudaStream_t stream) {
-  const long n = T * (Hq + 2 * Hkv) * (dh / 2);
+                            const uint8_t* valid, const float* cos_t, const float* sin_t, int P,
+                            void* q, void* kb, void* vbt, int ns_pad, long T, int N, int S, int Hq,
+                            int Hkv, int dh, bool f16, unsigned* status, cudaStream_t stream) {
+  if (dh % 8 != 0 || dh > 256) return cudaErrorInvalidValue;
+  const long n = T * (Hq + Hkv) * (dh / 8);
   const long stride = T * (long)(Hq + 2 * Hkv) * dh;
-  if (f16)
-    qkv_rope_kernel<__half><<<grid_for(n, 256), 256, 0, stream>>>(
+  const long B = T / ((long)N * S);
+  const int vblocks = (int)(B * Hkv * ((N * S + kVtSlots - 1) / kVtSlots));
+  if (f16) {
+    qk_rope_kernel<__half><<<grid_for(n, 256), 256, 0, stream>>>(
         y, nsplit, nsplit_dev, stride, pos, valid, cos_t, sin_t, P, static_cast<__half*>(q),
-        static_cast<__half*>(kb), static_cast<__half*>(vbt), ns_pad, T, N, S, Hq, Hkv, dh, status);
-  else
-    qkv_rope_kernel<float><<<grid_for(n, 256), 256, 0, stream>>>(
+        static_cast<__half*>(kb), T, N, S, Hq, Hkv, dh, status);
+    v_transpose_kernel<__half><<<vblocks, 256, 0, stream>>>(
+        y, nsplit, nsplit_dev, stride, valid, static_cast<__half*>(vbt), ns_pad, N, S, Hq, Hkv, dh);
+  } else {
+    qk_rope_kernel<float><<<grid_for(n, 256), 256, 0, stream>>>(
         y, nsplit, nsplit_dev, stride, pos, valid, cos_t, sin_t, P, static_cast<float*>(q),
-        static_cast<float*>(kb), static_cast<float*>(vbt), ns_pad, T, N, S, Hq, Hkv, dh, status);
+        static_cast<float*>(kb), T, N, S, Hq, Hkv, dh, status);
+    v_transpose_kernel<float><<<vblocks, 256, 0, stream>>>(
+        y, nsplit, nsplit_dev, stride, valid, static_cast<float*>(vbt), ns_pad, N, S, Hq, Hkv, dh);
+  }
   return cudaGetLastError();
 }
 

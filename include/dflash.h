@@ -77,7 +77,7 @@ extern "C" {
 #define DFLASH_FLAG_F16_LAYERS 4u
 
 /* Draft model shape ([P1] "Configuration"; the attention/MLP sizes of the draft layers).
- * num_heads % num_kv_heads == 0; head_dim even.  The bf16 configuration also needs
+ * num_heads % num_kv_heads == 0; head_dim a multiple of 8.  The bf16 configuration also needs
  * head_dim == 128, block_size * num_heads / num_kv_heads dividing 128, num_heads /
  * num_kv_heads dividing 16, and every matrix row width a multiple of 8
  * (DFLASH_ERR_UNSUPPORTED otherwise). */
