@@ -337,15 +337,25 @@ __global__ void __launch_bounds__(256) v_transpose_kernel(
   const int ks0 = bt * kVtSlots;
   const long width = (long)(Hq + 2 * Hkv) * dh;
   const int vcol = (Hq + Hkv + g) * dh;
-  for (int idx = threadIdx.x; idx < kVtSlots * dh; idx += blockDim.x) {
-    const int jj = idx / dh, d = idx - jj * dh;
-    const int ks = ks0 + jj;
-    float v = 0.f;
-    if (ks < NS) {
-      const long t = (long)b * NS + ks;
-      if (valid[t]) v = sum_splits(y, nsplit, split_stride, t * width + vcol + d);
+  // eight independent loads in flight per thread before they are stored
+  for (int idx0 = threadIdx.x; idx0 < kVtSlots * dh; idx0 += 8 * blockDim.x) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int idx = idx0 + u * blockDim.x;
+      const int jj = idx / dh, d = idx - jj * dh;
+      const int ks = ks0 + jj;
+      v[u] = 0.f;
+      if (idx < kVtSlots * dh && ks < NS) {
+        const long t = (long)b * NS + ks;
+        if (valid[t]) v[u] = sum_splits(y, nsplit, split_stride, t * width + vcol + d);
+      }
     }
-    tile[jj][d] = v;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int idx = idx0 + u * blockDim.x;
+      if (idx < kVtSlots * dh) tile[idx / dh][idx % dh] = v[u];
+    }
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < dh * kVtSlots; idx += blockDim.x) {
@@ -656,8 +666,20 @@ cudaError_t launch_convert_bf16_f16(const void* src, void* dst, size_t n, unsign
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // at most two CTAs per SM: enough bytes in flight for HBM, and room left beside them for
+  // a GEMM running concurrently on another stream
   long blocks = (n8 + 1023) / 1024;
-  const long cap = (long)(sms > 0 ? sms : 1) * 4;
+  const long cap = (long)(sms > 0 ? sms : 1) * 2;
+  // the SM's shared-memory carveout set to the maximum, as the tensor-core kernels use it:
+  // an SM holding these CTAs can then take a GEMM CTA at the same time
+  static bool carveout = false;
+  if (!carveout) {
+    cudaError_t e = cudaFuncSetAttribute(convert_bf16_f16_kernel,
+                                         cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    carveout = true;
+  }
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   convert_bf16_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(

@@ -73,6 +73,8 @@ def compare_hidden(got: np.ndarray, ref: np.ndarray, valid: np.ndarray, tol: dic
     stats = {"max_abs": float(np.max(np.abs(err))),
              "rel_rms": float(np.sqrt(np.sum(err * err) / max(np.sum(r * r), 1e-300))),
              "n": int(valid.sum())}
+    print(f"parity: max_abs={stats['max_abs']:.3e} rel_rms={stats['rel_rms']:.3e} "
+          f"over {stats['n']} slots")
     assert np.all(np.isfinite(g))
     assert stats["max_abs"] <= tol["max_abs"], stats
     assert stats["rel_rms"] <= tol["rel_rms"], stats
