@@ -86,6 +86,9 @@ struct AttnTcParams {
   float* part_l;  // [units][128]
   unsigned* status;
   float scale_log2;
+  int direct;   // one key chunk: the unit normalises and writes the output rows itself
+  int Hq;
+  ActOut out;   // [T][Hq*dh], written directly when `direct`
 };
 
 struct UnitInfo {
@@ -470,8 +473,33 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[i % kSP]);
     }
-    // final accumulator -> partial (m, l, O) of this unit; each half writes its 64 columns
-    if (ok && wait_all(&pv_done[(u.n - 1) % kSP], (uint32_t)((u.n - 1) / kSP) & 1u)) {
+    // final accumulator: with one key chunk, O / l straight to the output rows; otherwise a
+    // partial (m, l, O) of this unit.  Each half handles its 64 columns.
+    const bool fin = ok && wait_all(&pv_done[(u.n - 1) % kSP], (uint32_t)((u.n - 1) / kSP) & 1u);
+    if (fin && p.direct) {
+      tc_fence_after();
+      red_sum[half * 128 + r] = l_run;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sum_bar);
+      const bool sum_ok = wait_all(sum_bar, 0);
+      const float l = l_run + red_sum[(1 - half) * 128 + r];
+      // invalid slots of an existing block get exact zeros (the O projection reads them)
+      const float inv = sum_ok && row_valid && l > 0.f ? 1.f / l : 0.f;
+      const bool row_exists = kbo < p.bpt && kb < u.k1;
+      const int h = within - j * p.grp;
+      const long orow = (((long)u.b * p.N + kb) * p.S + j) * (long)p.Hq * kDH +
+                        (long)(u.g * p.grp + h) * kDH + half * 64;
+      for (int part = 0; part < 2; ++part) {
+        uint32_t ov[32];
+        tmem_ld_32x32b_x32(tmem_o + lane_off + half * 64 + part * 32, ov);
+        if (!row_exists) continue;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          p.out.store4(orow + part * 32 + 4 * e,
+                       make_float4(__uint_as_float(ov[4 * e]) * inv, __uint_as_float(ov[4 * e + 1]) * inv,
+                                   __uint_as_float(ov[4 * e + 2]) * inv, __uint_as_float(ov[4 * e + 3]) * inv));
+      }
+    } else if (fin) {
       tc_fence_after();
       const size_t rowi = (size_t)blockIdx.x * kM + r;
       float4* po = reinterpret_cast<float4*>(p.part_o + rowi * kDH + half * 64);
@@ -600,6 +628,11 @@ AttnTcLayout attention_tc_layout(int B, int N, int S, int L, int Hq, int Hkv, in
   const double per_unit = (double)L * B * Hkv * lay.tiles / (4.0 * (num_sms > 0 ? num_sms : 1));
   lay.chunk = 256;
   while (lay.chunk < 4096 && lay.chunk < per_unit) lay.chunk *= 2;
+  // one chunk when the (row, KV head, tile) units alone fill the SMs and no unit is long
+  // (each then normalises its own output: no partials, no combine pass)
+  const long base_units = (long)B * Hkv * lay.tiles;
+  if (L <= 4096 && base_units >= (num_sms > 0 ? num_sms : 1))
+    lay.chunk = (L + kKT - 1) / kKT * kKT;
   lay.max_chunks = (L + lay.chunk - 1) / lay.chunk;
   if (lay.max_chunks < 1) lay.max_chunks = 1;
   lay.units = (long)B * Hkv * lay.tiles * lay.max_chunks;
@@ -640,6 +673,9 @@ cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream) {
   p.part_l = p.part_m + lay.units * kM;
   p.status = a.status;
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)kDH));
+  p.direct = lay.max_chunks == 1 ? 1 : 0;
+  p.Hq = a.Hq;
+  p.out = a.out;
 
   CUtensorMap mkc, mvc, mkb, mvb;
   const long planes = (long)a.B * 2 * a.Hkv;
@@ -677,7 +713,7 @@ cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream) {
   }
   attn_tc_kernel<<<(unsigned)lay.units, kThreads, kSmemBytes, stream>>>(mkc, mvc, mkb, mvb, p);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || p.direct) return e;
   const long rows = (long)a.B * a.Hkv * lay.tiles * kM;
   const int threads = 256;
   const long blocks = (rows * 32 + threads - 1) / threads;
