@@ -183,23 +183,18 @@ class GpuStep:
         self._dev = dev
         top = di.gen_top_weights(model_w)
         layers = [di.gen_layer_weights(model_w, l) for l in range(s.num_layers)]
-        wts_given = dflash.Weights({k: dev(v) for k, v in top.items()},
-                                   [{k: dev(v) for k, v in lw.items()} for lw in layers])
-        # bf16 configuration: the layer GEMMs of many tokens read fp16 copies of the bf16
-        # layer matrices (DFLASH_FLAG_F16_LAYERS).  The training workloads refresh them inside
-        # every step (the weights change with every optimizer step); inference prepares them
-        # once, with the model.
-        self.f16 = s.dtype == "bf16"
-        self.conv_first, self.conv_rest = [], []
-        if self.f16:
-            self.wts = dflash.prepare_f16_layers(wts_given)
-            for lg, lp in zip(wts_given.tensors[1], self.wts.tensors[1]):
-                # w_qkv feeds the context K/V projection; the other three only the body
-                self.conv_first.append((lg["w_qkv"], lp["w_qkv"]))
-                self.conv_rest += [(lg[k], lp[k]) for k in ("w_o", "w_gate_up", "w_down")]
-        else:
-            self.wts = wts_given
-        self.cfg = dflash.make_config(s, f16_layers=self.f16)
+        # the model's bf16 weights as given: the training workloads pass them to every call
+        # (the weights change with every optimizer step; the library converts what its
+        # large-token GEMMs need inside the call).  Inference prepares fp16 copies of the layer
+        # matrices once, with the model (DFLASH_FLAG_F16_LAYERS).
+        self.wts_bf16 = dflash.Weights({k: dev(v) for k, v in top.items()},
+                                       [{k: dev(v) for k, v in lw.items()} for lw in layers])
+        self.cfg_bf16 = dflash.make_config(s)
+        self.wts_f16, self.cfg_f16 = self.wts_bf16, self.cfg_bf16
+        if s.dtype == "bf16":
+            self.wts_f16 = dflash.prepare_f16_layers(self.wts_bf16)
+            self.cfg_f16 = dflash.make_config(s, f16_layers=True)
+        self.use_f16_weights(w.inference)
         # host inputs (pinned for the end-to-end leg) and their device copies
         self.h_mask = torch.from_numpy(di.gen_mask(w)).pin_memory()
         self.h_sids = torch.from_numpy(di.gen_sample_ids(w)).pin_memory()
@@ -253,11 +248,9 @@ class GpuStep:
                              (() if w.inference else (self.h_hidden,)))
         self.d2h_bytes = sum(t.numel() * t.element_size() for t in (self.h_out, self.h_em, self.h_ne))
         self.stream = torch.cuda.current_stream(device)
-        # the body-only layer matrices are converted on a side stream while the context
-        # projection (tensor-core bound) runs on the main one
-        self.side = torch.cuda.Stream(device)
-        self.ev_fork = torch.cuda.Event()
-        self.ev_join = torch.cuda.Event()
+
+    def use_f16_weights(self, on: bool):
+        self.wts, self.cfg = (self.wts_f16, self.cfg_f16) if on else (self.wts_bf16, self.cfg_bf16)
 
     def build_cache(self):
         """The projected context of the inference workloads: built once, outside timing."""
@@ -276,21 +269,10 @@ class GpuStep:
                                    self.S - 1, self.V, -1, self.em, self.ne, self.ac, ws=self.ws,
                                    stream=st)
             return
-        self.ev_fork.record(self.stream)
-        for src, dst in self.conv_first:
-            d.dflash_convert_bf16_to_f16(src, dst, stream=st)
         d.dflash_plan(self.d_mask, self.d_sids, w.plan_step, w.plan_seed, self.N, self.S,
                       self.anchors, self.bv, self.lm, self.pid, ctx_len=self.ctx_len, stream=st)
         d.dflash_project_context(self.cfg, self.wts, self.d_hidden, self.B, self.L, 0, self.L,
                                  self.kv, ctx_len=self.ctx_len, ws=self.ws, stream=st)
-        if self.conv_rest:
-            # enqueued after the projection so its GEMM takes the SMs first and the
-            # conversion fills the thread slots it leaves
-            self.side.wait_event(self.ev_fork)
-            for src, dst in self.conv_rest:
-                d.dflash_convert_bf16_to_f16(src, dst, stream=self.side.cuda_stream)
-            self.ev_join.record(self.side)
-            self.stream.wait_event(self.ev_join)
         d.dflash_body_forward(self.cfg, self.wts, self.d_emb, self.anchors, self.bv, self.pid,
                               self.d_mask, self.kv, self.B, self.L, self.N, self.out, ws=self.ws,
                               stream=st)
@@ -363,15 +345,20 @@ def run_ours(args, rank, world, local_rank):
         work["gemm_flops"] -= work["proj_flops"] + work["ctxkv_flops"]
         work["total_flops"] -= work["proj_flops"] + work["ctxkv_flops"]
 
+    # headline: the step as a user runs it (no per-kernel events between the launches, which
+    # would serialise the programmatically dependent launches)
     sampler = ClockSampler(local_rank)
     launches0 = dflash.dflash_launch_count()
-    dflash.dflash_profile_enable(True)
     sampler.start()
     ms = timed(g.step, args.steps, torch, stream, barrier)
     clocks = sampler.stop()
+    launches = dflash.dflash_launch_count() - launches0
+    dflash.dflash_device_status()
+    # per-kernel split: the same steps again with CUDA events around every launch
+    dflash.dflash_profile_enable(True)
+    prof_ms = timed(g.step, args.steps, torch, stream, barrier)
     prof = dflash.dflash_profile_read()
     dflash.dflash_profile_enable(False)
-    launches = dflash.dflash_launch_count() - launches0
     dflash.dflash_device_status()
 
     # end to end: host buffers in, results out, inside the timed region
@@ -383,13 +370,12 @@ def run_ours(args, rank, world, local_rank):
     # as fp16 by the trainer (its optimizer writes the fp16 working copy), i.e. without the
     # per-step bf16 -> fp16 conversion that the headline number includes
     held_ms = 0.0
-    if g.conv_first or g.conv_rest:
-        saved = (g.conv_first, g.conv_rest)
-        g.conv_first, g.conv_rest = [], []
+    if not w.inference and w.shape.dtype == "bf16":
+        g.use_f16_weights(True)
         for _ in range(2):
             g.step()
         held_ms = timed(g.step, args.steps, torch, stream, barrier)
-        g.conv_first, g.conv_rest = saved
+        g.use_f16_weights(False)
 
     t = torch.tensor([ms, e2e_ms, held_ms], dtype=torch.float64, device=device)
     if world > 1:
@@ -411,8 +397,8 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f16",
         "precision": "bf16 inputs and weights; W_proj bf16 x bf16, draft-layer projections "
-                     "f16 x f16 (fp16 copies of the bf16 layer weights, refreshed inside every "
-                     "training step; fp16 activations), "
+                     "f16 x f16 (bf16 weight tiles converted to fp16 on chip for <= 512 tokens, "
+                     "fp16 copies converted inside the call above that; fp16 activations), "
                      "fp32 accumulation and residual stream, attention f16 x f16 over an "
                      "fp16 context K/V cache",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, bf16)",
@@ -438,6 +424,7 @@ def run_ours(args, rank, world, local_rank):
                           "achieved_tflops": work["total_flops"] / step_s / 1e12,
                           "frac_of_sustained_bf16": work["total_flops"] / step_s / 1e12 / peak},
         "kernel_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
+        "profiled_ms_per_step": prof_ms / args.steps,
         "clocks": clocks,
         "gpu_launches": launches,
         "e2e": {"value": e2e_value, "unit": "block-positions/s",
@@ -451,8 +438,9 @@ def run_ours(args, rank, world, local_rank):
             "value": units / (held_ms / 1e3), "unit": "block-positions/s",
             "ms_per_step": held_ms / args.steps,
             "frac_of_sustained_bf16": work["total_flops"] / held_s / 1e12 / peak,
-            "note": "same step without the per-step bf16->fp16 conversion of the layer weights "
-                    "(a trainer whose optimizer writes the fp16 working copy); not the headline"}
+            "note": "same step with fp16 copies of the layer weights held by the trainer (its "
+                    "optimizer writes the fp16 working copy) instead of the bf16 weights; not "
+                    "the headline"}
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(base, g.h_mask.numpy(), g.h_sids.numpy())
     return result

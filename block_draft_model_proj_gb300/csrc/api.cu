@@ -265,15 +265,22 @@ int layer_wdtype(const dflash_config_t* c) {
   return (c->flags & DFLASH_FLAG_F16_LAYERS) ? DFLASH_DTYPE_F16 : DFLASH_DTYPE_BF16;
 }
 
-// Layer projections of at most this many tokens (a decode step) run on the weight-streaming
-// GEMM, which reads bf16 weights as given; larger ones on the 128 x 256-tile GEMM, which
-// takes fp16 weights (the caller's, or copies converted at the start of the call).
-constexpr long kWsMaxTokens = 128;
+// Which GEMM runs the layer projections of a call with `tokens` rows.  The weight-streaming
+// GEMM reads the weights as given (bf16 tiles converted on chip); the 128 x 256-tile GEMM
+// is faster per FLOP from a few hundred tokens up but takes fp16 weights (the caller's,
+// or copies converted at the start of the call, one extra read and write of every matrix).
+// Up to 128 tokens the weight-streaming GEMM is faster outright; up to 512 it is cheaper
+// than converting bf16 weights; above that the conversion pays for itself.
+bool layer_gemm_ws(const dflash_config_t* c, long tokens) {
+  if (c->dtype != DFLASH_DTYPE_BF16) return false;
+  if (tokens <= 128) return true;
+  return layer_wdtype(c) == DFLASH_DTYPE_BF16 && tokens <= 512;
+}
 
 // fp16 copies of the layer matrices are made inside the call (bf16 weights, large calls)
 bool convert_layers(const dflash_config_t* c, long tokens) {
   return c->dtype == DFLASH_DTYPE_BF16 && layer_wdtype(c) == DFLASH_DTYPE_BF16 &&
-         tokens > kWsMaxTokens;
+         !layer_gemm_ws(c, tokens);
 }
 
 // Upper bound for a device-chosen K-split: about three waves of output tiles (tile_n
@@ -338,7 +345,7 @@ BodyLayout body_layout(const dflash_config_t* c, int B, int L, int N, void* ws) 
   const long T = (long)B * N * c->block_size;
   const int D = c->hidden, qw = c->num_heads * c->head_dim, kw = c->num_kv_heads * c->head_dim;
   const int qkvw = qw + 2 * kw, I = c->intermediate;
-  b.ws = c->dtype == DFLASH_DTYPE_BF16 && T <= kWsMaxTokens;
+  b.ws = layer_gemm_ws(c, T);
   if (b.ws) {
     b.sp_qkv = ws_max_splits(qkvw, T);
     b.sp_o = ws_max_splits(D, T);

@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant__ CUtensorMap map_vc,
                const __grid_constant__ CUtensorMap map_kb, const __grid_constant__ CUtensorMap map_vb,
                const AttnTcParams p) {
+  pdl_wait();
   const UnitInfo u = decode_unit(p, blockIdx.x);
   if (u.n == 0) return;  // a chunk past this tile's longest prefix: no work
 
@@ -174,6 +175,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the successor grid may be scheduled once this CTA holds its tensor memory
+  pdl_trigger();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tmem_q = tmem + kTmemQ, tmem_o = tmem + kTmemO, tmem_s0 = tmem + kTmemS;
 
@@ -531,6 +534,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
 // One warp per query row of a tile: merge the chunk partials in chunk order, normalise,
 // write the attention output row [t][(g*grp + h)*dh ...].
 __global__ void attn_combine_kernel(const AttnTcParams p, ActOut out, int Hq) {
+  pdl_wait();
+  pdl_trigger();
   const int warps = blockDim.x >> 5;
   const long gw = (long)blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -711,13 +716,21 @@ cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  attn_tc_kernel<<<(unsigned)lay.units, kThreads, kSmemBytes, stream>>>(mkc, mvc, mkb, mvb, p);
+  {
+    const cudaError_t le = launch_pdl(attn_tc_kernel, dim3((unsigned)lay.units), dim3(kThreads),
+        kSmemBytes, stream, mkc, mvc, mkb, mvb, p);
+    if (le != cudaSuccess) return le;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.direct) return e;
   const long rows = (long)a.B * a.Hkv * lay.tiles * kM;
   const int threads = 256;
   const long blocks = (rows * 32 + threads - 1) / threads;
-  attn_combine_kernel<<<(unsigned)blocks, threads, 0, stream>>>(p, a.out, a.Hq);
+  {
+    const cudaError_t le = launch_pdl(attn_combine_kernel, dim3((unsigned)blocks), dim3(threads), 0,
+        stream, p, a.out, a.Hq);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 

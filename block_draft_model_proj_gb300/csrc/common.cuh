@@ -122,6 +122,17 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return red[32];
 }
 
+// ---- programmatic dependent launch ----------------------------------------------------------
+// Kernels of the hot path are launched with programmatic stream serialization: a kernel may
+// start (its prologue, its launch latency) while its predecessor on the stream finishes.
+// pdl_wait() blocks until every predecessor grid has completed and its memory is visible;
+// each such kernel calls it before its first global-memory access.  pdl_trigger() lets the
+// successor grid be scheduled once every CTA of this grid has called it (or exited).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- time-bounded waits ----------------------------------------------------------------
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;

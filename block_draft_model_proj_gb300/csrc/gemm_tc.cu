@@ -266,6 +266,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // prologue done (barriers, tensor memory): wait for the predecessor grid's results, then
+  // let the successor grid be scheduled
+  pdl_wait();
+  pdl_trigger();
 
   const int m_cnt = active_m_tiles(p);
   int n_splits = p.splits, kb_per = p.kb_per_split;
@@ -471,8 +475,8 @@ cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const T
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_tc_kernel<kEpi><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, p);
-  return cudaGetLastError();
+  return launch_pdl(gemm_tc_kernel<kEpi>, dim3(grid), dim3(kThreads), kSmemBytes, stream, ma, mb,
+                    p);
 }
 
 cudaError_t launch_common(int elem, const void* A, long lda, const void* Bm, long ldb, float* C,

@@ -308,6 +308,10 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // prologue done (barriers, tensor memory): wait for the predecessor grid's results, then
+  // let the successor grid be scheduled
+  pdl_wait();
+  pdl_trigger();
 
   const Sched sc = schedule(p);
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.splits_out) *p.splits_out = sc.splits;
@@ -580,8 +584,7 @@ cudaError_t launch(const WsArgs& a, int epi, int w_tiles, int interleave, const 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_ws_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mw, mx, p);
-  return cudaGetLastError();
+  return launch_pdl(gemm_ws_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, mw, mx, p);
 }
 
 }  // namespace

@@ -57,6 +57,8 @@ plan_kernel(const uint8_t* __restrict__ mask, const int64_t* __restrict__ sids, 
             uint64_t step, uint64_t seed, int N, int S, int32_t* __restrict__ anchors,
             uint8_t* __restrict__ block_valid, uint8_t* __restrict__ loss_mask,
             int32_t* __restrict__ position_ids, int32_t* __restrict__ ctx_len) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ unsigned hist[256];
   __shared__ int warp_counts[kPlanThreads / 32];
   __shared__ int sh_sel_digit, sh_remaining, sh_cut, sh_equal;
@@ -208,8 +210,11 @@ cudaError_t launch_plan(const uint8_t* mask, const int64_t* sids, int B, int L, 
                         uint64_t seed, int N, int S, int32_t* anchors, uint8_t* block_valid,
                         uint8_t* loss_mask, int32_t* position_ids, int32_t* ctx_len,
                         cudaStream_t stream) {
-  plan_kernel<<<B, kPlanThreads, 0, stream>>>(mask, sids, B, L, step, seed, N, S, anchors,
-                                              block_valid, loss_mask, position_ids, ctx_len);
+  {
+    const cudaError_t le = launch_pdl(plan_kernel, dim3(B), dim3(kPlanThreads), 0, stream, mask,
+        sids, B, L, step, seed, N, S, anchors, block_valid, loss_mask, position_ids, ctx_len);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 

@@ -34,6 +34,8 @@ struct InvFreq {
 
 __global__ void rope_table_kernel(float* __restrict__ cos_t, float* __restrict__ sin_t, int p0,
                                   int P, int half, const InvFreq inv) {
+  pdl_wait();
+  pdl_trigger();
   const long n = (long)P * half;
   for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n;
        e += (long)gridDim.x * blockDim.x) {
@@ -54,6 +56,8 @@ __global__ void residual_norm_kernel(int mode, int dt, float* __restrict__ x,
                                      long split_stride, const void* __restrict__ g,
                                      float eps, ActOut h, float* __restrict__ out,
                                      const uint8_t* __restrict__ valid, bool final_norm, int D) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[33];
   const long r = blockIdx.x;
   if (nsplit_dev) nsplit = *nsplit_dev;
@@ -94,6 +98,8 @@ __global__ void residual_norm_kernel(int mode, int dt, float* __restrict__ x,
 __global__ void rows_norm_kernel(int dt, const float* __restrict__ y, int nsplit, long split_stride,
                                  const void* __restrict__ g, float eps, bool with_norm, ActOut out,
                                  int D) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[33];
   const long r = blockIdx.x;
   float ss = 0.f;
@@ -138,6 +144,8 @@ __global__ void residual_norm_vec_kernel(int mode, int dt, float* __restrict__ x
                                          long split_stride, const void* __restrict__ g,
                                          float eps, ActOut h, float* __restrict__ out,
                                          const uint8_t* __restrict__ valid, bool final_norm, int D) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[33];
   const long r = blockIdx.x;
   const int D4 = D / 4;
@@ -201,6 +209,8 @@ __global__ void rows_norm_vec_kernel(int dt, const float* __restrict__ y, int ns
                                      long split_stride, const void* __restrict__ g, float eps,
                                      bool with_norm, ActOut out, int D,
                                      const int32_t* __restrict__ ctx_len, int L) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[33];
   const long r = blockIdx.x;
   // context rows no block reads (c >= ctx_len[b]) are left unwritten
@@ -275,6 +285,8 @@ __global__ void qk_rope_kernel(const float* __restrict__ y, int nsplit,
                                const float* __restrict__ cos_t, const float* __restrict__ sin_t,
                                int P, OutT* __restrict__ q, OutT* __restrict__ kb, long T, int N,
                                int S, int Hq, int Hkv, int dh, unsigned* status) {
+  pdl_wait();
+  pdl_trigger();
   if (nsplit_dev) nsplit = *nsplit_dev;
   const int half = dh / 2, q4 = half / 4;
   const int heads = Hq + Hkv;  // Q then K heads (V is transposed by v_transpose_kernel)
@@ -327,6 +339,8 @@ __global__ void __launch_bounds__(256) v_transpose_kernel(
     const float* __restrict__ y, int nsplit, const int* __restrict__ nsplit_dev, long split_stride,
     const uint8_t* __restrict__ valid, OutT* __restrict__ vbt, int ns_pad, int N, int S, int Hq,
     int Hkv, int dh) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float tile[kVtSlots][257];
   if (nsplit_dev) nsplit = *nsplit_dev;
   const int NS = N * S;
@@ -443,7 +457,11 @@ cudaError_t launch_rope_table(float* cos_t, float* sin_t, int p0, int P, int hea
   InvFreq inv;
   for (int i = 0; i < half; ++i) inv.v[i] = pow(theta, -2.0 * (double)i / (double)head_dim);
   const long n = (long)P * half;
-  rope_table_kernel<<<grid_for(n, 256), 256, 0, stream>>>(cos_t, sin_t, p0, P, half, inv);
+  {
+    const cudaError_t le = launch_pdl(rope_table_kernel, dim3(grid_for(n, 256)), dim3(256), 0,
+        stream, cos_t, sin_t, p0, P, half, inv);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
@@ -458,19 +476,28 @@ cudaError_t launch_residual_norm(int mode, int dtype, float* x, const void* emb,
     const int threads = std::min(1024, std::max(32, ((D4 + 3) / 4 + 31) / 32 * 32));
     const int per = (D4 + threads - 1) / threads;
     if (per <= 1)
-      residual_norm_vec_kernel<1><<<rows, threads, 0, stream>>>(
-          mode, dtype, x, emb, y, nsplit, nsplit_dev, rows * D, g, (float)eps, h, out, valid,
-          final_norm, D);
+      {
+    const cudaError_t le = launch_pdl(residual_norm_vec_kernel<1>, dim3(rows), dim3(threads), 0,
+        stream, mode, dtype, x, emb, y, nsplit, nsplit_dev, rows * D, g, (float)eps, h, out, valid,
+        final_norm, D);
+    if (le != cudaSuccess) return le;
+  }
     else
-      residual_norm_vec_kernel<4><<<rows, threads, 0, stream>>>(
-          mode, dtype, x, emb, y, nsplit, nsplit_dev, rows * D, g, (float)eps, h, out, valid,
-          final_norm, D);
+      {
+    const cudaError_t le = launch_pdl(residual_norm_vec_kernel<4>, dim3(rows), dim3(threads), 0,
+        stream, mode, dtype, x, emb, y, nsplit, nsplit_dev, rows * D, g, (float)eps, h, out, valid,
+        final_norm, D);
+    if (le != cudaSuccess) return le;
+  }
     return cudaGetLastError();
   }
   const int threads = D >= 2048 ? 512 : 256;
-  residual_norm_kernel<<<rows, threads, 0, stream>>>(mode, dtype, x, emb, y, nsplit, nsplit_dev,
-                                                     rows * D, g, (float)eps, h, out, valid,
-                                                     final_norm, D);
+  {
+    const cudaError_t le = launch_pdl(residual_norm_kernel, dim3(rows), dim3(threads), 0, stream,
+        mode, dtype, x, emb, y, nsplit, nsplit_dev, rows * D, g, (float)eps, h, out, valid,
+        final_norm, D);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
@@ -484,18 +511,25 @@ cudaError_t launch_rows_norm(int dtype, const float* y, int nsplit, const void* 
     const int threads = std::min(1024, std::max(32, ((D4 + 3) / 4 + 31) / 32 * 32));
     const int per = (D4 + threads - 1) / threads;
     if (per <= 1)
-      rows_norm_vec_kernel<1><<<rows, threads, 0, stream>>>(dtype, y, nsplit, rows * D, g,
-                                                            (float)eps, with_norm, out, D,
-                                                            ctx_len, L);
+      {
+    const cudaError_t le = launch_pdl(rows_norm_vec_kernel<1>, dim3(rows), dim3(threads), 0, stream,
+        dtype, y, nsplit, rows * D, g, (float)eps, with_norm, out, D, ctx_len, L);
+    if (le != cudaSuccess) return le;
+  }
     else
-      rows_norm_vec_kernel<4><<<rows, threads, 0, stream>>>(dtype, y, nsplit, rows * D, g,
-                                                            (float)eps, with_norm, out, D,
-                                                            ctx_len, L);
+      {
+    const cudaError_t le = launch_pdl(rows_norm_vec_kernel<4>, dim3(rows), dim3(threads), 0, stream,
+        dtype, y, nsplit, rows * D, g, (float)eps, with_norm, out, D, ctx_len, L);
+    if (le != cudaSuccess) return le;
+  }
     return cudaGetLastError();
   }
   const int threads = D >= 2048 ? 512 : 256;
-  rows_norm_kernel<<<rows, threads, 0, stream>>>(dtype, y, nsplit, rows * D, g, (float)eps,
-                                                 with_norm, out, D);
+  {
+    const cudaError_t le = launch_pdl(rows_norm_kernel, dim3(rows), dim3(threads), 0, stream, dtype,
+        y, nsplit, rows * D, g, (float)eps, with_norm, out, D);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
@@ -509,17 +543,31 @@ cudaError_t launch_qkv_rope(const float* y, int nsplit, const int* nsplit_dev, c
   const long B = T / ((long)N * S);
   const int vblocks = (int)(B * Hkv * ((N * S + kVtSlots - 1) / kVtSlots));
   if (f16) {
-    qk_rope_kernel<__half><<<grid_for(n, 256), 256, 0, stream>>>(
-        y, nsplit, nsplit_dev, stride, pos, valid, cos_t, sin_t, P, static_cast<__half*>(q),
+    {
+    const cudaError_t le = launch_pdl(qk_rope_kernel<__half>, dim3(grid_for(n, 256)), dim3(256), 0,
+        stream, y, nsplit, nsplit_dev, stride, pos, valid, cos_t, sin_t, P, static_cast<__half*>(q),
         static_cast<__half*>(kb), T, N, S, Hq, Hkv, dh, status);
-    v_transpose_kernel<__half><<<vblocks, 256, 0, stream>>>(
-        y, nsplit, nsplit_dev, stride, valid, static_cast<__half*>(vbt), ns_pad, N, S, Hq, Hkv, dh);
+    if (le != cudaSuccess) return le;
+  }
+    {
+    const cudaError_t le = launch_pdl(v_transpose_kernel<__half>, dim3(vblocks), dim3(256), 0,
+        stream, y, nsplit, nsplit_dev, stride, valid, static_cast<__half*>(vbt), ns_pad, N, S, Hq,
+        Hkv, dh);
+    if (le != cudaSuccess) return le;
+  }
   } else {
-    qk_rope_kernel<float><<<grid_for(n, 256), 256, 0, stream>>>(
-        y, nsplit, nsplit_dev, stride, pos, valid, cos_t, sin_t, P, static_cast<float*>(q),
+    {
+    const cudaError_t le = launch_pdl(qk_rope_kernel<float>, dim3(grid_for(n, 256)), dim3(256), 0,
+        stream, y, nsplit, nsplit_dev, stride, pos, valid, cos_t, sin_t, P, static_cast<float*>(q),
         static_cast<float*>(kb), T, N, S, Hq, Hkv, dh, status);
-    v_transpose_kernel<float><<<vblocks, 256, 0, stream>>>(
-        y, nsplit, nsplit_dev, stride, valid, static_cast<float*>(vbt), ns_pad, N, S, Hq, Hkv, dh);
+    if (le != cudaSuccess) return le;
+  }
+    {
+    const cudaError_t le = launch_pdl(v_transpose_kernel<float>, dim3(vblocks), dim3(256), 0,
+        stream, y, nsplit, nsplit_dev, stride, valid, static_cast<float*>(vbt), ns_pad, N, S, Hq,
+        Hkv, dh);
+    if (le != cudaSuccess) return le;
+  }
   }
   return cudaGetLastError();
 }
@@ -556,6 +604,8 @@ __global__ void __launch_bounds__(256) convert_bf16_f16_kernel(
     const uint4* __restrict__ src, uint4* __restrict__ dst, long n8,
     const uint16_t* __restrict__ src_tail, uint16_t* __restrict__ dst_tail, int tail,
     unsigned* status) {
+  pdl_wait();
+  pdl_trigger();
   bool bad = false;
   const long stride = (long)gridDim.x * blockDim.x;
   long i = blockIdx.x * (long)blockDim.x + threadIdx.x;
@@ -619,6 +669,8 @@ __device__ __forceinline__ void compact_tiles(long tiles, int32_t* list, Pred ac
 __global__ void __launch_bounds__(1024) ctx_tile_list_kernel(const int32_t* __restrict__ ctx_len,
                                                              int B, int L, int32_t* list,
                                                              long tiles) {
+  pdl_wait();
+  pdl_trigger();
   compact_tiles(tiles, list, [&](long t) {
     const long m0 = t * kGemmTileM, m1 = min(m0 + kGemmTileM, (long)B * L);
     for (long m = m0; m < m1;) {
@@ -634,6 +686,8 @@ __global__ void __launch_bounds__(1024) ctx_tile_list_kernel(const int32_t* __re
 
 __global__ void __launch_bounds__(1024) slot_tile_list_kernel(const uint8_t* __restrict__ valid,
                                                               long T, int32_t* list, long tiles) {
+  pdl_wait();
+  pdl_trigger();
   compact_tiles(tiles, list, [&](long t) {
     for (long r = t * kGemmTileM; r < min((t + 1) * kGemmTileM, T); ++r)
       if (valid[r]) return true;
@@ -646,14 +700,22 @@ __global__ void __launch_bounds__(1024) slot_tile_list_kernel(const uint8_t* __r
 cudaError_t launch_ctx_tile_list(const int32_t* ctx_len, int B, int L, int32_t* list,
                                  cudaStream_t stream) {
   const long tiles = ((long)B * L + kGemmTileM - 1) / kGemmTileM;
-  ctx_tile_list_kernel<<<1, 1024, 0, stream>>>(ctx_len, B, L, list, tiles);
+  {
+    const cudaError_t le = launch_pdl(ctx_tile_list_kernel, dim3(1), dim3(1024), 0, stream, ctx_len,
+        B, L, list, tiles);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_slot_tile_list(const uint8_t* valid, long T, int32_t* list,
                                   cudaStream_t stream) {
   const long tiles = (T + kGemmTileM - 1) / kGemmTileM;
-  slot_tile_list_kernel<<<1, 1024, 0, stream>>>(valid, T, list, tiles);
+  {
+    const cudaError_t le = launch_pdl(slot_tile_list_kernel, dim3(1), dim3(1024), 0, stream, valid,
+        T, list, tiles);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
@@ -682,10 +744,13 @@ cudaError_t launch_convert_bf16_f16(const void* src, void* dst, size_t n, unsign
   }
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  convert_bf16_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-      static_cast<const uint4*>(src), static_cast<uint4*>(dst), n8,
-      static_cast<const uint16_t*>(src) + n8 * 8, static_cast<uint16_t*>(dst) + n8 * 8, tail,
-      status);
+  {
+    const cudaError_t le = launch_pdl(convert_bf16_f16_kernel, dim3((unsigned)blocks), dim3(256), 0,
+        stream, static_cast<const uint4*>(src), static_cast<uint4*>(dst), n8,
+        static_cast<const uint16_t*>(src) + n8 * 8, static_cast<uint16_t*>(dst) + n8 * 8, tail,
+        status);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 

@@ -49,6 +49,8 @@ template <typename T>
 __global__ void __launch_bounds__(kVerifyThreads)
 argmax_partial_kernel(const T* __restrict__ logits, int V, int chunks, int chunk_len,
                       bool vec_ok, float* __restrict__ part_v, int* __restrict__ part_i) {
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.y, chunk = blockIdx.x;
   const int c0 = chunk * chunk_len;
   const int c1 = min(V, c0 + chunk_len);
@@ -128,6 +130,8 @@ __global__ void verify_scan_kernel(const float* __restrict__ part_v, const int* 
                                    int32_t eos, int32_t* __restrict__ emitted,
                                    int32_t* __restrict__ num_emitted, int32_t* __restrict__ accepted,
                                    int32_t* __restrict__ choices_out) {
+  pdl_wait();
+  pdl_trigger();
   const int warps_per_block = blockDim.x >> 5;
   const int b = blockIdx.x * warps_per_block + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -191,18 +195,30 @@ cudaError_t launch_verify(const void* logits, int dtype, const int32_t* draft, i
   const bool vec_ok = ((uintptr_t)logits % 16 == 0) && ((size_t)V * elem % 16 == 0) &&
                       ((size_t)vp.chunk_len * elem % 16 == 0);
   if (dtype == DFLASH_DTYPE_BF16) {
-    argmax_partial_kernel<__nv_bfloat16><<<grid, kVerifyThreads, 0, stream>>>(
-        (const __nv_bfloat16*)logits, V, vp.chunks, vp.chunk_len, vec_ok, part_v, part_i);
+    {
+    const cudaError_t le = launch_pdl(argmax_partial_kernel<__nv_bfloat16>, dim3(grid),
+        dim3(kVerifyThreads), 0, stream, (const __nv_bfloat16*)logits, V, vp.chunks, vp.chunk_len,
+        vec_ok, part_v, part_i);
+    if (le != cudaSuccess) return le;
+  }
   } else {
-    argmax_partial_kernel<float><<<grid, kVerifyThreads, 0, stream>>>(
-        (const float*)logits, V, vp.chunks, vp.chunk_len, vec_ok, part_v, part_i);
+    {
+    const cudaError_t le = launch_pdl(argmax_partial_kernel<float>, dim3(grid),
+        dim3(kVerifyThreads), 0, stream, (const float*)logits, V, vp.chunks, vp.chunk_len, vec_ok,
+        part_v, part_i);
+    if (le != cudaSuccess) return le;
+  }
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = 4;
   const size_t smem = (size_t)warps * (gamma + 1) * sizeof(int);
-  verify_scan_kernel<<<(B + warps - 1) / warps, warps * 32, smem, stream>>>(
-      part_v, part_i, vp.chunks, draft, B, gamma, eos, emitted, num_emitted, accepted, choices);
+  {
+    const cudaError_t le = launch_pdl(verify_scan_kernel, dim3((B + warps - 1) / warps),
+        dim3(warps * 32), smem, stream, part_v, part_i, vp.chunks, draft, B, gamma, eos, emitted,
+        num_emitted, accepted, choices);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
