@@ -128,6 +128,17 @@ def test_train_8b_b4_parity(lib):
     c.compare(got, [(0, k) for k in range(c.N)] + [(2, 0), (2, 1)])
 
 
+def test_train_8b_b4_parity_with_prepared_f16_layers(lib):
+    """The same workload with fp16 copies of the layer matrices prepared once: more than 128
+    tokens with fp16 weights take the 128 x 256-tile GEMM instead of the weight-streaming
+    one; both meet the bound, and their outputs differ only by accumulation order."""
+    w = di.WORKLOADS["train_8b_b4_l2048"]
+    c = Case(w)
+    got = c.run_gpu(f16_layers=True)
+    assert np.all(got[3] == 0.0)
+    c.compare(got, [(0, k) for k in range(c.N)] + [(1, 3)])
+
+
 @pytest.mark.parametrize("batch", [1, 8])
 def test_decode_8b_parity(lib, batch):
     w = di.WORKLOADS[f"decode_8b_b{batch}_ctx4096"]
