@@ -36,14 +36,42 @@ __device__ __forceinline__ void consider(ArgMax& a, float v, int i) {
   if (better(v, i, a.v, a.i)) { a.v = v; a.i = i; }
 }
 
-__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+// 16-byte streaming load, issued where it stands (volatile asm): a batch of these is in
+// flight together before any of its values is used
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 u;
+  asm volatile("ld.global.cs.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+               : "l"(p));
+  return u;
+}
+
+// The 8 bf16 values of u against the running best of this thread, whose elements come in
+// increasing index order: only a strictly larger value replaces it (ties keep the earlier,
+// lower index); before anything is found (index sentinel) an equal value -- -inf -- is taken
+// too.  The vector's maximum comes from packed bf16 max instructions (which skip NaN); the
+// index search runs only when that maximum beats the running best.
+__device__ __forceinline__ void consider8(ArgMax& a, const uint4& u, int base) {
+  const __nv_bfloat162 w0 = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+  const __nv_bfloat162 w1 = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+  const __nv_bfloat162 w2 = *reinterpret_cast<const __nv_bfloat162*>(&u.z);
+  const __nv_bfloat162 w3 = *reinterpret_cast<const __nv_bfloat162*>(&u.w);
+  const __nv_bfloat162 m2 = __hmax2(__hmax2(w0, w1), __hmax2(w2, w3));
+  const float mv = fmaxf(__low2float(m2), __high2float(m2));
+  if (mv > a.v || (a.i == 0x7fffffff && mv == a.v)) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    f[2 * q] = __uint_as_float(w[q] << 16);
-    f[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+    for (int e = 0; e < 8; ++e) {
+      const float f = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
+      if (f == mv) {
+        a.v = mv;
+        a.i = base + e;
+        break;
+      }
+    }
   }
 }
+
 
 template <typename T>
 __global__ void __launch_bounds__(kVerifyThreads)
@@ -62,41 +90,32 @@ argmax_partial_kernel(const T* __restrict__ logits, int V, int chunks, int chunk
     const int nvec = (c1 - c0) / kVec;
     const uint4* pv = reinterpret_cast<const uint4*>(p + c0);
     int t = threadIdx.x;
-    // 8 independent 16-byte loads in flight per thread
-    constexpr int kUnroll = 8;
-    for (; t + (kUnroll - 1) * kVerifyThreads < nvec; t += kUnroll * kVerifyThreads) {
+    // batches of 4 independent 16-byte loads per thread (8 resident CTAs per SM keep ~128 KB
+    // in flight per SM), the last batch masked
+    constexpr int kUnroll = 4;
+    for (; t < nvec; t += kUnroll * kVerifyThreads) {
       uint4 u[kUnroll];
 #pragma unroll
-      for (int q = 0; q < kUnroll; ++q) u[q] = __ldcs(pv + t + q * kVerifyThreads);
+      for (int q = 0; q < kUnroll; ++q)
+        u[q] = t + q * kVerifyThreads < nvec ? ld_stream(pv + t + q * kVerifyThreads)
+                                             : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u,
+                                                          0xFF80FF80u);
 #pragma unroll
       for (int q = 0; q < kUnroll; ++q) {
+        if (t + q * kVerifyThreads >= nvec) break;
         const int base = c0 + (t + q * kVerifyThreads) * kVec;
         if constexpr (sizeof(T) == 2) {
-          float f[8];
-          unpack8(u[q], f);
+          consider8(best, u[q], base);
+        } else {  // strictly larger only: this thread's elements come in index order
+          const float f[4] = {__uint_as_float(u[q].x), __uint_as_float(u[q].y),
+                              __uint_as_float(u[q].z), __uint_as_float(u[q].w)};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) consider(best, f[e], base + e);
-        } else {
-          consider(best, __uint_as_float(u[q].x), base);
-          consider(best, __uint_as_float(u[q].y), base + 1);
-          consider(best, __uint_as_float(u[q].z), base + 2);
-          consider(best, __uint_as_float(u[q].w), base + 3);
+          for (int e = 0; e < 4; ++e)
+            if (f[e] > best.v || (best.i == 0x7fffffff && f[e] == best.v)) {
+              best.v = f[e];
+              best.i = base + e;
+            }
         }
-      }
-    }
-    for (; t < nvec; t += kVerifyThreads) {
-      const uint4 u = __ldcs(pv + t);
-      const int base = c0 + t * kVec;
-      if constexpr (sizeof(T) == 2) {
-        float f[8];
-        unpack8(u, f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) consider(best, f[e], base + e);
-      } else {
-        consider(best, __uint_as_float(u.x), base);
-        consider(best, __uint_as_float(u.y), base + 1);
-        consider(best, __uint_as_float(u.z), base + 2);
-        consider(best, __uint_as_float(u.w), base + 3);
       }
     }
     c = c0 + nvec * kVec;
@@ -172,12 +191,22 @@ __global__ void verify_scan_kernel(const float* __restrict__ part_v, const int* 
 VerifyPlan plan_verify(int B, int gamma, int V, int num_sms) {
   VerifyPlan vp;
   const long rows = (long)B * (gamma + 1);
-  // aim for ~8 CTAs per SM in total, chunks of at least 4096 elements, multiple of 8
-  long want = (8L * num_sms + rows - 1) / rows;
-  long max_chunks = (V + 4095) / 4096;
-  if (want > max_chunks) want = max_chunks;
-  if (want < 1) want = 1;
-  long len = (V + want - 1) / want;
+  // resident argmax CTAs on the whole GPU
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, argmax_partial_kernel<__nv_bfloat16>,
+                                                      kVerifyThreads, 0) != cudaSuccess || n < 1)
+      n = 4;
+    per_sm = n;
+  }
+  const long resident = (long)per_sm * (num_sms > 0 ? num_sms : 1);
+  // about three waves of resident CTAs, chunks of at least 4096 elements
+  long best = (3 * resident + rows - 1) / rows;
+  const long max_chunks = (V + 4095) / 4096;
+  if (best > max_chunks) best = max_chunks;
+  if (best < 1) best = 1;
+  long len = (V + best - 1) / best;
   len = (len + 7) / 8 * 8;
   vp.chunk_len = (int)len;
   vp.chunks = (int)((V + len - 1) / len);

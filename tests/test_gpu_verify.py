@@ -76,6 +76,22 @@ def test_ties_take_lowest_index(lib, dtype):
     assert np.all(ch < 50)   # ties resolve to early indices
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_ties_take_lowest_index_vector_path(lib, dtype):
+    """Exact ties across 16-byte vectors, threads and vocab chunks (V a multiple of 8), and a
+    row whose maximum is -inf everywhere."""
+    rng = np.random.default_rng(37)
+    B, S, V = 3, 4, 151936
+    x = rng.integers(-2, 3, size=(B, S, V)).astype(np.float32)
+    x[1, 2, :] = -np.inf
+    x[2, 1, :] = -2.0
+    x[2, 1, V - 5] = -1.0                     # a lone maximum near the end
+    t = di.Tensor(di.f32_to_bf16_bits(x), "bf16") if dtype == "bf16" else di.Tensor(x, "f32")
+    draft = rng.integers(0, 3, size=(B, S - 1)).astype(np.int32)
+    ch, *_ = check(t, draft)
+    assert ch[1, 2] == 0 and ch[2, 1] == V - 5
+
+
 @pytest.mark.parametrize("V", [1, 7, 8, 4096, 151936, 262144 + 3])
 def test_vocab_sizes_and_chunking(lib, V):
     rng = np.random.default_rng(V)
