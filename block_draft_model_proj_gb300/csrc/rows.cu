@@ -300,9 +300,11 @@ __global__ void qk_rope_kernel(const float* __restrict__ y, int nsplit,
     const int hd = rem / q4, i = (rem - hd * q4) * 4;
     const long base = t * width + (long)hd * dh;
     const bool vt = valid[t] != 0;
-    const float4 a = vt ? sum_splits4(y, nsplit, split_stride, base + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4 bb = vt ? sum_splits4(y, nsplit, split_stride, base + i + half)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    // loaded whatever the slot's validity (the rows exist; an invalid slot's may be
+    // unwritten) and discarded by the select: the loads do not wait for the flag
+    float4 a = sum_splits4(y, nsplit, split_stride, base + i);
+    float4 bb = sum_splits4(y, nsplit, split_stride, base + i + half);
+    if (!vt) a = bb = make_float4(0.f, 0.f, 0.f, 0.f);
     const int b = (int)(t / ((long)N * S));
     const int ks = (int)(t - (long)b * N * S);  // k * S + j
     const int k = ks / S, j = ks - k * S;
@@ -342,6 +344,7 @@ __global__ void __launch_bounds__(256) v_transpose_kernel(
   pdl_wait();
   pdl_trigger();
   __shared__ float tile[kVtSlots][257];
+  __shared__ uint8_t slot_ok[kVtSlots];
   if (nsplit_dev) nsplit = *nsplit_dev;
   const int NS = N * S;
   const int tiles = (NS + kVtSlots - 1) / kVtSlots;
@@ -351,24 +354,31 @@ __global__ void __launch_bounds__(256) v_transpose_kernel(
   const int ks0 = bt * kVtSlots;
   const long width = (long)(Hq + 2 * Hkv) * dh;
   const int vcol = (Hq + Hkv + g) * dh;
-  // eight independent loads in flight per thread before they are stored
+  if (threadIdx.x < kVtSlots) {
+    const int ks = ks0 + threadIdx.x;
+    slot_ok[threadIdx.x] = ks < NS && valid[(long)b * NS + ks] != 0;
+  }
+  // the loads do not wait for the validity flags: rows of invalid slots (whose GEMM rows may
+  // be unwritten) are read and then discarded by the select below
   for (int idx0 = threadIdx.x; idx0 < kVtSlots * dh; idx0 += 8 * blockDim.x) {
     float v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int idx = idx0 + u * blockDim.x;
-      const int jj = idx / dh, d = idx - jj * dh;
-      const int ks = ks0 + jj;
-      v[u] = 0.f;
-      if (idx < kVtSlots * dh && ks < NS) {
-        const long t = (long)b * NS + ks;
-        if (valid[t]) v[u] = sum_splits(y, nsplit, split_stride, t * width + vcol + d);
+    for (int u = 0; u < 8; ++u) v[u] = 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int idx = idx0 + u * blockDim.x;
+        const int jj = idx / dh, d = idx - jj * dh;
+        const int ks = min(ks0 + jj, NS - 1);
+        if (idx < kVtSlots * dh)
+          v[u] += y[sp * split_stride + ((long)b * NS + ks) * width + vcol + d];
       }
     }
+    __syncthreads();  // slot_ok is written
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int idx = idx0 + u * blockDim.x;
-      if (idx < kVtSlots * dh) tile[idx / dh][idx % dh] = v[u];
+      if (idx < kVtSlots * dh) tile[idx / dh][idx % dh] = slot_ok[idx / dh] ? v[u] : 0.f;
     }
   }
   __syncthreads();
