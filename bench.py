@@ -141,7 +141,7 @@ def profiled_traffic(workload: str):
     """DRAM bytes per GEMM launch from the committed ncu capture of this workload, or None
     when there is none or the GEMM kernel's sources changed since it was taken."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", f"gemm_tc_traffic_{workload}.json")
+    path = os.path.join(ROOT, "profiles", f"gemm_traffic_{workload}.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
