@@ -349,7 +349,9 @@ BodyLayout body_layout(const dflash_config_t* c, int B, int L, int N, void* ws) 
   if (b.ws) {
     b.sp_qkv = ws_max_splits(qkvw, T);
     b.sp_o = ws_max_splits(D, T);
-    b.sp_gu = 0;  // SiLU(gate) * up is formed in the GEMM epilogue
+    // up to 128 tokens gate/up is K-split (fp32 slices + the SwiGLU row kernel); above that
+    // SiLU(gate) * up is formed in the GEMM epilogue
+    b.sp_gu = T <= 128 ? ws_max_splits(2 * I, T) : 0;
     b.sp_down = ws_max_splits(D, T);
   } else if (c->dtype == DFLASH_DTYPE_BF16) {  // splits chosen on the device, these bound them
     b.sp_qkv = ws_max_splits(qkvw, T, 256);
@@ -712,7 +714,17 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
                                    tc ? lay.nsplit + 1 : nullptr, lw.g_post, cfg->rms_eps,
                                    lay.h.out(), nullptr, block_valid, false, T, D, s));
     }
-    if (use_ws) {
+    if (use_ws && lay.sp_gu > 0) {
+      // few tokens: K-split gate/up into fp32 slices (the fused epilogue would leave SMs
+      // idle), SiLU(gate) * up by the row kernel
+      {
+        Prof pr(DFLASH_PROF_GEMM, 1, s);
+        DF_CUDA(launch_gemm_ws(ws_args(lay.h.p, D, lw.w_gate_up, 2 * I, lay.sp_gu, lay.nsplit + 3),
+                               s));
+      }
+      Prof pr(DFLASH_PROF_ROWS, 1, s);
+      DF_CUDA(launch_swiglu(lay.y, lay.sp_gu, lay.nsplit + 3, lay.act.out(), T, I, block_valid, s));
+    } else if (use_ws) {
       // SiLU(gate) * up is formed in the GEMM epilogue
       Prof pr(DFLASH_PROF_GEMM, 1, s);
       DF_CUDA(launch_gemm_ws_swiglu(ws_args(lay.h.p, D, lw.w_gate_up, 2 * I, 1, nullptr),
@@ -727,7 +739,7 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
         DF_CUDA(gemm(dt, dt, lay.h.p, D, lw.w_gate_up, D, lay.y, 2 * I, T, 2 * I, D, lay.sp_gu, s));
       }
       Prof pr(DFLASH_PROF_ROWS, 1, s);
-      DF_CUDA(launch_swiglu(lay.y, lay.sp_gu, lay.act.out(), T, I, s));
+      DF_CUDA(launch_swiglu(lay.y, lay.sp_gu, nullptr, lay.act.out(), T, I, block_valid, s));
     }
     {
       Prof pr(DFLASH_PROF_GEMM, 1, s);

@@ -94,8 +94,9 @@ cudaError_t launch_ctx_kv_scatter(const float* y, int nsplit, const float* cos_t
                                   const int32_t* ctx_len, cudaStream_t stream);
 
 // SwiGLU epilogue: y [nsplit][T][2I] fp32 (gate | up) -> act [T][I] = SiLU(gate) * up.
-cudaError_t launch_swiglu(const float* y, int nsplit, ActOut act, long T, int I,
-                          cudaStream_t stream);
+// nsplit_dev (optional) overrides nsplit; valid (optional): invalid slots' rows get zeros.
+cudaError_t launch_swiglu(const float* y, int nsplit, const int* nsplit_dev, ActOut act, long T,
+                          int I, const uint8_t* valid, cudaStream_t stream);
 
 // ---- gemm_simt.cu: C[z][M][N] (fp32) = A[M][K] * B[N][K]^T over K-split z ----
 cudaError_t launch_gemm_simt(int dtype, const void* A, long lda, const void* Bm, long ldb,

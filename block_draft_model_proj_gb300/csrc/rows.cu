@@ -243,18 +243,27 @@ __global__ void rows_norm_vec_kernel(int dt, const float* __restrict__ y, int ns
 __device__ __forceinline__ float silu_mul(float gt, float up) { return gt / (1.f + expf(-gt)) * up; }
 
 // SwiGLU, four consecutive channels per thread (I % 4 == 0)
-__global__ void swiglu_vec_kernel(const float* __restrict__ y, int nsplit, long split_stride,
-                                  ActOut act, long T, int I) {
+// valid (optional): rows of invalid slots (whose GEMM rows may be unwritten) get zeros
+__global__ void swiglu_vec_kernel(const float* __restrict__ y, int nsplit,
+                                  const int* __restrict__ nsplit_dev, long split_stride,
+                                  ActOut act, long T, int I, const uint8_t* __restrict__ valid) {
+  pdl_wait();
+  pdl_trigger();
+  if (nsplit_dev) nsplit = *nsplit_dev;
   const int I4 = I / 4;
   const long n = T * I4;
   for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n;
        e += (long)gridDim.x * blockDim.x) {
     const long t = e / I4;
     const int i = (int)(e - t * I4) * 4;
-    const float4 gt = sum_splits4(y, nsplit, split_stride, t * 2 * I + i);
-    const float4 up = sum_splits4(y, nsplit, split_stride, t * 2 * I + I + i);
-    act.store4(t * I + i, make_float4(silu_mul(gt.x, up.x), silu_mul(gt.y, up.y),
-                                      silu_mul(gt.z, up.z), silu_mul(gt.w, up.w)));
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!valid || valid[t]) {
+      const float4 gt = sum_splits4(y, nsplit, split_stride, t * 2 * I + i);
+      const float4 up = sum_splits4(y, nsplit, split_stride, t * 2 * I + I + i);
+      o = make_float4(silu_mul(gt.x, up.x), silu_mul(gt.y, up.y), silu_mul(gt.z, up.z),
+                      silu_mul(gt.w, up.w));
+    }
+    act.store4(t * I + i, o);
   }
 }
 
@@ -438,13 +447,21 @@ __global__ void ctx_vt_scatter_kernel(const float* __restrict__ y, int nsplit, l
   }
 }
 
-__global__ void swiglu_kernel(const float* __restrict__ y, int nsplit, long split_stride,
-                              ActOut act, long T, int I) {
+__global__ void swiglu_kernel(const float* __restrict__ y, int nsplit,
+                              const int* __restrict__ nsplit_dev, long split_stride, ActOut act,
+                              long T, int I, const uint8_t* __restrict__ valid) {
+  pdl_wait();
+  pdl_trigger();
+  if (nsplit_dev) nsplit = *nsplit_dev;
   const long n = T * I;
   for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n;
        e += (long)gridDim.x * blockDim.x) {
     const long t = e / I;
     const int i = (int)(e - t * I);
+    if (valid && !valid[t]) {
+      act.store(e, 0.f);
+      continue;
+    }
     const float gt = sum_splits(y, nsplit, split_stride, t * 2 * I + i);
     const float up = sum_splits(y, nsplit, split_stride, t * 2 * I + I + i);
     act.store(e, gt / (1.f + expf(-gt)) * up);
@@ -764,16 +781,16 @@ cudaError_t launch_convert_bf16_f16(const void* src, void* dst, size_t n, unsign
   return cudaGetLastError();
 }
 
-cudaError_t launch_swiglu(const float* y, int nsplit, ActOut act, long T, int I,
-                          cudaStream_t stream) {
+cudaError_t launch_swiglu(const float* y, int nsplit, const int* nsplit_dev, ActOut act, long T,
+                          int I, const uint8_t* valid, cudaStream_t stream) {
   if (I % 4 == 0) {
     const long n4 = T * (I / 4);
-    swiglu_vec_kernel<<<grid_for(n4, 256), 256, 0, stream>>>(y, nsplit, T * 2L * I, act, T, I);
-    return cudaGetLastError();
+    return launch_pdl(swiglu_vec_kernel, dim3(grid_for(n4, 256)), dim3(256), 0, stream, y, nsplit,
+                      nsplit_dev, T * 2L * I, act, T, I, valid);
   }
   const long n = T * I;
-  swiglu_kernel<<<grid_for(n, 256), 256, 0, stream>>>(y, nsplit, T * 2L * I, act, T, I);
-  return cudaGetLastError();
+  return launch_pdl(swiglu_kernel, dim3(grid_for(n, 256)), dim3(256), 0, stream, y, nsplit,
+                    nsplit_dev, T * 2L * I, act, T, I, valid);
 }
 
 }  // namespace dflash
