@@ -77,7 +77,59 @@ def algorithmic_work(w: di.Workload, plan: dict, mask: np.ndarray) -> dict:
 # clocks sampled during the timed region
 # --------------------------------------------------------------------------------------
 
+class NvmlPoller:
+    """Read-only NVML queries (SM clock, its maximum, clock event reasons) polled about every
+    millisecond from a thread, so that timed regions of a few milliseconds get samples too."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device_index),
+                                                  ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.samples = []
+        self.stop_evt = threading.Event()
+        self.thread = None
+
+    def query(self):
+        ct = self.ct
+        mhz, mx, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz)) != 0:
+            return None
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ct.byref(mx))
+        self.reasons_fn(self.h, ct.byref(rs))
+        return mhz.value, mx.value, rs.value
+
+    def _run(self):
+        while not self.stop_evt.is_set():
+            q = self.query()
+            if q:
+                self.samples.append(q)
+            time.sleep(0.001)
+
+    def start(self):
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.stop_evt.set()
+        if self.thread:
+            self.thread.join(timeout=2)
+        return self.samples
+
+
 class ClockSampler:
+    """Clocks during the timed region: NVML polled about every millisecond, plus the
+    nvidia-smi query loop (200 ms) beside it; the median SM clock and every active slowdown
+    reason of both."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -87,6 +139,10 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self.thread = None
+        try:
+            self.nvml = NvmlPoller(device_index)
+        except (OSError, AttributeError):
+            self.nvml = None
 
     def start(self):
         try:
@@ -96,26 +152,32 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
-            return
-        self.thread = threading.Thread(target=self._read, daemon=True)
-        self.thread.start()
+        if self.proc is not None:
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        if self.nvml:
+            self.nvml.start()
 
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
     def stop(self) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        if self.thread:
-            self.thread.join(timeout=2)
+        nv = self.nvml.stop() if self.nvml else []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+        if self.proc is None and not nv:
+            return {"sm_mhz": None, "sm_max_mhz": None,
+                    "reasons": ["nvidia-smi and NVML unavailable"]}
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        n_smi = 0
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
@@ -125,12 +187,19 @@ class ClockSampler:
                 smax.append(float(parts[1]))
             except ValueError:
                 continue
+            n_smi += 1
             for n, v in zip(names, parts[4:8]):
                 if v.lower() == "active":
                     reasons.add(n)
+        for mhz, mx, rs in nv:
+            sm.append(float(mhz))
+            smax.append(float(mx))
+            for bit, n in NvmlPoller.REASONS.items():
+                if rs & bit:
+                    reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "samples_nvml": len(nv), "samples_nvidia_smi": n_smi}
 
 
 # --------------------------------------------------------------------------------------

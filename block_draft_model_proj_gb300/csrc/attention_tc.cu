@@ -28,21 +28,21 @@
 // with a lazily updated running maximum (the accumulator is rescaled only when the maximum
 // grows by more than 2^8, so P stays <= 256).
 //
-// Tensor memory holds the whole working set of a tile: Q (loaded once per unit from global
-// by the softmax warps, packed fp16 pairs), the O accumulator, and four S/P buffers (S = Q K^T
-// lands there; each softmax warp overwrites the first half of its own S columns with its
-// packed fp16 P, and O += P V reads P from there).  Shared memory holds only K and V^T tiles
-// of 64 keys in two separate 4-stage TMA rings.
+// Key tiles are 128 keys.  Tensor memory holds the whole working set of a tile: Q (loaded
+// once per unit from global by the softmax warps, packed fp16 pairs) [0,64), the O
+// accumulator [128,256), and two S/P buffers [256,384) and [384,512) (S = Q K^T lands there;
+// each softmax warp overwrites the first half of its own 64 S columns with its packed fp16
+// P, and O += P V reads P from there).  Shared memory holds only the K and V^T tiles, in two
+// 3-stage TMA rings of 32 KB stages.
 // Warp roles: warp 0 TMA producers (lane 0 the K ring, lane 1 the V^T ring); warp 1 MMA
-// issuer, which polls its barriers without blocking and issues S of the next tiles as soon as
-// a K tile and an S/P buffer are free, independently of the PV of earlier tiles; warps 2-9
-// softmax / correction / partial output: two warps per TMEM lane quarter, one per half of
-// the key columns (and of the O columns), so each SM sub-partition runs two softmax warps;
-// the halves agree on the running row maximum through shared memory behind an mbarrier.
-// Fully readable half-tiles take a short path (one zero-byte test per mask word), and
-// P = 2^(x - m) uses the special-function unit directly (an excluded key gives exactly 0).
-// Every mbarrier wait is bounded in time; on expiry the CTA reports DFLASH_ERR_TIMEOUT,
-// drains its own copies and MMAs, frees tensor memory and exits.
+// issuer, one thread, in a fixed order (S of the next-but-one tile right behind each PV);
+// warps 2-9 softmax / correction / partial output: two warps per TMEM lane quarter, one per
+// half of the key columns (and of the O columns), so each SM sub-partition runs two softmax
+// warps; the halves agree on the running row maximum through shared memory behind an
+// mbarrier.  Fully readable 16-key groups take a short path (one zero-byte test per mask
+// word), and P = 2^(x - m) uses the special-function unit directly (an excluded key gives
+// exactly 0).  Every mbarrier wait is bounded in time; on expiry the CTA reports
+// DFLASH_ERR_TIMEOUT, drains its own copies and MMAs, frees tensor memory and exits.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
@@ -55,21 +55,23 @@ using namespace tc;
 
 constexpr int kDH = 128;   // head dim handled by this kernel
 constexpr int kM = 128;    // query rows per tile (TMEM lanes)
-constexpr int kKT = 64;    // keys per tile
-constexpr int kRing = 4;   // stages of each of the K and V^T rings
-constexpr int kSP = 4;     // S/P buffers in tensor memory
+constexpr int kKT = 128;   // keys per tile (the N of the S MMA)
+constexpr int kRing = 3;   // stages of each of the K and V^T rings
+constexpr int kSP = 2;     // S/P buffers in tensor memory
 constexpr int kThreads = 320;          // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
 constexpr int kSoftmaxWarps = 8;       // two per TMEM lane quarter, each owns half the keys
-constexpr int kHalfKT = 32;            // key columns per softmax thread
-constexpr uint32_t kTmemCols = 512;    // Q [0,64), O [128,256), S/P 4 x 64 [256,512)
+constexpr int kHalfKT = 64;            // key columns per softmax thread
+constexpr uint32_t kTmemCols = 512;    // Q [0,64), O [128,256), S/P 2 x 128 [256,512)
 constexpr uint32_t kTmemQ = 0, kTmemO = 128, kTmemS = 256;
-constexpr uint32_t kKSub = kKT * 64 * 2;   // K [64 keys][64 dh] fp16, 8 KB
-constexpr uint32_t kKBytes = 2 * kKSub;    // 16 KB
-constexpr uint32_t kVBytes = kDH * kKT * 2;  // V^T [128 dh][64 keys] fp16, 16 KB
+constexpr uint32_t kKSub = kKT * 64 * 2;   // K [128 keys][64 dh] fp16, 16 KB
+constexpr uint32_t kKBytes = 2 * kKSub;    // 32 KB
+constexpr uint32_t kVSub = kDH * 64 * 2;   // V^T [128 dh][64 keys] fp16, 16 KB
+constexpr uint32_t kVBytes = 2 * kVSub;    // 32 KB
 constexpr uint32_t kBarBytes = 512;
 // K ring + V ring + barriers + row-max exchange [2][2][128] + row-sum exchange [2][128]
 constexpr size_t kSmemBytes = 1024 + kRing * (size_t)(kKBytes + kVBytes) + kBarBytes +
                               (4 * 128 + 2 * 128) * sizeof(float);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 constexpr uint32_t kIdescS = idesc_f16(kM, kKT);
 constexpr uint32_t kIdescPV = idesc_f16(kM, kDH);
 constexpr float kRescaleLog2 = 8.0f;
@@ -186,12 +188,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
 
   if (warp == 0) {
     // ---------------- TMA producers: lane 0 = the K ring, lane 1 = the V^T ring ----------------
+    // A K tile is two [128 keys][64 dh] boxes (the two halves of dh), a V^T tile two
+    // [128 dh][64 keys] boxes (the two halves of the keys), each 128-byte swizzled.
     if (lane < 2) {
       const bool is_k = lane == 0;
       uint64_t* full = is_k ? k_full : v_full;
       uint64_t* empty = is_k ? k_empty : v_empty;
-      int issued[kRing] = {0, 0, 0, 0};
-      uint32_t issued_ph[kRing] = {0, 0, 0, 0};
+      int issued[kRing] = {0, 0, 0};
+      uint32_t issued_ph[kRing] = {0, 0, 0};
       for (int i = 0; i < u.n; ++i) {
         const int st = i % kRing;
         const uint32_t ph = (uint32_t)(i / kRing) & 1u;
@@ -210,9 +214,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
           mbar_arrive_expect_tx(&full[st], kVBytes);
           uint8_t* dst = sV + st * kVBytes;
           if (i < u.nblk) {
-            tma_load_2d(&map_vb, &full[st], dst, u.k0 * p.S + i * kKT, (u.b * p.Hkv + u.g) * kDH);
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d(&map_vb, &full[st], dst + h * kVSub, u.k0 * p.S + i * kKT + 64 * h,
+                          (u.b * p.Hkv + u.g) * kDH);
           } else {
-            tma_load_3d(&map_vc, &full[st], dst, u.cs + (i - u.nblk) * kKT, 0, plane_v);
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(&map_vc, &full[st], dst + h * kVSub, u.cs + (i - u.nblk) * kKT + 64 * h, 0,
+                          plane_v);
           }
         }
         issued[st] = 1;
@@ -224,57 +232,47 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      // S(i) = Q K_i^T into S/P buffer i % kSP once K_i has landed and the PV that last read
-      // that buffer (tile i - kSP) is complete; O += P_j V_j once the softmax has written P_j
-      // and V_j has landed.  Both are polled without blocking, S first, so the S of the next
-      // tiles is computed while the softmax works on the current one.
+      // A fixed order with blocking waits: S(0), S(1); then per tile i: O += P_i V_i once the
+      // softmax has written P_i and V_i has landed, followed at once by S(i + 2) into the
+      // buffer P_i occupied.  The tensor core performs one thread's MMAs in issue order, so
+      // S(i + 2) overwrites that buffer only after PV(i) has read it.  Each MMA costs this
+      // thread about a hundred cycles whatever its N, so S uses N = 128 keys per instruction.
       bool ok = mbar_wait(q_ready, 0, abort_flag, kWaitLimitNs);
       tc_fence_after();
-      int ns = 0, npv = 0;
-      uint64_t t_idle = 0;
-      while (ok && npv < u.n) {
-        bool progressed = false;
-        if (ns < u.n && ns - npv < kSP &&
-            mbar_test(&k_full[ns % kRing], (uint32_t)(ns / kRing) & 1u) &&
-            (ns < kSP || mbar_test(&pv_done[ns % kSP], (uint32_t)((ns - kSP) / kSP) & 1u))) {
-          tc_fence_after();
-          const uint32_t k_addr = smem_u32(sK + (ns % kRing) * kKBytes);
-          const uint32_t s_tmem = tmem_s0 + (uint32_t)((ns % kSP) * kKT);
-          // K = 16 dh per MMA: Q columns 8k .. 8k+7 (packed pairs); K sub-tile k / 4, +32 bytes
+      auto issue_s = [&](int s) -> bool {
+        if (!mbar_wait(&k_full[s % kRing], (uint32_t)(s / kRing) & 1u, abort_flag, kWaitLimitNs))
+          return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sK + (s % kRing) * kKBytes);
+        const uint32_t s_tmem = tmem_s0 + (uint32_t)((s % kSP) * kKT);
+        // K = 16 dh per MMA: Q columns 8k .. 8k+7 (packed pairs); K sub-tile k / 4, +32 bytes
 #pragma unroll 1
-          for (int k = 0; k < kDH / 16; ++k)
-            umma_f16_ts(s_tmem, tmem_q + k * 8, sw128_desc(k_addr + (k >> 2) * kKSub + (k & 3) * 32),
-                        kIdescS, k ? 1u : 0u);
-          umma_commit(&s_full[ns % kSP]);
-          umma_commit(&k_empty[ns % kRing]);
-          ++ns;
-          progressed = true;
-        } else if (npv < ns && mbar_test(&p_full[npv % kSP], (uint32_t)(npv / kSP) & 1u) &&
-                   mbar_test(&v_full[npv % kRing], (uint32_t)(npv / kRing) & 1u)) {
-          tc_fence_after();
-          const uint32_t v_addr = smem_u32(sV + (npv % kRing) * kVBytes);
-          const uint32_t a_base = tmem_s0 + (uint32_t)((npv % kSP) * kKT);
-          // K = 16 keys per MMA: P of keys 16k .. 16k+15 sits at columns 32 * (k / 2) +
-          // 8 * (k % 2) of the buffer (each softmax half packs its 32 keys into the first 16
-          // of its own 32 S columns); V^T +32 bytes per 16 keys
+        for (int k = 0; k < kDH / 16; ++k)
+          umma_f16_ts(s_tmem, tmem_q + k * 8, sw128_desc(k_addr + (k >> 2) * kKSub + (k & 3) * 32),
+                      kIdescS, k ? 1u : 0u);
+        umma_commit(&s_full[s % kSP]);
+        umma_commit(&k_empty[s % kRing]);
+        return true;
+      };
+      for (int s = 0; s < kSP && s < u.n && ok; ++s) ok = issue_s(s);
+      for (int i = 0; i < u.n && ok; ++i) {
+        ok = mbar_wait(&p_full[i % kSP], (uint32_t)(i / kSP) & 1u, abort_flag, kWaitLimitNs) &&
+             mbar_wait(&v_full[i % kRing], (uint32_t)(i / kRing) & 1u, abort_flag, kWaitLimitNs);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sV + (i % kRing) * kVBytes);
+        const uint32_t a_base = tmem_s0 + (uint32_t)((i % kSP) * kKT);
+        // K = 16 keys per MMA: P of keys 16k .. 16k+15 sits at columns 64 * (k / 4) +
+        // 8 * (k % 4) of the buffer (each softmax half packs its 64 keys into the first 32 of
+        // its own 64 S columns); V^T sub-tile k / 4, +32 bytes per 16 keys inside it
 #pragma unroll 1
-          for (int k = 0; k < kKT / 16; ++k)
-            umma_f16_ts(tmem_o, a_base + (k >> 1) * 32 + (k & 1) * 8, sw128_desc(v_addr + k * 32),
-                        kIdescPV, (npv == 0 && k == 0) ? 0u : 1u);
-          umma_commit(&pv_done[npv % kSP]);
-          umma_commit(&v_empty[npv % kRing]);
-          ++npv;
-          progressed = true;
-        }
-        if (progressed) {
-          t_idle = 0;
-        } else {
-          __nanosleep(32);  // leave the issue slots to the softmax warps of this sub-partition
-          const uint64_t now = globaltimer_ns();
-          if (t_idle == 0) t_idle = now;
-          if (*abort_flag) ok = false;
-          else if (now - t_idle > kWaitLimitNs) { *abort_flag = 1; ok = false; }
-        }
+        for (int k = 0; k < kKT / 16; ++k)
+          umma_f16_ts(tmem_o, a_base + (k >> 2) * 64 + (k & 3) * 8,
+                      sw128_desc(v_addr + (k >> 2) * kVSub + (k & 3) * 32), kIdescPV,
+                      (i == 0 && k == 0) ? 0u : 1u);
+        umma_commit(&pv_done[i % kSP]);
+        umma_commit(&v_empty[i % kRing]);
+        if (i + kSP < u.n) ok = issue_s(i + kSP);
       }
       umma_commit(drain);
       mbar_wait(drain, 0, abort_flag, kWaitLimitNs / 4);
@@ -282,7 +280,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
   } else {
     // ---------------- softmax / correction / partial output (warps 2..9) ----------------
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;   // key columns [32*half, 32*half + 32) of each tile
+    const int half = (warp - 2) >> 2;   // key columns [64*half, 64*half + 64) of each tile
     const int r = quarter * 32 + lane;  // query row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int kbo = r / p.R;
@@ -323,70 +321,83 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, kWaitLimitNs) ? 1 : 0) != 0;
     };
-    // context mask words of this half of a tile, loaded one tile ahead so the global-memory
-    // latency is off the softmax's critical path
-    auto load_mask = [&](int i, uint32_t* mw) {
-      const int c0 = u.cs + (i - u.nblk) * kKT + half * kHalfKT;
-#pragma unroll
-      for (int w4 = 0; w4 < kHalfKT / 4; ++w4) {
-        const int c = c0 + 4 * w4;
-        mw[w4] = (i >= u.nblk && i < u.n && row_valid && c < a_row && c < u.ce)
-                     ? __ldg(reinterpret_cast<const uint32_t*>(mrow + c)) : 0u;
-      }
+    // context mask words of this half of a tile (the same for every row of the unit): lane
+    // w < 16 loads word w one tile ahead, so the global-memory latency is off the softmax's
+    // critical path; the words are broadcast by shuffles where they are used.  Words past
+    // the chunk read as 0; the row's own prefix limit is applied at use.
+    auto load_mask = [&](int i) -> uint32_t {
+      const int c = u.cs + (i - u.nblk) * kKT + half * kHalfKT + 4 * lane;
+      return (lane < kHalfKT / 4 && i >= u.nblk && i < u.n && c < u.ce)
+                 ? __ldg(reinterpret_cast<const uint32_t*>(mrow + c)) : 0u;
     };
-    uint32_t mask_next[kHalfKT / 4];
-    load_mask(0, mask_next);
+    uint32_t mword_next = load_mask(0);
     for (int i = 0; i < u.n && ok; ++i) {
-      uint32_t mask_cur[kHalfKT / 4];
-#pragma unroll
-      for (int w4 = 0; w4 < kHalfKT / 4; ++w4) mask_cur[w4] = mask_next[w4];
-      load_mask(i + 1, mask_next);
+      const uint32_t mword = mword_next;
+      mword_next = load_mask(i + 1);
       if (!wait_all(&s_full[i % kSP], (uint32_t)(i / kSP) & 1u)) { ok = false; break; }
       tc_fence_after();
       const uint32_t s_tmem = tmem_s0 + (uint32_t)((i % kSP) * kKT + half * kHalfKT) + lane_off;
       uint32_t sv[kHalfKT];
-      tmem_ld_32x32b_x32(s_tmem, sv);
+      tmem_ld_32x32b_x32_nowait(s_tmem, sv);
+      tmem_ld_32x32b_x32_nowait(s_tmem + 32, sv + 32);
+      tmem_wait_ld();
       const bool blk_tile = i < u.nblk;
       const int c0 = blk_tile ? 0 : u.cs + (i - u.nblk) * kKT + half * kHalfKT;
-      float x[kHalfKT];
+      // the tile's mask words to every lane (warp-uniform: before the per-row branches)
+      uint32_t mw_all[kHalfKT / 4];
+#pragma unroll
+      for (int w4 = 0; w4 < kHalfKT / 4; ++w4) mw_all[w4] = __shfl_sync(0xffffffffu, mword, w4);
+      // the scaled logits replace S in sv (as float bits)
       float mh = -INFINITY;
-      // short path: every key of this half-tile is readable (inside the row's prefix and the
-      // chunk, and no mask word has a zero byte)
-      bool all_ok = !blk_tile && row_valid && c0 + kHalfKT <= a_row && c0 + kHalfKT <= u.ce;
+      if (!row_valid) {
 #pragma unroll
-      for (int w4 = 0; w4 < kHalfKT / 4; ++w4) {
-        const uint32_t mw = mask_cur[w4];
-        all_ok = all_ok && (((mw - 0x01010101u) & ~mw & 0x80808080u) == 0u);
-      }
-      if (all_ok) {
-#pragma unroll
-        for (int kk = 0; kk < kHalfKT; ++kk) {
-          x[kk] = __uint_as_float(sv[kk]) * p.scale_log2;
-          mh = fmaxf(mh, x[kk]);
-        }
-      } else if (!row_valid) {
-#pragma unroll
-        for (int kk = 0; kk < kHalfKT; ++kk) x[kk] = -INFINITY;
+        for (int kk = 0; kk < kHalfKT; ++kk) sv[kk] = __float_as_uint(-INFINITY);
       } else if (blk_tile) {
+        // own-block keys: column kk of this half is slot kk - off of this row's block,
+        // readable when that slot is valid
+        const int off = kbo * p.S - i * kKT - half * kHalfKT;
+        const int j0 = max(0, -off), j1 = min(p.S, kHalfKT - off);
+        uint64_t bm = 0;
+        const uint8_t* vrow = p.valid + (size_t)(u.b * p.N + kb) * p.S;
+        for (int jj = j0; jj < j1; ++jj)
+          if (vrow[jj]) bm |= 1ull << (jj + off);
 #pragma unroll
         for (int kk = 0; kk < kHalfKT; ++kk) {
-          const int q = u.k0 * p.S + i * kKT + half * kHalfKT + kk;
-          const int kbk = q / p.S, jj = q - kbk * p.S;
-          const bool okk = kbk == kb && p.valid[(u.b * p.N + kbk) * p.S + jj] != 0;
-          x[kk] = okk ? __uint_as_float(sv[kk]) * p.scale_log2 : -INFINITY;
-          mh = fmaxf(mh, x[kk]);
+          const float v = ((bm >> kk) & 1ull) ? __uint_as_float(sv[kk]) * p.scale_log2 : -INFINITY;
+          sv[kk] = __float_as_uint(v);
+          mh = fmaxf(mh, v);
         }
       } else {
+        // per quarter of 16 keys: a short path when every key is readable (inside the row's
+        // prefix and the chunk, no zero byte in the mask words)
 #pragma unroll
-        for (int w4 = 0; w4 < kHalfKT / 4; ++w4) {
-          const int c = c0 + 4 * w4;
-          const uint32_t mw = mask_cur[w4];
+        for (int qt = 0; qt < kHalfKT / 16; ++qt) {
+          const int cq = c0 + 16 * qt;
+          bool all_ok = cq + 16 <= a_row && cq + 16 <= u.ce;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int kk = 4 * w4 + e;
-            const bool okk = ((mw >> (8 * e)) & 0xFFu) != 0 && c + e < a_row && c + e < u.ce;
-            x[kk] = okk ? __uint_as_float(sv[kk]) * p.scale_log2 : -INFINITY;
-            mh = fmaxf(mh, x[kk]);
+          for (int w4 = 4 * qt; w4 < 4 * qt + 4; ++w4)
+            all_ok = all_ok && (((mw_all[w4] - 0x01010101u) & ~mw_all[w4] & 0x80808080u) == 0u);
+          if (all_ok) {
+#pragma unroll
+            for (int kk = 16 * qt; kk < 16 * qt + 16; ++kk) {
+              const float v = __uint_as_float(sv[kk]) * p.scale_log2;
+              sv[kk] = __float_as_uint(v);
+              mh = fmaxf(mh, v);
+            }
+          } else {
+#pragma unroll
+            for (int w4 = 4 * qt; w4 < 4 * qt + 4; ++w4) {
+              const int c = c0 + 4 * w4;
+              const uint32_t mw = mw_all[w4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int kk = 4 * w4 + e;
+                const bool okk = ((mw >> (8 * e)) & 0xFFu) != 0 && c + e < a_row && c + e < u.ce;
+                const float v = okk ? __uint_as_float(sv[kk]) * p.scale_log2 : -INFINITY;
+                sv[kk] = __float_as_uint(v);
+                mh = fmaxf(mh, v);
+              }
+            }
           }
         }
       }
@@ -409,9 +420,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
           m_run = mt;
         }
       }
+      l_run *= factor;
+      // P = 2^(x - m): an excluded key (x = -inf) gives exactly +0; a row that has not seen
+      // a readable key yet (m_run = -inf) has only excluded keys here.  Packed as fp16 pairs
+      // into the first 32 of this half's 64 S columns.
+      float lsum = 0.f;
+      uint32_t pw[kHalfKT / 2];
+      if (m_run == -INFINITY) {
+#pragma unroll
+        for (int kk = 0; kk < kHalfKT / 2; ++kk) pw[kk] = 0u;
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < kHalfKT / 2; ++kk) {
+          const float p0 = ex2_approx(__uint_as_float(sv[2 * kk]) - m_run);
+          const float p1 = ex2_approx(__uint_as_float(sv[2 * kk + 1]) - m_run);
+          lsum += p0 + p1;
+          const __half2 h2 = __floats2half2_rn(p0, p1);
+          pw[kk] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+      }
+      l_run += lsum;
+      tmem_st_32x32b_x32(s_tmem, pw);
+      // the accumulator is rescaled before PV(i) (released below) adds to it; PV(i - 1)
+      // must have landed first (a finite m_run means there was an earlier tile).  This half
+      // rescales O columns [64*half, 64*half + 64).
       if (__any_sync(0xffffffffu, factor != 1.f)) {
-        // the PV of the previous tile must have landed before the accumulator is touched;
-        // this half rescales O columns [64*half, 64*half + 64)
         if (!wait_all(&pv_done[(i - 1) % kSP], (uint32_t)((i - 1) / kSP) & 1u)) { ok = false; break; }
         tc_fence_after();
         for (int part = 0; part < 2; ++part) {
@@ -422,28 +455,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
           for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
           tmem_st_32x32b_x32(oa, ov);
         }
-        tmem_wait_st();
-        l_run *= factor;
       }
-      // P = 2^(x - m): an excluded key (x = -inf) gives exactly +0; a row that has not seen
-      // a readable key yet (m_run = -inf) has only excluded keys here.  Packed as fp16 pairs
-      // into the first 16 of this half's S columns.
-      float lsum = 0.f;
-      uint32_t pw[kHalfKT / 2];
-      if (m_run == -INFINITY) {
-#pragma unroll
-        for (int kk = 0; kk < kHalfKT / 2; ++kk) pw[kk] = 0u;
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < kHalfKT / 2; ++kk) {
-          const float p0 = ex2_approx(x[2 * kk] - m_run), p1 = ex2_approx(x[2 * kk + 1] - m_run);
-          lsum += p0 + p1;
-          const __half2 h2 = __floats2half2_rn(p0, p1);
-          pw[kk] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
-      }
-      l_run += lsum;
-      tmem_st_32x32b_x16(s_tmem, pw);
       tmem_wait_st();
       // value columns past the last readable key of this tile: zero them (this thread owns
       // V^T row r of key sub-tile `half`) so that whatever the cache holds there cannot
@@ -451,12 +463,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       if (!blk_tile && u.cs + (i - u.nblk) * kKT + kKT > u.a_max) {
         const int st = i % kRing;
         if (!wait_all(&v_full[st], (uint32_t)(i / kRing) & 1u)) { ok = false; break; }
-        const int nvalid = u.a_max - (u.cs + (i - u.nblk) * kKT);
-        // row r of the swizzled [128][64] fp16 tile: 16-byte chunk c (keys 8c .. 8c+7) sits
-        // at chunk position c ^ (r % 8); this half owns chunks 4*half .. 4*half+3
-        uint8_t* rowp = sV + st * kVBytes + (r >> 3) * 1024 + (r & 7) * 128;
-        for (int cc = 0; cc < 4; ++cc) {
-          const int c = half * 4 + cc;
+        const int nvalid = u.a_max - (u.cs + (i - u.nblk) * kKT) - half * kHalfKT;
+        // row r of a swizzled [128][64] fp16 sub-tile: 16-byte chunk c (keys 8c .. 8c+7)
+        // sits at chunk position c ^ (r % 8)
+        uint8_t* rowp = sV + st * kVBytes + half * kVSub + (r >> 3) * 1024 + (r & 7) * 128;
+        for (int c = 0; c < 8; ++c) {
           const int key0 = c * 8;
           if (key0 + 8 <= nvalid) continue;
           uint4* dst = reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) * 16));
@@ -477,8 +488,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       if (lane == 0) mbar_arrive(&p_full[i % kSP]);
     }
     // final accumulator: with one key chunk, O / l straight to the output rows; otherwise a
-    // partial (m, l, O) of this unit.  Each half handles its 64 columns.
-    const bool fin = ok && wait_all(&pv_done[(u.n - 1) % kSP], (uint32_t)((u.n - 1) / kSP) & 1u);
+    // partial (m, l, O) of this unit.  Each half handles its 64 columns.  Every MMA of the
+    // unit has completed once the issuer's final commit (drain) has landed.
+    const bool fin = ok && wait_all(drain, 0);
     if (fin && p.direct) {
       tc_fence_after();
       red_sum[half * 128 + r] = l_run;
@@ -687,13 +699,13 @@ cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream) {
   {
     cuuint64_t dims[3] = {(cuuint64_t)kDH, (cuuint64_t)a.L, (cuuint64_t)planes};
     cuuint64_t str[2] = {(cuuint64_t)kDH * 2, (cuuint64_t)a.L * kDH * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)kKT, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)kKT, 1};  // [kKT keys][64 dh]
     if (!encode_f16(&mkc, a.kv_layer, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     cuuint64_t dims[3] = {(cuuint64_t)a.L, (cuuint64_t)kDH, (cuuint64_t)planes};
     cuuint64_t str[2] = {(cuuint64_t)a.L * 2, (cuuint64_t)a.L * kDH * 2};
-    cuuint32_t box[3] = {(cuuint32_t)kKT, (cuuint32_t)kDH, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)kDH, 1};  // [128 dh][64 keys]
     if (!encode_f16(&mvc, a.kv_layer, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
@@ -706,7 +718,7 @@ cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream) {
   {
     cuuint64_t dims[2] = {(cuuint64_t)a.N * a.S, (cuuint64_t)a.B * a.Hkv * kDH};
     cuuint64_t str[1] = {(cuuint64_t)a.ns_pad * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kKT, (cuuint32_t)kDH};
+    cuuint32_t box[2] = {64, (cuuint32_t)kDH};  // [128 dh][64 keys]
     if (!encode_f16(&mvb, a.vbt, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   static bool attr = false;
