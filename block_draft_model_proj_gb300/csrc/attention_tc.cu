@@ -142,8 +142,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
   uint64_t* v_empty = v_full + kRing;
   uint64_t* s_full = v_empty + kRing;
   uint64_t* p_full = s_full + kSP;
-  uint64_t* pv_done = p_full + kSP;
-  uint64_t* q_ready = pv_done + kSP;
+  uint64_t* q_ready = p_full + kSP;
   uint64_t* drain = q_ready + 1;
   uint64_t* max_bar = drain + 1;    // [2]: row-max exchange of tiles with parity 0 / 1
   uint64_t* sum_bar = max_bar + 2;  // row-sum exchange at the end
@@ -163,7 +162,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
     for (int i = 0; i < kSP; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], kSoftmaxWarps);
-      mbar_init(&pv_done[i], 1);
     }
     mbar_init(q_ready, kSoftmaxWarps);
     mbar_init(drain, 1);
@@ -236,7 +234,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       // softmax has written P_i and V_i has landed, followed at once by S(i + 2) into the
       // buffer P_i occupied.  The tensor core performs one thread's MMAs in issue order, so
       // S(i + 2) overwrites that buffer only after PV(i) has read it.  Each MMA costs this
-      // thread about a hundred cycles whatever its N, so S uses N = 128 keys per instruction.
+      // thread about a hundred cycles whatever its N, so S uses N = 128 keys per instruction,
+      // and one commit follows each group of MMAs (a second commit right behind the first
+      // holds this thread for a few hundred cycles more): PV(i)'s completion (v_empty) frees
+      // V stage i and tells the softmax the accumulator is up to date; S's (s_full) hands the
+      // scores to the softmax, whose first reader frees the K stage.
       bool ok = mbar_wait(q_ready, 0, abort_flag, kWaitLimitNs);
       tc_fence_after();
       auto issue_s = [&](int s) -> bool {
@@ -251,7 +253,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
           umma_f16_ts(s_tmem, tmem_q + k * 8, sw128_desc(k_addr + (k >> 2) * kKSub + (k & 3) * 32),
                       kIdescS, k ? 1u : 0u);
         umma_commit(&s_full[s % kSP]);
-        umma_commit(&k_empty[s % kRing]);
         return true;
       };
       for (int s = 0; s < kSP && s < u.n && ok; ++s) ok = issue_s(s);
@@ -270,7 +271,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
           umma_f16_ts(tmem_o, a_base + (k >> 2) * 64 + (k & 3) * 8,
                       sw128_desc(v_addr + (k >> 2) * kVSub + (k & 3) * 32), kIdescPV,
                       (i == 0 && k == 0) ? 0u : 1u);
-        umma_commit(&pv_done[i % kSP]);
         umma_commit(&v_empty[i % kRing]);
         if (i + kSP < u.n) ok = issue_s(i + kSP);
       }
@@ -335,6 +335,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       const uint32_t mword = mword_next;
       mword_next = load_mask(i + 1);
       if (!wait_all(&s_full[i % kSP], (uint32_t)(i / kSP) & 1u)) { ok = false; break; }
+      // S(i) has completed: its K stage may be refilled
+      if (warp == 2 && lane == 0) mbar_arrive(&k_empty[i % kRing]);
       tc_fence_after();
       const uint32_t s_tmem = tmem_s0 + (uint32_t)((i % kSP) * kKT + half * kHalfKT) + lane_off;
       uint32_t sv[kHalfKT];
@@ -442,10 +444,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       l_run += lsum;
       tmem_st_32x32b_x32(s_tmem, pw);
       // the accumulator is rescaled before PV(i) (released below) adds to it; PV(i - 1)
-      // must have landed first (a finite m_run means there was an earlier tile).  This half
-      // rescales O columns [64*half, 64*half + 64).
+      // must have landed first (a finite m_run means there was an earlier tile; its
+      // completion is the phase of v_empty that frees its V stage).  This half rescales O
+      // columns [64*half, 64*half + 64).
       if (__any_sync(0xffffffffu, factor != 1.f)) {
-        if (!wait_all(&pv_done[(i - 1) % kSP], (uint32_t)((i - 1) / kSP) & 1u)) { ok = false; break; }
+        if (!wait_all(&v_empty[(i - 1) % kRing], (uint32_t)((i - 1) / kRing) & 1u)) { ok = false; break; }
         tc_fence_after();
         for (int part = 0; part < 2; ++part) {
           uint32_t ov[32];
