@@ -648,10 +648,12 @@ AttnTcLayout attention_tc_layout(int B, int N, int S, int L, int Hq, int Hkv, in
   const double per_unit = (double)L * B * Hkv * lay.tiles / (4.0 * (num_sms > 0 ? num_sms : 1));
   lay.chunk = 256;
   while (lay.chunk < 4096 && lay.chunk < per_unit) lay.chunk *= 2;
-  // one chunk when the (row, KV head, tile) units alone fill the SMs and no unit is long
-  // (each then normalises its own output: no partials, no combine pass)
+  // one chunk when the (row, KV head, tile) units alone nearly fill the SMs (three
+  // quarters or more) and no unit is long: each unit then normalises its own output (no
+  // partials, no combine pass), and its fixed cost -- tensor memory, Q, the first K/V tiles
+  // in flight, about two key tiles' worth -- is paid once per tile instead of once per chunk
   const long base_units = (long)B * Hkv * lay.tiles;
-  if (L <= 4096 && base_units >= (num_sms > 0 ? num_sms : 1))
+  if (L <= 4096 && 4 * base_units >= 3L * (num_sms > 0 ? num_sms : 1))
     lay.chunk = (L + kKT - 1) / kKT * kKT;
   lay.max_chunks = (L + lay.chunk - 1) / lay.chunk;
   if (lay.max_chunks < 1) lay.max_chunks = 1;
