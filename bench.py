@@ -67,7 +67,12 @@ def algorithmic_work(w: di.Workload, plan: dict, mask: np.ndarray) -> dict:
     f_ctxkv = 2.0 * ctx_pos * D * kvw * NL
     f_layers = 2.0 * tv * D * (s.qkv_width + s.q_width + 2 * s.intermediate + s.intermediate) * NL
     f_attn = 4.0 * s.head_dim * s.num_heads * pairs * NL
+    # context K/V cache read by attention: every readable position of a row (c < its largest
+    # anchor, mask = 1) once per layer, K and V, fp16 (bf16 configuration) or fp32
+    cache_elem = 2.0 if s.dtype == "bf16" else 4.0
+    attn_bytes = ctx_pos * 2.0 * s.kv_width * cache_elem * NL
     return {"layer_weight_bytes": 2.0 * layer_params, "ctx_weight_bytes": 2.0 * ctx_params,
+            "attn_cache_bytes": attn_bytes,
             "ctx_positions": ctx_pos, "valid_slots": tv, "gemm_flops": f_proj + f_ctxkv + f_layers,
             "attn_flops": f_attn, "total_flops": f_proj + f_ctxkv + f_layers + f_attn,
             "proj_flops": f_proj, "ctxkv_flops": f_ctxkv, "layer_flops": f_layers}
@@ -387,6 +392,27 @@ def timed(fn, steps, torch, stream, barrier):
     return t0.elapsed_time(t1)
 
 
+def attention_roofline(work: dict, a_ms: float, steps: int, peak_tflops: float,
+                       hbm_gbs: float) -> dict:
+    """Attention against the roofline that binds it: its FLOPs at the tensor peak or its
+    context K/V bytes at the HBM peak, whichever takes longer (decode steps read a long cache
+    for few queries and are HBM-bound)."""
+    flops, nbytes = work["attn_flops"], work["attn_cache_bytes"]
+    t_tensor = flops / (peak_tflops * 1e12)
+    t_hbm = nbytes / (hbm_gbs * 1e9)
+    sec = a_ms / 1e3 / steps if a_ms else None
+    out = {"flop_per_step": flops, "bytes_per_step": nbytes,
+           "frac_tensor": t_tensor / sec if sec else None,
+           "frac_hbm": t_hbm / sec if sec else None}
+    if t_hbm > t_tensor:
+        out.update({"bound": "hbm", "achieved": nbytes / sec / 1e9 if sec else None,
+                    "peak": hbm_gbs, "unit": "GB/s", "frac": out["frac_hbm"]})
+    else:
+        out.update({"bound": "tensor", "achieved": flops / sec / 1e12 if sec else None,
+                    "peak": peak_tflops, "unit": "TFLOP/s", "frac": out["frac_tensor"]})
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import block_draft_model_proj_gb300 as dflash
@@ -496,11 +522,7 @@ def run_ours(args, rank, world, local_rank):
                    "achieved": v_bytes * args.steps / (v_ms / 1e3) / 1e9 if v_ms else None,
                    "peak": hbm, "unit": "GB/s",
                    "frac": v_bytes * args.steps / (v_ms / 1e3) / 1e9 / hbm if v_ms else None},
-        "attention": {"bound": "tensor", "flop_per_step": work["attn_flops"],
-                      "achieved": work["attn_flops"] * args.steps / (a_ms / 1e3) / 1e12
-                      if a_ms else None, "peak": peak, "unit": "TFLOP/s",
-                      "frac": work["attn_flops"] * args.steps / (a_ms / 1e3) / 1e12 / peak
-                      if a_ms else None},
+        "attention": attention_roofline(work, a_ms, args.steps, peak, hbm),
     }
     result = {
         "metric": METRIC, "value": value, "unit": "block-positions/s", "n_gpus": world,
