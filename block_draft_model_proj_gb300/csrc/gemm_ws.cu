@@ -56,7 +56,9 @@ constexpr uint32_t kWBytes = 128 * kBK * 2;             // 16 KB weight tile
 constexpr uint32_t kRingBytes = 196 * 1024;             // shared-memory ring budget
 constexpr uint32_t kTmemCols = 512;                     // acc 256, A ring 8 x 32
 constexpr uint32_t kTmemAcc = 0, kTmemA = 256;
-constexpr size_t kSmemBytes = 1024 + kRingBytes + 512;
+constexpr uint32_t kEpiBufFloats = 32 * 36;             // per epilogue warp: [32][32 + 4]
+constexpr size_t kSmemBytes = 1024 + kRingBytes + 512 + 4 * kEpiBufFloats * sizeof(float);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 struct WsParams {
   long M;            // token rows of X (and C)
@@ -80,6 +82,8 @@ struct WsParams {
   int epi;
   float* C;
   long ldc;
+  int c_vec;         // C rows 16-byte aligned (ldc % 4 == 0, C 16-byte aligned)
+  int act_vec;       // SwiGLU output rows 4-element aligned (I % 4 == 0, 8-byte base)
   ActOut act;        // kEpiSwiGLU
   int swiglu_I;
   KvCacheEpilogue kv;  // kEpiKvCache
@@ -148,15 +152,33 @@ __device__ __forceinline__ uint32_t cvt_pair(uint32_t w, bool bf16, uint32_t& ma
 // chunks of 32.
 
 __device__ __forceinline__ void epi_f32(const WsParams& p, uint32_t tacc, int wt, int tt, int rows,
-                                        int z, int r) {
+                                        int z, int r, int lane, float* buf) {
   float* Cz = p.C + (long)z * p.M * p.ldc;
-  const int n = wt * kWM + r;
+  const int n0 = wt * kWM + (r - lane);  // this warp's 32 weight rows start here
+  const int n = n0 + lane;
   const bool n_ok = n < p.Nw;
+  // 32 x 32 blocks turned through shared memory so each lane writes 16-byte pieces of token
+  // rows (a warp store covers four rows of 128 bytes) instead of one float per token
+  const bool vec = p.c_vec && n0 + 32 <= p.Nw;
 #pragma unroll 1
   for (int c = 0; c * 32 < rows; ++c) {
     uint32_t v[32];
     tmem_ld_32x32b_x32(tacc + c * 32, v);
     const long t0 = (long)tt * kTT + c * 32;
+    if (vec) {
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) buf[j * 36 + lane] = __uint_as_float(v[j]);
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int j = 4 * q + (lane >> 3);
+        if (c * 32 + j < rows)
+          *reinterpret_cast<float4*>(Cz + (t0 + j) * p.ldc + n0 + 4 * (lane & 7)) =
+              *reinterpret_cast<const float4*>(buf + j * 36 + 4 * (lane & 7));
+      }
+      continue;
+    }
     if (!n_ok) continue;
 #pragma unroll 8
     for (int j = 0; j < 32; ++j)
@@ -167,9 +189,10 @@ __device__ __forceinline__ void epi_f32(const WsParams& p, uint32_t tacc, int wt
 // Lanes 2i / 2i+1 hold gate / up of channel wt*64 + i.  The pair trades halves so that the
 // even lane forms tokens 0..15 and the odd lane tokens 16..31 of each chunk.
 __device__ __forceinline__ void epi_swiglu(const WsParams& p, uint32_t tacc, int wt, int tt,
-                                           int rows, int r, int lane) {
+                                           int rows, int r, int lane, float* buf) {
   const int I = p.swiglu_I;
   const int ch = wt * 64 + (r >> 1);
+  const int ch_w = wt * 64 + ((r - lane) >> 1);  // this warp's 16 channels start here
   const bool odd = lane & 1;
 #pragma unroll 1
   for (int c = 0; c * 32 < rows; ++c) {
@@ -177,6 +200,30 @@ __device__ __forceinline__ void epi_swiglu(const WsParams& p, uint32_t tacc, int
     tmem_ld_32x32b_x32(tacc + c * 32, v);
     const int j0 = c * 32 + (odd ? 16 : 0);
     const long t0 = (long)tt * kTT + j0;
+    if (p.act_vec) {
+      // [32 tokens][16 channels] through shared memory: each lane then writes runs of four
+      // channels of one token
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float mine = __uint_as_float(odd ? v[j] : v[16 + j]);
+        const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+        const float g = odd ? other : __uint_as_float(v[j]);
+        const float u = odd ? __uint_as_float(v[16 + j]) : other;
+        buf[((odd ? 16 : 0) + j) * 20 + (lane >> 1)] = g / (1.f + expf(-g)) * u;
+      }
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int idx = q * 32 + lane;
+        const int tok = idx >> 2, c4 = idx & 3;
+        const int ch0 = ch_w + 4 * c4;
+        if (c * 32 + tok < rows && ch0 < I)
+          p.act.store4(((long)tt * kTT + c * 32 + tok) * I + ch0,
+                       *reinterpret_cast<const float4*>(buf + tok * 20 + 4 * c4));
+      }
+      continue;
+    }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const float mine = __uint_as_float(odd ? v[j] : v[16 + j]);
@@ -280,6 +327,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
   uint64_t* drain = tempty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* epi_buf = reinterpret_cast<float*>(smem + kRingBytes + 512);  // [4][kEpiBufFloats]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -467,8 +515,9 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         const int rows = h ? x.rows1 : x.rows0;
         if (tt < 0) break;
         const uint32_t tacc = tmem + kTmemAcc + (uint32_t)(h * kTT) + lane_off;
-        if (p.epi == kEpiF32) epi_f32(p, tacc, x.wt, tt, rows, x.z, r);
-        else if (p.epi == kEpiSwiGLU) epi_swiglu(p, tacc, x.wt, tt, rows, r, lane);
+        float* buf = epi_buf + (warp - 10) * kEpiBufFloats;
+        if (p.epi == kEpiF32) epi_f32(p, tacc, x.wt, tt, rows, x.z, r, lane, buf);
+        else if (p.epi == kEpiSwiGLU) epi_swiglu(p, tacc, x.wt, tt, rows, r, lane, buf);
         else epi_kv(p, tacc, x.wt, tt, rows, r, lane, bad);
       }
       tc_fence_before();
@@ -566,8 +615,10 @@ cudaError_t launch(const WsArgs& a, int epi, int w_tiles, int interleave, const 
   p.epi = epi;
   p.C = a.C;
   p.ldc = a.ldc;
+  p.c_vec = (a.ldc % 4 == 0) && ((uintptr_t)a.C % 16 == 0);
   if (act) p.act = *act;
   p.swiglu_I = epi == kEpiSwiGLU ? a.Nw / 2 : 0;
+  p.act_vec = act && p.swiglu_I % 4 == 0 && ((uintptr_t)act->p % 16 == 0);
   if (kv) p.kv = *kv;
   p.status = a.status;
   // enough CTAs for the largest schedule the device can pick (all token tiles active)
