@@ -285,6 +285,14 @@ __device__ __forceinline__ void store4(__half* dst, float4 v) {
   *reinterpret_cast<uint2*>(dst) = w;
 }
 
+// two consecutive elements (dst 2-element aligned)
+__device__ __forceinline__ void store_pair(float* dst, float a, float b) {
+  *reinterpret_cast<float2*>(dst) = make_float2(a, b);
+}
+__device__ __forceinline__ void store_pair(__half* dst, float a, float b) {
+  *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(a, b);
+}
+
 // Q and K heads with RoPE: one thread per (row t, head, 4 consecutive pairs i .. i+3), the
 // pairs (i, i + dh/2) rotated by the angle of position pos[t].  dh % 8 == 0.
 template <typename OutT>
@@ -341,9 +349,11 @@ __global__ void qk_rope_kernel(const float* __restrict__ y, int nsplit,
   }
 }
 
-// V heads, transposed through shared memory: one block per (row b, KV head g, 32 slots);
-// reads 32 rows x dh channels (coalesced along the channels) and writes dh rows of 32
-// slots of vbt (coalesced along the slots).  dh <= 256.
+// V heads, transposed through shared memory: one block per (row b, KV head g, 32 slots).
+// Each thread loads float4 pieces of the slots' V rows (a warp reads one 128-float row,
+// coalesced along the channels), all of them before the first is used, then the block
+// writes dh rows of 32 slots of vbt, two slots per store (coalesced along the slots).
+// dh % 4 == 0, dh <= 256.
 constexpr int kVtSlots = 32;
 template <typename OutT>
 __global__ void __launch_bounds__(256) v_transpose_kernel(
@@ -353,7 +363,6 @@ __global__ void __launch_bounds__(256) v_transpose_kernel(
   pdl_wait();
   pdl_trigger();
   __shared__ float tile[kVtSlots][257];
-  __shared__ uint8_t slot_ok[kVtSlots];
   if (nsplit_dev) nsplit = *nsplit_dev;
   const int NS = N * S;
   const int tiles = (NS + kVtSlots - 1) / kVtSlots;
@@ -363,38 +372,54 @@ __global__ void __launch_bounds__(256) v_transpose_kernel(
   const int ks0 = bt * kVtSlots;
   const long width = (long)(Hq + 2 * Hkv) * dh;
   const int vcol = (Hq + Hkv + g) * dh;
-  if (threadIdx.x < kVtSlots) {
-    const int ks = ks0 + threadIdx.x;
-    slot_ok[threadIdx.x] = ks < NS && valid[(long)b * NS + ks] != 0;
-  }
-  // the loads do not wait for the validity flags: rows of invalid slots (whose GEMM rows may
-  // be unwritten) are read and then discarded by the select below
-  for (int idx0 = threadIdx.x; idx0 < kVtSlots * dh; idx0 += 8 * blockDim.x) {
-    float v[8];
+  const int d4n = dh / 4;                 // float4 pieces per row
+  const int pieces = kVtSlots * d4n;      // <= 2048
+  // up to 8 pieces per thread; rows of invalid slots (whose GEMM rows may be unwritten) are
+  // read and then discarded by the select, so the loads do not wait for the flags
+  float4 acc[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = 0.f;
-    for (int sp = 0; sp < nsplit; ++sp) {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int idx = idx0 + u * blockDim.x;
-        const int jj = idx / dh, d = idx - jj * dh;
-        const int ks = min(ks0 + jj, NS - 1);
-        if (idx < kVtSlots * dh)
-          v[u] += y[sp * split_stride + ((long)b * NS + ks) * width + vcol + d];
-      }
-    }
-    __syncthreads();  // slot_ok is written
+  for (int u = 0; u < 8; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int sp = 0; sp < nsplit; ++sp) {
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int idx = idx0 + u * blockDim.x;
-      if (idx < kVtSlots * dh) tile[idx / dh][idx % dh] = slot_ok[idx / dh] ? v[u] : 0.f;
+      const int pc = threadIdx.x + u * 256;
+      if (pc < pieces) {
+        const int jj = pc / d4n, d4 = pc - jj * d4n;
+        const int ks = min(ks0 + jj, NS - 1);
+        const float4 f = *reinterpret_cast<const float4*>(
+            y + sp * split_stride + ((long)b * NS + ks) * width + vcol + 4 * d4);
+        acc[u].x += f.x;
+        acc[u].y += f.y;
+        acc[u].z += f.z;
+        acc[u].w += f.w;
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int pc = threadIdx.x + u * 256;
+    if (pc < pieces) {
+      const int jj = pc / d4n, d4 = pc - jj * d4n;
+      const int ks = ks0 + jj;
+      const bool ok = ks < NS && valid[(long)b * NS + ks] != 0;
+      tile[jj][4 * d4] = ok ? acc[u].x : 0.f;
+      tile[jj][4 * d4 + 1] = ok ? acc[u].y : 0.f;
+      tile[jj][4 * d4 + 2] = ok ? acc[u].z : 0.f;
+      tile[jj][4 * d4 + 3] = ok ? acc[u].w : 0.f;
     }
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < dh * kVtSlots; idx += blockDim.x) {
-    const int d = idx / kVtSlots, jj = idx - d * kVtSlots;
-    const int ks = ks0 + jj;
-    if (ks < ns_pad) vbt[((long)bg * dh + d) * ns_pad + ks] = from_f<OutT>(tile[jj][d]);
+  // row d of vbt: slots ks0 .. ks0 + 31 as 16 pairs
+  for (int idx = threadIdx.x; idx < dh * (kVtSlots / 2); idx += blockDim.x) {
+    const int d = idx / (kVtSlots / 2), pr = idx - d * (kVtSlots / 2);
+    const int ks = ks0 + 2 * pr;
+    OutT* dst = vbt + ((long)bg * dh + d) * ns_pad + ks;
+    const float v0 = tile[2 * pr][d], v1 = tile[2 * pr + 1][d];
+    if (ks + 1 < ns_pad) {
+      store_pair(dst, v0, v1);
+    } else if (ks < ns_pad) {
+      dst[0] = from_f<OutT>(v0);
+    }
   }
 }
 
