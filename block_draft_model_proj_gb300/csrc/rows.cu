@@ -594,33 +594,23 @@ cudaError_t launch_qkv_rope(const float* y, int nsplit, const int* nsplit_dev, c
   const long stride = T * (long)(Hq + 2 * Hkv) * dh;
   const long B = T / ((long)N * S);
   const int vblocks = (int)(B * Hkv * ((N * S + kVtSlots - 1) / kVtSlots));
+  cudaError_t e;
   if (f16) {
-    {
-    const cudaError_t le = launch_pdl(qk_rope_kernel<__half>, dim3(grid_for(n, 256)), dim3(256), 0,
-        stream, y, nsplit, nsplit_dev, stride, pos, valid, cos_t, sin_t, P, static_cast<__half*>(q),
-        static_cast<__half*>(kb), T, N, S, Hq, Hkv, dh, status);
-    if (le != cudaSuccess) return le;
-  }
-    {
-    const cudaError_t le = launch_pdl(v_transpose_kernel<__half>, dim3(vblocks), dim3(256), 0,
-        stream, y, nsplit, nsplit_dev, stride, valid, static_cast<__half*>(vbt), ns_pad, N, S, Hq,
-        Hkv, dh);
-    if (le != cudaSuccess) return le;
-  }
+    e = launch_pdl(qk_rope_kernel<__half>, dim3(grid_for(n, 256)), dim3(256), 0, stream, y, nsplit,
+                   nsplit_dev, stride, pos, valid, cos_t, sin_t, P, static_cast<__half*>(q),
+                   static_cast<__half*>(kb), T, N, S, Hq, Hkv, dh, status);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(v_transpose_kernel<__half>, dim3(vblocks), dim3(256), 0, stream, y, nsplit,
+                   nsplit_dev, stride, valid, static_cast<__half*>(vbt), ns_pad, N, S, Hq, Hkv, dh);
   } else {
-    {
-    const cudaError_t le = launch_pdl(qk_rope_kernel<float>, dim3(grid_for(n, 256)), dim3(256), 0,
-        stream, y, nsplit, nsplit_dev, stride, pos, valid, cos_t, sin_t, P, static_cast<float*>(q),
-        static_cast<float*>(kb), T, N, S, Hq, Hkv, dh, status);
-    if (le != cudaSuccess) return le;
+    e = launch_pdl(qk_rope_kernel<float>, dim3(grid_for(n, 256)), dim3(256), 0, stream, y, nsplit,
+                   nsplit_dev, stride, pos, valid, cos_t, sin_t, P, static_cast<float*>(q),
+                   static_cast<float*>(kb), T, N, S, Hq, Hkv, dh, status);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(v_transpose_kernel<float>, dim3(vblocks), dim3(256), 0, stream, y, nsplit,
+                   nsplit_dev, stride, valid, static_cast<float*>(vbt), ns_pad, N, S, Hq, Hkv, dh);
   }
-    {
-    const cudaError_t le = launch_pdl(v_transpose_kernel<float>, dim3(vblocks), dim3(256), 0,
-        stream, y, nsplit, nsplit_dev, stride, valid, static_cast<float*>(vbt), ns_pad, N, S, Hq,
-        Hkv, dh);
-    if (le != cudaSuccess) return le;
-  }
-  }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

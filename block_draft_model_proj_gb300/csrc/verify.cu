@@ -223,31 +223,22 @@ cudaError_t launch_verify(const void* logits, int dtype, const int32_t* draft, i
   const size_t elem = dtype == DFLASH_DTYPE_BF16 ? 2 : 4;
   const bool vec_ok = ((uintptr_t)logits % 16 == 0) && ((size_t)V * elem % 16 == 0) &&
                       ((size_t)vp.chunk_len * elem % 16 == 0);
-  if (dtype == DFLASH_DTYPE_BF16) {
-    {
-    const cudaError_t le = launch_pdl(argmax_partial_kernel<__nv_bfloat16>, dim3(grid),
-        dim3(kVerifyThreads), 0, stream, (const __nv_bfloat16*)logits, V, vp.chunks, vp.chunk_len,
-        vec_ok, part_v, part_i);
-    if (le != cudaSuccess) return le;
-  }
-  } else {
-    {
-    const cudaError_t le = launch_pdl(argmax_partial_kernel<float>, dim3(grid),
-        dim3(kVerifyThreads), 0, stream, (const float*)logits, V, vp.chunks, vp.chunk_len, vec_ok,
-        part_v, part_i);
-    if (le != cudaSuccess) return le;
-  }
-  }
+  const cudaError_t le =
+      dtype == DFLASH_DTYPE_BF16
+          ? launch_pdl(argmax_partial_kernel<__nv_bfloat16>, dim3(grid), dim3(kVerifyThreads), 0,
+                       stream, (const __nv_bfloat16*)logits, V, vp.chunks, vp.chunk_len, vec_ok,
+                       part_v, part_i)
+          : launch_pdl(argmax_partial_kernel<float>, dim3(grid), dim3(kVerifyThreads), 0, stream,
+                       (const float*)logits, V, vp.chunks, vp.chunk_len, vec_ok, part_v, part_i);
+  if (le != cudaSuccess) return le;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = 4;
   const size_t smem = (size_t)warps * (gamma + 1) * sizeof(int);
-  {
-    const cudaError_t le = launch_pdl(verify_scan_kernel, dim3((B + warps - 1) / warps),
-        dim3(warps * 32), smem, stream, part_v, part_i, vp.chunks, draft, B, gamma, eos, emitted,
-        num_emitted, accepted, choices);
-    if (le != cudaSuccess) return le;
-  }
+  e = launch_pdl(verify_scan_kernel, dim3((B + warps - 1) / warps), dim3(warps * 32), smem, stream,
+                 part_v, part_i, vp.chunks, draft, B, gamma, eos, emitted, num_emitted, accepted,
+                 choices);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
