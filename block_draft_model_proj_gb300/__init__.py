@@ -85,6 +85,8 @@ _SIGS = {
     "dflash_testing_gemm": (_I, [_I, _I, _P, _L, _P, _L, _P, _L, _L, _I, _I, _I, _P]),
     "dflash_testing_gemm_splits": (_I, [_L, _I, _I]),
     "dflash_testing_gemm_ws": (_I, [_P, _L, _P, _I, _L, _P, _L, _L, _I, _I, _I, _P, _P, _P]),
+    "dflash_testing_verify_plan": (_I, [_I, _I, _I, _L, _L, ctypes.POINTER(_I),
+                                       ctypes.POINTER(_I)]),
     "dflash_profile_enable": (_I, [_I]),
     "dflash_profile_read": (_I, [_I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_L)]),
     "dflash_launch_count": (_L, []),
@@ -293,6 +295,14 @@ def dflash_testing_gemm_ws(X, W, w_dtype, C, max_splits, splits_out, tile_list=N
     _check(load().dflash_testing_gemm_ws(_ptr(X), X.stride(0), _ptr(W), w_dtype, W.stride(0),
                                          _ptr(C), C.stride(-2), M, N, K, max_splits,
                                          _ptr(tile_list), _ptr(splits_out), _stream(stream)))
+
+
+def dflash_testing_verify_plan(B, gamma, V, resident_ctas, static_entries=0) -> tuple:
+    """(chunks, chunk_len) of the verification argmax for these sizes (host arithmetic)."""
+    c, n = ctypes.c_int(), ctypes.c_int()
+    _check(load().dflash_testing_verify_plan(B, gamma, V, resident_ctas, static_entries,
+                                             ctypes.byref(c), ctypes.byref(n)))
+    return c.value, n.value
 
 
 def dflash_profile_enable(on: bool = True) -> None:

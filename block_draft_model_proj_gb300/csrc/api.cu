@@ -283,6 +283,12 @@ bool convert_layers(const dflash_config_t* c, long tokens) {
          !layer_gemm_ws(c, tokens);
 }
 
+// The context K/V projection (dflash_project_context) reads fp16 layer weights: bf16 ones
+// are converted inside the call, independently of how the body dispatches its projections.
+bool context_kv_needs_convert(const dflash_config_t* c) {
+  return c->dtype == DFLASH_DTYPE_BF16 && layer_wdtype(c) == DFLASH_DTYPE_BF16;
+}
+
 // Upper bound for a device-chosen K-split: about three waves of output tiles (tile_n
 // columns x 128 rows) when every row tile is active, at most 8.
 int ws_max_splits(int Nw, long T, int tile_n = 128) {
@@ -317,7 +323,9 @@ ProjLayout proj_layout(const dflash_config_t* c, int B, int L, void* ws) {
   p.cos_t = cv.take<float>((size_t)L * (c->head_dim / 2));
   p.sin_t = cv.take<float>((size_t)L * (c->head_dim / 2));
   p.tile_list = cv.take<int32_t>(1 + (size_t)(M + kGemmTileM - 1) / kGemmTileM);
-  p.wkv16 = convert_layers(c, M) ? cv.take<__half>((size_t)kvw * D) : nullptr;
+  // the context K/V projection always runs on the 128 x 256-tile GEMM with fp16 operands:
+  // bf16 layer weights are converted into the workspace whatever the row count
+  p.wkv16 = context_kv_needs_convert(c) ? cv.take<__half>((size_t)kvw * D) : nullptr;
   p.bytes = cv.off;
   return p;
 }
@@ -778,6 +786,8 @@ int dflash_verify_greedy(const void* logits, int logits_dtype, const int32_t* dr
   if (B < 1 || gamma < 0 || V < 1)
     return fail(DFLASH_ERR_INVALID_ARG,
                 "need B >= 1, gamma >= 0, V >= 1 (one target choice per draft token plus a bonus)");
+  if (gamma > kMaxVerifyGamma)
+    return fail(DFLASH_ERR_INVALID_ARG, "gamma (%d) must be <= %d", gamma, kMaxVerifyGamma);
   if (logits_dtype != DFLASH_DTYPE_BF16 && logits_dtype != DFLASH_DTYPE_F32)
     return fail(DFLASH_ERR_INVALID_ARG, "logits_dtype must be DFLASH_DTYPE_BF16 or _F32");
   if (!logits || (!draft && gamma > 0) || !emitted || !num_emitted || !accepted)

@@ -43,7 +43,19 @@ struct VerifyPlan {
   int chunk_len = 0;
   size_t ws_bytes = 0;
 };
+// Chunks per row for `rows` rows of V logits: about three waves of the resident CTAs,
+// chunks of at least 4096 elements, chunk_len a multiple of 8.
+VerifyPlan plan_verify_for(long rows, int V, long resident_ctas);
 VerifyPlan plan_verify(int B, int gamma, int V, int num_sms);
+// At most max_entries partials in all: fewer, longer chunks when rows * chunks exceeds it
+// (rows <= max_entries).  Keeps chunk_len % 8 == 0 and chunks * chunk_len >= V.
+VerifyPlan cap_verify_chunks(VerifyPlan vp, long rows, int V, long max_entries);
+// Dynamic shared memory of the prefix-scan kernel: (gamma + 1) ints per warp, up to four
+// warps; above the default 48 KB the launch raises the kernel's limit, up to kScanSmemMax.
+constexpr size_t kScanSmemDefault = 48 * 1024;
+constexpr size_t kScanSmemMax = 227 * 1024;
+// Largest gamma the verification calls accept: one warp's (gamma + 1) choices in shared memory.
+constexpr int kMaxVerifyGamma = (int)(kScanSmemMax / sizeof(int)) - 1;
 cudaError_t launch_verify(const void* logits, int dtype, const int32_t* draft, int B, int gamma,
                           int V, int32_t eos, int32_t* emitted, int32_t* num_emitted,
                           int32_t* accepted, int32_t* choices, float* part_v, int* part_i,

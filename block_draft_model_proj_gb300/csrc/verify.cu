@@ -13,6 +13,8 @@
 // keep the lower index, so the result does not depend on the split.
 // Kernel 2: one warp per request combines its rows' partials in chunk order and runs the
 // accepted-prefix scan.
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -21,6 +23,7 @@ namespace dflash {
 namespace {
 
 constexpr int kVerifyThreads = 256;
+constexpr int kMaxVerifyDevices = 64;
 
 struct ArgMax {
   float v;
@@ -188,21 +191,10 @@ __global__ void verify_scan_kernel(const float* __restrict__ part_v, const int* 
 
 }  // namespace
 
-VerifyPlan plan_verify(int B, int gamma, int V, int num_sms) {
+VerifyPlan plan_verify_for(long rows, int V, long resident_ctas) {
   VerifyPlan vp;
-  const long rows = (long)B * (gamma + 1);
-  // resident argmax CTAs on the whole GPU
-  static int per_sm = 0;
-  if (per_sm == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, argmax_partial_kernel<__nv_bfloat16>,
-                                                      kVerifyThreads, 0) != cudaSuccess || n < 1)
-      n = 4;
-    per_sm = n;
-  }
-  const long resident = (long)per_sm * (num_sms > 0 ? num_sms : 1);
   // about three waves of resident CTAs, chunks of at least 4096 elements
-  long best = (3 * resident + rows - 1) / rows;
+  long best = (3 * resident_ctas + rows - 1) / rows;
   const long max_chunks = (V + 4095) / 4096;
   if (best > max_chunks) best = max_chunks;
   if (best < 1) best = 1;
@@ -212,6 +204,41 @@ VerifyPlan plan_verify(int B, int gamma, int V, int num_sms) {
   vp.chunks = (int)((V + len - 1) / len);
   vp.ws_bytes = (size_t)rows * vp.chunks * (sizeof(float) + sizeof(int));
   return vp;
+}
+
+VerifyPlan cap_verify_chunks(VerifyPlan vp, long rows, int V, long max_entries) {
+  if ((long)vp.chunks * rows <= max_entries) return vp;
+  // fewer, longer chunks: at most max_entries / rows of them, each a multiple of 8
+  // elements (16-byte aligned vector loads); ceil(V / len) <= that count since
+  // len >= V / count
+  const long chunks = max_entries / rows;
+  long len = ((long)V + chunks - 1) / chunks;
+  len = (len + 7) / 8 * 8;
+  vp.chunk_len = (int)len;
+  vp.chunks = (int)(((long)V + len - 1) / len);
+  vp.ws_bytes = (size_t)rows * vp.chunks * (sizeof(float) + sizeof(int));
+  return vp;
+}
+
+VerifyPlan plan_verify(int B, int gamma, int V, int num_sms) {
+  const long rows = (long)B * (gamma + 1);
+  // resident argmax CTAs per SM, looked up once per device
+  static std::atomic<int> per_sm_cache[kMaxVerifyDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxVerifyDevices) dev = -1;
+  int per_sm = dev >= 0 ? per_sm_cache[dev].load(std::memory_order_relaxed) : 0;
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, argmax_partial_kernel<__nv_bfloat16>,
+                                                      kVerifyThreads, 0) != cudaSuccess || n < 1) {
+      cudaGetLastError();  // no device here: plan with a typical occupancy
+      n = 4;
+    } else if (dev >= 0) {
+      per_sm_cache[dev].store(n, std::memory_order_relaxed);
+    }
+    per_sm = n;
+  }
+  return plan_verify_for(rows, V, (long)per_sm * (num_sms > 0 ? num_sms : 1));
 }
 
 cudaError_t launch_verify(const void* logits, int dtype, const int32_t* draft, int B, int gamma,
@@ -233,8 +260,14 @@ cudaError_t launch_verify(const void* logits, int dtype, const int32_t* draft, i
   if (le != cudaSuccess) return le;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int warps = 4;
+  const int warps = B < 4 ? B : 4;
   const size_t smem = (size_t)warps * (gamma + 1) * sizeof(int);
+  if (smem > kScanSmemDefault) {
+    if (smem > kScanSmemMax) return cudaErrorInvalidValue;  // rejected on the host first
+    const cudaError_t ae = cudaFuncSetAttribute(
+        verify_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (ae != cudaSuccess) return ae;
+  }
   e = launch_pdl(verify_scan_kernel, dim3((B + warps - 1) / warps), dim3(warps * 32), smem, stream,
                  part_v, part_i, vp.chunks, draft, B, gamma, eos, emitted, num_emitted, accepted,
                  choices);

@@ -14,6 +14,9 @@
 // cudaGetSymbolAddress (with that device current) and caches it.
 #include <stdio.h>
 
+#include <atomic>
+
+#include "../../include/dflash_testing.h"
 #include "common.cuh"
 #include "internal.h"
 
@@ -28,7 +31,10 @@ constexpr size_t kStaticBytes = kStaticEntries * (sizeof(float) + sizeof(int));
 static __device__ __align__(256) unsigned char g_verify_scratch[kStaticBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
+// Per-device address of the scratch array.  Host threads may make their first call on a
+// device at the same time: each looks the address up and stores the same value, through an
+// atomic, so the cache itself is free of data races.
+std::atomic<void*> g_scratch_addr[kMaxDevices];
 
 // Looks up (once per device, with that device current) where the scratch array lives.
 cudaError_t scratch_address(void** out) {
@@ -36,13 +42,13 @@ cudaError_t scratch_address(void** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
+  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!p) {
     e = cudaGetSymbolAddress(&p, g_verify_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
+    g_scratch_addr[dev].store(p, std::memory_order_release);
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return cudaSuccess;
 }
 
@@ -75,6 +81,9 @@ int dflash_verify_greedy_static(const void* logits, int logits_dtype, const int3
                      "B * (gamma + 1) = %ld exceeds the static scratch limit of %zu rows; use "
                      "dflash_verify_greedy with a workspace", rows, kStaticEntries);
   }
+  if (gamma > kMaxVerifyGamma) {
+    return set_error(DFLASH_ERR_INVALID_ARG, "gamma (%d) must be <= %d", gamma, kMaxVerifyGamma);
+  }
   if (logits_dtype != DFLASH_DTYPE_BF16 && logits_dtype != DFLASH_DTYPE_F32) {
     return set_error(DFLASH_ERR_INVALID_ARG, "logits_dtype must be DFLASH_DTYPE_BF16 or _F32");
   }
@@ -83,14 +92,8 @@ int dflash_verify_greedy_static(const void* logits, int logits_dtype, const int3
   }
   // the same split of each vocab row as the workspace variant, capped so that all partials
   // fit in the static array (fewer, longer chunks when there are many rows)
-  VerifyPlan vp = plan_verify(B, gamma, V, num_sms_current());
-  if ((long)vp.chunks * rows > (long)kStaticEntries) {
-    long chunks = (long)kStaticEntries / rows;
-    long len = ((long)V + chunks - 1) / chunks;
-    len = (len + 7) / 8 * 8;
-    vp.chunk_len = (int)len;
-    vp.chunks = (int)(((long)V + len - 1) / len);
-  }
+  const VerifyPlan vp =
+      cap_verify_chunks(plan_verify(B, gamma, V, num_sms_current()), rows, V, (long)kStaticEntries);
   void* base = nullptr;
   cudaError_t e = scratch_address(&base);
   if (e != cudaSuccess) {
@@ -110,3 +113,20 @@ int dflash_verify_greedy_static(const void* logits, int logits_dtype, const int3
 }
 
 }  // extern "C"
+
+// ---- testing hook: the chunk plan of both verification entry points, on the host ----
+extern "C" int dflash_testing_verify_plan(int B, int gamma, int V, long resident_ctas,
+                                          long static_entries, int* chunks, int* chunk_len) {
+  if (B < 1 || gamma < 0 || V < 1 || resident_ctas < 1 || !chunks || !chunk_len)
+    return set_error(DFLASH_ERR_INVALID_ARG, "bad verify plan query");
+  const long rows = (long)B * (gamma + 1);
+  VerifyPlan vp = plan_verify_for(rows, V, resident_ctas);
+  if (static_entries > 0) {
+    if (rows > static_entries)
+      return set_error(DFLASH_ERR_INVALID_ARG, "more rows than static entries");
+    vp = cap_verify_chunks(vp, rows, V, static_entries);
+  }
+  *chunks = vp.chunks;
+  *chunk_len = vp.chunk_len;
+  return DFLASH_OK;
+}

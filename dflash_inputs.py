@@ -129,6 +129,16 @@ def _workloads() -> dict:
 WORKLOADS = _workloads()
 
 
+def smoke_workload() -> Workload:
+    """A small bf16 case of the whole path (several tiles in the GEMMs, one right-padded
+    row, a key range of one chunk, 24 draft slots) plus verification over a vocab of 5000."""
+    shape = DraftShape(target_hidden=128, num_target_layers=2, hidden=256, num_layers=2,
+                       num_heads=4, num_kv_heads=2, head_dim=128, intermediate=384,
+                       block_size=4, dtype="bf16")
+    return Workload("smoke", 9, shape, batch=2, seq_len=160, num_anchors=3,
+                    padded_rows=((1, 90),), verify_batch=3, vocab=5000)
+
+
 def scaled(w: Workload, **kw) -> Workload:
     """A copy of a workload with some fields (or shape fields) replaced; for small tests."""
     shape_kw = {k: kw.pop(k) for k in list(kw) if k in DraftShape.__dataclass_fields__}

@@ -42,6 +42,14 @@ DFLASH_API int dflash_testing_gemm_ws(const void* X, long ldx, const void* W, in
 /* The K-split the library picks for an M x N x K projection on the current device. */
 DFLASH_API int dflash_testing_gemm_splits(long M, int N, int K);
 
+/* The chunk plan of greedy verification, computed on the host (no device needed): each of
+ * the B*(gamma+1) logits rows of length V is cut into *chunks column ranges of *chunk_len
+ * elements (a multiple of 8), sized for `resident_ctas` resident argmax CTAs.  With
+ * static_entries > 0 the plan is then capped as dflash_verify_greedy_static caps it: at
+ * most static_entries partials in all.  Returns a DFLASH_* status. */
+DFLASH_API int dflash_testing_verify_plan(int B, int gamma, int V, long resident_ctas,
+                                          long static_entries, int* chunks, int* chunk_len);
+
 /* ---- live kernel timing ----------------------------------------------------------------
  * While enabled, every kernel launch of the four operations is bracketed by two CUDA events
  * recorded on the launch stream, grouped by kind.  Enabling clears earlier records. */

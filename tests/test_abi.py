@@ -81,3 +81,45 @@ def test_config_struct_layout_matches_header():
     assert ctypes.sizeof(dflash.dflash_config_t) == 12 * 4 + 2 * 8
     assert dflash.dflash_config_t.rope_theta.offset == 48
     assert ctypes.sizeof(dflash.dflash_layer_weights_t) == 6 * 8
+
+
+@pytest.mark.parametrize("B,gamma,V", [(1, 15, 151936), (64, 15, 151936), (256, 15, 151936),
+                                       (1024, 15, 151936), (1000, 15, 1001), (3, 0, 7),
+                                       (16384, 0, 100000), (17, 962, 5003)])
+@pytest.mark.parametrize("resident", [1, 152 * 8, 10 ** 6])
+@pytest.mark.parametrize("entries", [0, 16384])
+def test_verify_chunk_plan_covers_the_vocab(cpu_lib, B, gamma, V, resident, entries):
+    """The argmax chunk plan (host arithmetic): chunks of a multiple of 8 elements that cover
+    every vocab column exactly once; under the static variant's cap (16384 partials) the
+    rows * chunks partials fit, even for a GPU with far more resident CTAs than this one."""
+    rows = B * (gamma + 1)
+    if entries and rows > entries:
+        with pytest.raises(ValueError):
+            dflash.dflash_testing_verify_plan(B, gamma, V, resident, entries)
+        return
+    chunks, clen = dflash.dflash_testing_verify_plan(B, gamma, V, resident, entries)
+    assert clen % 8 == 0 and chunks >= 1
+    assert chunks * clen >= V > (chunks - 1) * clen
+    if entries:
+        assert rows * chunks <= entries
+
+
+def test_static_cap_branch_is_reached(cpu_lib):
+    # with many resident CTAs the uncapped plan wants more partials than the static array
+    # holds; the capped plan lengthens the chunks instead
+    free = dflash.dflash_testing_verify_plan(1024, 15, 151936, 10 ** 6)
+    capped = dflash.dflash_testing_verify_plan(1024, 15, 151936, 10 ** 6, 16384)
+    assert free[0] * 1024 * 16 > 16384
+    assert capped[0] == 1 and capped[1] >= 151936
+
+
+def test_verify_rejects_gamma_beyond_the_scan_limit(cpu_lib):
+    for fn in ("dflash_verify_greedy", "dflash_verify_greedy_static"):
+        args = [None, 1, None, 1, 60000, 10, -1, None, None, None, None]
+        if fn == "dflash_verify_greedy":
+            args += [None, 0, None]
+        else:
+            args += [None]
+        st = getattr(cpu_lib, fn)(*args)
+        assert st == dflash.DFLASH_ERR_INVALID_ARG
+        assert b"gamma" in cpu_lib.dflash_last_error()

@@ -5,100 +5,10 @@ import numpy as np
 import pytest
 
 import dflash_inputs as di
-from dflash_testlib import SynthModel, compare_hidden, np_to_device, to_device, tol_for
+from dflash_testlib import Case, small_bf16_workload
 from oracle import dflash_oracle as orc
 
 pytestmark = pytest.mark.gpu
-
-
-class Case:
-    """One workload's inputs, the GPU outputs, and oracle access to selected blocks."""
-
-    def __init__(self, w: di.Workload, gain_std=0.0, plan=None, mask=None):
-        self.w = w
-        s = w.shape
-        self.model = SynthModel(w, gain_std)
-        self.mask = di.gen_mask(w) if mask is None else mask
-        self.sids = di.gen_sample_ids(w)
-        if plan is None:
-            if w.inference:
-                a, v, p = di.inference_block_layout(w)
-                plan = {"anchors": a, "block_valid": v, "position_ids": p}
-            else:
-                plan = orc.build_plan(self.mask, self.sids, w.plan_step, w.plan_seed,
-                                      w.num_anchors, s.block_size)
-        self.plan = plan
-        self.emb = di.gen_block_emb(w)
-        self.N = plan["anchors"].shape[1]
-
-    def run_gpu(self, emb=None, hidden=None, mask=None, check_cache=False, ctx_len=None,
-                f16_layers=False):
-        """f16_layers: hand the library fp16 copies of the layer matrices (prepared once,
-        DFLASH_FLAG_F16_LAYERS) instead of the bf16 ones it converts inside each call."""
-        import torch
-        import block_draft_model_proj_gb300 as dflash
-        w, s = self.w, self.w.shape
-        B, L, N, S = w.batch, w.seq_len, self.N, s.block_size
-        cfg = dflash.make_config(s, f16_layers=f16_layers)
-        wts = self.model.lib_weights()
-        if f16_layers:
-            wts = dflash.prepare_f16_layers(wts)
-        H = to_device(di.gen_target_hidden(w) if hidden is None else hidden)
-        kv = torch.empty((s.num_layers, B, 2, s.num_kv_heads, L, s.head_dim),
-                         dtype=dflash.kv_cache_dtype(cfg),
-                         device="cuda")
-        cl = None if ctx_len is None else np_to_device(np.asarray(ctx_len, np.int32))
-        dflash.dflash_project_context(cfg, wts, H, B, L, 0, L, kv, ctx_len=cl)
-        del H
-        out = torch.full((B, N, S, s.hidden), float("nan"), dtype=torch.float32, device="cuda")
-        m = np_to_device(self.mask if mask is None else mask)
-        before = kv.clone() if check_cache else None
-        dflash.dflash_body_forward(cfg, wts, to_device(self.emb if emb is None else emb),
-                                   np_to_device(self.plan["anchors"]),
-                                   np_to_device(self.plan["block_valid"]),
-                                   np_to_device(self.plan["position_ids"]), m, kv, B, L, N, out)
-        dflash.dflash_device_status()
-        if check_cache:
-            assert torch.equal(before, kv), "the body must not write the context K/V"
-        return out.cpu().numpy()
-
-    def oracle_blocks(self, blocks, emb=None, hidden_fn=None, mask=None):
-        """blocks: list of (b, k).  Returns {(b, k): [S, D] fp64}."""
-        w, s = self.w, self.w.shape
-        mask = self.mask if mask is None else mask
-        emb = (self.emb if emb is None else emb).f64()
-        out = {}
-        by_row = {}
-        for b, k in blocks:
-            by_row.setdefault(b, []).append(k)
-        for b, ks in by_row.items():
-            need = max(min(int(self.plan["anchors"][b, k]), w.seq_len) for k in ks)
-            need = max(need, 1)
-            rows = (di.gen_target_hidden_rows(w, b, 0, need) if hidden_fn is None
-                    else hidden_fn(b, need))
-            kv = orc.project_context_row(s, self.model.top64(), self.model.layer64, rows.f64())
-            for k in ks:
-                out[(b, k)] = orc.block_forward(
-                    s, self.model.top64(), self.model.layer64, emb[b, k],
-                    int(self.plan["anchors"][b, k]), self.plan["block_valid"][b, k], mask[b], kv,
-                    self.plan["position_ids"][b, k])
-        return out
-
-    def compare(self, got, blocks, ref=None):
-        ref = self.oracle_blocks(blocks) if ref is None else ref
-        g = np.stack([got[b, k] for b, k in blocks])
-        r = np.stack([ref[(b, k)] for b, k in blocks])
-        v = np.stack([self.plan["block_valid"][b, k] for b, k in blocks])
-        return compare_hidden(g, r, v, tol_for(self.w.shape))
-
-
-def small_bf16_workload():
-    """Several tiles in every GEMM dimension plus ragged tails; masks with holes."""
-    shape = di.DraftShape(target_hidden=192, num_target_layers=2, hidden=256, num_layers=2,
-                          num_heads=4, num_kv_heads=2, head_dim=128, intermediate=392,
-                          block_size=4, dtype="bf16")
-    return di.Workload("small_bf16", 7, shape, batch=3, seq_len=304, num_anchors=5,
-                       padded_rows=((1, 170),), verify_batch=0, vocab=0)
 
 
 def test_small_bf16_full_parity_with_gains(lib):
@@ -139,7 +49,7 @@ def test_train_8b_b4_parity_with_prepared_f16_layers(lib):
     c.compare(got, [(0, k) for k in range(c.N)] + [(1, 3)])
 
 
-@pytest.mark.parametrize("batch", [1, 8])
+@pytest.mark.parametrize("batch", [1, 8, 32, 64])
 def test_decode_8b_parity(lib, batch):
     w = di.WORKLOADS[f"decode_8b_b{batch}_ctx4096"]
     c = Case(w)
@@ -152,7 +62,10 @@ def test_longctx_8b_sampled_parity(lib):
     c = Case(w)
     got = c.run_gpu()
     anchors = c.plan["anchors"][0]
-    ks = [int(k) for k in np.argsort(anchors)[:3]]        # shortest prefixes
+    # the three shortest prefixes and the longest one (several 4096-key chunks merged by
+    # the combine pass)
+    ks = [int(k) for k in np.argsort(anchors)[:3]] + [int(np.argmax(anchors))]
+    assert int(anchors[ks[-1]]) >= 16384
     c.compare(got, [(0, k) for k in ks])
     assert np.all(np.isfinite(got))
 
