@@ -205,6 +205,29 @@ def project_context_row(cfg, top, layers, hidden_row: np.ndarray, positions=None
     return out
 
 
+def commit_verified(cache_hidden: np.ndarray, verified_hidden: np.ndarray,
+                    accepted: int) -> np.ndarray:
+    """Cache rollback after greedy verification ("DFlash: drafting, verification, and
+    speed", One DFlash generation cycle, the paragraph after the worked example).
+
+    The target's verification pass computes states for every position of the block -- the
+    anchor and all gamma proposals -- but only the verified prefix may stay in a cache:
+    the anchor and the `accepted` proposals that matched.  The rejected proposal and its
+    suffix are dropped; the target's replacement token (or the bonus) has had no forward
+    pass yet and becomes the anchor of the next block, at the position right after the
+    retained prefix.  The draft's context cache must stay aligned with the target's, so it
+    retains the same positions.
+
+    cache_hidden [P0, W]: committed hidden states so far (positions 0 .. P0-1);
+    verified_hidden [S, W]: the block's states (anchor first), S = gamma + 1;
+    accepted: proposals accepted (0 .. gamma).  Returns the committed states [P0 + accepted
+    + 1, W]; the next block is anchored at position P0 + accepted + 1."""
+    S = verified_hidden.shape[0]
+    if not 0 <= accepted <= S - 1:
+        raise ValueError("accepted must lie in [0, gamma]")
+    return np.concatenate([cache_hidden, verified_hidden[:accepted + 1]], axis=0)
+
+
 # ======================================================================================
 # Draft body (one block at a time)
 # ======================================================================================

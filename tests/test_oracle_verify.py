@@ -110,3 +110,36 @@ def test_batched_verify_brute_force():
 def test_batched_verify_rejects_bad_shapes():
     with pytest.raises(ValueError):
         orc.verify_greedy(np.zeros((2, 4, 8)), np.zeros((2, 4), np.int32))
+
+
+def test_commit_keeps_anchor_and_accepted_proposals_only():
+    """The pages' worked example: proposals [10, 20, 99, 40] against target choices
+    [10, 20, 30, 40, 50] accept 2; the anchor and the two accepted proposals stay, the
+    rejected 99 and its suffix 40 go, although 40 matched its target choice."""
+    g = _read_golden("verify_worked_example.txt")
+    _, accepted = orc.verify_greedy_block(g["draft"], g["target_choices"])
+    prev = np.arange(6, dtype=np.float64).reshape(3, 2)          # 3 committed positions
+    # the verified block's states: anchor, then the four proposals (tagged by token id)
+    block = np.array([[-1, -1]] + [[t, t] for t in g["draft"]], np.float64)
+    out = orc.commit_verified(prev, block, accepted)
+    assert out.shape == (3 + accepted + 1, 2)
+    assert np.array_equal(out[:3], prev)
+    assert [int(x) for x in out[3:, 0]] == [-1, 10, 20]
+    assert 99 not in out and 40 not in out
+
+
+@pytest.mark.parametrize("gamma", [0, 1, 4, 15])
+def test_commit_length_follows_verification(gamma):
+    rng = np.random.default_rng(gamma)
+    for _ in range(20):
+        choices = list(rng.integers(0, 3, size=gamma + 1))
+        draft = list(rng.integers(0, 3, size=gamma))
+        emitted, acc = orc.verify_greedy_block(draft, choices)
+        block = rng.standard_normal((gamma + 1, 3))
+        out = orc.commit_verified(np.zeros((5, 3)), block, acc)
+        # the retained block positions are exactly the anchor plus the accepted proposals;
+        # without an EOS stop that is also the number of emitted tokens
+        assert out.shape[0] == 5 + acc + 1 == 5 + len(emitted)
+        assert np.array_equal(out[5:], block[:acc + 1])
+    with pytest.raises(ValueError):
+        orc.commit_verified(np.zeros((1, 3)), np.zeros((4, 3)), 4)
