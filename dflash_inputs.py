@@ -310,13 +310,33 @@ def gen_target_hidden_rows(w: Workload, b: int, c0: int, c1: int) -> Tensor:
     return Tensor(np.concatenate(parts, axis=0), s.dtype)
 
 
+def _parallel(fn, items) -> None:
+    """Runs fn over items on a few threads (NumPy's generators release the GIL while they
+    fill large arrays); the values do not depend on the thread count or order."""
+    import concurrent.futures as cf
+    import os
+    items = list(items)
+    n = min(len(items), os.cpu_count() or 1, 16)
+    if n <= 1:
+        for it in items:
+            fn(it)
+        return
+    with cf.ThreadPoolExecutor(max_workers=n) as ex:
+        list(ex.map(fn, items))
+
+
 def gen_target_hidden(w: Workload) -> Tensor:
     """All rows: [B, L, n_tl * D_t]."""
     s = w.shape
     dt = np.uint16 if s.dtype == "bf16" else np.float32
     out = np.empty((w.batch, w.seq_len, s.concat_width), dt)
-    for b in range(w.batch):
-        out[b] = gen_target_hidden_rows(w, b, 0, w.seq_len).data
+    chunks = (w.seq_len + HIDDEN_CHUNK - 1) // HIDDEN_CHUNK
+
+    def fill(item):
+        b, k = item
+        c0, c1 = k * HIDDEN_CHUNK, min(w.seq_len, (k + 1) * HIDDEN_CHUNK)
+        out[b, c0:c1] = gen_target_hidden_rows(w, b, c0, c1).data
+    _parallel(fill, [(b, k) for b in range(w.batch) for k in range(chunks)])
     return Tensor(out, s.dtype)
 
 
@@ -370,8 +390,14 @@ def gen_verify(w: Workload, batch: int | None = None, eos: int = -1) -> VerifyIn
     gamma = S - 1
     Bv = w.verify_batch if batch is None else batch
     V = w.vocab
-    rng = _rng(w.data_seed, _ID["logits"], Bv)
-    x = rng.standard_normal(size=(Bv, S, V), dtype=np.float32)
+    bf16 = w.verify_dtype == "bf16"
+    x = np.empty((Bv, S, V), np.float32)
+    out = np.empty((Bv, S, V), np.uint16) if bf16 else x
+
+    def fill(b):  # one stream per request
+        x[b] = _rng(w.data_seed, _ID["logits"], Bv, b).standard_normal(size=(S, V),
+                                                                        dtype=np.float32)
+    _parallel(fill, range(Bv))
     prng = _rng(w.data_seed, _ID["plant"], Bv)
     top = prng.integers(0, V, size=(Bv, S), dtype=np.int64).astype(np.int32)
     x[np.arange(Bv)[:, None], np.arange(S)[None, :], top] = PLANT_VALUE
@@ -384,8 +410,11 @@ def gen_verify(w: Workload, batch: int | None = None, eos: int = -1) -> VerifyIn
         draft[b, :k[b]] = top[b, :k[b]]
         if k[b] < gamma and draft[b, k[b]] == top[b, k[b]]:
             draft[b, k[b]] = (top[b, k[b]] + 1) % V
-    if w.verify_dtype == "bf16":
-        lt = Tensor(f32_to_bf16_bits(x), "bf16")
+    if bf16:
+        def conv(b):
+            out[b] = f32_to_bf16_bits(x[b])
+        _parallel(conv, range(Bv))
+        lt = Tensor(out, "bf16")
     else:
         lt = Tensor(x, "f32")
     return VerifyInputs(lt, draft, eos, k, top)

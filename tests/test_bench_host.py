@@ -95,3 +95,28 @@ def test_clock_sampler_without_any_source(monkeypatch):
     c.start()
     out = c.stop()
     assert out["sm_mhz"] is None and out["reasons"]
+
+
+def test_gemm_roofline_uses_burst_peak_and_picks_the_binding_side():
+    peaks = {"bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0, "hbm_gbs": 8000.0,
+             "source": "test"}
+    # 1e12 FLOP over 1e9 weight bytes: 1000 FLOP/B, above the ridge (250): tensor-bound
+    work = {"gemm_flops": 1e12, "layer_weight_bytes": 1e9, "ctx_weight_bytes": 0.0}
+    r = bench.gemm_roofline(work, False, 10.0, 10, 2, peaks)   # 1 ms per launch
+    assert r["bound"] == "tensor" and r["peak"] == 2000.0
+    assert r["algorithmic_per_launch"] == pytest.approx(2e11)
+    assert r["achieved"] == pytest.approx(2e11 / 1e-3 / 1e12)
+    assert r["frac"] == pytest.approx(r["achieved"] / 2000.0)
+    assert r["frac_of_sustained"] == pytest.approx(r["achieved"] / 1600.0)
+    # a decode step: 32 FLOP per weight byte, below the ridge: weight-read bound
+    work = {"gemm_flops": 3.2e10, "layer_weight_bytes": 1e9, "ctx_weight_bytes": 5e8}
+    r = bench.gemm_roofline(work, True, 10.0, 10, 2, peaks)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["algorithmic_per_launch"] == pytest.approx(1e9 * 2 / 10)
+
+
+def test_oracle_sample_prefix_is_bounded():
+    assert bench.oracle_prefix(di.WORKLOADS["train_8b_b16_l4096"]) == 1024
+    assert bench.oracle_prefix(di.WORKLOADS["longctx_8b_l32768"]) == 8192
+    assert bench.oracle_prefix(di.WORKLOADS["tiny_f32"]) == 128
+    assert bench.valid_rows(di.WORKLOADS["train_8b_b4_l2048"]) == [0, 1, 2]
