@@ -373,3 +373,98 @@ def verify_greedy(logits: np.ndarray, draft: np.ndarray, eos: int = -1):
         num[b] = len(e)
         acc[b] = a
     return choices, emitted, num, acc
+
+
+# ======================================================================================
+# Speculative-sampling verification
+# ======================================================================================
+
+
+def counter_uniform(seed: int, *counters: int) -> float:
+    """Counter-based uniform draw in (0, 1): the SplitMix64 finaliser chained over the seed
+    and the counters (each taken as uint64), as anchor_key chains it; the top 24 bits of
+    the result plus one half, times 2^-24.  Every value is a multiple of 2^-25 strictly
+    inside (0, 1), exact in fp32 and fp64, so both sides of a comparison draw identical
+    numbers from identical counters."""
+    h = splitmix64_mix(seed & U64)
+    for c in counters:
+        h = splitmix64_mix(h ^ (c & U64))
+    return ((h >> 40) + 0.5) * 2.0 ** -24
+
+
+def race_sample(weights: np.ndarray, seed: int, *counters: int) -> int:
+    """One draw from weights / sum(weights) (weights >= 0, at least one > 0) by the
+    exponential race: every index v with w_v > 0 gets an arrival time E_v / w_v with E_v =
+    -ln U_v i.i.d. Exp(1) (U_v = counter_uniform(seed, *counters, v)); the first arrival
+    wins (lowest index on an exact tie).  The minimum of independent exponentials of rates
+    w_v is attained at v with probability w_v / sum(w), so the draw is exact and needs no
+    normalisation or cumulative sum."""
+    best, best_t = -1, math.inf
+    for v in range(len(weights)):
+        w = float(weights[v])
+        if w > 0.0:
+            t = -math.log(counter_uniform(seed, *counters, v)) / w
+            if t < best_t:
+                best, best_t = v, t
+    return best
+
+
+def verify_sampling_block(p_rows: np.ndarray, q_rows: np.ndarray, draft, seed: int, b: int,
+                          eos_token=None):
+    """Speculative-sampling verification of one drafted block ("DFlash: drafting,
+    verification, and speed", Sampling with temperature is not argmax matching).
+
+    p_rows [gamma+1, V]: the target's distributions (row i after the anchor and draft[:i]);
+    q_rows [gamma, V]: the ACTUAL proposal distributions the draft tokens were drawn from
+    (after any top-k, temperature or selector).  For each proposal y = draft[i] in order:
+    accept with probability min(1, p_i(y) / q_i(y)) -- drawn as U < p_i(y) / q_i(y) with
+    U = counter_uniform(seed, b, i, 0); on the first rejection emit a sample of the
+    normalised residual [p_i - q_i]_+ and stop.  When every proposal is accepted, the block
+    ends with a sample of p_gamma, the counterpart of greedy verification's bonus token (this
+    reading: the pages state the acceptance and residual rules only).  A matched EOS
+    proposal ends the block as in greedy verification.  Samples use race_sample with
+    counters (b, i, 1).  If the residual is zero everywhere (p_i == q_i, where a rejection
+    cannot happen in exact arithmetic) the sample is drawn from p_i.
+    Returns (emitted, accepted)."""
+    draft = [int(t) for t in draft]
+    gamma = len(draft)
+    if p_rows.shape[0] != gamma + 1 or q_rows.shape[0] != gamma:
+        raise ValueError("need gamma + 1 target rows and gamma proposal rows")
+    out, acc = [], 0
+    for i, y in enumerate(draft):
+        u = counter_uniform(seed, b, i, 0)
+        py, qy = float(p_rows[i, y]), float(q_rows[i, y])
+        if u * qy < py:            # U < p/q, with q(y) = 0 always accepted
+            out.append(y)
+            acc += 1
+            if eos_token is not None and y == eos_token:
+                return out, acc
+            continue
+        r = np.maximum(p_rows[i] - q_rows[i], 0.0)
+        out.append(race_sample(r if np.any(r > 0) else p_rows[i], seed, b, i, 1))
+        return out, acc
+    out.append(race_sample(p_rows[gamma], seed, b, gamma, 1))
+    return out, acc
+
+
+def verify_sampling(logits: np.ndarray, temperature: float, q: np.ndarray, draft: np.ndarray,
+                    seed: int, eos: int = -1):
+    """Batched speculative-sampling verification.  logits [B, gamma+1, V] (the target's
+    distribution p = softmax(logits / temperature) per row, temperature > 0), q [B, gamma, V]
+    the actual proposal distributions, draft [B, gamma].  Returns (emitted [B, gamma+1]
+    padded with -1, num_emitted [B], accepted [B]), int32."""
+    B, S, V = logits.shape
+    if draft.shape != (B, S - 1) or q.shape != (B, S - 1, V) or not temperature > 0:
+        raise ValueError("need draft [B, gamma], q [B, gamma, V] and temperature > 0")
+    emitted = np.full((B, S), -1, np.int32)
+    num = np.zeros(B, np.int32)
+    acc = np.zeros(B, np.int32)
+    for b in range(B):
+        p = softmax_rows(np.asarray(logits[b], np.float64) / temperature)
+        e, a = verify_sampling_block(p, np.asarray(q[b], np.float64), draft[b], seed, b,
+                                     None if eos < 0 else eos)
+        emitted[b, :len(e)] = e
+        num[b] = len(e)
+        acc[b] = a
+    return emitted, num, acc
+
