@@ -382,14 +382,14 @@ def verify_greedy(logits: np.ndarray, draft: np.ndarray, eos: int = -1):
 
 def counter_uniform(seed: int, *counters: int) -> float:
     """Counter-based uniform draw in (0, 1): the SplitMix64 finaliser chained over the seed
-    and the counters (each taken as uint64), as anchor_key chains it; the top 24 bits of
-    the result plus one half, times 2^-24.  Every value is a multiple of 2^-25 strictly
-    inside (0, 1), exact in fp32 and fp64, so both sides of a comparison draw identical
-    numbers from identical counters."""
+    and the counters (each taken as uint64), as anchor_key chains it; the top 23 bits of
+    the result plus one half, times 2^-23.  Every value is an odd multiple of 2^-24 strictly
+    inside (0, 1) with at most 24 significant bits, exact in fp32 and fp64, so both sides of
+    a comparison draw identical numbers from identical counters."""
     h = splitmix64_mix(seed & U64)
     for c in counters:
         h = splitmix64_mix(h ^ (c & U64))
-    return ((h >> 40) + 0.5) * 2.0 ** -24
+    return ((h >> 41) + 0.5) * 2.0 ** -23
 
 
 def race_sample(weights: np.ndarray, seed: int, *counters: int) -> int:

@@ -15,9 +15,11 @@ from oracle import dflash_oracle as orc
 def test_counter_uniform_grid_and_spread():
     u = np.array([orc.counter_uniform(7, b, i) for b in range(40) for i in range(100)])
     assert np.all((u > 0) & (u < 1))
-    # every value is (k + 1/2) * 2^-24 for an integer k
-    k = u * 2 ** 24 - 0.5
+    # every value is (k + 1/2) * 2^-23 for an integer k, and survives a round trip to fp32
+    k = u * 2 ** 23 - 0.5
     assert np.array_equal(k, np.round(k))
+    assert np.array_equal(u.astype(np.float32).astype(np.float64), u)
+    assert orc.counter_uniform(0) == ((orc.splitmix64_mix(0) >> 41) + 0.5) * 2.0 ** -23
     assert len(set(u.tolist())) == len(u)
     # uniform over 16 bins (chi-square at 1e-3)
     counts = np.histogram(u, bins=16, range=(0, 1))[0]
