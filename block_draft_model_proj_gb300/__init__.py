@@ -74,6 +74,10 @@ _SIGS = {
     "dflash_project_context": (_I, [ctypes.POINTER(dflash_config_t),
                                     ctypes.POINTER(dflash_weights_t), _P, _I, _I, _I, _I, _P, _P,
                                     _P, _Z, _P]),
+    "dflash_append_context_workspace_size": (_Z, [ctypes.POINTER(dflash_config_t), _I, _I, _I]),
+    "dflash_append_context": (_I, [ctypes.POINTER(dflash_config_t),
+                                   ctypes.POINTER(dflash_weights_t), _P, _I, _I, _P, _P, _I, _P,
+                                   _P, _Z, _P]),
     "dflash_body_workspace_size": (_Z, [ctypes.POINTER(dflash_config_t), _I, _I, _I]),
     "dflash_body_forward": (_I, [ctypes.POINTER(dflash_config_t), ctypes.POINTER(dflash_weights_t),
                                  _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _Z, _P]),
@@ -84,6 +88,7 @@ _SIGS = {
                                          _P]),
     "dflash_testing_gemm": (_I, [_I, _I, _P, _L, _P, _L, _P, _L, _L, _I, _I, _I, _P]),
     "dflash_testing_gemm_splits": (_I, [_L, _I, _I]),
+    "dflash_testing_gemm_withheld": (_I, [_P, _L, _P, _L, _P, _L, _L, _I, _I, _L, _P]),
     "dflash_testing_gemm_ws": (_I, [_P, _L, _P, _I, _L, _P, _L, _L, _I, _I, _I, _P, _P, _P]),
     "dflash_testing_verify_plan": (_I, [_I, _I, _I, _L, _L, ctypes.POINTER(_I),
                                        ctypes.POINTER(_I)]),
@@ -239,6 +244,22 @@ def dflash_project_context(cfg, weights, target_hidden, B, L, pos_offset, L_cach
                                       _stream(stream)))
 
 
+def dflash_append_context_workspace_size(cfg, B, P, L_cache) -> int:
+    return load().dflash_append_context_workspace_size(ctypes.byref(cfg), B, P, L_cache)
+
+
+def dflash_append_context(cfg, weights, target_hidden, B, P, accepted, cache_len, L_cache,
+                          kv_cache, ws=None, stream=None):
+    lib = load()
+    if ws is None:
+        ws = workspace(dflash_append_context_workspace_size(cfg, B, P, L_cache),
+                       target_hidden.device)
+    _check(lib.dflash_append_context(ctypes.byref(cfg), ctypes.byref(weights.struct),
+                                     _ptr(target_hidden), B, P, _ptr(accepted), _ptr(cache_len),
+                                     L_cache, _ptr(kv_cache), _ptr(ws), ws.numel(),
+                                     _stream(stream)))
+
+
 def dflash_body_workspace_size(cfg, B, L, N) -> int:
     return load().dflash_body_workspace_size(ctypes.byref(cfg), B, L, N)
 
@@ -286,6 +307,14 @@ def dflash_testing_gemm(engine, dtype, A, B, C, splits=1, stream=None):
     N = B.shape[0]
     _check(load().dflash_testing_gemm(engine, dtype, _ptr(A), A.stride(0), _ptr(B), B.stride(0),
                                       _ptr(C), C.stride(-2), M, N, K, splits, _stream(stream)))
+
+
+def dflash_testing_gemm_withheld(A, B, C, wait_ns, stream=None):
+    M, K = A.shape
+    N = B.shape[0]
+    _check(load().dflash_testing_gemm_withheld(_ptr(A), A.stride(0), _ptr(B), B.stride(0), _ptr(C),
+                                               C.stride(-2), M, N, K, int(wait_ns),
+                                               _stream(stream)))
 
 
 def dflash_testing_gemm_ws(X, W, w_dtype, C, max_splits, splits_out, tile_list=None,

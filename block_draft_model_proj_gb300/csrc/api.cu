@@ -304,12 +304,19 @@ struct ProjLayout {
   float* cos_t;
   float* sin_t;
   int32_t* tile_list;
+  int32_t* n_commit;  // append: positions each row commits
+  int32_t* start;     // append: each row's first cache position
   int split_proj, split_kv;
   size_t bytes;
 };
 
-ProjLayout proj_layout(const dflash_config_t* c, int B, int L, void* ws) {
+// rope_rows: positions of the RoPE table (L for a projection at one offset; the cache
+// length for an append at per-row offsets, whose table starts at position 0).
+// append: also carve the per-row commit counts and start positions.
+ProjLayout proj_layout(const dflash_config_t* c, int B, int L, void* ws, int rope_rows = -1,
+                       bool append = false) {
   ProjLayout p;
+  if (rope_rows < 0) rope_rows = L;
   const long M = (long)B * L;
   const int D = c->hidden, Kc = c->target_hidden * c->num_target_layers;
   const int kvw = 2 * c->num_kv_heads * c->head_dim;
@@ -320,14 +327,84 @@ ProjLayout proj_layout(const dflash_config_t* c, int B, int L, void* ws) {
   Carver cv(ws);
   p.y = cv.take<float>((size_t)M * ycols);
   p.ctx = take_act(cv, (size_t)M * D, c->dtype);
-  p.cos_t = cv.take<float>((size_t)L * (c->head_dim / 2));
-  p.sin_t = cv.take<float>((size_t)L * (c->head_dim / 2));
+  p.cos_t = cv.take<float>((size_t)rope_rows * (c->head_dim / 2));
+  p.sin_t = cv.take<float>((size_t)rope_rows * (c->head_dim / 2));
   p.tile_list = cv.take<int32_t>(1 + (size_t)(M + kGemmTileM - 1) / kGemmTileM);
+  p.n_commit = append ? cv.take<int32_t>(B) : nullptr;
+  p.start = append ? cv.take<int32_t>(B) : nullptr;
   // the context K/V projection always runs on the 128 x 256-tile GEMM with fp16 operands:
   // bf16 layer weights are converted into the workspace whatever the row count
   p.wkv16 = context_kv_needs_convert(c) ? cv.take<__half>((size_t)kvw * D) : nullptr;
   p.bytes = cv.off;
   return p;
+}
+
+// The projection of rows m = b*L + c of target_hidden into every layer's cache planes at
+// positions (row_pos0 ? row_pos0[b] : pos_offset) + c, rows c >= ctx_len[b] skipped (the
+// RoPE table of `lay` is already built).
+int project_rows(const dflash_config_t* cfg, const dflash_weights_t* w, const void* target_hidden,
+                 int B, int L, int pos_offset, int L_cache, const int32_t* ctx_len,
+                 const int32_t* row_pos0, void* kv_cache, const ProjLayout& lay, cudaStream_t s) {
+  const long M = (long)B * L;
+  const int D = cfg->hidden, Kc = cfg->target_hidden * cfg->num_target_layers;
+  const int dh = cfg->head_dim, Hkv = cfg->num_kv_heads, qw = cfg->num_heads * dh;
+  const int kvw = 2 * Hkv * dh;
+  const size_t es = esize(cfg->dtype);
+  // 128-row tiles no block reads (all c >= ctx_len[b]) are skipped by every projection
+  const int32_t* flags = nullptr;
+  if (ctx_len && cfg->dtype == DFLASH_DTYPE_BF16) {
+    Prof pr(DFLASH_PROF_ROWS, 1, s);
+    DF_CUDA(launch_ctx_tile_list(ctx_len, B, L, lay.tile_list, s));
+    flags = lay.tile_list;
+  }
+  {
+    Prof pr(DFLASH_PROF_GEMM, 1, s);
+    DF_CUDA(gemm(cfg->dtype, DFLASH_DTYPE_BF16, target_hidden, Kc, w->w_proj, Kc, lay.y, D, M, D,
+                 Kc, lay.split_proj, s, flags));
+  }
+  {
+    Prof pr(DFLASH_PROF_ROWS, 1, s);
+    DF_CUDA(launch_rows_norm(cfg->dtype, lay.y, lay.split_proj, w->g_ctx, cfg->rms_eps,
+                             (cfg->flags & DFLASH_FLAG_CTX_NORM) != 0, lay.ctx.out(), M, D,
+                             ctx_len, L, s));
+  }
+  const size_t layer_elems = (size_t)B * 2 * Hkv * L_cache * dh;
+  for (int l = 0; l < cfg->num_layers; ++l) {
+    const void* wkv = static_cast<const uint8_t*>(w->layers[l].w_qkv) + (size_t)qw * D * es;
+    if (cfg->dtype == DFLASH_DTYPE_BF16) {
+      // RoPE and the fp16 cache layout are applied in the GEMM epilogue
+      KvCacheEpilogue kv;
+      kv.kv = static_cast<__half*>(kv_cache) + (size_t)l * layer_elems;
+      kv.cos_t = lay.cos_t;
+      kv.sin_t = lay.sin_t;
+      kv.ctx_len = ctx_len;
+      kv.row_pos0 = row_pos0;
+      kv.L = L;
+      kv.pos_offset = pos_offset;
+      kv.L_cache = L_cache;
+      kv.Hkv = Hkv;
+      const void* wkv16 = wkv;
+      if (lay.wkv16) {
+        Prof pc(DFLASH_PROF_CONVERT, 1, s);
+        DF_CUDA(launch_convert_bf16_f16(wkv, lay.wkv16, (size_t)kvw * D, status_ptr(), s));
+        wkv16 = lay.wkv16;
+      }
+      Prof pr(DFLASH_PROF_GEMM, 1, s);
+      DF_CUDA(launch_gemm_tc_kv_cache(DFLASH_DTYPE_F16, lay.ctx.p, D, wkv16, D, M, kvw, D, flags,
+                                      kv, status_ptr(), s));
+      continue;
+    }
+    {
+      Prof pr(DFLASH_PROF_GEMM, 1, s);
+      DF_CUDA(gemm(cfg->dtype, DFLASH_DTYPE_F16, lay.ctx.p, D, wkv, D, lay.y, kvw, M, kvw, D,
+                   lay.split_kv, s, flags));
+    }
+    Prof pr(DFLASH_PROF_ROWS, 2, s);
+    DF_CUDA(launch_ctx_kv_scatter(lay.y, lay.split_kv, lay.cos_t, lay.sin_t,
+                                  static_cast<float*>(kv_cache) + (size_t)l * layer_elems, B, L,
+                                  pos_offset, L_cache, Hkv, dh, ctx_len, row_pos0, s));
+  }
+  return DFLASH_OK;
 }
 
 struct BodyLayout {
@@ -500,69 +577,47 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
   const ProjLayout lay = proj_layout(cfg, B, L, ws);
   if ((r = check_ws(ws, ws_bytes, lay.bytes))) return r;
   cudaStream_t s = (cudaStream_t)stream;
-  const long M = (long)B * L;
-  const int D = cfg->hidden, Kc = cfg->target_hidden * cfg->num_target_layers;
-  const int dh = cfg->head_dim, Hkv = cfg->num_kv_heads, qw = cfg->num_heads * dh;
-  const int kvw = 2 * Hkv * dh;
-  const size_t es = esize(cfg->dtype);
   {
     Prof pr(DFLASH_PROF_ROWS, 1, s);
-    DF_CUDA(launch_rope_table(lay.cos_t, lay.sin_t, pos_offset, L, dh, cfg->rope_theta, s));
+    DF_CUDA(launch_rope_table(lay.cos_t, lay.sin_t, pos_offset, L, cfg->head_dim,
+                              cfg->rope_theta, s));
   }
-  // 128-row tiles no block reads (all c >= ctx_len[b]) are skipped by every projection
-  const int32_t* flags = nullptr;
-  if (ctx_len && cfg->dtype == DFLASH_DTYPE_BF16) {
-    Prof pr(DFLASH_PROF_ROWS, 1, s);
-    DF_CUDA(launch_ctx_tile_list(ctx_len, B, L, lay.tile_list, s));
-    flags = lay.tile_list;
-  }
+  return project_rows(cfg, w, target_hidden, B, L, pos_offset, L_cache, ctx_len, nullptr,
+                      kv_cache, lay, s);
+}
+
+size_t dflash_append_context_workspace_size(const dflash_config_t* cfg, int B, int P,
+                                            int L_cache) {
+  if (check_cfg(cfg) != DFLASH_OK || B < 1 || P < 1 || L_cache < P) return 0;
+  return proj_layout(cfg, B, P, nullptr, L_cache, true).bytes;
+}
+
+int dflash_append_context(const dflash_config_t* cfg, const dflash_weights_t* w,
+                          const void* target_hidden, int B, int P, const int32_t* accepted,
+                          int32_t* cache_len, int L_cache, void* kv_cache, void* ws,
+                          size_t ws_bytes, void* stream) {
+  int r;
+  if ((r = check_cfg(cfg))) return r;
+  if ((r = check_weights(cfg, w, false))) return r;
+  if (B < 1 || P < 1 || L_cache < P)
+    return fail(DFLASH_ERR_INVALID_ARG, "need B, P >= 1 and L_cache >= P");
+  if (!cache_len) return fail(DFLASH_ERR_INVALID_ARG, "cache_len is null");
+  if ((r = check_ptr16(target_hidden, "target_hidden", cfg->dtype))) return r;
+  if ((r = check_ptr16(kv_cache, "kv_cache", DFLASH_DTYPE_BF16))) return r;
+  if (cfg->dtype == DFLASH_DTYPE_BF16 && L_cache % 8 != 0)
+    return fail(DFLASH_ERR_INVALID_ARG, "L_cache must be a multiple of 8 (16-byte fp16 cache rows)");
+  const ProjLayout lay = proj_layout(cfg, B, P, ws, L_cache, true);
+  if ((r = check_ws(ws, ws_bytes, lay.bytes))) return r;
+  cudaStream_t s = (cudaStream_t)stream;
   {
-    Prof pr(DFLASH_PROF_GEMM, 1, s);
-    DF_CUDA(gemm(cfg->dtype, DFLASH_DTYPE_BF16, target_hidden, Kc, w->w_proj, Kc, lay.y, D, M, D,
-                 Kc, lay.split_proj, s, flags));
-  }
-  {
-    Prof pr(DFLASH_PROF_ROWS, 1, s);
-    DF_CUDA(launch_rows_norm(cfg->dtype, lay.y, lay.split_proj, w->g_ctx, cfg->rms_eps,
-                             (cfg->flags & DFLASH_FLAG_CTX_NORM) != 0, lay.ctx.out(), M, D,
-                             ctx_len, L, s));
-  }
-  const size_t layer_elems = (size_t)B * 2 * Hkv * L_cache * dh;
-  for (int l = 0; l < cfg->num_layers; ++l) {
-    const void* wkv = static_cast<const uint8_t*>(w->layers[l].w_qkv) + (size_t)qw * D * es;
-    if (cfg->dtype == DFLASH_DTYPE_BF16) {
-      // RoPE and the fp16 cache layout are applied in the GEMM epilogue
-      KvCacheEpilogue kv;
-      kv.kv = static_cast<__half*>(kv_cache) + (size_t)l * layer_elems;
-      kv.cos_t = lay.cos_t;
-      kv.sin_t = lay.sin_t;
-      kv.ctx_len = ctx_len;
-      kv.L = L;
-      kv.pos_offset = pos_offset;
-      kv.L_cache = L_cache;
-      kv.Hkv = Hkv;
-      const void* wkv16 = wkv;
-      if (lay.wkv16) {
-        Prof pc(DFLASH_PROF_CONVERT, 1, s);
-        DF_CUDA(launch_convert_bf16_f16(wkv, lay.wkv16, (size_t)kvw * D, status_ptr(), s));
-        wkv16 = lay.wkv16;
-      }
-      Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(launch_gemm_tc_kv_cache(DFLASH_DTYPE_F16, lay.ctx.p, D, wkv16, D, M, kvw, D, flags,
-                                      kv, status_ptr(), s));
-      continue;
-    }
-    {
-      Prof pr(DFLASH_PROF_GEMM, 1, s);
-      DF_CUDA(gemm(cfg->dtype, DFLASH_DTYPE_F16, lay.ctx.p, D, wkv, D, lay.y, kvw, M, kvw, D,
-                   lay.split_kv, s, flags));
-    }
     Prof pr(DFLASH_PROF_ROWS, 2, s);
-    DF_CUDA(launch_ctx_kv_scatter(lay.y, lay.split_kv, lay.cos_t, lay.sin_t,
-                                  static_cast<float*>(kv_cache) + (size_t)l * layer_elems, B, L,
-                                  pos_offset, L_cache, Hkv, dh, ctx_len, s));
+    DF_CUDA(launch_append_plan(accepted, cache_len, B, P, L_cache, lay.n_commit, lay.start,
+                               status_ptr(), s));
+    DF_CUDA(launch_rope_table(lay.cos_t, lay.sin_t, 0, L_cache, cfg->head_dim, cfg->rope_theta,
+                              s));
   }
-  return DFLASH_OK;
+  return project_rows(cfg, w, target_hidden, B, P, 0, L_cache, lay.n_commit, lay.start,
+                      kv_cache, lay, s);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -824,6 +879,17 @@ int dflash_testing_gemm(int engine, int dtype, const void* A, long lda, const vo
 }
 
 int dflash_testing_gemm_splits(long M, int N, int K) { return gemm_splits(M, N, K); }
+
+int dflash_testing_gemm_withheld(const void* A, long lda, const void* Bm, long ldb, float* C,
+                                 long ldc, long M, int N, int K, long wait_ns, void* stream) {
+  if (M < 1 || N < 1 || K < 1 || !A || !Bm || !C || wait_ns < 1000 || wait_ns > 100000000L)
+    return fail(DFLASH_ERR_INVALID_ARG, "bad withheld-gemm args (wait_ns in [1 us, 100 ms])");
+  if (!gemm_tc_supported(M, N, K, lda, ldb))
+    return fail(DFLASH_ERR_UNSUPPORTED, "tensor-core GEMM needs 16-byte rows");
+  DF_CUDA(launch_gemm_tc_withheld(A, lda, Bm, ldb, C, ldc, M, N, K, (uint64_t)wait_ns,
+                                  status_ptr(), (cudaStream_t)stream));
+  return DFLASH_OK;
+}
 
 int dflash_testing_gemm_ws(const void* X, long ldx, const void* W, int w_dtype, long ldw,
                            float* C, long ldc, long M, int N, int K, int max_splits,

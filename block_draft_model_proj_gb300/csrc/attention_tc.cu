@@ -225,7 +225,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
         issued_ph[st] = ph;
       }
       for (int s2 = 0; s2 < kRing; ++s2)
-        if (issued[s2]) mbar_wait(&full[s2], issued_ph[s2], abort_flag, kWaitLimitNs / 4);
+        if (issued[s2]) mbar_drain_wait(&full[s2], issued_ph[s2], kWaitLimitNs / 4);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -275,7 +275,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
         if (i + kSP < u.n) ok = issue_s(i + kSP);
       }
       umma_commit(drain);
-      mbar_wait(drain, 0, abort_flag, kWaitLimitNs / 4);
+      mbar_drain_wait(drain, 0, kWaitLimitNs / 4);
     }
   } else {
     // ---------------- softmax / correction / partial output (warps 2..9) ----------------

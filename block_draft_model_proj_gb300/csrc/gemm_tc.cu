@@ -84,6 +84,9 @@ struct TcParams {
   KvCacheEpilogue kv;          // used by the kEpiKvCache epilogue only
   ActOut act;                  // kEpiSwiGLU: SiLU(gate) * up, [M][swiglu_I]
   int swiglu_I;                // kEpiSwiGLU: B rows [0, I) gate, [I, 2I) up
+  uint64_t wait_ns;            // limit of every bounded wait (kWaitLimitNs)
+  int test_withhold;           // testing only: the producer issues no copy and no arrival,
+                               // so the first wait of the MMA thread runs out
 };
 
 // Number of M tiles the work list runs over: all, or the compacted active ones.
@@ -125,7 +128,8 @@ __device__ __forceinline__ void kv_cache_epilogue(const TcParams& p, uint32_t tb
   const int c = (int)(m - (long)b * e.L);
   bool row_ok = m < p.M;
   if (row_ok && e.ctx_len) row_ok = c < e.ctx_len[b];
-  const long pos = (long)e.pos_offset + c;
+  const long pos = (e.row_pos0 && row_ok ? (long)e.row_pos0[b] : (long)e.pos_offset) + c;
+  const long trow = e.row_pos0 ? pos : c;  // RoPE table row of this position
   const long plane = (long)e.L_cache * 128;
   bool bad = false;  // a value outside the fp16 range (or NaN) met the cache
 #pragma unroll 1
@@ -141,8 +145,8 @@ __device__ __forceinline__ void kv_cache_epilogue(const TcParams& p, uint32_t tb
         tmem_ld_32x32b_x32(hbase + ch * 32, lo);
         tmem_ld_32x32b_x32(hbase + 64 + ch * 32, hi);
         if (row_ok) {
-          const float* cs = e.cos_t + (long)c * 64 + ch * 32;
-          const float* sn = e.sin_t + (long)c * 64 + ch * 32;
+          const float* cs = e.cos_t + trow * 64 + ch * 32;
+          const float* sn = e.sin_t + trow * 64 + ch * 32;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {  // 8 channels (16 bytes of fp16) per step
             uint32_t wa[4], wb[4];
@@ -288,14 +292,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       int issued[kStages];
       uint32_t issued_ph[kStages];
       for (int s = 0; s < kStages; ++s) issued[s] = 0, issued_ph[s] = 0;
-      bool ok = true;
+      bool ok = p.test_withhold == 0;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         int m_t, n_t, z;
         decode_tile(p, m_cnt, t, m_t, n_t, z);
         const int kb0 = z * kb_per;
         const int kb1 = min(p.num_kb, kb0 + kb_per);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
+          if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, p.wait_ns)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], kTxBytes);
           uint8_t* a_dst = sA + stage * kStageABytes;
           uint8_t* b_dst = sB + stage * kStageBBytes;
@@ -313,7 +317,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       }
       // wait for this thread's own copies still in flight
       for (int s = 0; s < kStages; ++s)
-        if (issued[s]) mbar_wait(&full[s], issued_ph[s], abort_flag, kWaitLimitNs / 4);
+        if (issued[s]) mbar_drain_wait(&full[s], issued_ph[s], p.wait_ns / 4);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -328,11 +332,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         decode_tile(p, m_cnt, t, m_t, n_t, z);
         const int kb0 = z * kb_per;
         const int kb1 = min(p.num_kb, kb0 + kb_per);
-        if (!mbar_wait(&tempty[acc], acc_ph ^ 1u, abort_flag, kWaitLimitNs)) break;
+        if (!mbar_wait(&tempty[acc], acc_ph ^ 1u, abort_flag, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&full[stage], ph, abort_flag, kWaitLimitNs)) { ok = false; break; }
+          if (!mbar_wait(&full[stage], ph, abort_flag, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(sA + stage * kStageABytes);
           const uint32_t b_addr = smem_u32(sB + stage * kStageBBytes);
@@ -351,7 +355,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       }
       // all MMAs issued by this thread complete before tensor memory is released
       umma_commit(drain);
-      mbar_wait(drain, 0, abort_flag, kWaitLimitNs / 4);
+      mbar_drain_wait(drain, 0, p.wait_ns / 4);
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
@@ -363,7 +367,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       int m_t, n_t, z;
       decode_tile(p, m_cnt, t, m_t, n_t, z);
       // warp-uniform result: the tcgen05.ld below is .sync.aligned
-      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_ph, abort_flag, kWaitLimitNs) ? 1 : 0))
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_ph, abort_flag, p.wait_ns) ? 1 : 0))
         break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
@@ -482,7 +486,8 @@ cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const T
 cudaError_t launch_common(int elem, const void* A, long lda, const void* Bm, long ldb, float* C,
                           long ldc, long M, int N, int K, int splits, const int32_t* tile_list,
                           unsigned* status, int* splits_out, int epi, const KvCacheEpilogue* kv, const ActOut* act,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, uint64_t wait_ns = kWaitLimitNs,
+                          int test_withhold = 0) {
   if (elem != DFLASH_DTYPE_BF16 && elem != DFLASH_DTYPE_F16) return cudaErrorInvalidValue;
   if (((uintptr_t)A | (uintptr_t)Bm) % 16 != 0) return cudaErrorInvalidValue;
   const bool bf16 = elem == DFLASH_DTYPE_BF16;
@@ -516,6 +521,8 @@ cudaError_t launch_common(int elem, const void* A, long lda, const void* Bm, lon
   p.m_fastest = (double)M <= (double)N ? 1 : 0;
   p.idesc = idesc_16bit(bf16);
   p.status = status;
+  p.wait_ns = wait_ns;
+  p.test_withhold = test_withhold;
   if (kv) p.kv = *kv;
   const long tiles = (long)p.m_tiles * p.n_tiles * p.splits;
   const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
@@ -551,6 +558,13 @@ cudaError_t launch_gemm_tc_kv_cache(int elem, const void* A, long lda, const voi
     return cudaErrorInvalidValue;
   return launch_common(elem, A, lda, Bm, ldb, nullptr, 0, M, N, K, 1, tile_list, status, nullptr,
                        kEpiKvCache, &kv, nullptr, stream);
+}
+
+cudaError_t launch_gemm_tc_withheld(const void* A, long lda, const void* Bm, long ldb, float* C,
+                                    long ldc, long M, int N, int K, uint64_t wait_ns,
+                                    unsigned* status, cudaStream_t stream) {
+  return launch_common(DFLASH_DTYPE_BF16, A, lda, Bm, ldb, C, ldc, M, N, K, 1, nullptr, status,
+                       nullptr, kEpiStoreF32, nullptr, nullptr, stream, wait_ns, 1);
 }
 
 }  // namespace dflash

@@ -405,7 +405,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
       }
       // wait for this thread's own copies still in flight (the last S issued)
       for (long j = n_issued - S > 0 ? n_issued - S : 0; j < n_issued; ++j)
-        mbar_wait(&full[j % S], (uint32_t)((j / S) & 1), abort_flag, kWaitLimitNs / 4);
+        mbar_drain_wait(&full[j % S], (uint32_t)((j / S) & 1), kWaitLimitNs / 4);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -446,7 +446,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         acc_ph ^= 1u;
       }
       umma_commit(drain);
-      mbar_wait(drain, 0, abort_flag, kWaitLimitNs / 4);
+      mbar_drain_wait(drain, 0, kWaitLimitNs / 4);
     }
   } else if (warp < 10) {
     // ---------------- converters (warps 2..9): W tile -> fp16 A in tensor memory ----------------
@@ -657,7 +657,8 @@ cudaError_t launch_gemm_ws_swiglu(const WsArgs& a, const ActOut& act, cudaStream
 
 cudaError_t launch_gemm_ws_kv_cache(const WsArgs& a, const KvCacheEpilogue& kv,
                                     cudaStream_t stream) {
-  if (a.Nw != 2 * kv.Hkv * 128 || kv.L < 1 || kv.L % 8 != 0) return cudaErrorInvalidValue;
+  if (a.Nw != 2 * kv.Hkv * 128 || kv.L < 1 || kv.L % 8 != 0 || kv.row_pos0)
+    return cudaErrorInvalidValue;
   if (((uintptr_t)kv.kv | (uintptr_t)kv.cos_t | (uintptr_t)kv.sin_t) % 16 != 0)
     return cudaErrorInvalidValue;
   // K heads interleave their RoPE pairs; V heads keep the natural order

@@ -100,10 +100,20 @@ cudaError_t launch_qkv_rope(const float* y, int nsplit, const int* nsplit_dev, c
 // cache planes of one layer [B][2][Hkv]: K as [L_cache][dh] (RoPE'd; table row c = position
 // pos_offset + c) and V^T as [dh][L_cache], at positions pos_offset + c.
 // Rows c >= ctx_len[b] (when ctx_len is given) are not written.
+// row_pos0 (optional [B]): as in KvCacheEpilogue.
 cudaError_t launch_ctx_kv_scatter(const float* y, int nsplit, const float* cos_t,
                                   const float* sin_t, float* kv_layer, int B, int L,
                                   int pos_offset, int L_cache, int Hkv, int dh,
-                                  const int32_t* ctx_len, cudaStream_t stream);
+                                  const int32_t* ctx_len, const int32_t* row_pos0,
+                                  cudaStream_t stream);
+
+// Cache append after verification: for each row b, n[b] = accepted ? clamp(accepted[b] + 1,
+// 0, P) : P positions commit at start[b] = cache_len[b]; cache_len[b] += n[b].  A row whose
+// start is negative or whose new length would pass L_cache reports a device check and
+// commits nothing (n[b] = 0, cache_len unchanged).
+cudaError_t launch_append_plan(const int32_t* accepted, int32_t* cache_len, int B, int P,
+                               int L_cache, int32_t* n, int32_t* start, unsigned* status,
+                               cudaStream_t stream);
 
 // SwiGLU epilogue: y [nsplit][T][2I] fp32 (gate | up) -> act [T][I] = SiLU(gate) * up.
 // nsplit_dev (optional) overrides nsplit; valid (optional): invalid slots' rows get zeros.
@@ -150,6 +160,10 @@ struct KvCacheEpilogue {
   const float* cos_t = nullptr;  // [L][64], row c = position pos_offset + c
   const float* sin_t = nullptr;
   const int32_t* ctx_len = nullptr;  // optional [B]: rows c >= ctx_len[b] are not written
+  // optional [B]: row b's context index c is cache position row_pos0[b] + c and its RoPE
+  // angle is the table row of that absolute position (the table then starts at position 0);
+  // without it the position is pos_offset + c and the table row c
+  const int32_t* row_pos0 = nullptr;
   int L = 0, pos_offset = 0, L_cache = 0, Hkv = 0;
 };
 // act = SiLU(gate) * up with [gate | up] = A W_gate_up^T (W_gate_up [2I][K]: gate rows then
@@ -167,6 +181,13 @@ cudaError_t launch_gemm_tc_kv_cache(int elem, const void* A, long lda, const voi
 cudaError_t launch_gemm_tc(int elem, const void* A, long lda, const void* Bm, long ldb, float* C,
                            long ldc, long M, int N, int K, int splits, const int32_t* tile_list,
                            unsigned* status, cudaStream_t stream, int* splits_out = nullptr);
+
+// Testing only: the bf16 GEMM with its TMA producer withholding every copy and arrival and
+// every bounded wait limited to wait_ns, so the MMA thread's first wait runs out: the CTAs
+// report kStatusTimeout, drain, free their tensor memory and exit without writing C.
+cudaError_t launch_gemm_tc_withheld(const void* A, long lda, const void* Bm, long ldb, float* C,
+                                    long ldc, long M, int N, int K, uint64_t wait_ns,
+                                    unsigned* status, cudaStream_t stream);
 
 // ---- gemm_ws.cu: weight-streaming tcgen05 GEMM of the draft layers ----
 // C[z][t][n] = X[t, Kz] W[n, Kz]^T over the active 128-row token tiles: X fp16 [M][K] (row

@@ -428,7 +428,8 @@ __global__ void ctx_k_scatter_kernel(const float* __restrict__ y, int nsplit, lo
                                      const float* __restrict__ cos_t,
                                      const float* __restrict__ sin_t, float* __restrict__ kv,
                                      int B, int L, int pos_offset, int L_cache, int Hkv, int dh,
-                                     const int32_t* __restrict__ ctx_len) {
+                                     const int32_t* __restrict__ ctx_len,
+                                     const int32_t* __restrict__ row_pos0) {
   const int half = dh / 2;
   const long per_row = (long)Hkv * half;
   const long n = (long)B * L * per_row;
@@ -442,9 +443,11 @@ __global__ void ctx_k_scatter_kernel(const float* __restrict__ y, int nsplit, lo
     const long src = bc * 2L * Hkv * dh + (long)g * dh;
     const float a = sum_splits(y, nsplit, split_stride, src + i);
     const float bb = sum_splits(y, nsplit, split_stride, src + i + half);
-    // table row c holds position pos_offset + c
-    const float cs = cos_t[(long)c * half + i], sn = sin_t[(long)c * half + i];
-    float* dst = kv + ((((long)b * 2) * Hkv + g) * L_cache + pos_offset + c) * dh;
+    // table row c holds position pos_offset + c; with row_pos0 the table starts at 0
+    const long pos = (row_pos0 ? (long)row_pos0[b] : (long)pos_offset) + c;
+    const long trow = row_pos0 ? pos : c;
+    const float cs = cos_t[trow * half + i], sn = sin_t[trow * half + i];
+    float* dst = kv + ((((long)b * 2) * Hkv + g) * L_cache + pos) * dh;
     dst[i] = a * cs - bb * sn;
     dst[i + half] = bb * cs + a * sn;
   }
@@ -455,7 +458,8 @@ __global__ void ctx_k_scatter_kernel(const float* __restrict__ y, int nsplit, lo
 __global__ void ctx_vt_scatter_kernel(const float* __restrict__ y, int nsplit, long split_stride,
                                       float* __restrict__ kv, int B, int L, int pos_offset,
                                       int L_cache, int Hkv, int dh,
-                                      const int32_t* __restrict__ ctx_len) {
+                                      const int32_t* __restrict__ ctx_len,
+                                      const int32_t* __restrict__ row_pos0) {
   const long n = (long)B * Hkv * dh * L;
   for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n;
        e += (long)gridDim.x * blockDim.x) {
@@ -468,7 +472,8 @@ __global__ void ctx_vt_scatter_kernel(const float* __restrict__ y, int nsplit, l
     if (ctx_len && c >= ctx_len[b]) continue;
     const long src = ((long)b * L + c) * 2L * Hkv * dh + (long)(Hkv + g) * dh + d;
     const float v = sum_splits(y, nsplit, split_stride, src);
-    kv[((((long)b * 2 + 1) * Hkv + g) * dh + d) * L_cache + pos_offset + c] = v;
+    const long pos = (row_pos0 ? (long)row_pos0[b] : (long)pos_offset) + c;
+    kv[((((long)b * 2 + 1) * Hkv + g) * dh + d) * L_cache + pos] = v;
   }
 }
 
@@ -617,16 +622,18 @@ cudaError_t launch_qkv_rope(const float* y, int nsplit, const int* nsplit_dev, c
 cudaError_t launch_ctx_kv_scatter(const float* y, int nsplit, const float* cos_t,
                                   const float* sin_t, float* kv_layer, int B, int L,
                                   int pos_offset, int L_cache, int Hkv, int dh,
-                                  const int32_t* ctx_len, cudaStream_t stream) {
+                                  const int32_t* ctx_len, const int32_t* row_pos0,
+                                  cudaStream_t stream) {
   const long stride = (long)B * L * 2 * Hkv * dh;
   const long nk = (long)B * L * Hkv * (dh / 2);
   ctx_k_scatter_kernel<<<grid_for(nk, 256), 256, 0, stream>>>(
-      y, nsplit, stride, cos_t, sin_t, kv_layer, B, L, pos_offset, L_cache, Hkv, dh, ctx_len);
+      y, nsplit, stride, cos_t, sin_t, kv_layer, B, L, pos_offset, L_cache, Hkv, dh, ctx_len,
+      row_pos0);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long nv = (long)B * Hkv * dh * L;
   ctx_vt_scatter_kernel<<<grid_for(nv, 256), 256, 0, stream>>>(
-      y, nsplit, stride, kv_layer, B, L, pos_offset, L_cache, Hkv, dh, ctx_len);
+      y, nsplit, stride, kv_layer, B, L, pos_offset, L_cache, Hkv, dh, ctx_len, row_pos0);
   return cudaGetLastError();
 }
 
@@ -793,6 +800,42 @@ cudaError_t launch_convert_bf16_f16(const void* src, void* dst, size_t n, unsign
         status);
     if (le != cudaSuccess) return le;
   }
+  return cudaGetLastError();
+}
+
+namespace {
+
+// One thread per row: how many of the P verified positions commit, where they start, and
+// the new cache length ("DFlash: drafting, verification, and speed", One DFlash generation
+// cycle: only the anchor and the accepted proposals stay).
+__global__ void append_plan_kernel(const int32_t* __restrict__ accepted,
+                                   int32_t* __restrict__ cache_len, int B, int P, int L_cache,
+                                   int32_t* __restrict__ n_out, int32_t* __restrict__ start_out,
+                                   unsigned* status) {
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  int n = P;
+  if (accepted) n = min(max(accepted[b] + 1, 0), P);
+  const int start = cache_len[b];
+  if (start < 0 || (long)start + n > (long)L_cache) {
+    report(status, kStatusCheck, kKernEpilogue);
+    n = 0;
+  }
+  n_out[b] = n;
+  start_out[b] = start < 0 ? 0 : start;
+  cache_len[b] = start + n;
+}
+
+}  // namespace
+
+cudaError_t launch_append_plan(const int32_t* accepted, int32_t* cache_len, int B, int P,
+                               int L_cache, int32_t* n, int32_t* start, unsigned* status,
+                               cudaStream_t stream) {
+  const cudaError_t le = launch_pdl(append_plan_kernel, dim3((B + 255) / 256), dim3(256), 0,
+                                    stream, accepted, cache_len, B, P, L_cache, n, start, status);
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 

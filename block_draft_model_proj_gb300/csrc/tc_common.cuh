@@ -85,6 +85,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Bounded wait of the exit path: a thread waits for its own TMA copies or MMAs still in
+// flight before the CTA frees tensor memory and exits.  It ignores the abort flag (the copies
+// land whether or not the CTA is aborting) and gives up only after limit_ns.
+__device__ __forceinline__ bool mbar_drain_wait(uint64_t* bar, uint32_t parity,
+                                                uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_suspend(bar, parity, 1000u)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* bar, void* dst,
                                             int c0, int c1) {
   asm volatile(

@@ -181,11 +181,47 @@ DFLASH_API size_t dflash_project_context_workspace_size(const dflash_config_t* c
  *   ctx_len       optional [B] int32 (NULL = L): positions c >= ctx_len[b] of row b may be
  *                 left unwritten (no block of that row reads them); values are clamped to [0, L].
  * Requires 0 <= pos_offset, pos_offset + L <= L_cache.  RoPE positions are the absolute
- * positions pos_offset + c. */
+ * positions pos_offset + c.
+ * Range: in the bf16 configuration the context and the cache are fp16.  A value outside
+ * the fp16 range (or a NaN) sets DFLASH_ERR_RANGE in the sticky device status and is
+ * stored as inf/NaN: the call itself still returns DFLASH_OK, so a caller that needs to
+ * know polls dflash_device_status (which synchronizes the device). */
 DFLASH_API int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w,
                            const void* target_hidden, int B, int L, int pos_offset, int L_cache,
                            const int32_t* ctx_len, void* kv_cache, void* ws, size_t ws_bytes,
                            void* stream);
+
+/* ---- 2b. cache append after verification ([P3] One DFlash generation cycle: cache
+ *      rollback) --------------------------------------------------------------------- */
+
+DFLASH_API size_t dflash_append_context_workspace_size(const dflash_config_t* cfg, int B, int P,
+                                                       int L_cache);
+
+/* One inference cycle's cache update.  The target has verified one drafted block per
+ * request and computed hidden states for its P positions (the anchor and the P - 1
+ * proposals).  Only the verified prefix may stay in a cache: for request b the first
+ *   n_b = accepted[b] + 1   (the anchor and the accepted proposals; accepted as written by
+ *                            dflash_verify_greedy, clamped to [0, P - 1])
+ * positions commit -- all P when accepted is NULL.  The rejected proposal and its suffix
+ * never enter the cache; the target's replacement (or bonus) token has had no forward pass
+ * and anchors the next block at position cache_len[b] + n_b.
+ *   target_hidden [B, P, n_tl*D_t]: the verified block's selected target hidden states
+ *   accepted      [B] int32 (device) or NULL
+ *   cache_len     [B] int32 (device, in/out): committed length of each request's cache;
+ *                 the n_b positions are projected exactly as dflash_project_context projects
+ *                 a context (W_proj, RMSNorm, each layer's K/V with RoPE at the absolute
+ *                 position) and written at cache positions cache_len[b] .. cache_len[b] +
+ *                 n_b - 1; then cache_len[b] += n_b.  All on the device: no host round trip.
+ *   kv_cache      the planes of dflash_project_context with L_cache positions per plane.
+ * Positions at or past the new length keep what they held; a block anchored at
+ * cache_len[b] never reads them.  A row whose cache_len is negative or would pass L_cache
+ * commits nothing, keeps its length and sets DFLASH_ERR_DEVICE_CHECK.  The body then runs
+ * with L = L_cache and a mask [B, L_cache] (positions below each request's length valid).
+ * Range: as for dflash_project_context. */
+DFLASH_API int dflash_append_context(const dflash_config_t* cfg, const dflash_weights_t* w,
+                                     const void* target_hidden, int B, int P,
+                                     const int32_t* accepted, int32_t* cache_len, int L_cache,
+                                     void* kv_cache, void* ws, size_t ws_bytes, void* stream);
 
 /* ---- 3. draft body ([P2] How It Works, step 3; [P1] block-parallel prediction) -------- */
 
@@ -208,7 +244,10 @@ DFLASH_API size_t dflash_body_workspace_size(const dflash_config_t* cfg, int B, 
  * directions).  It never reads another block and never writes kv_cache.
  * Layer: x += W_o Attn(RMSNorm(x; g_in)); x += W_down(SiLU(h W_gate^T) * h W_up^T),
  * h = RMSNorm(x; g_post); out = RMSNorm(x; g_final) when DFLASH_FLAG_FINAL_NORM.
- * A valid slot whose position id is out of range sets DFLASH_ERR_DEVICE_CHECK. */
+ * A valid slot whose position id is out of range sets DFLASH_ERR_DEVICE_CHECK.
+ * Range: in the bf16 configuration the layer projections' inputs, Q/K/V and the attention
+ * output are fp16; a value outside the fp16 range sets DFLASH_ERR_RANGE in the sticky device
+ * status while the call returns DFLASH_OK: poll dflash_device_status to learn of it. */
 DFLASH_API int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
                         const void* block_emb, const int32_t* anchors,
                         const uint8_t* block_valid, const int32_t* position_ids,

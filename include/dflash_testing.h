@@ -39,6 +39,17 @@ DFLASH_API int dflash_testing_gemm_ws(const void* X, long ldx, const void* W, in
                                       int max_splits, const int32_t* tile_list,
                                       int32_t* splits_out, void* stream);
 
+/* Failure detection of the tensor-core kernels: the bf16 GEMM of dflash_testing_gemm
+ * (one K slice) with its TMA producer withholding every copy and every arrival, and every
+ * bounded device wait limited to wait_ns (1 us .. 100 ms).  Nothing ever fills the first
+ * shared-memory stage, so the MMA thread's wait runs out: each CTA raises its abort flag,
+ * reports DFLASH_ERR_TIMEOUT in the device status word, waits (bounded) for its own work in
+ * flight, frees its tensor memory and exits.  C is left unwritten; the device stays usable.
+ * No GPU fault, trap or endless wait is involved. */
+DFLASH_API int dflash_testing_gemm_withheld(const void* A, long lda, const void* B, long ldb,
+                                            float* C, long ldc, long M, int N, int K,
+                                            long wait_ns, void* stream);
+
 /* The K-split the library picks for an M x N x K projection on the current device. */
 DFLASH_API int dflash_testing_gemm_splits(long M, int N, int K);
 
