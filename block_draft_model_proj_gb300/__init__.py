@@ -84,6 +84,9 @@ _SIGS = {
     "dflash_verify_workspace_size": (_Z, [_I, _I, _I]),
     "dflash_verify_greedy": (_I, [_P, _I, _P, _I, _I, _I, ctypes.c_int32, _P, _P, _P, _P, _P, _Z,
                                   _P]),
+    "dflash_verify_sampling_workspace_size": (_Z, [_I, _I, _I]),
+    "dflash_verify_sampling": (_I, [_P, _I, ctypes.c_double, _P, _P, _I, _I, _I, ctypes.c_uint64,
+                                    ctypes.c_int32, _P, _P, _P, _P, _Z, _P]),
     "dflash_verify_greedy_static": (_I, [_P, _I, _P, _I, _I, _I, ctypes.c_int32, _P, _P, _P, _P,
                                          _P]),
     "dflash_testing_gemm": (_I, [_I, _I, _P, _L, _P, _L, _P, _L, _L, _I, _I, _I, _P]),
@@ -287,6 +290,18 @@ def dflash_verify_greedy(logits, logits_dtype, draft, B, gamma, V, eos, emitted,
     _check(lib.dflash_verify_greedy(_ptr(logits), logits_dtype, _ptr(draft), B, gamma, V,
                                     int(eos), _ptr(emitted), _ptr(num_emitted), _ptr(accepted),
                                     _ptr(target_choices), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def dflash_verify_sampling(logits, logits_dtype, temperature, draft_probs, draft, B, gamma, V,
+                           seed, eos, emitted, num_emitted, accepted, ws=None, stream=None):
+    lib = load()
+    if ws is None:
+        ws = workspace(lib.dflash_verify_sampling_workspace_size(B, gamma, V), logits.device)
+    _check(lib.dflash_verify_sampling(_ptr(logits), logits_dtype, float(temperature),
+                                      _ptr(draft_probs), _ptr(draft), B, gamma, V,
+                                      int(seed) & ((1 << 64) - 1), int(eos), _ptr(emitted),
+                                      _ptr(num_emitted), _ptr(accepted), _ptr(ws), ws.numel(),
+                                      _stream(stream)))
 
 
 def dflash_verify_greedy_static(logits, logits_dtype, draft, B, gamma, V, eos, emitted,

@@ -843,6 +843,8 @@ int dflash_verify_greedy(const void* logits, int logits_dtype, const int32_t* dr
                 "need B >= 1, gamma >= 0, V >= 1 (one target choice per draft token plus a bonus)");
   if (gamma > kMaxVerifyGamma)
     return fail(DFLASH_ERR_INVALID_ARG, "gamma (%d) must be <= %d", gamma, kMaxVerifyGamma);
+  if ((long)B * (gamma + 1) > kMaxVerifyRows)
+    return fail(DFLASH_ERR_UNSUPPORTED, "B * (gamma + 1) must be <= %ld", kMaxVerifyRows);
   if (logits_dtype != DFLASH_DTYPE_BF16 && logits_dtype != DFLASH_DTYPE_F32)
     return fail(DFLASH_ERR_INVALID_ARG, "logits_dtype must be DFLASH_DTYPE_BF16 or _F32");
   if (!logits || (!draft && gamma > 0) || !emitted || !num_emitted || !accepted)
@@ -857,6 +859,41 @@ int dflash_verify_greedy(const void* logits, int logits_dtype, const int32_t* dr
   Prof pr(DFLASH_PROF_VERIFY, 2, (cudaStream_t)stream);
   DF_CUDA(launch_verify(logits, logits_dtype, draft, B, gamma, V, eos, emitted, num_emitted,
                         accepted, target_choices, pv, pi, vp, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------------------------------
+size_t dflash_verify_sampling_workspace_size(int B, int gamma, int V) {
+  if (B < 1 || gamma < 0 || V < 1) return 0;
+  return plan_sampling(B, gamma, V, num_sms()).ws_bytes + 256;
+}
+
+int dflash_verify_sampling(const void* logits, int logits_dtype, double temperature,
+                           const float* draft_probs, const int32_t* draft, int B, int gamma,
+                           int V, uint64_t seed, int32_t eos, int32_t* emitted,
+                           int32_t* num_emitted, int32_t* accepted, void* ws, size_t ws_bytes,
+                           void* stream) {
+  if (B < 1 || gamma < 0 || V < 1)
+    return fail(DFLASH_ERR_INVALID_ARG,
+                "need B >= 1, gamma >= 0, V >= 1 (one target distribution per draft token "
+                "plus the final one)");
+  if ((long)B * (gamma + 1) > kMaxVerifyRows)
+    return fail(DFLASH_ERR_UNSUPPORTED, "B * (gamma + 1) must be <= %ld", kMaxVerifyRows);
+  if (!(temperature > 0.0) || !(1.0 / temperature < 3.0e38))
+    return fail(DFLASH_ERR_INVALID_ARG, "temperature must be > 0 (greedy verification is "
+                "dflash_verify_greedy)");
+  if (logits_dtype != DFLASH_DTYPE_BF16 && logits_dtype != DFLASH_DTYPE_F32)
+    return fail(DFLASH_ERR_INVALID_ARG, "logits_dtype must be DFLASH_DTYPE_BF16 or _F32");
+  if (!logits || (gamma > 0 && (!draft || !draft_probs)) || !emitted || !num_emitted ||
+      !accepted)
+    return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
+  const SamplingPlan sp = plan_sampling(B, gamma, V, num_sms());
+  int r;
+  if ((r = check_ws(ws, ws_bytes, sp.ws_bytes))) return r;
+  Prof pr(DFLASH_PROF_VERIFY, 4, (cudaStream_t)stream);
+  DF_CUDA(launch_verify_sampling(logits, logits_dtype, (float)(1.0 / temperature), draft_probs,
+                                 draft, B, gamma, V, seed, eos, emitted, num_emitted, accepted,
+                                 ws, sp, status_ptr(), (cudaStream_t)stream));
   return DFLASH_OK;
 }
 

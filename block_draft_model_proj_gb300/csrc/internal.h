@@ -54,12 +54,30 @@ VerifyPlan cap_verify_chunks(VerifyPlan vp, long rows, int V, long max_entries);
 // warps; above the default 48 KB the launch raises the kernel's limit, up to kScanSmemMax.
 constexpr size_t kScanSmemDefault = 48 * 1024;
 constexpr size_t kScanSmemMax = 227 * 1024;
+// Logits rows (B * (gamma + 1)) a verification call takes: one grid row of CTAs per logits row.
+constexpr long kMaxVerifyRows = 65535;
 // Largest gamma the verification calls accept: one warp's (gamma + 1) choices in shared memory.
 constexpr int kMaxVerifyGamma = (int)(kScanSmemMax / sizeof(int)) - 1;
 cudaError_t launch_verify(const void* logits, int dtype, const int32_t* draft, int B, int gamma,
                           int V, int32_t eos, int32_t* emitted, int32_t* num_emitted,
                           int32_t* accepted, int32_t* choices, float* part_v, int* part_i,
                           const VerifyPlan& vp, cudaStream_t stream);
+
+// ---- verify_sampling.cu: speculative-sampling verification ----
+struct SamplingPlan {
+  int chunks = 1, chunk_len = 0;            // softmax statistics: chunks per logits row
+  int race_chunks = 1, race_chunk_len = 0;  // the sampled row of each request
+  size_t ws_bytes = 0;
+};
+SamplingPlan plan_sampling(int B, int gamma, int V, int num_sms);
+// logits [B][gamma+1][V] (bf16 or fp32), q [B][gamma][V] fp32 (the actual proposal
+// distributions), draft [B][gamma]; ws holds plan.ws_bytes.  A draft token outside [0, V)
+// reports a device check and counts as rejected.
+cudaError_t launch_verify_sampling(const void* logits, int dtype, float inv_temp, const float* q,
+                                   const int32_t* draft, int B, int gamma, int V, uint64_t seed,
+                                   int32_t eos, int32_t* emitted, int32_t* num_emitted,
+                                   int32_t* accepted, void* ws, const SamplingPlan& sp,
+                                   unsigned* status, cudaStream_t stream);
 
 // ---- rows.cu: row-wise kernels (norms, RoPE table, GEMM epilogues) ----
 // RoPE table: cos/sin [P, dh/2] fp32 for positions p0 .. p0+P-1, angles formed and

@@ -274,6 +274,39 @@ DFLASH_API int dflash_verify_greedy(const void* logits, int logits_dtype, const 
                          int32_t* accepted, int32_t* target_choices, void* ws, size_t ws_bytes,
                          void* stream);
 
+/* ---- 4b. speculative-sampling verification ([P3] Sampling with temperature is not argmax
+ *      matching) ------------------------------------------------------------------------ */
+
+DFLASH_API size_t dflash_verify_sampling_workspace_size(int B, int gamma, int V);
+
+/* Speculative-sampling verification of B drafted blocks: the target distribution of row i is
+ * p_i = softmax(logits[b, i] / temperature); q_i = draft_probs[b, i] is the ACTUAL proposal
+ * distribution draft[b, i] was drawn from (after any top-k, temperature or selector on the
+ * draft side).  In block order, proposal y = draft[b, i] is accepted when
+ * U(seed, b, i, 0) < p_i(y) / q_i(y) -- probability min(1, p/q); at the first rejection the
+ * block ends with a sample of the normalised residual [p_i - q_i]_+.  If every proposal is
+ * accepted the block ends with a sample of p_gamma.  A matched EOS proposal ends the block
+ * (no sample).  The output tokens are distributed as the target's own samples.
+ *   logits       [B, gamma+1, V] of type logits_dtype (DFLASH_DTYPE_BF16 or _F32)
+ *   temperature  > 0 (host double)
+ *   draft_probs  [B, gamma, V] float32, rows summing to 1 (only the entries of the draft
+ *                tokens and the rejected row are read)
+ *   draft        [B, gamma] int32 in [0, V) (an entry outside sets DFLASH_ERR_DEVICE_CHECK)
+ *   seed         the sampling stream: U(seed, counters...) is the SplitMix64 finaliser
+ *                chained over the seed and the counters, top 23 bits + 1/2 times 2^-23;
+ *                samples use the exponential race (index v arrives at -ln U(seed, b, i, 1,
+ *                v) / w_v; the first arrival wins, lowest index on a tie), an exact draw
+ *                from w / sum(w).  Same seed, same inputs: same outputs.
+ * Outputs as dflash_verify_greedy: emitted [B, gamma+1] (accepted proposals, then the
+ * sample; -1 padded), num_emitted [B], accepted [B].  The probabilities are fp32; a
+ * decision within fp32 rounding of its threshold may come out either way.
+ * Errors: INVALID_ARG for B < 1, gamma < 0, V < 1, temperature <= 0, null pointers. */
+DFLASH_API int dflash_verify_sampling(const void* logits, int logits_dtype, double temperature,
+                                      const float* draft_probs, const int32_t* draft, int B,
+                                      int gamma, int V, uint64_t seed, int32_t eos,
+                                      int32_t* emitted, int32_t* num_emitted, int32_t* accepted,
+                                      void* ws, size_t ws_bytes, void* stream);
+
 /* ---- greedy verification without a workspace ----------------------------------------
  * The pages have no counterpart for this call: it is a deployment variant of
  * dflash_verify_greedy for callers that cannot allocate device memory -- code embedded in
