@@ -468,3 +468,51 @@ def verify_sampling(logits: np.ndarray, temperature: float, q: np.ndarray, draft
         acc[b] = a
     return emitted, num, acc
 
+
+# ======================================================================================
+# Training loss over the drafted blocks
+# ======================================================================================
+
+
+def position_weights(block_size: int, decay: float) -> np.ndarray:
+    """Loss weight of each block slot.  "DFlash" (How it works, Loss): cross-entropy with an
+    exponential positional decay that weights earlier in-block positions more heavily;
+    "DFlash: drafting, verification, and speed" (One DFlash generation cycle): greater loss
+    weight on early positions.  The pages give no constant.  Reading: slot j >= 1 (the
+    first predicted position is j = 1) weighs exp(-(j - 1) / decay), decay > 0 a caller
+    argument; the anchor slot j = 0 weighs 0 (loss_mask excludes it anyway)."""
+    if not decay > 0:
+        raise ValueError("decay must be > 0")
+    w = np.zeros(block_size, np.float64)
+    j = np.arange(1, block_size, dtype=np.float64)
+    w[1:] = np.exp(-(j - 1.0) / decay)
+    return w
+
+
+def decayed_ce_loss(hidden: np.ndarray, w_lm: np.ndarray, targets: np.ndarray,
+                    loss_mask: np.ndarray, decay: float):
+    """Draft loss of a batch of blocks: per slot, the cross-entropy of the frozen lm_head's
+    logits (hidden W_lm^T) against the ground-truth token, weighted by position_weights and
+    by loss_mask ("DFlash Draft Body", How It Works step 4: the loss mask excludes the anchor
+    and invalid positions); loss = sum(m w CE) / sum(m w) (0 when nothing is weighted).
+
+    hidden [B, N, S, D] (the body's output), w_lm [V, D], targets [B, N, S] int (read where
+    loss_mask is set), loss_mask [B, N, S].  Returns (loss, ce [B, N, S] with 0 where the
+    mask is 0)."""
+    B, N, S, D = hidden.shape
+    w = position_weights(S, decay)
+    ce = np.zeros((B, N, S), np.float64)
+    num = den = 0.0
+    for b in range(B):
+        for k in range(N):
+            for j in range(S):
+                if not loss_mask[b, k, j]:
+                    continue
+                logits = w_lm @ hidden[b, k, j]
+                m = np.max(logits)
+                lse = m + math.log(np.sum(np.exp(logits - m)))
+                ce[b, k, j] = lse - logits[int(targets[b, k, j])]
+                num += w[j] * ce[b, k, j]
+                den += w[j]
+    return (num / den if den > 0 else 0.0), ce
+
