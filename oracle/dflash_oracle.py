@@ -502,17 +502,16 @@ def decayed_ce_loss(hidden: np.ndarray, w_lm: np.ndarray, targets: np.ndarray,
     B, N, S, D = hidden.shape
     w = position_weights(S, decay)
     ce = np.zeros((B, N, S), np.float64)
+    idx = np.argwhere(np.asarray(loss_mask) != 0)          # masked slots (b, k, j)
+    if len(idx) == 0:
+        return 0.0, ce
+    logits = hidden[idx[:, 0], idx[:, 1], idx[:, 2]] @ w_lm.T   # [slots, V], one matmul
     num = den = 0.0
-    for b in range(B):
-        for k in range(N):
-            for j in range(S):
-                if not loss_mask[b, k, j]:
-                    continue
-                logits = w_lm @ hidden[b, k, j]
-                m = np.max(logits)
-                lse = m + math.log(np.sum(np.exp(logits - m)))
-                ce[b, k, j] = lse - logits[int(targets[b, k, j])]
-                num += w[j] * ce[b, k, j]
-                den += w[j]
+    for r, (b, k, j) in enumerate(idx):
+        m = np.max(logits[r])
+        lse = m + math.log(np.sum(np.exp(logits[r] - m)))
+        ce[b, k, j] = lse - logits[r, int(targets[b, k, j])]
+        num += w[j] * ce[b, k, j]
+        den += w[j]
     return (num / den if den > 0 else 0.0), ce
 
