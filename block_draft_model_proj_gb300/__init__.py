@@ -81,6 +81,9 @@ _SIGS = {
     "dflash_body_workspace_size": (_Z, [ctypes.POINTER(dflash_config_t), _I, _I, _I]),
     "dflash_body_forward": (_I, [ctypes.POINTER(dflash_config_t), ctypes.POINTER(dflash_weights_t),
                                  _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _Z, _P]),
+    "dflash_decayed_ce_workspace_size": (_Z, [_I, _I, _I]),
+    "dflash_decayed_ce_loss": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_double, _P, _P, _P,
+                                    _Z, _P]),
     "dflash_verify_workspace_size": (_Z, [_I, _I, _I]),
     "dflash_verify_greedy": (_I, [_P, _I, _P, _I, _I, _I, ctypes.c_int32, _P, _P, _P, _P, _P, _Z,
                                   _P]),
@@ -276,6 +279,16 @@ def dflash_body_forward(cfg, weights, block_emb, anchors, block_valid, position_
                                    _ptr(block_emb), _ptr(anchors), _ptr(block_valid),
                                    _ptr(position_ids), _ptr(mask), _ptr(kv_cache), B, L, N,
                                    _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def dflash_decayed_ce_loss(hidden, lm_head, targets, loss_mask, T, block_size, D, V, decay, ce,
+                           loss, ws=None, stream=None):
+    lib = load()
+    if ws is None:
+        ws = workspace(lib.dflash_decayed_ce_workspace_size(T, D, V), hidden.device)
+    _check(lib.dflash_decayed_ce_loss(_ptr(hidden), _ptr(lm_head), _ptr(targets),
+                                      _ptr(loss_mask), T, block_size, D, V, float(decay), _ptr(ce),
+                                      _ptr(loss), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def dflash_verify_workspace_size(B, gamma, V) -> int:

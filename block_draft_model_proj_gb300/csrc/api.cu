@@ -897,6 +897,35 @@ int dflash_verify_sampling(const void* logits, int logits_dtype, double temperat
   return DFLASH_OK;
 }
 
+// ---------------------------------------------------------------------------------------
+size_t dflash_decayed_ce_workspace_size(int T, int D, int V) {
+  if (T < 1 || D < 1 || V < 1) return 0;
+  return ce_layout(T, D, V, nullptr).bytes + 256;
+}
+
+int dflash_decayed_ce_loss(const float* hidden, const void* lm_head, const int32_t* targets,
+                           const uint8_t* loss_mask, int T, int block_size, int D, int V,
+                           double decay, float* ce, float* loss, void* ws, size_t ws_bytes,
+                           void* stream) {
+  if (T < 1 || block_size < 1 || D < 1 || V < 1 || T % block_size != 0)
+    return fail(DFLASH_ERR_INVALID_ARG, "need T, block_size, D, V >= 1 and T a multiple of "
+                "block_size");
+  if (!(decay > 0.0)) return fail(DFLASH_ERR_INVALID_ARG, "decay must be > 0");
+  if (D % 8 != 0)
+    return fail(DFLASH_ERR_UNSUPPORTED, "D must be a multiple of 8 (16-byte rows for TMA)");
+  if (!targets || !loss_mask || !ce || !loss)
+    return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
+  int r;
+  if ((r = check_ptr16(hidden, "hidden", DFLASH_DTYPE_F32))) return r;
+  if ((r = check_ptr16(lm_head, "lm_head", DFLASH_DTYPE_BF16))) return r;
+  const CeLayout l = ce_layout(T, D, V, ws);
+  if ((r = check_ws(ws, ws_bytes, l.bytes))) return r;
+  Prof pr(DFLASH_PROF_GEMM, 5, (cudaStream_t)stream);
+  DF_CUDA(launch_decayed_ce(hidden, lm_head, targets, loss_mask, T, block_size, D, V, decay, ce,
+                            loss, l, status_ptr(), (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
 // ---- testing hooks -----------------------------------------------------------------------
 int dflash_testing_gemm(int engine, int dtype, const void* A, long lda, const void* Bm, long ldb,
                         float* C, long ldc, long M, int N, int K, int splits, void* stream) {

@@ -67,7 +67,7 @@ __device__ __forceinline__ void umma_16bit(uint32_t tmem_d, uint64_t adesc, uint
       : "memory");
 }
 
-enum : int { kEpiStoreF32 = 0, kEpiKvCache = 1, kEpiSwiGLU = 2 };
+enum : int { kEpiStoreF32 = 0, kEpiKvCache = 1, kEpiSwiGLU = 2, kEpiCrossEntropy = 3 };
 
 struct TcParams {
   long M;
@@ -84,6 +84,7 @@ struct TcParams {
   KvCacheEpilogue kv;          // used by the kEpiKvCache epilogue only
   ActOut act;                  // kEpiSwiGLU: SiLU(gate) * up, [M][swiglu_I]
   int swiglu_I;                // kEpiSwiGLU: B rows [0, I) gate, [I, 2I) up
+  CrossEntropyEpilogue ce;     // kEpiCrossEntropy: per-tile softmax statistics of each row
   uint64_t wait_ns;            // limit of every bounded wait (kWaitLimitNs)
   int test_withhold;           // testing only: the producer issues no copy and no arrival,
                                // so the first wait of the MMA thread runs out
@@ -221,6 +222,49 @@ __device__ __forceinline__ void swiglu_epilogue(const TcParams& p, uint32_t tbas
           if (ch + t < I) p.act.store(m * I + ch + t, a[t]);
       }
     }
+  }
+}
+
+// Cross-entropy epilogue (lm_head logits, never stored): row m of the tile, columns
+// n_t*256 .. +255 below V.  Writes the tile's (max, sum of exp(logit - max)) of the row and,
+// from the one tile that holds it, the logit of the row's target token.
+__device__ __forceinline__ void cross_entropy_epilogue(const TcParams& p, uint32_t tbase, int m_t,
+                                                       int n_t, int quarter, int lane) {
+  const CrossEntropyEpilogue& e = p.ce;
+  const long m = (long)m_t * kBM + quarter * 32 + lane;
+  const bool row_ok = m < p.M;
+  const int tgt = row_ok ? e.targets[m] : -1;
+  float mx = -INFINITY, sum = 0.f, tlogit = 0.f;
+  bool has_t = false;
+#pragma unroll 1
+  for (int c = 0; c < kBN / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(tbase + c * 32, v);
+    const int col0 = n_t * kBN + c * 32;
+    if (col0 >= e.V) continue;  // warp-uniform; the loads above stay .sync.aligned
+    const int nv = min(32, e.V - col0);
+    float cm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nv) cm = fmaxf(cm, __uint_as_float(v[i]));
+    if (cm > mx) {
+      sum = mx == -INFINITY ? 0.f : sum * expf(mx - cm);
+      mx = cm;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i < nv) sum += expf(__uint_as_float(v[i]) - mx);
+      if (col0 + i == tgt) {
+        tlogit = __uint_as_float(v[i]);
+        has_t = true;
+      }
+    }
+  }
+  if (row_ok) {
+    float* part = e.part + ((size_t)m * p.n_tiles + n_t) * 2;
+    part[0] = mx;
+    part[1] = sum;
+    if (has_t) e.target_logit[m] = tlogit;
   }
 }
 
@@ -392,6 +436,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         }
       } else if constexpr (kEpi == kEpiKvCache) {
         kv_cache_epilogue(p, tbase, m_t, n_t, quarter, lane);
+      } else if constexpr (kEpi == kEpiCrossEntropy) {
+        cross_entropy_epilogue(p, tbase, m_t, n_t, quarter, lane);
       } else {
         swiglu_epilogue(p, tbase, m_t, n_t, quarter, lane);
       }
@@ -487,7 +533,7 @@ cudaError_t launch_common(int elem, const void* A, long lda, const void* Bm, lon
                           long ldc, long M, int N, int K, int splits, const int32_t* tile_list,
                           unsigned* status, int* splits_out, int epi, const KvCacheEpilogue* kv, const ActOut* act,
                           cudaStream_t stream, uint64_t wait_ns = kWaitLimitNs,
-                          int test_withhold = 0) {
+                          int test_withhold = 0, const CrossEntropyEpilogue* ce = nullptr) {
   if (elem != DFLASH_DTYPE_BF16 && elem != DFLASH_DTYPE_F16) return cudaErrorInvalidValue;
   if (((uintptr_t)A | (uintptr_t)Bm) % 16 != 0) return cudaErrorInvalidValue;
   const bool bf16 = elem == DFLASH_DTYPE_BF16;
@@ -524,9 +570,11 @@ cudaError_t launch_common(int elem, const void* A, long lda, const void* Bm, lon
   p.wait_ns = wait_ns;
   p.test_withhold = test_withhold;
   if (kv) p.kv = *kv;
+  if (ce) p.ce = *ce;
   const long tiles = (long)p.m_tiles * p.n_tiles * p.splits;
   const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
   if (epi == kEpiKvCache) return launch_variant<kEpiKvCache>(ma, mb, p, grid, stream);
+  if (epi == kEpiCrossEntropy) return launch_variant<kEpiCrossEntropy>(ma, mb, p, grid, stream);
   if (epi == kEpiSwiGLU) return launch_variant<kEpiSwiGLU>(ma, mb, p, grid, stream);
   return launch_variant<kEpiStoreF32>(ma, mb, p, grid, stream);
 }
@@ -558,6 +606,18 @@ cudaError_t launch_gemm_tc_kv_cache(int elem, const void* A, long lda, const voi
     return cudaErrorInvalidValue;
   return launch_common(elem, A, lda, Bm, ldb, nullptr, 0, M, N, K, 1, tile_list, status, nullptr,
                        kEpiKvCache, &kv, nullptr, stream);
+}
+
+cudaError_t launch_gemm_tc_cross_entropy(const void* A, long lda, const void* Bm, long ldb,
+                                         long M, int V, int K, const int32_t* tile_list,
+                                         const CrossEntropyEpilogue& ce, unsigned* status,
+                                         cudaStream_t stream) {
+  if (V < 1 || !ce.targets || !ce.part || !ce.target_logit) return cudaErrorInvalidValue;
+  CrossEntropyEpilogue e = ce;
+  e.V = V;
+  return launch_common(DFLASH_DTYPE_BF16, A, lda, Bm, ldb, nullptr, 0, M, V, K, 1, tile_list,
+                       status, nullptr, kEpiCrossEntropy, nullptr, nullptr, stream, kWaitLimitNs,
+                       0, &e);
 }
 
 cudaError_t launch_gemm_tc_withheld(const void* A, long lda, const void* Bm, long ldb, float* C,

@@ -79,6 +79,21 @@ cudaError_t launch_verify_sampling(const void* logits, int dtype, float inv_temp
                                    int32_t* accepted, void* ws, const SamplingPlan& sp,
                                    unsigned* status, cudaStream_t stream);
 
+// ---- loss.cu: decayed cross-entropy of the lm_head over the drafted blocks ----
+struct CeLayout {
+  int n_tiles = 0;                     // vocab tiles of 256 columns
+  __nv_bfloat16* hidden16 = nullptr;   // [T][D] bf16 GEMM operand
+  float* part = nullptr;               // [T][n_tiles][2]
+  float* tlogit = nullptr;             // [T]
+  int32_t* tile_list = nullptr;        // 128-row tiles with a masked slot
+  size_t bytes = 0;
+};
+CeLayout ce_layout(long T, int D, int V, void* ws);
+cudaError_t launch_decayed_ce(const float* hidden, const void* lm_head, const int32_t* targets,
+                              const uint8_t* mask, long T, int S, int D, int V, double decay,
+                              float* ce, float* loss, const CeLayout& l, unsigned* status,
+                              cudaStream_t stream);
+
 // ---- rows.cu: row-wise kernels (norms, RoPE table, GEMM epilogues) ----
 // RoPE table: cos/sin [P, dh/2] fp32 for positions p0 .. p0+P-1, angles formed and
 // range-reduced in fp64 (inverse frequencies computed on the host in fp64; dh <= 256).
@@ -184,6 +199,21 @@ struct KvCacheEpilogue {
   const int32_t* row_pos0 = nullptr;
   int L = 0, pos_offset = 0, L_cache = 0, Hkv = 0;
 };
+// Cross-entropy statistics of lm_head logits, computed in the GEMM epilogue (the logits are
+// never stored): for row m and vocab tile n_t (columns n_t*256 .. +255 below V),
+// part[(m * n_tiles + n_t) * 2 + {0, 1}] = (max, sum of exp(logit - max)); the tile holding
+// targets[m] writes that logit to target_logit[m].
+struct CrossEntropyEpilogue {
+  const int32_t* targets = nullptr;  // [M]
+  float* part = nullptr;             // [M][n_tiles][2]
+  float* target_logit = nullptr;     // [M]
+  int V = 0;
+};
+// A bf16 [M][K] (hidden states), Bm bf16 [V][K] (lm_head); tile_list as for launch_gemm_tc.
+cudaError_t launch_gemm_tc_cross_entropy(const void* A, long lda, const void* Bm, long ldb,
+                                         long M, int V, int K, const int32_t* tile_list,
+                                         const CrossEntropyEpilogue& ce, unsigned* status,
+                                         cudaStream_t stream);
 // act = SiLU(gate) * up with [gate | up] = A W_gate_up^T (W_gate_up [2I][K]: gate rows then
 // up rows), written by the epilogue (no K-split).
 cudaError_t launch_gemm_tc_swiglu(int elem, const void* A, long lda, const void* Bm, long ldb,

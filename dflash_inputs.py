@@ -197,7 +197,7 @@ class Tensor:
 # tensor ids of the per-tensor streams
 _ID = {"w_proj": 1, "g_ctx": 2, "g_final": 3, "g_in": 10, "w_qkv": 11, "w_o": 12,
        "g_post": 13, "w_gate_up": 14, "w_down": 15, "hidden": 20, "emb": 21, "sid": 22,
-       "logits": 30, "draft": 31, "accept": 32, "plant": 33}
+       "logits": 30, "draft": 31, "accept": 32, "plant": 33, "lm_head": 40, "targets": 41}
 
 HIDDEN_CHUNK = 256  # positions per independent stream of target hidden states
 
@@ -418,3 +418,32 @@ def gen_verify(w: Workload, batch: int | None = None, eos: int = -1) -> VerifyIn
     else:
         lt = Tensor(x, "f32")
     return VerifyInputs(lt, draft, eos, k, top)
+
+
+# --------------------------------------------------------------------------------------
+# draft loss inputs
+# --------------------------------------------------------------------------------------
+
+LM_CHUNK = 8192  # vocab rows per independent stream of the lm_head
+
+
+def gen_lm_head(w: Workload, vocab: int) -> Tensor:
+    """A frozen lm_head stand-in [V, D], iid N(0, 0.02) in the workload's dtype."""
+    s = w.shape
+    dt = np.uint16 if s.dtype == "bf16" else np.float32
+    out = np.empty((vocab, s.hidden), dt)
+
+    def fill(k):
+        r0, r1 = k * LM_CHUNK, min(vocab, (k + 1) * LM_CHUNK)
+        out[r0:r1] = _normal(_rng(w.data_seed, _ID["lm_head"], k), (r1 - r0, s.hidden), 0.02,
+                             s.dtype).data
+    _parallel(fill, range((vocab + LM_CHUNK - 1) // LM_CHUNK))
+    return Tensor(out, s.dtype)
+
+
+def gen_targets(w: Workload, vocab: int) -> np.ndarray:
+    """Ground-truth token of every block slot [B, N, S] int32, uniform over the vocab."""
+    rng = _rng(w.data_seed, _ID["targets"])
+    return rng.integers(0, vocab, size=(w.batch, w.num_anchors, w.shape.block_size),
+                        dtype=np.int64).astype(np.int32)
+

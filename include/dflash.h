@@ -254,6 +254,32 @@ DFLASH_API int dflash_body_forward(const dflash_config_t* cfg, const dflash_weig
                         const uint8_t* mask, const void* kv_cache, int B, int L, int N,
                         float* out, void* ws, size_t ws_bytes, void* stream);
 
+/* ---- 3b. draft loss over the blocks ([P1] How it works: Loss; [P2] How It Works step 4;
+ *      [P3] One DFlash generation cycle: greater weight on early positions) ------------- */
+
+DFLASH_API size_t dflash_decayed_ce_workspace_size(int T, int D, int V);
+
+/* The draft's training loss over T = B*N*S block slots: per slot t (slot j = t mod
+ * block_size of its block), CE_t = logsumexp(logits_t) - logits_t[targets[t]] with
+ * logits_t = hidden[t] lm_head^T over the V vocab entries; weights w_j = exp(-(j-1)/decay)
+ * for j >= 1 (the pages fix the exponential decay toward later positions, not its scale:
+ * decay is the caller's), 0 for the anchor; loss = sum(mask w CE) / sum(mask w), 0 when no
+ * slot is weighted.
+ *   hidden     [T, D] float32: dflash_body_forward's output (rounded to bf16 for the GEMM)
+ *   lm_head    [V, D] bf16: the frozen target lm_head
+ *   targets    [T] int32: the ground-truth token of each slot (read where the mask is set;
+ *              outside [0, V) sets DFLASH_ERR_DEVICE_CHECK and the slot counts 0)
+ *   loss_mask  [T] uint8: dflash_plan's loss_mask
+ * Outputs: ce [T] float32 (0 outside the mask) and loss [1] float32, device.  The logits
+ * are never stored: the lm_head GEMM's epilogue reduces each 128 x 256 tile to softmax
+ * statistics.  Deterministic (fixed reduction orders).
+ * Errors: INVALID_ARG for sizes < 1, T not a multiple of block_size, decay <= 0, null or
+ * misaligned pointers; UNSUPPORTED for D not a multiple of 8. */
+DFLASH_API int dflash_decayed_ce_loss(const float* hidden, const void* lm_head,
+                                      const int32_t* targets, const uint8_t* loss_mask, int T,
+                                      int block_size, int D, int V, double decay, float* ce,
+                                      float* loss, void* ws, size_t ws_bytes, void* stream);
+
 /* ---- 4. greedy verification ([P3] One DFlash generation cycle) ----------------------- */
 
 DFLASH_API size_t dflash_verify_workspace_size(int B, int gamma, int V);
