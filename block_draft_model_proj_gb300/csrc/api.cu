@@ -891,7 +891,9 @@ int dflash_verify_sampling(const void* logits, int logits_dtype, double temperat
   int r;
   if ((r = check_ws(ws, ws_bytes, sp.ws_bytes))) return r;
   Prof pr(DFLASH_PROF_VERIFY, 4, (cudaStream_t)stream);
-  DF_CUDA(launch_verify_sampling(logits, logits_dtype, (float)(1.0 / temperature), draft_probs,
+  // the kernels work in base 2: y = logit * log2(e) / temperature
+  DF_CUDA(launch_verify_sampling(logits, logits_dtype, (float)(1.4426950408889634 / temperature),
+                                 draft_probs,
                                  draft, B, gamma, V, seed, eos, emitted, num_emitted, accepted,
                                  ws, sp, status_ptr(), (cudaStream_t)stream));
   return DFLASH_OK;

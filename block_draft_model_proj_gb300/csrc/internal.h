@@ -71,9 +71,10 @@ struct SamplingPlan {
 };
 SamplingPlan plan_sampling(int B, int gamma, int V, int num_sms);
 // logits [B][gamma+1][V] (bf16 or fp32), q [B][gamma][V] fp32 (the actual proposal
-// distributions), draft [B][gamma]; ws holds plan.ws_bytes.  A draft token outside [0, V)
+// distributions), draft [B][gamma]; ws holds plan.ws_bytes.  y_scale = log2(e) / temperature:
+// the softmax runs in base 2 on y = logit * y_scale.  A draft token outside [0, V)
 // reports a device check and counts as rejected.
-cudaError_t launch_verify_sampling(const void* logits, int dtype, float inv_temp, const float* q,
+cudaError_t launch_verify_sampling(const void* logits, int dtype, float y_scale, const float* q,
                                    const int32_t* draft, int B, int gamma, int V, uint64_t seed,
                                    int32_t eos, int32_t* emitted, int32_t* num_emitted,
                                    int32_t* accepted, void* ws, const SamplingPlan& sp,

@@ -15,15 +15,21 @@
 // E_v / w_v with E_v = -ln U(seed, b, i, 1, v); the first arrival is an exact draw from
 // w / sum(w) (lowest index on an exact tie), so no normalisation or prefix sum is needed.
 //
-// Kernel 1 (HBM-bound, one pass over every logits row): per (row, chunk) the maximum of
-//   x = logit / temperature and the sum of exp(x - max), merged online.
+// All softmax arithmetic runs in base 2 on the special-function unit: y = logit *
+// log2(e) / temperature, p = 2^(y - max) / sum 2^(y - max).
+// Kernel 1 (HBM-bound, one pass over every logits row): per (row, chunk) the maximum of y
+//   and the sum of 2^(y - max), merged online (each 16-byte vector: its maximum first, one
+//   rescale, then its exponentials).
 // Kernel 2 (one warp per request): rows' (max, sum) from their chunks in chunk order; the
 //   acceptance scan in block order (p(y) from the row's statistics, q(y) read directly);
 //   writes the accepted proposals and which row, if any, is sampled.
 // Kernel 3 (per (request, chunk)): the race over that row -- weights [p - q]_+ after a
-//   rejection, p for the final sample -- to a (time, index) pair per chunk; a residual that
+//   rejection, p for the final sample -- to a (key, index) pair per chunk; a residual that
 //   is zero everywhere (p == q, possible only through rounding) falls back to p, whose
-//   race is run in the same pass from the same arrival draws.
+//   race is run in the same pass from the same arrival draws.  Arrival E_v / w_v is ranked
+//   as -log2(U_v) / w_v (the factor ln 2 is common to all v); the race of p is ranked as
+//   y_v - log2(-log2 U_v), the logarithm of the reciprocal arrival up to constants (the
+//   Gumbel form: no exponential, no division), which orders the indices identically.
 // Kernel 4 (one thread per request): the first arrival over the chunks, in chunk order.
 #include "common.cuh"
 #include "internal.h"
@@ -50,7 +56,18 @@ __device__ __forceinline__ float logit_at(const T* p, long i) {
   return to_f(p[i]);
 }
 
-// (max, sum of exp(x - max)) merge
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2f(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// (max, sum of 2^(y - max)) merge
 __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2) {
   if (m2 == -INFINITY) return;
   if (m == -INFINITY) {
@@ -59,22 +76,26 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2)
     return;
   }
   if (m2 > m) {
-    s = s * expf(m - m2) + s2;
+    s = s * ex2f(m - m2) + s2;
     m = m2;
   } else {
-    s += s2 * expf(m2 - m);
+    s += s2 * ex2f(m2 - m);
   }
 }
 
-// online (max, sum) of one more value (a -inf logit adds nothing)
-__device__ __forceinline__ void push_ms(float& m, float& s, float x) {
-  if (x == -INFINITY) return;
-  if (x > m) {
-    s = (m == -INFINITY ? 0.f : s * expf(m - x)) + 1.f;
-    m = x;
-  } else {
-    s += expf(x - m);
+// the (max, sum) of n more values y[0..n-1] (a -inf value adds nothing)
+template <int n>
+__device__ __forceinline__ void push_n(float& m, float& s, const float* y) {
+  float lm = y[0];
+#pragma unroll
+  for (int e = 1; e < n; ++e) lm = fmaxf(lm, y[e]);
+  if (lm == -INFINITY) return;
+  if (lm > m) {
+    s = m == -INFINITY ? 0.f : s * ex2f(m - lm);
+    m = lm;
   }
+#pragma unroll
+  for (int e = 0; e < n; ++e) s += ex2f(y[e] - m);
 }
 
 template <typename T>
@@ -97,19 +118,26 @@ softmax_stats_kernel(const T* __restrict__ logits, int V, int chunks, int chunk_
       const uint4 u = __ldcs(pv + t);
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
       if constexpr (sizeof(T) == 2) {
+        float y[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          push_ms(m, s, __uint_as_float(w[e] << 16) * inv_temp);
-          push_ms(m, s, __uint_as_float(w[e] & 0xFFFF0000u) * inv_temp);
+          y[2 * e] = __uint_as_float(w[e] << 16) * inv_temp;
+          y[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u) * inv_temp;
         }
+        push_n<8>(m, s, y);
       } else {
+        float y[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) push_ms(m, s, __uint_as_float(w[e]) * inv_temp);
+        for (int e = 0; e < 4; ++e) y[e] = __uint_as_float(w[e]) * inv_temp;
+        push_n<4>(m, s, y);
       }
     }
     c = c0 + nvec * kVec;
   }
-  for (int v = c + threadIdx.x; v < c1; v += kThreads) push_ms(m, s, logit_at(p, v) * inv_temp);
+  for (int v = c + threadIdx.x; v < c1; v += kThreads) {
+    const float y = logit_at(p, v) * inv_temp;
+    push_n<1>(m, s, &y);
+  }
   // block merge of the (max, sum) pairs, in a fixed order
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -172,7 +200,7 @@ __global__ void sampling_scan_kernel(const T* __restrict__ logits, const float* 
         float M = -INFINITY, Z = 0.f;
         const size_t row = (size_t)b * S + i;
         for (int c = 0; c < chunks; ++c) merge_ms(M, Z, part_m[row * chunks + c], part_s[row * chunks + c]);
-        const float py = expf(logit_at(logits + row * V, y) * inv_temp - M) / Z;
+        const float py = ex2f(logit_at(logits + row * V, y) * inv_temp - M) / Z;
         const float qy = q[((size_t)b * gamma + i) * V + y];
         const float u = grid_uniform(mix64(mix64(hb ^ (uint64_t)i) ^ 0ull));
         acc_i = u * qy < py;
@@ -218,7 +246,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 race_kernel(const T* __restrict__ logits, const float* __restrict__ q,
             const SamplePlan* __restrict__ plan, int gamma, int V, int chunks, int chunk_len,
-            float inv_temp, uint64_t seed, float* __restrict__ race_t,
+            bool vec_ok, float inv_temp, uint64_t seed, float* __restrict__ race_t,
             int* __restrict__ race_i, float* __restrict__ race_tp, int* __restrict__ race_ip) {
   pdl_wait();
   pdl_trigger();
@@ -240,24 +268,54 @@ race_kernel(const T* __restrict__ logits, const float* __restrict__ q,
   const uint64_t hr = mix64(mix64(mix64(mix64(seed) ^ (uint64_t)(int64_t)b) ^ (uint64_t)sp.row) ^ 1ull);
   const float inv_z = 1.f / sp.z;
   const int c0 = chunk * chunk_len, c1 = min(V, c0 + chunk_len);
-  // arrival times: the race of the weights and (after a rejection) the fallback race of p,
-  // both from the same draws
+  // ranking keys, smaller first: after a rejection -log2(U) / [p - q]_+ for the residual and
+  // -(y - log2(-log2 U)) for the fallback race of p; for the final sample the latter alone.
+  // Both from the same draw U_v.
   float bt = INFINITY, btp = INFINITY;
   int bi = 0x7fffffff, bip = 0x7fffffff;
-  for (int v = c0 + threadIdx.x; v < c1; v += kThreads) {
-    const float pv = expf(logit_at(lrow, v) * inv_temp - sp.m) * inv_z;
-    const float w = qrow ? fmaxf(pv - qrow[v], 0.f) : pv;
-    if (!(w > 0.f) && !(pv > 0.f)) continue;
-    const float e = -logf(grid_uniform(mix64(hr ^ (uint64_t)v)));
-    if (w > 0.f) {
-      const float t = e / w;
-      if (t < bt) { bt = t; bi = v; }   // a thread's indices increase: strict < keeps the lowest
+  auto consider = [&](int v, float y, float qv) {
+    if (y == -INFINITY) return;                         // p_v = 0
+    const float nl = -lg2f(grid_uniform(mix64(hr ^ (uint64_t)v)));   // -log2 U > 0
+    const float tp = lg2f(nl) - (y - sp.m);             // Gumbel form of the race of p
+    if (qrow) {
+      const float w = ex2f(y - sp.m) * inv_z - qv;
+      if (w > 0.f) {
+        const float t = __fdividef(nl, w);
+        if (t < bt) { bt = t; bi = v; }   // a thread's indices increase: strict < keeps the lowest
+      }
+      if (tp < btp) { btp = tp; bip = v; }
+    } else if (tp < bt) {
+      bt = tp;
+      bi = v;
     }
-    if (qrow && pv > 0.f) {
-      const float t = e / pv;
-      if (t < btp) { btp = t; bip = v; }
+  };
+  int v0 = c0;
+  if constexpr (sizeof(T) == 2) {
+    if (vec_ok) {
+      // 8 consecutive entries per thread and step: one 16-byte load of logits (and two of q),
+      // all loads of a step issued before the arithmetic
+      const int nvec = (c1 - c0) / 8;
+      for (int t = threadIdx.x; t < nvec; t += kThreads) {
+        const int v = c0 + 8 * t;
+        const uint4 u = __ldcs(reinterpret_cast<const uint4*>(lrow + v));
+        float4 qa = make_float4(0.f, 0.f, 0.f, 0.f), qb = qa;
+        if (qrow) {
+          qa = __ldcs(reinterpret_cast<const float4*>(qrow + v));
+          qb = __ldcs(reinterpret_cast<const float4*>(qrow + v + 4));
+        }
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t bits = (e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16);
+          consider(v + e, __uint_as_float(bits) * inv_temp, qv[e]);
+        }
+      }
+      v0 = c0 + nvec * 8;
     }
   }
+  for (int v = v0 + threadIdx.x; v < c1; v += kThreads)
+    consider(v, logit_at(lrow, v) * inv_temp, qrow ? qrow[v] : 0.f);
   // block minimum of (time, index), lowest index on equal times
   __shared__ float st[kThreads / 32], stp[kThreads / 32];
   __shared__ int si[kThreads / 32], sip[kThreads / 32];
@@ -290,6 +348,8 @@ race_kernel(const T* __restrict__ logits, const float* __restrict__ q,
   }
 }
 
+// One warp per request: lanes take chunks c = lane, lane + 32, ..., then a butterfly; the
+// winner is the smallest key, the lowest index on equal keys -- the same whatever the order.
 __global__ void race_finish_kernel(const SamplePlan* __restrict__ plan,
                                    const float* __restrict__ race_t, const int* __restrict__ race_i,
                                    const float* __restrict__ race_tp,
@@ -298,19 +358,33 @@ __global__ void race_finish_kernel(const SamplePlan* __restrict__ plan,
                                    int32_t* __restrict__ emitted) {
   pdl_wait();
   pdl_trigger();
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
   if (b >= B || plan[b].row < 0) return;
   float bt = INFINITY, btp = INFINITY;
   int bi = 0x7fffffff, bip = 0x7fffffff;
-  for (int c = 0; c < chunks; ++c) {
+  for (int c = lane; c < chunks; c += 32) {
     const size_t k = (size_t)b * chunks + c;
-    if (race_t[k] < bt || (race_t[k] == bt && race_i[k] < bi)) { bt = race_t[k]; bi = race_i[k]; }
-    if (race_tp[k] < btp || (race_tp[k] == btp && race_ip[k] < bip)) { btp = race_tp[k]; bip = race_ip[k]; }
+    const float t = race_t[k], tp = race_tp[k];
+    const int i = race_i[k], ip = race_ip[k];
+    if (t < bt || (t == bt && i < bi)) { bt = t; bi = i; }
+    if (tp < btp || (tp == btp && ip < bip)) { btp = tp; bip = ip; }
   }
-  // an empty residual (p == q after rounding) samples p instead
-  int tok = bi != 0x7fffffff ? bi : bip;
-  if (tok == 0x7fffffff) tok = 0;
-  emitted[(size_t)b * (gamma + 1) + accepted[b]] = tok;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float t2 = __shfl_xor_sync(0xffffffffu, bt, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (t2 < bt || (t2 == bt && i2 < bi)) { bt = t2; bi = i2; }
+    const float tp2 = __shfl_xor_sync(0xffffffffu, btp, o);
+    const int ip2 = __shfl_xor_sync(0xffffffffu, bip, o);
+    if (tp2 < btp || (tp2 == btp && ip2 < bip)) { btp = tp2; bip = ip2; }
+  }
+  if (lane == 0) {
+    // an empty residual (p == q after rounding) samples p instead
+    int tok = bi != 0x7fffffff ? bi : bip;
+    if (tok == 0x7fffffff) tok = 0;
+    emitted[(size_t)b * (gamma + 1) + accepted[b]] = tok;
+  }
 }
 
 }  // namespace
@@ -320,13 +394,15 @@ SamplingPlan plan_sampling(int B, int gamma, int V, int num_sms) {
   const VerifyPlan vp = plan_verify(B, gamma, V, num_sms);
   sp.chunks = vp.chunks;
   sp.chunk_len = vp.chunk_len;
-  // the race covers one row per request: split it further to fill the GPU
+  // the race covers one row per request: about two waves of four resident 256-thread CTAs
+  // per SM over all requests, at least 8192 vocab entries per chunk
   const long rows = B;
-  long best = (3L * 8 * (num_sms > 0 ? num_sms : 1) + rows - 1) / rows;
-  const long max_chunks = (V + 2047) / 2048;
+  long best = (2L * 4 * (num_sms > 0 ? num_sms : 1) + rows - 1) / rows;
+  const long max_chunks = (V + 8191) / 8192;
   if (best > max_chunks) best = max_chunks;
   if (best < 1) best = 1;
   long len = (V + best - 1) / best;
+  len = (len + 7) / 8 * 8;
   sp.race_chunk_len = (int)len;
   sp.race_chunks = (int)((V + len - 1) / len);
   const size_t srows = (size_t)B * (gamma + 1);
@@ -378,14 +454,18 @@ cudaError_t launch_verify_sampling(const void* logits, int dtype, float inv_temp
                         inv_temp, seed, eos, emitted, num_emitted, accepted, plan, status);
   if (e != cudaSuccess) return e;
   const dim3 g3(sp.race_chunks, B);
+  // 16-byte vectors: rows of bf16 logits and of fp32 q start 16-byte aligned, as do chunks
+  const bool race_vec = bf16 && ((uintptr_t)logits % 16 == 0) && ((uintptr_t)q % 16 == 0) &&
+                        (V % 8 == 0) && (sp.race_chunk_len % 8 == 0);
   e = bf16 ? launch_pdl(race_kernel<__nv_bfloat16>, g3, dim3(kThreads), 0, stream,
                         (const __nv_bfloat16*)logits, q, plan, gamma, V, sp.race_chunks,
-                        sp.race_chunk_len, inv_temp, seed, race_t, race_i, race_tp, race_ip)
+                        sp.race_chunk_len, race_vec, inv_temp, seed, race_t, race_i, race_tp,
+                        race_ip)
            : launch_pdl(race_kernel<float>, g3, dim3(kThreads), 0, stream, (const float*)logits,
-                        q, plan, gamma, V, sp.race_chunks, sp.race_chunk_len, inv_temp, seed,
-                        race_t, race_i, race_tp, race_ip);
+                        q, plan, gamma, V, sp.race_chunks, sp.race_chunk_len, false, inv_temp,
+                        seed, race_t, race_i, race_tp, race_ip);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(race_finish_kernel, dim3((B + 127) / 128), dim3(128), 0, stream, plan, race_t,
+  e = launch_pdl(race_finish_kernel, dim3((B + 3) / 4), dim3(128), 0, stream, plan, race_t,
                  race_i, race_tp, race_ip, sp.race_chunks, B, gamma, accepted, emitted);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -4,6 +4,8 @@
     python -m block_draft_model_proj_gb300.kernel_cases gemm --m 512 --n 24576 --k 4096 --f16
     python -m block_draft_model_proj_gb300.kernel_cases body --workload train_8b_b4_l2048
     python -m block_draft_model_proj_gb300.kernel_cases verify --workload decode_8b_b64_ctx4096
+    python -m block_draft_model_proj_gb300.kernel_cases sampling --workload decode_8b_b64_ctx4096
+    python -m block_draft_model_proj_gb300.kernel_cases loss --workload train_8b_b4_l2048
 
 Each case builds its inputs once, runs the kernel `--iters` times and prints the mean
 CUDA-event time per launch (a number printed under a profiler is not a benchmark).
@@ -78,6 +80,11 @@ def case_body(args):
     import block_draft_model_proj_gb300 as dflash
     import dflash_inputs as di
     w = di.WORKLOADS[args.workload]
+    if args.batch:
+        w = di.scaled(w, batch=args.batch,
+                      shared_sid_groups=tuple(g for g in w.shared_sid_groups
+                                              if max(g) < args.batch),
+                      padded_rows=tuple(r for r in w.padded_rows if r[0] < args.batch))
     s = w.shape
     B, L, N, S = w.batch, w.seq_len, w.num_anchors, s.block_size
 
@@ -153,9 +160,69 @@ def case_verify(args):
           f"the device ({n} launches), {nbytes / dev / 1e6:.1f} GB/s")
 
 
+def case_sampling(args):
+    import torch
+    import block_draft_model_proj_gb300 as dflash
+    import dflash_inputs as di
+    w = di.WORKLOADS[args.workload]
+    vi = di.gen_verify(w)
+    Bv, S, V = vi.logits.shape
+    logits = torch.from_numpy(vi.logits.data.view(np.int16)).cuda().view(torch.bfloat16)
+    draft = torch.from_numpy(vi.draft).cuda()
+    # proposal distributions: the target's own at a higher temperature (a stand-in for the
+    # drafter's), normalised per row
+    q = torch.softmax(logits[:, :S - 1].float() / 1.3, dim=-1).contiguous()
+    em = torch.empty((Bv, S), dtype=torch.int32, device="cuda")
+    ne = torch.empty((Bv,), dtype=torch.int32, device="cuda")
+    ac = torch.empty_like(ne)
+    ws = dflash.workspace(dflash.load().dflash_verify_sampling_workspace_size(Bv, S - 1, V))
+
+    def run():
+        dflash.dflash_verify_sampling(logits, dflash.DFLASH_DTYPE_BF16, 1.0, q, draft, Bv, S - 1, V,
+                                      1234, -1, em, ne, ac, ws=ws)
+    run()
+    dflash.dflash_device_status()
+    dflash.dflash_profile_enable(True)
+    _timed(run, args.iters)
+    dev_ms, n = dflash.dflash_profile_read()["verify"]
+    dflash.dflash_profile_enable(False)
+    dev = dev_ms / max(args.iters, 1)
+    nbytes = Bv * S * V * 2
+    print(f"sampling verify [{Bv},{S},{V}] bf16: {dev * 1e3:.2f} us/call on the device "
+          f"({n} launches), logits read at {nbytes / dev / 1e6:.1f} GB/s")
+
+
+def case_loss(args):
+    import torch
+    import block_draft_model_proj_gb300 as dflash
+    import dflash_inputs as di
+    w = di.WORKLOADS[args.workload]
+    s = w.shape
+    T = w.tokens
+    V = args.vocab
+    g = torch.Generator(device="cuda").manual_seed(0)
+    hidden = torch.randn((T, s.hidden), generator=g, device="cuda")
+    lm = (torch.randn((V, s.hidden), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    targets = torch.randint(0, V, (T,), generator=g, device="cuda", dtype=torch.int32)
+    mask = torch.ones((T,), dtype=torch.uint8, device="cuda")
+    mask.view(-1, s.block_size)[:, 0] = 0
+    ce = torch.empty((T,), dtype=torch.float32, device="cuda")
+    loss = torch.empty((1,), dtype=torch.float32, device="cuda")
+    ws = dflash.workspace(dflash.load().dflash_decayed_ce_workspace_size(T, s.hidden, V))
+
+    def run():
+        dflash.dflash_decayed_ce_loss(hidden, lm, targets, mask, T, s.block_size, s.hidden, V, 4.0,
+                                      ce, loss, ws=ws)
+    run()
+    dflash.dflash_device_status()
+    ms = _timed(run, args.iters)
+    flops = 2.0 * int(mask.sum()) * V * s.hidden
+    print(f"decayed CE T={T} D={s.hidden} V={V}: {ms:.4f} ms/call, {flops / ms / 1e9:.1f} TFLOP/s")
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["gemm", "gemm_ws", "body", "verify"])
+    ap.add_argument("case", choices=["gemm", "gemm_ws", "body", "verify", "sampling", "loss"])
     ap.add_argument("--m", type=int, default=8192)
     ap.add_argument("--n", type=int, default=4096)
     ap.add_argument("--k", type=int, default=20480)
@@ -163,11 +230,13 @@ def main(argv=None):
     ap.add_argument("--f16", action="store_true", help="fp16 operands (else bf16)")
     ap.add_argument("--workload", default="train_8b_b4_l2048")
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--batch", type=int, default=0, help="body: override the workload's batch")
+    ap.add_argument("--vocab", type=int, default=151936, help="loss: vocab size")
     args = ap.parse_args(argv)
     from block_draft_model_proj_gb300 import build as b
     b.build()
     {"gemm": case_gemm, "gemm_ws": case_gemm_ws, "body": case_body,
-     "verify": case_verify}[args.case](args)
+     "verify": case_verify, "sampling": case_sampling, "loss": case_loss}[args.case](args)
 
 
 if __name__ == "__main__":
