@@ -421,9 +421,16 @@ struct BodyLayout {
   int* nsplit;          // weight-streaming GEMM: K-splits chosen on the device (QKV, O, down)
   __half* wl16;         // one layer's four matrices as fp16 (converted in the call), or null
   int sp_qkv, sp_o, sp_gu, sp_down;  // host K-splits, or the device upper bounds
+  // 128 x 256 GEMM without a K-split: Q/K RoPE and the attention layouts in the QKV
+  // epilogue, the residual add in the O and down epilogues
+  bool fuse_qkv, fuse_o, fuse_down;
   int P;
   size_t bytes;
 };
+
+// Testing override of the fused-epilogue choice: 0 = by the split bound, 1 = always (on the
+// 128 x 256 GEMM), 2 = never.
+std::atomic<int> g_fused_mode{0};
 
 BodyLayout body_layout(const dflash_config_t* c, int B, int L, int N, void* ws) {
   BodyLayout b;
@@ -449,6 +456,14 @@ BodyLayout body_layout(const dflash_config_t* c, int B, int L, int N, void* ws) 
     b.sp_gu = gemm_splits(T, 2 * I, D);
     b.sp_down = gemm_splits(T, D, I);
   }
+  // Enough output tiles for three waves without a K-split (bound 1): the epilogues write
+  // the attention operands / add into the residual stream directly, and the row passes that
+  // would read fp32 slices drop out.
+  const int fm = g_fused_mode.load();
+  const bool tc_path = c->dtype == DFLASH_DTYPE_BF16 && !b.ws && fm != 2;
+  b.fuse_qkv = tc_path && (fm == 1 || b.sp_qkv == 1);
+  b.fuse_o = tc_path && (fm == 1 || b.sp_o == 1);
+  b.fuse_down = tc_path && (fm == 1 || b.sp_down == 1);
   long ycols = (long)b.sp_qkv * qkvw;
   if ((long)b.sp_o * D > ycols) ycols = (long)b.sp_o * D;
   if ((long)b.sp_gu * 2 * I > ycols) ycols = (long)b.sp_gu * 2 * I;
@@ -670,6 +685,12 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
                                  block_valid, false, T, D, s));
   }
   const bool tc = dt == DFLASH_DTYPE_BF16;
+  if (lay.fuse_qkv) {
+    // the fused QKV epilogue writes active tiles only: zero the rest (and the V^T pad) once
+    Prof pr(DFLASH_PROF_ROWS, 1, s);
+    DF_CUDA(launch_qkv_clear(block_valid, static_cast<__half*>(lay.q), static_cast<__half*>(lay.kb),
+                             static_cast<__half*>(lay.vbt), lay.ns_pad, T, N, S, Hq, Hkv, dh, s));
+  }
   // weight-streaming GEMM of one layer projection: X (fp16) [T][K] x W [Nw][K]^T
   auto ws_args = [&](const void* X, int K, const void* W, int Nw, int max_splits, int* nsplit) {
     WsArgs a;
@@ -704,16 +725,33 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
         dst += sizes[m];
       }
     }
-    {
+    if (lay.fuse_qkv) {
+      QkvEpilogue qe;
+      qe.pos = position_ids;
+      qe.valid = block_valid;
+      qe.cos_t = lay.cos_t;
+      qe.sin_t = lay.sin_t;
+      qe.q = static_cast<__half*>(lay.q);
+      qe.kb = static_cast<__half*>(lay.kb);
+      qe.vbt = static_cast<__half*>(lay.vbt);
+      qe.P = lay.P;
+      qe.ns_pad = lay.ns_pad;
+      qe.NS = N * S;
+      qe.S = S;
+      qe.Hq = Hq;
+      qe.Hkv = Hkv;
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      if (use_ws)
-        DF_CUDA(launch_gemm_ws(ws_args(lay.h.p, D, lw.w_qkv, qkvw, lay.sp_qkv, lay.nsplit), s));
-      else
-        DF_CUDA(gemm(dt, DFLASH_DTYPE_F16, lay.h.p, D, lw.w_qkv, D, lay.y, qkvw, T, qkvw, D,
-                     lay.sp_qkv, s, flags, tc ? lay.nsplit : nullptr));
-    }
-    {
-      Prof pr(DFLASH_PROF_ROWS, 1, s);
+      DF_CUDA(launch_gemm_tc_qkv(lay.h.p, D, lw.w_qkv, D, T, qkvw, D, flags, qe, st, s));
+    } else {
+      {
+        Prof pr(DFLASH_PROF_GEMM, 1, s);
+        if (use_ws)
+          DF_CUDA(launch_gemm_ws(ws_args(lay.h.p, D, lw.w_qkv, qkvw, lay.sp_qkv, lay.nsplit), s));
+        else
+          DF_CUDA(gemm(dt, DFLASH_DTYPE_F16, lay.h.p, D, lw.w_qkv, D, lay.y, qkvw, T, qkvw, D,
+                       lay.sp_qkv, s, flags, tc ? lay.nsplit : nullptr));
+      }
+      Prof pr(DFLASH_PROF_ROWS, 2, s);
       DF_CUDA(launch_qkv_rope(lay.y, lay.sp_qkv, tc ? lay.nsplit : nullptr, position_ids,
                               block_valid, lay.cos_t, lay.sin_t,
                               lay.P, lay.q, lay.kb, lay.vbt, lay.ns_pad, T, N, S, Hq, Hkv, dh,
@@ -739,7 +777,8 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
       aa.Hkv = Hkv;
       aa.num_sms = num_sms();
       aa.status = st;
-      Prof pr(DFLASH_PROF_ATTENTION, 2, s);
+      const AttnTcLayout al = attention_tc_layout(B, N, S, L, Hq, Hkv, num_sms());
+      Prof pr(DFLASH_PROF_ATTENTION, al.max_chunks == 1 ? 1 : 2, s);  // + combine pass
       DF_CUDA(launch_attention_tc(aa, s));
     } else {
       AttnArgs aa;
@@ -765,7 +804,10 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
     }
     {
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      if (use_ws)
+      if (lay.fuse_o)
+        DF_CUDA(launch_gemm_tc_residual(lay.attn.p, qw, lw.w_o, qw, lay.x, D, T, D, qw, flags,
+                                        block_valid, st, s));
+      else if (use_ws)
         DF_CUDA(launch_gemm_ws(ws_args(lay.attn.p, qw, lw.w_o, D, lay.sp_o, lay.nsplit + 1), s));
       else
         DF_CUDA(gemm(dt, DFLASH_DTYPE_F16, lay.attn.p, qw, lw.w_o, qw, lay.y, D, T, D, qw, lay.sp_o,
@@ -773,9 +815,14 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
     }
     {
       Prof pr(DFLASH_PROF_ROWS, 1, s);
-      DF_CUDA(launch_residual_norm(kNormAdd, dt, lay.x, nullptr, lay.y, lay.sp_o,
-                                   tc ? lay.nsplit + 1 : nullptr, lw.g_post, cfg->rms_eps,
-                                   lay.h.out(), nullptr, block_valid, false, T, D, s));
+      if (lay.fuse_o)  // x already holds the sum: the norm only
+        DF_CUDA(launch_residual_norm(kNormAdd, dt, lay.x, nullptr, nullptr, 0, nullptr, lw.g_post,
+                                     cfg->rms_eps, lay.h.out(), nullptr, block_valid, false, T, D,
+                                     s));
+      else
+        DF_CUDA(launch_residual_norm(kNormAdd, dt, lay.x, nullptr, lay.y, lay.sp_o,
+                                     tc ? lay.nsplit + 1 : nullptr, lw.g_post, cfg->rms_eps,
+                                     lay.h.out(), nullptr, block_valid, false, T, D, s));
     }
     if (use_ws && lay.sp_gu > 0) {
       // few tokens: K-split gate/up into fp32 slices (the fused epilogue would leave SMs
@@ -806,21 +853,26 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
     }
     {
       Prof pr(DFLASH_PROF_GEMM, 1, s);
-      if (use_ws)
+      if (lay.fuse_down)
+        DF_CUDA(launch_gemm_tc_residual(lay.act.p, I, lw.w_down, I, lay.x, D, T, D, I, flags,
+                                        block_valid, st, s));
+      else if (use_ws)
         DF_CUDA(launch_gemm_ws(ws_args(lay.act.p, I, lw.w_down, D, lay.sp_down, lay.nsplit + 2), s));
       else
         DF_CUDA(gemm(dt, DFLASH_DTYPE_F16, lay.act.p, I, lw.w_down, I, lay.y, D, T, D, I,
                      lay.sp_down, s, flags, tc ? lay.nsplit + 2 : nullptr));
     }
     Prof pr(DFLASH_PROF_ROWS, 1, s);
+    // fused: x already holds the sum (no slices to add)
+    const float* yd = lay.fuse_down ? nullptr : lay.y;
+    const int nsd = lay.fuse_down ? 0 : lay.sp_down;
+    const int* nsd_dev = lay.fuse_down || !tc ? nullptr : lay.nsplit + 2;
     if (l + 1 < cfg->num_layers) {
-      DF_CUDA(launch_residual_norm(kNormAdd, dt, lay.x, nullptr, lay.y, lay.sp_down,
-                                   tc ? lay.nsplit + 2 : nullptr,
+      DF_CUDA(launch_residual_norm(kNormAdd, dt, lay.x, nullptr, yd, nsd, nsd_dev,
                                    w->layers[l + 1].g_in, cfg->rms_eps, lay.h.out(), nullptr,
                                    block_valid, false, T, D, s));
     } else {
-      DF_CUDA(launch_residual_norm(kNormFinal, dt, lay.x, nullptr, lay.y, lay.sp_down,
-                                   tc ? lay.nsplit + 2 : nullptr, w->g_final,
+      DF_CUDA(launch_residual_norm(kNormFinal, dt, lay.x, nullptr, yd, nsd, nsd_dev, w->g_final,
                                    cfg->rms_eps, ActOut(), out, block_valid,
                                    (cfg->flags & DFLASH_FLAG_FINAL_NORM) != 0, T, D, s));
     }
@@ -947,6 +999,12 @@ int dflash_testing_gemm(int engine, int dtype, const void* A, long lda, const vo
 }
 
 int dflash_testing_gemm_splits(long M, int N, int K) { return gemm_splits(M, N, K); }
+
+int dflash_testing_fused_epilogues(int mode) {
+  if (mode < 0 || mode > 2) return fail(DFLASH_ERR_INVALID_ARG, "mode must be 0, 1 or 2");
+  g_fused_mode.store(mode);
+  return DFLASH_OK;
+}
 
 int dflash_testing_gemm_withheld(const void* A, long lda, const void* Bm, long ldb, float* C,
                                  long ldc, long M, int N, int K, long wait_ns, void* stream) {

@@ -67,7 +67,14 @@ __device__ __forceinline__ void umma_16bit(uint32_t tmem_d, uint64_t adesc, uint
       : "memory");
 }
 
-enum : int { kEpiStoreF32 = 0, kEpiKvCache = 1, kEpiSwiGLU = 2, kEpiCrossEntropy = 3 };
+enum : int {
+  kEpiStoreF32 = 0,
+  kEpiKvCache = 1,
+  kEpiSwiGLU = 2,
+  kEpiCrossEntropy = 3,
+  kEpiQkv = 4,
+  kEpiResidual = 5
+};
 
 struct TcParams {
   long M;
@@ -85,6 +92,8 @@ struct TcParams {
   ActOut act;                  // kEpiSwiGLU: SiLU(gate) * up, [M][swiglu_I]
   int swiglu_I;                // kEpiSwiGLU: B rows [0, I) gate, [I, 2I) up
   CrossEntropyEpilogue ce;     // kEpiCrossEntropy: per-tile softmax statistics of each row
+  QkvEpilogue qkv;             // kEpiQkv: attention-ready Q / K (RoPE) and V^T
+  const uint8_t* row_valid;    // kEpiResidual: rows added into C (= the residual stream)
   uint64_t wait_ns;            // limit of every bounded wait (kWaitLimitNs)
   int test_withhold;           // testing only: the producer issues no copy and no arrival,
                                // so the first wait of the MMA thread runs out
@@ -114,13 +123,70 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int m_cnt, int t,
 }
 
 
+// Rotate-half RoPE of one 128-channel head held in tensor-memory columns hbase .. +127 of
+// the thread's lane (channel i pairs with i + 64; cs / sn = the position's table row of 64
+// angles), rounded to fp16 and stored as dst[0 .. 127].  Every lane takes part in the
+// tensor-memory loads (.sync.aligned); only lanes with `write` store, zeros when !live.
+__device__ __forceinline__ void rope_head_f16(uint32_t hbase, const float* cs, const float* sn,
+                                              __half* dst, bool write, bool live, bool& bad) {
+#pragma unroll 1
+  for (int ch = 0; ch < 2; ++ch) {  // channel chunks (32ch .. 32ch+31) and their pairs +64
+    uint32_t lo[32], hi[32];
+    tmem_ld_32x32b_x32(hbase + ch * 32, lo);
+    tmem_ld_32x32b_x32(hbase + 64 + ch * 32, hi);
+    if (!write) continue;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // 8 channels (16 bytes of fp16) per step
+      uint32_t wa[4] = {0u, 0u, 0u, 0u}, wb[4] = {0u, 0u, 0u, 0u};
+      if (live) {
+#pragma unroll
+        for (int t2 = 0; t2 < 4; ++t2) {
+          const int t = 8 * q + 2 * t2;
+          const float2 c2 = *reinterpret_cast<const float2*>(cs + ch * 32 + t);
+          const float2 s2 = *reinterpret_cast<const float2*>(sn + ch * 32 + t);
+          const float x00 = __uint_as_float(lo[t]), x10 = __uint_as_float(hi[t]);
+          const float x01 = __uint_as_float(lo[t + 1]), x11 = __uint_as_float(hi[t + 1]);
+          const float a0 = x00 * c2.x - x10 * s2.x, a1 = x01 * c2.y - x11 * s2.y;
+          const float b0 = x10 * c2.x + x00 * s2.x, b1 = x11 * c2.y + x01 * s2.y;
+          bad = bad || !(fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))) +
+                         0.f * (a0 + a1 + b0 + b1) < 65520.f);
+          const __half2 ha = __floats2half2_rn(a0, a1);
+          const __half2 hb = __floats2half2_rn(b0, b1);
+          wa[t2] = *reinterpret_cast<const uint32_t*>(&ha);
+          wb[t2] = *reinterpret_cast<const uint32_t*>(&hb);
+        }
+      }
+      reinterpret_cast<uint4*>(dst + ch * 32)[q] = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+      reinterpret_cast<uint4*>(dst + 64 + ch * 32)[q] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+    }
+  }
+}
+
+// One 128-channel V head of the thread's lane, rounded to fp16 and stored transposed:
+// channel d at dst[d * stride] (consecutive lanes hold consecutive positions, so the stores
+// of a warp are coalesced).  Zeros when !live; nothing stored without `write`.
+__device__ __forceinline__ void v_head_f16(uint32_t hbase, __half* dst, long stride, bool write,
+                                           bool live, bool& bad) {
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(hbase + ch * 32, v);
+    if (!write) continue;
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      const float x = live ? __uint_as_float(v[t]) : 0.f;
+      bad = bad || !(fabsf(x) < 65520.f);
+      dst[(long)(ch * 32 + t) * stride] = __float2half_rn(x);
+    }
+  }
+}
+
 // Context K/V epilogue of the per-layer K/V projection (N = 2*Hkv*dh, dh = 128: every
 // 256-column tile holds two whole heads; K heads first).  Row m of the tile is context
 // position c = m mod L of row b = m / L, cache position pos_offset + c.  K heads get RoPE
 // (rotate-half: channel i pairs with i + 64; table row c) and are written as cache rows
-// [pos][dh]; V heads are written transposed, [dh][pos] -- consecutive lanes hold consecutive
-// positions, so those stores are coalesced.  Rows at or past ctx_len[b] are not written.
-// The cache holds fp16 (round to nearest even).
+// [pos][dh]; V heads are written transposed, [dh][pos].  Rows at or past ctx_len[b] are not
+// written.  The cache holds fp16 (round to nearest even).
 __device__ __forceinline__ void kv_cache_epilogue(const TcParams& p, uint32_t tbase, int m_t,
                                                   int n_t, int quarter, int lane) {
   const KvCacheEpilogue& e = p.kv;
@@ -140,56 +206,88 @@ __device__ __forceinline__ void kv_cache_epilogue(const TcParams& p, uint32_t tb
     const uint32_t hbase = tbase + hh * 128;
     if (head < e.Hkv) {
       __half* dst = e.kv + ((long)b * 2 * e.Hkv + head) * plane + pos * 128;
-#pragma unroll 1
-      for (int ch = 0; ch < 2; ++ch) {  // channel chunks (32ch .. 32ch+31) and their pairs +64
-        uint32_t lo[32], hi[32];
-        tmem_ld_32x32b_x32(hbase + ch * 32, lo);
-        tmem_ld_32x32b_x32(hbase + 64 + ch * 32, hi);
-        if (row_ok) {
-          const float* cs = e.cos_t + trow * 64 + ch * 32;
-          const float* sn = e.sin_t + trow * 64 + ch * 32;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {  // 8 channels (16 bytes of fp16) per step
-            uint32_t wa[4], wb[4];
-#pragma unroll
-            for (int t2 = 0; t2 < 4; ++t2) {
-              const int t = 8 * q + 2 * t2;
-              const float2 c2 = *reinterpret_cast<const float2*>(cs + t);
-              const float2 s2 = *reinterpret_cast<const float2*>(sn + t);
-              const float x00 = __uint_as_float(lo[t]), x10 = __uint_as_float(hi[t]);
-              const float x01 = __uint_as_float(lo[t + 1]), x11 = __uint_as_float(hi[t + 1]);
-              const float a0 = x00 * c2.x - x10 * s2.x, a1 = x01 * c2.y - x11 * s2.y;
-              const float b0 = x10 * c2.x + x00 * s2.x, b1 = x11 * c2.y + x01 * s2.y;
-              bad = bad || !(fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))) +
-                             0.f * (a0 + a1 + b0 + b1) < 65520.f);
-              const __half2 ha = __floats2half2_rn(a0, a1);
-              const __half2 hb = __floats2half2_rn(b0, b1);
-              wa[t2] = *reinterpret_cast<const uint32_t*>(&ha);
-              wb[t2] = *reinterpret_cast<const uint32_t*>(&hb);
-            }
-            reinterpret_cast<uint4*>(dst + ch * 32)[q] = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-            reinterpret_cast<uint4*>(dst + 64 + ch * 32)[q] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
-          }
-        }
-      }
+      rope_head_f16(hbase, e.cos_t + trow * 64, e.sin_t + trow * 64, dst, row_ok, true, bad);
     } else {
       __half* dst = e.kv + ((long)b * 2 * e.Hkv + e.Hkv + (head - e.Hkv)) * plane + pos;
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(hbase + ch * 32, v);
-        if (row_ok) {
-#pragma unroll
-          for (int t = 0; t < 32; ++t) {
-            const float x = __uint_as_float(v[t]);
-            bad = bad || !(fabsf(x) < 65520.f);
-            dst[(long)(ch * 32 + t) * e.L_cache] = __float2half_rn(x);
-          }
-        }
-      }
+      v_head_f16(hbase, dst, e.L_cache, row_ok, true, bad);
     }
   }
   if (bad) report(p.status, kStatusRange, kKernEpilogue);
+}
+
+// QKV epilogue of a draft layer (N = (Hq + 2 Hkv) * 128: every 256-column tile holds two
+// whole heads, Q heads first, then K, then V).  Row m is slot m = (b, k, j) of the blocks
+// (b = m / NS, ks = k * S + j = m mod NS).  Q and K heads get RoPE at the slot's position
+// ("DFlash Draft Body", How It Works step 3: position ids of the drafted slots) into
+// q [B][Hkv][NS][grp][128] and kb [B][Hkv][NS][128]; V heads go transposed into
+// vbt [B][Hkv][128][ns_pad].  An invalid slot is written as zeros.
+__device__ __forceinline__ void qkv_epilogue(const TcParams& p, uint32_t tbase, int m_t, int n_t,
+                                             int quarter, int lane) {
+  const QkvEpilogue& e = p.qkv;
+  const long m = (long)m_t * kBM + quarter * 32 + lane;
+  const bool row_ok = m < p.M;
+  const bool live = row_ok && e.valid[m] != 0;
+  const long b = m / e.NS;
+  const long ks = m - b * e.NS;
+  int pp = 0;
+  if (live) {
+    pp = e.pos[m];
+    if (pp < 0 || pp >= e.P) {
+      report(p.status, kStatusCheck, kKernEpilogue);
+      pp = 0;
+    }
+  }
+  const int grp = e.Hq / e.Hkv;
+  const int heads = e.Hq + 2 * e.Hkv;
+  bool bad = false;
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    const int hd = n_t * 2 + hh;
+    if (hd >= heads) break;  // warp-uniform
+    const uint32_t hbase = tbase + hh * 128;
+    if (hd < e.Hq + e.Hkv) {
+      __half* dst;
+      if (hd < e.Hq) {
+        const int g = hd / grp, h = hd - g * grp;
+        dst = e.q + (((b * e.Hkv + g) * e.NS + ks) * grp + h) * 128;
+      } else {
+        dst = e.kb + ((b * e.Hkv + (hd - e.Hq)) * e.NS + ks) * 128;
+      }
+      rope_head_f16(hbase, e.cos_t + (long)pp * 64, e.sin_t + (long)pp * 64, dst, row_ok, live,
+                    bad);
+    } else {
+      __half* dst = e.vbt + (b * e.Hkv + (hd - e.Hq - e.Hkv)) * 128 * (long)e.ns_pad + ks;
+      v_head_f16(hbase, dst, e.ns_pad, row_ok, live, bad);
+    }
+  }
+  if (bad) report(p.status, kStatusRange, kKernEpilogue);
+}
+
+// Residual epilogue: C[row][col] += tile for the valid rows (C is the fp32 residual stream,
+// row stride ldc a multiple of 4).  The thread owns its TMEM lane's row: for each 32-column
+// chunk it issues the eight 16-byte loads of its 128-byte piece of the row first, then reads
+// the accumulator chunk, adds and stores.
+__device__ __forceinline__ void residual_epilogue(const TcParams& p, uint32_t tbase, int m_t,
+                                                  int n_t, int quarter, int lane) {
+  const long row = (long)m_t * kBM + quarter * 32 + lane;
+  const bool live = row < p.M && p.row_valid[row] != 0;
+#pragma unroll 1
+  for (int c = 0; c < kBN / 32; ++c) {
+    const int col0 = n_t * kBN + c * 32;
+    const bool ok = live && col0 < p.N;  // N is a multiple of 32
+    float4* xp = reinterpret_cast<float4*>(p.C + row * p.ldc + col0);
+    float4 xr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) xr[i] = ok ? xp[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(tbase + c * 32, v);
+    if (!ok) continue;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      xp[i] = make_float4(xr[i].x + __uint_as_float(v[4 * i]), xr[i].y + __uint_as_float(v[4 * i + 1]),
+                          xr[i].z + __uint_as_float(v[4 * i + 2]),
+                          xr[i].w + __uint_as_float(v[4 * i + 3]));
+  }
 }
 
 // SwiGLU epilogue: accumulator columns [0, 128) are the gate and [128, 256) the up
@@ -438,6 +536,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         kv_cache_epilogue(p, tbase, m_t, n_t, quarter, lane);
       } else if constexpr (kEpi == kEpiCrossEntropy) {
         cross_entropy_epilogue(p, tbase, m_t, n_t, quarter, lane);
+      } else if constexpr (kEpi == kEpiQkv) {
+        qkv_epilogue(p, tbase, m_t, n_t, quarter, lane);
+      } else if constexpr (kEpi == kEpiResidual) {
+        residual_epilogue(p, tbase, m_t, n_t, quarter, lane);
       } else {
         swiglu_epilogue(p, tbase, m_t, n_t, quarter, lane);
       }
@@ -533,7 +635,8 @@ cudaError_t launch_common(int elem, const void* A, long lda, const void* Bm, lon
                           long ldc, long M, int N, int K, int splits, const int32_t* tile_list,
                           unsigned* status, int* splits_out, int epi, const KvCacheEpilogue* kv, const ActOut* act,
                           cudaStream_t stream, uint64_t wait_ns = kWaitLimitNs,
-                          int test_withhold = 0, const CrossEntropyEpilogue* ce = nullptr) {
+                          int test_withhold = 0, const CrossEntropyEpilogue* ce = nullptr,
+                          const QkvEpilogue* qkv = nullptr, const uint8_t* row_valid = nullptr) {
   if (elem != DFLASH_DTYPE_BF16 && elem != DFLASH_DTYPE_F16) return cudaErrorInvalidValue;
   if (((uintptr_t)A | (uintptr_t)Bm) % 16 != 0) return cudaErrorInvalidValue;
   const bool bf16 = elem == DFLASH_DTYPE_BF16;
@@ -571,11 +674,15 @@ cudaError_t launch_common(int elem, const void* A, long lda, const void* Bm, lon
   p.test_withhold = test_withhold;
   if (kv) p.kv = *kv;
   if (ce) p.ce = *ce;
+  if (qkv) p.qkv = *qkv;
+  p.row_valid = row_valid;
   const long tiles = (long)p.m_tiles * p.n_tiles * p.splits;
   const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
   if (epi == kEpiKvCache) return launch_variant<kEpiKvCache>(ma, mb, p, grid, stream);
   if (epi == kEpiCrossEntropy) return launch_variant<kEpiCrossEntropy>(ma, mb, p, grid, stream);
   if (epi == kEpiSwiGLU) return launch_variant<kEpiSwiGLU>(ma, mb, p, grid, stream);
+  if (epi == kEpiQkv) return launch_variant<kEpiQkv>(ma, mb, p, grid, stream);
+  if (epi == kEpiResidual) return launch_variant<kEpiResidual>(ma, mb, p, grid, stream);
   return launch_variant<kEpiStoreF32>(ma, mb, p, grid, stream);
 }
 
@@ -618,6 +725,30 @@ cudaError_t launch_gemm_tc_cross_entropy(const void* A, long lda, const void* Bm
   return launch_common(DFLASH_DTYPE_BF16, A, lda, Bm, ldb, nullptr, 0, M, V, K, 1, tile_list,
                        status, nullptr, kEpiCrossEntropy, nullptr, nullptr, stream, kWaitLimitNs,
                        0, &e);
+}
+
+cudaError_t launch_gemm_tc_qkv(const void* A, long lda, const void* Bm, long ldb, long M, int N,
+                               int K, const int32_t* tile_list, const QkvEpilogue& e,
+                               unsigned* status, cudaStream_t stream) {
+  if (e.Hq < 1 || e.Hkv < 1 || e.Hq % e.Hkv != 0 || N != (e.Hq + 2 * e.Hkv) * 128 || e.NS < 1 ||
+      e.ns_pad < e.NS || M % e.NS != 0 || e.P < 1 || !e.pos || !e.valid || !e.q || !e.kb ||
+      !e.vbt)
+    return cudaErrorInvalidValue;
+  if (((uintptr_t)e.q | (uintptr_t)e.kb | (uintptr_t)e.cos_t | (uintptr_t)e.sin_t) % 16 != 0)
+    return cudaErrorInvalidValue;
+  return launch_common(DFLASH_DTYPE_F16, A, lda, Bm, ldb, nullptr, 0, M, N, K, 1, tile_list,
+                       status, nullptr, kEpiQkv, nullptr, nullptr, stream, kWaitLimitNs, 0,
+                       nullptr, &e);
+}
+
+cudaError_t launch_gemm_tc_residual(const void* A, long lda, const void* Bm, long ldb, float* x,
+                                    long ldx, long M, int N, int K, const int32_t* tile_list,
+                                    const uint8_t* valid, unsigned* status, cudaStream_t stream) {
+  if (!x || !valid || ldx < N || N % 32 != 0 || ldx % 4 != 0 || (uintptr_t)x % 16 != 0)
+    return cudaErrorInvalidValue;
+  return launch_common(DFLASH_DTYPE_F16, A, lda, Bm, ldb, x, ldx, M, N, K, 1, tile_list, status,
+                       nullptr, kEpiResidual, nullptr, nullptr, stream, kWaitLimitNs, 0, nullptr,
+                       nullptr, valid);
 }
 
 cudaError_t launch_gemm_tc_withheld(const void* A, long lda, const void* Bm, long ldb, float* C,

@@ -59,6 +59,7 @@ constexpr uint32_t kTmemAcc = 0, kTmemA = 256;
 constexpr uint32_t kEpiBufFloats = 32 * 36;             // per epilogue warp: [32][32 + 4]
 constexpr size_t kSmemBytes = 1024 + kRingBytes + 512 + 4 * kEpiBufFloats * sizeof(float);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+static_assert(kMaxStages % 2 == 0, "the converter groups need an even weight-stage count");
 
 struct WsParams {
   long M;            // token rows of X (and C)
@@ -609,6 +610,11 @@ cudaError_t launch(const WsArgs& a, int epi, int w_tiles, int interleave, const 
   p.x_stages = p.x_stage_bytes <= 4096 ? kMaxStages : 4;
   p.w_stages = (int)((kRingBytes - (uint32_t)p.x_stages * p.x_stage_bytes) / kWBytes);
   if (p.w_stages > kMaxStages) p.w_stages = kMaxStages;
+  // the two converter groups take alternate K-steps: with an even stage count every stage
+  // stays with one group (step i and step i + w_stages have the same parity), so a group can
+  // never mistake the other group's phase of a stage for its own
+  p.w_stages &= ~1;
+  if (p.w_stages < 2) return cudaErrorInvalidValue;
   p.splits_out = a.splits_out;
   p.w_bf16 = a.w_dtype == DFLASH_DTYPE_BF16;
   p.interleave = interleave;

@@ -108,7 +108,8 @@ enum NormMode { kNormInit = 0, kNormAdd = 1, kNormFinal = 2 };
 //  kNormFinal: x += sum_s y[s]; out = valid ? (final_norm ? RMSNorm(x) * g : x) : 0
 // y: nsplit partial results [nsplit][rows][D] (fp32; the count read from *nsplit_dev when
 // that is given); emb and g have type `dtype`.  With `valid`, a row of an invalid slot
-// writes zeros (h, or out) and reads nothing.
+// writes zeros (h, or out) and reads nothing.  nsplit = 0 without nsplit_dev: x already
+// holds the sum (the GEMM epilogue added into it) and is only read.
 cudaError_t launch_residual_norm(int mode, int dtype, float* x, const void* emb, const float* y,
                                  int nsplit, const int* nsplit_dev, const void* g, double eps,
                                  ActOut h, float* out, const uint8_t* valid, bool final_norm,
@@ -129,6 +130,12 @@ cudaError_t launch_qkv_rope(const float* y, int nsplit, const int* nsplit_dev, c
                             const float* cos_t, const float* sin_t, int P, void* q, void* kb,
                             void* vbt, int ns_pad, long T, int N, int S, int Hq, int Hkv, int dh,
                             bool f16, unsigned* status, cudaStream_t stream);
+
+// Zeroes what the fused QKV epilogue (launch_gemm_tc_qkv) never writes: q, kb and vbt of
+// every slot of a 128-slot tile without a valid slot, and the pad columns N*S .. ns_pad-1 of
+// vbt (fp16 operands, head_dim dh).  Run once per call, before the first layer.
+cudaError_t launch_qkv_clear(const uint8_t* valid, __half* q, __half* kb, __half* vbt, int ns_pad,
+                             long T, int N, int S, int Hq, int Hkv, int dh, cudaStream_t stream);
 
 // Context K/V epilogue (fp32 configuration): y [nsplit][B*L][2*Hkv*dh] fp32 -> the fp32
 // cache planes of one layer [B][2][Hkv]: K as [L_cache][dh] (RoPE'd; table row c = position
@@ -200,6 +207,31 @@ struct KvCacheEpilogue {
   const int32_t* row_pos0 = nullptr;
   int L = 0, pos_offset = 0, L_cache = 0, Hkv = 0;
 };
+// Attention-ready Q / K / V of the draft body's QKV projection written straight from the
+// GEMM epilogue (head_dim 128, no K-split): GEMM row t is slot t = (b, k, j) of the blocks,
+// columns are the Q heads, then the K heads, then the V heads.  Q and K get RoPE at
+// position pos[t] (table rows [P][64]) and land in q [B][Hkv][N][S][grp][128] and
+// kb [B][Hkv][N*S][128]; V lands transposed in vbt [B][Hkv][128][ns_pad].  Invalid slots
+// are written as zeros.  Slots of 128-row tiles the GEMM skips and the pad columns
+// N*S .. ns_pad-1 of vbt are not written (launch_qkv_clear zeroes them once per call).
+struct QkvEpilogue {
+  const int32_t* pos = nullptr;
+  const uint8_t* valid = nullptr;
+  const float* cos_t = nullptr;
+  const float* sin_t = nullptr;
+  __half* q = nullptr;
+  __half* kb = nullptr;
+  __half* vbt = nullptr;
+  int P = 0, ns_pad = 0, NS = 0, S = 0, Hq = 0, Hkv = 0;
+};
+cudaError_t launch_gemm_tc_qkv(const void* A, long lda, const void* Bm, long ldb, long M, int N,
+                               int K, const int32_t* tile_list, const QkvEpilogue& e,
+                               unsigned* status, cudaStream_t stream);
+// x[t][:] += (A Bm^T)[t][:] for the valid rows t (fp16 operands, fp32 residual stream of
+// width N = ldx, no K-split): the O and down projections add into the residual stream.
+cudaError_t launch_gemm_tc_residual(const void* A, long lda, const void* Bm, long ldb, float* x,
+                                    long ldx, long M, int N, int K, const int32_t* tile_list,
+                                    const uint8_t* valid, unsigned* status, cudaStream_t stream);
 // Cross-entropy statistics of lm_head logits, computed in the GEMM epilogue (the logits are
 // never stored): for row m and vocab tile n_t (columns n_t*256 .. +255 below V),
 // part[(m * n_tiles + n_t) * 2 + {0, 1}] = (max, sum of exp(logit - max)); the tile holding

@@ -78,7 +78,7 @@ __global__ void residual_norm_kernel(int mode, int dt, float* __restrict__ x,
       v = xr[c];
       for (int s = 0; s < nsplit; ++s) v += y[s * split_stride + r * D + c];
     }
-    xr[c] = v;
+    if (mode == kNormInit || nsplit > 0) xr[c] = v;
     ss += v * v;
   }
   ss = block_sum(ss, red);
@@ -177,7 +177,8 @@ __global__ void residual_norm_vec_kernel(int mode, int dt, float* __restrict__ x
       t.z += a.z;
       t.w += a.w;
     }
-    *reinterpret_cast<float4*>(x + idx) = t;
+    // nsplit 0: x already holds the sum (added by the GEMM epilogue), nothing to write back
+    if (mode == kNormInit || nsplit > 0) *reinterpret_cast<float4*>(x + idx) = t;
     v[k] = t;
     ss += t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w;
   }
@@ -587,6 +588,57 @@ cudaError_t launch_rows_norm(int dtype, const float* y, int nsplit, const void* 
         y, nsplit, rows * D, g, (float)eps, with_norm, out, D);
     if (le != cudaSuccess) return le;
   }
+  return cudaGetLastError();
+}
+
+// One CTA of 128 threads per 128-slot tile: when no slot of the tile is valid, thread i
+// zeroes q, kb and the vbt column of slot tile*128 + i.  The extra CTA(s) past the last
+// tile zero the pad columns N*S .. ns_pad-1 of every vbt row.
+__global__ void __launch_bounds__(128) qkv_clear_kernel(const uint8_t* __restrict__ valid,
+                                                         __half* __restrict__ q,
+                                                         __half* __restrict__ kb,
+                                                         __half* __restrict__ vbt, int ns_pad,
+                                                         long T, int NS, int Hq, int Hkv, int dh,
+                                                         long tiles) {
+  pdl_wait();
+  pdl_trigger();
+  if (blockIdx.x < tiles) {
+    const long t = (long)blockIdx.x * 128 + threadIdx.x;
+    const int any = __syncthreads_or(t < T && valid[t] != 0);
+    if (any || t >= T) return;
+    const long b = t / NS, ks = t - b * NS;
+    const int grp = Hq / Hkv;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (int g = 0; g < Hkv; ++g) {
+      uint4* qd = reinterpret_cast<uint4*>(q + ((b * Hkv + g) * NS + ks) * grp * dh);
+      for (int i = 0; i < grp * dh / 8; ++i) qd[i] = z;
+      uint4* kd = reinterpret_cast<uint4*>(kb + ((b * Hkv + g) * NS + ks) * dh);
+      for (int i = 0; i < dh / 8; ++i) kd[i] = z;
+      __half* vd = vbt + (b * Hkv + g) * (long)dh * ns_pad + ks;
+      for (int d = 0; d < dh; ++d) vd[(long)d * ns_pad] = __float2half_rn(0.f);
+    }
+    return;
+  }
+  const int pad = ns_pad - NS;
+  if (pad <= 0) return;
+  const long rows = T / NS * Hkv * dh;  // vbt rows (b, g, d)
+  for (long e = (long)(blockIdx.x - tiles) * 128 + threadIdx.x; e < rows * pad;
+       e += (long)(gridDim.x - tiles) * 128) {
+    const long r = e / pad;
+    vbt[r * ns_pad + NS + (e - r * pad)] = __float2half_rn(0.f);
+  }
+}
+
+cudaError_t launch_qkv_clear(const uint8_t* valid, __half* q, __half* kb, __half* vbt, int ns_pad,
+                             long T, int N, int S, int Hq, int Hkv, int dh, cudaStream_t stream) {
+  const int NS = N * S;
+  if (T < 1 || NS < 1 || T % NS != 0 || dh % 8 != 0 || Hq % Hkv != 0 || ns_pad < NS)
+    return cudaErrorInvalidValue;
+  const long tiles = (T + 127) / 128;
+  const long grid = tiles + 16;  // 16 CTAs for the pad columns
+  cudaError_t e = launch_pdl(qkv_clear_kernel, dim3((unsigned)grid), dim3(128), 0, stream, valid,
+                             q, kb, vbt, ns_pad, T, NS, Hq, Hkv, dh, tiles);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

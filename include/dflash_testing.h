@@ -53,6 +53,16 @@ DFLASH_API int dflash_testing_gemm_withheld(const void* A, long lda, const void*
 /* The K-split the library picks for an M x N x K projection on the current device. */
 DFLASH_API int dflash_testing_gemm_splits(long M, int N, int K);
 
+/* Which body projections of the bf16 configuration use the fused epilogues of the
+ * 128 x 256-tile GEMM (Q/K RoPE and the attention layouts written by the QKV projection's
+ * epilogue; the residual add done by the O and down projections' epilogues), for the calls
+ * of dflash_body_forward that follow:
+ *   0 (default) where the projection's output tiles fill three waves of the SMs without a
+ *     K-split; 1 on every call that runs on the 128 x 256-tile GEMM; 2 never.
+ * The results agree with the unfused path within fp32 rounding of the RoPE products.
+ * Process-wide; returns a DFLASH_* status. */
+DFLASH_API int dflash_testing_fused_epilogues(int mode);
+
 /* The chunk plan of greedy verification, computed on the host (no device needed): each of
  * the B*(gamma+1) logits rows of length V is cut into *chunks column ranges of *chunk_len
  * elements (a multiple of 8), sized for `resident_ctas` resident argmax CTAs.  With

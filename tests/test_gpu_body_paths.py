@@ -153,3 +153,34 @@ def test_every_slot_invalid_in_a_row(lib):
     exactly zero and the other rows are unaffected."""
     check(workload("nowin", index=26, batch=3, seq_len=160, num_anchors=4,
                    padded_rows=((0, 1),)))
+
+
+@pytest.fixture
+def fused_epilogues(lib):
+    """Every projection on the 128 x 256-tile GEMM uses the fused epilogues (Q/K RoPE and the
+    attention layouts from the QKV projection, the residual add from O and down); at these
+    sizes the library would otherwise pick a K-split and the row passes."""
+    import block_draft_model_proj_gb300 as dflash
+    dflash.dflash_testing_fused_epilogues(1)
+    yield
+    dflash.dflash_testing_fused_epilogues(0)
+
+
+# (B, N, S, Hq, Hkv, padded rows, fp16 layers held): slots T = B*N*S above 128 (fp16 held) or
+# 512 (bf16 converted in the call) run on the 128 x 256-tile GEMM.  N*S not a multiple of 8
+# leaves pad columns in V^T; a row with a single valid token makes whole 128-slot tiles
+# invalid (skipped by the GEMM, zeroed once per call); T not a multiple of 128 is ragged.
+FUSED_CASES = [
+    (2, 65, 4, 4, 2, ((1, 200),), True),     # T = 520, N*S = 260 (pad 4)
+    (2, 65, 4, 4, 2, ((1, 200),), False),    # the same with bf16 weights (converted)
+    (3, 64, 4, 4, 2, ((0, 1),), False),      # row 0 invalid: tiles 0, 1 skipped
+    (2, 17, 16, 8, 2, ((1, 150),), True),    # 4 blocks per query tile, T = 544
+    (3, 33, 4, 8, 8, ((2, 100),), True),     # Hq = Hkv: 24 heads, N*S = 132 (pad 4)
+]
+
+
+@pytest.mark.parametrize("B,N,S,Hq,Hkv,pad,f16", FUSED_CASES)
+def test_fused_epilogues(lib, fused_epilogues, B, N, S, Hq, Hkv, pad, f16):
+    check(workload(f"fused_{B}_{N}_{S}_{Hq}_{Hkv}", index=27,
+                   shape=dict(block_size=S, num_heads=Hq, num_kv_heads=Hkv),
+                   batch=B, num_anchors=N, seq_len=304, padded_rows=pad), f16_layers=f16)
