@@ -95,6 +95,7 @@ _SIGS = {
     "dflash_testing_gemm": (_I, [_I, _I, _P, _L, _P, _L, _P, _L, _L, _I, _I, _I, _P]),
     "dflash_testing_gemm_splits": (_I, [_L, _I, _I]),
     "dflash_testing_fused_epilogues": (_I, [_I]),
+    "dflash_testing_gemm_pairs": (_I, [_I]),
     "dflash_testing_gemm_withheld": (_I, [_P, _L, _P, _L, _P, _L, _L, _I, _I, _L, _P]),
     "dflash_testing_gemm_ws": (_I, [_P, _L, _P, _I, _L, _P, _L, _L, _I, _I, _I, _P, _P, _P]),
     "dflash_testing_verify_plan": (_I, [_I, _I, _I, _L, _L, ctypes.POINTER(_I),
@@ -353,6 +354,12 @@ def dflash_testing_gemm_ws(X, W, w_dtype, C, max_splits, splits_out, tile_list=N
     _check(load().dflash_testing_gemm_ws(_ptr(X), X.stride(0), _ptr(W), w_dtype, W.stride(0),
                                          _ptr(C), C.stride(-2), M, N, K, max_splits,
                                          _ptr(tile_list), _ptr(splits_out), _stream(stream)))
+
+
+def dflash_testing_gemm_pairs(mode: int) -> None:
+    """0: the 128 x 256-tile GEMM runs as CTA pairs from two M tiles up (default); 1: one
+    CTA per tile everywhere."""
+    _check(load().dflash_testing_gemm_pairs(mode))
 
 
 def dflash_testing_fused_epilogues(mode: int) -> None:

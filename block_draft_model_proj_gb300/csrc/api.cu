@@ -1000,6 +1000,12 @@ int dflash_testing_gemm(int engine, int dtype, const void* A, long lda, const vo
 
 int dflash_testing_gemm_splits(long M, int N, int K) { return gemm_splits(M, N, K); }
 
+int dflash_testing_gemm_pairs(int mode) {
+  if (mode < 0 || mode > 1) return fail(DFLASH_ERR_INVALID_ARG, "mode must be 0 or 1");
+  set_gemm_tc_pairs(mode);
+  return DFLASH_OK;
+}
+
 int dflash_testing_fused_epilogues(int mode) {
   if (mode < 0 || mode > 2) return fail(DFLASH_ERR_INVALID_ARG, "mode must be 0, 1 or 2");
   g_fused_mode.store(mode);

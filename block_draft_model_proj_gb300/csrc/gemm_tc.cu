@@ -26,6 +26,8 @@
 // outstanding TMA copies and MMAs, frees its tensor memory and exits.
 #include <cuda.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
@@ -43,18 +45,28 @@ constexpr uint32_t kTileABytes = kBM * kBK * 2;    // 16 KB
 constexpr uint32_t kStageBBytes = kBN * kBK * 2;   // 32 KB
 constexpr uint32_t kStagingFloats = 32 * 33;       // per epilogue warp
 
-constexpr int kStages = 4;
 constexpr uint32_t kStageABytes = kTileABytes;
-constexpr uint32_t kTxBytes = kStageABytes + kStageBBytes;
-constexpr size_t kSmemBytes = 1024 + kStages * (size_t)(kStageABytes + kStageBBytes) +
+// One CTA: a 128 x 256 tile, B stage 256 rows, 4 stages.  CTA pair (kPair): a 256 x 256 tile,
+// each CTA holds its 128 A rows and half of the B rows (128), 6 stages of 32 KB.
+template <int kPair>
+struct Ring {
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr uint32_t kStageB = kPair ? kStageBBytes / 2 : kStageBBytes;
+  // bytes one stage's full barrier waits for: the leader's barrier counts both CTAs' copies
+  static constexpr uint32_t kTx = (kPair ? 2u : 1u) * (kStageABytes + kStageB);
+};
+constexpr size_t kSmemBytes = 1024 + 4 * (size_t)(kStageABytes + kStageBBytes) +
                               4 * kStagingFloats * sizeof(float) + 256;
+static_assert(Ring<1>::kStages * (kStageABytes + Ring<1>::kStageB) ==
+                  Ring<0>::kStages * (kStageABytes + Ring<0>::kStageB),
+              "both rings fill the same shared memory");
 
 // Instruction descriptor, kind::f16: D = fp32 (bits 4-5 = 1), A and B format at bits 7-9
 // and 10-12 (0 = fp16, 1 = bf16), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
 // M >> 4 at bits 24-28.
-constexpr uint32_t idesc_16bit(bool bf16) {
+constexpr uint32_t idesc_16bit(bool bf16, int M = kBM) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-         ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+         ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void umma_16bit(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
@@ -63,6 +75,19 @@ __device__ __forceinline__ void umma_16bit(uint32_t tmem_d, uint64_t adesc, uint
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The CTA pair's MMA (M = 256): A rows 0-127 from this CTA's shared memory and 128-255 from
+// the peer's, B columns 0-127 from this CTA's and 128-255 from the peer's (same offsets);
+// each CTA's tensor memory receives its own 128 rows.  Issued by the even CTA only.
+__device__ __forceinline__ void umma_16bit_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -94,6 +119,7 @@ struct TcParams {
   CrossEntropyEpilogue ce;     // kEpiCrossEntropy: per-tile softmax statistics of each row
   QkvEpilogue qkv;             // kEpiQkv: attention-ready Q / K (RoPE) and V^T
   const uint8_t* row_valid;    // kEpiResidual: rows added into C (= the residual stream)
+  uint32_t idesc_pair;         // the CTA pair's instruction descriptor (M = 256)
   uint64_t wait_ns;            // limit of every bounded wait (kWaitLimitNs)
   int test_withhold;           // testing only: the producer issues no copy and no arrival,
                                // so the first wait of the MMA thread runs out
@@ -104,24 +130,32 @@ __device__ __forceinline__ int active_m_tiles(const TcParams& p) {
   return p.tile_list ? p.tile_list[0] : p.m_tiles;
 }
 
-// Work item t -> (M tile, N tile, K split).  Every role walks the same sequence.
-__device__ __forceinline__ void decode_tile(const TcParams& p, int m_cnt, int t, int& m_t, int& n_t,
-                                            int& z) {
-  int mi;
+// Work item t -> (M unit, N tile, K split).  Every role walks the same sequence.  A unit is
+// one M tile, or for a CTA pair two consecutive entries of the M tile order.
+__device__ __forceinline__ void decode_tile(const TcParams& p, int m_units, int t, int& mu,
+                                            int& n_t, int& z) {
   if (p.m_fastest) {
-    mi = t % m_cnt;
-    const int rest = t / m_cnt;
+    mu = t % m_units;
+    const int rest = t / m_units;
     n_t = rest % p.n_tiles;
     z = rest / p.n_tiles;
   } else {
     n_t = t % p.n_tiles;
     const int rest = t / p.n_tiles;
-    mi = rest % m_cnt;
-    z = rest / m_cnt;
+    mu = rest % m_units;
+    z = rest / m_units;
   }
-  m_t = p.tile_list ? p.tile_list[1 + mi] : mi;
 }
 
+// This CTA's M tile of unit mu.  The second tile of a pair's last unit may not exist (an odd
+// tile count): the CTA then takes tile m_tiles, whose rows lie past M -- its loads read the
+// zero fill and its epilogue writes nothing.
+__device__ __forceinline__ int unit_m_tile(const TcParams& p, int m_cnt, int mu, int pair,
+                                           uint32_t rank) {
+  const int mi = pair ? 2 * mu + (int)rank : mu;
+  if (mi >= m_cnt) return p.m_tiles;
+  return p.tile_list ? p.tile_list[1 + mi] : mi;
+}
 
 // Rotate-half RoPE of one 128-channel head held in tensor-memory columns hbase .. +127 of
 // the thread's lane (channel i pairs with i + 64; cs / sn = the position's table row of 64
@@ -366,16 +400,18 @@ __device__ __forceinline__ void cross_entropy_epilogue(const TcParams& p, uint32
   }
 }
 
-template <int kEpi>
+template <int kEpi, int kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const TcParams p) {
+  using R = Ring<kPair>;
+  constexpr int kStages = R::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kStageABytes;
-  float* staging = reinterpret_cast<float*>(sB + kStages * kStageBBytes);
+  float* staging = reinterpret_cast<float*>(sB + kStages * R::kStageB);
   uint64_t* bars = reinterpret_cast<uint64_t*>(staging + 4 * kStagingFloats);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
@@ -386,6 +422,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CTA pair: rank 0 (the leader) issues the MMAs and owns the full / tempty barriers that
+  // count both CTAs; each CTA loads its own A rows and half of B and stores its own rows.
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -393,7 +432,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], kPair ? 8 : 4);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -402,14 +441,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_slot)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (kPair) {
+      tmem_alloc_pair(tmem_slot, kTmemCols);
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_slot)),
+                   "r"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync();  // the peer's barriers are initialised before any use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // prologue done (barriers, tensor memory): wait for the predecessor grid's results, then
@@ -418,13 +462,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   pdl_trigger();
 
   const int m_cnt = active_m_tiles(p);
+  const int m_units = kPair ? (m_cnt + 1) / 2 : m_cnt;
+  const int workers = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;  // CTAs or CTA pairs
+  const int worker = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   int n_splits = p.splits, kb_per = p.kb_per_split;
   if (p.splits_out) {
-    n_splits = choose_splits((long)m_cnt * p.n_tiles, p.num_kb, p.splits, p.sms);
+    n_splits = choose_splits((long)m_units * p.n_tiles, p.num_kb, p.splits, p.sms / (kPair + 1));
     kb_per = (p.num_kb + n_splits - 1) / n_splits;
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.splits_out = n_splits;
   }
-  const int total = m_cnt * p.n_tiles * n_splits;
+  const int total = m_units * p.n_tiles * n_splits;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -435,43 +482,58 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       uint32_t issued_ph[kStages];
       for (int s = 0; s < kStages; ++s) issued[s] = 0, issued_ph[s] = 0;
       bool ok = p.test_withhold == 0;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        int m_t, n_t, z;
-        decode_tile(p, m_cnt, t, m_t, n_t, z);
+      for (int t = worker; t < total && ok; t += workers) {
+        int mu, n_t, z;
+        decode_tile(p, m_units, t, mu, n_t, z);
+        const int m_t = unit_m_tile(p, m_cnt, mu, kPair, rank);
         const int kb0 = z * kb_per;
         const int kb1 = min(p.num_kb, kb0 + kb_per);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, p.wait_ns)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[stage], kTxBytes);
           uint8_t* a_dst = sA + stage * kStageABytes;
-          uint8_t* b_dst = sB + stage * kStageBBytes;
-          tma_load_2d(&map_a, &full[stage], a_dst, kb * kBK, m_t * kBM);
-          // the two 128-row halves of the B tile: consecutive rows, or (SwiGLU) the gate
-          // rows of 128 channels and the up rows of the same channels
-          const int brow0 = kEpi == kEpiSwiGLU ? n_t * 128 : n_t * kBN;
-          const int brow1 = kEpi == kEpiSwiGLU ? p.swiglu_I + n_t * 128 : n_t * kBN + 128;
-          tma_load_2d(&map_b, &full[stage], b_dst, kb * kBK, brow0);
-          tma_load_2d(&map_b, &full[stage], b_dst + kStageBBytes / 2, kb * kBK, brow1);
+          uint8_t* b_dst = sB + stage * R::kStageB;
+          if constexpr (kPair) {
+            // the leader's full barrier counts both CTAs' bytes of the stage
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], R::kTx);
+            const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+            tma_load_2d_pair(&map_a, fb, a_dst, kb * kBK, m_t * kBM);
+            // this CTA's half of the B tile: columns 128*rank .. +127 of the output tile, or
+            // (SwiGLU) the gate rows of 128 channels (leader) and their up rows (peer)
+            const int brow = kEpi == kEpiSwiGLU ? (rank ? p.swiglu_I : 0) + n_t * 128
+                                                : n_t * kBN + (int)rank * 128;
+            tma_load_2d_pair(&map_b, fb, b_dst, kb * kBK, brow);
+          } else {
+            mbar_arrive_expect_tx(&full[stage], R::kTx);
+            tma_load_2d(&map_a, &full[stage], a_dst, kb * kBK, m_t * kBM);
+            // the two 128-row halves of the B tile: consecutive rows, or (SwiGLU) the gate
+            // rows of 128 channels and the up rows of the same channels
+            const int brow0 = kEpi == kEpiSwiGLU ? n_t * 128 : n_t * kBN;
+            const int brow1 = kEpi == kEpiSwiGLU ? p.swiglu_I + n_t * 128 : n_t * kBN + 128;
+            tma_load_2d(&map_b, &full[stage], b_dst, kb * kBK, brow0);
+            tma_load_2d(&map_b, &full[stage], b_dst + R::kStageB / 2, kb * kBK, brow1);
+          }
           issued[stage] = 1;
           issued_ph[stage] = ph;
           if (++stage == kStages) { stage = 0; ph ^= 1u; }
         }
       }
-      // wait for this thread's own copies still in flight
-      for (int s = 0; s < kStages; ++s)
-        if (issued[s]) mbar_drain_wait(&full[s], issued_ph[s], p.wait_ns / 4);
+      // wait for the copies still in flight (a pair's leader: both CTAs' copies, which its
+      // full barriers count; the peer's copies complete on those barriers only)
+      if (!kPair || rank == 0)
+        for (int s = 0; s < kStages; ++s)
+          if (issued[s]) mbar_drain_wait(&full[s], issued_ph[s], p.wait_ns / 4);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && (!kPair || rank == 0)) {
       // ---------------- MMA issuer ----------------
       int stage = 0;
       uint32_t ph = 0;
       int acc = 0;
       uint32_t acc_ph = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        int m_t, n_t, z;
-        decode_tile(p, m_cnt, t, m_t, n_t, z);
+      for (int t = worker; t < total && ok; t += workers) {
+        int mu, n_t, z;
+        decode_tile(p, m_units, t, mu, n_t, z);
         const int kb0 = z * kb_per;
         const int kb1 = min(p.num_kb, kb0 + kb_per);
         if (!mbar_wait(&tempty[acc], acc_ph ^ 1u, abort_flag, p.wait_ns)) break;
@@ -481,33 +543,44 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           if (!mbar_wait(&full[stage], ph, abort_flag, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(sA + stage * kStageABytes);
-          const uint32_t b_addr = smem_u32(sB + stage * kStageBBytes);
+          const uint32_t b_addr = smem_u32(sB + stage * R::kStageB);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            // advancing K by 16 bf16 = 32 bytes inside the 128-byte swizzle atom
-            umma_16bit(d_tmem, sw128_desc(a_addr + k * 32), sw128_desc(b_addr + k * 32), p.idesc,
-                       (kb > kb0 || k > 0) ? 1u : 0u);
+            // advancing K by 16 elements = 32 bytes inside the 128-byte swizzle atom
+            const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
+            if constexpr (kPair)
+              umma_16bit_pair(d_tmem, sw128_desc(a_addr + k * 32), sw128_desc(b_addr + k * 32),
+                              p.idesc_pair, accum);
+            else
+              umma_16bit(d_tmem, sw128_desc(a_addr + k * 32), sw128_desc(b_addr + k * 32),
+                         p.idesc, accum);
           }
-          umma_commit(&empty[stage]);
+          if constexpr (kPair) umma_commit_pair_multicast(&empty[stage], 3);  // both CTAs' stage
+          else umma_commit(&empty[stage]);
           if (++stage == kStages) { stage = 0; ph ^= 1u; }
         }
         if (!ok) break;
-        umma_commit(&tfull[acc]);
+        if constexpr (kPair) umma_commit_pair_multicast(&tfull[acc], 3);
+        else umma_commit(&tfull[acc]);
         if (++acc == 2) { acc = 0; acc_ph ^= 1u; }
       }
       // all MMAs issued by this thread complete before tensor memory is released
-      umma_commit(drain);
+      if constexpr (kPair) umma_commit_pair(drain);
+      else umma_commit(drain);
       mbar_drain_wait(drain, 0, p.wait_ns / 4);
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     float* stg = staging + (warp - 2) * kStagingFloats;
+    // a pair's accumulator is released on the leader's barrier (8 arrivals: both CTAs)
+    const uint32_t tempty_leader = kPair ? mapa_shared(smem_u32(tempty), 0) : 0u;
     int acc = 0;
     uint32_t acc_ph = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      int m_t, n_t, z;
-      decode_tile(p, m_cnt, t, m_t, n_t, z);
+    for (int t = worker; t < total; t += workers) {
+      int mu, n_t, z;
+      decode_tile(p, m_units, t, mu, n_t, z);
+      const int m_t = unit_m_tile(p, m_cnt, mu, kPair, rank);
       // warp-uniform result: the tcgen05.ld below is .sync.aligned
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_ph, abort_flag, p.wait_ns) ? 1 : 0))
         break;
@@ -545,18 +618,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) {
+        if constexpr (kPair) mbar_arrive_cluster(tempty_leader + (uint32_t)(acc * 8));
+        else mbar_arrive(&tempty[acc]);
+      }
       if (++acc == 2) { acc = 0; acc_ph ^= 1u; }
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync();  // the leader's MMAs into the peer's memory are done
   tc_fence_after();
   if (warp == 1) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(kTmemCols)
-                 : "memory");
+    if constexpr (kPair) {
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    } else {
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(kTmemCols)
+                   : "memory");
+    }
   }
   if (threadIdx.x == 0 && *abort_flag) report(p.status, kStatusTimeout, kKernGemmTc);
 }
@@ -616,19 +697,55 @@ bool gemm_tc_supported(long M, int N, int K, long lda, long ldb) {
 
 namespace {
 
+std::atomic<int> g_pair_mode{0};  // 0: CTA pairs from two M tiles up; 1: one CTA per tile
+
+// CTA pairs the device can hold at once with this kernel's shared memory (once per kernel).
+template <int kEpi>
+int max_active_pairs() {
+  static int cached = 0;
+  if (cached > 0) return cached;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 256);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<kEpi, 1>, &cfg) != cudaSuccess || n < 1)
+    n = sm_count() / 2;
+  cached = n;
+  return n;
+}
+
 template <int kEpi>
 cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p,
-                           int grid, cudaStream_t stream) {
+                           long units, bool pair, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<kEpi>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<kEpi, 0>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemm_tc_kernel<kEpi, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_pdl(gemm_tc_kernel<kEpi>, dim3(grid), dim3(kThreads), kSmemBytes, stream, ma, mb,
-                    p);
+  if (pair) {
+    const long pairs = max_active_pairs<kEpi>();
+    const int grid = 2 * (int)(units < pairs ? units : pairs);
+    return launch_pdl_cluster(gemm_tc_kernel<kEpi, 1>, dim3(grid), dim3(kThreads), kSmemBytes,
+                              stream, 2, ma, mb, p);
+  }
+  const int sms = sm_count();
+  const int grid = (int)(units < sms ? units : sms);
+  return launch_pdl(gemm_tc_kernel<kEpi, 0>, dim3(grid), dim3(kThreads), kSmemBytes, stream, ma,
+                    mb, p);
 }
 
 cudaError_t launch_common(int elem, const void* A, long lda, const void* Bm, long ldb, float* C,
@@ -669,6 +786,7 @@ cudaError_t launch_common(int elem, const void* A, long lda, const void* Bm, lon
   // in the same wave and read it once
   p.m_fastest = (double)M <= (double)N ? 1 : 0;
   p.idesc = idesc_16bit(bf16);
+  p.idesc_pair = idesc_16bit(bf16, 2 * kBM);
   p.status = status;
   p.wait_ns = wait_ns;
   p.test_withhold = test_withhold;
@@ -676,14 +794,19 @@ cudaError_t launch_common(int elem, const void* A, long lda, const void* Bm, lon
   if (ce) p.ce = *ce;
   if (qkv) p.qkv = *qkv;
   p.row_valid = row_valid;
-  const long tiles = (long)p.m_tiles * p.n_tiles * p.splits;
-  const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-  if (epi == kEpiKvCache) return launch_variant<kEpiKvCache>(ma, mb, p, grid, stream);
-  if (epi == kEpiCrossEntropy) return launch_variant<kEpiCrossEntropy>(ma, mb, p, grid, stream);
-  if (epi == kEpiSwiGLU) return launch_variant<kEpiSwiGLU>(ma, mb, p, grid, stream);
-  if (epi == kEpiQkv) return launch_variant<kEpiQkv>(ma, mb, p, grid, stream);
-  if (epi == kEpiResidual) return launch_variant<kEpiResidual>(ma, mb, p, grid, stream);
-  return launch_variant<kEpiStoreF32>(ma, mb, p, grid, stream);
+  // Two or more M tiles: CTA pairs (M = 256 MMAs, each CTA reading half of every B tile),
+  // whose MMAs run at the tensor cores' full rate; the one-CTA kernel's A-and-B-from-shared-
+  // memory MMA is bound by shared-memory operand reads.
+  const bool pair = g_pair_mode.load() == 0 && p.m_tiles >= 2;
+  const long m_units = pair ? (p.m_tiles + 1) / 2 : p.m_tiles;
+  const long units = m_units * p.n_tiles * p.splits;
+  if (epi == kEpiKvCache) return launch_variant<kEpiKvCache>(ma, mb, p, units, pair, stream);
+  if (epi == kEpiCrossEntropy)
+    return launch_variant<kEpiCrossEntropy>(ma, mb, p, units, pair, stream);
+  if (epi == kEpiSwiGLU) return launch_variant<kEpiSwiGLU>(ma, mb, p, units, pair, stream);
+  if (epi == kEpiQkv) return launch_variant<kEpiQkv>(ma, mb, p, units, pair, stream);
+  if (epi == kEpiResidual) return launch_variant<kEpiResidual>(ma, mb, p, units, pair, stream);
+  return launch_variant<kEpiStoreF32>(ma, mb, p, units, pair, stream);
 }
 
 }  // namespace
@@ -750,6 +873,8 @@ cudaError_t launch_gemm_tc_residual(const void* A, long lda, const void* Bm, lon
                        nullptr, kEpiResidual, nullptr, nullptr, stream, kWaitLimitNs, 0, nullptr,
                        nullptr, valid);
 }
+
+void set_gemm_tc_pairs(int mode) { g_pair_mode.store(mode); }
 
 cudaError_t launch_gemm_tc_withheld(const void* A, long lda, const void* Bm, long ldb, float* C,
                                     long ldc, long M, int N, int K, uint64_t wait_ns,

@@ -27,6 +27,28 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// The same, launched as thread-block clusters of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                                      size_t smem, cudaStream_t stream, int cluster_x,
+                                      Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- api.cu ----
 // Records the thread-local message returned by dflash_last_error(); returns `code`.
 int set_error(int code, const char* fmt, ...);
@@ -262,6 +284,10 @@ cudaError_t launch_gemm_tc_kv_cache(int elem, const void* A, long lda, const voi
 cudaError_t launch_gemm_tc(int elem, const void* A, long lda, const void* Bm, long ldb, float* C,
                            long ldc, long M, int N, int K, int splits, const int32_t* tile_list,
                            unsigned* status, cudaStream_t stream, int* splits_out = nullptr);
+
+// 0 (default): the 128 x 256-tile GEMMs run as CTA pairs (256 x 256 per pair) from two M
+// tiles up; 1: one CTA per 128 x 256 tile everywhere.  Process-wide.
+void set_gemm_tc_pairs(int mode);
 
 // Testing only: the bf16 GEMM with its TMA producer withholding every copy and arrival and
 // every bounded wait limited to wait_ns, so the MMA thread's first wait runs out: the CTAs

@@ -53,6 +53,15 @@ DFLASH_API int dflash_testing_gemm_withheld(const void* A, long lda, const void*
 /* The K-split the library picks for an M x N x K projection on the current device. */
 DFLASH_API int dflash_testing_gemm_splits(long M, int N, int K);
 
+/* How the 128 x 256-tile tensor-core GEMM behind every 16-bit projection runs, for the
+ * calls that follow: 0 (default) as pairs of CTAs (a thread-block cluster of two computing a
+ * 256 x 256 tile with tcgen05 cta_group::2 MMAs, each CTA loading its 128 rows of A and
+ * half of the B tile) whenever the GEMM has at least two 128-row M tiles, else one CTA per
+ * 128 x 256 tile; 1: one CTA per tile everywhere.  Results are bit-identical between the
+ * two (same MMA shapes per output element and K order).  Process-wide; returns a DFLASH_*
+ * status. */
+DFLASH_API int dflash_testing_gemm_pairs(int mode);
+
 /* Which body projections of the bf16 configuration use the fused epilogues of the
  * 128 x 256-tile GEMM (Q/K RoPE and the attention layouts written by the QKV projection's
  * epilogue; the residual add done by the O and down projections' epilogues), for the calls

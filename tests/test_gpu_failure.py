@@ -11,9 +11,20 @@ import pytest
 pytestmark = pytest.mark.gpu
 
 
-def test_withheld_producer_runs_out_its_wait_and_reports_timeout(lib):
+@pytest.mark.parametrize("pairs", [0, 1], ids=["cta_pairs", "one_cta"])
+def test_withheld_producer_runs_out_its_wait_and_reports_timeout(lib, pairs):
+    """Both forms of the 128 x 256-tile GEMM: CTA pairs (256 rows = two M tiles) and one
+    CTA per tile."""
     import torch
     import block_draft_model_proj_gb300 as dflash
+    dflash.dflash_testing_gemm_pairs(pairs)
+    try:
+        _withheld_case(torch, dflash)
+    finally:
+        dflash.dflash_testing_gemm_pairs(0)
+
+
+def _withheld_case(torch, dflash):
     g = torch.Generator(device="cuda").manual_seed(3)
     A = torch.randn((256, 128), generator=g, device="cuda").to(torch.bfloat16)
     B = torch.randn((512, 128), generator=g, device="cuda").to(torch.bfloat16)

@@ -69,6 +69,25 @@ def test_tcgen05_gemm(lib, M, N, K, splits):
     assert_close(got, ref, K)
 
 
+@pytest.mark.parametrize("M,N,K,splits", [(300, 520, 200, 1), (1000, 300, 4104, 2),
+                                          (128 * 24 + 64, 256 * 16, 192, 1)])
+def test_tcgen05_gemm_cta_pairs_match_one_cta(lib, M, N, K, splits):
+    """The CTA-pair form (256 x 256 per pair, cta_group::2 MMAs with M = 256) against the
+    one-CTA form of the same GEMM: an odd M tile count (the last pair's second tile empty),
+    K-splits, more pair units than pairs."""
+    import block_draft_model_proj_gb300 as dflash
+    got_pair, ref, _ = run(dflash.DFLASH_TESTING_ENGINE_TC, "bf16", M, N, K, splits, seed=7)
+    dflash.dflash_testing_gemm_pairs(1)
+    try:
+        got_one, _, _ = run(dflash.DFLASH_TESTING_ENGINE_TC, "bf16", M, N, K, splits, seed=7)
+    finally:
+        dflash.dflash_testing_gemm_pairs(0)
+    assert_close(got_pair, ref, K)
+    assert_close(got_one, ref, K)
+    diff = float(np.abs(got_pair - got_one).max())
+    assert diff == 0.0, diff
+
+
 @pytest.mark.parametrize("M,N,K,splits", [(128, 256, 64, 1), (300, 520, 200, 1),
                                           (16, 6144, 4096, 4), (1000, 300, 4104, 2)])
 def test_tcgen05_gemm_f16(lib, M, N, K, splits):
