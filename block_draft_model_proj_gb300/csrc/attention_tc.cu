@@ -28,21 +28,21 @@
 // with a lazily updated running maximum (the accumulator is rescaled only when the maximum
 // grows by more than 2^8, so P stays <= 256).
 //
-// Key tiles are 128 keys.  Tensor memory holds the whole working set of a tile: Q (loaded
-// once per unit from global by the softmax warps, packed fp16 pairs) [0,64), the O
-// accumulator [128,256), and two S/P buffers [256,384) and [384,512) (S = Q K^T lands there;
-// each softmax warp overwrites the first half of its own 64 S columns with its packed fp16
-// P, and O += P V reads P from there).  Shared memory holds only the K and V^T tiles, in two
-// 3-stage TMA rings of 32 KB stages.
-// Warp roles: warp 0 TMA producers (lane 0 the K ring, lane 1 the V^T ring); warp 1 MMA
-// issuer, one thread, in a fixed order (S of the next-but-one tile right behind each PV);
+// Key tiles are 128 keys.  Tensor memory holds the O accumulator [0,128) and three S/P
+// buffers [128,256), [256,384), [384,512) (S = Q K^T lands there; each softmax warp
+// overwrites the first half of its own 64 S columns with its packed fp16 P, and O += P V
+// reads P from there).  Shared memory holds Q (TMA, once per unit), a 3-stage K ring and a
+// 2-stage V^T ring of 32 KB stages.
+// Warp roles: warp 0 TMA producers (lane 0 Q and the K ring, lane 1 the V^T ring); warp 1
+// MMA issuer, one thread, in a fixed order (S of the tile three ahead right behind each PV);
 // warps 2-9 softmax / correction / partial output: two warps per TMEM lane quarter, one per
 // half of the key columns (and of the O columns), so each SM sub-partition runs two softmax
 // warps; the halves agree on the running row maximum through shared memory behind an
-// mbarrier.  Fully readable 16-key groups take a short path (one zero-byte test per mask
-// word), and P = 2^(x - m) uses the special-function unit directly (an excluded key gives
-// exactly 0).  Every mbarrier wait is bounded in time; on expiry the CTA reports
-// DFLASH_ERR_TIMEOUT, drains its own copies and MMAs, frees tensor memory and exits.
+// mbarrier per lane quarter.  A half tile whose 64 mask bytes are all set takes a short path
+// (one warp vote over its 16 mask words), and P = 2^(x * scale - m) is one FMA into the
+// special-function unit's exponential (an excluded key gives exactly 0).  Every mbarrier
+// wait is bounded in time; on expiry the CTA reports DFLASH_ERR_TIMEOUT, drains its own
+// copies and MMAs, frees tensor memory and exits.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
@@ -56,21 +56,24 @@ using namespace tc;
 constexpr int kDH = 128;   // head dim handled by this kernel
 constexpr int kM = 128;    // query rows per tile (TMEM lanes)
 constexpr int kKT = 128;   // keys per tile (the N of the S MMA)
-constexpr int kRing = 3;   // stages of each of the K and V^T rings
-constexpr int kSP = 2;     // S/P buffers in tensor memory
+constexpr int kRingK = 3;  // stages of the K ring
+constexpr int kRingV = 2;  // stages of the V^T ring
+constexpr int kSP = 3;     // S/P buffers in tensor memory
+static_assert(kSP == kRingK, "S(i) completing frees K stage i % kRingK and S buffer i % kSP");
 constexpr int kThreads = 320;          // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
 constexpr int kSoftmaxWarps = 8;       // two per TMEM lane quarter, each owns half the keys
 constexpr int kHalfKT = 64;            // key columns per softmax thread
-constexpr uint32_t kTmemCols = 512;    // Q [0,64), O [128,256), S/P 2 x 128 [256,512)
-constexpr uint32_t kTmemQ = 0, kTmemO = 128, kTmemS = 256;
+constexpr uint32_t kTmemCols = 512;    // O [0,128), S/P 3 x 128 [128,512)
+constexpr uint32_t kTmemO = 0, kTmemS = 128;
 constexpr uint32_t kKSub = kKT * 64 * 2;   // K [128 keys][64 dh] fp16, 16 KB
 constexpr uint32_t kKBytes = 2 * kKSub;    // 32 KB
 constexpr uint32_t kVSub = kDH * 64 * 2;   // V^T [128 dh][64 keys] fp16, 16 KB
 constexpr uint32_t kVBytes = 2 * kVSub;    // 32 KB
+constexpr uint32_t kQBytes = 2 * kKSub;   // Q [128 rows][64 dh] x 2 fp16, 32 KB
 constexpr uint32_t kBarBytes = 512;
-// K ring + V ring + barriers + row-max exchange [2][2][128] + row-sum exchange [2][128]
-constexpr size_t kSmemBytes = 1024 + kRing * (size_t)(kKBytes + kVBytes) + kBarBytes +
-                              (4 * 128 + 2 * 128) * sizeof(float);
+// K ring + V ring + Q + barriers + row-max exchange [2][2][128] + row-sum exchange [2][128]
+constexpr size_t kSmemBytes = 1024 + kRingK * (size_t)kKBytes + kRingV * (size_t)kVBytes +
+                              kQBytes + kBarBytes + (4 * 128 + 2 * 128) * sizeof(float);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 constexpr uint32_t kIdescS = idesc_f16(kM, kKT);
 constexpr uint32_t kIdescPV = idesc_f16(kM, kDH);
@@ -125,7 +128,7 @@ __device__ __forceinline__ UnitInfo decode_unit(const AttnTcParams& p, int unit)
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant__ CUtensorMap map_vc,
                const __grid_constant__ CUtensorMap map_kb, const __grid_constant__ CUtensorMap map_vb,
-               const AttnTcParams p) {
+               const __grid_constant__ CUtensorMap map_q, const AttnTcParams p) {
   pdl_wait();
   const UnitInfo u = decode_unit(p, blockIdx.x);
   if (u.n == 0) return;  // a chunk past this tile's longest prefix: no work
@@ -134,28 +137,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* sK = smem;                        // K ring: stage s at s * kKBytes
-  uint8_t* sV = sK + kRing * kKBytes;        // V^T ring: stage s at s * kVBytes
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kRing * kVBytes);
+  uint8_t* sV = sK + kRingK * kKBytes;       // V^T ring: stage s at s * kVBytes
+  uint8_t* sQ = sV + kRingV * kVBytes;       // Q of the tile: two [128 rows][64 dh] boxes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sQ + kQBytes);
   uint64_t* k_full = bars;
-  uint64_t* k_empty = k_full + kRing;
-  uint64_t* v_full = k_empty + kRing;
-  uint64_t* v_empty = v_full + kRing;
-  uint64_t* s_full = v_empty + kRing;
+  uint64_t* v_full = k_full + kRingK;
+  uint64_t* v_empty = v_full + kRingV;
+  uint64_t* s_full = v_empty + kRingV;
   uint64_t* p_full = s_full + kSP;
-  uint64_t* q_ready = p_full + kSP;
-  uint64_t* drain = q_ready + 1;
-  uint64_t* max_bar = drain + 1;    // [2]: row-max exchange of tiles with parity 0 / 1
-  uint64_t* sum_bar = max_bar + 2;  // row-sum exchange at the end
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sum_bar + 1);
+  uint64_t* q_full = p_full + kSP;
+  uint64_t* drain = q_full + 1;
+  // row-max exchange between the two warps of a TMEM lane quarter: [quarter][tile parity]
+  uint64_t* max_bar = drain + 1;
+  uint64_t* sum_bar = max_bar + 8;  // [quarter]: row-sum exchange at the end
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sum_bar + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* red_max = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + kBarBytes);  // [2][2][128]
   float* red_sum = red_max + 4 * 128;                                                       // [2][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s2 = 0; s2 < kRing; ++s2) {
+    for (int s2 = 0; s2 < kRingK; ++s2) {
       mbar_init(&k_full[s2], 1);
-      mbar_init(&k_empty[s2], 1);
+    }
+    for (int s2 = 0; s2 < kRingV; ++s2) {
       mbar_init(&v_full[s2], 1);
       mbar_init(&v_empty[s2], 1);
     }
@@ -163,11 +168,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], kSoftmaxWarps);
     }
-    mbar_init(q_ready, kSoftmaxWarps);
+    mbar_init(q_full, 1);
     mbar_init(drain, 1);
-    mbar_init(&max_bar[0], kSoftmaxWarps);
-    mbar_init(&max_bar[1], kSoftmaxWarps);
-    mbar_init(sum_bar, kSoftmaxWarps);
+    for (int i = 0; i < 8; ++i) mbar_init(&max_bar[i], 2);
+    for (int i = 0; i < 4; ++i) mbar_init(&sum_bar[i], 2);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -178,25 +182,34 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
   // the successor grid may be scheduled once this CTA holds its tensor memory
   pdl_trigger();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_q = tmem + kTmemQ, tmem_o = tmem + kTmemO, tmem_s0 = tmem + kTmemS;
+  const uint32_t tmem_o = tmem + kTmemO, tmem_s0 = tmem + kTmemS;
 
   const int planes_per_b = 2 * p.Hkv;
   const int plane_k = u.b * planes_per_b + u.g;
   const int plane_v = u.b * planes_per_b + p.Hkv + u.g;
 
   if (warp == 0) {
-    // ---------------- TMA producers: lane 0 = the K ring, lane 1 = the V^T ring ----------------
-    // A K tile is two [128 keys][64 dh] boxes (the two halves of dh), a V^T tile two
-    // [128 dh][64 keys] boxes (the two halves of the keys), each 128-byte swizzled.
+    // ---------------- TMA producers: lane 0 = Q, then the K ring; lane 1 = the V^T ring ----------------
+    // Q is two [128 rows][64 dh] boxes, a K tile two [128 keys][64 dh] boxes (the two halves
+    // of dh), a V^T tile two [128 dh][64 keys] boxes (the two halves of the keys), each
+    // 128-byte swizzled.
     if (lane < 2) {
       const bool is_k = lane == 0;
+      const int ring = is_k ? kRingK : kRingV;
       uint64_t* full = is_k ? k_full : v_full;
-      uint64_t* empty = is_k ? k_empty : v_empty;
-      int issued[kRing] = {0, 0, 0};
-      uint32_t issued_ph[kRing] = {0, 0, 0};
+      // a K stage is free once the S MMAs that read it have completed: the K ring and the S
+      // buffers have the same depth, so that is the previous phase of s_full of the same index
+      uint64_t* empty = is_k ? s_full : v_empty;
+      if (is_k) {
+        const int qrow0 = ((u.b * p.Hkv + u.g) * p.N + u.k0) * p.R;
+        mbar_arrive_expect_tx(q_full, kQBytes);
+        for (int h = 0; h < 2; ++h) tma_load_2d(&map_q, q_full, sQ + h * kKSub, h * 64, qrow0);
+      }
+      int issued[kRingK] = {0, 0, 0};
+      uint32_t issued_ph[kRingK] = {0, 0, 0};
       for (int i = 0; i < u.n; ++i) {
-        const int st = i % kRing;
-        const uint32_t ph = (uint32_t)(i / kRing) & 1u;
+        const int st = i % ring;
+        const uint32_t ph = (uint32_t)(i / ring) & 1u;
         if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, kWaitLimitNs)) break;
         if (is_k) {
           mbar_arrive_expect_tx(&full[st], kKBytes);
@@ -224,54 +237,59 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
         issued[st] = 1;
         issued_ph[st] = ph;
       }
-      for (int s2 = 0; s2 < kRing; ++s2)
+      for (int s2 = 0; s2 < ring; ++s2)
         if (issued[s2]) mbar_drain_wait(&full[s2], issued_ph[s2], kWaitLimitNs / 4);
+      if (is_k) mbar_drain_wait(q_full, 0, kWaitLimitNs / 4);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      // A fixed order with blocking waits: S(0), S(1); then per tile i: O += P_i V_i once the
-      // softmax has written P_i and V_i has landed, followed at once by S(i + 2) into the
-      // buffer P_i occupied.  The tensor core performs one thread's MMAs in issue order, so
-      // S(i + 2) overwrites that buffer only after PV(i) has read it.  Each MMA costs this
-      // thread about a hundred cycles whatever its N, so S uses N = 128 keys per instruction,
-      // and one commit follows each group of MMAs (a second commit right behind the first
-      // holds this thread for a few hundred cycles more): PV(i)'s completion (v_empty) frees
-      // V stage i and tells the softmax the accumulator is up to date; S's (s_full) hands the
-      // scores to the softmax, whose first reader frees the K stage.
-      bool ok = mbar_wait(q_ready, 0, abort_flag, kWaitLimitNs);
+      // A fixed order with blocking waits: S(0), S(1), S(2); then per tile i: O += P_i V_i
+      // once the softmax has written P_i and V_i has landed, followed at once by S(i + 3) into
+      // the buffer P_i occupied.  The tensor core performs one thread's MMAs in issue order, so
+      // S(i + 3) overwrites that buffer only after PV(i) has read it; with three buffers the
+      // chain softmax(i) -> PV(i) -> S(i + 3) -> softmax(i + 3) spans the softmax of two other
+      // tiles.  The MMAs of a group are issued back to back (unrolled, descriptors formed
+      // from one base: the address field counts 16-byte units), one commit per group:
+      // PV(i)'s completion (v_empty) frees V stage i and tells the softmax the accumulator is
+      // up to date; S's (s_full) hands the scores to the softmax, whose first reader frees the
+      // K stage.
+      bool ok = mbar_wait(q_full, 0, abort_flag, kWaitLimitNs);
       tc_fence_after();
+      const uint64_t q_desc = sw128_desc(smem_u32(sQ));
       auto issue_s = [&](int s) -> bool {
-        if (!mbar_wait(&k_full[s % kRing], (uint32_t)(s / kRing) & 1u, abort_flag, kWaitLimitNs))
+        if (!mbar_wait(&k_full[s % kRingK], (uint32_t)(s / kRingK) & 1u, abort_flag, kWaitLimitNs))
           return false;
         tc_fence_after();
-        const uint32_t k_addr = smem_u32(sK + (s % kRing) * kKBytes);
+        const uint64_t k_desc = sw128_desc(smem_u32(sK + (s % kRingK) * kKBytes));
         const uint32_t s_tmem = tmem_s0 + (uint32_t)((s % kSP) * kKT);
-        // K = 16 dh per MMA: Q columns 8k .. 8k+7 (packed pairs); K sub-tile k / 4, +32 bytes
-#pragma unroll 1
-        for (int k = 0; k < kDH / 16; ++k)
-          umma_f16_ts(s_tmem, tmem_q + k * 8, sw128_desc(k_addr + (k >> 2) * kKSub + (k & 3) * 32),
-                      kIdescS, k ? 1u : 0u);
+        // K = 16 dh per MMA: Q and K sub-tile k / 4, +32 bytes inside it
+#pragma unroll
+        for (int k = 0; k < kDH / 16; ++k) {
+          const uint64_t off = (uint64_t)(((k >> 2) * kKSub + (k & 3) * 32) >> 4);
+          umma_f16_ss(s_tmem, q_desc + off, k_desc + off, kIdescS, k ? 1u : 0u);
+        }
         umma_commit(&s_full[s % kSP]);
         return true;
       };
       for (int s = 0; s < kSP && s < u.n && ok; ++s) ok = issue_s(s);
       for (int i = 0; i < u.n && ok; ++i) {
         ok = mbar_wait(&p_full[i % kSP], (uint32_t)(i / kSP) & 1u, abort_flag, kWaitLimitNs) &&
-             mbar_wait(&v_full[i % kRing], (uint32_t)(i / kRing) & 1u, abort_flag, kWaitLimitNs);
+             mbar_wait(&v_full[i % kRingV], (uint32_t)(i / kRingV) & 1u, abort_flag, kWaitLimitNs);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t v_addr = smem_u32(sV + (i % kRing) * kVBytes);
+        const uint64_t v_desc = sw128_desc(smem_u32(sV + (i % kRingV) * kVBytes));
         const uint32_t a_base = tmem_s0 + (uint32_t)((i % kSP) * kKT);
         // K = 16 keys per MMA: P of keys 16k .. 16k+15 sits at columns 64 * (k / 4) +
         // 8 * (k % 4) of the buffer (each softmax half packs its 64 keys into the first 32 of
         // its own 64 S columns); V^T sub-tile k / 4, +32 bytes per 16 keys inside it
-#pragma unroll 1
+        const uint32_t first = i == 0 ? 0u : 1u;
+#pragma unroll
         for (int k = 0; k < kKT / 16; ++k)
           umma_f16_ts(tmem_o, a_base + (k >> 2) * 64 + (k & 3) * 8,
-                      sw128_desc(v_addr + (k >> 2) * kVSub + (k & 3) * 32), kIdescPV,
-                      (i == 0 && k == 0) ? 0u : 1u);
-        umma_commit(&v_empty[i % kRing]);
+                      v_desc + (uint64_t)(((k >> 2) * kVSub + (k & 3) * 32) >> 4), kIdescPV,
+                      k == 0 ? first : 1u);
+        umma_commit(&v_empty[i % kRingV]);
         if (i + kSP < u.n) ok = issue_s(i + kSP);
       }
       umma_commit(drain);
@@ -294,26 +312,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       row_valid = a >= 0 && p.valid[(u.b * p.N + kb) * p.S + j] != 0;
       a_row = min(max(a, 0), p.L);
     }
-    // this thread's half of the query row (dh [64*half, +64), 32 packed fp16 pairs) ->
-    // tensor memory columns [32*half, +32) of Q
-    {
-      const long qrow = (long)((u.b * p.Hkv + u.g) * p.N + u.k0) * p.R + r;
-      const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + qrow * kDH + half * 64);
-      uint32_t qv[32];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint4 f = qrow < p.q_rows ? __ldg(qsrc + e) : make_uint4(0u, 0u, 0u, 0u);
-        qv[4 * e] = f.x;
-        qv[4 * e + 1] = f.y;
-        qv[4 * e + 2] = f.z;
-        qv[4 * e + 3] = f.w;
-      }
-      tmem_st_32x32b_x32(tmem_q + lane_off + half * 32, qv);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_ready);
-    }
     const uint8_t* mrow = p.mask + (size_t)u.b * p.L;
     float m_run = -INFINITY, l_run = 0.f;  // l_run: this half's share of the row sum
     bool ok = true;
@@ -335,8 +333,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       const uint32_t mword = mword_next;
       mword_next = load_mask(i + 1);
       if (!wait_all(&s_full[i % kSP], (uint32_t)(i / kSP) & 1u)) { ok = false; break; }
-      // S(i) has completed: its K stage may be refilled
-      if (warp == 2 && lane == 0) mbar_arrive(&k_empty[i % kRing]);
       tc_fence_after();
       const uint32_t s_tmem = tmem_s0 + (uint32_t)((i % kSP) * kKT + half * kHalfKT) + lane_off;
       uint32_t sv[kHalfKT];
@@ -345,11 +341,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       tmem_wait_ld();
       const bool blk_tile = i < u.nblk;
       const int c0 = blk_tile ? 0 : u.cs + (i - u.nblk) * kKT + half * kHalfKT;
-      // the tile's mask words to every lane (warp-uniform: before the per-row branches)
-      uint32_t mw_all[kHalfKT / 4];
-#pragma unroll
-      for (int w4 = 0; w4 < kHalfKT / 4; ++w4) mw_all[w4] = __shfl_sync(0xffffffffu, mword, w4);
-      // the scaled logits replace S in sv (as float bits)
+      // Readable keys keep their raw score, the others become -inf (selection); the scale
+      // 1/sqrt(dh) * log2(e) is applied later inside the exponent's FMA.
       float mh = -INFINITY;
       if (!row_valid) {
 #pragma unroll
@@ -365,40 +358,50 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
           if (vrow[jj]) bm |= 1ull << (jj + off);
 #pragma unroll
         for (int kk = 0; kk < kHalfKT; ++kk) {
-          const float v = ((bm >> kk) & 1ull) ? __uint_as_float(sv[kk]) * p.scale_log2 : -INFINITY;
+          const float v = ((bm >> kk) & 1ull) ? __uint_as_float(sv[kk]) : -INFINITY;
           sv[kk] = __float_as_uint(v);
           mh = fmaxf(mh, v);
         }
-      } else {
-        // per quarter of 16 keys: a short path when every key is readable (inside the row's
-        // prefix and the chunk, no zero byte in the mask words)
+      }
+      if (!blk_tile) {
+        // context keys c0 .. c0 + 63.  Warp-uniform test: no zero byte in the 16 mask words of
+        // this half tile (words past the chunk read as 0).  Then a row only cuts at its own
+        // prefix limit; otherwise every key is tested against its mask byte.
+        const bool word_ok = lane >= kHalfKT / 4 ||
+                             ((mword - 0x01010101u) & ~mword & 0x80808080u) == 0u;
+        const bool mask_full = __all_sync(0xffffffffu, word_ok);
+        if (mask_full) {
+          if (!row_valid) {
+          } else if (c0 + kHalfKT <= a_row) {
 #pragma unroll
-        for (int qt = 0; qt < kHalfKT / 16; ++qt) {
-          const int cq = c0 + 16 * qt;
-          bool all_ok = cq + 16 <= a_row && cq + 16 <= u.ce;
+            for (int kk = 0; kk < kHalfKT; kk += 8) {  // eight independent chains
+              float m8 = __uint_as_float(sv[kk]);
 #pragma unroll
-          for (int w4 = 4 * qt; w4 < 4 * qt + 4; ++w4)
-            all_ok = all_ok && (((mw_all[w4] - 0x01010101u) & ~mw_all[w4] & 0x80808080u) == 0u);
-          if (all_ok) {
-#pragma unroll
-            for (int kk = 16 * qt; kk < 16 * qt + 16; ++kk) {
-              const float v = __uint_as_float(sv[kk]) * p.scale_log2;
-              sv[kk] = __float_as_uint(v);
-              mh = fmaxf(mh, v);
+              for (int e = 1; e < 8; ++e) m8 = fmaxf(m8, __uint_as_float(sv[kk + e]));
+              mh = fmaxf(mh, m8);
             }
           } else {
 #pragma unroll
-            for (int w4 = 4 * qt; w4 < 4 * qt + 4; ++w4) {
-              const int c = c0 + 4 * w4;
-              const uint32_t mw = mw_all[w4];
+            for (int kk = 0; kk < kHalfKT; ++kk) {
+              const float v = c0 + kk < a_row ? __uint_as_float(sv[kk]) : -INFINITY;
+              sv[kk] = __float_as_uint(v);
+              mh = fmaxf(mh, v);
+            }
+          }
+        } else {
+          // mask word w4 from lane w4 to every lane (all lanes take part in the shuffle)
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int kk = 4 * w4 + e;
-                const bool okk = ((mw >> (8 * e)) & 0xFFu) != 0 && c + e < a_row && c + e < u.ce;
-                const float v = okk ? __uint_as_float(sv[kk]) * p.scale_log2 : -INFINITY;
-                sv[kk] = __float_as_uint(v);
-                mh = fmaxf(mh, v);
-              }
+          for (int w4 = 0; w4 < kHalfKT / 4; ++w4) {
+            const uint32_t mw = __shfl_sync(0xffffffffu, mword, w4);
+            if (!row_valid) continue;
+            const int c = c0 + 4 * w4;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int kk = 4 * w4 + e;
+              const bool okk = ((mw >> (8 * e)) & 0xFFu) != 0 && c + e < a_row && c + e < u.ce;
+              const float v = okk ? __uint_as_float(sv[kk]) : -INFINITY;
+              sv[kk] = __float_as_uint(v);
+              mh = fmaxf(mh, v);
             }
           }
         }
@@ -407,9 +410,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       float* xm = red_max + (i & 1) * 256;
       xm[half * 128 + r] = mh;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&max_bar[i & 1]);
-      if (!wait_all(&max_bar[i & 1], (uint32_t)(i >> 1) & 1u)) { ok = false; break; }
-      const float mt = fmaxf(mh, xm[(1 - half) * 128 + r]);
+      if (lane == 0) mbar_arrive(&max_bar[quarter * 2 + (i & 1)]);
+      if (!wait_all(&max_bar[quarter * 2 + (i & 1)], (uint32_t)(i >> 1) & 1u)) { ok = false; break; }
+      const float mt = fmaxf(mh, xm[(1 - half) * 128 + r]) * p.scale_log2;  // -inf stays
       // running maximum: taken as is the first time a row sees a key, otherwise kept
       // unless the tile's maximum exceeds it by more than 2^8 (then the accumulator and
       // the row sum are rescaled)
@@ -426,7 +429,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       // P = 2^(x - m): an excluded key (x = -inf) gives exactly +0; a row that has not seen
       // a readable key yet (m_run = -inf) has only excluded keys here.  Packed as fp16 pairs
       // into the first 32 of this half's 64 S columns.
-      float lsum = 0.f;
+      // four partial row sums (independent addition chains)
+      float lsum4[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pw[kHalfKT / 2];
       if (m_run == -INFINITY) {
 #pragma unroll
@@ -434,21 +438,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       } else {
 #pragma unroll
         for (int kk = 0; kk < kHalfKT / 2; ++kk) {
-          const float p0 = ex2_approx(__uint_as_float(sv[2 * kk]) - m_run);
-          const float p1 = ex2_approx(__uint_as_float(sv[2 * kk + 1]) - m_run);
-          lsum += p0 + p1;
+          const float x0 = fmaf(__uint_as_float(sv[2 * kk]), p.scale_log2, -m_run);
+          const float x1 = fmaf(__uint_as_float(sv[2 * kk + 1]), p.scale_log2, -m_run);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          lsum4[kk & 3] += p0 + p1;
           const __half2 h2 = __floats2half2_rn(p0, p1);
           pw[kk] = *reinterpret_cast<const uint32_t*>(&h2);
         }
       }
-      l_run += lsum;
+      l_run += (lsum4[0] + lsum4[1]) + (lsum4[2] + lsum4[3]);
       tmem_st_32x32b_x32(s_tmem, pw);
       // the accumulator is rescaled before PV(i) (released below) adds to it; PV(i - 1)
       // must have landed first (a finite m_run means there was an earlier tile; its
       // completion is the phase of v_empty that frees its V stage).  This half rescales O
       // columns [64*half, 64*half + 64).
       if (__any_sync(0xffffffffu, factor != 1.f)) {
-        if (!wait_all(&v_empty[(i - 1) % kRing], (uint32_t)((i - 1) / kRing) & 1u)) { ok = false; break; }
+        if (!wait_all(&v_empty[(i - 1) % kRingV], (uint32_t)((i - 1) / kRingV) & 1u)) { ok = false; break; }
         tc_fence_after();
         for (int part = 0; part < 2; ++part) {
           uint32_t ov[32];
@@ -464,8 +470,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       // V^T row r of key sub-tile `half`) so that whatever the cache holds there cannot
       // meet a zero P as NaN
       if (!blk_tile && u.cs + (i - u.nblk) * kKT + kKT > u.a_max) {
-        const int st = i % kRing;
-        if (!wait_all(&v_full[st], (uint32_t)(i / kRing) & 1u)) { ok = false; break; }
+        const int st = i % kRingV;
+        if (!wait_all(&v_full[st], (uint32_t)(i / kRingV) & 1u)) { ok = false; break; }
         const int nvalid = u.a_max - (u.cs + (i - u.nblk) * kKT) - half * kHalfKT;
         // row r of a swizzled [128][64] fp16 sub-tile: 16-byte chunk c (keys 8c .. 8c+7)
         // sits at chunk position c ^ (r % 8)
@@ -498,8 +504,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       tc_fence_after();
       red_sum[half * 128 + r] = l_run;
       __syncwarp();
-      if (lane == 0) mbar_arrive(sum_bar);
-      const bool sum_ok = wait_all(sum_bar, 0);
+      if (lane == 0) mbar_arrive(&sum_bar[quarter]);
+      const bool sum_ok = wait_all(&sum_bar[quarter], 0);
       const float l = l_run + red_sum[(1 - half) * 128 + r];
       // invalid slots of an existing block get exact zeros (the O projection reads them)
       const float inv = sum_ok && row_valid && l > 0.f ? 1.f / l : 0.f;
@@ -531,8 +537,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap map_kc, const __grid_constant
       }
       red_sum[half * 128 + r] = l_run;
       __syncwarp();
-      if (lane == 0) mbar_arrive(sum_bar);
-      if (wait_all(sum_bar, 0) && half == 0) {
+      if (lane == 0) mbar_arrive(&sum_bar[quarter]);
+      if (wait_all(&sum_bar[quarter], 0) && half == 0) {
         p.part_m[rowi] = m_run;
         p.part_l[rowi] = l_run + red_sum[128 + r];
       }
@@ -699,7 +705,7 @@ cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream) {
   p.Hq = a.Hq;
   p.out = a.out;
 
-  CUtensorMap mkc, mvc, mkb, mvb;
+  CUtensorMap mkc, mvc, mkb, mvb, mq;
   const long planes = (long)a.B * 2 * a.Hkv;
   {
     cuuint64_t dims[3] = {(cuuint64_t)kDH, (cuuint64_t)a.L, (cuuint64_t)planes};
@@ -726,6 +732,13 @@ cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream) {
     cuuint32_t box[2] = {64, (cuuint32_t)kDH};  // [128 dh][64 keys]
     if (!encode_f16(&mvb, a.vbt, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
+  {
+    // Q rows [B][Hkv][N][R] x dh; rows past the end read the zero fill
+    cuuint64_t dims[2] = {(cuuint64_t)kDH, (cuuint64_t)p.q_rows};
+    cuuint64_t str[1] = {(cuuint64_t)kDH * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kM};
+    if (!encode_f16(&mq, a.q, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -735,7 +748,7 @@ cudaError_t launch_attention_tc(const AttnTcArgs& a, cudaStream_t stream) {
   }
   {
     const cudaError_t le = launch_pdl(attn_tc_kernel, dim3((unsigned)lay.units), dim3(kThreads),
-        kSmemBytes, stream, mkc, mvc, mkb, mvb, p);
+        kSmemBytes, stream, mkc, mvc, mkb, mvb, mq, p);
     if (le != cudaSuccess) return le;
   }
   cudaError_t e = cudaGetLastError();

@@ -542,18 +542,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], ph, abort_flag, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * kStageABytes);
-          const uint32_t b_addr = smem_u32(sB + stage * R::kStageB);
+          const uint64_t a_desc = sw128_desc(smem_u32(sA + stage * kStageABytes));
+          const uint64_t b_desc = sw128_desc(smem_u32(sB + stage * R::kStageB));
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            // advancing K by 16 elements = 32 bytes inside the 128-byte swizzle atom
+            // advancing K by 16 elements = 32 bytes inside the 128-byte swizzle atom (the
+            // descriptor's address field counts 16-byte units)
             const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
             if constexpr (kPair)
-              umma_16bit_pair(d_tmem, sw128_desc(a_addr + k * 32), sw128_desc(b_addr + k * 32),
-                              p.idesc_pair, accum);
+              umma_16bit_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, p.idesc_pair, accum);
             else
-              umma_16bit(d_tmem, sw128_desc(a_addr + k * 32), sw128_desc(b_addr + k * 32),
-                         p.idesc, accum);
+              umma_16bit(d_tmem, a_desc + 2 * k, b_desc + 2 * k, p.idesc, accum);
           }
           if constexpr (kPair) umma_commit_pair_multicast(&empty[stage], 3);  // both CTAs' stage
           else umma_commit(&empty[stage]);
