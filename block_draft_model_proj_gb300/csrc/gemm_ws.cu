@@ -60,6 +60,7 @@ constexpr uint32_t kEpiBufFloats = 32 * 36;             // per epilogue warp: [3
 constexpr size_t kSmemBytes = 1024 + kRingBytes + 512 + 4 * kEpiBufFloats * sizeof(float);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 static_assert(kMaxStages % 2 == 0, "the converter groups need an even weight-stage count");
+static_assert(kMaxStages <= kASlots, "a token stage is released through the K-step barriers");
 
 struct WsParams {
   long M;            // token rows of X (and C)
@@ -320,9 +321,10 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
   uint64_t* wfull = bars;                   // weight tile landed
   uint64_t* wempty = wfull + kMaxStages;    // converters done reading it
   uint64_t* xfull = wempty + kMaxStages;    // token tiles landed
-  uint64_t* xempty = xfull + kMaxStages;    // MMA done with them
-  uint64_t* afull = xempty + kMaxStages;    // [8] converted A in tensor memory
-  uint64_t* aempty = afull + kASlots;       // [8] MMA done with the A slot
+  uint64_t* afull = xfull + kMaxStages;     // [8] converted A in tensor memory
+  // [8] the MMAs of K-step i (counted over the CTA's whole schedule) are done: A slot i % 8
+  // and token stage i % SX are free again (one commit per K-step serves both)
+  uint64_t* aempty = afull + kASlots;
   uint64_t* tfull = aempty + kASlots;       // accumulator ready
   uint64_t* tempty = tfull + 1;             // accumulator drained
   uint64_t* drain = tempty + 1;
@@ -338,7 +340,6 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
     }
     for (int s = 0; s < SX; ++s) {
       mbar_init(&xfull[s], 1);
-      mbar_init(&xempty[s], 1);
     }
     for (int a = 0; a < kASlots; ++a) {
       mbar_init(&afull[a], 4);
@@ -372,7 +373,6 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
       const bool is_w = lane == 0;
       const int S = is_w ? SW : SX;
       uint64_t* full = is_w ? wfull : xfull;
-      uint64_t* empty = is_w ? wempty : xempty;
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -383,7 +383,14 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         // a missing second tile is read past the last row: zeros, never stored
         const int t1row = (x.t1 >= 0 ? x.t1 : p.m_tiles) * kTT;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
+          // weight stage: the converters of its previous use are done; token stage: the MMAs
+          // of K-step n_issued - SX are done (phase (n_issued - SX) / 8 of aempty)
+          const bool freed =
+              is_w ? mbar_wait(&wempty[stage], ph ^ 1u, abort_flag, kWaitLimitNs)
+                   : (n_issued < S ||
+                      mbar_wait(&aempty[(n_issued - S) % kASlots],
+                                (uint32_t)(((n_issued - S) / kASlots) & 1), abort_flag, kWaitLimitNs));
+          if (!freed) { ok = false; break; }
           if (is_w) {
             mbar_arrive_expect_tx(&full[stage], kWBytes);
             uint8_t* dst = wring + (size_t)stage * kWBytes;
@@ -438,7 +445,6 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
           for (int k = 0; k < kBK / 16; ++k)
             umma_f16_ts(d_tmem, a_tmem + k * 8, sw128_desc(x_addr + k * 32), idesc,
                         (kb > kb0 || k > 0) ? 1u : 0u);
-          umma_commit(&xempty[stage]);
           umma_commit(&aempty[slot]);
           if (++stage == SX) { stage = 0; ph ^= 1u; }
         }
