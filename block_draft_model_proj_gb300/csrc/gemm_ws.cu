@@ -9,13 +9,14 @@
 // to a few thousand tokens against 4096 x 4096 .. 24576 x 4096 weights.
 //
 //  * The weights arrive as bf16 (the model's own) or fp16 and are read from global memory
-//    exactly as given: TMA brings a 128 x 64 tile into shared memory, four converter warps
+//    exactly as given: TMA brings a 128 x 128 tile (two 64-column boxes) into shared
+//    memory, four converter warps
 //    turn it into fp16 (round to nearest even; exact for bf16 values of magnitude in
 //    [2^-14, 65504]) and store it into tensor memory, where the MMA reads its A operand
 //    (tcgen05.mma ... kind::f16 with A in tensor memory).  No converted copy of the
 //    weights ever exists in global memory.
 //  * The activations X are fp16 (their 11 significant bits keep the body within its error
-//    bound); TMA loads 128 x 64 tiles of the active token tiles only, two per unit, and the
+//    bound); TMA loads 128 x 128 tiles of the active token tiles only, two per unit, and the
 //    MMA's N covers only the rows present (16 for a 16-token decode step).
 //  * K is cut into `splits` slices when the (weight tile, token tile) units alone would
 //    leave SMs idle.  The count is chosen on the device from the number of active token
@@ -28,8 +29,9 @@
 // weight ring, lane 1 the token ring); warp 1 MMA issuer; warps 2-9 converters in two
 // groups of four that take alternate K-steps; warps 10-13 epilogue.  Shared memory holds
 // two rings: weight tiles, freed as soon as the converters have read them, and token tiles,
-// freed by the MMA.  Tensor memory holds one 256-column accumulator and an 8-slot ring of
-// converted A tiles (32 columns each), so the conversion runs ahead of the MMA and the
+// freed by the MMA.  A K-step is 128 wide (eight MMAs per barrier wait and per commit).
+// Tensor memory holds one 256-column accumulator and a 4-slot ring of converted A tiles (64
+// columns each), so the conversion runs ahead of the MMA and the
 // weight tiles' load-and-convert latency stays off the token ring.  The converters and the
 // producers run ahead into the next unit while the epilogue drains.
 // Every mbarrier wait is bounded
@@ -48,19 +50,23 @@ using namespace tc;
 
 constexpr int kWM = 128;   // weight rows per unit (MMA M)
 constexpr int kTT = 128;   // rows of a token tile; a unit takes two (MMA N <= 256)
-constexpr int kBK = 64;    // K per stage
-constexpr int kMaxStages = 8;   // per ring
-constexpr int kASlots = 8;  // converted A tiles in tensor memory
+constexpr int kBK = 128;   // K per stage: two boxes of 64 (a 128-byte swizzled row each)
+constexpr int kBox = 64;   // K of one TMA box
+constexpr int kMaxWStages = 6;  // weight ring
+constexpr int kMaxXStages = 4;  // token ring
+constexpr int kASlots = 4;  // converted A tiles in tensor memory (64 columns each)
 constexpr int kThreads = 448;
-constexpr uint32_t kWBytes = 128 * kBK * 2;             // 16 KB weight tile
+constexpr uint32_t kWSub = 128 * kBox * 2;              // 16 KB: 128 weight rows x 64 K
+constexpr uint32_t kWBytes = 2 * kWSub;                 // 32 KB weight stage
 constexpr uint32_t kRingBytes = 196 * 1024;             // shared-memory ring budget
-constexpr uint32_t kTmemCols = 512;                     // acc 256, A ring 8 x 32
+constexpr uint32_t kTmemCols = 512;                     // acc 256, A ring 4 x 64
 constexpr uint32_t kTmemAcc = 0, kTmemA = 256;
 constexpr uint32_t kEpiBufFloats = 32 * 36;             // per epilogue warp: [32][32 + 4]
 constexpr size_t kSmemBytes = 1024 + kRingBytes + 512 + 4 * kEpiBufFloats * sizeof(float);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-static_assert(kMaxStages % 2 == 0, "the converter groups need an even weight-stage count");
-static_assert(kMaxStages <= kASlots, "a token stage is released through the K-step barriers");
+static_assert(kMaxWStages % 2 == 0, "the converter groups need an even weight-stage count");
+static_assert(kMaxXStages <= kASlots, "a token stage is released through the K-step barriers");
+static_assert(kTmemA + kASlots * 64 <= kTmemCols, "tensor memory");
 
 struct WsParams {
   long M;            // token rows of X (and C)
@@ -74,7 +80,7 @@ struct WsParams {
   const int32_t* tile_list;  // optional: [0] = count, [1..] = active token tiles
   int xrows;                 // rows of a token-tile load (128, or M rounded up to 16)
   int two_tiles;             // units take two token tiles (M > 128)
-  int w_stages;              // weight ring stages (16 KB each)
+  int w_stages;              // weight ring stages (32 KB each)
   int x_stages;              // token ring stages
   uint32_t x_stage_bytes;    // token tile(s) of one K-step
   int* splits_out;           // optional: the split count chosen on the device
@@ -319,10 +325,10 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
   uint8_t* xring = smem + (size_t)SW * kWBytes;           // SX x x_stage_bytes
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes);
   uint64_t* wfull = bars;                   // weight tile landed
-  uint64_t* wempty = wfull + kMaxStages;    // converters done reading it
-  uint64_t* xfull = wempty + kMaxStages;    // token tiles landed
-  uint64_t* afull = xfull + kMaxStages;     // [8] converted A in tensor memory
-  // [8] the MMAs of K-step i (counted over the CTA's whole schedule) are done: A slot i % 8
+  uint64_t* wempty = wfull + kMaxWStages;   // converters done reading it
+  uint64_t* xfull = wempty + kMaxWStages;   // token tiles landed
+  uint64_t* afull = xfull + kMaxXStages;    // [4] converted A in tensor memory
+  // [4] the MMAs of K-step i (counted over the CTA's whole schedule) are done: A slot i % 4
   // and token stage i % SX are free again (one commit per K-step serves both)
   uint64_t* aempty = afull + kASlots;
   uint64_t* tfull = aempty + kASlots;       // accumulator ready
@@ -365,7 +371,10 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
 
   const Sched sc = schedule(p);
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.splits_out) *p.splits_out = sc.splits;
-  const uint32_t xtile_bytes = (uint32_t)p.xrows * kBK * 2;
+  // a token stage: for each of the two K boxes, the unit's token tiles one after the other
+  // (one K-major operand of up to 256 rows per box)
+  const uint32_t xtile_bytes = (uint32_t)p.xrows * kBox * 2;
+  const uint32_t xsub_bytes = p.x_stage_bytes / 2;
 
   if (warp == 0) {
     if (lane < 2) {
@@ -393,19 +402,24 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
           if (!freed) { ok = false; break; }
           if (is_w) {
             mbar_arrive_expect_tx(&full[stage], kWBytes);
-            uint8_t* dst = wring + (size_t)stage * kWBytes;
-            if (p.epi == kEpiSwiGLU) {  // 64 gate rows, then the 64 up rows of the same channels
-              tma_load_2d(&map_w, &full[stage], dst, kb * kBK, x.wt * 64);
-              tma_load_2d(&map_w, &full[stage], dst + kWBytes / 2, kb * kBK,
-                          p.swiglu_I + x.wt * 64);
-            } else {
-              tma_load_2d(&map_w, &full[stage], dst, kb * kBK, x.wt * kWM);
+            for (int h = 0; h < 2; ++h) {
+              uint8_t* dst = wring + (size_t)stage * kWBytes + h * kWSub;
+              const int k0 = kb * kBK + h * kBox;
+              if (p.epi == kEpiSwiGLU) {  // 64 gate rows, then the 64 up rows of the same channels
+                tma_load_2d(&map_w, &full[stage], dst, k0, x.wt * 64);
+                tma_load_2d(&map_w, &full[stage], dst + kWSub / 2, k0, p.swiglu_I + x.wt * 64);
+              } else {
+                tma_load_2d(&map_w, &full[stage], dst, k0, x.wt * kWM);
+              }
             }
           } else {
             mbar_arrive_expect_tx(&full[stage], p.x_stage_bytes);
-            uint8_t* dst = xring + (size_t)stage * p.x_stage_bytes;
-            tma_load_2d(&map_x, &full[stage], dst, kb * kBK, x.t0 * kTT);
-            if (p.two_tiles) tma_load_2d(&map_x, &full[stage], dst + xtile_bytes, kb * kBK, t1row);
+            for (int h = 0; h < 2; ++h) {
+              uint8_t* dst = xring + (size_t)stage * p.x_stage_bytes + h * xsub_bytes;
+              const int k0 = kb * kBK + h * kBox;
+              tma_load_2d(&map_x, &full[stage], dst, k0, x.t0 * kTT);
+              if (p.two_tiles) tma_load_2d(&map_x, &full[stage], dst + xtile_bytes, k0, t1row);
+            }
           }
           ++n_issued;
           if (++stage == S) { stage = 0; ph ^= 1u; }
@@ -438,13 +452,15 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
             break;
           }
           tc_fence_after();
-          const uint32_t a_tmem = tmem + kTmemA + (uint32_t)(slot * 32);
-          // the token tiles of a stage are consecutive: one K-major operand of 256 rows
-          const uint32_t x_addr = smem_u32(xring + (size_t)stage * p.x_stage_bytes);
+          const uint32_t a_tmem = tmem + kTmemA + (uint32_t)(slot * 64);
+          // K = 16 per MMA: A columns 8k .. 8k+7 (packed pairs); token box k / 4, +32 bytes
+          // inside it (the descriptor's address field counts 16-byte units)
+          const uint64_t x_desc = sw128_desc(smem_u32(xring + (size_t)stage * p.x_stage_bytes));
+          const uint64_t x_sub = xsub_bytes >> 4;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            umma_f16_ts(d_tmem, a_tmem + k * 8, sw128_desc(x_addr + k * 32), idesc,
-                        (kb > kb0 || k > 0) ? 1u : 0u);
+            umma_f16_ts(d_tmem, a_tmem + k * 8, x_desc + (k >> 2) * x_sub + (uint64_t)((k & 3) * 2),
+                        idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           umma_commit(&aempty[slot]);
           if (++stage == SX) { stage = 0; ph ^= 1u; }
         }
@@ -482,21 +498,28 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
                                    kWaitLimitNs);
         if (!__all_sync(0xffffffffu, got ? 1 : 0)) { ok = false; break; }
         tc_fence_after();
-        // row srow of the 128-byte-swizzled tile: 16-byte chunk c at chunk position c ^ (row % 8)
-        const uint8_t* row = wring + (size_t)stage * kWBytes + (srow >> 3) * 1024 + (srow & 7) * 128;
-        uint32_t a[32];
+        // row srow of each 128-byte-swizzled 64-K box: 16-byte chunk c at chunk position
+        // c ^ (row % 8); box h lands in A columns [32h, 32h + 32) of the slot
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          const uint8_t* row = wring + (size_t)stage * kWBytes + h * kWSub + (srow >> 3) * 1024 +
+                               (srow & 7) * 128;
+          uint32_t a[32];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 w = *reinterpret_cast<const uint4*>(row + ((c ^ (srow & 7)) * 16));
-          a[4 * c] = cvt_pair(w.x, wbf16, mag);
-          a[4 * c + 1] = cvt_pair(w.y, wbf16, mag);
-          a[4 * c + 2] = cvt_pair(w.z, wbf16, mag);
-          a[4 * c + 3] = cvt_pair(w.w, wbf16, mag);
+          for (int c = 0; c < 8; ++c) {
+            const uint4 w = *reinterpret_cast<const uint4*>(row + ((c ^ (srow & 7)) * 16));
+            a[4 * c] = cvt_pair(w.x, wbf16, mag);
+            a[4 * c + 1] = cvt_pair(w.y, wbf16, mag);
+            a[4 * c + 2] = cvt_pair(w.z, wbf16, mag);
+            a[4 * c + 3] = cvt_pair(w.w, wbf16, mag);
+          }
+          if (h == 1) {
+            // the weight stage is in registers: hand it back before the last tensor-memory store
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&wempty[stage]);
+          }
+          tmem_st_32x32b_x32(tmem + kTmemA + (uint32_t)(slot * 64 + h * 32) + lane_off, a);
         }
-        // the weight tile is in registers: hand the stage back before the tensor-memory store
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&wempty[stage]);
-        tmem_st_32x32b_x32(tmem + kTmemA + (uint32_t)(slot * 32) + lane_off, a);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -572,7 +595,7 @@ bool encode_rows(CUtensorMap* map, const void* base, long rows, int cols, long l
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)kBox, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -613,9 +636,10 @@ cudaError_t launch(const WsArgs& a, int epi, int w_tiles, int interleave, const 
   p.xrows = xrows;
   p.two_tiles = a.M > kTT ? 1 : 0;
   p.x_stage_bytes = (uint32_t)(p.two_tiles ? 2 : 1) * xrows * kBK * 2;
-  p.x_stages = p.x_stage_bytes <= 4096 ? kMaxStages : 4;
+  // tokens: 4 stages when they are small (decode), else 2; the weights take the rest
+  p.x_stages = p.x_stage_bytes <= 16384 ? kMaxXStages : 2;
   p.w_stages = (int)((kRingBytes - (uint32_t)p.x_stages * p.x_stage_bytes) / kWBytes);
-  if (p.w_stages > kMaxStages) p.w_stages = kMaxStages;
+  if (p.w_stages > kMaxWStages) p.w_stages = kMaxWStages;
   // the two converter groups take alternate K-steps: with an even stage count every stage
   // stays with one group (step i and step i + w_stages have the same parity), so a group can
   // never mistake the other group's phase of a stage for its own
