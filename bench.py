@@ -6,8 +6,8 @@ The headline workload is the largest single-GPU training configuration (B=16, L=
 32 anchors of 16 slots per row, W_proj 20480->4096, 5 draft layers of the Qwen3-8B shape,
 four row pairs sharing sample ids), with greedy verification of every drafted block against
 synthetic target logits [B*N, 16, 151936].  The same JSON line carries the B=4 L=2048
-training step, the decode steps at batch 1 and 64 over a cached 4096-position context, and
-verification alone on [32|64, 16, 151936].
+training step, the long-context step (B=1 L=32768, 64 anchors), the decode steps at batch 1
+and 64 over a cached 4096-position context, and verification alone on [32|64, 16, 151936].
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--headline-only] [--no-cpu-baseline]
@@ -590,7 +590,8 @@ def verify_alone(args, device, Bv: int) -> dict:
             "l2": "logits larger than L2, read once per call"}
 
 
-SECONDARY = ("train_8b_b4_l2048", "decode_8b_b1_ctx4096", "decode_8b_b64_ctx4096")
+SECONDARY = ("train_8b_b4_l2048", "longctx_8b_l32768", "decode_8b_b1_ctx4096",
+             "decode_8b_b64_ctx4096")
 
 
 def run_ours(args, rank, world, local_rank):
