@@ -116,6 +116,32 @@ int num_sms() {
   return cached[dev];
 }
 
+// A side stream of the calling host thread on the current device, with the events that fork
+// work onto it and join it back (per thread, so concurrent callers never share events).
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr;
+  cudaEvent_t done[2] = {nullptr, nullptr};
+};
+
+cudaError_t side_stream(SideStream** out) {
+  thread_local SideStream per_dev[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  SideStream& ss = per_dev[dev];
+  if (!ss.s) {
+    if ((e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    for (int i = 0; i < 2; ++i)
+      if ((e = cudaEventCreateWithFlags(&ss.done[i], cudaEventDisableTiming)) != cudaSuccess)
+        return e;
+  }
+  *out = &ss;
+  return cudaSuccess;
+}
+
 // ---- workspace carving -----------------------------------------------------------------
 struct Carver {
   uint8_t* base;
@@ -419,7 +445,9 @@ struct BodyLayout {
   float* sin_t;
   bool ws;              // layer projections on the weight-streaming GEMM (few tokens)
   int* nsplit;          // weight-streaming GEMM: K-splits chosen on the device (QKV, O, down)
-  __half* wl16;         // one layer's four matrices as fp16 (converted in the call), or null
+  __half* wl16;         // fp16 copies of the layer matrices converted in the call, or null:
+                        // two layers' buffers (layer l in buffer l % 2) when NL > 1
+  size_t wl16_layer;    // elements of one layer's four matrices
   int sp_qkv, sp_o, sp_gu, sp_down;  // host K-splits, or the device upper bounds
   // 128 x 256 GEMM without a K-split: Q/K RoPE and the attention layouts in the QKV
   // epilogue, the residual add in the O and down epilogues
@@ -495,9 +523,10 @@ BodyLayout body_layout(const dflash_config_t* c, int B, int L, int N, void* ws) 
   b.cos_t = cv.take<float>((size_t)b.P * (c->head_dim / 2));
   b.sin_t = cv.take<float>((size_t)b.P * (c->head_dim / 2));
   b.nsplit = cv.take<int>(4);
-  b.wl16 = convert_layers(c, T) ? cv.take<__half>((size_t)qkvw * D + (size_t)D * qw +
-                                                  (size_t)2 * I * D + (size_t)D * I)
-                                : nullptr;
+  b.wl16_layer = (size_t)qkvw * D + (size_t)D * qw + (size_t)2 * I * D + (size_t)D * I;
+  b.wl16 = convert_layers(c, T)
+               ? cv.take<__half>(b.wl16_layer * (c->num_layers > 1 ? 2 : 1))
+               : nullptr;
   b.bytes = cv.off;
   return b;
 }
@@ -711,18 +740,41 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
     return a;
   };
   const bool use_ws = lay.ws;
+  // fp16 copies of the layer matrices (exact for bf16 values in the fp16 range) are made on
+  // a side stream, one layer ahead: the conversion (HBM-bound) of layer l + 1 runs beside
+  // layer l's tensor-core work, into the buffer layer l - 1 used.
+  const size_t sizes[4] = {(size_t)qkvw * D, (size_t)D * qw, (size_t)2 * I * D, (size_t)D * I};
+  SideStream* side = nullptr;
+  auto convert_layer = [&](int l) -> int {
+    // after everything already on the caller's stream (layer l - 2's use of this buffer)
+    DF_CUDA(cudaEventRecord(side->fork, s));
+    DF_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
+    const dflash_layer_weights_t& src = w->layers[l];
+    const void* mats[4] = {src.w_qkv, src.w_o, src.w_gate_up, src.w_down};
+    __half* dst = lay.wl16 + (size_t)(l % 2) * lay.wl16_layer;
+    Prof pc(DFLASH_PROF_CONVERT, 4, side->s);
+    for (int m = 0; m < 4; ++m) {
+      DF_CUDA(launch_convert_bf16_f16(mats[m], dst, sizes[m], st, side->s));
+      dst += sizes[m];
+    }
+    DF_CUDA(cudaEventRecord(side->done[l % 2], side->s));
+    return DFLASH_OK;
+  };
+  if (lay.wl16) {
+    DF_CUDA(side_stream(&side));
+    if ((r = convert_layer(0)) != DFLASH_OK) return r;
+  }
   for (int l = 0; l < cfg->num_layers; ++l) {
     dflash_layer_weights_t lw = w->layers[l];
     if (lay.wl16) {
-      // fp16 copies of this layer's matrices (exact for bf16 values in the fp16 range)
-      __half* dst = lay.wl16;
+      // this layer's fp16 matrices are ready; then the next layer's conversion starts
+      DF_CUDA(cudaStreamWaitEvent(s, side->done[l % 2], 0));
+      if (l + 1 < cfg->num_layers && (r = convert_layer(l + 1)) != DFLASH_OK) return r;
+      __half* buf = lay.wl16 + (size_t)(l % 2) * lay.wl16_layer;
       const void** mats[4] = {&lw.w_qkv, &lw.w_o, &lw.w_gate_up, &lw.w_down};
-      const size_t sizes[4] = {(size_t)qkvw * D, (size_t)D * qw, (size_t)2 * I * D, (size_t)D * I};
-      Prof pc(DFLASH_PROF_CONVERT, 4, s);
       for (int m = 0; m < 4; ++m) {
-        DF_CUDA(launch_convert_bf16_f16(*mats[m], dst, sizes[m], st, s));
-        *mats[m] = dst;
-        dst += sizes[m];
+        *mats[m] = buf;
+        buf += sizes[m];
       }
     }
     if (lay.fuse_qkv) {
