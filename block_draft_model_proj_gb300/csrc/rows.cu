@@ -136,9 +136,7 @@ __device__ __forceinline__ float4 sum_splits4(const float* y, int nsplit, long s
 }
 
 // Vectorised residual step: one CTA per row, each thread owns kV float4 groups of the row
-// (D % 4 == 0, D <= 4 * kV * blockDim.x), a single pass over global memory.  Every load of
-// the row -- its validity flag, the residual / embedding, the partial sums and the gains --
-// is issued before the first one is used (an invalid row's values are loaded and dropped).
+// (D % 4 == 0, D <= 4 * kV * blockDim.x), a single pass over global memory.
 template <int kV>
 __global__ void residual_norm_vec_kernel(int mode, int dt, float* __restrict__ x,
                                          const void* __restrict__ emb, const float* __restrict__ y,
@@ -151,36 +149,9 @@ __global__ void residual_norm_vec_kernel(int mode, int dt, float* __restrict__ x
   __shared__ float red[33];
   const long r = blockIdx.x;
   const int D4 = D / 4;
-  const bool row_ok = !valid || valid[r] != 0;
   if (nsplit_dev) nsplit = *nsplit_dev;
-  float4 v[kV], gg[kV];
-#pragma unroll
-  for (int k = 0; k < kV; ++k) {
-    const int q = threadIdx.x + k * blockDim.x;
-    v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    gg[k] = v[k];
-    if (q >= D4) continue;
-    const long idx = r * D + 4L * q;
-    v[k] = mode == kNormInit ? load4(emb, dt, idx) : *reinterpret_cast<const float4*>(x + idx);
-    gg[k] = load4(g, dt, 4L * q);
-  }
-  if (mode != kNormInit && nsplit > 0) {
-#pragma unroll
-    for (int k = 0; k < kV; ++k) {
-      const int q = threadIdx.x + k * blockDim.x;
-      if (q >= D4) continue;
-      const float4 a = sum_splits4(y, nsplit, split_stride, r * D + 4L * q);
-      v[k].x += a.x;
-      v[k].y += a.y;
-      v[k].z += a.z;
-      v[k].w += a.w;
-    }
-  }
-  if (!row_ok) {  // an invalid slot: zero output / zero GEMM input; x is left as it was
-#pragma unroll
-    for (int k = 0; k < kV; ++k) {
-      const int q = threadIdx.x + k * blockDim.x;
-      if (q >= D4) continue;
+  if (valid && valid[r] == 0) {  // an invalid slot: zero output / zero GEMM input, y unread
+    for (int q = threadIdx.x; q < D4; q += blockDim.x) {
       if (mode == kNormFinal)
         *reinterpret_cast<float4*>(out + r * D + 4L * q) = make_float4(0.f, 0.f, 0.f, 0.f);
       else
@@ -188,29 +159,49 @@ __global__ void residual_norm_vec_kernel(int mode, int dt, float* __restrict__ x
     }
     return;
   }
+  float4 v[kV];
   float ss = 0.f;
 #pragma unroll
   for (int k = 0; k < kV; ++k) {
     const int q = threadIdx.x + k * blockDim.x;
-    if (q >= D4) continue;
+    if (q >= D4) { v[k] = make_float4(0.f, 0.f, 0.f, 0.f); continue; }
+    const long idx = r * D + 4L * q;
+    float4 t;
+    if (mode == kNormInit) {
+      t = load4(emb, dt, idx);
+    } else {
+      t = *reinterpret_cast<const float4*>(x + idx);
+      const float4 a = sum_splits4(y, nsplit, split_stride, idx);
+      t.x += a.x;
+      t.y += a.y;
+      t.z += a.z;
+      t.w += a.w;
+    }
     // nsplit 0: x already holds the sum (added by the GEMM epilogue), nothing to write back
-    if (mode == kNormInit || nsplit > 0)
-      *reinterpret_cast<float4*>(x + r * D + 4L * q) = v[k];
-    ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+    if (mode == kNormInit || nsplit > 0) *reinterpret_cast<float4*>(x + idx) = t;
+    v[k] = t;
+    ss += t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w;
   }
   ss = block_sum(ss, red);
   const float rstd = rsqrtf(ss / (float)D + eps);
+  const bool ok = mode != kNormFinal || valid[r] != 0;
 #pragma unroll
   for (int k = 0; k < kV; ++k) {
     const int q = threadIdx.x + k * blockDim.x;
     if (q >= D4) continue;
     const long idx = r * D + 4L * q;
-    const float4 o = make_float4(v[k].x * rstd * gg[k].x, v[k].y * rstd * gg[k].y,
-                                 v[k].z * rstd * gg[k].z, v[k].w * rstd * gg[k].w);
-    if (mode == kNormFinal)
-      *reinterpret_cast<float4*>(out + idx) = final_norm ? o : v[k];
-    else
-      h.store4(idx, o);
+    const float4 gg = load4(g, dt, 4L * q);
+    if (mode == kNormFinal) {
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ok)
+        o = final_norm ? make_float4(v[k].x * rstd * gg.x, v[k].y * rstd * gg.y,
+                                     v[k].z * rstd * gg.z, v[k].w * rstd * gg.w)
+                       : v[k];
+      *reinterpret_cast<float4*>(out + idx) = o;
+    } else {
+      h.store4(idx, make_float4(v[k].x * rstd * gg.x, v[k].y * rstd * gg.y, v[k].z * rstd * gg.z,
+                                v[k].w * rstd * gg.w));
+    }
   }
 }
 
@@ -223,23 +214,18 @@ __global__ void rows_norm_vec_kernel(int dt, const float* __restrict__ y, int ns
   pdl_trigger();
   __shared__ float red[33];
   const long r = blockIdx.x;
+  // context rows no block reads (c >= ctx_len[b]) are left unwritten
+  if (ctx_len && (int)(r % L) >= ctx_len[r / L]) return;
   const int D4 = D / 4;
-  // every load first (the row, its gains, its context length); context rows no block reads
-  // (c >= ctx_len[b]) are then left unwritten
-  const bool skip = ctx_len && (int)(r % L) >= ctx_len[r / L];
-  float4 v[kV], gg[kV];
+  float4 v[kV];
+  float ss = 0.f;
 #pragma unroll
   for (int k = 0; k < kV; ++k) {
     const int q = threadIdx.x + k * blockDim.x;
     v[k] = q < D4 ? sum_splits4(y, nsplit, split_stride, r * D + 4L * q)
                   : make_float4(0.f, 0.f, 0.f, 0.f);
-    gg[k] = q < D4 && with_norm ? load4(g, dt, 4L * q) : make_float4(1.f, 1.f, 1.f, 1.f);
-  }
-  if (skip) return;
-  float ss = 0.f;
-#pragma unroll
-  for (int k = 0; k < kV; ++k)
     ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+  }
   ss = with_norm ? block_sum(ss, red) : 0.f;
   const float rstd = with_norm ? rsqrtf(ss / (float)D + eps) : 1.f;
 #pragma unroll
@@ -247,9 +233,10 @@ __global__ void rows_norm_vec_kernel(int dt, const float* __restrict__ y, int ns
     const int q = threadIdx.x + k * blockDim.x;
     if (q >= D4) continue;
     float4 o = v[k];
-    if (with_norm)
-      o = make_float4(o.x * rstd * gg[k].x, o.y * rstd * gg[k].y, o.z * rstd * gg[k].z,
-                      o.w * rstd * gg[k].w);
+    if (with_norm) {
+      const float4 gg = load4(g, dt, 4L * q);
+      o = make_float4(o.x * rstd * gg.x, o.y * rstd * gg.y, o.z * rstd * gg.z, o.w * rstd * gg.w);
+    }
     out.store4(r * D + 4L * q, o);
   }
 }
