@@ -247,7 +247,12 @@ DFLASH_API size_t dflash_body_workspace_size(const dflash_config_t* cfg, int B, 
  * A valid slot whose position id is out of range sets DFLASH_ERR_DEVICE_CHECK.
  * Range: in the bf16 configuration the layer projections' inputs, Q/K/V and the attention
  * output are fp16; a value outside the fp16 range sets DFLASH_ERR_RANGE in the sticky device
- * status while the call returns DFLASH_OK: poll dflash_device_status to learn of it. */
+ * status while the call returns DFLASH_OK: poll dflash_device_status to learn of it.
+ * Streams: with bf16 layer weights and more than 512 draft slots the fp16 copies of the layer
+ * matrices are made in the workspace on a library-owned stream of the calling host thread,
+ * one layer ahead of the layer that reads them; events order that work after what `stream`
+ * already holds and before the layer that reads it, so every result is ordered on `stream`
+ * as for any other call (a graph captured from `stream` includes it). */
 DFLASH_API int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
                         const void* block_emb, const int32_t* anchors,
                         const uint8_t* block_valid, const int32_t* position_ids,
