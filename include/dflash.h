@@ -252,7 +252,7 @@ DFLASH_API size_t dflash_body_workspace_size(const dflash_config_t* cfg, int B, 
  * matrices are made in the workspace on a library-owned stream of the calling host thread,
  * one layer ahead of the layer that reads them; events order that work after what `stream`
  * already holds and before the layer that reads it, so every result is ordered on `stream`
- * as for any other call (a graph captured from `stream` includes it). */
+ * as for any other call. */
 DFLASH_API int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
                         const void* block_emb, const int32_t* anchors,
                         const uint8_t* block_valid, const int32_t* position_ids,
