@@ -2,7 +2,7 @@
 //
 // C[z][t][n] (fp32) = sum over the K slice z of X[t][k] * W[n][k] for the token rows t of the
 // active 128-row tiles, computed transposed: D[n][t] = W[n, :] X[t, :]^T with the weight rows
-// as the MMA's M = 128 operand and up to 256 tokens (two 128-row token tiles) as N.  This
+// as the MMA's M = 128 operand and up to 128 tokens (one 128-row token tile) as N.  This
 // is the form of the draft
 // layers' projections ("DFlash Draft Body", How It Works step 3: QKV, O, gate/up, down; and
 // the per-layer context K/V projection of the "DFlash" page, How it works): a few hundred
@@ -16,7 +16,7 @@
 //    (tcgen05.mma ... kind::f16 with A in tensor memory).  No converted copy of the
 //    weights ever exists in global memory.
 //  * The activations X are fp16 (their 11 significant bits keep the body within its error
-//    bound); TMA loads 128 x 128 tiles of the active token tiles only, two per unit, and the
+//    bound); TMA loads 128 x 128 tiles of the active token tiles only, one per unit, and the
 //    MMA's N covers only the rows present (16 for a 16-token decode step).
 //  * K is cut into `splits` slices when the (weight tile, token tile) units alone would
 //    leave SMs idle.  The count is chosen on the device from the number of active token
@@ -30,8 +30,9 @@
 // groups of four that take alternate K-steps; warps 10-13 epilogue.  Shared memory holds
 // two rings: weight tiles, freed as soon as the converters have read them, and token tiles,
 // freed by the MMA.  A K-step is 128 wide (eight MMAs per barrier wait and per commit).
-// Tensor memory holds one 256-column accumulator and a 4-slot ring of converted A tiles (64
-// columns each), so the conversion runs ahead of the MMA and the
+// Tensor memory holds two 128-column accumulators (the epilogue of one unit overlaps the next
+// unit's MMAs) and a 4-slot ring of converted A tiles (64 columns each), so the conversion
+// runs ahead of the MMA and the
 // weight tiles' load-and-convert latency stays off the token ring.  The converters and the
 // producers run ahead into the next unit while the epilogue drains.
 // Every mbarrier wait is bounded
@@ -59,7 +60,7 @@ constexpr int kThreads = 448;
 constexpr uint32_t kWSub = 128 * kBox * 2;              // 16 KB: 128 weight rows x 64 K
 constexpr uint32_t kWBytes = 2 * kWSub;                 // 32 KB weight stage
 constexpr uint32_t kRingBytes = 196 * 1024;             // shared-memory ring budget
-constexpr uint32_t kTmemCols = 512;                     // acc 256, A ring 4 x 64
+constexpr uint32_t kTmemCols = 512;                     // two accumulators 2 x 128, A ring 4 x 64
 constexpr uint32_t kTmemAcc = 0, kTmemA = 256;
 constexpr uint32_t kEpiBufFloats = 32 * 36;             // per epilogue warp: [32][32 + 4]
 constexpr size_t kSmemBytes = 1024 + kRingBytes + 512 + 4 * kEpiBufFloats * sizeof(float);
@@ -79,7 +80,6 @@ struct WsParams {
   int sms;
   const int32_t* tile_list;  // optional: [0] = count, [1..] = active token tiles
   int xrows;                 // rows of a token-tile load (128, or M rounded up to 16)
-  int two_tiles;             // units take two token tiles (M > 128)
   int w_stages;              // weight ring stages (32 KB each)
   int x_stages;              // token ring stages
   uint32_t x_stage_bytes;    // token tile(s) of one K-step
@@ -101,8 +101,7 @@ struct WsParams {
 enum : int { kEpiF32 = 0, kEpiSwiGLU = 1, kEpiKvCache = 2 };
 
 struct Sched {
-  int tiles;   // active token tiles
-  int pairs;   // units along the tokens: pairs of active token tiles
+  int tiles;   // active token tiles (the units along the tokens)
   int splits;
   int per;     // K-steps per slice
   long units;
@@ -111,39 +110,33 @@ struct Sched {
 __device__ __forceinline__ Sched schedule(const WsParams& p) {
   Sched s;
   s.tiles = p.tile_list ? p.tile_list[0] : p.m_tiles;
-  s.pairs = p.two_tiles ? (s.tiles + 1) / 2 : s.tiles;
-  const long units1 = (long)p.w_tiles * s.pairs;
+  const long units1 = (long)p.w_tiles * s.tiles;
   s.splits = choose_splits(units1, p.num_kb, p.max_splits, p.sms);
   s.per = (p.num_kb + s.splits - 1) / s.splits;
   s.units = units1 * s.splits;
   return s;
 }
 
-// A unit: weight tile wt, token tiles t0 and t1 (t1 < 0: none), K slice z.  The token
-// pairs of one weight tile are consecutive so the CTAs that share a weight tile run
-// together.  rows0 / rows1: token rows present in each tile.
+// A unit: weight tile wt, token tile t0, K slice z.  The token tiles of one weight tile are
+// consecutive so the CTAs that share a weight tile run together.  rows0: token rows present.
 struct Unit {
-  int wt, t0, t1, z, rows0, rows1;
+  int wt, t0, z, rows0;
 };
 
 __device__ __forceinline__ Unit decode(const WsParams& p, const Sched& s, long u) {
   Unit x;
-  const int pi = (int)(u % s.pairs);
-  const long rest = u / s.pairs;
+  const int pi = (int)(u % s.tiles);
+  const long rest = u / s.tiles;
   x.wt = (int)(rest % p.w_tiles);
   x.z = (int)(rest / p.w_tiles);
-  const int i0 = p.two_tiles ? 2 * pi : pi, i1 = 2 * pi + 1;
-  x.t0 = p.tile_list ? p.tile_list[1 + i0] : i0;
-  x.t1 = p.two_tiles && i1 < s.tiles ? (p.tile_list ? p.tile_list[1 + i1] : i1) : -1;
+  x.t0 = p.tile_list ? p.tile_list[1 + pi] : pi;
   x.rows0 = (int)min((long)kTT, p.M - (long)x.t0 * kTT);
-  x.rows1 = x.t1 >= 0 ? (int)min((long)kTT, p.M - (long)x.t1 * kTT) : 0;
   return x;
 }
 
-// MMA N of a unit: the rows present, rounded up to 16 (the second tile starts at column 128)
+// MMA N of a unit: the rows present, rounded up to 16
 __device__ __forceinline__ uint32_t unit_idesc(const Unit& x) {
-  const int n = x.t1 >= 0 ? kTT + ((x.rows1 + 15) & ~15) : ((x.rows0 + 15) & ~15);
-  return idesc_f16(kWM, n);
+  return idesc_f16(kWM, (x.rows0 + 15) & ~15);
 }
 
 // bf16 pair -> fp16 pair (round to nearest even); `mag` collects the largest bf16 magnitude
@@ -331,9 +324,9 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
   // [4] the MMAs of K-step i (counted over the CTA's whole schedule) are done: A slot i % 4
   // and token stage i % SX are free again (one commit per K-step serves both)
   uint64_t* aempty = afull + kASlots;
-  uint64_t* tfull = aempty + kASlots;       // accumulator ready
-  uint64_t* tempty = tfull + 1;             // accumulator drained
-  uint64_t* drain = tempty + 1;
+  uint64_t* tfull = aempty + kASlots;       // [2] accumulator ready
+  uint64_t* tempty = tfull + 2;             // [2] accumulator drained
+  uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* epi_buf = reinterpret_cast<float*>(smem + kRingBytes + 512);  // [4][kEpiBufFloats]
@@ -351,8 +344,10 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
       mbar_init(&afull[a], 4);
       mbar_init(&aempty[a], 1);
     }
-    mbar_init(tfull, 1);
-    mbar_init(tempty, 4);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -371,9 +366,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
 
   const Sched sc = schedule(p);
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.splits_out) *p.splits_out = sc.splits;
-  // a token stage: for each of the two K boxes, the unit's token tiles one after the other
-  // (one K-major operand of up to 256 rows per box)
-  const uint32_t xtile_bytes = (uint32_t)p.xrows * kBox * 2;
+  // a token stage: the unit's token tile, one K-major operand of up to 128 rows per K box
   const uint32_t xsub_bytes = p.x_stage_bytes / 2;
 
   if (warp == 0) {
@@ -389,8 +382,6 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
       for (long u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
         const Unit x = decode(p, sc, u);
         const int kb0 = x.z * sc.per, kb1 = min(p.num_kb, kb0 + sc.per);
-        // a missing second tile is read past the last row: zeros, never stored
-        const int t1row = (x.t1 >= 0 ? x.t1 : p.m_tiles) * kTT;
         for (int kb = kb0; kb < kb1; ++kb) {
           // weight stage: the converters of its previous use are done; token stage: the MMAs
           // of K-step n_issued - SX are done (phase (n_issued - SX) / 8 of aempty)
@@ -418,7 +409,6 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
               uint8_t* dst = xring + (size_t)stage * p.x_stage_bytes + h * xsub_bytes;
               const int k0 = kb * kBK + h * kBox;
               tma_load_2d(&map_x, &full[stage], dst, k0, x.t0 * kTT);
-              if (p.two_tiles) tma_load_2d(&map_x, &full[stage], dst + xtile_bytes, k0, t1row);
             }
           }
           ++n_issued;
@@ -435,15 +425,16 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
       int stage = 0;  // token ring
       uint32_t ph = 0;
       long i = 0;  // K-step counter: A slot i % 8
+      int acc = 0;  // two accumulators: the epilogue of one unit overlaps the next unit
       uint32_t acc_ph = 0;
       bool ok = true;
       for (long u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
         const Unit x = decode(p, sc, u);
         const int kb0 = x.z * sc.per, kb1 = min(p.num_kb, kb0 + sc.per);
         const uint32_t idesc = unit_idesc(x);
-        if (!mbar_wait(tempty, acc_ph ^ 1u, abort_flag, kWaitLimitNs)) break;
+        if (!mbar_wait(&tempty[acc], acc_ph ^ 1u, abort_flag, kWaitLimitNs)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + kTmemAcc;
+        const uint32_t d_tmem = tmem + kTmemAcc + (uint32_t)(acc * kTT);
         for (int kb = kb0; kb < kb1; ++kb, ++i) {
           const int slot = (int)(i % kASlots);
           if (!mbar_wait(&afull[slot], (uint32_t)((i / kASlots) & 1), abort_flag, kWaitLimitNs) ||
@@ -465,8 +456,8 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
           if (++stage == SX) { stage = 0; ph ^= 1u; }
         }
         if (!ok) break;
-        umma_commit(tfull);
-        acc_ph ^= 1u;
+        umma_commit(&tfull[acc]);
+        if (++acc == 2) { acc = 0; acc_ph ^= 1u; }
       }
       umma_commit(drain);
       mbar_drain_wait(drain, 0, kWaitLimitNs / 4);
@@ -534,26 +525,23 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     bool bad = false;
+    int acc = 0;
     uint32_t acc_ph = 0;
     for (long u = blockIdx.x; u < sc.units; u += gridDim.x) {
       const Unit x = decode(p, sc, u);
-      if (!__all_sync(0xffffffffu, mbar_wait(tfull, acc_ph, abort_flag, kWaitLimitNs) ? 1 : 0))
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&tfull[acc], acc_ph, abort_flag, kWaitLimitNs) ? 1 : 0))
         break;
       tc_fence_after();
-      for (int h = 0; h < 2; ++h) {
-        const int tt = h ? x.t1 : x.t0;
-        const int rows = h ? x.rows1 : x.rows0;
-        if (tt < 0) break;
-        const uint32_t tacc = tmem + kTmemAcc + (uint32_t)(h * kTT) + lane_off;
-        float* buf = epi_buf + (warp - 10) * kEpiBufFloats;
-        if (p.epi == kEpiF32) epi_f32(p, tacc, x.wt, tt, rows, x.z, r, lane, buf);
-        else if (p.epi == kEpiSwiGLU) epi_swiglu(p, tacc, x.wt, tt, rows, r, lane, buf);
-        else epi_kv(p, tacc, x.wt, tt, rows, r, lane, bad);
-      }
+      const uint32_t tacc = tmem + kTmemAcc + (uint32_t)(acc * kTT) + lane_off;
+      float* buf = epi_buf + (warp - 10) * kEpiBufFloats;
+      if (p.epi == kEpiF32) epi_f32(p, tacc, x.wt, x.t0, x.rows0, x.z, r, lane, buf);
+      else if (p.epi == kEpiSwiGLU) epi_swiglu(p, tacc, x.wt, x.t0, x.rows0, r, lane, buf);
+      else epi_kv(p, tacc, x.wt, x.t0, x.rows0, r, lane, bad);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
-      acc_ph ^= 1u;
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == 2) { acc = 0; acc_ph ^= 1u; }
     }
     if (bad) report(p.status, kStatusRange, kKernEpilogue);
   }
@@ -634,8 +622,7 @@ cudaError_t launch(const WsArgs& a, int epi, int w_tiles, int interleave, const 
   p.sms = sm_count();
   p.tile_list = a.tile_list;
   p.xrows = xrows;
-  p.two_tiles = a.M > kTT ? 1 : 0;
-  p.x_stage_bytes = (uint32_t)(p.two_tiles ? 2 : 1) * xrows * kBK * 2;
+  p.x_stage_bytes = (uint32_t)xrows * kBK * 2;
   // tokens: 4 stages when they are small (decode), else 2; the weights take the rest
   p.x_stages = p.x_stage_bytes <= 16384 ? kMaxXStages : 2;
   p.w_stages = (int)((kRingBytes - (uint32_t)p.x_stages * p.x_stage_bytes) / kWBytes);
@@ -660,7 +647,7 @@ cudaError_t launch(const WsArgs& a, int epi, int w_tiles, int interleave, const 
   // enough CTAs for the largest schedule the device can pick (all token tiles active)
   long max_units = 0;
   for (int s = 1; s <= p.max_splits; ++s) {
-    const long u = (long)w_tiles * (p.two_tiles ? (p.m_tiles + 1) / 2 : p.m_tiles) * s;
+    const long u = (long)w_tiles * p.m_tiles * s;
     if (u > max_units) max_units = u;
   }
   const int grid = (int)(max_units < p.sms ? max_units : p.sms);
