@@ -698,11 +698,15 @@ namespace {
 
 std::atomic<int> g_pair_mode{0};  // 0: CTA pairs from two M tiles up; 1: one CTA per tile
 
-// CTA pairs the device can hold at once with this kernel's shared memory (once per kernel).
+// CTA pairs the device can hold at once with this kernel's shared memory (once per kernel
+// and device).
 template <int kEpi>
 int max_active_pairs() {
-  static int cached = 0;
-  if (cached > 0) return cached;
+  static int cached[64] = {};  // per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] > 0) return cached[dev];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * 256);
   cfg.blockDim = dim3(kThreads);
@@ -717,7 +721,7 @@ int max_active_pairs() {
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<kEpi, 1>, &cfg) != cudaSuccess || n < 1)
     n = sm_count() / 2;
-  cached = n;
+  cached[dev] = n;
   return n;
 }
 
