@@ -2,11 +2,10 @@
 //
 // C[z][t][n] (fp32) = sum over the K slice z of X[t][k] * W[n][k] for the token rows t of the
 // active 128-row tiles, computed transposed: D[n][t] = W[n, :] X[t, :]^T with the weight rows
-// as the MMA's M = 128 operand and up to 128 tokens (one 128-row token tile) as N.  This
-// is the form of the draft
-// layers' projections ("DFlash Draft Body", How It Works step 3: QKV, O, gate/up, down; and
-// the per-layer context K/V projection of the "DFlash" page, How it works): a few hundred
-// to a few thousand tokens against 4096 x 4096 .. 24576 x 4096 weights.
+// as the MMA's M = 128 operand and up to 128 tokens (one 128-row token tile) as N.  This is
+// the form of the draft layers' projections ("DFlash Draft Body", How It Works step 3: QKV,
+// O, gate/up, down) in calls of up to 512 draft slots, against 4096 x 4096 .. 24576 x 4096
+// weights.
 //
 //  * The weights arrive as bf16 (the model's own) or fp16 and are read from global memory
 //    exactly as given: TMA brings a 128 x 128 tile (two 64-column boxes) into shared
@@ -22,8 +21,7 @@
 //    leave SMs idle.  The count is chosen on the device from the number of active token
 //    tiles, written to *splits_out, and read by the kernel that sums the slices.
 //  * Epilogues: fp32 slices; SiLU(gate) * up (weight rows of a tile interleaved gate / up,
-//    so each pair of TMEM lanes holds one channel); the context K/V cache (a tile is one
-//    K or V head; K rows interleaved (i, i + 64) so RoPE pairs meet in neighbouring lanes).
+//    so each pair of TMEM lanes holds one channel).
 //
 // Warp roles (448 threads, one CTA per SM, persistent): warp 0 TMA producers (lane 0 the
 // weight ring, lane 1 the token ring); warp 1 MMA issuer; warps 2-9 converters in two
@@ -50,7 +48,7 @@ namespace {
 using namespace tc;
 
 constexpr int kWM = 128;   // weight rows per unit (MMA M)
-constexpr int kTT = 128;   // rows of a token tile; a unit takes two (MMA N <= 256)
+constexpr int kTT = 128;   // rows of a token tile, one per unit (MMA N <= 128)
 constexpr int kBK = 128;   // K per stage: two boxes of 64 (a 128-byte swizzled row each)
 constexpr int kBox = 64;   // K of one TMA box
 constexpr int kMaxWStages = 6;  // weight ring
@@ -85,8 +83,7 @@ struct WsParams {
   uint32_t x_stage_bytes;    // token tile(s) of one K-step
   int* splits_out;           // optional: the split count chosen on the device
   int w_bf16;                // weights bf16 (converted here) or fp16
-  int interleave;            // TMEM lane 2i <- weight row i, lane 2i+1 <- row 64 + i:
-                             // 0 never, 1 always, 2 for the K heads of the K/V cache only
+  int interleave;            // TMEM lane 2i <- weight row i, lane 2i+1 <- row 64 + i
   int epi;
   float* C;
   long ldc;
@@ -94,11 +91,10 @@ struct WsParams {
   int act_vec;       // SwiGLU output rows 4-element aligned (I % 4 == 0, 8-byte base)
   ActOut act;        // kEpiSwiGLU
   int swiglu_I;
-  KvCacheEpilogue kv;  // kEpiKvCache
   unsigned* status;
 };
 
-enum : int { kEpiF32 = 0, kEpiSwiGLU = 1, kEpiKvCache = 2 };
+enum : int { kEpiF32 = 0, kEpiSwiGLU = 1 };
 
 struct Sched {
   int tiles;   // active token tiles (the units along the tokens)
@@ -232,77 +228,6 @@ __device__ __forceinline__ void epi_swiglu(const WsParams& p, uint32_t tacc, int
       const float g = odd ? other : __uint_as_float(v[j]);
       const float u = odd ? __uint_as_float(v[16 + j]) : other;
       if (ch < I && j0 + j < rows) p.act.store((t0 + j) * I + ch, g / (1.f + expf(-g)) * u);
-    }
-  }
-}
-
-// Context K/V cache.  Unit wt is head wt of the 2*Hkv K-then-V heads.  K: lanes 2i / 2i+1 hold
-// channels i / i+64 (interleaved), rotated by RoPE at the token's position and written to
-// rows [pos][dh]; V: lane d holds channel d, written to the transposed plane [dh][pos].
-__device__ __forceinline__ void epi_kv(const WsParams& p, uint32_t tacc, int wt, int tt, int rows,
-                                       int r, int lane, bool& bad) {
-  const KvCacheEpilogue& e = p.kv;
-  const long plane = (long)e.L_cache * 128;
-  const bool is_k = wt < e.Hkv;
-  const bool odd = lane & 1;
-  const long tend = (long)tt * kTT + rows;  // rows of this tile end here
-#pragma unroll 1
-  for (int c = 0; c * 32 < rows; ++c) {
-    uint32_t v[32];
-    tmem_ld_32x32b_x32(tacc + c * 32, v);
-    const long tbase = (long)tt * kTT + c * 32;
-    if (is_k) {
-      const int i = r >> 1;  // frequency index; this pair holds channels i and i + 64
-#pragma unroll 4
-      for (int j = 0; j < 16; ++j) {
-        const float mine = __uint_as_float(odd ? v[j] : v[16 + j]);
-        const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-        const float x0 = odd ? other : __uint_as_float(v[j]);        // channel i
-        const float x1 = odd ? __uint_as_float(v[16 + j]) : other;   // channel i + 64
-        const long m = tbase + j + (odd ? 16 : 0);
-        if (m >= tend) continue;
-        const int b = (int)(m / e.L);
-        const int cpos = (int)(m - (long)b * e.L);
-        if (e.ctx_len && cpos >= e.ctx_len[b]) continue;
-        const float cs = e.cos_t[(long)cpos * 64 + i], sn = e.sin_t[(long)cpos * 64 + i];
-        const float a0 = x0 * cs - x1 * sn, a1 = x1 * cs + x0 * sn;
-        bad = bad || !(fmaxf(fabsf(a0), fabsf(a1)) + 0.f * (a0 + a1) < 65520.f);
-        __half* dst = e.kv + ((long)b * 2 * e.Hkv + wt) * plane + ((long)e.pos_offset + cpos) * 128;
-        dst[i] = __float2half_rn(a0);
-        dst[i + 64] = __float2half_rn(a1);
-      }
-    } else {
-      const int g = wt - e.Hkv;
-      // 8 consecutive tokens stay in one batch row (L % 8 == 0) and are 8 consecutive
-      // positions: one 16-byte store when the destination is aligned and all are kept
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        const long m0 = tbase + q * 8;
-        if (m0 >= tend) break;
-        const int b = (int)(m0 / e.L);
-        const int c0 = (int)(m0 - (long)b * e.L);
-        const int lim = e.ctx_len ? min(e.ctx_len[b], e.L) : e.L;
-        __half* dst = e.kv + ((long)b * 2 * e.Hkv + e.Hkv + g) * plane + (long)r * e.L_cache +
-                      e.pos_offset + c0;
-        float f[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          f[k] = __uint_as_float(v[q * 8 + k]);
-          bad = bad || !(fabsf(f[k]) < 65520.f);
-        }
-        if (c0 + 8 <= lim && m0 + 8 <= tend && ((e.pos_offset + c0) & 7) == 0) {
-          uint32_t w[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const __half2 h = __floats2half2_rn(f[2 * k], f[2 * k + 1]);
-            w[k] = *reinterpret_cast<const uint32_t*>(&h);
-          }
-          *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-        } else {
-          for (int k = 0; k < 8; ++k)
-            if (c0 + k < lim && m0 + k < tend) dst[k] = __float2half_rn(f[k]);
-        }
-      }
     }
   }
 }
@@ -477,7 +402,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
     bool ok = true;
     for (long u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
       const Unit x = decode(p, sc, u);
-      const bool inter = p.interleave == 1 || (p.interleave == 2 && x.wt < p.kv.Hkv);
+      const bool inter = p.interleave != 0;
       const int srow = inter ? srow_inter : r;
       const int kb0 = x.z * sc.per, kb1 = min(p.num_kb, kb0 + sc.per);
       for (int kb = kb0; kb < kb1; ++kb, ++i) {
@@ -524,7 +449,6 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    bool bad = false;
     int acc = 0;
     uint32_t acc_ph = 0;
     for (long u = blockIdx.x; u < sc.units; u += gridDim.x) {
@@ -536,14 +460,12 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
       const uint32_t tacc = tmem + kTmemAcc + (uint32_t)(acc * kTT) + lane_off;
       float* buf = epi_buf + (warp - 10) * kEpiBufFloats;
       if (p.epi == kEpiF32) epi_f32(p, tacc, x.wt, x.t0, x.rows0, x.z, r, lane, buf);
-      else if (p.epi == kEpiSwiGLU) epi_swiglu(p, tacc, x.wt, x.t0, x.rows0, r, lane, buf);
-      else epi_kv(p, tacc, x.wt, x.t0, x.rows0, r, lane, bad);
+      else epi_swiglu(p, tacc, x.wt, x.t0, x.rows0, r, lane, buf);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
       if (++acc == 2) { acc = 0; acc_ph ^= 1u; }
     }
-    if (bad) report(p.status, kStatusRange, kKernEpilogue);
   }
 
   tc_fence_before();
@@ -599,7 +521,7 @@ int sm_count() {
 }
 
 cudaError_t launch(const WsArgs& a, int epi, int w_tiles, int interleave, const ActOut* act,
-                   const KvCacheEpilogue* kv, cudaStream_t stream) {
+                   cudaStream_t stream) {
   if (a.w_dtype != DFLASH_DTYPE_BF16 && a.w_dtype != DFLASH_DTYPE_F16) return cudaErrorInvalidValue;
   if (((uintptr_t)a.X | (uintptr_t)a.W) % 16 != 0 || a.ldx % 8 != 0 || a.ldw % 8 != 0 ||
       a.K < 1 || a.M < 1 || a.Nw < 1)
@@ -642,7 +564,6 @@ cudaError_t launch(const WsArgs& a, int epi, int w_tiles, int interleave, const 
   if (act) p.act = *act;
   p.swiglu_I = epi == kEpiSwiGLU ? a.Nw / 2 : 0;
   p.act_vec = act && p.swiglu_I % 4 == 0 && ((uintptr_t)act->p % 16 == 0);
-  if (kv) p.kv = *kv;
   p.status = a.status;
   // enough CTAs for the largest schedule the device can pick (all token tiles active)
   long max_units = 0;
@@ -668,24 +589,14 @@ int gemm_ws_splits(long units1, int K, int max_splits) {
 }
 
 cudaError_t launch_gemm_ws(const WsArgs& a, cudaStream_t stream) {
-  return launch(a, kEpiF32, (a.Nw + kWM - 1) / kWM, 0, nullptr, nullptr, stream);
+  return launch(a, kEpiF32, (a.Nw + kWM - 1) / kWM, 0, nullptr, stream);
 }
 
 cudaError_t launch_gemm_ws_swiglu(const WsArgs& a, const ActOut& act, cudaStream_t stream) {
   if (a.Nw % 2 != 0) return cudaErrorInvalidValue;
   // a unit covers 64 channels: its 64 gate rows and the 64 up rows of the same channels
   // (rows past 2I read as zeros; channels past I are not stored)
-  return launch(a, kEpiSwiGLU, (a.Nw / 2 + 63) / 64, 1, &act, nullptr, stream);
-}
-
-cudaError_t launch_gemm_ws_kv_cache(const WsArgs& a, const KvCacheEpilogue& kv,
-                                    cudaStream_t stream) {
-  if (a.Nw != 2 * kv.Hkv * 128 || kv.L < 1 || kv.L % 8 != 0 || kv.row_pos0)
-    return cudaErrorInvalidValue;
-  if (((uintptr_t)kv.kv | (uintptr_t)kv.cos_t | (uintptr_t)kv.sin_t) % 16 != 0)
-    return cudaErrorInvalidValue;
-  // K heads interleave their RoPE pairs; V heads keep the natural order
-  return launch(a, kEpiKvCache, 2 * kv.Hkv, 2, nullptr, &kv, stream);
+  return launch(a, kEpiSwiGLU, (a.Nw / 2 + 63) / 64, 1, &act, stream);
 }
 
 }  // namespace dflash

@@ -322,9 +322,6 @@ int gemm_ws_splits(long units1, int K, int max_splits);
 cudaError_t launch_gemm_ws(const WsArgs& a, cudaStream_t stream);
 // act[t][i] = SiLU(gate) * up, W = W_gate_up [2I][K] (gate rows, then up rows); Nw = 2I.
 cudaError_t launch_gemm_ws_swiglu(const WsArgs& a, const ActOut& act, cudaStream_t stream);
-// The context K/V cache of one layer from W = the K then V rows of w_qkv (Nw = 2*Hkv*128).
-cudaError_t launch_gemm_ws_kv_cache(const WsArgs& a, const KvCacheEpilogue& kv,
-                                    cudaStream_t stream);
 
 // ---- rows.cu: bf16 -> fp16 conversion (weights) ----
 // dst[i] = fp16(src[i]), round to nearest even; exact for bf16 values of magnitude in
