@@ -326,7 +326,9 @@ int ws_max_splits(int Nw, long T, int tile_n = 128) {
 struct ProjLayout {
   float* y;
   Act ctx;
-  __half* wkv16;  // one layer's K/V rows of w_qkv as fp16 (converted in the call), or null
+  __half* wkv16;  // the K/V rows of w_qkv as fp16 (converted in the call), or null: every
+                  // layer's, stacked, when kv_merged, else one layer's
+  bool kv_merged;  // one K/V GEMM over all layers (N = NL * 2*Hkv*dh) instead of one per layer
   float* cos_t;
   float* sin_t;
   int32_t* tile_list;
@@ -359,8 +361,16 @@ ProjLayout proj_layout(const dflash_config_t* c, int B, int L, void* ws, int rop
   p.n_commit = append ? cv.take<int32_t>(B) : nullptr;
   p.start = append ? cv.take<int32_t>(B) : nullptr;
   // the context K/V projection always runs on the 128 x 256-tile GEMM with fp16 operands:
-  // bf16 layer weights are converted into the workspace whatever the row count
-  p.wkv16 = context_kv_needs_convert(c) ? cv.take<__half>((size_t)kvw * D) : nullptr;
+  // bf16 layer weights are converted into the workspace whatever the row count.  When one
+  // layer's GEMM would fill fewer than eight waves of CTA pairs, the converted rows of every
+  // layer are stacked and projected by one GEMM: the context rows are read once and the
+  // waves come out even.
+  const long pair_units = ((M + 255) / 256) * ((kvw + 255) / 256);
+  p.kv_merged = context_kv_needs_convert(c) && c->num_layers > 1 &&
+                pair_units < 8L * (num_sms() / 2);
+  p.wkv16 = context_kv_needs_convert(c)
+                ? cv.take<__half>((size_t)kvw * D * (p.kv_merged ? c->num_layers : 1))
+                : nullptr;
   p.bytes = cv.off;
   return p;
 }
@@ -395,20 +405,43 @@ int project_rows(const dflash_config_t* cfg, const dflash_weights_t* w, const vo
                              ctx_len, L, s));
   }
   const size_t layer_elems = (size_t)B * 2 * Hkv * L_cache * dh;
+  auto kv_epilogue = [&](int l0, int layers) {
+    KvCacheEpilogue kv;
+    kv.kv = static_cast<__half*>(kv_cache) + (size_t)l0 * layer_elems;
+    kv.cos_t = lay.cos_t;
+    kv.sin_t = lay.sin_t;
+    kv.ctx_len = ctx_len;
+    kv.row_pos0 = row_pos0;
+    kv.L = L;
+    kv.pos_offset = pos_offset;
+    kv.L_cache = L_cache;
+    kv.Hkv = Hkv;
+    kv.layers = layers;
+    kv.layer_elems = (long)layer_elems;
+    return kv;
+  };
+  if (lay.kv_merged) {
+    // every layer's K/V rows, converted and stacked: one GEMM, RoPE and the fp16 cache layout
+    // in its epilogue
+    {
+      Prof pc(DFLASH_PROF_CONVERT, cfg->num_layers, s);
+      for (int l = 0; l < cfg->num_layers; ++l) {
+        const void* wkv = static_cast<const uint8_t*>(w->layers[l].w_qkv) + (size_t)qw * D * es;
+        DF_CUDA(launch_convert_bf16_f16(wkv, lay.wkv16 + (size_t)l * kvw * D, (size_t)kvw * D,
+                                        status_ptr(), s));
+      }
+    }
+    Prof pr(DFLASH_PROF_GEMM, 1, s);
+    DF_CUDA(launch_gemm_tc_kv_cache(DFLASH_DTYPE_F16, lay.ctx.p, D, lay.wkv16, D, M,
+                                    cfg->num_layers * kvw, D, flags,
+                                    kv_epilogue(0, cfg->num_layers), status_ptr(), s));
+    return DFLASH_OK;
+  }
   for (int l = 0; l < cfg->num_layers; ++l) {
     const void* wkv = static_cast<const uint8_t*>(w->layers[l].w_qkv) + (size_t)qw * D * es;
     if (cfg->dtype == DFLASH_DTYPE_BF16) {
       // RoPE and the fp16 cache layout are applied in the GEMM epilogue
-      KvCacheEpilogue kv;
-      kv.kv = static_cast<__half*>(kv_cache) + (size_t)l * layer_elems;
-      kv.cos_t = lay.cos_t;
-      kv.sin_t = lay.sin_t;
-      kv.ctx_len = ctx_len;
-      kv.row_pos0 = row_pos0;
-      kv.L = L;
-      kv.pos_offset = pos_offset;
-      kv.L_cache = L_cache;
-      kv.Hkv = Hkv;
+      const KvCacheEpilogue kv = kv_epilogue(l, 1);
       const void* wkv16 = wkv;
       if (lay.wkv16) {
         Prof pc(DFLASH_PROF_CONVERT, 1, s);

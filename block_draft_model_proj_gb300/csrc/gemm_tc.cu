@@ -215,8 +215,9 @@ __device__ __forceinline__ void v_head_f16(uint32_t hbase, __half* dst, long str
   }
 }
 
-// Context K/V epilogue of the per-layer K/V projection (N = 2*Hkv*dh, dh = 128: every
-// 256-column tile holds two whole heads; K heads first).  Row m of the tile is context
+// Context K/V epilogue of the K/V projection of e.layers consecutive layers (N = layers *
+// 2*Hkv*dh, dh = 128: every 256-column tile holds two whole heads; per layer the K heads, then
+// the V heads).  Row m of the tile is context
 // position c = m mod L of row b = m / L, cache position pos_offset + c.  K heads get RoPE
 // (rotate-half: channel i pairs with i + 64; table row c) and are written as cache rows
 // [pos][dh]; V heads are written transposed, [dh][pos].  Rows at or past ctx_len[b] are not
@@ -235,14 +236,17 @@ __device__ __forceinline__ void kv_cache_epilogue(const TcParams& p, uint32_t tb
   bool bad = false;  // a value outside the fp16 range (or NaN) met the cache
 #pragma unroll 1
   for (int hh = 0; hh < 2; ++hh) {
-    const int head = n_t * 2 + hh;  // 0 .. 2*Hkv-1: K heads, then V heads
-    if (head >= 2 * e.Hkv) break;   // warp-uniform
+    const int hg = n_t * 2 + hh;               // head over all layers
+    if (hg >= e.layers * 2 * e.Hkv) break;     // warp-uniform
+    const int l = hg / (2 * e.Hkv);
+    const int head = hg - l * 2 * e.Hkv;       // 0 .. 2*Hkv-1: K heads, then V heads
+    __half* kvl = e.kv + (long)l * e.layer_elems;
     const uint32_t hbase = tbase + hh * 128;
     if (head < e.Hkv) {
-      __half* dst = e.kv + ((long)b * 2 * e.Hkv + head) * plane + pos * 128;
+      __half* dst = kvl + ((long)b * 2 * e.Hkv + head) * plane + pos * 128;
       rope_head_f16(hbase, e.cos_t + trow * 64, e.sin_t + trow * 64, dst, row_ok, true, bad);
     } else {
-      __half* dst = e.kv + ((long)b * 2 * e.Hkv + e.Hkv + (head - e.Hkv)) * plane + pos;
+      __half* dst = kvl + ((long)b * 2 * e.Hkv + e.Hkv + (head - e.Hkv)) * plane + pos;
       v_head_f16(hbase, dst, e.L_cache, row_ok, true, bad);
     }
   }
@@ -834,7 +838,9 @@ cudaError_t launch_gemm_tc_kv_cache(int elem, const void* A, long lda, const voi
                                     long M, int N, int K, const int32_t* tile_list,
                                     const KvCacheEpilogue& kv, unsigned* status,
                                     cudaStream_t stream) {
-  if (N != 2 * kv.Hkv * 128 || kv.L < 1) return cudaErrorInvalidValue;
+  if (kv.layers < 1 || N != kv.layers * 2 * kv.Hkv * 128 || kv.L < 1 ||
+      (kv.layers > 1 && kv.layer_elems < (long)2 * kv.Hkv * kv.L_cache * 128))
+    return cudaErrorInvalidValue;
   if (((uintptr_t)kv.kv | (uintptr_t)kv.cos_t | (uintptr_t)kv.sin_t) % 16 != 0)
     return cudaErrorInvalidValue;
   return launch_common(elem, A, lda, Bm, ldb, nullptr, 0, M, N, K, 1, tile_list, status, nullptr,

@@ -219,7 +219,7 @@ bool gemm_tc_supported(long M, int N, int K, long lda, long ldb);
 // Destination of the context K/V projection written straight from the GEMM epilogue
 // (head_dim 128): rows m = b*L + c of the GEMM are cache positions pos_offset + c.
 struct KvCacheEpilogue {
-  __half* kv = nullptr;          // one layer: [B][2][Hkv] fp16 planes, K [L_cache][128], V^T [128][L_cache]
+  __half* kv = nullptr;          // first layer: [B][2][Hkv] fp16 planes, K [L_cache][128], V^T [128][L_cache]
   const float* cos_t = nullptr;  // [L][64], row c = position pos_offset + c
   const float* sin_t = nullptr;
   const int32_t* ctx_len = nullptr;  // optional [B]: rows c >= ctx_len[b] are not written
@@ -228,6 +228,10 @@ struct KvCacheEpilogue {
   // without it the position is pos_offset + c and the table row c
   const int32_t* row_pos0 = nullptr;
   int L = 0, pos_offset = 0, L_cache = 0, Hkv = 0;
+  // `layers` consecutive layers in one GEMM: columns [l * 2*Hkv*128, (l+1) * 2*Hkv*128) are
+  // layer l's K then V heads, written to the planes at kv + l * layer_elems
+  int layers = 1;
+  long layer_elems = 0;
 };
 // Attention-ready Q / K / V of the draft body's QKV projection written straight from the
 // GEMM epilogue (head_dim 128, no K-split): GEMM row t is slot t = (b, k, j) of the blocks,
@@ -274,7 +278,7 @@ cudaError_t launch_gemm_tc_cross_entropy(const void* A, long lda, const void* Bm
 cudaError_t launch_gemm_tc_swiglu(int elem, const void* A, long lda, const void* Bm, long ldb,
                                   long M, int I, int K, const int32_t* tile_list,
                                   const ActOut& act, unsigned* status, cudaStream_t stream);
-// C = A B^T with N = 2*Hkv*128, written to the cache by the epilogue (no K-split).
+// C = A B^T with N = kv.layers * 2*Hkv*128, written to the cache by the epilogue (no K-split).
 cudaError_t launch_gemm_tc_kv_cache(int elem, const void* A, long lda, const void* Bm, long ldb,
                                     long M, int N, int K, const int32_t* tile_list,
                                     const KvCacheEpilogue& kv, unsigned* status,
