@@ -386,6 +386,24 @@ int project_rows(const dflash_config_t* cfg, const dflash_weights_t* w, const vo
   const int dh = cfg->head_dim, Hkv = cfg->num_kv_heads, qw = cfg->num_heads * dh;
   const int kvw = 2 * Hkv * dh;
   const size_t es = esize(cfg->dtype);
+  // Stacked K/V rows: their conversion (HBM-bound, independent of the context) runs on a side
+  // stream of this thread beside the tensor-bound W_proj GEMM; it starts after everything
+  // already on `s` (the previous reader of the buffer) and is joined before the K/V GEMM.
+  SideStream* side = nullptr;
+  if (lay.kv_merged) {
+    DF_CUDA(side_stream(&side));
+    DF_CUDA(cudaEventRecord(side->fork, s));
+    DF_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
+    {
+      Prof pc(DFLASH_PROF_CONVERT, cfg->num_layers, side->s);
+      for (int l = 0; l < cfg->num_layers; ++l) {
+        const void* wkv = static_cast<const uint8_t*>(w->layers[l].w_qkv) + (size_t)qw * D * es;
+        DF_CUDA(launch_convert_bf16_f16(wkv, lay.wkv16 + (size_t)l * kvw * D, (size_t)kvw * D,
+                                        status_ptr(), side->s));
+      }
+    }
+    DF_CUDA(cudaEventRecord(side->done[0], side->s));
+  }
   // 128-row tiles no block reads (all c >= ctx_len[b]) are skipped by every projection
   const int32_t* flags = nullptr;
   if (ctx_len && cfg->dtype == DFLASH_DTYPE_BF16) {
@@ -421,16 +439,9 @@ int project_rows(const dflash_config_t* cfg, const dflash_weights_t* w, const vo
     return kv;
   };
   if (lay.kv_merged) {
-    // every layer's K/V rows, converted and stacked: one GEMM, RoPE and the fp16 cache layout
-    // in its epilogue
-    {
-      Prof pc(DFLASH_PROF_CONVERT, cfg->num_layers, s);
-      for (int l = 0; l < cfg->num_layers; ++l) {
-        const void* wkv = static_cast<const uint8_t*>(w->layers[l].w_qkv) + (size_t)qw * D * es;
-        DF_CUDA(launch_convert_bf16_f16(wkv, lay.wkv16 + (size_t)l * kvw * D, (size_t)kvw * D,
-                                        status_ptr(), s));
-      }
-    }
+    // every layer's K/V rows, converted and stacked (joined from the side stream): one GEMM,
+    // RoPE and the fp16 cache layout in its epilogue
+    DF_CUDA(cudaStreamWaitEvent(s, side->done[0], 0));
     Prof pr(DFLASH_PROF_GEMM, 1, s);
     DF_CUDA(launch_gemm_tc_kv_cache(DFLASH_DTYPE_F16, lay.ctx.p, D, lay.wkv16, D, M,
                                     cfg->num_layers * kvw, D, flags,
@@ -836,7 +847,7 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
           DF_CUDA(gemm(dt, DFLASH_DTYPE_F16, lay.h.p, D, lw.w_qkv, D, lay.y, qkvw, T, qkvw, D,
                        lay.sp_qkv, s, flags, tc ? lay.nsplit : nullptr));
       }
-      Prof pr(DFLASH_PROF_ROWS, 2, s);
+      Prof pr(DFLASH_PROF_ROWS, 1, s);
       DF_CUDA(launch_qkv_rope(lay.y, lay.sp_qkv, tc ? lay.nsplit : nullptr, position_ids,
                               block_valid, lay.cos_t, lay.sin_t,
                               lay.P, lay.q, lay.kb, lay.vbt, lay.ns_pad, T, N, S, Hq, Hkv, dh,

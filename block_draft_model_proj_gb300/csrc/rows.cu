@@ -28,23 +28,36 @@ __device__ __forceinline__ float ld(const void* p, int dt, long i) {
                                  : static_cast<const float*>(p)[i];
 }
 
-struct InvFreq {
-  double v[128];
+// Inverse frequencies theta^(-2i/dh) as float pairs (hi + lo carries about 48 bits) and 2*pi
+// as a float pair, for the angle reduction below.
+struct RopeConsts {
+  float inv_hi[128], inv_lo[128];
+  float two_pi_hi, two_pi_lo, inv_two_pi;
 };
 
+// cos / sin of the angle (p0 + p) * inv_i for p < P, i < half.  The angle is reduced to
+// [-pi, pi] in fp32 by Cody and Waite's method (the multiple of 2*pi taken off in two float
+// pieces), the product carried as a float pair (the rounding error of the leading product
+// from an FMA): the reduced angle is within about 4e-7 of the exact one for positions below
+// 2^24 (2.4e-7 measured against fp64 over positions up to 2^20, theta 1e6, dh 128), then
+// sincosf evaluates it.
 __global__ void rope_table_kernel(float* __restrict__ cos_t, float* __restrict__ sin_t, int p0,
-                                  int P, int half, const InvFreq inv) {
+                                  int P, int half, const RopeConsts rc) {
   pdl_wait();
   pdl_trigger();
   const long n = (long)P * half;
   for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n;
        e += (long)gridDim.x * blockDim.x) {
     const int p = (int)(e / half), i = (int)(e - (long)p * half);
-    const double ang = (double)(p0 + p) * inv.v[i];
-    // reduce to [-pi, pi] in fp64, then evaluate in fp32
-    const double r = fma(-rint(ang / kTwoPi), kTwoPi, ang);
+    const float pf = (float)(p0 + p);  // exact below 2^24
+    const float a_hi = pf * rc.inv_hi[i];
+    const float a_lo = fmaf(pf, rc.inv_lo[i], fmaf(pf, rc.inv_hi[i], -a_hi));
+    const float k = rintf(a_hi * rc.inv_two_pi);
+    float r = fmaf(-k, rc.two_pi_hi, a_hi);
+    r = fmaf(-k, rc.two_pi_lo, r);
+    r += a_lo;
     float s, c;
-    sincosf((float)r, &s, &c);
+    sincosf(r, &s, &c);
     cos_t[e] = c;
     sin_t[e] = s;
   }
@@ -295,24 +308,21 @@ __device__ __forceinline__ void store_pair(__half* dst, float a, float b) {
 }
 
 // Q and K heads with RoPE: one thread per (row t, head, 4 consecutive pairs i .. i+3), the
-// pairs (i, i + dh/2) rotated by the angle of position pos[t].  dh % 8 == 0.
+// pairs (i, i + dh/2) rotated by the angle of position pos[t].  dh % 8 == 0.  Run by blocks
+// blk = 0 .. nblk-1 of the launch (grid-stride over the elements).
 template <typename OutT>
-__global__ void qk_rope_kernel(const float* __restrict__ y, int nsplit,
-                               const int* __restrict__ nsplit_dev, long split_stride,
-                               const int32_t* __restrict__ pos, const uint8_t* __restrict__ valid,
-                               const float* __restrict__ cos_t, const float* __restrict__ sin_t,
-                               int P, OutT* __restrict__ q, OutT* __restrict__ kb, long T, int N,
-                               int S, int Hq, int Hkv, int dh, unsigned* status) {
-  pdl_wait();
-  pdl_trigger();
-  if (nsplit_dev) nsplit = *nsplit_dev;
+__device__ __forceinline__ void qk_rope_blocks(
+    int blk, int nblk, const float* __restrict__ y, int nsplit, long split_stride,
+    const int32_t* __restrict__ pos, const uint8_t* __restrict__ valid,
+    const float* __restrict__ cos_t, const float* __restrict__ sin_t, int P,
+    OutT* __restrict__ q, OutT* __restrict__ kb, long T, int N, int S, int Hq, int Hkv, int dh,
+    unsigned* status) {
   const int half = dh / 2, q4 = half / 4;
-  const int heads = Hq + Hkv;  // Q then K heads (V is transposed by v_transpose_kernel)
+  const int heads = Hq + Hkv;  // Q then K heads (the V heads are transposed by other blocks)
   const int grp = Hq / Hkv;
   const long width = (long)(Hq + 2 * Hkv) * dh;
   const long n = T * heads * q4;
-  for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n;
-       e += (long)gridDim.x * blockDim.x) {
+  for (long e = blk * (long)blockDim.x + threadIdx.x; e < n; e += (long)nblk * blockDim.x) {
     const long t = e / ((long)heads * q4);
     const int rem = (int)(e - t * heads * q4);
     const int hd = rem / q4, i = (rem - hd * q4) * 4;
@@ -357,18 +367,14 @@ __global__ void qk_rope_kernel(const float* __restrict__ y, int nsplit,
 // dh % 4 == 0, dh <= 256.
 constexpr int kVtSlots = 32;
 template <typename OutT>
-__global__ void __launch_bounds__(256) v_transpose_kernel(
-    const float* __restrict__ y, int nsplit, const int* __restrict__ nsplit_dev, long split_stride,
+__device__ __forceinline__ void v_transpose_block(
+    int bi, float (*tile)[257], const float* __restrict__ y, int nsplit, long split_stride,
     const uint8_t* __restrict__ valid, OutT* __restrict__ vbt, int ns_pad, int N, int S, int Hq,
     int Hkv, int dh) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ float tile[kVtSlots][257];
-  if (nsplit_dev) nsplit = *nsplit_dev;
   const int NS = N * S;
   const int tiles = (NS + kVtSlots - 1) / kVtSlots;
-  const int bt = blockIdx.x % tiles;
-  const int bg = blockIdx.x / tiles;  // b * Hkv + g
+  const int bt = bi % tiles;
+  const int bg = bi / tiles;  // b * Hkv + g
   const int b = bg / Hkv, g = bg - b * Hkv;
   const int ks0 = bt * kVtSlots;
   const long width = (long)(Hq + 2 * Hkv) * dh;
@@ -422,6 +428,29 @@ __global__ void __launch_bounds__(256) v_transpose_kernel(
       dst[0] = from_f<OutT>(v0);
     }
   }
+}
+
+// The attention operands from the QKV projection's fp32 slices, one launch: blocks
+// 0 .. vblocks-1 transpose the V heads (one per row b, KV head g and 32 slots), the others
+// apply RoPE to the Q and K heads.
+template <typename OutT>
+__global__ void __launch_bounds__(256) qkv_rope_kernel(
+    const float* __restrict__ y, int nsplit, const int* __restrict__ nsplit_dev, long split_stride,
+    const int32_t* __restrict__ pos, const uint8_t* __restrict__ valid,
+    const float* __restrict__ cos_t, const float* __restrict__ sin_t, int P, OutT* __restrict__ q,
+    OutT* __restrict__ kb, OutT* __restrict__ vbt, int ns_pad, long T, int N, int S, int Hq,
+    int Hkv, int dh, int vblocks, unsigned* status) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float tile[kVtSlots][257];
+  if (nsplit_dev) nsplit = *nsplit_dev;
+  if ((int)blockIdx.x < vblocks)
+    v_transpose_block<OutT>((int)blockIdx.x, tile, y, nsplit, split_stride, valid, vbt, ns_pad, N,
+                            S, Hq, Hkv, dh);
+  else
+    qk_rope_blocks<OutT>((int)blockIdx.x - vblocks, (int)gridDim.x - vblocks, y, nsplit,
+                         split_stride, pos, valid, cos_t, sin_t, P, q, kb, T, N, S, Hq, Hkv, dh,
+                         status);
 }
 
 // Context K: one thread per (b, c, head, pair i); plane (b, 0, g) holds K as [L_cache][dh].
@@ -512,12 +541,20 @@ cudaError_t launch_rope_table(float* cos_t, float* sin_t, int p0, int P, int hea
                               double theta, cudaStream_t stream) {
   const int half = head_dim / 2;
   if (half > 128) return cudaErrorInvalidValue;
-  InvFreq inv;
-  for (int i = 0; i < half; ++i) inv.v[i] = pow(theta, -2.0 * (double)i / (double)head_dim);
+  if (p0 < 0 || (long)p0 + P > (1L << 24)) return cudaErrorInvalidValue;
+  RopeConsts rc;
+  for (int i = 0; i < half; ++i) {
+    const double v = pow(theta, -2.0 * (double)i / (double)head_dim);
+    rc.inv_hi[i] = (float)v;
+    rc.inv_lo[i] = (float)(v - (double)rc.inv_hi[i]);
+  }
+  rc.two_pi_hi = (float)kTwoPi;
+  rc.two_pi_lo = (float)(kTwoPi - (double)rc.two_pi_hi);
+  rc.inv_two_pi = (float)(1.0 / kTwoPi);
   const long n = (long)P * half;
   {
     const cudaError_t le = launch_pdl(rope_table_kernel, dim3(grid_for(n, 256)), dim3(256), 0,
-        stream, cos_t, sin_t, p0, P, half, inv);
+        stream, cos_t, sin_t, p0, P, half, rc);
     if (le != cudaSuccess) return le;
   }
   return cudaGetLastError();
@@ -651,22 +688,18 @@ cudaError_t launch_qkv_rope(const float* y, int nsplit, const int* nsplit_dev, c
   const long stride = T * (long)(Hq + 2 * Hkv) * dh;
   const long B = T / ((long)N * S);
   const int vblocks = (int)(B * Hkv * ((N * S + kVtSlots - 1) / kVtSlots));
+  const int grid = vblocks + grid_for(n, 256);
   cudaError_t e;
-  if (f16) {
-    e = launch_pdl(qk_rope_kernel<__half>, dim3(grid_for(n, 256)), dim3(256), 0, stream, y, nsplit,
+  if (f16)
+    e = launch_pdl(qkv_rope_kernel<__half>, dim3(grid), dim3(256), 0, stream, y, nsplit,
                    nsplit_dev, stride, pos, valid, cos_t, sin_t, P, static_cast<__half*>(q),
-                   static_cast<__half*>(kb), T, N, S, Hq, Hkv, dh, status);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(v_transpose_kernel<__half>, dim3(vblocks), dim3(256), 0, stream, y, nsplit,
-                   nsplit_dev, stride, valid, static_cast<__half*>(vbt), ns_pad, N, S, Hq, Hkv, dh);
-  } else {
-    e = launch_pdl(qk_rope_kernel<float>, dim3(grid_for(n, 256)), dim3(256), 0, stream, y, nsplit,
+                   static_cast<__half*>(kb), static_cast<__half*>(vbt), ns_pad, T, N, S, Hq, Hkv,
+                   dh, vblocks, status);
+  else
+    e = launch_pdl(qkv_rope_kernel<float>, dim3(grid), dim3(256), 0, stream, y, nsplit,
                    nsplit_dev, stride, pos, valid, cos_t, sin_t, P, static_cast<float*>(q),
-                   static_cast<float*>(kb), T, N, S, Hq, Hkv, dh, status);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(v_transpose_kernel<float>, dim3(vblocks), dim3(256), 0, stream, y, nsplit,
-                   nsplit_dev, stride, valid, static_cast<float*>(vbt), ns_pad, N, S, Hq, Hkv, dh);
-  }
+                   static_cast<float*>(kb), static_cast<float*>(vbt), ns_pad, T, N, S, Hq, Hkv,
+                   dh, vblocks, status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
