@@ -377,10 +377,12 @@ ProjLayout proj_layout(const dflash_config_t* c, int B, int L, void* ws, int rop
 
 // The projection of rows m = b*L + c of target_hidden into every layer's cache planes at
 // positions (row_pos0 ? row_pos0[b] : pos_offset) + c, rows c >= ctx_len[b] skipped (the
-// RoPE table of `lay` is already built).
+// RoPE table of `lay` is already built, and with it the list of 128-row tiles holding a row
+// c < ctx_len[b], `flags`, or null: every tile).
 int project_rows(const dflash_config_t* cfg, const dflash_weights_t* w, const void* target_hidden,
                  int B, int L, int pos_offset, int L_cache, const int32_t* ctx_len,
-                 const int32_t* row_pos0, void* kv_cache, const ProjLayout& lay, cudaStream_t s) {
+                 const int32_t* row_pos0, void* kv_cache, const ProjLayout& lay, cudaStream_t s,
+                 const int32_t* flags) {
   const long M = (long)B * L;
   const int D = cfg->hidden, Kc = cfg->target_hidden * cfg->num_target_layers;
   const int dh = cfg->head_dim, Hkv = cfg->num_kv_heads, qw = cfg->num_heads * dh;
@@ -403,13 +405,6 @@ int project_rows(const dflash_config_t* cfg, const dflash_weights_t* w, const vo
       }
     }
     DF_CUDA(cudaEventRecord(side->done[0], side->s));
-  }
-  // 128-row tiles no block reads (all c >= ctx_len[b]) are skipped by every projection
-  const int32_t* flags = nullptr;
-  if (ctx_len && cfg->dtype == DFLASH_DTYPE_BF16) {
-    Prof pr(DFLASH_PROF_ROWS, 1, s);
-    DF_CUDA(launch_ctx_tile_list(ctx_len, B, L, lay.tile_list, s));
-    flags = lay.tile_list;
   }
   {
     Prof pr(DFLASH_PROF_GEMM, 1, s);
@@ -665,13 +660,23 @@ int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w
   const ProjLayout lay = proj_layout(cfg, B, L, ws);
   if ((r = check_ws(ws, ws_bytes, lay.bytes))) return r;
   cudaStream_t s = (cudaStream_t)stream;
+  // 128-row tiles no block reads (all c >= ctx_len[b]) are skipped by every projection; their
+  // list is built by one block of the RoPE-table launch
+  TileJob tj;
+  if (ctx_len && cfg->dtype == DFLASH_DTYPE_BF16) {
+    tj.kind = TileJob::kContext;
+    tj.ctx_len = ctx_len;
+    tj.B = B;
+    tj.L = L;
+    tj.list = lay.tile_list;
+  }
   {
     Prof pr(DFLASH_PROF_ROWS, 1, s);
     DF_CUDA(launch_rope_table(lay.cos_t, lay.sin_t, pos_offset, L, cfg->head_dim,
-                              cfg->rope_theta, s));
+                              cfg->rope_theta, s, tj));
   }
   return project_rows(cfg, w, target_hidden, B, L, pos_offset, L_cache, ctx_len, nullptr,
-                      kv_cache, lay, s);
+                      kv_cache, lay, s, tj.kind != TileJob::kNone ? lay.tile_list : nullptr);
 }
 
 size_t dflash_append_context_workspace_size(const dflash_config_t* cfg, int B, int P,
@@ -697,15 +702,24 @@ int dflash_append_context(const dflash_config_t* cfg, const dflash_weights_t* w,
   const ProjLayout lay = proj_layout(cfg, B, P, ws, L_cache, true);
   if ((r = check_ws(ws, ws_bytes, lay.bytes))) return r;
   cudaStream_t s = (cudaStream_t)stream;
+  // the rows each request commits (n_commit, from the plan kernel) decide the active tiles
+  TileJob tj;
+  if (cfg->dtype == DFLASH_DTYPE_BF16) {
+    tj.kind = TileJob::kContext;
+    tj.ctx_len = lay.n_commit;
+    tj.B = B;
+    tj.L = P;
+    tj.list = lay.tile_list;
+  }
   {
     Prof pr(DFLASH_PROF_ROWS, 2, s);
     DF_CUDA(launch_append_plan(accepted, cache_len, B, P, L_cache, lay.n_commit, lay.start,
                                status_ptr(), s));
     DF_CUDA(launch_rope_table(lay.cos_t, lay.sin_t, 0, L_cache, cfg->head_dim, cfg->rope_theta,
-                              s));
+                              s, tj));
   }
   return project_rows(cfg, w, target_hidden, B, P, 0, L_cache, lay.n_commit, lay.start,
-                      kv_cache, lay, s);
+                      kv_cache, lay, s, tj.kind != TileJob::kNone ? lay.tile_list : nullptr);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -743,16 +757,20 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
   unsigned* st = status_ptr();
   const size_t layer_elems = (size_t)B * 2 * Hkv * L * dh;
 
-  // 128-slot tiles without a valid slot are skipped by every projection
+  // 128-slot tiles without a valid slot are skipped by every projection; their list is built
+  // by one block of the RoPE-table launch
   const int32_t* flags = nullptr;
+  TileJob tj;
   if (dt == DFLASH_DTYPE_BF16) {
-    Prof pr(DFLASH_PROF_ROWS, 1, s);
-    DF_CUDA(launch_slot_tile_list(block_valid, T, lay.tile_list, s));
+    tj.kind = TileJob::kSlots;
+    tj.valid = block_valid;
+    tj.T = T;
+    tj.list = lay.tile_list;
     flags = lay.tile_list;
   }
   {
     Prof pr(DFLASH_PROF_ROWS, 2, s);
-    DF_CUDA(launch_rope_table(lay.cos_t, lay.sin_t, 0, lay.P, dh, cfg->rope_theta, s));
+    DF_CUDA(launch_rope_table(lay.cos_t, lay.sin_t, 0, lay.P, dh, cfg->rope_theta, s, tj));
     DF_CUDA(launch_residual_norm(kNormInit, dt, lay.x, block_emb, nullptr, 0, nullptr,
                                  w->layers[0].g_in, cfg->rms_eps, lay.h.out(), nullptr,
                                  block_valid, false, T, D, s));

@@ -120,8 +120,21 @@ cudaError_t launch_decayed_ce(const float* hidden, const void* lm_head, const in
 // ---- rows.cu: row-wise kernels (norms, RoPE table, GEMM epilogues) ----
 // RoPE table: cos/sin [P, dh/2] fp32 for positions p0 .. p0+P-1, angles formed and
 // range-reduced in fp64 (inverse frequencies computed on the host in fp64; dh <= 256).
+// Active 128-row tiles, built by one extra block of the RoPE-table launch: list[0] = count,
+// list[1..] = the tiles in order.  kContext: context rows m = b*L + c with c < ctx_len[b];
+// kSlots: slots t < T with valid[t] != 0.
+struct TileJob {
+  enum : int { kNone = 0, kContext = 1, kSlots = 2 };
+  int kind = kNone;
+  const int32_t* ctx_len = nullptr;
+  const uint8_t* valid = nullptr;
+  int B = 0, L = 0;
+  long T = 0;
+  long tiles = 0;  // set by the launcher
+  int32_t* list = nullptr;
+};
 cudaError_t launch_rope_table(float* cos_t, float* sin_t, int p0, int P, int head_dim,
-                              double theta, cudaStream_t stream);
+                              double theta, cudaStream_t stream, const TileJob& job = TileJob());
 
 enum NormMode { kNormInit = 0, kNormAdd = 1, kNormFinal = 2 };
 // Residual-stream step on rows of width D:
@@ -335,10 +348,8 @@ cudaError_t launch_convert_bf16_f16(const void* src, void* dst, size_t n, unsign
 
 // ---- rows.cu: compacted lists of active 128-row M tiles for the GEMMs ----
 // list[0] = count, list[1..] = tile indices in increasing order; list holds 1 + tiles ints.
-// Context rows m = b*L + c: tile active iff some row has c < ctx_len[b].
-cudaError_t launch_ctx_tile_list(const int32_t* ctx_len, int B, int L, int32_t* list,
-                                 cudaStream_t stream);
-// Body rows t: tile active iff some row is a valid slot.
+// Rows t: tile active iff some row is a valid slot (the body builds its list inside the
+// RoPE-table launch, TileJob).
 cudaError_t launch_slot_tile_list(const uint8_t* valid, long T, int32_t* list,
                                   cudaStream_t stream);
 

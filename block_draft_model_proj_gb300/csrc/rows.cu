@@ -28,6 +28,51 @@ __device__ __forceinline__ float ld(const void* p, int dt, long i) {
                                  : static_cast<const float*>(p)[i];
 }
 
+// Ordered compaction of the active tiles by one CTA (up to 1024 threads).
+template <typename Pred>
+__device__ __forceinline__ void compact_tiles(long tiles, int32_t* list, Pred active) {
+  __shared__ int warp_counts[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int base = 0;
+  for (long t0 = 0; t0 < tiles; t0 += blockDim.x) {
+    const long t = t0 + threadIdx.x;
+    const bool on = t < tiles && active(t);
+    const unsigned bal = __ballot_sync(0xffffffffu, on);
+    __syncthreads();
+    if (lane == 0) warp_counts[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0, sum = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+      if (w < warp) before += warp_counts[w];
+      sum += warp_counts[w];
+    }
+    if (on) list[1 + base + before + __popc(bal & ((1u << lane) - 1u))] = (int32_t)t;
+    base += sum;
+  }
+  if (threadIdx.x == 0) list[0] = base;
+}
+
+
+// A 128-row tile of the context rows m = b*L + c holding a row with c < ctx_len[b].
+__device__ __forceinline__ bool ctx_tile_active(long t, const int32_t* ctx_len, int B, int L) {
+  const long m0 = t * kGemmTileM, m1 = min(m0 + kGemmTileM, (long)B * L);
+  for (long m = m0; m < m1;) {
+    const int b = (int)(m / L);
+    int cl = ctx_len[b];
+    cl = cl < 0 ? 0 : (cl > L ? L : cl);
+    if ((int)(m - (long)b * L) < cl) return true;
+    m = (long)(b + 1) * L;
+  }
+  return false;
+}
+
+// A 128-row tile of the T slots holding a valid slot.
+__device__ __forceinline__ bool slot_tile_active(long t, const uint8_t* valid, long T) {
+  for (long r = t * kGemmTileM; r < min((t + 1) * kGemmTileM, T); ++r)
+    if (valid[r]) return true;
+  return false;
+}
+
 // Inverse frequencies theta^(-2i/dh) as float pairs (hi + lo carries about 48 bits) and 2*pi
 // as a float pair, for the angle reduction below.
 struct RopeConsts {
@@ -41,13 +86,27 @@ struct RopeConsts {
 // from an FMA): the reduced angle is within about 4e-7 of the exact one for positions below
 // 2^24 (2.4e-7 measured against fp64 over positions up to 2^20, theta 1e6, dh 128), then
 // sincosf evaluates it.
+// With a tile job, block 0 builds the active-tile list instead (one launch fewer).
 __global__ void rope_table_kernel(float* __restrict__ cos_t, float* __restrict__ sin_t, int p0,
-                                  int P, int half, const RopeConsts rc) {
+                                  int P, int half, const RopeConsts rc, const TileJob job) {
   pdl_wait();
   pdl_trigger();
+  long blk = blockIdx.x, nblk = gridDim.x;
+  if (job.kind != TileJob::kNone) {
+    if (blockIdx.x == 0) {
+      if (job.kind == TileJob::kContext)
+        compact_tiles(job.tiles, job.list,
+                      [&](long t) { return ctx_tile_active(t, job.ctx_len, job.B, job.L); });
+      else
+        compact_tiles(job.tiles, job.list,
+                      [&](long t) { return slot_tile_active(t, job.valid, job.T); });
+      return;
+    }
+    blk -= 1;
+    nblk -= 1;
+  }
   const long n = (long)P * half;
-  for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n;
-       e += (long)gridDim.x * blockDim.x) {
+  for (long e = blk * blockDim.x + threadIdx.x; e < n; e += nblk * blockDim.x) {
     const int p = (int)(e / half), i = (int)(e - (long)p * half);
     const float pf = (float)(p0 + p);  // exact below 2^24
     const float a_hi = pf * rc.inv_hi[i];
@@ -538,7 +597,7 @@ inline int grid_for(long n, int threads) {
 }  // namespace
 
 cudaError_t launch_rope_table(float* cos_t, float* sin_t, int p0, int P, int head_dim,
-                              double theta, cudaStream_t stream) {
+                              double theta, cudaStream_t stream, const TileJob& job) {
   const int half = head_dim / 2;
   if (half > 128) return cudaErrorInvalidValue;
   if (p0 < 0 || (long)p0 + P > (1L << 24)) return cudaErrorInvalidValue;
@@ -553,8 +612,12 @@ cudaError_t launch_rope_table(float* cos_t, float* sin_t, int p0, int P, int hea
   rc.inv_two_pi = (float)(1.0 / kTwoPi);
   const long n = (long)P * half;
   {
-    const cudaError_t le = launch_pdl(rope_table_kernel, dim3(grid_for(n, 256)), dim3(256), 0,
-        stream, cos_t, sin_t, p0, P, half, rc);
+    TileJob j = job;
+    if (j.kind == TileJob::kContext) j.tiles = ((long)j.B * j.L + kGemmTileM - 1) / kGemmTileM;
+    if (j.kind == TileJob::kSlots) j.tiles = (j.T + kGemmTileM - 1) / kGemmTileM;
+    const int grid = grid_for(n, 256) + (j.kind != TileJob::kNone ? 1 : 0);
+    const cudaError_t le = launch_pdl(rope_table_kernel, dim3(grid), dim3(256), 0, stream, cos_t,
+                                      sin_t, p0, P, half, rc, j);
     if (le != cudaSuccess) return le;
   }
   return cudaGetLastError();
@@ -776,71 +839,14 @@ __global__ void __launch_bounds__(256) convert_bf16_f16_kernel(
   if (bad) report(status, kStatusRange, kKernConvert);
 }
 
-// Ordered compaction of the active tiles by one CTA of 1024 threads.
-template <typename Pred>
-__device__ __forceinline__ void compact_tiles(long tiles, int32_t* list, Pred active) {
-  __shared__ int warp_counts[32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int base = 0;
-  for (long t0 = 0; t0 < tiles; t0 += blockDim.x) {
-    const long t = t0 + threadIdx.x;
-    const bool on = t < tiles && active(t);
-    const unsigned bal = __ballot_sync(0xffffffffu, on);
-    __syncthreads();
-    if (lane == 0) warp_counts[warp] = __popc(bal);
-    __syncthreads();
-    int before = 0, sum = 0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-      if (w < warp) before += warp_counts[w];
-      sum += warp_counts[w];
-    }
-    if (on) list[1 + base + before + __popc(bal & ((1u << lane) - 1u))] = (int32_t)t;
-    base += sum;
-  }
-  if (threadIdx.x == 0) list[0] = base;
-}
-
-__global__ void __launch_bounds__(1024) ctx_tile_list_kernel(const int32_t* __restrict__ ctx_len,
-                                                             int B, int L, int32_t* list,
-                                                             long tiles) {
-  pdl_wait();
-  pdl_trigger();
-  compact_tiles(tiles, list, [&](long t) {
-    const long m0 = t * kGemmTileM, m1 = min(m0 + kGemmTileM, (long)B * L);
-    for (long m = m0; m < m1;) {
-      const int b = (int)(m / L);
-      int cl = ctx_len[b];
-      cl = cl < 0 ? 0 : (cl > L ? L : cl);
-      if ((int)(m - (long)b * L) < cl) return true;
-      m = (long)(b + 1) * L;
-    }
-    return false;
-  });
-}
-
 __global__ void __launch_bounds__(1024) slot_tile_list_kernel(const uint8_t* __restrict__ valid,
                                                               long T, int32_t* list, long tiles) {
   pdl_wait();
   pdl_trigger();
-  compact_tiles(tiles, list, [&](long t) {
-    for (long r = t * kGemmTileM; r < min((t + 1) * kGemmTileM, T); ++r)
-      if (valid[r]) return true;
-    return false;
-  });
+  compact_tiles(tiles, list, [&](long t) { return slot_tile_active(t, valid, T); });
 }
 
 }  // namespace
-
-cudaError_t launch_ctx_tile_list(const int32_t* ctx_len, int B, int L, int32_t* list,
-                                 cudaStream_t stream) {
-  const long tiles = ((long)B * L + kGemmTileM - 1) / kGemmTileM;
-  {
-    const cudaError_t le = launch_pdl(ctx_tile_list_kernel, dim3(1), dim3(1024), 0, stream, ctx_len,
-        B, L, list, tiles);
-    if (le != cudaSuccess) return le;
-  }
-  return cudaGetLastError();
-}
 
 cudaError_t launch_slot_tile_list(const uint8_t* valid, long T, int32_t* list,
                                   cudaStream_t stream) {
