@@ -142,6 +142,23 @@ cudaError_t side_stream(SideStream** out) {
   return cudaSuccess;
 }
 
+// Joins the side stream back into `s` when the scope ends on a path that has not joined it
+// itself (an early error return): no work of the call is left behind on the side stream
+// unordered with the caller's stream.  The normal paths join explicitly and set `joined`, so
+// no extra cross-stream wait sits between two kernels of `s` (it would stop the next kernel's
+// programmatic early launch).
+struct SideJoin {
+  cudaStream_t s;
+  SideStream* const* side;
+  bool joined = false;
+  ~SideJoin() {
+    if (*side && !joined) {
+      cudaEventRecord((*side)->done[0], (*side)->s);
+      cudaStreamWaitEvent(s, (*side)->done[0], 0);
+    }
+  }
+};
+
 // ---- workspace carving -----------------------------------------------------------------
 struct Carver {
   uint8_t* base;
@@ -392,6 +409,7 @@ int project_rows(const dflash_config_t* cfg, const dflash_weights_t* w, const vo
   // stream of this thread beside the tensor-bound W_proj GEMM; it starts after everything
   // already on `s` (the previous reader of the buffer) and is joined before the K/V GEMM.
   SideStream* side = nullptr;
+  SideJoin join{s, &side};
   if (lay.kv_merged) {
     DF_CUDA(side_stream(&side));
     DF_CUDA(cudaEventRecord(side->fork, s));
@@ -437,6 +455,7 @@ int project_rows(const dflash_config_t* cfg, const dflash_weights_t* w, const vo
     // every layer's K/V rows, converted and stacked (joined from the side stream): one GEMM,
     // RoPE and the fp16 cache layout in its epilogue
     DF_CUDA(cudaStreamWaitEvent(s, side->done[0], 0));
+    join.joined = true;
     Prof pr(DFLASH_PROF_GEMM, 1, s);
     DF_CUDA(launch_gemm_tc_kv_cache(DFLASH_DTYPE_F16, lay.ctx.p, D, lay.wkv16, D, M,
                                     cfg->num_layers * kvw, D, flags,
@@ -807,8 +826,10 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
   // layer l's tensor-core work, into the buffer layer l - 1 used.
   const size_t sizes[4] = {(size_t)qkvw * D, (size_t)D * qw, (size_t)2 * I * D, (size_t)D * I};
   SideStream* side = nullptr;
+  SideJoin join{s, &side};
   auto convert_layer = [&](int l) -> int {
     // after everything already on the caller's stream (layer l - 2's use of this buffer)
+    join.joined = false;
     DF_CUDA(cudaEventRecord(side->fork, s));
     DF_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
     const dflash_layer_weights_t& src = w->layers[l];
@@ -831,6 +852,7 @@ int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
     if (lay.wl16) {
       // this layer's fp16 matrices are ready; then the next layer's conversion starts
       DF_CUDA(cudaStreamWaitEvent(s, side->done[l % 2], 0));
+      join.joined = true;  // every conversion forked so far is ordered before this layer
       if (l + 1 < cfg->num_layers && (r = convert_layer(l + 1)) != DFLASH_OK) return r;
       __half* buf = lay.wl16 + (size_t)(l % 2) * lay.wl16_layer;
       const void** mats[4] = {&lw.w_qkv, &lw.w_o, &lw.w_gate_up, &lw.w_down};

@@ -185,7 +185,12 @@ DFLASH_API size_t dflash_project_context_workspace_size(const dflash_config_t* c
  * Range: in the bf16 configuration the context and the cache are fp16.  A value outside
  * the fp16 range (or a NaN) sets DFLASH_ERR_RANGE in the sticky device status and is
  * stored as inf/NaN: the call itself still returns DFLASH_OK, so a caller that needs to
- * know polls dflash_device_status (which synchronizes the device). */
+ * know polls dflash_device_status (which synchronizes the device).
+ * Streams: with bf16 layer weights and few context rows (a per-layer K/V GEMM under eight
+ * waves of CTA pairs) the K/V rows of every layer are converted to fp16 on a library-owned
+ * stream of the calling host thread, beside the W_proj GEMM; events order that work after
+ * what `stream` already holds and join it back before the call's last kernel, on every
+ * return path, so every result is ordered on `stream` as for any other call. */
 DFLASH_API int dflash_project_context(const dflash_config_t* cfg, const dflash_weights_t* w,
                            const void* target_hidden, int B, int L, int pos_offset, int L_cache,
                            const int32_t* ctx_len, void* kv_cache, void* ws, size_t ws_bytes,
@@ -217,7 +222,7 @@ DFLASH_API size_t dflash_append_context_workspace_size(const dflash_config_t* cf
  * cache_len[b] never reads them.  A row whose cache_len is negative or would pass L_cache
  * commits nothing, keeps its length and sets DFLASH_ERR_DEVICE_CHECK.  The body then runs
  * with L = L_cache and a mask [B, L_cache] (positions below each request's length valid).
- * Range: as for dflash_project_context. */
+ * Range and streams: as for dflash_project_context. */
 DFLASH_API int dflash_append_context(const dflash_config_t* cfg, const dflash_weights_t* w,
                                      const void* target_hidden, int B, int P,
                                      const int32_t* accepted, int32_t* cache_len, int L_cache,
@@ -251,8 +256,8 @@ DFLASH_API size_t dflash_body_workspace_size(const dflash_config_t* cfg, int B, 
  * Streams: with bf16 layer weights and more than 512 draft slots the fp16 copies of the layer
  * matrices are made in the workspace on a library-owned stream of the calling host thread,
  * one layer ahead of the layer that reads them; events order that work after what `stream`
- * already holds and before the layer that reads it, so every result is ordered on `stream`
- * as for any other call. */
+ * already holds and before the layer that reads it (and joins it back on every return
+ * path), so every result is ordered on `stream` as for any other call. */
 DFLASH_API int dflash_body_forward(const dflash_config_t* cfg, const dflash_weights_t* w,
                         const void* block_emb, const int32_t* anchors,
                         const uint8_t* block_valid, const int32_t* position_ids,
