@@ -96,6 +96,7 @@ _SIGS = {
     "dflash_testing_gemm_splits": (_I, [_L, _I, _I]),
     "dflash_testing_fused_epilogues": (_I, [_I]),
     "dflash_testing_gemm_pairs": (_I, [_I]),
+    "dflash_testing_rope_table": (_I, [_P, _P, _I, _I, _I, ctypes.c_double, _P]),
     "dflash_testing_gemm_withheld": (_I, [_P, _L, _P, _L, _P, _L, _L, _I, _I, _L, _P]),
     "dflash_testing_gemm_ws": (_I, [_P, _L, _P, _I, _L, _P, _L, _L, _I, _I, _I, _P, _P, _P]),
     "dflash_testing_verify_plan": (_I, [_I, _I, _I, _L, _L, ctypes.POINTER(_I),
@@ -360,6 +361,14 @@ def dflash_testing_gemm_pairs(mode: int) -> None:
     """0: the 128 x 256-tile GEMM runs as CTA pairs from two M tiles up (default); 1: one
     CTA per tile everywhere."""
     _check(load().dflash_testing_gemm_pairs(mode))
+
+
+def dflash_testing_rope_table(cos_t, sin_t, p0: int, head_dim: int, theta: float,
+                              stream=None) -> None:
+    """The device RoPE table: cos_t / sin_t float32 [P, head_dim / 2] for positions p0 .. p0+P-1."""
+    P = cos_t.shape[0]
+    _check(load().dflash_testing_rope_table(_ptr(cos_t), _ptr(sin_t), p0, P, head_dim, theta,
+                                            _stream(stream)))
 
 
 def dflash_testing_fused_epilogues(mode: int) -> None:

@@ -1136,6 +1136,18 @@ int dflash_testing_gemm(int engine, int dtype, const void* A, long lda, const vo
 
 int dflash_testing_gemm_splits(long M, int N, int K) { return gemm_splits(M, N, K); }
 
+int dflash_testing_rope_table(float* cos_t, float* sin_t, int p0, int P, int head_dim,
+                              double theta, void* stream) {
+  if (!cos_t || !sin_t || ((uintptr_t)cos_t | (uintptr_t)sin_t) % 16 != 0)
+    return fail(DFLASH_ERR_INVALID_ARG, "cos_t / sin_t must be non-null and 16-byte aligned");
+  if (head_dim < 2 || head_dim % 2 != 0 || head_dim > 256 || P < 1 || p0 < 0 ||
+      (long)p0 + P > (1L << 24) || !(theta > 1.0))
+    return fail(DFLASH_ERR_INVALID_ARG,
+                "need head_dim even in [2, 256], P >= 1, 0 <= p0, p0 + P <= 2^24, theta > 1");
+  DF_CUDA(launch_rope_table(cos_t, sin_t, p0, P, head_dim, theta, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
 int dflash_testing_gemm_pairs(int mode) {
   if (mode < 0 || mode > 1) return fail(DFLASH_ERR_INVALID_ARG, "mode must be 0 or 1");
   set_gemm_tc_pairs(mode);

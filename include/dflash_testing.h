@@ -80,6 +80,15 @@ DFLASH_API int dflash_testing_fused_epilogues(int mode);
 DFLASH_API int dflash_testing_verify_plan(int B, int gamma, int V, long resident_ctas,
                                           long static_entries, int* chunks, int* chunk_len);
 
+/* The RoPE table the draft body and the context projection build on the device ("DFlash",
+ * Configuration: rotary position embedding with base rope_theta): cos_t[p][i] and
+ * sin_t[p][i] of the angle (p0 + p) * theta^(-2i / head_dim) for p < P, i < head_dim / 2,
+ * float32, row-major [P][head_dim / 2], device pointers 16-byte aligned.  Needs head_dim even
+ * and <= 256, P >= 1, 0 <= p0 and p0 + P <= 2^24 (positions exact in float32).  Enqueued on
+ * `stream`; returns a DFLASH_* status. */
+DFLASH_API int dflash_testing_rope_table(float* cos_t, float* sin_t, int p0, int P, int head_dim,
+                                         double theta, void* stream);
+
 /* ---- live kernel timing ----------------------------------------------------------------
  * While enabled, every kernel launch of the four operations is bracketed by two CUDA events
  * recorded on the launch stream, grouped by kind.  Enabling clears earlier records. */
